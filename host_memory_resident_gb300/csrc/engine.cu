@@ -1,0 +1,922 @@
+// Streaming engine and C ABI of the training step.
+//
+// The step follows the RAM-centric method of the MegaTrain articles:
+//  * host-resident state: FP32 master / m / v / grad in caller memory, a
+//    pinned bf16 flat store of all weights ("layer_pinned_flats", lqnn.cn
+//    article section 三.1) that the host Adam rewrites per unit;
+//  * two fixed device flat buffers ("gpu_flat_buffers", same section) that
+//    units (embedding, each layer, final norm + head) are copied into on a
+//    host-to-device stream; the compute stream waits a weight_ready event
+//    and records buffer_free when done, the copy stream waits buffer_free
+//    before overwriting (section 三.2: three streams, weight_ready_events /
+//    buffer_free_events; zhichai.net article point 2, ping-pong buffers);
+//  * checkpoint recompute: the input of every C-th layer is kept, backward
+//    walks segments from last to first and recomputes each from its
+//    checkpoint (section 三.4; zhichai.net article point 3);
+//  * a K-slab device gradient pool: a unit's weight gradients land in a free
+//    slab, a device-to-host stream copies it to pinned staging, and a host
+//    worker thread adds it into the FP32 gradient and runs Adam on that unit
+//    (section 三.3, "GPU backward -> gradient DMA -> CPU accumulate").
+// Everything on the device is the library's own kernels; there is no CPU
+// fallback for the layer compute.
+#include <omp.h>
+
+#include <algorithm>
+#include <atomic>
+#include <chrono>
+#include <cmath>
+#include <condition_variable>
+#include <cstdio>
+#include <cstring>
+#include <deque>
+#include <mutex>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "common.cuh"
+#include "host_math.h"
+#include "mt_internal.h"
+
+namespace mt {
+namespace {
+
+thread_local std::string g_thread_error;
+std::atomic<int> g_fail_next_alloc{0};
+
+using Clock = std::chrono::steady_clock;
+
+double seconds_since(Clock::time_point t0) {
+  return std::chrono::duration<double>(Clock::now() - t0).count();
+}
+
+struct StepError {
+  int code;
+  std::string msg;
+};
+
+#define CK(call)                                                                                     \
+  do {                                                                                               \
+    cudaError_t e_ = (call);                                                                         \
+    if (e_ != cudaSuccess) throw StepError{MT_ECUDA, std::string(#call ": ") + cudaGetErrorString(e_)}; \
+  } while (0)
+
+#define KK(call)                                                                      \
+  do {                                                                                \
+    int r_ = (call);                                                                  \
+    if (r_ != MT_OK) throw StepError{r_, std::string("kernel launch failed: ") + #call}; \
+  } while (0)
+
+// Device arena: one allocation carved into 256-byte aligned pieces.
+struct Arena {
+  uint8_t* base = nullptr;
+  size_t cap = 0, used = 0;
+  void* take(size_t bytes) {
+    size_t off = (used + 255) & ~size_t(255);
+    if (off + bytes > cap) throw StepError{MT_ENOMEM, "device arena exhausted"};
+    used = off + bytes;
+    return base + off;
+  }
+};
+
+template <typename T>
+T* take(Arena& a, size_t n) {
+  return reinterpret_cast<T*>(a.take(sizeof(T) * (n ? n : 1)));
+}
+
+// Activations saved for one layer's backward.
+struct Saved {
+  bf16* x;     // layer input [M, d]
+  bf16* u;     // attention-norm output [M, d]
+  float* r1;   // its rstd [M]
+  bf16* qkv;   // q, k (after RoPE), v [M, qkvN]
+  bf16* o;     // attention output [M, hq]
+  float* lse;  // [B, H, s]
+  bf16* h;     // after attention residual [M, d]
+  bf16* z;     // mlp-norm output [M, d]
+  float* r2;   // [M]
+  bf16* gu;    // gate | up [M, 2f]
+  bf16* a;     // silu(g) * u [M, f]
+};
+
+struct Job {
+  int unit;
+  int slab;
+  int64_t t;
+};
+
+}  // namespace
+}  // namespace mt
+
+struct mt_handle {
+  mt_config cfg;
+  mt::FlatLayout lay;
+  float *master, *adam_m, *adam_v, *grad;
+  int64_t n_total;
+  int threads;
+  int64_t t = 0;  // Adam steps taken
+  int broken = 0;
+  std::string err;
+
+  // dims
+  int L, d, H, Hkv, hd, f, V, qkvN, hq, nseg, Mmax, Mchunk;
+
+  // host memory (pinned)
+  uint16_t* store = nullptr;
+  std::vector<uint16_t*> staging;
+  int32_t* tok_pinned = nullptr;  // tokens | labels
+  float* loss_pinned = nullptr;
+  int32_t* flag_pinned = nullptr;
+
+  // device memory
+  void* dmem = nullptr;
+  size_t dbytes = 0;
+  mt::bf16* wbuf[2] = {nullptr, nullptr};
+  mt::bf16* resident = nullptr;
+  std::vector<mt::bf16*> slab;
+  int32_t *d_tok = nullptr, *d_lab = nullptr, *d_flag = nullptr, *d_ework = nullptr;
+  float *cos_t = nullptr, *sin_t = nullptr;
+  mt::bf16 *xa = nullptr, *xb = nullptr;
+  std::vector<mt::bf16*> ckpt;
+  std::vector<mt::Saved> saved;
+  mt::bf16 *xh = nullptr, *dz = nullptr;
+  float *rf = nullptr, *logits = nullptr, *loss_rows = nullptr, *loss_dev = nullptr;
+  float *dx32 = nullptr, *dh32 = nullptr, *dn32 = nullptr, *delta = nullptr, *npart = nullptr;
+  mt::bf16 *dxb = nullptr, *dhb = nullptr, *da = nullptr, *dgu = nullptr, *dob = nullptr, *dqkv = nullptr;
+  mt::bf16 *wT = nullptr, *tA = nullptr, *tB = nullptr;
+
+  // streams and events
+  cudaStream_t s_comp = nullptr, s_h2d = nullptr, s_d2h = nullptr;
+  cudaEvent_t ev_ready[2] = {nullptr, nullptr}, ev_free[2] = {nullptr, nullptr};
+  std::vector<cudaEvent_t> ev_slab_ready, ev_d2h_done;
+  cudaEvent_t ev_loss = nullptr, ev_resident = nullptr;
+  int slot_unit[2] = {-1, -1};
+  int slot_last_use[2] = {0, 0};
+  int use_clock = 0;
+  int next_slab = 0;
+
+  // worker
+  std::thread worker;
+  std::mutex mu;
+  std::condition_variable cv;
+  std::deque<mt::Job> jobs;
+  std::vector<int> staging_busy;
+  int units_done = 0;
+  int in_flight = 0;
+  bool stop = false;
+  int worker_error = 0;
+  std::string worker_msg;
+  int loss_state = 0;  // 0 unknown, 1 finite, 2 non-finite
+  int64_t inject_sleep_ms = 0, inject_fail_at = 0, deadline_ms = 600000;
+  int64_t worker_units_total = 0;
+
+  // stats
+  mt_stats st{};
+};
+
+namespace mt {
+namespace {
+
+void set_err(mt_handle* h, const std::string& m) {
+  if (h) h->err = m;
+  g_thread_error = m;
+}
+
+// ------------------------------------------------------------------ worker
+void worker_main(mt_handle* h) {
+  for (;;) {
+    Job job;
+    {
+      std::unique_lock<std::mutex> lk(h->mu);
+      h->cv.wait(lk, [&] { return h->stop || !h->jobs.empty(); });
+      if (h->stop && h->jobs.empty()) return;
+      job = h->jobs.front();
+      h->jobs.pop_front();
+      h->in_flight = 1;
+    }
+    int code = MT_OK;
+    std::string msg;
+    const auto t0 = Clock::now();
+    const auto deadline = t0 + std::chrono::milliseconds(h->deadline_ms);
+    if (h->inject_sleep_ms > 0) std::this_thread::sleep_for(std::chrono::milliseconds(h->inject_sleep_ms));
+    ++h->worker_units_total;
+    if (h->inject_fail_at > 0 && h->worker_units_total == h->inject_fail_at) {
+      code = MT_EWORKER;
+      msg = "injected worker failure";
+    }
+    // wait for the slab copy (and, once per step, the loss) to land
+    auto wait_event = [&](cudaEvent_t ev) -> bool {
+      for (;;) {
+        cudaError_t q = cudaEventQuery(ev);
+        if (q == cudaSuccess) return true;
+        if (q != cudaErrorNotReady) {
+          code = MT_ECUDA;
+          msg = std::string("worker event query: ") + cudaGetErrorString(q);
+          return false;
+        }
+        if (Clock::now() > deadline) {
+          code = MT_ETIMEOUT;
+          msg = "worker timed out waiting for a device-to-host copy";
+          return false;
+        }
+        std::this_thread::sleep_for(std::chrono::microseconds(20));
+      }
+    };
+    if (code == MT_OK && wait_event(h->ev_d2h_done[job.slab]) && h->loss_state == 0 && wait_event(h->ev_loss)) {
+      const float total = *h->loss_pinned;
+      h->loss_state = std::isfinite(total) ? 1 : 2;
+    }
+    if (code == MT_OK) {
+      AdamArgs a;
+      const int64_t off = h->lay.unit_off[job.unit];
+      a.w = h->master + off;
+      a.m = h->adam_m + off;
+      a.v = h->adam_v + off;
+      a.grad_out = h->grad + off;
+      a.grad_in = nullptr;
+      a.slab = h->staging[job.slab];
+      a.store = h->store + off;
+      a.n = h->lay.unit_len[job.unit];
+      a.t = job.t;
+      a.lr = h->cfg.lr;
+      a.beta1 = h->cfg.beta1;
+      a.beta2 = h->cfg.beta2;
+      a.eps = h->cfg.adam_eps;
+      a.apply = h->loss_state == 1;
+      adam_pass(a, h->threads);
+    }
+    {
+      std::lock_guard<std::mutex> lk(h->mu);
+      h->st.host_adam_s += seconds_since(t0);
+      h->staging_busy[job.slab] = 0;
+      h->in_flight = 0;
+      ++h->units_done;
+      if (code != MT_OK && h->worker_error == 0) {
+        h->worker_error = code;
+        h->worker_msg = msg;
+      }
+    }
+    h->cv.notify_all();
+  }
+}
+
+// ------------------------------------------------------------ the step
+struct Step {
+  mt_handle* h;
+  int B, s, M;
+  int64_t t_next;
+  long long ldT;  // row pitch of transposed activations: M rounded up to 8
+
+  cudaStream_t cs() const { return h->s_comp; }
+
+  // Make unit `u`'s weights usable on the compute stream; returns its base.
+  bf16* acquire(int u) {
+    if (!h->cfg.streamed) return h->resident + h->lay.unit_off[u];
+    int slot = -1;
+    for (int i = 0; i < 2; ++i)
+      if (h->slot_unit[i] == u) slot = i;
+    if (slot < 0) {
+      slot = h->slot_last_use[0] <= h->slot_last_use[1] ? 0 : 1;
+      const size_t bytes = sizeof(uint16_t) * h->lay.unit_len[u];
+      CK(cudaStreamWaitEvent(h->s_h2d, h->ev_free[slot], 0));
+      CK(cudaMemcpyAsync(h->wbuf[slot], h->store + h->lay.unit_off[u], bytes, cudaMemcpyHostToDevice, h->s_h2d));
+      CK(cudaEventRecord(h->ev_ready[slot], h->s_h2d));
+      h->slot_unit[slot] = u;
+      h->st.h2d_bytes += (int64_t)bytes;
+      h->st.h2d_units += 1;
+    }
+    h->slot_last_use[slot] = ++h->use_clock;
+    CK(cudaStreamWaitEvent(h->s_comp, h->ev_ready[slot], 0));
+    cur_slot = slot;
+    return h->wbuf[slot];
+  }
+  int cur_slot = -1;
+  void release() {
+    if (h->cfg.streamed && cur_slot >= 0) CK(cudaEventRecord(h->ev_free[cur_slot], h->s_comp));
+    cur_slot = -1;
+  }
+
+  // Take the next slab for a unit's weight gradients.
+  int slab_begin() {
+    const int k = h->next_slab;
+    h->next_slab = (h->next_slab + 1) % h->cfg.n_slabs;
+    CK(cudaStreamWaitEvent(h->s_comp, h->ev_d2h_done[k], 0));
+    return k;
+  }
+  // Ship slab k of unit u to the host and queue it for the worker.
+  void slab_end(int k, int u) {
+    CK(cudaEventRecord(h->ev_slab_ready[k], h->s_comp));
+    // back-pressure: staging k must have been consumed by the worker
+    const auto t0 = Clock::now();
+    {
+      std::unique_lock<std::mutex> lk(h->mu);
+      const bool ok = h->cv.wait_for(lk, std::chrono::milliseconds(h->deadline_ms),
+                                     [&] { return !h->staging_busy[k] || h->worker_error; });
+      h->st.host_wait_s += seconds_since(t0);
+      if (h->worker_error) throw StepError{h->worker_error, h->worker_msg};
+      if (!ok) throw StepError{MT_ETIMEOUT, "timed out waiting for a free gradient slab"};
+      h->staging_busy[k] = 1;
+    }
+    const size_t bytes = sizeof(uint16_t) * h->lay.unit_len[u];
+    CK(cudaStreamWaitEvent(h->s_d2h, h->ev_slab_ready[k], 0));
+    CK(cudaMemcpyAsync(h->staging[k], h->slab[k], bytes, cudaMemcpyDeviceToHost, h->s_d2h));
+    CK(cudaEventRecord(h->ev_d2h_done[k], h->s_d2h));
+    h->st.d2h_bytes += (int64_t)bytes;
+    {
+      std::lock_guard<std::mutex> lk(h->mu);
+      h->jobs.push_back(Job{u, k, t_next});
+    }
+    h->cv.notify_all();
+  }
+
+  // C[M,N] = A[M,K] * B[N,K]^T (+R)
+  void gemm(const bf16* A, long long lda, const bf16* Bm, long long ldb, void* C, long long ldc, bool f32,
+            const bf16* R, long long ldr, int m, int n, int k) {
+    KK(gemm_abt(A, lda, Bm, ldb, C, ldc, f32 ? 1 : 0, R, ldr, m, n, k, cs()));
+  }
+  // out[c, r] = in[r, c]; `rows` is M for activations (pitch ldT), else the
+  // weight's row count (pitch = rows).
+  void transpose(const bf16* in, long long ldi, bf16* out, int rows, int cols) {
+    const long long ldo = rows == M ? ldT : rows;
+    KK(mt_k_transpose(in, ldi, out, ldo, rows, cols, cs()));
+  }
+
+  // Forward of layer l with weights W; writes the saved activations into S and
+  // the layer output into x_out.
+  void layer_fwd(const bf16* W, const Saved& S, bf16* x_out) {
+    const LayerOffsets& o = h->lay.layer;
+    const int d = h->d, f = h->f;
+    KK(mt_k_rmsnorm_fwd(S.x, W + o.attn_norm, S.u, S.r1, M, d, h->cfg.rms_eps, cs()));
+    gemm(S.u, d, W + o.wqkv, d, S.qkv, h->qkvN, false, nullptr, 0, M, h->qkvN, d);
+    KK(mt_k_rope(S.qkv, h->qkvN, B, s, h->H + h->Hkv, h->hd, h->cos_t, h->sin_t, 0, cs()));
+    KK(mt_k_attn_fwd(S.qkv, h->qkvN, S.o, h->hq, S.lse, B, s, h->H, h->Hkv, h->hd, cs()));
+    gemm(S.o, h->hq, W + o.wo, h->hq, S.h, d, false, S.x, d, M, d, h->hq);
+    KK(mt_k_rmsnorm_fwd(S.h, W + o.mlp_norm, S.z, S.r2, M, d, h->cfg.rms_eps, cs()));
+    gemm(S.z, d, W + o.wgu, d, S.gu, 2 * f, false, nullptr, 0, M, 2 * f, d);
+    KK(mt_k_swiglu_fwd(S.gu, S.a, M, f, cs()));
+    gemm(S.a, f, W + o.wdown, f, x_out, d, false, S.h, d, M, d, f);
+  }
+
+  // Backward of one layer: reads dx32/dxb (gradient w.r.t. the layer output),
+  // writes the gradient w.r.t. its input back into dx32/dxb and the weight
+  // gradients into slab `g`.
+  void layer_bwd(const bf16* W, const Saved& S, bf16* g) {
+    const LayerOffsets& o = h->lay.layer;
+    const int d = h->d, f = h->f, hq = h->hq, qn = h->qkvN;
+    // down projection: dWdown = dy^T a ; da = dy Wdown
+    transpose(h->dxb, d, h->tA, M, d);
+    transpose(S.a, f, h->tB, M, f);
+    gemm(h->tA, ldT, h->tB, ldT, g + o.wdown, f, false, nullptr, 0, d, f, M);
+    transpose(W + o.wdown, f, h->wT, d, f);
+    gemm(h->dxb, d, h->wT, d, h->da, f, false, nullptr, 0, M, f, d);
+    KK(mt_k_swiglu_bwd(h->da, S.gu, h->dgu, M, f, cs()));
+    // gate/up projection
+    transpose(h->dgu, 2 * f, h->tA, M, 2 * f);
+    transpose(S.z, d, h->tB, M, d);
+    gemm(h->tA, ldT, h->tB, ldT, g + o.wgu, d, false, nullptr, 0, 2 * f, d, M);
+    transpose(W + o.wgu, d, h->wT, 2 * f, d);
+    gemm(h->dgu, 2 * f, h->wT, 2 * f, h->dn32, d, true, nullptr, 0, M, d, 2 * f);
+    KK(mt_k_rmsnorm_bwd(h->dn32, S.h, W + o.mlp_norm, S.r2, h->dx32, h->dh32, h->dhb, h->npart, g + o.mlp_norm, M,
+                        d, cs()));
+    // output projection
+    transpose(h->dhb, d, h->tA, M, d);
+    transpose(S.o, hq, h->tB, M, hq);
+    gemm(h->tA, ldT, h->tB, ldT, g + o.wo, hq, false, nullptr, 0, d, hq, M);
+    transpose(W + o.wo, hq, h->wT, d, hq);
+    gemm(h->dhb, d, h->wT, d, h->dob, hq, false, nullptr, 0, M, hq, d);
+    // attention and RoPE
+    KK(mt_k_attn_bwd(S.qkv, qn, S.o, hq, h->dob, hq, S.lse, h->delta, h->dqkv, qn, B, s, h->H, h->Hkv, h->hd, cs()));
+    KK(mt_k_rope(h->dqkv, qn, B, s, h->H + h->Hkv, h->hd, h->cos_t, h->sin_t, 1, cs()));
+    // qkv projection
+    transpose(h->dqkv, qn, h->tA, M, qn);
+    transpose(S.u, d, h->tB, M, d);
+    gemm(h->tA, ldT, h->tB, ldT, g + o.wqkv, d, false, nullptr, 0, qn, d, M);
+    transpose(W + o.wqkv, d, h->wT, qn, d);
+    gemm(h->dqkv, qn, h->wT, qn, h->dn32, d, true, nullptr, 0, M, d, qn);
+    KK(mt_k_rmsnorm_bwd(h->dn32, S.x, W + o.attn_norm, S.r1, h->dh32, h->dx32, h->dxb, h->npart, g + o.attn_norm, M,
+                        d, cs()));
+  }
+
+  // Final norm, logits, cross entropy and their backward (head unit).
+  void head(const bf16* W, const bf16* xL, bf16* g) {
+    const int d = h->d, V = h->V;
+    const bf16* wf = W + h->lay.final_norm;
+    const bf16* head = W + h->lay.head;
+    KK(mt_k_rmsnorm_fwd(xL, wf, h->xh, h->rf, M, d, h->cfg.rms_eps, cs()));
+    const float scale = 1.f / (float)M;
+    for (int r0 = 0; r0 < M; r0 += h->Mchunk) {
+      const int mc = std::min(h->Mchunk, M - r0);
+      gemm(h->xh + (size_t)r0 * d, d, head, d, h->logits, V, true, nullptr, 0, mc, V, d);
+      KK(mt_k_cross_entropy(h->logits, V, h->d_lab + r0, h->dz + (size_t)r0 * V, V, h->loss_rows + r0, mc, V, scale,
+                            cs()));
+    }
+    KK(mt_k_sum(h->loss_rows, M, h->loss_dev, cs()));
+    CK(cudaMemcpyAsync(h->loss_pinned, h->loss_dev, sizeof(float), cudaMemcpyDeviceToHost, cs()));
+    CK(cudaEventRecord(h->ev_loss, cs()));
+    // dHead = dz^T xh ; dxh = dz Head
+    transpose(h->dz, V, h->tA, M, V);
+    transpose(h->xh, d, h->tB, M, d);
+    gemm(h->tA, ldT, h->tB, ldT, g + h->lay.head, d, false, nullptr, 0, V, d, M);
+    transpose(head, d, h->wT, V, d);
+    gemm(h->dz, V, h->wT, V, h->dn32, d, true, nullptr, 0, M, d, V);
+    KK(mt_k_rmsnorm_bwd(h->dn32, xL, wf, h->rf, nullptr, h->dx32, h->dxb, h->npart, g + h->lay.final_norm, M, d,
+                        cs()));
+  }
+
+  void run() {
+    mt_handle& hh = *h;
+    const int L = hh.L, C = hh.cfg.ckpt_interval;
+    hh.loss_state = 0;
+    if (!hh.cfg.streamed) {
+      const size_t bytes = sizeof(uint16_t) * hh.n_total;
+      CK(cudaMemcpyAsync(hh.resident, hh.store, bytes, cudaMemcpyHostToDevice, hh.s_h2d));
+      CK(cudaEventRecord(hh.ev_resident, hh.s_h2d));
+      CK(cudaStreamWaitEvent(hh.s_comp, hh.ev_resident, 0));
+      hh.st.h2d_bytes += (int64_t)bytes;
+      hh.st.h2d_units += L + 2;
+    }
+    // ---- forward: embedding, layers (checkpoint every C), head
+    {
+      bf16* E = acquire(0);
+      KK(mt_k_embedding_fwd(E + (hh.lay.embed - hh.lay.unit_off[0]), hh.d_tok, hh.ckpt[0], M, hh.d, hh.V, cs()));
+      release();
+    }
+    bf16* x = hh.ckpt[0];
+    for (int l = 0; l < L; ++l) {
+      bf16* W = acquire(1 + l);
+      Saved S = hh.saved[0];
+      S.x = x;
+      bf16* out;
+      if ((l + 1) % C == 0 && l + 1 < L) out = hh.ckpt[(l + 1) / C];
+      else out = (x == hh.xa) ? hh.xb : hh.xa;
+      layer_fwd(W, S, out);
+      release();
+      x = out;
+    }
+    {
+      bf16* W = acquire(L + 1);
+      const int k = slab_begin();
+      head(W, x, hh.slab[k]);
+      release();
+      slab_end(k, L + 1);
+    }
+    // ---- backward over segments, last to first, recomputing each
+    for (int seg = hh.nseg - 1; seg >= 0; --seg) {
+      const int a = seg * C, b = std::min(L, a + C);
+      for (int l = a; l < b; ++l) {
+        bf16* W = acquire(1 + l);
+        Saved& S = hh.saved[l - a];
+        if (l == a) S.x = hh.ckpt[seg];
+        bf16* out = (l + 1 < b) ? hh.saved[l + 1 - a].x : hh.xa;
+        layer_fwd(W, S, out);
+        release();
+      }
+      for (int l = b - 1; l >= a; --l) {
+        bf16* W = acquire(1 + l);
+        const int k = slab_begin();
+        layer_bwd(W, hh.saved[l - a], hh.slab[k]);
+        release();
+        slab_end(k, 1 + l);
+      }
+    }
+    {
+      const int k = slab_begin();
+      KK(mt_k_embedding_bwd(hh.dx32, hh.d_tok, hh.slab[k] + 0, M, hh.d, hh.V, hh.d_ework, cs()));
+      slab_end(k, 0);
+    }
+  }
+};
+
+void destroy_resources(mt_handle* h) {
+  if (h->worker.joinable()) {
+    {
+      std::lock_guard<std::mutex> lk(h->mu);
+      h->stop = true;
+    }
+    h->cv.notify_all();
+    h->worker.join();
+  }
+  if (h->s_comp) cudaStreamSynchronize(h->s_comp);
+  if (h->s_h2d) cudaStreamSynchronize(h->s_h2d);
+  if (h->s_d2h) cudaStreamSynchronize(h->s_d2h);
+  for (int i = 0; i < 2; ++i) {
+    if (h->ev_ready[i]) cudaEventDestroy(h->ev_ready[i]);
+    if (h->ev_free[i]) cudaEventDestroy(h->ev_free[i]);
+  }
+  for (auto e : h->ev_slab_ready) if (e) cudaEventDestroy(e);
+  for (auto e : h->ev_d2h_done) if (e) cudaEventDestroy(e);
+  if (h->ev_loss) cudaEventDestroy(h->ev_loss);
+  if (h->ev_resident) cudaEventDestroy(h->ev_resident);
+  if (h->s_comp) cudaStreamDestroy(h->s_comp);
+  if (h->s_h2d) cudaStreamDestroy(h->s_h2d);
+  if (h->s_d2h) cudaStreamDestroy(h->s_d2h);
+  if (h->dmem) cudaFree(h->dmem);
+  if (h->store) cudaFreeHost(h->store);
+  for (auto p : h->staging) if (p) cudaFreeHost(p);
+  if (h->tok_pinned) cudaFreeHost(h->tok_pinned);
+  if (h->loss_pinned) cudaFreeHost(h->loss_pinned);
+  if (h->flag_pinned) cudaFreeHost(h->flag_pinned);
+}
+
+// Lay out all device buffers in one arena (first pass measures, second assigns).
+void plan_device(mt_handle* h, Arena& A) {
+  const size_t M = (size_t)h->Mmax, d = h->d, f = h->f, V = h->V, qn = h->qkvN, hq = h->hq;
+  const size_t H = h->H;
+  if (h->cfg.streamed) {
+    h->wbuf[0] = take<bf16>(A, h->lay.max_unit);
+    h->wbuf[1] = take<bf16>(A, h->lay.max_unit);
+  } else {
+    h->resident = take<bf16>(A, h->n_total);
+  }
+  h->slab.assign(h->cfg.n_slabs, nullptr);
+  for (auto& p : h->slab) p = take<bf16>(A, h->lay.max_unit);
+  h->d_tok = take<int32_t>(A, 2 * M);
+  h->d_lab = h->d_tok + M;
+  h->d_flag = take<int32_t>(A, 4);
+  h->d_ework = take<int32_t>(A, (size_t)mt_k_embedding_bwd_work((int)M, (int)V));
+  h->cos_t = take<float>(A, (size_t)h->cfg.max_seq * (h->hd / 2));
+  h->sin_t = take<float>(A, (size_t)h->cfg.max_seq * (h->hd / 2));
+  h->xa = take<bf16>(A, M * d);
+  h->xb = take<bf16>(A, M * d);
+  h->ckpt.assign(h->nseg, nullptr);
+  for (auto& p : h->ckpt) p = take<bf16>(A, M * d);
+  const int slots = std::min(h->cfg.ckpt_interval, h->L);
+  h->saved.assign(slots, Saved{});
+  for (int i = 0; i < slots; ++i) {
+    Saved& S = h->saved[i];
+    S.x = take<bf16>(A, M * d);
+    S.u = take<bf16>(A, M * d);
+    S.r1 = take<float>(A, M);
+    S.qkv = take<bf16>(A, M * qn);
+    S.o = take<bf16>(A, M * hq);
+    S.lse = take<float>(A, M * H);
+    S.h = take<bf16>(A, M * d);
+    S.z = take<bf16>(A, M * d);
+    S.r2 = take<float>(A, M);
+    S.gu = take<bf16>(A, M * 2 * f);
+    S.a = take<bf16>(A, M * f);
+  }
+  h->xh = take<bf16>(A, M * d);
+  h->rf = take<float>(A, M);
+  h->logits = take<float>(A, (size_t)h->Mchunk * V);
+  h->dz = take<bf16>(A, M * V);
+  h->loss_rows = take<float>(A, M);
+  h->loss_dev = take<float>(A, 4);
+  h->dx32 = take<float>(A, M * d);
+  h->dh32 = take<float>(A, M * d);
+  h->dn32 = take<float>(A, M * d);
+  h->dxb = take<bf16>(A, M * d);
+  h->dhb = take<bf16>(A, M * d);
+  h->da = take<bf16>(A, M * f);
+  h->dgu = take<bf16>(A, M * 2 * f);
+  h->dob = take<bf16>(A, M * hq);
+  h->dqkv = take<bf16>(A, M * qn);
+  h->delta = take<float>(A, M * H);
+  h->npart = take<float>(A, (size_t)mt_k_rmsnorm_bwd_parts((int)M) * d);
+  const size_t wmax = std::max({qn * d, hq * d, 2 * f * d, d * f, V * d});
+  h->wT = take<bf16>(A, wmax);
+  const size_t cmax = std::max({d, qn, hq, 2 * f, V});
+  const size_t ldT = (M + 7) / 8 * 8;
+  h->tA = take<bf16>(A, cmax * ldT);
+  h->tB = take<bf16>(A, std::max({d, f, hq}) * ldT);
+}
+
+int fail(mt_handle* h, int code, const std::string& msg) {
+  set_err(h, msg);
+  return code;
+}
+
+}  // namespace
+}  // namespace mt
+
+using namespace mt;
+
+extern "C" {
+
+int mt_layout(const mt_config* cfg, mt_tensor_desc* out, int cap, int* n_out, int64_t* n_total) {
+  const char* why = nullptr;
+  if (!cfg || !config_valid(*cfg, &why)) return fail(nullptr, MT_EINVAL, why ? why : "null config");
+  FlatLayout L = build_layout(*cfg);
+  const int n = (int)L.tensors.size();
+  if (n_out) *n_out = n;
+  if (n_total) *n_total = L.n_total;
+  if (out) {
+    for (int i = 0; i < n && i < cap; ++i) {
+      const TensorDesc& t = L.tensors[i];
+      out[i].unit = t.unit;
+      out[i].kind = t.kind;
+      out[i].offset = t.offset;
+      out[i].rows = t.rows;
+      out[i].cols = t.cols;
+      std::memcpy(out[i].name, t.name, sizeof(out[i].name));
+    }
+  }
+  return MT_OK;
+}
+
+int mt_unit_range(const mt_config* cfg, int unit, int64_t* offset, int64_t* length) {
+  const char* why = nullptr;
+  if (!cfg || !config_valid(*cfg, &why)) return fail(nullptr, MT_EINVAL, why ? why : "null config");
+  if (unit < 0 || unit > cfg->n_layers + 1) return fail(nullptr, MT_EINVAL, "unit out of range");
+  FlatLayout L = build_layout(*cfg);
+  if (offset) *offset = L.unit_off[unit];
+  if (length) *length = L.unit_len[unit];
+  return MT_OK;
+}
+
+int mt_debug_inject_global(int what, int64_t value) {
+  if (what == 4) {
+    g_fail_next_alloc.store(value ? 1 : 0);
+    return MT_OK;
+  }
+  return MT_EINVAL;
+}
+
+int mt_init(const mt_config* cfg, float* master, float* adam_m, float* adam_v, float* grad, int64_t n_total,
+            mt_handle** out) {
+  if (!out) return fail(nullptr, MT_EINVAL, "null output handle");
+  *out = nullptr;
+  const char* why = nullptr;
+  if (!cfg || !config_valid(*cfg, &why)) return fail(nullptr, MT_EINVAL, why ? why : "null config");
+  if (!master || !adam_m || !adam_v || !grad) return fail(nullptr, MT_EINVAL, "null host state array");
+  mt_handle* h = new (std::nothrow) mt_handle();
+  if (!h) return fail(nullptr, MT_ENOMEM, "out of host memory");
+  h->cfg = *cfg;
+  h->lay = build_layout(*cfg);
+  if (n_total != h->lay.n_total) {
+    delete h;
+    return fail(nullptr, MT_EINVAL, "n_total does not match the layout");
+  }
+  h->master = master;
+  h->adam_m = adam_m;
+  h->adam_v = adam_v;
+  h->grad = grad;
+  h->n_total = n_total;
+  h->threads = cfg->host_threads > 0 ? cfg->host_threads : default_threads();
+  h->L = cfg->n_layers;
+  h->d = cfg->d_model;
+  h->H = cfg->n_heads;
+  h->Hkv = cfg->n_kv_heads;
+  h->hd = cfg->head_dim;
+  h->f = cfg->ffn_dim;
+  h->V = cfg->vocab;
+  h->qkvN = (h->H + 2 * h->Hkv) * h->hd;
+  h->hq = h->H * h->hd;
+  h->nseg = (h->L + cfg->ckpt_interval - 1) / cfg->ckpt_interval;
+  h->Mmax = cfg->max_batch * cfg->max_seq;
+  {
+    int64_t mc = (1LL << 28) / h->V;
+    mc = mc / 128 * 128;
+    if (mc < 128) mc = 128;
+    h->Mchunk = (int)std::min<int64_t>(mc, h->Mmax);
+  }
+  try {
+    if (g_fail_next_alloc.exchange(0)) throw StepError{MT_ENOMEM, "injected device allocation failure"};
+    CK(cudaSetDevice(cfg->device));
+    // device arena: measure, allocate, assign
+    Arena probe;
+    probe.cap = ~size_t(0) >> 1;
+    plan_device(h, probe);
+    Arena A;
+    if (cudaMalloc(&h->dmem, probe.used) != cudaSuccess) {
+      cudaGetLastError();
+      throw StepError{MT_ENOMEM, "device allocation of " + std::to_string(probe.used) + " bytes failed"};
+    }
+    h->dbytes = probe.used;
+    A.base = (uint8_t*)h->dmem;
+    A.cap = probe.used;
+    plan_device(h, A);
+    // pinned host memory
+    auto pin = [&](void** p, size_t bytes) {
+      if (cudaHostAlloc(p, bytes, cudaHostAllocDefault) != cudaSuccess) {
+        cudaGetLastError();
+        *p = nullptr;
+        throw StepError{MT_ENOMEM, "pinned allocation of " + std::to_string(bytes) + " bytes failed"};
+      }
+      h->st.pinned_bytes += (int64_t)bytes;
+    };
+    pin((void**)&h->store, sizeof(uint16_t) * n_total);
+    h->staging.assign(cfg->n_slabs, nullptr);
+    for (auto& p : h->staging) pin((void**)&p, sizeof(uint16_t) * h->lay.max_unit);
+    pin((void**)&h->tok_pinned, sizeof(int32_t) * 2 * h->Mmax);
+    pin((void**)&h->loss_pinned, sizeof(float) * 4);
+    pin((void**)&h->flag_pinned, sizeof(int32_t) * 4);
+    emit_bf16(master, h->store, n_total, h->threads);
+    // streams and events
+    CK(cudaStreamCreateWithFlags(&h->s_comp, cudaStreamNonBlocking));
+    CK(cudaStreamCreateWithFlags(&h->s_h2d, cudaStreamNonBlocking));
+    CK(cudaStreamCreateWithFlags(&h->s_d2h, cudaStreamNonBlocking));
+    for (int i = 0; i < 2; ++i) {
+      CK(cudaEventCreateWithFlags(&h->ev_ready[i], cudaEventDisableTiming));
+      CK(cudaEventCreateWithFlags(&h->ev_free[i], cudaEventDisableTiming));
+    }
+    h->ev_slab_ready.assign(cfg->n_slabs, nullptr);
+    h->ev_d2h_done.assign(cfg->n_slabs, nullptr);
+    for (int k = 0; k < cfg->n_slabs; ++k) {
+      CK(cudaEventCreateWithFlags(&h->ev_slab_ready[k], cudaEventDisableTiming));
+      CK(cudaEventCreateWithFlags(&h->ev_d2h_done[k], cudaEventDisableTiming));
+    }
+    CK(cudaEventCreateWithFlags(&h->ev_loss, cudaEventDisableTiming));
+    CK(cudaEventCreateWithFlags(&h->ev_resident, cudaEventDisableTiming));
+    // RoPE tables in double precision on the host
+    {
+      const int half = h->hd / 2;
+      std::vector<float> c((size_t)cfg->max_seq * half), s((size_t)cfg->max_seq * half);
+      for (int t = 0; t < cfg->max_seq; ++t)
+        for (int i = 0; i < half; ++i) {
+          const double inv = std::pow((double)cfg->rope_theta, -2.0 * i / h->hd);
+          const double ang = (double)t * inv;
+          c[(size_t)t * half + i] = (float)std::cos(ang);
+          s[(size_t)t * half + i] = (float)std::sin(ang);
+        }
+      CK(cudaMemcpy(h->cos_t, c.data(), sizeof(float) * c.size(), cudaMemcpyHostToDevice));
+      CK(cudaMemcpy(h->sin_t, s.data(), sizeof(float) * s.size(), cudaMemcpyHostToDevice));
+    }
+    h->staging_busy.assign(cfg->n_slabs, 0);
+    h->st.device_bytes = (int64_t)h->dbytes;
+    h->worker = std::thread(worker_main, h);
+  } catch (const StepError& e) {
+    set_err(nullptr, e.msg);
+    destroy_resources(h);
+    delete h;
+    return e.code;
+  } catch (const std::exception& e) {
+    set_err(nullptr, e.what());
+    destroy_resources(h);
+    delete h;
+    return MT_ENOMEM;
+  }
+  *out = h;
+  return MT_OK;
+}
+
+static int run_step(mt_handle* h, const int32_t* tokens, const int32_t* labels, int B, int s, bool on_device,
+                    float* loss_out) {
+  if (!h) return fail(nullptr, MT_EINVAL, "null handle");
+  if (h->broken) return fail(h, MT_ESTATE, "handle is unusable after an earlier timeout or device error");
+  if (!tokens || !labels || B <= 0 || s <= 0 || B > h->cfg.max_batch || s > h->cfg.max_seq)
+    return fail(h, MT_EINVAL, "bad tokens/labels or batch/seq outside the configured maxima");
+  const int M = B * s;
+  const auto t0 = Clock::now();
+  Step st{h, B, s, M, h->t + 1, ((long long)M + 7) / 8 * 8};
+  try {
+    CK(cudaSetDevice(h->cfg.device));
+    if (!on_device) {
+      for (int i = 0; i < M; ++i)
+        if (tokens[i] < 0 || tokens[i] >= h->V || labels[i] < 0 || labels[i] >= h->V)
+          return fail(h, MT_EINVAL, "token or label id outside [0, vocab)");
+      std::memcpy(h->tok_pinned, tokens, sizeof(int32_t) * M);
+      std::memcpy(h->tok_pinned + M, labels, sizeof(int32_t) * M);
+      CK(cudaMemcpyAsync(h->d_tok, h->tok_pinned, sizeof(int32_t) * M, cudaMemcpyHostToDevice, h->s_comp));
+      CK(cudaMemcpyAsync(h->d_lab, h->tok_pinned + M, sizeof(int32_t) * M, cudaMemcpyHostToDevice, h->s_comp));
+    } else {
+      CK(cudaMemcpyAsync(h->d_tok, tokens, sizeof(int32_t) * M, cudaMemcpyDeviceToDevice, h->s_comp));
+      CK(cudaMemcpyAsync(h->d_lab, labels, sizeof(int32_t) * M, cudaMemcpyDeviceToDevice, h->s_comp));
+      CK(cudaMemsetAsync(h->d_flag, 0, sizeof(int32_t), h->s_comp));
+      KK(mt_k_check_ids(h->d_tok, 2 * M, h->V, h->d_flag, h->s_comp));
+      CK(cudaMemcpyAsync(h->flag_pinned, h->d_flag, sizeof(int32_t), cudaMemcpyDeviceToHost, h->s_comp));
+      CK(cudaStreamSynchronize(h->s_comp));
+      if (*h->flag_pinned) return fail(h, MT_EDEVICE, "token or label id outside [0, vocab) (device check)");
+    }
+    {
+      std::lock_guard<std::mutex> lk(h->mu);
+      h->units_done = 0;
+      h->worker_error = 0;
+      h->worker_msg.clear();
+    }
+    st.run();
+    // wait for the worker to finish every unit of this step
+    {
+      std::unique_lock<std::mutex> lk(h->mu);
+      const bool ok = h->cv.wait_for(lk, std::chrono::milliseconds(h->deadline_ms),
+                                     [&] { return h->units_done == h->L + 2 || h->worker_error; });
+      if (h->worker_error) throw StepError{h->worker_error, h->worker_msg};
+      if (!ok) throw StepError{MT_ETIMEOUT, "timed out waiting for the host optimizer"};
+    }
+    CK(cudaStreamSynchronize(h->s_comp));
+    CK(cudaStreamSynchronize(h->s_d2h));
+    CK(cudaStreamSynchronize(h->s_h2d));
+    int dev_err = 0;
+    if (mt_k_device_error(&dev_err, 1) != MT_OK) throw StepError{MT_ECUDA, "reading the device error word failed"};
+    if (dev_err) throw StepError{MT_EDEVICE, "a kernel reported device error " + std::to_string(dev_err)};
+  } catch (const StepError& e) {
+    // drain: nothing may stay in flight when the call returns
+    cudaStreamSynchronize(h->s_comp);
+    cudaStreamSynchronize(h->s_h2d);
+    cudaStreamSynchronize(h->s_d2h);
+    std::unique_lock<std::mutex> lk(h->mu);
+    h->jobs.clear();
+    const bool idle = h->cv.wait_for(lk, std::chrono::milliseconds(std::min<int64_t>(h->deadline_ms, 60000)),
+                                     [&] { return h->in_flight == 0; });
+    if (e.code == MT_ETIMEOUT || e.code == MT_EDEVICE || e.code == MT_ECUDA || !idle) h->broken = 1;
+    for (auto& b : h->staging_busy) b = 0;
+    h->err = e.msg;
+    g_thread_error = e.msg;
+    return e.code;
+  }
+  const float total = *h->loss_pinned;
+  const float loss = total / (float)M;
+  if (loss_out) *loss_out = loss;
+  h->st.steps += 1;
+  h->st.last_step_s = seconds_since(t0);
+  if (h->loss_state != 1) return fail(h, MT_ENONFINITE, "non-finite loss: no Adam update was applied");
+  h->t += 1;
+  return MT_OK;
+}
+
+int mt_train_step(mt_handle* h, const int32_t* tokens, const int32_t* labels, int32_t batch, int32_t seq,
+                  float* loss_out) {
+  return run_step(h, tokens, labels, batch, seq, false, loss_out);
+}
+
+int mt_train_step_device(mt_handle* h, const int32_t* d_tokens, const int32_t* d_labels, int32_t batch, int32_t seq,
+                         float* loss_out) {
+  return run_step(h, d_tokens, d_labels, batch, seq, true, loss_out);
+}
+
+int mt_read_grads(mt_handle* h, float* dst, int64_t n) {
+  if (!h || !dst || n < 0 || n > h->n_total) return fail(h, MT_EINVAL, "bad arguments to mt_read_grads");
+  if (dst != h->grad) std::memcpy(dst, h->grad, sizeof(float) * n);
+  return MT_OK;
+}
+
+int mt_get_step(mt_handle* h, int64_t* t) {
+  if (!h || !t) return MT_EINVAL;
+  *t = h->t;
+  return MT_OK;
+}
+
+int mt_set_step(mt_handle* h, int64_t t) {
+  if (!h || t < 0) return MT_EINVAL;
+  h->t = t;
+  return MT_OK;
+}
+
+int mt_sync_store(mt_handle* h) {
+  if (!h) return MT_EINVAL;
+  emit_bf16(h->master, h->store, h->n_total, h->threads);
+  return MT_OK;
+}
+
+int mt_get_stats(mt_handle* h, mt_stats* out) {
+  if (!h || !out) return MT_EINVAL;
+  std::lock_guard<std::mutex> lk(h->mu);
+  *out = h->st;
+  return MT_OK;
+}
+
+int mt_get_stream(mt_handle* h, int which, void** stream) {
+  if (!h || !stream || which < 0 || which > 2) return MT_EINVAL;
+  *stream = which == 0 ? (void*)h->s_comp : which == 1 ? (void*)h->s_h2d : (void*)h->s_d2h;
+  return MT_OK;
+}
+
+int mt_destroy(mt_handle* h) {
+  if (!h) return MT_EINVAL;
+  destroy_resources(h);
+  delete h;
+  return MT_OK;
+}
+
+const char* mt_last_error(mt_handle* h) { return h ? h->err.c_str() : g_thread_error.c_str(); }
+
+int mt_debug_inject(mt_handle* h, int what, int64_t value) {
+  if (!h) return MT_EINVAL;
+  std::lock_guard<std::mutex> lk(h->mu);
+  switch (what) {
+    case 1: h->inject_sleep_ms = value; return MT_OK;
+    case 2: h->inject_fail_at = value > 0 ? h->worker_units_total + value : 0; return MT_OK;
+    case 3: h->deadline_ms = value > 0 ? value : 600000; return MT_OK;
+    default: return MT_EINVAL;
+  }
+}
+
+int mt_host_adam(float* w, float* m, float* v, const float* g, uint16_t* store, int64_t n, int64_t t, float lr,
+                 float beta1, float beta2, float eps, int threads) {
+  if (!w || !m || !v || !g || n < 0 || t < 1) return MT_EINVAL;
+  AdamArgs a{};
+  a.w = w;
+  a.m = m;
+  a.v = v;
+  a.grad_out = nullptr;
+  a.grad_in = g;
+  a.slab = nullptr;
+  a.store = store;
+  a.n = n;
+  a.t = t;
+  a.lr = lr;
+  a.beta1 = beta1;
+  a.beta2 = beta2;
+  a.eps = eps;
+  a.apply = true;
+  adam_pass(a, threads > 0 ? threads : default_threads());
+  return MT_OK;
+}
+
+int mt_host_to_bf16(const float* src, uint16_t* dst, int64_t n) {
+  if (!src || !dst || n < 0) return MT_EINVAL;
+  emit_bf16(src, dst, n, default_threads());
+  return MT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,151 @@
+// Host-side arithmetic of the step: the flat layout, round-to-nearest-even
+// fp32 -> bf16, and the fused "slab accumulate + Adam + bf16 emit" pass the
+// worker thread runs per unit. Plain C++ with OpenMP; portable (no ISA
+// intrinsics) so it builds the same on x86-64 and on Grace (aarch64).
+//
+// Placement follows the RAM-centric method: FP32 master, grad, m and v live in
+// host memory and Adam runs on the CPU (zhichai.net article,
+// "以内存为中心的训练新范式" point 1; lqnn.cn article section 二,
+// ParameterState and the SIMD CPU Adam); slab contents are added into the FP32
+// master gradient by a CPU worker (lqnn.cn article section 三.3).
+#include <omp.h>
+
+#include <cmath>
+#include <cstring>
+
+#include "host_math.h"
+
+namespace mt {
+
+static int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+bool config_valid(const mt_config& c, const char** why) {
+  auto bad = [&](const char* w) {
+    if (why) *why = w;
+    return false;
+  };
+  if (c.n_layers <= 0) return bad("n_layers must be > 0");
+  if (c.d_model <= 0 || c.d_model % 64) return bad("d_model must be a positive multiple of 64");
+  if (c.n_heads <= 0 || c.n_kv_heads <= 0 || c.n_heads % c.n_kv_heads) return bad("n_kv_heads must divide n_heads");
+  if (c.head_dim != 16 && c.head_dim != 64 && c.head_dim != 128) return bad("head_dim must be 16, 64 or 128");
+  if (c.ffn_dim <= 0 || c.ffn_dim % 64) return bad("ffn_dim must be a positive multiple of 64");
+  if (c.vocab <= 0 || c.vocab % 8) return bad("vocab must be a positive multiple of 8");
+  if (c.max_batch <= 0 || c.max_seq <= 0) return bad("max_batch and max_seq must be > 0");
+  if ((int64_t)c.max_batch * c.max_seq > (1LL << 30)) return bad("max_batch * max_seq too large");
+  if (c.ckpt_interval < 1) return bad("ckpt_interval must be >= 1");
+  if (c.n_slabs < 2) return bad("n_slabs must be >= 2");
+  if (!(c.rms_eps > 0.f) || !(c.rope_theta > 0.f)) return bad("rms_eps and rope_theta must be > 0");
+  if (!(c.lr >= 0.f) || !(c.beta1 >= 0.f && c.beta1 < 1.f) || !(c.beta2 >= 0.f && c.beta2 < 1.f) ||
+      !(c.adam_eps >= 0.f))
+    return bad("bad Adam hyper-parameters");
+  return true;
+}
+
+FlatLayout build_layout(const mt_config& c) {
+  FlatLayout L;
+  const int64_t d = c.d_model, V = c.vocab, f = c.ffn_dim;
+  const int64_t qkv = (int64_t)(c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
+  const int64_t hq = (int64_t)c.n_heads * c.head_dim;
+  int64_t cur = 0;
+  auto tensor = [&](int unit, int kind, const char* name, int64_t rows, int64_t cols) {
+    cur = round_up(cur, kAlign);
+    TensorDesc t;
+    t.unit = unit;
+    t.kind = kind;
+    t.offset = cur;
+    t.rows = rows;
+    t.cols = cols;
+    std::strncpy(t.name, name, sizeof(t.name) - 1);
+    t.name[sizeof(t.name) - 1] = 0;
+    L.tensors.push_back(t);
+    cur += rows * cols;
+    return t.offset;
+  };
+  auto close_unit = [&](int64_t start) {
+    cur = round_up(cur, kAlign);
+    L.unit_off.push_back(start);
+    L.unit_len.push_back(cur - start);
+  };
+  int64_t s0 = cur;
+  L.embed = tensor(0, 0, "embed", V, d);
+  close_unit(s0);
+  for (int l = 0; l < c.n_layers; ++l) {
+    s0 = cur;
+    LayerOffsets o;
+    o.attn_norm = tensor(1 + l, 1, "attn_norm", d, 1) - s0;
+    o.wqkv = tensor(1 + l, 0, "wqkv", qkv, d) - s0;
+    o.wo = tensor(1 + l, 0, "wo", d, hq) - s0;
+    o.mlp_norm = tensor(1 + l, 1, "mlp_norm", d, 1) - s0;
+    o.wgu = tensor(1 + l, 0, "wgu", 2 * f, d) - s0;
+    o.wdown = tensor(1 + l, 0, "wdown", d, f) - s0;
+    L.layer = o;  // identical relative offsets for every layer
+    close_unit(s0);
+  }
+  s0 = cur;
+  L.final_norm = tensor(c.n_layers + 1, 1, "final_norm", d, 1) - s0;
+  L.head = tensor(c.n_layers + 1, 0, "head", V, d) - s0;
+  close_unit(s0);
+  L.n_total = cur;
+  L.max_unit = 0;
+  for (int64_t n : L.unit_len) L.max_unit = n > L.max_unit ? n : L.max_unit;
+  return L;
+}
+
+uint16_t to_bf16_rne(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return 0x7fc0;  // NaN
+  const uint32_t lsb = (u >> 16) & 1u;
+  u += 0x7fffu + lsb;
+  return (uint16_t)(u >> 16);
+}
+
+static inline float bf16_to_f32(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return f;
+}
+
+void emit_bf16(const float* src, uint16_t* dst, int64_t n, int threads) {
+#pragma omp parallel for schedule(static) num_threads(threads)
+  for (int64_t i = 0; i < n; ++i) dst[i] = to_bf16_rne(src[i]);
+}
+
+void adam_pass(const AdamArgs& a, int threads) {
+  const double bc1 = 1.0 - std::pow((double)a.beta1, (double)a.t);
+  const double bc2 = 1.0 - std::pow((double)a.beta2, (double)a.t);
+  const float lr = a.lr, b1 = a.beta1, b2 = a.beta2, eps = a.eps;
+  const float inv_bc1 = (float)(1.0 / bc1);
+  const float inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
+  float* __restrict__ w = a.w;
+  float* __restrict__ m = a.m;
+  float* __restrict__ v = a.v;
+  float* __restrict__ gout = a.grad_out;
+  const float* __restrict__ gin = a.grad_in;
+  const uint16_t* __restrict__ slab = a.slab;
+  uint16_t* __restrict__ store = a.store;
+  const bool apply = a.apply;
+  const int64_t n = a.n;
+#pragma omp parallel for schedule(static) num_threads(threads)
+  for (int64_t i = 0; i < n; ++i) {
+    const float g = slab ? bf16_to_f32(slab[i]) : gin[i];
+    if (gout) gout[i] = g;
+    if (!apply) continue;
+    const float mi = b1 * m[i] + (1.f - b1) * g;
+    const float vi = b2 * v[i] + (1.f - b2) * g * g;
+    m[i] = mi;
+    v[i] = vi;
+    // m_hat / (sqrt(v_hat) + eps) with m_hat = m / bc1, v_hat = v / bc2
+    const float wi = w[i] - lr * (mi * inv_bc1) / (std::sqrt(vi) * inv_sqrt_bc2 + eps);
+    w[i] = wi;
+    if (store) store[i] = to_bf16_rne(wi);
+  }
+}
+
+int default_threads() {
+  int n = omp_get_num_procs();
+  return n > 0 ? n : 1;
+}
+
+}  // namespace mt

@@ -1,0 +1,649 @@
+// Memory-bound kernels of the stateless layer template: RMSNorm, RoPE,
+// SwiGLU, transpose, embedding gather / deterministic scatter-add, cross
+// entropy, fixed-order sums. Each is a plain streaming pass with 16-byte
+// vector accesses where the layout allows; their cost is HBM bandwidth.
+// The operators are those of a Llama-style decoder layer run through the
+// per-layer template of the zhichai.net article ("以内存为中心的训练新范式",
+// point 4) with the backward written by hand (travelaiplan blog, 核心功能
+// point 3).
+#include <cfloat>
+#include <cmath>
+#include <mutex>
+
+#include "common.cuh"
+#include "mt_internal.h"
+
+namespace mt {
+
+int* device_error_word() {
+  static int* words[64] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!words[dev]) {
+    int* p = nullptr;
+    if (cudaMalloc(&p, sizeof(int)) != cudaSuccess || cudaMemset(p, 0, sizeof(int)) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    words[dev] = p;
+  }
+  return words[dev];
+}
+
+namespace {
+
+constexpr int kNormBwdMaxVec = 4;       // 16-byte vectors per thread: d <= 8192
+constexpr int kNormBwdThreads = 256;
+constexpr int kNormBwdMaxParts = 608;   // 4 blocks per SM on 152 SMs
+
+inline int launch_ok() { return cudaGetLastError() == cudaSuccess ? MT_OK : MT_ECUDA; }
+
+__device__ __forceinline__ void load_bf16x8(const bf16* p, float (&f)[8]) {
+  uint4 u = *reinterpret_cast<const uint4*>(p);
+  float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y), c = unpack_bf16x2(u.z), d = unpack_bf16x2(u.w);
+  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y; f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+}
+
+__device__ __forceinline__ void store_bf16x8(bf16* p, const float (&f)[8]) {
+  uint4 u;
+  u.x = pack_bf16x2(f[0], f[1]);
+  u.y = pack_bf16x2(f[2], f[3]);
+  u.z = pack_bf16x2(f[4], f[5]);
+  u.w = pack_bf16x2(f[6], f[7]);
+  *reinterpret_cast<uint4*>(p) = u;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ------------------------------------------------------------ RMSNorm fwd
+// One warp per row: sum of squares, then y = x * rstd * w.
+__global__ void rmsnorm_fwd_kernel(const bf16* __restrict__ x, const bf16* __restrict__ w, bf16* __restrict__ y,
+                                   float* __restrict__ rstd, int M, int d, float eps) {
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= M) return;
+  const bf16* xr = x + (long long)row * d;
+  const int nvec = d >> 3;
+  float ss = 0.f;
+  for (int v = lane; v < nvec; v += 32) {
+    float f[8];
+    load_bf16x8(xr + v * 8, f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss += f[i] * f[i];
+  }
+  ss = warp_sum(ss);
+  const float r = rsqrtf(ss / (float)d + eps);
+  if (lane == 0) rstd[row] = r;
+  bf16* yr = y + (long long)row * d;
+  for (int v = lane; v < nvec; v += 32) {
+    float f[8], g[8];
+    load_bf16x8(xr + v * 8, f);
+    load_bf16x8(w + v * 8, g);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] = f[i] * r * g[i];
+    store_bf16x8(yr + v * 8, f);
+  }
+}
+
+// ------------------------------------------------------------ RMSNorm bwd
+// Block b handles a contiguous row range; per row: dot = sum(dy*w*x),
+// dx = rstd*w*dy - x*rstd^3*dot/d (+ dres); dw partial += dy*x*rstd.
+__global__ void __launch_bounds__(kNormBwdThreads)
+    rmsnorm_bwd_kernel(const float* __restrict__ dy, const bf16* __restrict__ x, const bf16* __restrict__ w,
+                       const float* __restrict__ rstd, const float* dres, float* dx_f32, bf16* __restrict__ dx_bf16,
+                       float* __restrict__ partial, int M, int d, int rows_per_block) {
+  __shared__ float red[kNormBwdThreads / 32];
+  const int tid = threadIdx.x;
+  const int nvec = d >> 3;
+  const int r0 = blockIdx.x * rows_per_block;
+  const int r1 = min(M, r0 + rows_per_block);
+  float wv[kNormBwdMaxVec][8];
+  float acc[kNormBwdMaxVec][8];
+#pragma unroll
+  for (int k = 0; k < kNormBwdMaxVec; ++k) {
+    const int v = tid + k * kNormBwdThreads;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { acc[k][i] = 0.f; wv[k][i] = 0.f; }
+    if (v < nvec) load_bf16x8(w + v * 8, wv[k]);
+  }
+  for (int row = r0; row < r1; ++row) {
+    const float r = rstd[row];
+    const float* dyr = dy + (long long)row * d;
+    const bf16* xr = x + (long long)row * d;
+    float dyv[kNormBwdMaxVec][8], xv[kNormBwdMaxVec][8];
+    float dot = 0.f;
+#pragma unroll
+    for (int k = 0; k < kNormBwdMaxVec; ++k) {
+      const int v = tid + k * kNormBwdThreads;
+      if (v < nvec) {
+        float4 a = reinterpret_cast<const float4*>(dyr + v * 8)[0];
+        float4 b = reinterpret_cast<const float4*>(dyr + v * 8)[1];
+        dyv[k][0] = a.x; dyv[k][1] = a.y; dyv[k][2] = a.z; dyv[k][3] = a.w;
+        dyv[k][4] = b.x; dyv[k][5] = b.y; dyv[k][6] = b.z; dyv[k][7] = b.w;
+        load_bf16x8(xr + v * 8, xv[k]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dot += dyv[k][i] * wv[k][i] * xv[k][i];
+      }
+    }
+    dot = warp_sum(dot);
+    if ((tid & 31) == 0) red[tid >> 5] = dot;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int i = 0; i < kNormBwdThreads / 32; ++i) tot += red[i];
+    __syncthreads();
+    const float c = r * r * r * tot / (float)d;
+#pragma unroll
+    for (int k = 0; k < kNormBwdMaxVec; ++k) {
+      const int v = tid + k * kNormBwdThreads;
+      if (v < nvec) {
+        float o[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          o[i] = r * wv[k][i] * dyv[k][i] - xv[k][i] * c;
+          acc[k][i] += dyv[k][i] * xv[k][i] * r;
+        }
+        const long long off = (long long)row * d + v * 8;
+        if (dres != nullptr) {
+          float4 a = reinterpret_cast<const float4*>(dres + off)[0];
+          float4 b = reinterpret_cast<const float4*>(dres + off)[1];
+          o[0] += a.x; o[1] += a.y; o[2] += a.z; o[3] += a.w;
+          o[4] += b.x; o[5] += b.y; o[6] += b.z; o[7] += b.w;
+        }
+        if (dx_f32 != nullptr) {
+          reinterpret_cast<float4*>(dx_f32 + off)[0] = make_float4(o[0], o[1], o[2], o[3]);
+          reinterpret_cast<float4*>(dx_f32 + off)[1] = make_float4(o[4], o[5], o[6], o[7]);
+        }
+        if (dx_bf16 != nullptr) store_bf16x8(dx_bf16 + off, o);
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kNormBwdMaxVec; ++k) {
+    const int v = tid + k * kNormBwdThreads;
+    if (v < nvec) {
+      float* p = partial + (long long)blockIdx.x * d + v * 8;
+      reinterpret_cast<float4*>(p)[0] = make_float4(acc[k][0], acc[k][1], acc[k][2], acc[k][3]);
+      reinterpret_cast<float4*>(p)[1] = make_float4(acc[k][4], acc[k][5], acc[k][6], acc[k][7]);
+    }
+  }
+}
+
+// dw[c] = sum over parts p (in order) of partial[p, c], rounded to bf16.
+__global__ void colsum_to_bf16_kernel(const float* __restrict__ partial, int n_part, int d, bf16* __restrict__ out) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= d) return;
+  float s = 0.f;
+  for (int p = 0; p < n_part; ++p) s += partial[(long long)p * d + c];
+  out[c] = __float2bfloat16_rn(s);
+}
+
+// ------------------------------------------------------------------ RoPE
+// Thread per (row, head, pair of adjacent rotation pairs).
+__global__ void rope_kernel(bf16* __restrict__ xbuf, long long ld, int M, int s, int nheads, int hd,
+                            const float* __restrict__ cos_t, const float* __restrict__ sin_t, float sign) {
+  const int half = hd >> 1;
+  const int quarter = half >> 1;  // thread handles pairs 2p, 2p+1
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long total = (long long)M * nheads * quarter;
+  if (idx >= total) return;
+  const int p = (int)(idx % quarter);
+  const long long rh = idx / quarter;
+  const int head = (int)(rh % nheads);
+  const int row = (int)(rh / nheads);
+  const int t = row % s;
+  bf16* base = xbuf + (long long)row * ld + (long long)head * hd;
+  const int i = 2 * p;
+  __nv_bfloat162* pa = reinterpret_cast<__nv_bfloat162*>(base + i);
+  __nv_bfloat162* pb = reinterpret_cast<__nv_bfloat162*>(base + i + half);
+  const float2 a = __bfloat1622float2(*pa);
+  const float2 b = __bfloat1622float2(*pb);
+  const float c0 = cos_t[(long long)t * half + i], c1 = cos_t[(long long)t * half + i + 1];
+  const float s0 = sign * sin_t[(long long)t * half + i], s1 = sign * sin_t[(long long)t * half + i + 1];
+  *pa = __floats2bfloat162_rn(a.x * c0 - b.x * s0, a.y * c1 - b.y * s1);
+  *pb = __floats2bfloat162_rn(b.x * c0 + a.x * s0, b.y * c1 + a.y * s1);
+}
+
+// ---------------------------------------------------------------- SwiGLU
+__device__ __forceinline__ float sigmoidf_(float g) { return 1.f / (1.f + expf(-g)); }
+
+__global__ void swiglu_fwd_kernel(const bf16* __restrict__ gu, bf16* __restrict__ a, int M, int f) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int nv = f >> 3;
+  if (idx >= (long long)M * nv) return;
+  const int row = (int)(idx / nv);
+  const int v = (int)(idx % nv);
+  const bf16* gr = gu + (long long)row * 2 * f + v * 8;
+  float g[8], u[8], o[8];
+  load_bf16x8(gr, g);
+  load_bf16x8(gr + f, u);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o[i] = g[i] * sigmoidf_(g[i]) * u[i];
+  store_bf16x8(a + (long long)row * f + v * 8, o);
+}
+
+__global__ void swiglu_bwd_kernel(const bf16* __restrict__ da, const bf16* __restrict__ gu, bf16* __restrict__ dgu,
+                                  int M, int f) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int nv = f >> 3;
+  if (idx >= (long long)M * nv) return;
+  const int row = (int)(idx / nv);
+  const int v = (int)(idx % nv);
+  const bf16* gr = gu + (long long)row * 2 * f + v * 8;
+  float g[8], u[8], d[8], dg[8], du[8];
+  load_bf16x8(gr, g);
+  load_bf16x8(gr + f, u);
+  load_bf16x8(da + (long long)row * f + v * 8, d);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float sg = sigmoidf_(g[i]);
+    dg[i] = d[i] * u[i] * sg * (1.f + g[i] * (1.f - sg));
+    du[i] = d[i] * g[i] * sg;
+  }
+  bf16* o = dgu + (long long)row * 2 * f + v * 8;
+  store_bf16x8(o, dg);
+  store_bf16x8(o + f, du);
+}
+
+// ------------------------------------------------------------- transpose
+constexpr int kTT = 64;
+__global__ void transpose_kernel(const bf16* __restrict__ in, long long ld_in, bf16* __restrict__ out,
+                                 long long ld_out, int rows, int cols) {
+  __shared__ bf16 tile[kTT][kTT + 2];
+  const int c0 = blockIdx.x * kTT, r0 = blockIdx.y * kTT;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
+  for (int i = ty; i < kTT; i += 8) {
+    const int r = r0 + i;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int c = c0 + tx + 32 * j;
+      tile[i][tx + 32 * j] = (r < rows && c < cols) ? in[(long long)r * ld_in + c] : __float2bfloat16_rn(0.f);
+    }
+  }
+  __syncthreads();
+  for (int i = ty; i < kTT; i += 8) {
+    const int c = c0 + i;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int r = r0 + tx + 32 * j;
+      if (c < cols && r < rows) out[(long long)c * ld_out + r] = tile[tx + 32 * j][i];
+    }
+  }
+}
+
+// ------------------------------------------------------------- embedding
+__global__ void embedding_fwd_kernel(const bf16* __restrict__ E, const int32_t* __restrict__ tok, bf16* __restrict__ x,
+                                     int M, int d, int V, int* err) {
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= M) return;
+  const int id = tok[row];
+  const bool ok = id >= 0 && id < V;
+  if (!ok && lane == 0) set_device_error(err, kDevErrBadToken);
+  const uint4* src = reinterpret_cast<const uint4*>(E + (long long)(ok ? id : 0) * d);
+  uint4* dst = reinterpret_cast<uint4*>(x + (long long)row * d);
+  for (int v = lane; v < (d >> 3); v += 32) dst[v] = ok ? src[v] : make_uint4(0, 0, 0, 0);
+}
+
+// Stable counting sort of token positions by id, in one CTA of 1024 threads.
+// work layout (int32): start[V + 1] | cursor[V] | perm[M].
+constexpr int kSortThreads = 1024;
+
+__device__ __forceinline__ int block_inclusive_max(int v, int* scratch) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v = max(v, n);
+  }
+  if (lane == 31) scratch[wid] = v;
+  __syncthreads();
+  if (wid == 0) {
+    int w = scratch[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w = max(w, n);
+    }
+    scratch[lane] = w;
+  }
+  __syncthreads();
+  if (wid > 0) v = max(v, scratch[wid - 1]);
+  __syncthreads();
+  return v;
+}
+
+__device__ __forceinline__ int block_exclusive_sum(int v, int* scratch, int* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += n;
+  }
+  if (lane == 31) scratch[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int w = scratch[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += n;
+    }
+    scratch[lane] = w;
+  }
+  __syncthreads();
+  const int before = (wid > 0 ? scratch[wid - 1] : 0) + x - v;
+  *total = scratch[31];
+  __syncthreads();
+  return before;
+}
+
+__global__ void __launch_bounds__(kSortThreads) token_sort_kernel(const int32_t* __restrict__ tok, int M, int V,
+                                                                  int32_t* __restrict__ work, int* err) {
+  __shared__ unsigned long long keys[kSortThreads];
+  __shared__ int scratch[32];
+  int32_t* start = work;
+  int32_t* cursor = work + V + 1;
+  int32_t* perm = cursor + V;
+  const int tid = threadIdx.x;
+  for (int v = tid; v < V; v += kSortThreads) cursor[v] = 0;
+  __syncthreads();
+  for (int m = tid; m < M; m += kSortThreads) {
+    const int id = tok[m];
+    if (id >= 0 && id < V) atomicAdd(&cursor[id], 1);
+    else set_device_error(err, kDevErrBadToken);
+  }
+  __syncthreads();
+  int carry = 0;
+  for (int v0 = 0; v0 < V; v0 += kSortThreads) {
+    const int v = v0 + tid;
+    const int c = v < V ? cursor[v] : 0;
+    int total;
+    const int ex = block_exclusive_sum(c, scratch, &total);
+    if (v < V) start[v] = carry + ex;
+    carry += total;
+  }
+  if (tid == 0) start[V] = carry;
+  for (int v = tid; v < V; v += kSortThreads) cursor[v] = 0;
+  __syncthreads();
+  for (int m0 = 0; m0 < M; m0 += kSortThreads) {
+    const int m = m0 + tid;
+    unsigned long long key = ~0ull;
+    if (m < M) {
+      const int id = tok[m];
+      if (id >= 0 && id < V) key = ((unsigned long long)(unsigned)id << 32) | (unsigned)m;
+    }
+    keys[tid] = key;
+    __syncthreads();
+    // bitonic sort of 1024 keys, ascending
+    for (int k = 2; k <= kSortThreads; k <<= 1) {
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        const int p = tid ^ j;
+        if (p > tid) {
+          const unsigned long long a = keys[tid], b = keys[p];
+          const bool up = (tid & k) == 0;
+          if ((a > b) == up) { keys[tid] = b; keys[p] = a; }
+        }
+        __syncthreads();
+      }
+    }
+    const unsigned long long me = keys[tid];
+    const bool valid = me != ~0ull;
+    const unsigned id = (unsigned)(me >> 32);
+    const bool head = tid == 0 || (keys[tid - 1] >> 32) != id;
+    const int seg = block_inclusive_max(head ? tid : 0, scratch);
+    const int rank = tid - seg;
+    if (valid) perm[start[id] + cursor[id] + rank] = (int)(me & 0xffffffffu);
+    const bool tail = tid == kSortThreads - 1 || (keys[tid + 1] >> 32) != id;
+    __syncthreads();
+    if (valid && tail) cursor[id] += rank + 1;
+    __syncthreads();
+  }
+}
+
+// dE[v, c..c+3] = sum_{p in [start[v], start[v+1])} dx[perm[p], c..c+3]
+__global__ void embedding_bwd_reduce_kernel(const float* __restrict__ dx, const int32_t* __restrict__ work,
+                                            bf16* __restrict__ dE, int d, int V) {
+  const int v = blockIdx.x;
+  const int c = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
+  if (c >= d) return;
+  const int32_t* start = work;
+  const int32_t* perm = work + 2 * V + 1;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int p1 = start[v + 1];
+  for (int p = start[v]; p < p1; ++p) {
+    const float4 x = *reinterpret_cast<const float4*>(dx + (long long)perm[p] * d + c);
+    acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+  }
+  uint2 u;
+  u.x = pack_bf16x2(acc.x, acc.y);
+  u.y = pack_bf16x2(acc.z, acc.w);
+  *reinterpret_cast<uint2*>(dE + (long long)v * d + c) = u;
+}
+
+// ---------------------------------------------------------- cross entropy
+constexpr int kCeThreads = 256;
+
+__device__ __forceinline__ void online_merge(float& m, float& s, float m2, float s2) {
+  if (m2 > m) {
+    s = s * expf(m - m2) + s2;
+    m = m2;
+  } else if (m2 != -INFINITY) {
+    s += s2 * expf(m2 - m);
+  }
+}
+
+__global__ void __launch_bounds__(kCeThreads)
+    cross_entropy_kernel(const float* __restrict__ logits, long long ldl, const int32_t* __restrict__ labels,
+                         bf16* __restrict__ dz, long long lddz, float* __restrict__ loss_rows, int V, float scale,
+                         int* err) {
+  __shared__ float sm_m[kCeThreads / 32], sm_s[kCeThreads / 32];
+  const int row = blockIdx.x;
+  const float* z = logits + (long long)row * ldl;
+  const int tid = threadIdx.x;
+  float m = -INFINITY, s = 0.f;
+  const int nv = V >> 2;
+  for (int v = tid; v < nv; v += kCeThreads) {
+    const float4 q = reinterpret_cast<const float4*>(z)[v];
+    const float mx = fmaxf(fmaxf(q.x, q.y), fmaxf(q.z, q.w));
+    const float ls = expf(q.x - mx) + expf(q.y - mx) + expf(q.z - mx) + expf(q.w - mx);
+    online_merge(m, s, mx, ls);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    online_merge(m, s, m2, s2);
+  }
+  if ((tid & 31) == 0) { sm_m[tid >> 5] = m; sm_s[tid >> 5] = s; }
+  __syncthreads();
+  m = sm_m[0];
+  s = sm_s[0];
+  for (int i = 1; i < kCeThreads / 32; ++i) online_merge(m, s, sm_m[i], sm_s[i]);
+  const float lse = m + logf(s);
+  const int label = labels[row];
+  const bool lab_ok = label >= 0 && label < V;
+  if (tid == 0) {
+    if (!lab_ok) set_device_error(err, kDevErrBadToken);
+    loss_rows[row] = lse - (lab_ok ? z[label] : 0.f);
+  }
+  bf16* dr = dz + (long long)row * lddz;
+  for (int v = tid; v < nv; v += kCeThreads) {
+    const float4 q = reinterpret_cast<const float4*>(z)[v];
+    const int j = v * 4;
+    float p0 = expf(q.x - lse), p1 = expf(q.y - lse), p2 = expf(q.z - lse), p3 = expf(q.w - lse);
+    if (j == label) p0 -= 1.f;
+    if (j + 1 == label) p1 -= 1.f;
+    if (j + 2 == label) p2 -= 1.f;
+    if (j + 3 == label) p3 -= 1.f;
+    uint2 u;
+    u.x = pack_bf16x2(p0 * scale, p1 * scale);
+    u.y = pack_bf16x2(p2 * scale, p3 * scale);
+    *reinterpret_cast<uint2*>(dr + j) = u;
+  }
+}
+
+// Single-block fixed-order sum (fp64 accumulation).
+__global__ void sum_kernel(const float* __restrict__ x, int n, float* __restrict__ out) {
+  __shared__ double red[1024];
+  double s = 0.0;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) s += (double)x[i];
+  red[threadIdx.x] = s;
+  __syncthreads();
+  for (int w = blockDim.x >> 1; w > 0; w >>= 1) {
+    if ((int)threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) out[0] = (float)red[0];
+}
+
+__global__ void check_ids_kernel(const int32_t* __restrict__ ids, int n, int V, int32_t* bad) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    const int v = ids[i];
+    if (v < 0 || v >= V) *bad = 1;
+  }
+}
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+}  // namespace mt
+
+using namespace mt;
+
+extern "C" {
+
+int mt_k_gemm(const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, int c_f32,
+              const void* R, int64_t ldr, int M, int N, int K, void* stream) {
+  return gemm_abt(A, lda, B, ldb, C, ldc, c_f32, R, ldr, M, N, K, (cudaStream_t)stream);
+}
+
+int mt_k_transpose(const void* in, int64_t ld_in, void* out, int64_t ld_out, int rows, int cols, void* stream) {
+  if (rows < 0 || cols < 0 || ld_in < cols || ld_out < rows) return MT_EINVAL;
+  if (rows == 0 || cols == 0) return MT_OK;
+  dim3 grid((cols + kTT - 1) / kTT, (rows + kTT - 1) / kTT);
+  transpose_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>((const bf16*)in, ld_in, (bf16*)out, ld_out, rows, cols);
+  return launch_ok();
+}
+
+int mt_k_rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int M, int d, float eps, void* stream) {
+  if (M < 0 || d <= 0 || d % 8 || !al16(x) || !al16(w) || !al16(y)) return MT_EINVAL;
+  if (M == 0) return MT_OK;
+  const int rows_per_block = 8;
+  rmsnorm_fwd_kernel<<<(M + rows_per_block - 1) / rows_per_block, 32 * rows_per_block, 0, (cudaStream_t)stream>>>(
+      (const bf16*)x, (const bf16*)w, (bf16*)y, rstd, M, d, eps);
+  return launch_ok();
+}
+
+int mt_k_rmsnorm_bwd_parts(int M) { return M < kNormBwdMaxParts ? (M > 0 ? M : 1) : kNormBwdMaxParts; }
+
+int mt_k_rmsnorm_bwd(const float* dy, const void* x, const void* w, const float* rstd, const float* dres,
+                     float* dx_f32, void* dx_bf16, float* partial, void* dw_out, int M, int d, void* stream) {
+  if (M < 0 || d <= 0 || d % 8 || d > 8 * kNormBwdThreads * kNormBwdMaxVec) return MT_EINVAL;
+  if (!al16(dy) || !al16(x) || !al16(w) || (dres && !al16(dres)) || (dx_f32 && !al16(dx_f32)) ||
+      (dx_bf16 && !al16(dx_bf16)) || !al16(partial))
+    return MT_EINVAL;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int parts = mt_k_rmsnorm_bwd_parts(M);
+  if (M > 0) {
+    const int rpb = (M + parts - 1) / parts;
+    rmsnorm_bwd_kernel<<<parts, kNormBwdThreads, 0, st>>>(dy, (const bf16*)x, (const bf16*)w, rstd, dres, dx_f32,
+                                                          (bf16*)dx_bf16, partial, M, d, rpb);
+  } else {
+    cudaMemsetAsync(partial, 0, sizeof(float) * d, st);
+  }
+  colsum_to_bf16_kernel<<<(d + 255) / 256, 256, 0, st>>>(partial, parts, d, (bf16*)dw_out);
+  return launch_ok();
+}
+
+int mt_k_rope(void* x, int64_t ld, int B, int s, int n_rot_heads, int hd, const float* cos_t, const float* sin_t,
+              int inverse, void* stream) {
+  if (B < 0 || s <= 0 || n_rot_heads < 0 || hd < 4 || hd % 4 || ld < (int64_t)n_rot_heads * hd || ld % 2)
+    return MT_EINVAL;
+  const long long total = (long long)B * s * n_rot_heads * (hd / 4);
+  if (total == 0) return MT_OK;
+  const int threads = 256;
+  rope_kernel<<<(unsigned)((total + threads - 1) / threads), threads, 0, (cudaStream_t)stream>>>(
+      (bf16*)x, ld, B * s, s, n_rot_heads, hd, cos_t, sin_t, inverse ? -1.f : 1.f);
+  return launch_ok();
+}
+
+int mt_k_swiglu_fwd(const void* gu, void* a, int M, int f, void* stream) {
+  if (M < 0 || f <= 0 || f % 8 || !al16(gu) || !al16(a)) return MT_EINVAL;
+  const long long total = (long long)M * (f / 8);
+  if (total == 0) return MT_OK;
+  swiglu_fwd_kernel<<<(unsigned)((total + 255) / 256), 256, 0, (cudaStream_t)stream>>>((const bf16*)gu, (bf16*)a,
+                                                                                      M, f);
+  return launch_ok();
+}
+
+int mt_k_swiglu_bwd(const void* da, const void* gu, void* dgu, int M, int f, void* stream) {
+  if (M < 0 || f <= 0 || f % 8 || !al16(da) || !al16(gu) || !al16(dgu)) return MT_EINVAL;
+  const long long total = (long long)M * (f / 8);
+  if (total == 0) return MT_OK;
+  swiglu_bwd_kernel<<<(unsigned)((total + 255) / 256), 256, 0, (cudaStream_t)stream>>>(
+      (const bf16*)da, (const bf16*)gu, (bf16*)dgu, M, f);
+  return launch_ok();
+}
+
+int mt_k_cross_entropy(const float* logits, int64_t ldl, const int32_t* labels, void* dz, int64_t lddz,
+                       float* loss_rows, int M, int V, float scale, void* stream) {
+  if (M < 0 || V <= 0 || V % 4 || ldl < V || ldl % 4 || lddz < V || lddz % 4 || !al16(logits)) return MT_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(dz) & 7) != 0) return MT_EINVAL;
+  if (M == 0) return MT_OK;
+  cross_entropy_kernel<<<M, kCeThreads, 0, (cudaStream_t)stream>>>(logits, ldl, labels, (bf16*)dz, lddz, loss_rows,
+                                                                   V, scale, device_error_word());
+  return launch_ok();
+}
+
+int mt_k_sum(const float* x, int n, float* out, void* stream) {
+  if (n < 0) return MT_EINVAL;
+  sum_kernel<<<1, 1024, 0, (cudaStream_t)stream>>>(x, n, out);
+  return launch_ok();
+}
+
+int mt_k_embedding_fwd(const void* E, const int32_t* tok, void* x, int M, int d, int V, void* stream) {
+  if (M < 0 || d <= 0 || d % 8 || V <= 0 || !al16(E) || !al16(x)) return MT_EINVAL;
+  if (M == 0) return MT_OK;
+  embedding_fwd_kernel<<<(M + 7) / 8, 256, 0, (cudaStream_t)stream>>>((const bf16*)E, tok, (bf16*)x, M, d, V,
+                                                                      device_error_word());
+  return launch_ok();
+}
+
+int64_t mt_k_embedding_bwd_work(int M, int V) { return 2LL * V + 1 + (M > 0 ? M : 0); }
+
+int mt_k_embedding_bwd(const float* dx, const int32_t* tok, void* dE, int M, int d, int V, int32_t* work,
+                       void* stream) {
+  if (M < 0 || d <= 0 || d % 4 || V <= 0 || !al16(dx) || (reinterpret_cast<uintptr_t>(dE) & 7)) return MT_EINVAL;
+  cudaStream_t st = (cudaStream_t)stream;
+  token_sort_kernel<<<1, kSortThreads, 0, st>>>(tok, M, V, work, device_error_word());
+  dim3 grid(V, (d / 4 + 255) / 256);
+  embedding_bwd_reduce_kernel<<<grid, 256, 0, st>>>(dx, work, (bf16*)dE, d, V);
+  return launch_ok();
+}
+
+int mt_k_check_ids(const int32_t* ids, int n, int V, int32_t* bad, void* stream) {
+  if (n < 0 || V <= 0) return MT_EINVAL;
+  if (n == 0) return MT_OK;
+  const int blocks = (n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024;
+  check_ids_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(ids, n, V, bad);
+  return launch_ok();
+}
+
+int mt_k_device_error(int* code, int reset) {
+  if (!code) return MT_EINVAL;
+  int* w = device_error_word();
+  if (!w) return MT_ECUDA;
+  if (cudaMemcpy(code, w, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MT_ECUDA;
+  if (reset && cudaMemset(w, 0, sizeof(int)) != cudaSuccess) return MT_ECUDA;
+  return MT_OK;
+}
+
+}  // extern "C"

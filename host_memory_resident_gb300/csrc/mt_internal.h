@@ -1,0 +1,21 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/mt.h"
+#include "../../include/mt_kernels.h"
+
+namespace mt {
+
+// Address of the current device's error word (allocated on first use,
+// zero-initialised, kept until process exit); null if allocation failed.
+int* device_error_word();
+
+// C = A * B^T (+ R); see mt_k_gemm.
+int gemm_abt(const void* A, long long lda, const void* B, long long ldb, void* C, long long ldc, int c_f32,
+             const void* R, long long ldr, int M, int N, int K, cudaStream_t stream);
+
+}  // namespace mt

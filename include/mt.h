@@ -1,0 +1,168 @@
+/*
+ * mt.h - C ABI of the streamed-layer training step (libmt.so).
+ *
+ * One training step of a Llama-style decoder whose persistent state lives in
+ * host memory, as the RAM-centric training articles describe:
+ *
+ *  - "MegaTrain：单卡训百亿大模型的突破与实践" (zhichai.net), section
+ *    "以内存为中心的训练新范式": parameters, gradients and Adam moments stay
+ *    in host RAM (point 1); layers are prefetched into two ping-pong device
+ *    buffers and released after use, gradients go back layer by layer
+ *    (point 2); activations are checkpointed every few layers and recomputed
+ *    (point 3); a stateless layer template runs each layer (point 4).
+ *  - lqnn.cn MegaTrain article, section 三: "gpu_flat_buffers" (two fixed
+ *    device flat buffers), "layer_pinned_flats" (pinned flat per-layer
+ *    weights), three CUDA streams gated by weight_ready / buffer_free events,
+ *    a K-slab flat gradient pool drained by a CPU worker thread that adds the
+ *    slabs into FP32 master gradients, checkpoint_interval (default 4);
+ *    section 二: ParameterState = FP32 master, grad, m, v; Adam runs on the CPU.
+ *
+ * Every function returns MT_OK (0) or a negative MT_E* code; no C++
+ * exception crosses this boundary and nothing aborts. After any error the
+ * handle can still be destroyed. mt_last_error() gives a text message.
+ */
+#ifndef MT_H_
+#define MT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MT_OK 0
+#define MT_EINVAL (-1)     /* bad argument, shape or token id; nothing ran */
+#define MT_ENOMEM (-2)     /* host or device allocation failed */
+#define MT_ECUDA (-3)      /* a CUDA runtime call failed */
+#define MT_ETIMEOUT (-4)   /* a host wait (worker, event) passed its deadline */
+#define MT_EWORKER (-5)    /* the host worker thread failed */
+#define MT_ENONFINITE (-6) /* the loss was NaN or Inf; master/m/v were not updated */
+#define MT_ESTATE (-7)     /* handle in a state that forbids the call */
+#define MT_EDEVICE (-8)    /* a kernel recorded an error in the device error word */
+
+/* Model shape and run settings. All counts are positive. */
+typedef struct mt_config {
+  int32_t n_layers;      /* L */
+  int32_t d_model;       /* d, multiple of 64 */
+  int32_t n_heads;       /* H */
+  int32_t n_kv_heads;    /* Hkv, divides H */
+  int32_t head_dim;      /* hd in {16, 64, 128} */
+  int32_t ffn_dim;       /* f, multiple of 64 */
+  int32_t vocab;         /* V, multiple of 8 */
+  int32_t max_batch;     /* largest B a step may use */
+  int32_t max_seq;       /* largest s a step may use */
+  int32_t ckpt_interval; /* C >= 1: checkpoint the input of every C-th layer */
+  int32_t n_slabs;       /* K >= 2 gradient slabs (device + pinned host staging) */
+  int32_t streamed;      /* 1: stream units through two buffers; 0: all units resident */
+  float rms_eps;         /* RMSNorm epsilon, e.g. 1e-5 */
+  float rope_theta;      /* RoPE base, e.g. 10000 */
+  float lr, beta1, beta2, adam_eps; /* Adam, no weight decay */
+  int32_t device;        /* CUDA device ordinal */
+  int32_t host_threads;  /* threads for host accumulate + Adam; 0 = all cores */
+} mt_config;
+
+/* One tensor of the flat layout. kind 0 = matrix, 1 = norm weight. */
+typedef struct mt_tensor_desc {
+  int32_t unit;   /* 0 = embedding, 1..L = layer l-1, L+1 = final norm + head */
+  int32_t kind;
+  int64_t offset; /* absolute element offset in the flat arrays */
+  int64_t rows, cols; /* matrices [out, in]; vectors have cols = 1 */
+  char name[24];
+} mt_tensor_desc;
+
+typedef struct mt_stats {
+  int64_t steps;
+  int64_t h2d_bytes;       /* weight bytes copied host->device, all steps */
+  int64_t d2h_bytes;       /* gradient bytes copied device->host, all steps */
+  int64_t h2d_units;       /* unit copies issued (forward + recompute) */
+  double host_adam_s;      /* worker time in accumulate + Adam + bf16 emit */
+  double host_wait_s;      /* main-thread time blocked on slab back-pressure */
+  double last_step_s;      /* wall time of the last mt_train_step */
+  int64_t device_bytes;    /* device memory owned by the handle */
+  int64_t pinned_bytes;    /* pinned host memory owned by the handle */
+} mt_stats;
+
+typedef struct mt_handle mt_handle;
+
+/*
+ * Flat layout of `cfg` (no GPU needed). Writes up to `cap` descriptors and
+ * the total element count n_total (tensor offsets are multiples of 64; the
+ * padding counts). Order: embed; per layer attn_norm, wqkv, wo, mlp_norm,
+ * wgu, wdown; final_norm, head. Returns MT_EINVAL on a bad shape.
+ */
+int mt_layout(const mt_config* cfg, mt_tensor_desc* out, int cap, int* n_out, int64_t* n_total);
+
+/* Element range [offset, offset + length) of unit `unit` (0 .. L+1). */
+int mt_unit_range(const mt_config* cfg, int unit, int64_t* offset, int64_t* length);
+
+/*
+ * Creates a handle. master, adam_m, adam_v, grad are caller-owned FP32 host
+ * arrays of n_total elements in the flat layout; they must stay valid until
+ * mt_destroy. The caller initialises master and zeroes m and v. The library
+ * allocates the pinned bf16 flat store (filled with round-to-nearest-even
+ * bf16 of master), the pinned staging slabs, all device memory and the
+ * three streams, and starts the host worker thread. Returns MT_ENOMEM,
+ * MT_ECUDA or MT_EINVAL on failure (nothing leaks).
+ */
+int mt_init(const mt_config* cfg, float* master, float* adam_m, float* adam_v, float* grad, int64_t n_total,
+            mt_handle** out);
+
+/*
+ * One training step on host token and label arrays (int32 [batch, seq],
+ * row-major, every id in [0, V), read only during the call). Computes the
+ * mean cross-entropy loss of the current master (written to *loss_out),
+ * overwrites `grad` with this step's FP32 gradient, and applies one Adam step
+ * (t += 1) to master / m / v and to the bf16 store. Returns after all of it
+ * is done. On MT_ENONFINITE the gradient is written but no Adam update
+ * happens.
+ */
+int mt_train_step(mt_handle* h, const int32_t* tokens, const int32_t* labels, int32_t batch, int32_t seq,
+                  float* loss_out);
+
+/* Same as mt_train_step with tokens and labels already in device memory
+ * (int32 [batch, seq]); ids are checked on the device and a bad id returns
+ * MT_EDEVICE before any weight is touched by Adam. */
+int mt_train_step_device(mt_handle* h, const int32_t* d_tokens, const int32_t* d_labels, int32_t batch,
+                         int32_t seq, float* loss_out);
+
+/* Copies the FP32 gradient of the last step (n elements, n <= n_total). */
+int mt_read_grads(mt_handle* h, float* dst, int64_t n);
+
+int mt_get_step(mt_handle* h, int64_t* t);
+int mt_set_step(mt_handle* h, int64_t t);     /* for resume from a checkpoint */
+/* Re-emits the bf16 store from master (after the caller rewrote master). */
+int mt_sync_store(mt_handle* h);
+int mt_get_stats(mt_handle* h, mt_stats* out);
+/* Returns the handle's CUDA stream: which 0 = compute, 1 = H2D, 2 = D2H. */
+int mt_get_stream(mt_handle* h, int which, void** stream);
+int mt_destroy(mt_handle* h);
+/* Last error message of `h`, or of the calling thread when h is NULL. */
+const char* mt_last_error(mt_handle* h);
+
+/*
+ * Host-side fault injection for tests (no GPU fault is ever caused):
+ *  what 1: the worker sleeps `value` ms before each unit (deadline tests);
+ *  what 2: the worker reports a failure on its `value`-th unit;
+ *  what 3: host wait deadline in ms (default 600000);
+ *  what 4: next device allocation in mt_init fails (value 1).
+ */
+int mt_debug_inject(mt_handle* h, int what, int64_t value);
+/* Global (pre-handle) injection: what 4 = fail the next mt_init allocation. */
+int mt_debug_inject_global(int what, int64_t value);
+
+/*
+ * Host Adam of the library on caller arrays (n elements, step t >= 1), the
+ * same code the worker runs per unit: m, v, w updated in place; `g` FP32;
+ * `store` (may be NULL) receives bf16(w) with round-to-nearest-even.
+ */
+int mt_host_adam(float* w, float* m, float* v, const float* g, uint16_t* store, int64_t n, int64_t t, float lr,
+                 float beta1, float beta2, float eps, int threads);
+
+/* Round-to-nearest-even FP32 -> bf16 bits on the host; every NaN becomes 0x7fc0. */
+int mt_host_to_bf16(const float* src, uint16_t* dst, int64_t n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MT_H_ */

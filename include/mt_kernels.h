@@ -1,0 +1,131 @@
+/*
+ * mt_kernels.h - C ABI of the individual sm_103a kernels of the stateless
+ * layer template (libmt.so). The training step (mt.h) is built from these;
+ * they are exported so each one can be checked on its own.
+ *
+ * The template is the per-layer compute of the RAM-centric method
+ * ("MegaTrain：单卡训百亿大模型的突破与实践", zhichai.net, section
+ * "以内存为中心的训练新范式" point 4: a lightweight stateless template per
+ * layer, parameters bound at run time; travelaiplan blog "單卡也能練 100B+",
+ * 核心功能 point 3: hand-written backward per layer instead of autograd).
+ *
+ * Conventions for every function below:
+ *  - all array arguments are DEVICE pointers, caller-owned; nothing is
+ *    allocated or freed; outputs are fully overwritten unless stated;
+ *  - bf16 = IEEE bfloat16 bits (uint16), fp32 = float; matrices are
+ *    row-major with the given leading dimension (elements);
+ *  - tokens are laid out row-major (batch, position): row m = b * s + t;
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream); the call only
+ *    enqueues work and returns;
+ *  - return MT_OK, MT_EINVAL (bad shape / alignment; nothing enqueued) or
+ *    MT_ECUDA (launch failed).
+ */
+#ifndef MT_KERNELS_H_
+#define MT_KERNELS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * Dense product on tcgen05 tensor cores: C[M,N] = A[M,K] * B[N,K]^T (+ R).
+ * A, B bf16 K-contiguous, 16-byte aligned, lda/ldb multiples of 8. C is bf16
+ * (c_f32 = 0, ldc multiple of 8) or fp32 (c_f32 = 1, ldc multiple of 4). R is
+ * an optional bf16 [M,N] residual (ldr multiple of 8) added before rounding.
+ * The linear layers y = x W^T of a decoder layer (W stored [out, in]).
+ */
+int mt_k_gemm(const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, int c_f32,
+              const void* R, int64_t ldr, int M, int N, int K, void* stream);
+
+/* out[c, r] = in[r, c] for a bf16 [rows, cols] matrix (ld_in >= cols, ld_out >= rows). */
+int mt_k_transpose(const void* in, int64_t ld_in, void* out, int64_t ld_out, int rows, int cols, void* stream);
+
+/*
+ * RMSNorm forward: y[m,:] = x[m,:] * rstd[m] * w, rstd = 1/sqrt(mean(x^2)+eps).
+ * x, y bf16 [M, d] (ld = d), w bf16 [d], rstd fp32 [M]. d multiple of 8.
+ */
+int mt_k_rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int M, int d, float eps, void* stream);
+
+/*
+ * RMSNorm backward. dy: gradient w.r.t. y, fp32 [M, d]; x bf16 [M, d];
+ * dres: optional fp32 [M, d] added to dx (the residual branch). Writes
+ * dx_f32 (fp32 [M,d], may be NULL) and dx_bf16 (bf16 [M,d], may be NULL),
+ * per-block partial sums of dw into `partial` (fp32 [n_part, d], scratch)
+ * and the final dw (summed over rows in a fixed order) as bf16 into dw_out.
+ * dx_f32 may alias dres. mt_k_rmsnorm_bwd_parts() gives n_part for M.
+ */
+int mt_k_rmsnorm_bwd(const float* dy, const void* x, const void* w, const float* rstd, const float* dres,
+                     float* dx_f32, void* dx_bf16, float* partial, void* dw_out, int M, int d, void* stream);
+int mt_k_rmsnorm_bwd_parts(int M);
+
+/*
+ * Rotate-half RoPE in place on the first `n_rot_heads` heads of each token
+ * row of a bf16 [B*s, ld] buffer (heads of hd contiguous elements starting at
+ * column 0). cos/sin fp32 [s_max, hd/2] tables. inverse = 1 rotates by the
+ * negative angle (the backward).
+ */
+int mt_k_rope(void* x, int64_t ld, int B, int s, int n_rot_heads, int hd, const float* cos_t, const float* sin_t,
+              int inverse, void* stream);
+
+/* a[m, j] = silu(gu[m, j]) * gu[m, f + j]; gu bf16 [M, 2f], a bf16 [M, f]. */
+int mt_k_swiglu_fwd(const void* gu, void* a, int M, int f, void* stream);
+
+/* dgu[m, j] = da*u*sig(g)*(1+g(1-sig(g))), dgu[m, f+j] = da*silu(g); da bf16 [M, f]. */
+int mt_k_swiglu_bwd(const void* da, const void* gu, void* dgu, int M, int f, void* stream);
+
+/*
+ * Causal grouped-query attention forward (flash style, KV streamed in tiles).
+ * qkv bf16 [B*s, ldqkv]: q heads at columns [0, H*hd), k heads at
+ * [H*hd, (H+Hkv)*hd), v heads after; o bf16 [B*s, ldo] (H*hd columns);
+ * lse fp32 [B, H, s] natural-log softmax denominators. hd in {16, 64, 128}.
+ */
+int mt_k_attn_fwd(const void* qkv, int64_t ldqkv, void* o, int64_t ldo, float* lse, int B, int s, int H, int Hkv,
+                  int hd, void* stream);
+
+/*
+ * Attention backward, deterministic (no float atomics). Inputs as the
+ * forward plus dout bf16 [B*s, lddo] and the forward's lse. delta is fp32
+ * scratch [B, H, s]. Writes dq, dk, dv into dqkv bf16 [B*s, lddqkv] in the
+ * qkv column layout.
+ */
+int mt_k_attn_bwd(const void* qkv, int64_t ldqkv, const void* o, int64_t ldo, const void* dout, int64_t lddo,
+                  const float* lse, float* delta, void* dqkv, int64_t lddqkv, int B, int s, int H, int Hkv, int hd,
+                  void* stream);
+
+/*
+ * Cross entropy over a vocabulary row block: logits fp32 [M, ldl], labels
+ * int32 [M]. Writes dz bf16 [M, lddz] = (softmax - onehot) * scale and
+ * loss_rows fp32 [M] = logsumexp - z[label] (unscaled).
+ */
+int mt_k_cross_entropy(const float* logits, int64_t ldl, const int32_t* labels, void* dz, int64_t lddz,
+                       float* loss_rows, int M, int V, float scale, void* stream);
+
+/* out[0] = sum of x[0..n) in a fixed order (fp64 accumulation), fp32 result. */
+int mt_k_sum(const float* x, int n, float* out, void* stream);
+
+/* x[m, :] = E[tok[m], :]; E bf16 [V, d], x bf16 [M, d]. Ids outside [0, V)
+ * give a zero row and set the device error word. */
+int mt_k_embedding_fwd(const void* E, const int32_t* tok, void* x, int M, int d, int V, void* stream);
+
+/*
+ * dE[v, :] = sum over m with tok[m] = v of dx[m, :], bf16 [V, d] output,
+ * fp32 dx [M, d]. Deterministic: rows are summed in increasing m. `work` is
+ * int32 scratch of mt_k_embedding_bwd_work(M, V) elements.
+ */
+int mt_k_embedding_bwd(const float* dx, const int32_t* tok, void* dE, int M, int d, int V, int32_t* work,
+                       void* stream);
+int64_t mt_k_embedding_bwd_work(int M, int V);
+
+/* Sets *bad = 1 if any of the n ids lies outside [0, V) (device check). */
+int mt_k_check_ids(const int32_t* ids, int n, int V, int32_t* bad, void* stream);
+
+/* Reads (and with reset = 1 clears) the device error word of the current device. */
+int mt_k_device_error(int* code, int reset);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MT_KERNELS_H_ */

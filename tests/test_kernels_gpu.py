@@ -1,0 +1,299 @@
+"""Per-kernel parity of libmt.so's sm_103a kernels against the oracle.
+
+Every kernel is called through the C ABI on seeded inputs and compared
+element by element with the oracle's function evaluated in float64 on the
+same (bf16-rounded) inputs. Sizes span several tiles with ragged tails and
+include one full-width layer shape of each large workload.
+
+Tolerances follow from the arithmetic: inputs and outputs are bf16 (relative
+rounding 2^-9), accumulation is fp32. A bf16 output is within ~2^-8 of the
+exact value relative to the row/column scale, so element checks use
+|err| <= 2e-2 * scale and relative L2 error <= 1e-2 (5e-3 for a single
+rounding); integer / byte work (transpose, gather) is bit-exact.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import host_memory_resident_gb300 as mt  # noqa: E402
+from oracle import ops  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def bf(a):
+    """numpy -> (device bf16 tensor, float64 numpy of its exact values)."""
+    t = torch.from_numpy(np.asarray(a, dtype=np.float32)).to(DEV).to(torch.bfloat16)
+    return t, t.float().cpu().numpy().astype(np.float64)
+
+
+def f32(a):
+    t = torch.from_numpy(np.asarray(a, dtype=np.float32)).to(DEV)
+    return t, t.cpu().numpy().astype(np.float64)
+
+
+def host(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def rel_l2(a, b):
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def assert_close(got, ref, l2=1e-2, elem=2e-2, what=""):
+    scale = max(np.abs(ref).max(), 1e-30)
+    e = rel_l2(got, ref)
+    assert e <= l2, f"{what}: rel L2 {e:.3e}"
+    m = np.abs(got - ref).max() / scale
+    assert m <= elem, f"{what}: max err / scale {m:.3e}"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    mt.lib()
+    mt.device_error(reset=True)
+    yield
+    torch.cuda.synchronize()
+    assert mt.device_error(reset=True) == 0
+
+
+# --------------------------------------------------------------------- GEMM
+@pytest.mark.parametrize("M,N,K,out,res", [
+    (64, 192, 64, "bf16", False),      # tiny QKV
+    (200, 296, 136, "bf16", True),     # ragged M, N, K
+    (200, 300, 72, "f32", False),      # ragged N with fp32 output
+    (130, 8, 8, "bf16", False),        # smallest N and K
+    (2048, 2048, 512, "f32", True),
+    (4096, 4096, 1024, "bf16", False),  # several tiles per CTA (TMEM ping-pong)
+    (512, 12288, 4096, "bf16", False),  # 7B QKV, 512 tokens
+    (384, 5120, 13824, "f32", False),   # 14B down projection K
+])
+def test_gemm(M, N, K, out, res):
+    rng = np.random.default_rng(M * 7 + N * 3 + K)
+    A, Ah = bf(rng.standard_normal((M, K)))
+    B, Bh = bf(rng.standard_normal((N, K)) / np.sqrt(K))
+    R, Rh = bf(rng.standard_normal((M, N))) if res else (None, 0.0)
+    Cout = torch.empty((M, N), device=DEV, dtype=torch.float32 if out == "f32" else torch.bfloat16)
+    mt.k_gemm(A, B, Cout, R)
+    torch.cuda.synchronize()
+    ref = ops.linear_fwd(Ah, Bh) + Rh
+    assert_close(host(Cout), ref, l2=5e-3 if out == "bf16" else 1e-4, elem=1e-2 if out == "bf16" else 1e-3,
+                 what=f"gemm {M}x{N}x{K}")
+
+
+def test_gemm_strided_operands_and_rejects_misaligned():
+    rng = np.random.default_rng(1)
+    big, bigh = bf(rng.standard_normal((256, 200)))
+    A = big[:, 8:136]            # row pitch 200, K = 128
+    B, Bh = bf(rng.standard_normal((64, 128)))
+    Cout = torch.empty((256, 64), device=DEV, dtype=torch.float32)
+    mt.k_gemm(A, B, Cout)
+    torch.cuda.synchronize()
+    assert_close(host(Cout), bigh[:, 8:136] @ Bh.T, l2=1e-4, elem=1e-3, what="strided")
+    bad = big[:, 1:129]          # not 16-byte aligned
+    with pytest.raises(mt.MtError):
+        mt.k_gemm(bad, B, Cout)
+
+
+def test_gemm_deterministic():
+    rng = np.random.default_rng(2)
+    A, _ = bf(rng.standard_normal((1000, 777 // 8 * 8)))
+    B, _ = bf(rng.standard_normal((600, 777 // 8 * 8)))
+    c1 = torch.empty((1000, 600), device=DEV)
+    c2 = torch.empty((1000, 600), device=DEV)
+    mt.k_gemm(A, B, c1)
+    mt.k_gemm(A, B, c2)
+    torch.cuda.synchronize()
+    assert torch.equal(c1, c2)
+
+
+# ---------------------------------------------------------------- transpose
+@pytest.mark.parametrize("rows,cols", [(1, 1), (64, 64), (100, 37), (2048, 5632)])
+def test_transpose_exact(rows, cols):
+    x = torch.randn(rows, cols, device=DEV).to(torch.bfloat16)
+    out = torch.empty(cols, rows, device=DEV, dtype=torch.bfloat16)
+    mt.k_transpose(x, out)
+    torch.cuda.synchronize()
+    assert torch.equal(out, x.t().contiguous())
+
+
+# ------------------------------------------------------------------ RMSNorm
+@pytest.mark.parametrize("M,d", [(64, 64), (333, 2048), (257, 5120)])
+def test_rmsnorm_fwd_bwd(M, d):
+    rng = np.random.default_rng(M + d)
+    x, xh = bf(rng.standard_normal((M, d)) * 3.0)
+    w, wh = bf(1.0 + 0.1 * rng.standard_normal(d))
+    y = torch.empty((M, d), device=DEV, dtype=torch.bfloat16)
+    rstd = torch.empty(M, device=DEV)
+    mt.k_rmsnorm_fwd(x, w, y, rstd, 1e-5)
+    yr, rr = ops.rmsnorm_fwd(xh, wh, 1e-5)
+    torch.cuda.synchronize()
+    assert_close(host(y), yr, l2=5e-3, elem=1e-2, what="rmsnorm y")
+    np.testing.assert_allclose(host(rstd), rr, rtol=1e-5)
+    dy, dyh = f32(rng.standard_normal((M, d)))
+    dres, dresh = f32(rng.standard_normal((M, d)))
+    dx32 = torch.empty((M, d), device=DEV)
+    dxb = torch.empty((M, d), device=DEV, dtype=torch.bfloat16)
+    part = torch.empty((mt.k_rmsnorm_bwd_parts(M), d), device=DEV)
+    dw = torch.empty(d, device=DEV, dtype=torch.bfloat16)
+    mt.k_rmsnorm_bwd(dy, x, w, rstd, dres, dx32, dxb, part, dw)
+    dxr, dwr = ops.rmsnorm_bwd(dyh, xh, wh, host(rstd))
+    torch.cuda.synchronize()
+    assert_close(host(dx32), dxr + dresh, l2=1e-5, elem=1e-4, what="rmsnorm dx")
+    assert_close(host(dxb), dxr + dresh, l2=5e-3, elem=1e-2, what="rmsnorm dx bf16")
+    assert_close(host(dw), dwr, l2=5e-3, elem=1e-2, what="rmsnorm dw")
+
+
+# --------------------------------------------------------------------- RoPE
+@pytest.mark.parametrize("B,s,H,Hkv,hd", [(2, 32, 4, 4, 16), (1, 300, 4, 2, 64), (2, 129, 2, 2, 128)])
+def test_rope_fwd_inverse(B, s, H, Hkv, hd):
+    rng = np.random.default_rng(s + hd)
+    qn = (H + 2 * Hkv) * hd
+    x, xh = bf(rng.standard_normal((B * s, qn)))
+    cos, sin = ops.rope_tables(s, hd, 10000.0)
+    ct, _ = f32(cos)
+    st, _ = f32(sin)
+    y = x.clone()
+    mt.k_rope(y, B, s, H + Hkv, hd, ct, st)
+    torch.cuda.synchronize()
+    rot = (H + Hkv) * hd
+    ref = xh.copy()
+    ref[:, :rot] = ops.rope_fwd(xh[:, :rot].reshape(B, s, H + Hkv, hd), cos, sin).reshape(B * s, rot)
+    assert_close(host(y), ref, l2=5e-3, elem=1e-2, what="rope")
+    assert torch.equal(y[:, rot:], x[:, rot:])                 # v untouched
+    z = y.clone()
+    mt.k_rope(z, B, s, H + Hkv, hd, ct, st, inverse=True)
+    torch.cuda.synchronize()
+    back = ops.rope_bwd(host(y)[:, :rot].reshape(B, s, H + Hkv, hd), cos, sin).reshape(B * s, rot)
+    assert_close(host(z)[:, :rot], back, l2=5e-3, elem=1e-2, what="rope inverse")
+
+
+# ------------------------------------------------------------------- SwiGLU
+@pytest.mark.parametrize("M,f", [(64, 256), (199, 5632)])
+def test_swiglu(M, f):
+    rng = np.random.default_rng(M + f)
+    gu, guh = bf(rng.standard_normal((M, 2 * f)) * 2)
+    a = torch.empty((M, f), device=DEV, dtype=torch.bfloat16)
+    mt.k_swiglu_fwd(gu, a)
+    da, dah = bf(rng.standard_normal((M, f)))
+    dgu = torch.empty((M, 2 * f), device=DEV, dtype=torch.bfloat16)
+    mt.k_swiglu_bwd(da, gu, dgu)
+    torch.cuda.synchronize()
+    assert_close(host(a), ops.swiglu_fwd(guh[:, :f], guh[:, f:]), l2=5e-3, elem=1e-2, what="swiglu")
+    dg, du = ops.swiglu_bwd(dah, guh[:, :f], guh[:, f:])
+    assert_close(host(dgu), np.concatenate([dg, du], 1), l2=5e-3, elem=1e-2, what="swiglu bwd")
+
+
+# ---------------------------------------------------------------- attention
+ATTN_CASES = [
+    (2, 32, 4, 4, 16),     # tiny
+    (1, 100, 4, 2, 16),    # ragged s, GQA
+    (2, 130, 4, 1, 64),    # ragged, 4 query heads per KV head
+    (1, 257, 2, 2, 128),   # ragged, hd 128
+    (1, 1, 2, 1, 64),      # single token: output = v
+    (1, 1024, 2, 2, 128),
+]
+
+
+def _attn_inputs(B, s, H, Hkv, hd, seed):
+    rng = np.random.default_rng(seed)
+    qn = (H + 2 * Hkv) * hd
+    qkv, qkvh = bf(rng.standard_normal((B * s, qn)))
+    q = qkvh[:, :H * hd].reshape(B, s, H, hd)
+    k = qkvh[:, H * hd:(H + Hkv) * hd].reshape(B, s, Hkv, hd)
+    v = qkvh[:, (H + Hkv) * hd:].reshape(B, s, Hkv, hd)
+    return qkv, q, k, v
+
+
+@pytest.mark.parametrize("B,s,H,Hkv,hd", ATTN_CASES)
+def test_attention_fwd(B, s, H, Hkv, hd):
+    qkv, q, k, v = _attn_inputs(B, s, H, Hkv, hd, s * hd)
+    o = torch.empty((B * s, H * hd), device=DEV, dtype=torch.bfloat16)
+    lse = torch.empty((B, H, s), device=DEV)
+    mt.k_attn_fwd(qkv, o, lse, B, s, H, Hkv, hd)
+    torch.cuda.synchronize()
+    orf, lr = ops.attention_fwd(q, k, v)
+    assert_close(host(o), orf.reshape(B * s, H * hd), l2=1e-2, elem=2e-2, what="attn o")
+    np.testing.assert_allclose(host(lse), lr, rtol=0, atol=2e-2)
+
+
+@pytest.mark.parametrize("B,s,H,Hkv,hd", ATTN_CASES)
+def test_attention_bwd(B, s, H, Hkv, hd):
+    qkv, q, k, v = _attn_inputs(B, s, H, Hkv, hd, s * hd + 1)
+    o = torch.empty((B * s, H * hd), device=DEV, dtype=torch.bfloat16)
+    lse = torch.empty((B, H, s), device=DEV)
+    mt.k_attn_fwd(qkv, o, lse, B, s, H, Hkv, hd)
+    rng = np.random.default_rng(s)
+    do, doh = bf(rng.standard_normal((B * s, H * hd)))
+    delta = torch.empty((B, H, s), device=DEV)
+    dqkv = torch.zeros_like(qkv)
+    mt.k_attn_bwd(qkv, o, do, lse, delta, dqkv, B, s, H, Hkv, hd)
+    dqkv2 = torch.zeros_like(qkv)
+    mt.k_attn_bwd(qkv, o, do, lse, delta, dqkv2, B, s, H, Hkv, hd)
+    torch.cuda.synchronize()
+    assert torch.equal(dqkv, dqkv2)                    # deterministic
+    dq, dk, dv = ops.attention_bwd(q, k, v, doh.reshape(B, s, H, hd))
+    g = host(dqkv)
+    assert_close(g[:, :H * hd], dq.reshape(B * s, -1), l2=2e-2, elem=3e-2, what="dq")
+    assert_close(g[:, H * hd:(H + Hkv) * hd], dk.reshape(B * s, -1), l2=2e-2, elem=3e-2, what="dk")
+    assert_close(g[:, (H + Hkv) * hd:], dv.reshape(B * s, -1), l2=2e-2, elem=3e-2, what="dv")
+
+
+# ------------------------------------------------------------ cross entropy
+@pytest.mark.parametrize("M,V", [(64, 512), (37, 32000), (5, 152064)])
+def test_cross_entropy(M, V):
+    rng = np.random.default_rng(M + V)
+    z, zh = f32(rng.standard_normal((M, V)) * 3)
+    lab_np = rng.integers(0, V, size=M).astype(np.int32)
+    lab = torch.from_numpy(lab_np).to(DEV)
+    dz = torch.empty((M, V), device=DEV, dtype=torch.bfloat16)
+    rows = torch.empty(M, device=DEV)
+    total = torch.empty(1, device=DEV)
+    mt.k_cross_entropy(z, lab, dz, rows, 1.0 / M)
+    mt.k_sum(rows, total)
+    torch.cuda.synchronize()
+    loss, dref = ops.cross_entropy_fwd_bwd(zh, lab_np)
+    assert float(total.item()) / M == pytest.approx(loss, rel=1e-5)
+    assert_close(host(dz), dref, l2=5e-3, elem=1e-2, what="dz")
+
+
+def test_cross_entropy_zero_logits_is_ln_v():
+    M, V = 8, 32000
+    z = torch.zeros((M, V), device=DEV)
+    lab = torch.arange(M, device=DEV, dtype=torch.int32)
+    dz = torch.empty((M, V), device=DEV, dtype=torch.bfloat16)
+    rows = torch.empty(M, device=DEV)
+    mt.k_cross_entropy(z, lab, dz, rows, 1.0)
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(host(rows), np.log(V), rtol=1e-6)
+
+
+# ---------------------------------------------------------------- embedding
+@pytest.mark.parametrize("M,V,d,dup", [(64, 512, 64, False), (1000, 97, 128, True), (4096, 152064, 512, False),
+                                       (3000, 5, 64, True)])
+def test_embedding_fwd_bwd(M, V, d, dup):
+    rng = np.random.default_rng(M + V)
+    E, Eh = bf(rng.standard_normal((V, d)))
+    tok_np = (rng.integers(0, min(V, 3), size=M) if dup else rng.integers(0, V, size=M)).astype(np.int32)
+    tok = torch.from_numpy(tok_np).to(DEV)
+    x = torch.empty((M, d), device=DEV, dtype=torch.bfloat16)
+    mt.k_embedding_fwd(E, tok, x)
+    torch.cuda.synchronize()
+    assert torch.equal(x, E[tok.long()])
+    dx, dxh = f32(rng.standard_normal((M, d)))
+    work = torch.empty(mt.k_embedding_bwd_work(M, V), device=DEV, dtype=torch.int32)
+    dE = torch.empty((V, d), device=DEV, dtype=torch.bfloat16)
+    dE2 = torch.empty_like(dE)
+    mt.k_embedding_bwd(dx, tok, dE, work)
+    mt.k_embedding_bwd(dx, tok, dE2, work)
+    torch.cuda.synchronize()
+    assert torch.equal(dE, dE2)
+    ref = ops.embedding_bwd(dxh, tok_np, V)
+    assert_close(host(dE), ref, l2=5e-3, elem=1e-2, what="dE")
+    untouched = np.setdiff1d(np.arange(V), tok_np)
+    assert np.all(host(dE)[untouched] == 0)
