@@ -1,0 +1,448 @@
+#!/usr/bin/env python
+"""Throughput of the streamed-layer training step on one GB300 (per rank).
+
+One step = one mt_train_step of the decoder workload: stream every unit's
+bf16 weights host->device through two buffers, forward with checkpoints,
+fused head + cross entropy, segment recompute + backward, K-slab gradient
+offload, host accumulate + Adam on the FP32 master (all through libmt.so).
+
+Prints one JSON line (rank 0):
+  value  tokens/s over all ranks, token/label arrays already in device memory
+  e2e    the same through mt_train_step with host token/label arrays
+  roofline  the dominant kernel (the tcgen05 GEMM): algorithmic FLOPs of its
+         launches in the timed region / their CUDA-event device time
+  step_roofline  model FLOPs at the bf16 peak vs weight + gradient bytes over
+         the measured host link, whichever is slower
+  cpu_baseline  the oracle on this host's cores on a bounded sample
+``--impl reference`` times the oracle (plain numpy CPU restatement) instead.
+``--kernel gemm --shape M,N,K`` runs one GEMM shape (for profiler captures).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "train tokens/s & model TFLOPS on 1 GB300 vs min(TC peak, host-link) roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def model_flops(shape, B, s):
+    """6 * N_mm + 6 * L * s * H * hd per token (causal attention), times B*s."""
+    d, f, V = shape.d_model, shape.ffn_dim, shape.vocab
+    qkv = (shape.n_heads + 2 * shape.n_kv_heads) * shape.head_dim
+    hq = shape.n_heads * shape.head_dim
+    n_mm = shape.n_layers * (qkv * d + d * hq + 2 * f * d + d * f) + V * d
+    per_tok = 6.0 * n_mm + 6.0 * shape.n_layers * s * shape.n_heads * shape.head_dim
+    return per_tok * B * s
+
+
+def workload_desc(shape):
+    return (f"{shape.name} decoder: {shape.n_layers} layers, d={shape.d_model}, {shape.n_heads}x{shape.head_dim} "
+            f"heads ({shape.n_kv_heads} KV), ffn={shape.ffn_dim}, vocab={shape.vocab}, batch={shape.batch}, "
+            f"seq={shape.seq}, ckpt_interval={shape.ckpt_interval}, slabs={shape.n_slabs}")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.device = device
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.device)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- host link
+def host_link_probe(torch, dev, nbytes=1 << 30, reps=5):
+    """Pinned cudaMemcpyAsync bandwidth: H2D alone, D2H alone, both at once."""
+    n = nbytes // 2
+    hs = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
+    hd = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
+    d1 = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    d2 = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def timed(fn):
+        best = 1e30
+        for _ in range(reps):
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize(dev)
+            best = min(best, time.perf_counter() - t0)
+        return best
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            d1.copy_(hs, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s2):
+            hd.copy_(d2, non_blocking=True)
+
+    def both():
+        h2d()
+        d2h()
+
+    t_h, t_d, t_b = timed(h2d), timed(d2h), timed(both)
+    gb = nbytes / 1e9
+    return {"h2d_gbs": gb / t_h, "d2h_gbs": gb / t_d, "bidir_h2d_gbs": gb / t_b, "bidir_d2h_gbs": gb / t_b}
+
+
+def gemm_traffic_record():
+    """DRAM bytes per GEMM launch from the committed ncu summary, if it was
+    taken on the current GEMM source (else None)."""
+    p = os.path.join(ROOT, "profiles", "gemm_traffic.json")
+    src = os.path.join(ROOT, "host_memory_resident_gb300", "csrc", "gemm_tc.cu")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return rec if rec.get("gemm_source_sha") == h else None
+
+
+# ----------------------------------------------------------- CPU baseline
+def oracle_sample(shape):
+    """Time the oracle on a bounded sample of the workload and compose the
+    full step: B * (L * t_layer + t_rest) + t_adam(N). The sample is one
+    sequence at full width and full length through a 1-layer and a 2-layer
+    model (t_layer = their difference), plus Adam on a 2^24-element slice."""
+    import oracle
+    s = shape.seq
+    toks, labs = synth.make_tokens(shape.vocab, 1, s, seed=1)
+    times = {}
+    for L in (1, 2):
+        sh = shape.with_(n_layers=L, ckpt_interval=1)
+        lay = oracle.build_layout(sh)
+        master = synth.init_master(lay.n_total, lay.segments(), seed=0)
+        t0 = time.perf_counter()
+        oracle.step_grads(sh, master, toks, labs, dtype=np.float32)
+        times[L] = time.perf_counter() - t0
+        del master
+    n = 1 << 24
+    rng = np.random.default_rng(0)
+    w = rng.standard_normal(n).astype(np.float32)
+    g = rng.standard_normal(n).astype(np.float32) * 1e-3
+    t0 = time.perf_counter()
+    oracle.adam_update(w, np.zeros(n, np.float32), np.zeros(n, np.float32), g, 1, shape.lr, shape.beta1,
+                       shape.beta2, shape.adam_eps, dtype=np.float32)
+    t_adam_slice = time.perf_counter() - t0
+    t_layer = max(times[2] - times[1], 1e-9)
+    t_rest = max(times[1] - t_layer, 0.0)
+    lay_full = oracle.build_layout(shape)
+    t_adam = t_adam_slice * lay_full.n_total / n
+    t_step = shape.batch * (shape.n_layers * t_layer + t_rest) + t_adam
+    return {
+        "value": shape.batch * s / t_step, "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
+        "sample": (f"composed: 1 sequence of {s} tokens through 1- and 2-layer full-width models "
+                   f"(t_layer {t_layer:.2f} s, rest {t_rest:.2f} s, float32 numpy) + Adam on 2^24 elements "
+                   f"scaled to {lay_full.n_total} params; step = {shape.batch} x ({shape.n_layers} t_layer + rest)"
+                   f" + Adam = {t_step:.1f} s"),
+    }
+
+
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        return int(max((i.get("num_threads", 1) for i in info), default=1))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ ranks
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        pg = dist
+    return world, rank, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def reduce_over_ranks(pg, x, op):
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64)
+    pg.all_reduce(t, op=op(pg))
+    return float(t.item())
+
+
+def max_over_ranks(pg, x):
+    return reduce_over_ranks(pg, x, lambda d: d.ReduceOp.MAX)
+
+
+def sum_over_ranks(pg, x):
+    return reduce_over_ranks(pg, x, lambda d: d.ReduceOp.SUM)
+
+
+# ------------------------------------------------------------------- arms
+def run_reference(args, shape, world, rank, pg):
+    """The oracle as it stands, on this host's cores (rank 0 only)."""
+    if rank != 0:
+        return 0
+    vals = []
+    base = None
+    for i in range(args.warmup + args.steps):
+        b = oracle_sample(shape)
+        if i >= args.warmup:
+            vals.append(b["value"])
+            base = b
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": shape.batch * shape.seq / value * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded uniform token ids, normal(0, 0.02) weights)",
+        "config": {"workload": workload_desc(shape), "parallelism": "none (host cores)"},
+        "cpu_baseline": {k: base[k] for k in ("value", "unit", "cores", "kind", "sample")},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gemm_kernel(args):
+    """One GEMM shape through mt_k_gemm (a small case for profiler captures)."""
+    import torch
+    import host_memory_resident_gb300 as mt
+    M, N, K = (int(x) for x in args.shape.split(","))
+    torch.manual_seed(0)
+    A = torch.randn(M, K, device="cuda").to(torch.bfloat16)
+    B = (torch.randn(N, K, device="cuda") / math.sqrt(K)).to(torch.bfloat16)
+    Cm = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+    for _ in range(2):
+        mt.k_gemm(A, B, Cm)
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record()
+    for _ in range(args.iters):
+        mt.k_gemm(A, B, Cm)
+    s1.record()
+    torch.cuda.synchronize()
+    ms = s0.elapsed_time(s1) / args.iters
+    ref = A[:256].float() @ B.float().t()
+    err = (Cm[:256].float() - ref).abs().max().item() / ref.abs().max().item()
+    print(json.dumps({"kernel": "gemm_abt", "M": M, "N": N, "K": K, "ms": ms,
+                      "tflops": 2.0 * M * N * K / ms / 1e9, "max_rel_err_rows0_255": err}), flush=True)
+    return 0 if err < 2e-2 else 1
+
+
+def run_ours(args, shape, world, rank, local, pg):
+    import torch
+    import host_memory_resident_gb300 as mt
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = mt.make_config(shape, device=local, host_threads=args.host_threads)
+    descs, n_total = mt.layout(cfg)
+    segs = [(t["offset"], t["rows"] * t["cols"], "normal" if t["kind"] == 0 else "ones") for t in descs]
+    master = synth.init_master(n_total, segs, seed=0)
+    B, s = shape.batch, shape.seq
+    M = B * s
+    W, K = args.warmup, args.steps
+    batches = [synth.make_tokens(shape.vocab, B, s, seed=1 + 1000 * rank, step=i) for i in range(W + 2 * K)]
+    dev_batches = [(torch.from_numpy(t).to(dev), torch.from_numpy(l).to(dev)) for t, l in batches[:W + K]]
+    link = host_link_probe(torch, dev)
+    torch.cuda.empty_cache()
+
+    tr = mt.Trainer(cfg, master)
+    comp = torch.cuda.ExternalStream(tr.stream(0), device=dev)
+    for i in range(W):
+        tr.step_device(dev_batches[i][0].data_ptr(), dev_batches[i][1].data_ptr(), B, s)
+
+    # ---- timed region: K steps, token/label arrays resident in device memory
+    tr.profile(True)
+    tr.read_profile(reset=True)
+    st0 = tr.stats()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.5)
+    barrier(pg)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(comp)
+    t0 = time.perf_counter()
+    losses = []
+    for i in range(K):
+        tk, lb = dev_batches[W + i]
+        losses.append(tr.step_device(tk.data_ptr(), lb.data_ptr(), B, s))
+    e1.record(comp)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t0
+    barrier(pg)
+    clk = clocks.stop()
+    st1 = tr.stats()
+    prof = tr.read_profile(reset=True)
+    tr.profile(False)
+    t_max = max_over_ranks(pg, e0.elapsed_time(e1) / 1e3)
+
+    # ---- end to end: host token/label arrays through mt_train_step
+    barrier(pg)
+    torch.cuda.synchronize(dev)
+    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2.record(comp)
+    for i in range(K):
+        tk, lb = batches[W + K + i]
+        losses.append(tr.step(tk, lb))
+    e3.record(comp)
+    torch.cuda.synchronize(dev)
+    barrier(pg)
+    e2e_max = max_over_ranks(pg, e2.elapsed_time(e3) / 1e3)
+    stats = tr.stats()
+    tr.close()
+
+    tokens_all = sum_over_ranks(pg, float(M * K))
+    value = tokens_all / t_max
+    pk, pk_kind = peaks()
+    F = model_flops(shape, B, s)
+    t_step = t_max / K
+    g = prof["gemm"]
+    gemm_tf = g["flops"] / (g["ms"] / 1e3) / 1e12 if g["ms"] > 0 else None
+    peak_tf = pk["bf16_tflops_sustained"]
+    traffic = gemm_traffic_record()
+    w_bytes = 2.0 * n_total
+    t_comp = F / (pk["bf16_tflops"] * 1e12)
+    t_link = max(2 * w_bytes / (link["bidir_h2d_gbs"] * 1e9), w_bytes / (link["bidir_d2h_gbs"] * 1e9))
+    t_roof = max(t_comp, t_link)
+    prof_out = {k: {"launches": v["launches"], "ms_per_step": v["ms"] / K,
+                    "tflops": (v["flops"] / (v["ms"] / 1e3) / 1e12) if v["flops"] and v["ms"] else None,
+                    "gbs": (v["bytes"] / (v["ms"] / 1e3) / 1e9) if v["bytes"] and v["ms"] else None}
+                for k, v in prof.items() if v["launches"]}
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded uniform token ids, normal(0, 0.02) weights, norms 1.0)",
+        "config": {"workload": workload_desc(shape), "global_batch_tokens": M * world, "seq_len": s,
+                   "parallelism": f"replicas x{world} (no collective)" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2: each step streams the whole bf16 store "
+                         f"({w_bytes / 1e9:.2f} GB) and the activations"},
+        "model_tflops": F / t_step / 1e12,
+        "step_roofline": {"model_flops": F, "t_compute_s": t_comp, "t_link_s": t_link, "t_roof_s": t_roof,
+                          "frac": t_roof / t_step, "peak_tflops": pk["bf16_tflops"], "host_link": link,
+                          "weight_bytes": w_bytes, "peak_source": pk_kind},
+        "roofline": {"bound": "tensor", "kernel": "gemm_abt (tcgen05)", "achieved": gemm_tf, "peak": peak_tf,
+                     "unit": "TFLOP/s", "frac": (gemm_tf / peak_tf) if gemm_tf else None,
+                     "peak_source": f"bf16_tflops_sustained, of {pk_kind}",
+                     "traffic": traffic["dram_bytes_per_launch"] if traffic else None},
+        "kernels": prof_out,
+        "host": {"adam_s_per_step": (st1["host_adam_s"] - st0["host_adam_s"]) / K,
+                 "slab_wait_s_per_step": (st1["host_wait_s"] - st0["host_wait_s"]) / K,
+                 "h2d_gb_per_step": (st1["h2d_bytes"] - st0["h2d_bytes"]) / K / 1e9,
+                 "d2h_gb_per_step": (st1["d2h_bytes"] - st0["d2h_bytes"]) / K / 1e9,
+                 "threads": args.host_threads or os.cpu_count(),
+                 "device_gb": stats["device_bytes"] / 1e9, "pinned_gb": stats["pinned_bytes"] / 1e9},
+        "clocks": clk,
+        "gpu_launches": int(st1["kernel_launches"] - st0["kernel_launches"]),
+        "e2e": {"value": tokens_all / e2e_max, "unit": "tokens/s", "h2d_bytes_per_step": 2 * 4 * M,
+                "d2h_bytes_per_step": 4},
+        "loss": {"first": losses[0], "last": losses[-1]},
+        "wall_s_timed": wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = oracle_sample(shape)
+        line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="1.1b", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--kernel", default=None, choices=[None, "gemm"])
+    ap.add_argument("--shape", default="8192,8192,2048")
+    ap.add_argument("--iters", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--host-threads", type=int, default=0)
+    args = ap.parse_args()
+    if args.kernel == "gemm":
+        return run_gemm_kernel(args)
+    shape = synth.workload(args.config)
+    world, rank, local, pg = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, shape, world, rank, pg)
+    return run_ours(args, shape, world, rank, local, pg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

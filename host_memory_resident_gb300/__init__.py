@@ -49,13 +49,22 @@ class TensorDesc(C.Structure):
 class Stats(C.Structure):
     _fields_ = [("steps", C.c_int64), ("h2d_bytes", C.c_int64), ("d2h_bytes", C.c_int64),
                 ("h2d_units", C.c_int64), ("host_adam_s", C.c_double), ("host_wait_s", C.c_double),
-                ("last_step_s", C.c_double), ("device_bytes", C.c_int64), ("pinned_bytes", C.c_int64)]
+                ("last_step_s", C.c_double), ("device_bytes", C.c_int64), ("pinned_bytes", C.c_int64),
+                ("kernel_launches", C.c_int64)]
+
+
+PROF_CLASSES = ["gemm", "attn_fwd", "attn_bwd", "norm", "rope", "swiglu", "transpose", "ce", "embed", "other"]
+
+
+class KernelProfile(C.Structure):
+    _fields_ = [("launches", C.c_int64 * 10), ("ms", C.c_double * 10), ("flops", C.c_double * 10),
+                ("bytes", C.c_double * 10)]
 
 
 EXPORTS = [
     "mt_layout", "mt_unit_range", "mt_init", "mt_train_step", "mt_train_step_device",
     "mt_read_grads", "mt_get_step", "mt_set_step", "mt_sync_store", "mt_get_stats",
-    "mt_get_stream", "mt_destroy", "mt_last_error", "mt_debug_inject", "mt_debug_inject_global",
+    "mt_get_stream", "mt_profile_enable", "mt_profile_read", "mt_destroy", "mt_last_error", "mt_debug_inject", "mt_debug_inject_global",
     "mt_host_adam", "mt_host_to_bf16",
     "mt_k_gemm", "mt_k_transpose", "mt_k_rmsnorm_fwd", "mt_k_rmsnorm_bwd", "mt_k_rmsnorm_bwd_parts",
     "mt_k_rope", "mt_k_swiglu_fwd", "mt_k_swiglu_bwd", "mt_k_attn_fwd", "mt_k_attn_bwd",
@@ -90,6 +99,8 @@ def lib():
         "mt_sync_store": ([P], I),
         "mt_get_stats": ([P, C.POINTER(Stats)], I),
         "mt_get_stream": ([P, I, C.POINTER(P)], I),
+        "mt_profile_enable": ([P, I], I),
+        "mt_profile_read": ([P, C.POINTER(KernelProfile), I], I),
         "mt_destroy": ([P], I),
         "mt_last_error": ([P], C.c_char_p),
         "mt_debug_inject": ([P, I, I64], I),
@@ -230,6 +241,15 @@ class Trainer:
         s = Stats()
         check(lib().mt_get_stats(self.h, C.byref(s)), self.h)
         return {k: getattr(s, k) for k, _ in Stats._fields_}
+
+    def profile(self, on: bool = True):
+        check(lib().mt_profile_enable(self.h, 1 if on else 0))
+
+    def read_profile(self, reset: bool = False) -> dict:
+        p = KernelProfile()
+        check(lib().mt_profile_read(self.h, C.byref(p), 1 if reset else 0))
+        return {name: dict(launches=p.launches[i], ms=p.ms[i], flops=p.flops[i], bytes=p.bytes[i])
+                for i, name in enumerate(PROF_CLASSES)}
 
     def get_step(self) -> int:
         t = C.c_int64()

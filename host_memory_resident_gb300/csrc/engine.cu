@@ -170,8 +170,13 @@ struct mt_handle {
   int64_t inject_sleep_ms = 0, inject_fail_at = 0, deadline_ms = 600000;
   int64_t worker_units_total = 0;
 
-  // stats
+  // stats and the optional per-kernel profile (CUDA events on the compute stream)
   mt_stats st{};
+  int prof_on = 0;
+  std::vector<cudaEvent_t> prof_events;
+  struct ProfRec { int cat; double flops, bytes; };
+  std::vector<ProfRec> prof_recs;
+  mt_kernel_profile prof{};
 };
 
 namespace mt {
@@ -329,31 +334,69 @@ struct Step {
     h->cv.notify_all();
   }
 
+  // Kernel launch bookkeeping: count launches and, when profiling is on,
+  // bracket the launch with a pair of events on the compute stream.
+  size_t prof_next = 0;
+  void prof_begin() {
+    if (!h->prof_on) return;
+    while (h->prof_events.size() < 2 * (prof_next + 1)) {
+      cudaEvent_t e;
+      CK(cudaEventCreate(&e));
+      h->prof_events.push_back(e);
+    }
+    CK(cudaEventRecord(h->prof_events[2 * prof_next], cs()));
+  }
+  void prof_end(int cat, int launches, double flops, double bytes) {
+    h->st.kernel_launches += launches;
+    h->prof.launches[cat] += launches;
+    if (!h->prof_on) return;
+    CK(cudaEventRecord(h->prof_events[2 * prof_next + 1], cs()));
+    h->prof_recs.push_back({cat, flops, bytes});
+    ++prof_next;
+  }
+#define KP(cat, nl, fl, by, call) \
+  do {                            \
+    prof_begin();                 \
+    KK(call);                     \
+    prof_end(cat, nl, fl, by);    \
+  } while (0)
+
   // C[M,N] = A[M,K] * B[N,K]^T (+R)
   void gemm(const bf16* A, long long lda, const bf16* Bm, long long ldb, void* C, long long ldc, bool f32,
             const bf16* R, long long ldr, int m, int n, int k) {
-    KK(gemm_abt(A, lda, Bm, ldb, C, ldc, f32 ? 1 : 0, R, ldr, m, n, k, cs()));
+    const double bytes = 2.0 * ((double)m * k + (double)n * k) + (f32 ? 4.0 : 2.0) * m * n + (R ? 2.0 * m * n : 0.0);
+    KP(MT_PROF_GEMM, 1, 2.0 * m * n * k, bytes,
+       gemm_abt(A, lda, Bm, ldb, C, ldc, f32 ? 1 : 0, R, ldr, m, n, k, cs()));
   }
   // out[c, r] = in[r, c]; `rows` is M for activations (pitch ldT), else the
   // weight's row count (pitch = rows).
   void transpose(const bf16* in, long long ldi, bf16* out, int rows, int cols) {
     const long long ldo = rows == M ? ldT : rows;
-    KK(mt_k_transpose(in, ldi, out, ldo, rows, cols, cs()));
+    KP(MT_PROF_TRANSPOSE, 1, 0.0, 4.0 * rows * cols, mt_k_transpose(in, ldi, out, ldo, rows, cols, cs()));
   }
+  double attn_flops(bool bwd) const {
+    // causal: half of the s x s score matrix; forward 2 products, backward 5
+    const double per = 2.0 * B * (double)h->H * s * (double)s * h->hd / 2.0;
+    return (bwd ? 5.0 : 2.0) * per;
+  }
+  double norm_fwd_bytes() const { return 4.0 * M * h->d + 4.0 * M; }
+  double norm_bwd_bytes(bool res) const { return (4.0 + 2.0 + 4.0 + 2.0 + (res ? 4.0 : 0.0)) * M * h->d; }
+  double rope_bytes() const { return 4.0 * M * (h->H + h->Hkv) * h->hd; }
 
   // Forward of layer l with weights W; writes the saved activations into S and
   // the layer output into x_out.
   void layer_fwd(const bf16* W, const Saved& S, bf16* x_out) {
     const LayerOffsets& o = h->lay.layer;
     const int d = h->d, f = h->f;
-    KK(mt_k_rmsnorm_fwd(S.x, W + o.attn_norm, S.u, S.r1, M, d, h->cfg.rms_eps, cs()));
+    KP(MT_PROF_NORM, 1, 0.0, norm_fwd_bytes(), mt_k_rmsnorm_fwd(S.x, W + o.attn_norm, S.u, S.r1, M, d, h->cfg.rms_eps, cs()));
     gemm(S.u, d, W + o.wqkv, d, S.qkv, h->qkvN, false, nullptr, 0, M, h->qkvN, d);
-    KK(mt_k_rope(S.qkv, h->qkvN, B, s, h->H + h->Hkv, h->hd, h->cos_t, h->sin_t, 0, cs()));
-    KK(mt_k_attn_fwd(S.qkv, h->qkvN, S.o, h->hq, S.lse, B, s, h->H, h->Hkv, h->hd, cs()));
+    KP(MT_PROF_ROPE, 1, 0.0, rope_bytes(), mt_k_rope(S.qkv, h->qkvN, B, s, h->H + h->Hkv, h->hd, h->cos_t, h->sin_t, 0, cs()));
+    KP(MT_PROF_ATTN_FWD, 1, attn_flops(false), 0.0,
+       mt_k_attn_fwd(S.qkv, h->qkvN, S.o, h->hq, S.lse, B, s, h->H, h->Hkv, h->hd, cs()));
     gemm(S.o, h->hq, W + o.wo, h->hq, S.h, d, false, S.x, d, M, d, h->hq);
-    KK(mt_k_rmsnorm_fwd(S.h, W + o.mlp_norm, S.z, S.r2, M, d, h->cfg.rms_eps, cs()));
+    KP(MT_PROF_NORM, 1, 0.0, norm_fwd_bytes(), mt_k_rmsnorm_fwd(S.h, W + o.mlp_norm, S.z, S.r2, M, d, h->cfg.rms_eps, cs()));
     gemm(S.z, d, W + o.wgu, d, S.gu, 2 * f, false, nullptr, 0, M, 2 * f, d);
-    KK(mt_k_swiglu_fwd(S.gu, S.a, M, f, cs()));
+    KP(MT_PROF_SWIGLU, 1, 0.0, 6.0 * M * f, mt_k_swiglu_fwd(S.gu, S.a, M, f, cs()));
     gemm(S.a, f, W + o.wdown, f, x_out, d, false, S.h, d, M, d, f);
   }
 
@@ -369,14 +412,15 @@ struct Step {
     gemm(h->tA, ldT, h->tB, ldT, g + o.wdown, f, false, nullptr, 0, d, f, M);
     transpose(W + o.wdown, f, h->wT, d, f);
     gemm(h->dxb, d, h->wT, d, h->da, f, false, nullptr, 0, M, f, d);
-    KK(mt_k_swiglu_bwd(h->da, S.gu, h->dgu, M, f, cs()));
+    KP(MT_PROF_SWIGLU, 1, 0.0, 10.0 * M * f, mt_k_swiglu_bwd(h->da, S.gu, h->dgu, M, f, cs()));
     // gate/up projection
     transpose(h->dgu, 2 * f, h->tA, M, 2 * f);
     transpose(S.z, d, h->tB, M, d);
     gemm(h->tA, ldT, h->tB, ldT, g + o.wgu, d, false, nullptr, 0, 2 * f, d, M);
     transpose(W + o.wgu, d, h->wT, 2 * f, d);
     gemm(h->dgu, 2 * f, h->wT, 2 * f, h->dn32, d, true, nullptr, 0, M, d, 2 * f);
-    KK(mt_k_rmsnorm_bwd(h->dn32, S.h, W + o.mlp_norm, S.r2, h->dx32, h->dh32, h->dhb, h->npart, g + o.mlp_norm, M,
+    KP(MT_PROF_NORM, 2, 0.0, norm_bwd_bytes(true),
+       mt_k_rmsnorm_bwd(h->dn32, S.h, W + o.mlp_norm, S.r2, h->dx32, h->dh32, h->dhb, h->npart, g + o.mlp_norm, M,
                         d, cs()));
     // output projection
     transpose(h->dhb, d, h->tA, M, d);
@@ -385,15 +429,17 @@ struct Step {
     transpose(W + o.wo, hq, h->wT, d, hq);
     gemm(h->dhb, d, h->wT, d, h->dob, hq, false, nullptr, 0, M, hq, d);
     // attention and RoPE
-    KK(mt_k_attn_bwd(S.qkv, qn, S.o, hq, h->dob, hq, S.lse, h->delta, h->dqkv, qn, B, s, h->H, h->Hkv, h->hd, cs()));
-    KK(mt_k_rope(h->dqkv, qn, B, s, h->H + h->Hkv, h->hd, h->cos_t, h->sin_t, 1, cs()));
+    KP(MT_PROF_ATTN_BWD, 3, attn_flops(true), 0.0,
+       mt_k_attn_bwd(S.qkv, qn, S.o, hq, h->dob, hq, S.lse, h->delta, h->dqkv, qn, B, s, h->H, h->Hkv, h->hd, cs()));
+    KP(MT_PROF_ROPE, 1, 0.0, rope_bytes(), mt_k_rope(h->dqkv, qn, B, s, h->H + h->Hkv, h->hd, h->cos_t, h->sin_t, 1, cs()));
     // qkv projection
     transpose(h->dqkv, qn, h->tA, M, qn);
     transpose(S.u, d, h->tB, M, d);
     gemm(h->tA, ldT, h->tB, ldT, g + o.wqkv, d, false, nullptr, 0, qn, d, M);
     transpose(W + o.wqkv, d, h->wT, qn, d);
     gemm(h->dqkv, qn, h->wT, qn, h->dn32, d, true, nullptr, 0, M, d, qn);
-    KK(mt_k_rmsnorm_bwd(h->dn32, S.x, W + o.attn_norm, S.r1, h->dh32, h->dx32, h->dxb, h->npart, g + o.attn_norm, M,
+    KP(MT_PROF_NORM, 2, 0.0, norm_bwd_bytes(true),
+       mt_k_rmsnorm_bwd(h->dn32, S.x, W + o.attn_norm, S.r1, h->dh32, h->dx32, h->dxb, h->npart, g + o.attn_norm, M,
                         d, cs()));
   }
 
@@ -402,15 +448,16 @@ struct Step {
     const int d = h->d, V = h->V;
     const bf16* wf = W + h->lay.final_norm;
     const bf16* head = W + h->lay.head;
-    KK(mt_k_rmsnorm_fwd(xL, wf, h->xh, h->rf, M, d, h->cfg.rms_eps, cs()));
+    KP(MT_PROF_NORM, 1, 0.0, norm_fwd_bytes(), mt_k_rmsnorm_fwd(xL, wf, h->xh, h->rf, M, d, h->cfg.rms_eps, cs()));
     const float scale = 1.f / (float)M;
     for (int r0 = 0; r0 < M; r0 += h->Mchunk) {
       const int mc = std::min(h->Mchunk, M - r0);
       gemm(h->xh + (size_t)r0 * d, d, head, d, h->logits, V, true, nullptr, 0, mc, V, d);
-      KK(mt_k_cross_entropy(h->logits, V, h->d_lab + r0, h->dz + (size_t)r0 * V, V, h->loss_rows + r0, mc, V, scale,
+      KP(MT_PROF_CE, 1, 0.0, 6.0 * mc * (double)V,
+         mt_k_cross_entropy(h->logits, V, h->d_lab + r0, h->dz + (size_t)r0 * V, V, h->loss_rows + r0, mc, V, scale,
                             cs()));
     }
-    KK(mt_k_sum(h->loss_rows, M, h->loss_dev, cs()));
+    KP(MT_PROF_OTHER, 1, 0.0, 4.0 * M, mt_k_sum(h->loss_rows, M, h->loss_dev, cs()));
     CK(cudaMemcpyAsync(h->loss_pinned, h->loss_dev, sizeof(float), cudaMemcpyDeviceToHost, cs()));
     CK(cudaEventRecord(h->ev_loss, cs()));
     // dHead = dz^T xh ; dxh = dz Head
@@ -419,7 +466,8 @@ struct Step {
     gemm(h->tA, ldT, h->tB, ldT, g + h->lay.head, d, false, nullptr, 0, V, d, M);
     transpose(head, d, h->wT, V, d);
     gemm(h->dz, V, h->wT, V, h->dn32, d, true, nullptr, 0, M, d, V);
-    KK(mt_k_rmsnorm_bwd(h->dn32, xL, wf, h->rf, nullptr, h->dx32, h->dxb, h->npart, g + h->lay.final_norm, M, d,
+    KP(MT_PROF_NORM, 2, 0.0, norm_bwd_bytes(false),
+       mt_k_rmsnorm_bwd(h->dn32, xL, wf, h->rf, nullptr, h->dx32, h->dxb, h->npart, g + h->lay.final_norm, M, d,
                         cs()));
   }
 
@@ -438,7 +486,8 @@ struct Step {
     // ---- forward: embedding, layers (checkpoint every C), head
     {
       bf16* E = acquire(0);
-      KK(mt_k_embedding_fwd(E + (hh.lay.embed - hh.lay.unit_off[0]), hh.d_tok, hh.ckpt[0], M, hh.d, hh.V, cs()));
+      KP(MT_PROF_EMBED, 1, 0.0, 4.0 * M * hh.d,
+         mt_k_embedding_fwd(E + (hh.lay.embed - hh.lay.unit_off[0]), hh.d_tok, hh.ckpt[0], M, hh.d, hh.V, cs()));
       release();
     }
     bf16* x = hh.ckpt[0];
@@ -481,7 +530,8 @@ struct Step {
     }
     {
       const int k = slab_begin();
-      KK(mt_k_embedding_bwd(hh.dx32, hh.d_tok, hh.slab[k] + 0, M, hh.d, hh.V, hh.d_ework, cs()));
+      KP(MT_PROF_EMBED, 2, 0.0, 4.0 * M * hh.d + 2.0 * hh.V * (double)hh.d,
+         mt_k_embedding_bwd(hh.dx32, hh.d_tok, hh.slab[k] + 0, M, hh.d, hh.V, hh.d_ework, cs()));
       slab_end(k, 0);
     }
   }
@@ -505,6 +555,7 @@ void destroy_resources(mt_handle* h) {
   }
   for (auto e : h->ev_slab_ready) if (e) cudaEventDestroy(e);
   for (auto e : h->ev_d2h_done) if (e) cudaEventDestroy(e);
+  for (auto e : h->prof_events) if (e) cudaEventDestroy(e);
   if (h->ev_loss) cudaEventDestroy(h->ev_loss);
   if (h->ev_resident) cudaEventDestroy(h->ev_resident);
   if (h->s_comp) cudaStreamDestroy(h->s_comp);
@@ -796,6 +847,17 @@ static int run_step(mt_handle* h, const int32_t* tokens, const int32_t* labels, 
     CK(cudaStreamSynchronize(h->s_comp));
     CK(cudaStreamSynchronize(h->s_d2h));
     CK(cudaStreamSynchronize(h->s_h2d));
+    if (h->prof_on) {
+      for (size_t i = 0; i < h->prof_recs.size(); ++i) {
+        float ms = 0.f;
+        CK(cudaEventElapsedTime(&ms, h->prof_events[2 * i], h->prof_events[2 * i + 1]));
+        const auto& r = h->prof_recs[i];
+        h->prof.ms[r.cat] += ms;
+        h->prof.flops[r.cat] += r.flops;
+        h->prof.bytes[r.cat] += r.bytes;
+      }
+    }
+    h->prof_recs.clear();
     int dev_err = 0;
     if (mt_k_device_error(&dev_err, 1) != MT_OK) throw StepError{MT_ECUDA, "reading the device error word failed"};
     if (dev_err) throw StepError{MT_EDEVICE, "a kernel reported device error " + std::to_string(dev_err)};
@@ -810,6 +872,7 @@ static int run_step(mt_handle* h, const int32_t* tokens, const int32_t* labels, 
                                      [&] { return h->in_flight == 0; });
     if (e.code == MT_ETIMEOUT || e.code == MT_EDEVICE || e.code == MT_ECUDA || !idle) h->broken = 1;
     for (auto& b : h->staging_busy) b = 0;
+    h->prof_recs.clear();
     h->err = e.msg;
     g_thread_error = e.msg;
     return e.code;
@@ -868,6 +931,19 @@ int mt_get_stats(mt_handle* h, mt_stats* out) {
 int mt_get_stream(mt_handle* h, int which, void** stream) {
   if (!h || !stream || which < 0 || which > 2) return MT_EINVAL;
   *stream = which == 0 ? (void*)h->s_comp : which == 1 ? (void*)h->s_h2d : (void*)h->s_d2h;
+  return MT_OK;
+}
+
+int mt_profile_enable(mt_handle* h, int on) {
+  if (!h) return MT_EINVAL;
+  h->prof_on = on ? 1 : 0;
+  return MT_OK;
+}
+
+int mt_profile_read(mt_handle* h, mt_kernel_profile* out, int reset) {
+  if (!h || !out) return MT_EINVAL;
+  *out = h->prof;
+  if (reset) h->prof = mt_kernel_profile{};
   return MT_OK;
 }
 

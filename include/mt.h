@@ -81,7 +81,31 @@ typedef struct mt_stats {
   double last_step_s;      /* wall time of the last mt_train_step */
   int64_t device_bytes;    /* device memory owned by the handle */
   int64_t pinned_bytes;    /* pinned host memory owned by the handle */
+  int64_t kernel_launches; /* kernels launched by the handle, all steps */
 } mt_stats;
+
+/* Kernel classes of the per-kernel profile. */
+#define MT_PROF_GEMM 0
+#define MT_PROF_ATTN_FWD 1
+#define MT_PROF_ATTN_BWD 2
+#define MT_PROF_NORM 3
+#define MT_PROF_ROPE 4
+#define MT_PROF_SWIGLU 5
+#define MT_PROF_TRANSPOSE 6
+#define MT_PROF_CE 7
+#define MT_PROF_EMBED 8
+#define MT_PROF_OTHER 9
+#define MT_PROF_N 10
+
+/* Per-class totals: launches, device time (CUDA events around each launch
+ * on the compute stream, only while profiling is enabled), algorithmic
+ * FLOPs and algorithmic HBM bytes of the timed launches. */
+typedef struct mt_kernel_profile {
+  int64_t launches[MT_PROF_N];
+  double ms[MT_PROF_N];
+  double flops[MT_PROF_N];
+  double bytes[MT_PROF_N];
+} mt_kernel_profile;
 
 typedef struct mt_handle mt_handle;
 
@@ -136,6 +160,12 @@ int mt_sync_store(mt_handle* h);
 int mt_get_stats(mt_handle* h, mt_stats* out);
 /* Returns the handle's CUDA stream: which 0 = compute, 1 = H2D, 2 = D2H. */
 int mt_get_stream(mt_handle* h, int which, void** stream);
+/* Brackets every kernel launch of later steps with CUDA events on the
+ * compute stream (on = 1) so mt_profile_read() can report device time per
+ * kernel class; adds two event records per launch. */
+int mt_profile_enable(mt_handle* h, int on);
+/* Copies the accumulated per-class profile; reset = 1 clears it. */
+int mt_profile_read(mt_handle* h, mt_kernel_profile* out, int reset);
 int mt_destroy(mt_handle* h);
 /* Last error message of `h`, or of the calling thread when h is NULL. */
 const char* mt_last_error(mt_handle* h);
