@@ -638,6 +638,9 @@ int fail(mt_handle* h, int code, const std::string& msg) {
 }
 
 }  // namespace
+
+void set_last_error_message(const std::string& msg) { g_thread_error = msg; }
+
 }  // namespace mt
 
 using namespace mt;

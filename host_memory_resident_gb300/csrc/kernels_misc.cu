@@ -9,6 +9,7 @@
 #include <cfloat>
 #include <cmath>
 #include <mutex>
+#include <string>
 
 #include "common.cuh"
 #include "mt_internal.h"
@@ -647,3 +648,66 @@ int mt_k_device_error(int* code, int reset) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------
+// Embedding backward that allocates nothing (see mt_k_embedding_bwd_noalloc
+// in mt_kernels.h). Its sort workspace lives in this fixed device array,
+// which every GPU that loads the library keeps until the process exits.
+namespace {
+
+constexpr int kNoAllocMaxV = MT_NOALLOC_EMBED_MAX_VOCAB;
+constexpr int kNoAllocMaxM = MT_NOALLOC_EMBED_MAX_TOKENS;
+static __device__ __align__(256) int32_t g_embed_bwd_scratch[2 * kNoAllocMaxV + 1 + kNoAllocMaxM];
+
+// Device address of g_embed_bwd_scratch for the current device, looked up
+// once per device (host code may not use the symbol itself: on the host it
+// names a stand-in, not device memory).
+int32_t* embed_scratch_address(cudaError_t* err) {
+  static int32_t* addr[64] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= 64) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_embed_bwd_scratch);
+    if (*err != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<int32_t*>(p);
+  }
+  return addr[dev];
+}
+
+}  // namespace
+
+extern "C" int mt_k_embedding_bwd_noalloc(const float* dx, const int32_t* tok, void* dE, int M, int d, int V,
+                                          void* stream) {
+  if (M > kNoAllocMaxM || V > kNoAllocMaxV) {
+    set_last_error_message("mt_k_embedding_bwd_noalloc: M (" + std::to_string(M) + ") or V (" +
+                           std::to_string(V) + ") above the fixed workspace limits of " +
+                           std::to_string(kNoAllocMaxM) + " tokens and " + std::to_string(kNoAllocMaxV) +
+                           " vocabulary rows");
+    return MT_EINVAL;
+  }
+  if (M < 0 || d <= 0 || d % 4 || V <= 0 || !al16(dx) || (reinterpret_cast<uintptr_t>(dE) & 7)) return MT_EINVAL;
+  cudaError_t err = cudaSuccess;
+  int32_t* work = embed_scratch_address(&err);
+  if (!work) {
+    set_last_error_message(std::string("mt_k_embedding_bwd_noalloc: cudaGetSymbolAddress failed: ") +
+                           cudaGetErrorString(err));
+    return MT_ECUDA;
+  }
+  // The sort kernel clears its own counters and rewrites every bucket start
+  // and every position it later reads, so nothing left by an earlier call
+  // is used. No error word is passed: the library's error word is allocated
+  // on first use, which this entry point must not do.
+  cudaStream_t st = (cudaStream_t)stream;
+  token_sort_kernel<<<1, kSortThreads, 0, st>>>(tok, M, V, work, nullptr);
+  dim3 grid(V, (d / 4 + 255) / 256);
+  embedding_bwd_reduce_kernel<<<grid, 256, 0, st>>>(dx, work, (bf16*)dE, d, V);
+  return launch_ok();
+}

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <string>
 
 #include "../../include/mt.h"
 #include "../../include/mt_kernels.h"
@@ -13,6 +14,9 @@ namespace mt {
 // Address of the current device's error word (allocated on first use,
 // zero-initialised, kept until process exit); null if allocation failed.
 int* device_error_word();
+
+// Sets the calling thread's message returned by mt_last_error(NULL).
+void set_last_error_message(const std::string& msg);
 
 // C = A * B^T (+ R); see mt_k_gemm.
 int gemm_abt(const void* A, long long lda, const void* B, long long ldb, void* C, long long ldc, int c_f32,

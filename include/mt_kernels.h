@@ -119,6 +119,31 @@ int mt_k_embedding_bwd(const float* dx, const int32_t* tok, void* dE, int M, int
                        void* stream);
 int64_t mt_k_embedding_bwd_work(int M, int V);
 
+/*
+ * Embedding backward for callers that cannot allocate device memory (for
+ * example code running inside another framework's memory pool, or a
+ * process whose allocator is owned by someone else), so they cannot pass the
+ * `work` buffer mt_k_embedding_bwd needs. The articles describe no such
+ * entry point; it exists for this library's users only.
+ *
+ * Same arguments and result as mt_k_embedding_bwd without `work`: the sort
+ * workspace is a fixed array of (2 * 262144 + 1 + 524288) int32 (4 MiB) in
+ * the library's device memory, held by every GPU that loads the library
+ * until the process exits. It therefore accepts at most
+ * MT_NOALLOC_EMBED_MAX_TOKENS tokens (M) and MT_NOALLOC_EMBED_MAX_VOCAB rows
+ * (V); larger sizes return MT_EINVAL with a message in mt_last_error(NULL).
+ * It calls no allocation routine. The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress, with that device current);
+ * make that first call before any stream capture. All calls share the one
+ * array: calls that can overlap on the GPU (other streams, other threads)
+ * race and must be serialised by the caller. Nothing a previous call left in
+ * the array affects the result. Ids outside [0, V) are left out of the sums
+ * without a report (check them first with mt_k_check_ids if needed).
+ */
+#define MT_NOALLOC_EMBED_MAX_TOKENS 524288
+#define MT_NOALLOC_EMBED_MAX_VOCAB 262144
+int mt_k_embedding_bwd_noalloc(const float* dx, const int32_t* tok, void* dE, int M, int d, int V, void* stream);
+
 /* Sets *bad = 1 if any of the n ids lies outside [0, V) (device check). */
 int mt_k_check_ids(const int32_t* ids, int n, int V, int32_t* bad, void* stream);
 
