@@ -402,10 +402,14 @@ def run_ours(args, shape, world, rank, local, pg):
                      "traffic": traffic["dram_bytes_per_launch"] if traffic else None},
         "kernels": prof_out,
         "host": {"adam_s_per_step": (st1["host_adam_s"] - st0["host_adam_s"]) / K,
+                 "adam_compute_s_per_step": (st1["host_compute_s"] - st0["host_compute_s"]) / K,
+                 "adam_compute_gbs": 32.0 * n_total * K / max(st1["host_compute_s"] - st0["host_compute_s"], 1e-9)
+                 / 1e9,
+                 "copy_wait_s_per_step": (st1["host_copy_wait_s"] - st0["host_copy_wait_s"]) / K,
                  "slab_wait_s_per_step": (st1["host_wait_s"] - st0["host_wait_s"]) / K,
                  "h2d_gb_per_step": (st1["h2d_bytes"] - st0["h2d_bytes"]) / K / 1e9,
                  "d2h_gb_per_step": (st1["d2h_bytes"] - st0["d2h_bytes"]) / K / 1e9,
-                 "threads": args.host_threads or os.cpu_count(),
+                 "threads": args.host_threads or (os.cpu_count() - 2 if os.cpu_count() > 4 else os.cpu_count()),
                  "device_gb": stats["device_bytes"] / 1e9, "pinned_gb": stats["pinned_bytes"] / 1e9},
         "clocks": clk,
         "gpu_launches": int(st1["kernel_launches"] - st0["kernel_launches"]),

@@ -50,7 +50,7 @@ class Stats(C.Structure):
     _fields_ = [("steps", C.c_int64), ("h2d_bytes", C.c_int64), ("d2h_bytes", C.c_int64),
                 ("h2d_units", C.c_int64), ("host_adam_s", C.c_double), ("host_wait_s", C.c_double),
                 ("last_step_s", C.c_double), ("device_bytes", C.c_int64), ("pinned_bytes", C.c_int64),
-                ("kernel_launches", C.c_int64)]
+                ("kernel_launches", C.c_int64), ("host_compute_s", C.c_double), ("host_copy_wait_s", C.c_double)]
 
 
 PROF_CLASSES = ["gemm", "attn_fwd", "attn_bwd", "norm", "rope", "swiglu", "transpose", "ce", "embed", "other"]

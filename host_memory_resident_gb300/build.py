@@ -71,7 +71,7 @@ def build(verbose: bool = False, force: bool = False, ptxas_verbose: bool = Fals
         objs.append(o)
         if force or _stale(o, [s] + headers):
             cxx = shutil.which("g++") or "g++"
-            jobs.append([cxx, "-O3", "-std=c++17", "-fPIC", "-fopenmp", "-c", s, "-o", o])
+            jobs.append([cxx, "-O3", "-std=c++17", "-fPIC", "-fopenmp", "-fno-math-errno", "-c", s, "-o", o])
     with cf.ThreadPoolExecutor(max(1, min(len(jobs), os.cpu_count() or 1))) as ex:
         results = list(ex.map(lambda c: _run(c, verbose), jobs))
     if ptxas_verbose:

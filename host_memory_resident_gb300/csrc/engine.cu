@@ -201,6 +201,7 @@ void worker_main(mt_handle* h) {
     }
     int code = MT_OK;
     std::string msg;
+    double wait_s = 0.0, compute_s = 0.0;
     const auto t0 = Clock::now();
     const auto deadline = t0 + std::chrono::milliseconds(h->deadline_ms);
     if (h->inject_sleep_ms > 0) std::this_thread::sleep_for(std::chrono::milliseconds(h->inject_sleep_ms));
@@ -227,6 +228,7 @@ void worker_main(mt_handle* h) {
         std::this_thread::sleep_for(std::chrono::microseconds(20));
       }
     };
+    const auto tw = Clock::now();
     if (code == MT_OK && wait_event(h->ev_d2h_done[job.slab]) && h->loss_state == 0 && wait_event(h->ev_loss)) {
       const float total = *h->loss_pinned;
       h->loss_state = std::isfinite(total) ? 1 : 2;
@@ -248,11 +250,16 @@ void worker_main(mt_handle* h) {
       a.beta2 = h->cfg.beta2;
       a.eps = h->cfg.adam_eps;
       a.apply = h->loss_state == 1;
+      const auto tc = Clock::now();
+      wait_s = std::chrono::duration<double>(tc - tw).count();
       adam_pass(a, h->threads);
+      compute_s = seconds_since(tc);
     }
     {
       std::lock_guard<std::mutex> lk(h->mu);
       h->st.host_adam_s += seconds_since(t0);
+      h->st.host_compute_s += compute_s;
+      h->st.host_copy_wait_s += wait_s;
       h->staging_busy[job.slab] = 0;
       h->in_flight = 0;
       ++h->units_done;
@@ -475,6 +482,9 @@ struct Step {
     mt_handle& hh = *h;
     const int L = hh.L, C = hh.cfg.ckpt_interval;
     hh.loss_state = 0;
+    // The host Adam rewrote the bf16 store since the last step, so nothing
+    // left in the two device buffers may be reused: forget their contents.
+    hh.slot_unit[0] = hh.slot_unit[1] = -1;
     if (!hh.cfg.streamed) {
       const size_t bytes = sizeof(uint16_t) * hh.n_total;
       CK(cudaMemcpyAsync(hh.resident, hh.store, bytes, cudaMemcpyHostToDevice, hh.s_h2d));

@@ -91,17 +91,19 @@ FlatLayout build_layout(const mt_config& c) {
   return L;
 }
 
-uint16_t to_bf16_rne(float f) {
+// Round-to-nearest-even of the top 16 bits; every NaN becomes 0x7fc0.
+// Branch-free so the loops below vectorize.
+static inline uint16_t rne_bits(float f) {
   uint32_t u;
   std::memcpy(&u, &f, 4);
-  if ((u & 0x7fffffffu) > 0x7f800000u) return 0x7fc0;  // NaN
-  const uint32_t lsb = (u >> 16) & 1u;
-  u += 0x7fffu + lsb;
-  return (uint16_t)(u >> 16);
+  const uint32_t r = (u + 0x7fffu + ((u >> 16) & 1u)) >> 16;
+  return (uint16_t)(((u & 0x7fffffffu) > 0x7f800000u) ? 0x7fc0u : r);
 }
 
+uint16_t to_bf16_rne(float f) { return rne_bits(f); }
+
 static inline float bf16_to_f32(uint16_t h) {
-  uint32_t u = (uint32_t)h << 16;
+  const uint32_t u = (uint32_t)h << 16;
   float f;
   std::memcpy(&f, &u, 4);
   return f;
@@ -109,13 +111,18 @@ static inline float bf16_to_f32(uint16_t h) {
 
 void emit_bf16(const float* src, uint16_t* dst, int64_t n, int threads) {
 #pragma omp parallel for schedule(static) num_threads(threads)
-  for (int64_t i = 0; i < n; ++i) dst[i] = to_bf16_rne(src[i]);
+  for (int64_t i = 0; i < n; ++i) dst[i] = rne_bits(src[i]);
 }
 
-void adam_pass(const AdamArgs& a, int threads) {
+// One streaming pass per element: gradient in (bf16 slab or fp32), gradient
+// out, m, v, w updated, bf16 copy of w out. The variants are compile-time
+// so the loop body has no control flow.
+template <bool kSlab, bool kGradOut, bool kStore>
+static void adam_loop(const AdamArgs& a, int threads) {
   const double bc1 = 1.0 - std::pow((double)a.beta1, (double)a.t);
   const double bc2 = 1.0 - std::pow((double)a.beta2, (double)a.t);
   const float lr = a.lr, b1 = a.beta1, b2 = a.beta2, eps = a.eps;
+  const float c1 = 1.f - b1, c2 = 1.f - b2;
   const float inv_bc1 = (float)(1.0 / bc1);
   const float inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
   float* __restrict__ w = a.w;
@@ -125,27 +132,50 @@ void adam_pass(const AdamArgs& a, int threads) {
   const float* __restrict__ gin = a.grad_in;
   const uint16_t* __restrict__ slab = a.slab;
   uint16_t* __restrict__ store = a.store;
-  const bool apply = a.apply;
   const int64_t n = a.n;
 #pragma omp parallel for schedule(static) num_threads(threads)
   for (int64_t i = 0; i < n; ++i) {
-    const float g = slab ? bf16_to_f32(slab[i]) : gin[i];
-    if (gout) gout[i] = g;
-    if (!apply) continue;
-    const float mi = b1 * m[i] + (1.f - b1) * g;
-    const float vi = b2 * v[i] + (1.f - b2) * g * g;
+    const float g = kSlab ? bf16_to_f32(slab[i]) : gin[i];
+    if (kGradOut) gout[i] = g;
+    const float mi = b1 * m[i] + c1 * g;
+    const float vi = b2 * v[i] + c2 * g * g;
     m[i] = mi;
     v[i] = vi;
     // m_hat / (sqrt(v_hat) + eps) with m_hat = m / bc1, v_hat = v / bc2
     const float wi = w[i] - lr * (mi * inv_bc1) / (std::sqrt(vi) * inv_sqrt_bc2 + eps);
     w[i] = wi;
-    if (store) store[i] = to_bf16_rne(wi);
+    if (kStore) store[i] = rne_bits(wi);
   }
 }
 
+void adam_pass(const AdamArgs& a, int threads) {
+  if (!a.apply) {
+    // gradient only (non-finite loss): no optimizer update
+    if (!a.grad_out) return;
+    float* __restrict__ gout = a.grad_out;
+    const uint16_t* __restrict__ slab = a.slab;
+    const float* __restrict__ gin = a.grad_in;
+    const int64_t n = a.n;
+#pragma omp parallel for schedule(static) num_threads(threads)
+    for (int64_t i = 0; i < n; ++i) gout[i] = slab ? bf16_to_f32(slab[i]) : gin[i];
+    return;
+  }
+  const bool sl = a.slab != nullptr, go = a.grad_out != nullptr, st = a.store != nullptr;
+  if (sl && go && st) adam_loop<true, true, true>(a, threads);
+  else if (sl && go) adam_loop<true, true, false>(a, threads);
+  else if (sl && st) adam_loop<true, false, true>(a, threads);
+  else if (sl) adam_loop<true, false, false>(a, threads);
+  else if (go && st) adam_loop<false, true, true>(a, threads);
+  else if (go) adam_loop<false, true, false>(a, threads);
+  else if (st) adam_loop<false, false, true>(a, threads);
+  else adam_loop<false, false, false>(a, threads);
+}
+
+// All cores but two: the main thread keeps enqueueing device work and the
+// CUDA driver runs its own threads while the worker's team runs Adam.
 int default_threads() {
-  int n = omp_get_num_procs();
-  return n > 0 ? n : 1;
+  const int n = omp_get_num_procs();
+  return n > 4 ? n - 2 : (n > 0 ? n : 1);
 }
 
 }  // namespace mt

@@ -82,6 +82,8 @@ typedef struct mt_stats {
   int64_t device_bytes;    /* device memory owned by the handle */
   int64_t pinned_bytes;    /* pinned host memory owned by the handle */
   int64_t kernel_launches; /* kernels launched by the handle, all steps */
+  double host_compute_s;   /* worker time inside accumulate + Adam + emit only */
+  double host_copy_wait_s; /* worker time waiting for slab copies and the loss */
 } mt_stats;
 
 /* Kernel classes of the per-kernel profile. */

@@ -341,3 +341,27 @@ def test_planted_mistake_is_caught(tiny, monkeypatch, name, fn):
         if not np.allclose(a, b, rtol=1e-9, atol=1e-12 * np.abs(b).max()):
             caught = True
     assert caught
+
+
+def test_bf16_emulation_rounding_matches_torch():
+    """The rounding used to derive tolerance floors is torch's bf16 rounding."""
+    from oracle.bf16_emulation import to_bf16
+    rng = np.random.default_rng(9)
+    x = np.concatenate([rng.standard_normal(200000) * 10.0 ** rng.integers(-38, 38, 200000),
+                        [np.inf, -np.inf, np.nan, 0.0, -0.0, 1.00390625, 1.01171875, 3.4e38]]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).float().numpy()
+    got = to_bf16(x)
+    nan = np.isnan(ref)
+    np.testing.assert_array_equal(got[~nan], ref[~nan].astype(np.float64))
+    assert np.isnan(got[nan]).all()
+
+
+def test_bf16_emulation_is_close_to_exact_step(tiny):
+    """With bf16 storage the tiny step moves by well under 1%: the emulation
+    is the exact step plus rounding, not a different computation."""
+    from oracle.bf16_emulation import step_grads_bf16_storage
+    lay, master, tokens, labels = _inputs(tiny)
+    loss, g = step_grads_bf16_storage(tiny, master, tokens, labels)
+    rl, rg = oracle.step_grads(tiny, master, tokens, labels)
+    assert abs(loss - rl) / rl < 1e-3
+    assert np.linalg.norm(g - rg) / np.linalg.norm(rg) < 1e-2

