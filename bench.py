@@ -399,7 +399,11 @@ def run_ours(args, shape, world, rank, local, pg):
         "roofline": {"bound": "tensor", "kernel": "gemm_abt (tcgen05)", "achieved": gemm_tf, "peak": peak_tf,
                      "unit": "TFLOP/s", "frac": (gemm_tf / peak_tf) if gemm_tf else None,
                      "peak_source": f"bf16_tflops_sustained, of {pk_kind}",
-                     "traffic": traffic["dram_bytes_per_launch"] if traffic else None},
+                     "traffic": (traffic["traffic_over_algorithmic"] * g["bytes"] / max(g["launches"], 1))
+                     if traffic else None,
+                     "traffic_note": "ncu DRAM bytes of one captured GEMM launch (profiles/gemm_traffic.json) as a "
+                                     "ratio to its algorithmic bytes, times the step's mean algorithmic bytes per "
+                                     "GEMM launch" if traffic else "no capture of the current GEMM source"},
         "kernels": prof_out,
         "host": {"adam_s_per_step": (st1["host_adam_s"] - st0["host_adam_s"]) / K,
                  "adam_compute_s_per_step": (st1["host_compute_s"] - st0["host_compute_s"]) / K,

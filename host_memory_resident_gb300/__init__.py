@@ -65,7 +65,7 @@ EXPORTS = [
     "mt_layout", "mt_unit_range", "mt_init", "mt_train_step", "mt_train_step_device",
     "mt_read_grads", "mt_get_step", "mt_set_step", "mt_sync_store", "mt_get_stats",
     "mt_get_stream", "mt_profile_enable", "mt_profile_read", "mt_destroy", "mt_last_error", "mt_debug_inject", "mt_debug_inject_global",
-    "mt_host_adam", "mt_host_to_bf16",
+    "mt_host_adam", "mt_host_adam_slab", "mt_host_to_bf16",
     "mt_k_gemm", "mt_k_transpose", "mt_k_rmsnorm_fwd", "mt_k_rmsnorm_bwd", "mt_k_rmsnorm_bwd_parts",
     "mt_k_rope", "mt_k_swiglu_fwd", "mt_k_swiglu_bwd", "mt_k_attn_fwd", "mt_k_attn_bwd",
     "mt_k_cross_entropy", "mt_k_sum", "mt_k_embedding_fwd", "mt_k_embedding_bwd",
@@ -106,6 +106,7 @@ def lib():
         "mt_debug_inject": ([P, I, I64], I),
         "mt_debug_inject_global": ([I, I64], I),
         "mt_host_adam": ([P, P, P, P, P, I64, I64, F, F, F, F, I], I),
+        "mt_host_adam_slab": ([P, P, P, P, P, P, I64, I64, F, F, F, F, I], I),
         "mt_host_to_bf16": ([P, P, I64], I),
         "mt_k_gemm": ([P, I64, P, I64, P, I64, I, P, I64, I, I, I, P], I),
         "mt_k_transpose": ([P, I64, P, I64, I, I, P], I),
@@ -291,6 +292,14 @@ def host_adam(w, m, v, g, t, lr, beta1, beta2, eps, store=None, threads=0):
     n = w.shape[0]
     sp = _ptr(store) if store is not None else None
     check(lib().mt_host_adam(_ptr(w), _ptr(m), _ptr(v), _ptr(g), sp, n, t, lr, beta1, beta2, eps, threads))
+
+
+def host_adam_slab(w, m, v, slab, t, lr, beta1, beta2, eps, grad_out=None, store=None, threads=0):
+    """The worker's pass: bf16 slab -> FP32 grad_out, Adam, bf16 store (numpy arrays)."""
+    n = w.shape[0]
+    check(lib().mt_host_adam_slab(_ptr(w), _ptr(m), _ptr(v), _ptr(slab),
+                                  _ptr(grad_out) if grad_out is not None else None,
+                                  _ptr(store) if store is not None else None, n, t, lr, beta1, beta2, eps, threads))
 
 
 def host_to_bf16(x: np.ndarray) -> np.ndarray:

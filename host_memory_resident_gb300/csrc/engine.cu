@@ -1002,6 +1002,28 @@ int mt_host_adam(float* w, float* m, float* v, const float* g, uint16_t* store, 
   return MT_OK;
 }
 
+int mt_host_adam_slab(float* w, float* m, float* v, const uint16_t* slab, float* grad_out, uint16_t* store,
+                      int64_t n, int64_t t, float lr, float beta1, float beta2, float eps, int threads) {
+  if (!w || !m || !v || !slab || n < 0 || t < 1) return MT_EINVAL;
+  AdamArgs a{};
+  a.w = w;
+  a.m = m;
+  a.v = v;
+  a.grad_out = grad_out;
+  a.grad_in = nullptr;
+  a.slab = slab;
+  a.store = store;
+  a.n = n;
+  a.t = t;
+  a.lr = lr;
+  a.beta1 = beta1;
+  a.beta2 = beta2;
+  a.eps = eps;
+  a.apply = true;
+  adam_pass(a, threads > 0 ? threads : default_threads());
+  return MT_OK;
+}
+
 int mt_host_to_bf16(const float* src, uint16_t* dst, int64_t n) {
   if (!src || !dst || n < 0) return MT_EINVAL;
   emit_bf16(src, dst, n, default_threads());

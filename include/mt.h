@@ -191,6 +191,16 @@ int mt_debug_inject_global(int what, int64_t value);
 int mt_host_adam(float* w, float* m, float* v, const float* g, uint16_t* store, int64_t n, int64_t t, float lr,
                  float beta1, float beta2, float eps, int threads);
 
+/*
+ * The worker's per-unit pass on caller arrays: gradient from a bf16 slab
+ * (`slab`, n elements), written as FP32 to `grad_out` (may be NULL), then
+ * Adam on w / m / v and the bf16 emit into `store` (may be NULL). The
+ * slab accumulation of the lqnn.cn article's section 三.3 fused with the
+ * host Adam of its section 二.
+ */
+int mt_host_adam_slab(float* w, float* m, float* v, const uint16_t* slab, float* grad_out, uint16_t* store,
+                      int64_t n, int64_t t, float lr, float beta1, float beta2, float eps, int threads);
+
 /* Round-to-nearest-even FP32 -> bf16 bits on the host; every NaN becomes 0x7fc0. */
 int mt_host_to_bf16(const float* src, uint16_t* dst, int64_t n);
 
