@@ -66,7 +66,7 @@ EXPORTS = [
     "mt_read_grads", "mt_get_step", "mt_set_step", "mt_sync_store", "mt_get_stats",
     "mt_get_stream", "mt_profile_enable", "mt_profile_read", "mt_destroy", "mt_last_error", "mt_debug_inject", "mt_debug_inject_global",
     "mt_host_adam", "mt_host_adam_slab", "mt_host_to_bf16",
-    "mt_k_gemm", "mt_k_transpose", "mt_k_rmsnorm_fwd", "mt_k_rmsnorm_bwd", "mt_k_rmsnorm_bwd_parts",
+    "mt_k_gemm", "mt_k_gemm_ex", "mt_k_transpose", "mt_k_rmsnorm_fwd", "mt_k_rmsnorm_bwd", "mt_k_rmsnorm_bwd_parts",
     "mt_k_rope", "mt_k_swiglu_fwd", "mt_k_swiglu_bwd", "mt_k_attn_fwd", "mt_k_attn_bwd",
     "mt_k_cross_entropy", "mt_k_sum", "mt_k_embedding_fwd", "mt_k_embedding_bwd",
     "mt_k_embedding_bwd_work", "mt_k_check_ids", "mt_k_device_error",
@@ -109,6 +109,7 @@ def lib():
         "mt_host_adam_slab": ([P, P, P, P, P, P, I64, I64, F, F, F, F, I], I),
         "mt_host_to_bf16": ([P, P, I64], I),
         "mt_k_gemm": ([P, I64, P, I64, P, I64, I, P, I64, I, I, I, P], I),
+        "mt_k_gemm_ex": ([P, I64, I, P, I64, I, P, I64, I, P, I64, I, I, I, P], I),
         "mt_k_transpose": ([P, I64, P, I64, I, I, P], I),
         "mt_k_rmsnorm_fwd": ([P, P, P, P, I, I, F, P], I),
         "mt_k_rmsnorm_bwd": ([P, P, P, P, P, P, P, P, P, I, I, P], I),
@@ -328,6 +329,17 @@ def k_gemm(A, B, Cout, R=None, stream=None):
     f32 = 1 if Cout.dtype == torch.float32 else 0
     check(lib().mt_k_gemm(_dp(A), A.stride(0), _dp(B), B.stride(0), _dp(Cout), Cout.stride(0), f32, _dp(R),
                           R.stride(0) if R is not None else 0, M, N, K, _st(stream)))
+
+
+def k_gemm_ex(A, a_mn, B, b_mn, Cout, R=None, stream=None):
+    """Cout = op(A) op(B)^T (+ R): A is [M,K] (a_mn False) or stored [K,M] (a_mn True);
+    B is [N,K] (b_mn False) or stored [K,N] (b_mn True)."""
+    import torch
+    M, N = Cout.shape
+    K = A.shape[0] if a_mn else A.shape[1]
+    f32 = 1 if Cout.dtype == torch.float32 else 0
+    check(lib().mt_k_gemm_ex(_dp(A), A.stride(0), 1 if a_mn else 0, _dp(B), B.stride(0), 1 if b_mn else 0, _dp(Cout),
+                             Cout.stride(0), f32, _dp(R), R.stride(0) if R is not None else 0, M, N, K, _st(stream)))
 
 
 def k_transpose(x, out, stream=None):

@@ -174,13 +174,31 @@ __device__ __forceinline__ uint64_t smem_desc_kmajor_sw128(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t m, uint32_t n) {
-  return (1u << 4)            // D format fp32
-         | (1u << 7)          // A format bf16
-         | (1u << 10)         // B format bf16
-         | ((n >> 3) << 17)   // N / 8
-         | ((m >> 4) << 24);  // M / 16
+// Shared-memory matrix descriptor for an MN-major operand tile written by
+// TMA with 128-byte swizzle as boxes of 64 MN x 64 K: each K row of a box is
+// 64 contiguous MN elements (128 B), 8 K rows make a 1024-B atom (stride
+// byte offset), and the next 64 MN elements sit in the next box, `mn_pitch`
+// bytes further (leading byte offset).
+__device__ __forceinline__ uint64_t smem_desc_mnmajor_sw128(uint32_t saddr, uint32_t mn_pitch) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);        // start address
+  d |= (uint64_t)((mn_pitch >> 4) & 0x3FFFu) << 16;  // leading byte offset: next 64 MN elements
+  d |= (uint64_t)(1024u >> 4) << 32;               // stride byte offset: next 8 K rows
+  d |= (uint64_t)1u << 46;                         // descriptor version for tcgen05
+  d |= (uint64_t)2u << 61;                         // layout: 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D; a_mn / b_mn set
+// the operand's transpose bit (MN-major in shared memory).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t m, uint32_t n, bool a_mn = false, bool b_mn = false) {
+  return (1u << 4)                  // D format fp32
+         | (1u << 7)                // A format bf16
+         | (1u << 10)               // B format bf16
+         | ((a_mn ? 1u : 0u) << 15) // A major
+         | ((b_mn ? 1u : 0u) << 16) // B major
+         | ((n >> 3) << 17)         // N / 8
+         | ((m >> 4) << 24);        // M / 16
 }
 
 // ------------------------------------------------------ legacy mma.sync

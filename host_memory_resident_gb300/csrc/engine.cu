@@ -143,7 +143,6 @@ struct mt_handle {
   float *rf = nullptr, *logits = nullptr, *loss_rows = nullptr, *loss_dev = nullptr;
   float *dx32 = nullptr, *dh32 = nullptr, *dn32 = nullptr, *delta = nullptr, *npart = nullptr;
   mt::bf16 *dxb = nullptr, *dhb = nullptr, *da = nullptr, *dgu = nullptr, *dob = nullptr, *dqkv = nullptr;
-  mt::bf16 *wT = nullptr, *tA = nullptr, *tB = nullptr;
 
   // streams and events
   cudaStream_t s_comp = nullptr, s_h2d = nullptr, s_d2h = nullptr;
@@ -277,7 +276,6 @@ struct Step {
   mt_handle* h;
   int B, s, M;
   int64_t t_next;
-  long long ldT;  // row pitch of transposed activations: M rounded up to 8
 
   cudaStream_t cs() const { return h->s_comp; }
 
@@ -375,11 +373,12 @@ struct Step {
     KP(MT_PROF_GEMM, 1, 2.0 * m * n * k, bytes,
        gemm_abt(A, lda, Bm, ldb, C, ldc, f32 ? 1 : 0, R, ldr, m, n, k, cs()));
   }
-  // out[c, r] = in[r, c]; `rows` is M for activations (pitch ldT), else the
-  // weight's row count (pitch = rows).
-  void transpose(const bf16* in, long long ldi, bf16* out, int rows, int cols) {
-    const long long ldo = rows == M ? ldT : rows;
-    KP(MT_PROF_TRANSPOSE, 1, 0.0, 4.0 * rows * cols, mt_k_transpose(in, ldi, out, ldo, rows, cols, cs()));
+  // C[M,N] = op(A) * op(B)^T (+R) with A and/or B read MN-major in place
+  void gemm_mn(const bf16* A, long long lda, bool a_mn, const bf16* Bm, long long ldb, bool b_mn, void* C,
+               long long ldc, bool f32, int m, int n, int k) {
+    const double bytes = 2.0 * ((double)m * k + (double)n * k) + (f32 ? 4.0 : 2.0) * m * n;
+    KP(MT_PROF_GEMM, 1, 2.0 * m * n * k, bytes,
+       gemm_ex(A, lda, a_mn ? 1 : 0, Bm, ldb, b_mn ? 1 : 0, C, ldc, f32 ? 1 : 0, nullptr, 0, m, n, k, cs()));
   }
   double attn_flops(bool bwd) const {
     // causal: half of the s x s score matrix; forward 2 products, backward 5
@@ -413,38 +412,29 @@ struct Step {
   void layer_bwd(const bf16* W, const Saved& S, bf16* g) {
     const LayerOffsets& o = h->lay.layer;
     const int d = h->d, f = h->f, hq = h->hq, qn = h->qkvN;
+    // Weight gradients dW = dY^T X read both token-major activations in place
+    // (MN-major operands, K = tokens); input gradients dX = dY W read the
+    // weight [out, in] in place as a [K, N] operand. Nothing is transposed.
     // down projection: dWdown = dy^T a ; da = dy Wdown
-    transpose(h->dxb, d, h->tA, M, d);
-    transpose(S.a, f, h->tB, M, f);
-    gemm(h->tA, ldT, h->tB, ldT, g + o.wdown, f, false, nullptr, 0, d, f, M);
-    transpose(W + o.wdown, f, h->wT, d, f);
-    gemm(h->dxb, d, h->wT, d, h->da, f, false, nullptr, 0, M, f, d);
+    gemm_mn(h->dxb, d, true, S.a, f, true, g + o.wdown, f, false, d, f, M);
+    gemm_mn(h->dxb, d, false, W + o.wdown, f, true, h->da, f, false, M, f, d);
     KP(MT_PROF_SWIGLU, 1, 0.0, 10.0 * M * f, mt_k_swiglu_bwd(h->da, S.gu, h->dgu, M, f, cs()));
     // gate/up projection
-    transpose(h->dgu, 2 * f, h->tA, M, 2 * f);
-    transpose(S.z, d, h->tB, M, d);
-    gemm(h->tA, ldT, h->tB, ldT, g + o.wgu, d, false, nullptr, 0, 2 * f, d, M);
-    transpose(W + o.wgu, d, h->wT, 2 * f, d);
-    gemm(h->dgu, 2 * f, h->wT, 2 * f, h->dn32, d, true, nullptr, 0, M, d, 2 * f);
+    gemm_mn(h->dgu, 2 * f, true, S.z, d, true, g + o.wgu, d, false, 2 * f, d, M);
+    gemm_mn(h->dgu, 2 * f, false, W + o.wgu, d, true, h->dn32, d, true, M, d, 2 * f);
     KP(MT_PROF_NORM, 2, 0.0, norm_bwd_bytes(true),
        mt_k_rmsnorm_bwd(h->dn32, S.h, W + o.mlp_norm, S.r2, h->dx32, h->dh32, h->dhb, h->npart, g + o.mlp_norm, M,
                         d, cs()));
     // output projection
-    transpose(h->dhb, d, h->tA, M, d);
-    transpose(S.o, hq, h->tB, M, hq);
-    gemm(h->tA, ldT, h->tB, ldT, g + o.wo, hq, false, nullptr, 0, d, hq, M);
-    transpose(W + o.wo, hq, h->wT, d, hq);
-    gemm(h->dhb, d, h->wT, d, h->dob, hq, false, nullptr, 0, M, hq, d);
+    gemm_mn(h->dhb, d, true, S.o, hq, true, g + o.wo, hq, false, d, hq, M);
+    gemm_mn(h->dhb, d, false, W + o.wo, hq, true, h->dob, hq, false, M, hq, d);
     // attention and RoPE
     KP(MT_PROF_ATTN_BWD, 3, attn_flops(true), 0.0,
        mt_k_attn_bwd(S.qkv, qn, S.o, hq, h->dob, hq, S.lse, h->delta, h->dqkv, qn, B, s, h->H, h->Hkv, h->hd, cs()));
     KP(MT_PROF_ROPE, 1, 0.0, rope_bytes(), mt_k_rope(h->dqkv, qn, B, s, h->H + h->Hkv, h->hd, h->cos_t, h->sin_t, 1, cs()));
     // qkv projection
-    transpose(h->dqkv, qn, h->tA, M, qn);
-    transpose(S.u, d, h->tB, M, d);
-    gemm(h->tA, ldT, h->tB, ldT, g + o.wqkv, d, false, nullptr, 0, qn, d, M);
-    transpose(W + o.wqkv, d, h->wT, qn, d);
-    gemm(h->dqkv, qn, h->wT, qn, h->dn32, d, true, nullptr, 0, M, d, qn);
+    gemm_mn(h->dqkv, qn, true, S.u, d, true, g + o.wqkv, d, false, qn, d, M);
+    gemm_mn(h->dqkv, qn, false, W + o.wqkv, d, true, h->dn32, d, true, M, d, qn);
     KP(MT_PROF_NORM, 2, 0.0, norm_bwd_bytes(true),
        mt_k_rmsnorm_bwd(h->dn32, S.x, W + o.attn_norm, S.r1, h->dh32, h->dx32, h->dxb, h->npart, g + o.attn_norm, M,
                         d, cs()));
@@ -467,12 +457,9 @@ struct Step {
     KP(MT_PROF_OTHER, 1, 0.0, 4.0 * M, mt_k_sum(h->loss_rows, M, h->loss_dev, cs()));
     CK(cudaMemcpyAsync(h->loss_pinned, h->loss_dev, sizeof(float), cudaMemcpyDeviceToHost, cs()));
     CK(cudaEventRecord(h->ev_loss, cs()));
-    // dHead = dz^T xh ; dxh = dz Head
-    transpose(h->dz, V, h->tA, M, V);
-    transpose(h->xh, d, h->tB, M, d);
-    gemm(h->tA, ldT, h->tB, ldT, g + h->lay.head, d, false, nullptr, 0, V, d, M);
-    transpose(head, d, h->wT, V, d);
-    gemm(h->dz, V, h->wT, V, h->dn32, d, true, nullptr, 0, M, d, V);
+    // dHead = dz^T xh ; dxh = dz Head (both read in place)
+    gemm_mn(h->dz, V, true, h->xh, d, true, g + h->lay.head, d, false, V, d, M);
+    gemm_mn(h->dz, V, false, head, d, true, h->dn32, d, true, M, d, V);
     KP(MT_PROF_NORM, 2, 0.0, norm_bwd_bytes(false),
        mt_k_rmsnorm_bwd(h->dn32, xL, wf, h->rf, nullptr, h->dx32, h->dxb, h->npart, g + h->lay.final_norm, M, d,
                         cs()));
@@ -634,12 +621,7 @@ void plan_device(mt_handle* h, Arena& A) {
   h->dqkv = take<bf16>(A, M * qn);
   h->delta = take<float>(A, M * H);
   h->npart = take<float>(A, (size_t)mt_k_rmsnorm_bwd_parts((int)M) * d);
-  const size_t wmax = std::max({qn * d, hq * d, 2 * f * d, d * f, V * d});
-  h->wT = take<bf16>(A, wmax);
-  const size_t cmax = std::max({d, qn, hq, 2 * f, V});
-  const size_t ldT = (M + 7) / 8 * 8;
-  h->tA = take<bf16>(A, cmax * ldT);
-  h->tB = take<bf16>(A, std::max({d, f, hq}) * ldT);
+
 }
 
 int fail(mt_handle* h, int code, const std::string& msg) {
@@ -822,7 +804,7 @@ static int run_step(mt_handle* h, const int32_t* tokens, const int32_t* labels, 
     return fail(h, MT_EINVAL, "bad tokens/labels or batch/seq outside the configured maxima");
   const int M = B * s;
   const auto t0 = Clock::now();
-  Step st{h, B, s, M, h->t + 1, ((long long)M + 7) / 8 * 8};
+  Step st{h, B, s, M, h->t + 1};
   try {
     CK(cudaSetDevice(h->cfg.device));
     if (!on_device) {

@@ -66,6 +66,11 @@ __device__ __forceinline__ void tile_coords(int t, int num_mb, int num_nb, int& 
   nb = r / gsz;
 }
 
+// A_MN / B_MN: the operand is stored MN-major in global memory (A as
+// [K][M], B as [K][N], MN contiguous) and staged as 64 x 64 boxes.
+constexpr uint32_t kBoxBytes = 64 * 64 * 2;  // one 64 MN x 64 K box
+
+template <bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_abt_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     GemmArgs args) {
@@ -116,8 +121,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sa = smem + stage * kStageBytes;
           uint8_t* sb = sa + kABytes;
           mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
-          tma_load_2d(sa, &tmap_a, kb * kBK, mb * kBM, &full_bar[stage]);
-          tma_load_2d(sb, &tmap_b, kb * kBK, nb * kBN, &full_bar[stage]);
+          if (A_MN) {
+#pragma unroll
+            for (int j = 0; j < kBM / 64; ++j)
+              tma_load_2d(sa + j * kBoxBytes, &tmap_a, mb * kBM + j * 64, kb * kBK, &full_bar[stage]);
+          } else {
+            tma_load_2d(sa, &tmap_a, kb * kBK, mb * kBM, &full_bar[stage]);
+          }
+          if (B_MN) {
+#pragma unroll
+            for (int j = 0; j < kBN / 64; ++j)
+              tma_load_2d(sb + j * kBoxBytes, &tmap_b, nb * kBN + j * 64, kb * kBK, &full_bar[stage]);
+          } else {
+            tma_load_2d(sb, &tmap_b, kb * kBK, nb * kBN, &full_bar[stage]);
+          }
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
       }
@@ -125,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN);
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
@@ -143,8 +160,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sb = sa + kABytes;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t ad = smem_desc_kmajor_sw128(sa + kk * 32);
-            const uint64_t bd = smem_desc_kmajor_sw128(sb + kk * 32);
+            // K step of 16: 32 bytes along a K-major row, or 16 K rows (2 KiB) down an MN-major box
+            const uint64_t ad = A_MN ? smem_desc_mnmajor_sw128(sa + kk * 2048, kBoxBytes)
+                                     : smem_desc_kmajor_sw128(sa + kk * 32);
+            const uint64_t bd = B_MN ? smem_desc_mnmajor_sw128(sb + kk * 2048, kBoxBytes)
+                                     : smem_desc_kmajor_sw128(sb + kk * 32);
             tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           tc_commit(&empty_bar[stage]);
@@ -255,17 +275,21 @@ int get_encode() {
     int dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaFuncSetAttribute(gemm_abt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    cudaFuncSetAttribute(gemm_abt_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    cudaFuncSetAttribute(gemm_abt_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    cudaFuncSetAttribute(gemm_abt_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    cudaFuncSetAttribute(gemm_abt_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   });
   return g_encode ? 0 : -1;
 }
 
 // Row-major bf16 matrix [rows, cols] with row pitch `ld` elements, boxes of
-// box_rows x 64 with 128-byte swizzle.
-int make_tmap(CUtensorMap* m, const void* ptr, long long rows, long long cols, long long ld, int box_rows) {
+// box_rows x box_cols with 128-byte swizzle (box_cols * 2 bytes = 128).
+int make_tmap(CUtensorMap* m, const void* ptr, long long rows, long long cols, long long ld, int box_rows,
+              int box_cols) {
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-  cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -275,8 +299,8 @@ int make_tmap(CUtensorMap* m, const void* ptr, long long rows, long long cols, l
 
 }  // namespace
 
-int gemm_abt(const void* A, long long lda, const void* B, long long ldb, void* C, long long ldc, int c_f32,
-             const void* R, long long ldr, int M, int N, int K, cudaStream_t stream) {
+int gemm_ex(const void* A, long long lda, int a_mn, const void* B, long long ldb, int b_mn, void* C, long long ldc,
+            int c_f32, const void* R, long long ldr, int M, int N, int K, cudaStream_t stream) {
   if (M < 0 || N < 0 || K < 0) return MT_EINVAL;
   if (M == 0 || N == 0) return MT_OK;
   if (K == 0) return MT_EINVAL;
@@ -284,11 +308,17 @@ int gemm_abt(const void* A, long long lda, const void* B, long long ldb, void* C
   // TMA: 16-byte aligned bases and row pitches; vector epilogue: 16-byte rows.
   auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
   if (!al16(A) || !al16(B) || !al16(C) || (R && !al16(R))) return MT_EINVAL;
-  if ((lda * 2) % 16 || (ldb * 2) % 16 || lda < K || ldb < K || ldc < N) return MT_EINVAL;
-  if (c_f32 ? (ldc % 4) : (ldc % 8)) return MT_EINVAL;
+  if ((lda * 2) % 16 || (ldb * 2) % 16) return MT_EINVAL;
+  if (a_mn ? lda < M : lda < K) return MT_EINVAL;
+  if (b_mn ? ldb < N : ldb < K) return MT_EINVAL;
+  if (ldc < N || (c_f32 ? (ldc % 4) : (ldc % 8))) return MT_EINVAL;
   if (R && (ldr % 8 || ldr < N)) return MT_EINVAL;
   CUtensorMap ta, tb;
-  if (make_tmap(&ta, A, M, K, lda, kBM) || make_tmap(&tb, B, N, K, ldb, kBN)) return MT_EINVAL;
+  // K-major: rows = M (or N), cols = K, box kBM (kBN) x 64; MN-major: rows = K,
+  // cols = M (or N), box 64 x 64.
+  const int ea = a_mn ? make_tmap(&ta, A, K, M, lda, kBK, 64) : make_tmap(&ta, A, M, K, lda, kBM, kBK);
+  const int eb = b_mn ? make_tmap(&tb, B, K, N, ldb, kBK, 64) : make_tmap(&tb, B, N, K, ldb, kBN, kBK);
+  if (ea || eb) return MT_EINVAL;
   GemmArgs args;
   args.M = M;
   args.N = N;
@@ -303,8 +333,16 @@ int gemm_abt(const void* A, long long lda, const void* B, long long ldb, void* C
   args.err = device_error_word();
   const int tiles = args.num_mb * args.num_nb;
   const int grid = tiles < g_num_sms ? tiles : g_num_sms;
-  gemm_abt_kernel<<<grid, kThreads, kSmemBytes, stream>>>(ta, tb, args);
+  if (!a_mn && !b_mn) gemm_abt_kernel<false, false><<<grid, kThreads, kSmemBytes, stream>>>(ta, tb, args);
+  else if (!a_mn) gemm_abt_kernel<false, true><<<grid, kThreads, kSmemBytes, stream>>>(ta, tb, args);
+  else if (!b_mn) gemm_abt_kernel<true, false><<<grid, kThreads, kSmemBytes, stream>>>(ta, tb, args);
+  else gemm_abt_kernel<true, true><<<grid, kThreads, kSmemBytes, stream>>>(ta, tb, args);
   return cudaGetLastError() == cudaSuccess ? MT_OK : MT_ECUDA;
+}
+
+int gemm_abt(const void* A, long long lda, const void* B, long long ldb, void* C, long long ldc, int c_f32,
+             const void* R, long long ldr, int M, int N, int K, cudaStream_t stream) {
+  return gemm_ex(A, lda, 0, B, ldb, 0, C, ldc, c_f32, R, ldr, M, N, K, stream);
 }
 
 }  // namespace mt

@@ -526,6 +526,11 @@ int mt_k_gemm(const void* A, int64_t lda, const void* B, int64_t ldb, void* C, i
   return gemm_abt(A, lda, B, ldb, C, ldc, c_f32, R, ldr, M, N, K, (cudaStream_t)stream);
 }
 
+int mt_k_gemm_ex(const void* A, int64_t lda, int a_mn_major, const void* B, int64_t ldb, int b_mn_major, void* C,
+                 int64_t ldc, int c_f32, const void* R, int64_t ldr, int M, int N, int K, void* stream) {
+  return gemm_ex(A, lda, a_mn_major, B, ldb, b_mn_major, C, ldc, c_f32, R, ldr, M, N, K, (cudaStream_t)stream);
+}
+
 int mt_k_transpose(const void* in, int64_t ld_in, void* out, int64_t ld_out, int rows, int cols, void* stream) {
   if (rows < 0 || cols < 0 || ld_in < cols || ld_out < rows) return MT_EINVAL;
   if (rows == 0 || cols == 0) return MT_OK;

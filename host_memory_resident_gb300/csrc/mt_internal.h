@@ -18,6 +18,10 @@ int* device_error_word();
 // Sets the calling thread's message returned by mt_last_error(NULL).
 void set_last_error_message(const std::string& msg);
 
+// C = op(A) * op(B) (+ R) with either operand K-major or MN-major; see mt_k_gemm_ex.
+int gemm_ex(const void* A, long long lda, int a_mn, const void* B, long long ldb, int b_mn, void* C, long long ldc,
+            int c_f32, const void* R, long long ldr, int M, int N, int K, cudaStream_t stream);
+
 // C = A * B^T (+ R); see mt_k_gemm.
 int gemm_abt(const void* A, long long lda, const void* B, long long ldb, void* C, long long ldc, int c_f32,
              const void* R, long long ldr, int M, int N, int K, cudaStream_t stream);

@@ -40,6 +40,18 @@ extern "C" {
 int mt_k_gemm(const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, int c_f32,
               const void* R, int64_t ldr, int M, int N, int K, void* stream);
 
+/*
+ * The same product with either operand read in place in the other layout:
+ * a_mn_major = 1 means A is stored [K, M] (M contiguous, row pitch lda >= M),
+ * i.e. the product uses A^T of that array; b_mn_major = 1 means B is stored
+ * [K, N] (row pitch ldb >= N). This covers a linear layer's backward without
+ * transposing anything: dX = dY W (B = W [out, in] as [K, N]) and
+ * dW = dY^T X (A = dY [tokens, out], B = X [tokens, in], both [K, *]).
+ * Pitches are multiples of 8 elements; other rules as mt_k_gemm.
+ */
+int mt_k_gemm_ex(const void* A, int64_t lda, int a_mn_major, const void* B, int64_t ldb, int b_mn_major, void* C,
+                 int64_t ldc, int c_f32, const void* R, int64_t ldr, int M, int N, int K, void* stream);
+
 /* out[c, r] = in[r, c] for a bf16 [rows, cols] matrix (ld_in >= cols, ld_out >= rows). */
 int mt_k_transpose(const void* in, int64_t ld_in, void* out, int64_t ld_out, int rows, int cols, void* stream);
 

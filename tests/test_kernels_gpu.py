@@ -300,3 +300,28 @@ def test_embedding_fwd_bwd(M, V, d, dup):
     assert_close(host(dE), ref, l2=5e-3, elem=1e-2, what="dE")
     untouched = np.setdiff1d(np.arange(V), tok_np)
     assert np.all(host(dE)[untouched] == 0)
+
+
+# ------------------------------------------------- GEMM with MN-major operands
+@pytest.mark.parametrize("a_mn,b_mn", [(False, True), (True, False), (True, True)])
+@pytest.mark.parametrize("M,N,K,out", [
+    (64, 192, 64, "f32"),          # tiny
+    (200, 296, 136, "bf16"),       # ragged M, N, K
+    (2048, 5632, 2048, "bf16"),    # 1.1B down-projection dgrad / wgrad shapes
+    (4096, 4096, 1000, "f32"),     # ragged K (tokens) for a weight gradient
+])
+def test_gemm_mn_major(M, N, K, out, a_mn, b_mn):
+    rng = np.random.default_rng(M + N + K + 7 * a_mn + 3 * b_mn)
+    Ah = rng.standard_normal((M, K))
+    Bh = rng.standard_normal((N, K)) / np.sqrt(K)
+    # store MN-major operands as [K, M] / [K, N] arrays (the product uses their transposes)
+    A, Ab = bf(Ah.T.copy() if a_mn else Ah)
+    B, Bb = bf(Bh.T.copy() if b_mn else Bh)
+    Aop = Ab.T if a_mn else Ab
+    Bop = Bb.T if b_mn else Bb
+    Cout = torch.empty((M, N), device=DEV, dtype=torch.float32 if out == "f32" else torch.bfloat16)
+    mt.k_gemm_ex(A, a_mn, B, b_mn, Cout)
+    torch.cuda.synchronize()
+    ref = Aop @ Bop.T
+    assert_close(host(Cout), ref, l2=5e-3 if out == "bf16" else 1e-4, elem=1e-2 if out == "bf16" else 1e-3,
+                 what=f"gemm_ex a_mn={a_mn} b_mn={b_mn} {M}x{N}x{K}")
