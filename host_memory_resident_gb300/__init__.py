@@ -37,7 +37,7 @@ class Config(C.Structure):
         ("ckpt_interval", C.c_int32), ("n_slabs", C.c_int32), ("streamed", C.c_int32),
         ("rms_eps", C.c_float), ("rope_theta", C.c_float), ("lr", C.c_float),
         ("beta1", C.c_float), ("beta2", C.c_float), ("adam_eps", C.c_float),
-        ("device", C.c_int32), ("host_threads", C.c_int32),
+        ("device", C.c_int32), ("host_threads", C.c_int32), ("overlap_adam", C.c_int32),
     ]
 
 
@@ -63,7 +63,7 @@ class KernelProfile(C.Structure):
 
 EXPORTS = [
     "mt_layout", "mt_unit_range", "mt_init", "mt_train_step", "mt_train_step_device",
-    "mt_read_grads", "mt_get_step", "mt_set_step", "mt_sync_store", "mt_get_stats",
+    "mt_read_grads", "mt_sync", "mt_get_step", "mt_set_step", "mt_sync_store", "mt_get_stats",
     "mt_get_stream", "mt_profile_enable", "mt_profile_read", "mt_destroy", "mt_last_error", "mt_debug_inject", "mt_debug_inject_global",
     "mt_host_adam", "mt_host_adam_slab", "mt_host_to_bf16",
     "mt_k_gemm", "mt_k_gemm_ex", "mt_k_transpose", "mt_k_rmsnorm_fwd", "mt_k_rmsnorm_bwd", "mt_k_rmsnorm_bwd_parts",
@@ -94,6 +94,7 @@ def lib():
         "mt_train_step": ([P, P, P, C.c_int32, C.c_int32, C.POINTER(F)], I),
         "mt_train_step_device": ([P, P, P, C.c_int32, C.c_int32, C.POINTER(F)], I),
         "mt_read_grads": ([P, P, I64], I),
+        "mt_sync": ([P], I),
         "mt_get_step": ([P, C.POINTER(I64)], I),
         "mt_set_step": ([P, I64], I),
         "mt_sync_store": ([P], I),
@@ -143,7 +144,7 @@ def check(code, handle=None):
 
 
 def make_config(shape, batch=None, seq=None, streamed=True, device=0, host_threads=0, ckpt_interval=None,
-                n_slabs=None) -> Config:
+                n_slabs=None, overlap_adam=False) -> Config:
     """mt_config from a synth.ModelShape-like object."""
     c = Config()
     c.n_layers = shape.n_layers
@@ -166,6 +167,7 @@ def make_config(shape, batch=None, seq=None, streamed=True, device=0, host_threa
     c.adam_eps = shape.adam_eps
     c.device = device
     c.host_threads = host_threads
+    c.overlap_adam = 1 if overlap_adam else 0
     return c
 
 
@@ -238,6 +240,10 @@ class Trainer:
         out = np.empty(self.n_total, np.float32)
         check(lib().mt_read_grads(self.h, _ptr(out), self.n_total), self.h)
         return out
+
+    def sync(self):
+        """Wait for the host worker (needed with overlap_adam before reading master/m/v)."""
+        check(lib().mt_sync(self.h), self.h)
 
     def stats(self) -> dict:
         s = Stats()

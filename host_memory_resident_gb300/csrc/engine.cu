@@ -103,6 +103,8 @@ struct Job {
   int unit;
   int slab;
   int64_t t;
+  int parity;     // step parity: selects the step's loss event / state
+  int64_t seq;    // step sequence number (monotonic per handle)
 };
 
 }  // namespace
@@ -148,7 +150,7 @@ struct mt_handle {
   cudaStream_t s_comp = nullptr, s_h2d = nullptr, s_d2h = nullptr;
   cudaEvent_t ev_ready[2] = {nullptr, nullptr}, ev_free[2] = {nullptr, nullptr};
   std::vector<cudaEvent_t> ev_slab_ready, ev_d2h_done;
-  cudaEvent_t ev_loss = nullptr, ev_resident = nullptr;
+  cudaEvent_t ev_loss[2] = {nullptr, nullptr}, ev_resident = nullptr;
   int slot_unit[2] = {-1, -1};
   int slot_last_use[2] = {0, 0};
   int use_clock = 0;
@@ -165,7 +167,10 @@ struct mt_handle {
   bool stop = false;
   int worker_error = 0;
   std::string worker_msg;
-  int loss_state = 0;  // 0 unknown, 1 finite, 2 non-finite
+  int loss_state[2] = {0, 0};  // per step parity: 0 unknown, 1 finite, 2 non-finite
+  std::vector<int> unit_pending;  // queued or running jobs per unit
+  int64_t step_seq = 0;        // sequence number of the step being enqueued
+  int64_t enqueued_seq = 0;    // last step whose units are all queued
   int64_t inject_sleep_ms = 0, inject_fail_at = 0, deadline_ms = 600000;
   int64_t worker_units_total = 0;
 
@@ -194,8 +199,16 @@ void worker_main(mt_handle* h) {
       std::unique_lock<std::mutex> lk(h->mu);
       h->cv.wait(lk, [&] { return h->stop || !h->jobs.empty(); });
       if (h->stop && h->jobs.empty()) return;
-      job = h->jobs.front();
-      h->jobs.pop_front();
+      // Units of a fully enqueued step go first, in the order the next
+      // forward needs them (lowest unit first); units of the step whose
+      // backward is still being enqueued go in arrival order, which frees
+      // staging slabs soonest.
+      auto it = h->jobs.end();
+      for (auto j = h->jobs.begin(); j != h->jobs.end(); ++j)
+        if (j->seq <= h->enqueued_seq && (it == h->jobs.end() || j->unit < it->unit)) it = j;
+      if (it == h->jobs.end()) it = h->jobs.begin();
+      job = *it;
+      h->jobs.erase(it);
       h->in_flight = 1;
     }
     int code = MT_OK;
@@ -228,9 +241,10 @@ void worker_main(mt_handle* h) {
       }
     };
     const auto tw = Clock::now();
-    if (code == MT_OK && wait_event(h->ev_d2h_done[job.slab]) && h->loss_state == 0 && wait_event(h->ev_loss)) {
-      const float total = *h->loss_pinned;
-      h->loss_state = std::isfinite(total) ? 1 : 2;
+    if (code == MT_OK && wait_event(h->ev_d2h_done[job.slab]) && h->loss_state[job.parity] == 0 &&
+        wait_event(h->ev_loss[job.parity])) {
+      const float total = h->loss_pinned[job.parity];
+      h->loss_state[job.parity] = std::isfinite(total) ? 1 : 2;
     }
     if (code == MT_OK) {
       AdamArgs a;
@@ -248,7 +262,7 @@ void worker_main(mt_handle* h) {
       a.beta1 = h->cfg.beta1;
       a.beta2 = h->cfg.beta2;
       a.eps = h->cfg.adam_eps;
-      a.apply = h->loss_state == 1;
+      a.apply = h->loss_state[job.parity] == 1;
       const auto tc = Clock::now();
       wait_s = std::chrono::duration<double>(tc - tw).count();
       adam_pass(a, h->threads);
@@ -261,6 +275,7 @@ void worker_main(mt_handle* h) {
       h->st.host_copy_wait_s += wait_s;
       h->staging_busy[job.slab] = 0;
       h->in_flight = 0;
+      --h->unit_pending[job.unit];
       ++h->units_done;
       if (code != MT_OK && h->worker_error == 0) {
         h->worker_error = code;
@@ -280,12 +295,29 @@ struct Step {
   cudaStream_t cs() const { return h->s_comp; }
 
   // Make unit `u`'s weights usable on the compute stream; returns its base.
+  int parity() const { return (int)(t_next & 1); }
+
+  // With overlap, a unit's bf16 store may still be rewritten by the previous
+  // step's Adam: wait (on the host, before its upload is enqueued) until the
+  // worker has no job left for it.
+  void wait_unit_updated(int u) {
+    if (!h->cfg.overlap_adam) return;
+    const auto t0 = Clock::now();
+    std::unique_lock<std::mutex> lk(h->mu);
+    const bool ok = h->cv.wait_for(lk, std::chrono::milliseconds(h->deadline_ms),
+                                   [&] { return h->unit_pending[u] == 0 || h->worker_error; });
+    h->st.host_wait_s += seconds_since(t0);
+    if (h->worker_error) throw StepError{h->worker_error, h->worker_msg};
+    if (!ok) throw StepError{MT_ETIMEOUT, "timed out waiting for a unit's host optimizer update"};
+  }
+
   bf16* acquire(int u) {
     if (!h->cfg.streamed) return h->resident + h->lay.unit_off[u];
     int slot = -1;
     for (int i = 0; i < 2; ++i)
       if (h->slot_unit[i] == u) slot = i;
     if (slot < 0) {
+      wait_unit_updated(u);
       slot = h->slot_last_use[0] <= h->slot_last_use[1] ? 0 : 1;
       const size_t bytes = sizeof(uint16_t) * h->lay.unit_len[u];
       CK(cudaStreamWaitEvent(h->s_h2d, h->ev_free[slot], 0));
@@ -334,7 +366,8 @@ struct Step {
     h->st.d2h_bytes += (int64_t)bytes;
     {
       std::lock_guard<std::mutex> lk(h->mu);
-      h->jobs.push_back(Job{u, k, t_next});
+      h->jobs.push_back(Job{u, k, t_next, parity(), h->step_seq});
+      ++h->unit_pending[u];
     }
     h->cv.notify_all();
   }
@@ -455,8 +488,8 @@ struct Step {
                             cs()));
     }
     KP(MT_PROF_OTHER, 1, 0.0, 4.0 * M, mt_k_sum(h->loss_rows, M, h->loss_dev, cs()));
-    CK(cudaMemcpyAsync(h->loss_pinned, h->loss_dev, sizeof(float), cudaMemcpyDeviceToHost, cs()));
-    CK(cudaEventRecord(h->ev_loss, cs()));
+    CK(cudaMemcpyAsync(h->loss_pinned + parity(), h->loss_dev, sizeof(float), cudaMemcpyDeviceToHost, cs()));
+    CK(cudaEventRecord(h->ev_loss[parity()], cs()));
     // dHead = dz^T xh ; dxh = dz Head (both read in place)
     gemm_mn(h->dz, V, true, h->xh, d, true, g + h->lay.head, d, false, V, d, M);
     gemm_mn(h->dz, V, false, head, d, true, h->dn32, d, true, M, d, V);
@@ -468,11 +501,18 @@ struct Step {
   void run() {
     mt_handle& hh = *h;
     const int L = hh.L, C = hh.cfg.ckpt_interval;
-    hh.loss_state = 0;
+    {
+      // the state of this parity belongs to the step before last, whose
+      // units were all updated before the previous forward could use them
+      std::lock_guard<std::mutex> lk(hh.mu);
+      hh.loss_state[parity()] = 0;
+      ++hh.step_seq;
+    }
     // The host Adam rewrote the bf16 store since the last step, so nothing
     // left in the two device buffers may be reused: forget their contents.
     hh.slot_unit[0] = hh.slot_unit[1] = -1;
     if (!hh.cfg.streamed) {
+      for (int u = 0; u < L + 2; ++u) wait_unit_updated(u);
       const size_t bytes = sizeof(uint16_t) * hh.n_total;
       CK(cudaMemcpyAsync(hh.resident, hh.store, bytes, cudaMemcpyHostToDevice, hh.s_h2d));
       CK(cudaEventRecord(hh.ev_resident, hh.s_h2d));
@@ -553,7 +593,8 @@ void destroy_resources(mt_handle* h) {
   for (auto e : h->ev_slab_ready) if (e) cudaEventDestroy(e);
   for (auto e : h->ev_d2h_done) if (e) cudaEventDestroy(e);
   for (auto e : h->prof_events) if (e) cudaEventDestroy(e);
-  if (h->ev_loss) cudaEventDestroy(h->ev_loss);
+  for (int i = 0; i < 2; ++i)
+    if (h->ev_loss[i]) cudaEventDestroy(h->ev_loss[i]);
   if (h->ev_resident) cudaEventDestroy(h->ev_resident);
   if (h->s_comp) cudaStreamDestroy(h->s_comp);
   if (h->s_h2d) cudaStreamDestroy(h->s_h2d);
@@ -762,7 +803,8 @@ int mt_init(const mt_config* cfg, float* master, float* adam_m, float* adam_v, f
       CK(cudaEventCreateWithFlags(&h->ev_slab_ready[k], cudaEventDisableTiming));
       CK(cudaEventCreateWithFlags(&h->ev_d2h_done[k], cudaEventDisableTiming));
     }
-    CK(cudaEventCreateWithFlags(&h->ev_loss, cudaEventDisableTiming));
+    CK(cudaEventCreateWithFlags(&h->ev_loss[0], cudaEventDisableTiming));
+    CK(cudaEventCreateWithFlags(&h->ev_loss[1], cudaEventDisableTiming));
     CK(cudaEventCreateWithFlags(&h->ev_resident, cudaEventDisableTiming));
     // RoPE tables in double precision on the host
     {
@@ -779,6 +821,7 @@ int mt_init(const mt_config* cfg, float* master, float* adam_m, float* adam_v, f
       CK(cudaMemcpy(h->sin_t, s.data(), sizeof(float) * s.size(), cudaMemcpyHostToDevice));
     }
     h->staging_busy.assign(cfg->n_slabs, 0);
+    h->unit_pending.assign(h->L + 2, 0);
     h->st.device_bytes = (int64_t)h->dbytes;
     h->worker = std::thread(worker_main, h);
   } catch (const StepError& e) {
@@ -826,13 +869,23 @@ static int run_step(mt_handle* h, const int32_t* tokens, const int32_t* labels, 
     }
     {
       std::lock_guard<std::mutex> lk(h->mu);
+      if (h->worker_error) {
+        // an overlapped Adam of the previous step failed: report it now
+        const int code = h->worker_error;
+        h->worker_error = 0;
+        return fail(h, code, h->worker_msg);
+      }
       h->units_done = 0;
-      h->worker_error = 0;
       h->worker_msg.clear();
     }
     st.run();
-    // wait for the worker to finish every unit of this step
     {
+      std::lock_guard<std::mutex> lk(h->mu);
+      h->enqueued_seq = h->step_seq;  // every unit of the step is queued
+    }
+    h->cv.notify_all();
+    if (!h->cfg.overlap_adam) {
+      // wait for the worker to finish every unit of this step
       std::unique_lock<std::mutex> lk(h->mu);
       const bool ok = h->cv.wait_for(lk, std::chrono::milliseconds(h->deadline_ms),
                                      [&] { return h->units_done == h->L + 2 || h->worker_error; });
@@ -863,21 +916,24 @@ static int run_step(mt_handle* h, const int32_t* tokens, const int32_t* labels, 
     cudaStreamSynchronize(h->s_d2h);
     std::unique_lock<std::mutex> lk(h->mu);
     h->jobs.clear();
+    h->enqueued_seq = h->step_seq;
     const bool idle = h->cv.wait_for(lk, std::chrono::milliseconds(std::min<int64_t>(h->deadline_ms, 60000)),
                                      [&] { return h->in_flight == 0; });
     if (e.code == MT_ETIMEOUT || e.code == MT_EDEVICE || e.code == MT_ECUDA || !idle) h->broken = 1;
+    if (idle) std::fill(h->unit_pending.begin(), h->unit_pending.end(), 0);
+    h->worker_error = 0;  // reported by this call
     for (auto& b : h->staging_busy) b = 0;
     h->prof_recs.clear();
     h->err = e.msg;
     g_thread_error = e.msg;
     return e.code;
   }
-  const float total = *h->loss_pinned;
+  const float total = h->loss_pinned[st.parity()];
   const float loss = total / (float)M;
   if (loss_out) *loss_out = loss;
   h->st.steps += 1;
   h->st.last_step_s = seconds_since(t0);
-  if (h->loss_state != 1) return fail(h, MT_ENONFINITE, "non-finite loss: no Adam update was applied");
+  if (!std::isfinite(total)) return fail(h, MT_ENONFINITE, "non-finite loss: no Adam update was applied");
   h->t += 1;
   return MT_OK;
 }
@@ -892,8 +948,29 @@ int mt_train_step_device(mt_handle* h, const int32_t* d_tokens, const int32_t* d
   return run_step(h, d_tokens, d_labels, batch, seq, true, loss_out);
 }
 
+int mt_sync(mt_handle* h) {
+  if (!h) return fail(nullptr, MT_EINVAL, "null handle");
+  std::unique_lock<std::mutex> lk(h->mu);
+  const bool ok = h->cv.wait_for(lk, std::chrono::milliseconds(h->deadline_ms),
+                                 [&] { return (h->jobs.empty() && h->in_flight == 0) || h->worker_error; });
+  if (h->worker_error) {
+    const int code = h->worker_error;
+    h->worker_error = 0;
+    h->err = h->worker_msg;
+    g_thread_error = h->worker_msg;
+    return code;
+  }
+  if (!ok) {
+    h->err = "timed out waiting for the host optimizer";
+    g_thread_error = h->err;
+    return MT_ETIMEOUT;
+  }
+  return MT_OK;
+}
+
 int mt_read_grads(mt_handle* h, float* dst, int64_t n) {
   if (!h || !dst || n < 0 || n > h->n_total) return fail(h, MT_EINVAL, "bad arguments to mt_read_grads");
+  if (const int r = mt_sync(h)) return r;
   if (dst != h->grad) std::memcpy(dst, h->grad, sizeof(float) * n);
   return MT_OK;
 }
@@ -906,12 +983,14 @@ int mt_get_step(mt_handle* h, int64_t* t) {
 
 int mt_set_step(mt_handle* h, int64_t t) {
   if (!h || t < 0) return MT_EINVAL;
+  if (const int r = mt_sync(h)) return r;
   h->t = t;
   return MT_OK;
 }
 
 int mt_sync_store(mt_handle* h) {
   if (!h) return MT_EINVAL;
+  if (const int r = mt_sync(h)) return r;
   emit_bf16(h->master, h->store, h->n_total, h->threads);
   return MT_OK;
 }

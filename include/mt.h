@@ -59,7 +59,11 @@ typedef struct mt_config {
   float rope_theta;      /* RoPE base, e.g. 10000 */
   float lr, beta1, beta2, adam_eps; /* Adam, no weight decay */
   int32_t device;        /* CUDA device ordinal */
-  int32_t host_threads;  /* threads for host accumulate + Adam; 0 = all cores */
+  int32_t host_threads;  /* threads for host accumulate + Adam; 0 = all cores but two */
+  int32_t overlap_adam;  /* 1: mt_train_step returns once the device work and the loss are done while
+                            the host worker finishes Adam on the last units; the next step uploads each
+                            unit only after its Adam has finished. Results are identical to 0. Call
+                            mt_sync before reading master / m / v yourself. */
 } mt_config;
 
 /* One tensor of the flat layout. kind 0 = matrix, 1 = norm weight. */
@@ -154,6 +158,11 @@ int mt_train_step_device(mt_handle* h, const int32_t* d_tokens, const int32_t* d
 
 /* Copies the FP32 gradient of the last step (n elements, n <= n_total). */
 int mt_read_grads(mt_handle* h, float* dst, int64_t n);
+
+/* Waits until the host worker has finished every queued unit (Adam of the
+ * last step included); returns a worker error if one occurred. Needed only
+ * with overlap_adam = 1, before reading master / m / v / grad directly. */
+int mt_sync(mt_handle* h);
 
 int mt_get_step(mt_handle* h, int64_t* t);
 int mt_set_step(mt_handle* h, int64_t t);     /* for resume from a checkpoint */

@@ -317,3 +317,43 @@ def test_worker_failure_reported_and_recoverable(tiny):
         w[:] = master
         loss = tr.step(tokens, labels)
         assert math.isfinite(loss)
+
+
+# ------------------------------------------------------ overlapped optimizer
+@pytest.mark.parametrize("variant", ["tiny4", "gqa"])
+def test_overlap_adam_matches_synchronous(tiny, variant):
+    """overlap_adam = 1 lets the host Adam of one step run under the next
+    step's device work; every loss, gradient and optimizer state must be
+    bit-identical to the synchronous mode after three steps."""
+    shape = tiny.with_(n_layers=4, ckpt_interval=2) if variant == "tiny4" else \
+        tiny.with_(n_heads=4, n_kv_heads=2, n_layers=3, ckpt_interval=1)
+    lay, master, _, _ = _setup(shape)
+    batches = [synth.make_tokens(shape.vocab, shape.batch, shape.seq, seed=1, step=i) for i in range(3)]
+    out = []
+    for overlap in (False, True):
+        w = master.copy()
+        with mt.Trainer(mt.make_config(shape, overlap_adam=overlap), w) as tr:
+            losses = [tr.step(tk, lb) for tk, lb in batches]
+            tr.sync()
+            out.append((losses, w.copy(), tr.m.copy(), tr.v.copy(), tr.read_grads(), tr.get_step()))
+    (l0, w0, m0, v0, g0, t0), (l1, w1, m1, v1, g1, t1) = out
+    assert l0 == l1 and t0 == t1 == 3
+    for a, b in ((w0, w1), (m0, m1), (v0, v1), (g0, g1)):
+        assert np.array_equal(a, b)
+
+
+def test_overlap_worker_failure_is_reported(tiny):
+    lay, master, tokens, labels = _setup(tiny)
+    w = master.copy()
+    with mt.Trainer(mt.make_config(tiny, overlap_adam=True), w) as tr:
+        tr.step(tokens, labels)
+        tr.inject(2, 1)    # the next unit the worker takes fails
+        code, _ = tr.step_code(tokens, labels)
+        if code == mt.MT_OK:
+            # the failure hit a unit that was still queued when the step returned
+            with pytest.raises(mt.MtError) as e:
+                tr.sync()
+            assert e.value.code == mt.MT_EWORKER
+        else:
+            assert code == mt.MT_EWORKER
+        assert "injected" in tr.last_error()
