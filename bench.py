@@ -322,6 +322,32 @@ def run_gemm_kernel(args):
     return 0 if err < 2e-2 else 1
 
 
+def run_attn_kernel(args):
+    """One attention forward shape through mt_k_attn_fwd (profiler captures)."""
+    import torch
+    import host_memory_resident_gb300 as mt
+    B, s, H, Hkv, hd = (int(x) for x in args.shape.split(","))
+    torch.manual_seed(0)
+    qkv = torch.randn(B * s, (H + 2 * Hkv) * hd, device="cuda").to(torch.bfloat16)
+    o = torch.empty(B * s, H * hd, device="cuda", dtype=torch.bfloat16)
+    lse = torch.empty(B, H, s, device="cuda")
+    fn = mt.k_attn_fwd_mma if args.legacy else mt.k_attn_fwd
+    for _ in range(2):
+        fn(qkv, o, lse, B, s, H, Hkv, hd)
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record()
+    for _ in range(args.iters):
+        fn(qkv, o, lse, B, s, H, Hkv, hd)
+    s1.record()
+    torch.cuda.synchronize()
+    ms = s0.elapsed_time(s1) / args.iters
+    flops = 2.0 * B * H * s * s * hd  # causal: two products over half the score matrix
+    print(json.dumps({"kernel": "attn_fwd" + ("_mma" if args.legacy else ""), "shape": [B, s, H, Hkv, hd], "ms": ms,
+                      "tflops": flops / ms / 1e9}), flush=True)
+    return 0
+
+
 def run_ours(args, shape, world, rank, local, pg):
     import torch
     import host_memory_resident_gb300 as mt
@@ -463,7 +489,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="1.1b", choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--kernel", default=None, choices=[None, "gemm"])
+    ap.add_argument("--kernel", default=None, choices=[None, "gemm", "attn"])
+    ap.add_argument("--legacy", action="store_true", help="with --kernel attn: the mma.sync forward")
     ap.add_argument("--shape", default="8192,8192,2048")
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -473,6 +500,8 @@ def main():
     args = ap.parse_args()
     if args.kernel == "gemm":
         return run_gemm_kernel(args)
+    if args.kernel == "attn":
+        return run_attn_kernel(args)
     shape = synth.workload(args.config)
     world, rank, local, pg = dist_setup()
     if args.impl == "reference":

@@ -598,6 +598,17 @@ using namespace mt;
 
 extern "C" int mt_k_attn_fwd(const void* qkv, int64_t ldqkv, void* o, int64_t ldo, float* lse, int B, int s, int H,
                              int Hkv, int hd, void* stream) {
+  if ((hd == 64 || hd == 128) && attn_args_ok(qkv, ldqkv, B, s, H, Hkv, hd) &&
+      ldqkv >= (int64_t)(H + 2 * Hkv) * hd && ldo >= (int64_t)H * hd && ldo % 8 == 0 &&
+      (reinterpret_cast<uintptr_t>(o) & 15) == 0) {
+    if (B == 0 || s == 0) return MT_OK;
+    return attn_fwd_tc(qkv, ldqkv, o, ldo, lse, B, s, H, Hkv, hd, (cudaStream_t)stream);
+  }
+  return mt_k_attn_fwd_mma(qkv, ldqkv, o, ldo, lse, B, s, H, Hkv, hd, stream);
+}
+
+extern "C" int mt_k_attn_fwd_mma(const void* qkv, int64_t ldqkv, void* o, int64_t ldo, float* lse, int B, int s,
+                                 int H, int Hkv, int hd, void* stream) {
   if (!attn_args_ok(qkv, ldqkv, B, s, H, Hkv, hd) || ldqkv < (int64_t)(H + 2 * Hkv) * hd || ldo < (int64_t)H * hd ||
       ldo % 2 || (reinterpret_cast<uintptr_t>(o) & 3))
     return MT_EINVAL;

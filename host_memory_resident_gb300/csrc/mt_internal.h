@@ -22,6 +22,10 @@ void set_last_error_message(const std::string& msg);
 int gemm_ex(const void* A, long long lda, int a_mn, const void* B, long long ldb, int b_mn, void* C, long long ldc,
             int c_f32, const void* R, long long ldr, int M, int N, int K, cudaStream_t stream);
 
+// Causal GQA attention forward on tcgen05 (hd 64 or 128); see mt_k_attn_fwd.
+int attn_fwd_tc(const void* qkv, long long ld, void* o, long long ldo, float* lse, int B, int s, int H, int Hkv,
+                int hd, cudaStream_t stream);
+
 // C = A * B^T (+ R); see mt_k_gemm.
 int gemm_abt(const void* A, long long lda, const void* B, long long ldb, void* C, long long ldc, int c_f32,
              const void* R, long long ldr, int M, int N, int K, cudaStream_t stream);

@@ -92,10 +92,19 @@ int mt_k_swiglu_bwd(const void* da, const void* gu, void* dgu, int M, int f, voi
  * Causal grouped-query attention forward (flash style, KV streamed in tiles).
  * qkv bf16 [B*s, ldqkv]: q heads at columns [0, H*hd), k heads at
  * [H*hd, (H+Hkv)*hd), v heads after; o bf16 [B*s, ldo] (H*hd columns);
- * lse fp32 [B, H, s] natural-log softmax denominators. hd in {16, 64, 128}.
+ * lse fp32 [B, H, s] natural-log softmax denominators. hd in {16, 64, 128};
+ * hd 64 / 128 run on tcgen05 (o 16-byte aligned, ldo multiple of 8).
  */
 int mt_k_attn_fwd(const void* qkv, int64_t ldqkv, void* o, int64_t ldo, float* lse, int B, int s, int H, int Hkv,
                   int hd, void* stream);
+
+/*
+ * The same forward on the legacy warp-level mma.sync tensor-core path
+ * (any hd in {16, 64, 128}); mt_k_attn_fwd uses it for hd = 16 and runs
+ * hd 64 / 128 on tcgen05 with TMEM accumulators. Kept for comparison.
+ */
+int mt_k_attn_fwd_mma(const void* qkv, int64_t ldqkv, void* o, int64_t ldo, float* lse, int B, int s, int H,
+                      int Hkv, int hd, void* stream);
 
 /*
  * Attention backward, deterministic (no float atomics). Inputs as the

@@ -325,3 +325,23 @@ def test_gemm_mn_major(M, N, K, out, a_mn, b_mn):
     ref = Aop @ Bop.T
     assert_close(host(Cout), ref, l2=5e-3 if out == "bf16" else 1e-4, elem=1e-2 if out == "bf16" else 1e-3,
                  what=f"gemm_ex a_mn={a_mn} b_mn={b_mn} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("B,s,H,Hkv,hd", [(3, 200, 4, 2, 128), (2, 129, 8, 2, 64), (1, 2048, 4, 4, 64),
+                                          (2, 640, 2, 1, 128)])
+def test_attention_fwd_tcgen05_matches_mma_and_oracle(B, s, H, Hkv, hd):
+    """The tcgen05/TMEM forward against the oracle and against the mma.sync
+    kernel (several sequences per batch with ragged length: rows past each
+    sequence's end must read as zeros)."""
+    qkv, q, k, v = _attn_inputs(B, s, H, Hkv, hd, 11 * s + hd)
+    o = torch.empty((B * s, H * hd), device=DEV, dtype=torch.bfloat16)
+    lse = torch.empty((B, H, s), device=DEV)
+    o2 = torch.empty_like(o)
+    lse2 = torch.empty_like(lse)
+    mt.k_attn_fwd(qkv, o, lse, B, s, H, Hkv, hd)
+    mt.k_attn_fwd_mma(qkv, o2, lse2, B, s, H, Hkv, hd)
+    torch.cuda.synchronize()
+    orf, lr = ops.attention_fwd(q, k, v)
+    assert_close(host(o), orf.reshape(B * s, H * hd), l2=1e-2, elem=2e-2, what="tc o")
+    np.testing.assert_allclose(host(lse), lr, rtol=0, atol=2e-2)
+    assert_close(host(o), host(o2), l2=1e-2, elem=2e-2, what="tc vs mma")
