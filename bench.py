@@ -331,7 +331,18 @@ def run_attn_kernel(args):
     qkv = torch.randn(B * s, (H + 2 * Hkv) * hd, device="cuda").to(torch.bfloat16)
     o = torch.empty(B * s, H * hd, device="cuda", dtype=torch.bfloat16)
     lse = torch.empty(B, H, s, device="cuda")
-    fn = mt.k_attn_fwd_mma if args.legacy else mt.k_attn_fwd
+    fwd = mt.k_attn_fwd_mma if args.legacy else mt.k_attn_fwd
+    if args.backward:
+        fwd(qkv, o, lse, B, s, H, Hkv, hd)
+        dout = torch.randn(B * s, H * hd, device="cuda").to(torch.bfloat16)
+        delta = torch.empty(B, H, s, device="cuda")
+        dqkv = torch.empty_like(qkv)
+        bwd = mt.k_attn_bwd_mma if args.legacy else mt.k_attn_bwd
+
+        def fn(*_):
+            bwd(qkv, o, dout, lse, delta, dqkv, B, s, H, Hkv, hd)
+    else:
+        fn = fwd
     for _ in range(2):
         fn(qkv, o, lse, B, s, H, Hkv, hd)
     torch.cuda.synchronize()
@@ -342,8 +353,10 @@ def run_attn_kernel(args):
     s1.record()
     torch.cuda.synchronize()
     ms = s0.elapsed_time(s1) / args.iters
-    flops = 2.0 * B * H * s * s * hd  # causal: two products over half the score matrix
-    print(json.dumps({"kernel": "attn_fwd" + ("_mma" if args.legacy else ""), "shape": [B, s, H, Hkv, hd], "ms": ms,
+    # causal: two (forward) or five (backward) products over half the score matrix
+    flops = (5.0 if args.backward else 2.0) * B * H * s * s * hd
+    name = ("attn_bwd" if args.backward else "attn_fwd") + ("_mma" if args.legacy else "")
+    print(json.dumps({"kernel": name, "shape": [B, s, H, Hkv, hd], "ms": ms,
                       "tflops": flops / ms / 1e9}), flush=True)
     return 0
 
@@ -490,7 +503,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="1.1b", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--kernel", default=None, choices=[None, "gemm", "attn"])
-    ap.add_argument("--legacy", action="store_true", help="with --kernel attn: the mma.sync forward")
+    ap.add_argument("--legacy", action="store_true", help="with --kernel attn: the mma.sync kernels")
+    ap.add_argument("--backward", action="store_true", help="with --kernel attn: time the backward")
     ap.add_argument("--shape", default="8192,8192,2048")
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")

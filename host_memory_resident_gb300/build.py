@@ -18,7 +18,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmt.so")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
-CU_SOURCES = ["gemm_tc.cu", "attention.cu", "attention_tc.cu", "kernels_misc.cu", "engine.cu"]
+CU_SOURCES = ["gemm_tc.cu", "attention.cu", "attention_tc.cu", "attention_bwd_tc.cu", "kernels_misc.cu", "engine.cu"]
 CXX_SOURCES = ["host_math.cpp"]
 
 

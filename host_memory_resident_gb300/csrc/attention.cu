@@ -625,6 +625,28 @@ extern "C" int mt_k_attn_fwd_mma(const void* qkv, int64_t ldqkv, void* o, int64_
 extern "C" int mt_k_attn_bwd(const void* qkv, int64_t ldqkv, const void* o, int64_t ldo, const void* dout,
                              int64_t lddo, const float* lse, float* delta, void* dqkv, int64_t lddqkv, int B, int s,
                              int H, int Hkv, int hd, void* stream) {
+  if ((hd == 64 || hd == 128) && attn_args_ok(qkv, ldqkv, B, s, H, Hkv, hd) &&
+      attn_args_ok(dout, lddo, B, s, H, Hkv, hd) && attn_args_ok(dqkv, lddqkv, B, s, H, Hkv, hd) &&
+      ldqkv >= (int64_t)(H + 2 * Hkv) * hd && lddqkv >= (int64_t)(H + 2 * Hkv) * hd && ldo % 2 == 0 &&
+      lddo >= (int64_t)H * hd) {
+    if (B == 0 || s == 0) return MT_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    const long long warps = (long long)B * s * H;
+    if (hd == 64)
+      attn_delta_kernel<64><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>((const bf16*)o, ldo, (const bf16*)dout,
+                                                                        lddo, delta, B, s, H);
+    else
+      attn_delta_kernel<128><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>((const bf16*)o, ldo, (const bf16*)dout,
+                                                                         lddo, delta, B, s, H);
+    if (cudaGetLastError() != cudaSuccess) return MT_ECUDA;
+    return attn_bwd_tc(qkv, ldqkv, dout, lddo, lse, delta, dqkv, lddqkv, B, s, H, Hkv, hd, st);
+  }
+  return mt_k_attn_bwd_mma(qkv, ldqkv, o, ldo, dout, lddo, lse, delta, dqkv, lddqkv, B, s, H, Hkv, hd, stream);
+}
+
+extern "C" int mt_k_attn_bwd_mma(const void* qkv, int64_t ldqkv, const void* o, int64_t ldo, const void* dout,
+                                 int64_t lddo, const float* lse, float* delta, void* dqkv, int64_t lddqkv, int B,
+                                 int s, int H, int Hkv, int hd, void* stream) {
   if (!attn_args_ok(qkv, ldqkv, B, s, H, Hkv, hd) || !attn_args_ok(dout, lddo, B, s, H, Hkv, hd) ||
       !attn_args_ok(dqkv, lddqkv, B, s, H, Hkv, hd) || ldqkv < (int64_t)(H + 2 * Hkv) * hd ||
       lddqkv < (int64_t)(H + 2 * Hkv) * hd || ldo % 2 || lddo < (int64_t)H * hd)

@@ -1,0 +1,488 @@
+// Causal grouped-query attention backward on the 5th-generation tensor cores.
+// Deterministic: every gradient element is accumulated by one CTA in a fixed
+// order (no atomics). Two kernels, both warp-specialised like the forward
+// (warp 0 TMA, warp 1 TMEM allocation + tcgen05.mma, warps 2-9 element-wise
+// work with two threads per TMEM lane):
+//
+//  dK/dV: one CTA per (128-key tile, KV head, batch). For every query head
+//         of the group and every query tile at or after the diagonal:
+//           S^T  = K Q^T,  dP^T = V dO^T                       (TMEM)
+//           P^T  = exp(S^T * scale - lse[q]),  dS^T = P^T (dP^T - delta[q])
+//                                                              (bf16, smem)
+//           dV  += P^T dO,  dK += dS^T Q   with dO and Q read MN-major
+//         then dK *= scale.
+//  dQ:    one CTA per (128-query tile, head, batch). For every key tile up to
+//         the diagonal:  S = Q K^T, dP = dO V^T (TMEM); dS (bf16, smem);
+//           dQ += dS K with K read MN-major; then dQ *= scale.
+// delta = rowsum(dO * O) comes from the pre-pass in attention.cu. This is the
+// backward of the stateless layer template's attention (travelaiplan blog,
+// 核心功能 point 3: a hand-written backward per layer instead of autograd).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "common.cuh"
+#include "mt_internal.h"
+
+namespace mt {
+namespace {
+
+constexpr int kT = 128;               // rows of a tile (keys or queries)
+constexpr int kThr = 320;
+constexpr uint32_t kBox = 128 * 128;  // 64 columns x 128 rows of bf16
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ uint8_t* align1024b(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Store one 64-column half-row of a 128 x 128 bf16 K-major operand tile
+// (128-byte swizzle); `pk` holds 32 packed bf16 pairs.
+__device__ __forceinline__ void store_half_row(uint8_t* tile, int half, int row, const uint32_t (&pk)[32]) {
+  uint8_t* base = tile + half * kBox + row * 128;
+  const uint32_t rsw = (uint32_t)(row & 7);
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<uint4*>(base + (((uint32_t)c ^ rsw) * 16)) =
+        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+}
+
+// Write `ncols` fp32 TMEM columns of this thread's lane as bf16 (times scale).
+__device__ __forceinline__ void tmem_row_to_bf16(uint32_t taddr, int ncols, float scale, bf16* dst, bool store) {
+#pragma unroll 1
+  for (int c = 0; c < ncols / 32; ++c) {
+    uint32_t v[32];
+    tmem_ld_32x32b_x32(taddr + c * 32, v);
+    tmem_ld_wait();
+    if (store) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint4 u;
+        u.x = pack_bf16x2(__uint_as_float(v[8 * k + 0]) * scale, __uint_as_float(v[8 * k + 1]) * scale);
+        u.y = pack_bf16x2(__uint_as_float(v[8 * k + 2]) * scale, __uint_as_float(v[8 * k + 3]) * scale);
+        u.z = pack_bf16x2(__uint_as_float(v[8 * k + 4]) * scale, __uint_as_float(v[8 * k + 5]) * scale);
+        u.w = pack_bf16x2(__uint_as_float(v[8 * k + 6]) * scale, __uint_as_float(v[8 * k + 7]) * scale);
+        *reinterpret_cast<uint4*>(dst + c * 32 + 8 * k) = u;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ dK / dV
+template <int HD>
+struct KvTc {
+  static constexpr int kBoxes = HD / 64;
+  static constexpr uint32_t kTile = kBoxes * kBox;
+  static constexpr int kStages = HD == 128 ? 1 : 2;     // Q + dO stages
+  static constexpr uint32_t kKOff = 0;
+  static constexpr uint32_t kVOff = kTile;
+  static constexpr uint32_t kQOff = 2 * kTile;           // [stage] Q then dO
+  static constexpr uint32_t kPOff = kQOff + kStages * 2 * kTile;  // P^T tile
+  static constexpr uint32_t kDSOff = kPOff + 2 * kBox;            // dS^T tile
+  static constexpr uint32_t kBarOff = kDSOff + 2 * kBox;
+  static constexpr uint32_t kVecOff = kBarOff + 256;     // [2][2][128] floats: lse*log2e, delta
+  static constexpr size_t kSmem = 1024 + kVecOff + 2 * 2 * 128 * 4;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kThr, 1)
+    attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tqkv, const __grid_constant__ CUtensorMap tdo,
+                            const float* __restrict__ lse, const float* __restrict__ delta, bf16* __restrict__ dqkv,
+                            long long lddq, int s, int H, int Hkv, int* err) {
+  using C = KvTc<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024b(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
+  uint64_t* kv_full = bars;          // K and V tiles
+  uint64_t* ld_full = bars + 1;      // [2] Q + dO stage
+  uint64_t* ld_empty = bars + 3;     // [2]
+  uint64_t* s_full = bars + 5;       // S^T and dP^T in TMEM
+  uint64_t* p_full = bars + 6;       // P^T, dS^T written (TMEM read)
+  uint64_t* p_empty = bars + 7;      // dV, dK MMAs done with them
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 8);
+  float* vec = reinterpret_cast<float*>(sm + C::kVecOff);
+
+  const int nt = (s + kT - 1) / kT;
+  const int kt = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int grp = H / Hkv;
+  const int k0 = kt * kT;
+  const int per_head = nt - kt;       // query tiles kt .. nt-1
+  const int total = grp * per_head;
+  const int kcol = (H + g) * HD, vcol = (H + Hkv + g) * HD;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tqkv);
+    tma_prefetch_desc(&tdo);
+    mbar_init(kv_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ld_full[i], 1);
+      mbar_init(&ld_empty[i], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 256);
+    mbar_init(p_empty, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_holder, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + HD;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(kv_full, 2 * C::kTile);
+      for (int bx = 0; bx < C::kBoxes; ++bx) {
+        tma_load_3d(sm + C::kKOff + bx * kBox, &tqkv, kcol + bx * 64, k0, b, kv_full);
+        tma_load_3d(sm + C::kVOff + bx * kBox, &tqkv, vcol + bx * 64, k0, b, kv_full);
+      }
+      for (int it = 0; it < total; ++it) {
+        const int st = it % C::kStages, use = it / C::kStages;
+        if (!mbar_wait(&ld_empty[st], (use & 1) ^ 1, err)) break;
+        const int h = g * grp + it / per_head;
+        const int q0 = (kt + it % per_head) * kT;
+        uint8_t* qs = sm + C::kQOff + st * 2 * C::kTile;
+        mbar_arrive_expect_tx(&ld_full[st], 2 * C::kTile);
+        for (int bx = 0; bx < C::kBoxes; ++bx) {
+          tma_load_3d(qs + bx * kBox, &tqkv, h * HD + bx * 64, q0, b, &ld_full[st]);
+          tma_load_3d(qs + C::kTile + bx * kBox, &tdo, h * HD + bx * 64, q0, b, &ld_full[st]);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16_f32(kT, kT, false, false);   // S^T, dP^T
+      constexpr uint32_t id_g = idesc_bf16_f32(kT, HD, false, true);    // dV, dK (B MN-major)
+      const uint32_t sK = smem_u32(sm + C::kKOff), sV = smem_u32(sm + C::kVOff);
+      const uint32_t sP = smem_u32(sm + C::kPOff), sDS = smem_u32(sm + C::kDSOff);
+      bool ok = mbar_wait(kv_full, 0, err);
+      for (int it = 0; ok && it < total; ++it) {
+        const int st = it % C::kStages, use = it / C::kStages;
+        if (!mbar_wait(&ld_full[st], use & 1, err)) break;
+        // S^T / dP^T TMEM is free once the previous iteration's softmax read it
+        if (it > 0 && !mbar_wait(p_full, (it - 1) & 1, err)) break;
+        tc_fence_after();
+        const uint32_t sQ = smem_u32(sm + C::kQOff + st * 2 * C::kTile), sO = sQ + C::kTile;
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+          tc_mma_bf16(tS, smem_desc_kmajor_sw128(sK + off), smem_desc_kmajor_sw128(sQ + off), id_s, kk > 0);
+          tc_mma_bf16(tdP, smem_desc_kmajor_sw128(sV + off), smem_desc_kmajor_sw128(sO + off), id_s, kk > 0);
+        }
+        tc_commit(s_full);
+        if (!mbar_wait(p_full, it & 1, err)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk) {
+          const uint32_t aoff = (kk >> 2) * kBox + (kk & 3) * 32;
+          const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+          tc_mma_bf16(tdV, smem_desc_kmajor_sw128(sP + aoff), smem_desc_mnmajor_sw128(sO + kk * 2048, kBox), id_g, acc);
+          tc_mma_bf16(tdK, smem_desc_kmajor_sw128(sDS + aoff), smem_desc_mnmajor_sw128(sQ + kk * 2048, kBox), id_g,
+                      acc);
+        }
+        tc_commit(p_empty);
+        tc_commit(&ld_empty[st]);
+      }
+    }
+  } else {
+    const int q = warp & 3, half = (warp - 2) >> 2;
+    const int row = q * 32 + lane;  // key row within the tile
+    const int key = k0 + row;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    const float sc = rsqrtf((float)HD) * kLog2e;
+    const int tid = threadIdx.x - 64;  // 0..255
+    bool ok = true;
+    for (int it = 0; it < total && ok; ++it) {
+      const int h = g * grp + it / per_head;
+      const int q0 = (kt + it % per_head) * kT;
+      float* lv = vec + (it & 1) * 256;  // [lse*log2e | delta] for this query tile
+      {
+        const int qi = tid & 127;
+        const int qq = q0 + qi;
+        const long long idx = ((long long)b * H + h) * s + qq;
+        if (tid < 128) lv[qi] = qq < s ? lse[idx] * kLog2e : INFINITY;
+        else lv[128 + qi] = qq < s ? delta[idx] : 0.f;
+      }
+      asm volatile("bar.sync 5, 256;" ::: "memory");
+      if (!mbar_wait(s_full, it & 1, err)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t rs[2][32], rp[2][32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        tmem_ld_32x32b_x32(tS + lane_off + half * 64 + c * 32, rs[c]);
+        tmem_ld_32x32b_x32(tdP + lane_off + half * 64 + c * 32, rp[c]);
+      }
+      tmem_ld_wait();
+      const bool diag = (q0 == k0);
+      uint32_t pk[32], dk[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        float pv[2], dv[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int ci = 2 * i + e;  // column within this half
+          const int qi = half * 64 + ci;
+          const float sv = __uint_as_float(rs[ci >> 5][ci & 31]);
+          float p = ex2_approx(fmaf(sv, sc, -lv[qi]));
+          if (diag && q0 + qi < key) p = 0.f;
+          pv[e] = p;
+          dv[e] = p * (__uint_as_float(rp[ci >> 5][ci & 31]) - lv[128 + qi]);
+        }
+        pk[i] = pack_bf16x2(pv[0], pv[1]);
+        dk[i] = pack_bf16x2(dv[0], dv[1]);
+      }
+      // P^T / dS^T smem is free once the previous dV / dK MMAs finished
+      if (it > 0 && !mbar_wait(p_empty, (it - 1) & 1, err)) { ok = false; break; }
+      store_half_row(sm + C::kPOff, half, row, pk);
+      store_half_row(sm + C::kDSOff, half, row, dk);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    if (ok && total > 0 && mbar_wait(p_empty, (total - 1) & 1, err)) {
+      tc_fence_after();
+      const bool store = key < s;
+      const long long r0 = (long long)b * s + key;
+      bf16* dkrow = dqkv + r0 * lddq + (long long)kcol + half * (HD / 2);
+      bf16* dvrow = dqkv + r0 * lddq + (long long)vcol + half * (HD / 2);
+      tmem_row_to_bf16(tdK + lane_off + half * (HD / 2), HD / 2, rsqrtf((float)HD), dkrow, store);
+      tmem_row_to_bf16(tdV + lane_off + half * (HD / 2), HD / 2, 1.f, dvrow, store);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------------- dQ
+template <int HD>
+struct QTc {
+  static constexpr int kBoxes = HD / 64;
+  static constexpr uint32_t kTile = kBoxes * kBox;
+  static constexpr uint32_t kQOff = 0;
+  static constexpr uint32_t kOOff = kTile;                 // dO
+  static constexpr uint32_t kKVOff = 2 * kTile;            // [2] K then V
+  static constexpr uint32_t kDSOff = kKVOff + 2 * 2 * kTile;
+  static constexpr uint32_t kBarOff = kDSOff + 2 * kBox;
+  static constexpr size_t kSmem = 1024 + kBarOff + 256;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kThr, 1)
+    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tqkv, const __grid_constant__ CUtensorMap tdo,
+                          const float* __restrict__ lse, const float* __restrict__ delta, bf16* __restrict__ dqkv,
+                          long long lddq, int s, int H, int Hkv, int* err) {
+  using C = QTc<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024b(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;   // [2]
+  uint64_t* kv_empty = bars + 3;  // [2]
+  uint64_t* s_full = bars + 5;
+  uint64_t* p_full = bars + 6;
+  uint64_t* p_empty = bars + 7;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 8);
+
+  const int nt = (s + kT - 1) / kT;
+  const int qt = nt - 1 - blockIdx.x;  // heaviest first
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int g = h / (H / Hkv);
+  const int q0 = qt * kT;
+  const int n_kv = qt + 1;
+  const int kcol = (H + g) * HD, vcol = (H + Hkv + g) * HD;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tqkv);
+    tma_prefetch_desc(&tdo);
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 256);
+    mbar_init(p_empty, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_holder, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, 2 * C::kTile);
+      for (int bx = 0; bx < C::kBoxes; ++bx) {
+        tma_load_3d(sm + C::kQOff + bx * kBox, &tqkv, h * HD + bx * 64, q0, b, q_full);
+        tma_load_3d(sm + C::kOOff + bx * kBox, &tdo, h * HD + bx * 64, q0, b, q_full);
+      }
+      for (int j = 0; j < n_kv; ++j) {
+        const int st = j & 1;
+        if (!mbar_wait(&kv_empty[st], ((j >> 1) & 1) ^ 1, err)) break;
+        uint8_t* ks = sm + C::kKVOff + st * 2 * C::kTile;
+        mbar_arrive_expect_tx(&kv_full[st], 2 * C::kTile);
+        for (int bx = 0; bx < C::kBoxes; ++bx) {
+          tma_load_3d(ks + bx * kBox, &tqkv, kcol + bx * 64, j * kT, b, &kv_full[st]);
+          tma_load_3d(ks + C::kTile + bx * kBox, &tqkv, vcol + bx * 64, j * kT, b, &kv_full[st]);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16_f32(kT, kT, false, false);
+      constexpr uint32_t id_q = idesc_bf16_f32(kT, HD, false, true);
+      const uint32_t sQ = smem_u32(sm + C::kQOff), sO = smem_u32(sm + C::kOOff);
+      const uint32_t sDS = smem_u32(sm + C::kDSOff);
+      bool ok = mbar_wait(q_full, 0, err);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int st = j & 1;
+        if (!mbar_wait(&kv_full[st], (j >> 1) & 1, err)) break;
+        if (j > 0 && !mbar_wait(p_full, (j - 1) & 1, err)) break;
+        tc_fence_after();
+        const uint32_t sK = smem_u32(sm + C::kKVOff + st * 2 * C::kTile), sV = sK + C::kTile;
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+          tc_mma_bf16(tS, smem_desc_kmajor_sw128(sQ + off), smem_desc_kmajor_sw128(sK + off), id_s, kk > 0);
+          tc_mma_bf16(tdP, smem_desc_kmajor_sw128(sO + off), smem_desc_kmajor_sw128(sV + off), id_s, kk > 0);
+        }
+        tc_commit(s_full);
+        if (!mbar_wait(p_full, j & 1, err)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk) {
+          const uint32_t aoff = (kk >> 2) * kBox + (kk & 3) * 32;
+          tc_mma_bf16(tdQ, smem_desc_kmajor_sw128(sDS + aoff), smem_desc_mnmajor_sw128(sK + kk * 2048, kBox), id_q,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(p_empty);
+        tc_commit(&kv_empty[st]);
+      }
+    }
+  } else {
+    const int q = warp & 3, half = (warp - 2) >> 2;
+    const int row = q * 32 + lane;
+    const int qpos = q0 + row;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    const float sc = rsqrtf((float)HD) * kLog2e;
+    const long long vidx = ((long long)b * H + h) * s + qpos;
+    const float l2 = qpos < s ? lse[vidx] * kLog2e : INFINITY;
+    const float dl = qpos < s ? delta[vidx] : 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv && ok; ++j) {
+      if (!mbar_wait(s_full, j & 1, err)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t rs[2][32], rp[2][32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        tmem_ld_32x32b_x32(tS + lane_off + half * 64 + c * 32, rs[c]);
+        tmem_ld_32x32b_x32(tdP + lane_off + half * 64 + c * 32, rp[c]);
+      }
+      tmem_ld_wait();
+      const bool diag = (j == n_kv - 1);
+      const int kb = j * kT + half * 64;
+      uint32_t dk[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        float dv[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int ci = 2 * i + e;
+          float p = ex2_approx(fmaf(__uint_as_float(rs[ci >> 5][ci & 31]), sc, -l2));
+          if (diag && kb + ci > qpos) p = 0.f;
+          dv[e] = p * (__uint_as_float(rp[ci >> 5][ci & 31]) - dl);
+        }
+        dk[i] = pack_bf16x2(dv[0], dv[1]);
+      }
+      if (j > 0 && !mbar_wait(p_empty, (j - 1) & 1, err)) { ok = false; break; }
+      store_half_row(sm + C::kDSOff, half, row, dk);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    if (ok && mbar_wait(p_empty, (n_kv - 1) & 1, err)) {
+      tc_fence_after();
+      bf16* dqrow = dqkv + ((long long)b * s + qpos) * lddq + (long long)h * HD + half * (HD / 2);
+      tmem_row_to_bf16(tdQ + lane_off + half * (HD / 2), HD / 2, rsqrtf((float)HD), dqrow, qpos < s);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_enc = nullptr;
+std::once_flag g_once;
+
+void init_once() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)KvTc<64>::kSmem);
+  cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)KvTc<128>::kSmem);
+  cudaFuncSetAttribute(attn_bwd_dq_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)QTc<64>::kSmem);
+  cudaFuncSetAttribute(attn_bwd_dq_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)QTc<128>::kSmem);
+}
+
+bool make_map3(CUtensorMap* m, const void* p, long long ld, int s, int B) {
+  cuuint64_t dims[3] = {(cuuint64_t)ld, (cuuint64_t)s, (cuuint64_t)B};
+  cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)s * ld * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)kT, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return g_enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+// Backward matrix products of attention on tcgen05 (hd 64 or 128); delta must
+// already hold rowsum(dO * O). Writes dq, dk, dv into dqkv.
+int attn_bwd_tc(const void* qkv, long long ld, const void* dout, long long lddo, const float* lse,
+                const float* delta, void* dqkv, long long lddq, int B, int s, int H, int Hkv, int hd,
+                cudaStream_t stream) {
+  std::call_once(g_once, init_once);
+  if (!g_enc) return MT_ECUDA;
+  if (hd != 64 && hd != 128) return MT_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(qkv) & 15) || (reinterpret_cast<uintptr_t>(dout) & 15) ||
+      (reinterpret_cast<uintptr_t>(dqkv) & 15) || ld % 8 || lddo % 8 || lddq % 8)
+    return MT_EINVAL;
+  CUtensorMap tq, td;
+  if (!make_map3(&tq, qkv, ld, s, B) || !make_map3(&td, dout, lddo, s, B)) return MT_EINVAL;
+  const int nt = (s + kT - 1) / kT;
+  int* err = device_error_word();
+  dim3 g1(nt, Hkv, B), g2(nt, H, B);
+  if (hd == 64) {
+    attn_bwd_dkdv_tc_kernel<64><<<g1, kThr, KvTc<64>::kSmem, stream>>>(tq, td, lse, delta, (bf16*)dqkv, lddq, s, H,
+                                                                       Hkv, err);
+    attn_bwd_dq_tc_kernel<64><<<g2, kThr, QTc<64>::kSmem, stream>>>(tq, td, lse, delta, (bf16*)dqkv, lddq, s, H, Hkv,
+                                                                   err);
+  } else {
+    attn_bwd_dkdv_tc_kernel<128><<<g1, kThr, KvTc<128>::kSmem, stream>>>(tq, td, lse, delta, (bf16*)dqkv, lddq, s,
+                                                                         H, Hkv, err);
+    attn_bwd_dq_tc_kernel<128><<<g2, kThr, QTc<128>::kSmem, stream>>>(tq, td, lse, delta, (bf16*)dqkv, lddq, s, H,
+                                                                     Hkv, err);
+  }
+  return cudaGetLastError() == cudaSuccess ? MT_OK : MT_ECUDA;
+}
+
+}  // namespace mt

@@ -26,6 +26,11 @@ int gemm_ex(const void* A, long long lda, int a_mn, const void* B, long long ldb
 int attn_fwd_tc(const void* qkv, long long ld, void* o, long long ldo, float* lse, int B, int s, int H, int Hkv,
                 int hd, cudaStream_t stream);
 
+// Attention backward products on tcgen05 (hd 64 or 128); delta precomputed.
+int attn_bwd_tc(const void* qkv, long long ld, const void* dout, long long lddo, const float* lse,
+                const float* delta, void* dqkv, long long lddq, int B, int s, int H, int Hkv, int hd,
+                cudaStream_t stream);
+
 // C = A * B^T (+ R); see mt_k_gemm.
 int gemm_abt(const void* A, long long lda, const void* B, long long ldb, void* C, long long ldc, int c_f32,
              const void* R, long long ldr, int M, int N, int K, cudaStream_t stream);

@@ -116,6 +116,12 @@ int mt_k_attn_bwd(const void* qkv, int64_t ldqkv, const void* o, int64_t ldo, co
                   const float* lse, float* delta, void* dqkv, int64_t lddqkv, int B, int s, int H, int Hkv, int hd,
                   void* stream);
 
+/* The same backward on the legacy mma.sync path (any hd); mt_k_attn_bwd uses
+ * it for hd = 16 and runs hd 64 / 128 on tcgen05. Kept for comparison. */
+int mt_k_attn_bwd_mma(const void* qkv, int64_t ldqkv, const void* o, int64_t ldo, const void* dout, int64_t lddo,
+                      const float* lse, float* delta, void* dqkv, int64_t lddqkv, int B, int s, int H, int Hkv,
+                      int hd, void* stream);
+
 /*
  * Cross entropy over a vocabulary row block: logits fp32 [M, ldl], labels
  * int32 [M]. Writes dz bf16 [M, lddz] = (softmax - onehot) * scale and

@@ -345,3 +345,30 @@ def test_attention_fwd_tcgen05_matches_mma_and_oracle(B, s, H, Hkv, hd):
     assert_close(host(o), orf.reshape(B * s, H * hd), l2=1e-2, elem=2e-2, what="tc o")
     np.testing.assert_allclose(host(lse), lr, rtol=0, atol=2e-2)
     assert_close(host(o), host(o2), l2=1e-2, elem=2e-2, what="tc vs mma")
+
+
+@pytest.mark.parametrize("B,s,H,Hkv,hd", [(3, 200, 4, 2, 128), (2, 129, 8, 2, 64), (1, 1024, 4, 4, 64),
+                                          (2, 384, 2, 1, 128)])
+def test_attention_bwd_tcgen05_matches_mma_and_oracle(B, s, H, Hkv, hd):
+    """The tcgen05 backward (dK/dV and dQ kernels) against the oracle and the
+    mma.sync backward, several ragged sequences per batch; deterministic."""
+    qkv, q, k, v = _attn_inputs(B, s, H, Hkv, hd, 13 * s + hd)
+    o = torch.empty((B * s, H * hd), device=DEV, dtype=torch.bfloat16)
+    lse = torch.empty((B, H, s), device=DEV)
+    mt.k_attn_fwd(qkv, o, lse, B, s, H, Hkv, hd)
+    rng = np.random.default_rng(s + 1)
+    do, doh = bf(rng.standard_normal((B * s, H * hd)))
+    delta = torch.empty((B, H, s), device=DEV)
+    g1, g2, g3 = (torch.zeros_like(qkv) for _ in range(3))
+    mt.k_attn_bwd(qkv, o, do, lse, delta, g1, B, s, H, Hkv, hd)
+    mt.k_attn_bwd(qkv, o, do, lse, delta, g2, B, s, H, Hkv, hd)
+    mt.k_attn_bwd_mma(qkv, o, do, lse, delta, g3, B, s, H, Hkv, hd)
+    torch.cuda.synchronize()
+    assert torch.equal(g1, g2)
+    dq, dk, dv = ops.attention_bwd(q, k, v, doh.reshape(B, s, H, hd))
+    g = host(g1)
+    fl = 1e-3 * np.abs(dv).max()
+    assert_close(g[:, :H * hd], dq.reshape(B * s, -1), l2=2e-2, elem=3e-2, what="dq", floor=fl)
+    assert_close(g[:, H * hd:(H + Hkv) * hd], dk.reshape(B * s, -1), l2=2e-2, elem=3e-2, what="dk", floor=fl)
+    assert_close(g[:, (H + Hkv) * hd:], dv.reshape(B * s, -1), l2=2e-2, elem=3e-2, what="dv")
+    assert_close(g, host(g3), l2=2e-2, elem=3e-2, what="tc vs mma", floor=fl)
