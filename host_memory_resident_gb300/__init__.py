@@ -62,7 +62,7 @@ class KernelProfile(C.Structure):
 
 
 EXPORTS = [
-    "mt_layout", "mt_unit_range", "mt_init", "mt_train_step", "mt_train_step_device",
+    "mt_layout", "mt_unit_range", "mt_plan", "mt_init", "mt_train_step", "mt_train_step_device", "mt_train_step_accum",
     "mt_read_grads", "mt_sync", "mt_get_step", "mt_set_step", "mt_sync_store", "mt_get_stats",
     "mt_get_stream", "mt_profile_enable", "mt_profile_read", "mt_destroy", "mt_last_error", "mt_debug_inject", "mt_debug_inject_global",
     "mt_host_adam", "mt_host_adam_slab", "mt_host_to_bf16",
@@ -90,9 +90,11 @@ def lib():
     sig = {
         "mt_layout": ([C.POINTER(Config), C.POINTER(TensorDesc), I, C.POINTER(I), C.POINTER(I64)], I),
         "mt_unit_range": ([C.POINTER(Config), I, C.POINTER(I64), C.POINTER(I64)], I),
+        "mt_plan": ([C.POINTER(Config), C.POINTER(I64), C.POINTER(I64), C.POINTER(I64)], I),
         "mt_init": ([C.POINTER(Config), P, P, P, P, I64, C.POINTER(P)], I),
         "mt_train_step": ([P, P, P, C.c_int32, C.c_int32, C.POINTER(F)], I),
         "mt_train_step_device": ([P, P, P, C.c_int32, C.c_int32, C.POINTER(F)], I),
+        "mt_train_step_accum": ([P, P, P, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.POINTER(F)], I),
         "mt_read_grads": ([P, P, I64], I),
         "mt_sync": ([P], I),
         "mt_get_step": ([P, C.POINTER(I64)], I),
@@ -192,6 +194,13 @@ def unit_range(cfg: Config, unit: int):
     return off.value, ln.value
 
 
+def plan(cfg: Config) -> dict:
+    """Exact memory plan of a handle for `cfg` (no GPU, nothing allocated)."""
+    dev, pin, state = C.c_int64(), C.c_int64(), C.c_int64()
+    check(lib().mt_plan(C.byref(cfg), C.byref(dev), C.byref(pin), C.byref(state)))
+    return {"device_bytes": dev.value, "pinned_bytes": pin.value, "host_state_bytes": state.value}
+
+
 def _ptr(a: np.ndarray):
     return a.ctypes.data_as(C.c_void_p)
 
@@ -221,6 +230,16 @@ class Trainer:
         B, s = tokens.shape
         loss = C.c_float()
         check(lib().mt_train_step(self.h, _ptr(tokens), _ptr(labels), B, s, C.byref(loss)), self.h)
+        return loss.value
+
+    def step_accum(self, tokens, labels, micro_index: int, n_micro: int) -> float:
+        """One micro-step of gradient accumulation (Adam after the last)."""
+        tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+        labels = np.ascontiguousarray(labels, dtype=np.int32)
+        B, s = tokens.shape
+        loss = C.c_float()
+        check(lib().mt_train_step_accum(self.h, _ptr(tokens), _ptr(labels), B, s, micro_index, n_micro,
+                                        C.byref(loss)), self.h)
         return loss.value
 
     def step_device(self, tok_ptr: int, lab_ptr: int, B: int, s: int) -> float:

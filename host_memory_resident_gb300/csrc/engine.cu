@@ -105,6 +105,9 @@ struct Job {
   int64_t t;
   int parity;     // step parity: selects the step's loss event / state
   int64_t seq;    // step sequence number (monotonic per handle)
+  bool acc;       // add to the running gradient sum (micro-steps after the first)
+  bool adam;      // last micro-step: apply Adam to (sum) * scale
+  float scale;
 };
 
 }  // namespace
@@ -170,6 +173,7 @@ struct mt_handle {
   int loss_state[2] = {0, 0};  // per step parity: 0 unknown, 1 finite, 2 non-finite
   std::vector<int> unit_pending;  // queued or running jobs per unit
   int64_t step_seq = 0;        // sequence number of the step being enqueued
+  bool accum_nonfinite = false;  // a micro-step of the current accumulation had a non-finite loss
   int64_t enqueued_seq = 0;    // last step whose units are all queued
   int64_t inject_sleep_ms = 0, inject_fail_at = 0, deadline_ms = 600000;
   int64_t worker_units_total = 0;
@@ -262,7 +266,9 @@ void worker_main(mt_handle* h) {
       a.beta1 = h->cfg.beta1;
       a.beta2 = h->cfg.beta2;
       a.eps = h->cfg.adam_eps;
-      a.apply = h->loss_state[job.parity] == 1;
+      a.apply = job.adam && h->loss_state[job.parity] == 1 && !h->accum_nonfinite;
+      a.accumulate = job.acc;
+      a.grad_scale = job.scale;
       const auto tc = Clock::now();
       wait_s = std::chrono::duration<double>(tc - tw).count();
       adam_pass(a, h->threads);
@@ -291,6 +297,8 @@ struct Step {
   mt_handle* h;
   int B, s, M;
   int64_t t_next;
+  bool acc = false, adam = true;
+  float gscale = 1.f;
 
   cudaStream_t cs() const { return h->s_comp; }
 
@@ -366,7 +374,7 @@ struct Step {
     h->st.d2h_bytes += (int64_t)bytes;
     {
       std::lock_guard<std::mutex> lk(h->mu);
-      h->jobs.push_back(Job{u, k, t_next, parity(), h->step_seq});
+      h->jobs.push_back(Job{u, k, t_next, parity(), h->step_seq, acc, adam, gscale});
       ++h->unit_pending[u];
     }
     h->cv.notify_all();
@@ -665,6 +673,24 @@ void plan_device(mt_handle* h, Arena& A) {
 
 }
 
+void set_dims(mt_handle* h, const mt_config& c) {
+  h->L = c.n_layers;
+  h->d = c.d_model;
+  h->H = c.n_heads;
+  h->Hkv = c.n_kv_heads;
+  h->hd = c.head_dim;
+  h->f = c.ffn_dim;
+  h->V = c.vocab;
+  h->qkvN = (h->H + 2 * h->Hkv) * h->hd;
+  h->hq = h->H * h->hd;
+  h->nseg = (h->L + c.ckpt_interval - 1) / c.ckpt_interval;
+  h->Mmax = c.max_batch * c.max_seq;
+  int64_t mc = (1LL << 28) / h->V;
+  mc = mc / 128 * 128;
+  if (mc < 128) mc = 128;
+  h->Mchunk = (int)std::min<int64_t>(mc, h->Mmax);
+}
+
 int fail(mt_handle* h, int code, const std::string& msg) {
   set_err(h, msg);
   return code;
@@ -711,6 +737,29 @@ int mt_unit_range(const mt_config* cfg, int unit, int64_t* offset, int64_t* leng
   return MT_OK;
 }
 
+int mt_plan(const mt_config* cfg, int64_t* device_bytes, int64_t* pinned_bytes, int64_t* host_state_bytes) {
+  const char* why = nullptr;
+  if (!cfg || !config_valid(*cfg, &why)) return fail(nullptr, MT_EINVAL, why ? why : "null config");
+  mt_handle h;
+  h.cfg = *cfg;
+  h.lay = build_layout(*cfg);
+  h.n_total = h.lay.n_total;
+  set_dims(&h, *cfg);
+  try {
+    Arena probe;
+    probe.cap = ~size_t(0) >> 1;
+    plan_device(&h, probe);
+    if (device_bytes) *device_bytes = (int64_t)probe.used;
+  } catch (const StepError& e) {
+    return fail(nullptr, e.code, e.msg);
+  }
+  if (pinned_bytes)
+    *pinned_bytes = (int64_t)(sizeof(uint16_t) * h.n_total + (size_t)cfg->n_slabs * sizeof(uint16_t) * h.lay.max_unit +
+                              sizeof(int32_t) * 2 * (size_t)h.Mmax + sizeof(float) * 4 + sizeof(int32_t) * 4);
+  if (host_state_bytes) *host_state_bytes = (int64_t)(4 * sizeof(float)) * h.n_total;
+  return MT_OK;
+}
+
 int mt_debug_inject_global(int what, int64_t value) {
   if (what == 4) {
     g_fail_next_alloc.store(value ? 1 : 0);
@@ -740,23 +789,7 @@ int mt_init(const mt_config* cfg, float* master, float* adam_m, float* adam_v, f
   h->grad = grad;
   h->n_total = n_total;
   h->threads = cfg->host_threads > 0 ? cfg->host_threads : default_threads();
-  h->L = cfg->n_layers;
-  h->d = cfg->d_model;
-  h->H = cfg->n_heads;
-  h->Hkv = cfg->n_kv_heads;
-  h->hd = cfg->head_dim;
-  h->f = cfg->ffn_dim;
-  h->V = cfg->vocab;
-  h->qkvN = (h->H + 2 * h->Hkv) * h->hd;
-  h->hq = h->H * h->hd;
-  h->nseg = (h->L + cfg->ckpt_interval - 1) / cfg->ckpt_interval;
-  h->Mmax = cfg->max_batch * cfg->max_seq;
-  {
-    int64_t mc = (1LL << 28) / h->V;
-    mc = mc / 128 * 128;
-    if (mc < 128) mc = 128;
-    h->Mchunk = (int)std::min<int64_t>(mc, h->Mmax);
-  }
+  set_dims(h, *cfg);
   try {
     if (g_fail_next_alloc.exchange(0)) throw StepError{MT_ENOMEM, "injected device allocation failure"};
     CK(cudaSetDevice(cfg->device));
@@ -840,14 +873,20 @@ int mt_init(const mt_config* cfg, float* master, float* adam_m, float* adam_v, f
 }
 
 static int run_step(mt_handle* h, const int32_t* tokens, const int32_t* labels, int B, int s, bool on_device,
-                    float* loss_out) {
+                    float* loss_out, int micro_index = 0, int n_micro = 1) {
   if (!h) return fail(nullptr, MT_EINVAL, "null handle");
   if (h->broken) return fail(h, MT_ESTATE, "handle is unusable after an earlier timeout or device error");
   if (!tokens || !labels || B <= 0 || s <= 0 || B > h->cfg.max_batch || s > h->cfg.max_seq)
     return fail(h, MT_EINVAL, "bad tokens/labels or batch/seq outside the configured maxima");
   const int M = B * s;
   const auto t0 = Clock::now();
+  if (n_micro < 1 || micro_index < 0 || micro_index >= n_micro)
+    return fail(h, MT_EINVAL, "micro_index must lie in [0, n_micro)");
   Step st{h, B, s, M, h->t + 1};
+  st.acc = micro_index > 0;
+  st.adam = micro_index == n_micro - 1;
+  st.gscale = 1.f / (float)n_micro;
+  if (micro_index == 0) h->accum_nonfinite = false;
   try {
     CK(cudaSetDevice(h->cfg.device));
     if (!on_device) {
@@ -933,8 +972,11 @@ static int run_step(mt_handle* h, const int32_t* tokens, const int32_t* labels, 
   if (loss_out) *loss_out = loss;
   h->st.steps += 1;
   h->st.last_step_s = seconds_since(t0);
-  if (!std::isfinite(total)) return fail(h, MT_ENONFINITE, "non-finite loss: no Adam update was applied");
-  h->t += 1;
+  if (!std::isfinite(total)) {
+    h->accum_nonfinite = true;
+    return fail(h, MT_ENONFINITE, "non-finite loss: no Adam update was applied");
+  }
+  if (st.adam && !h->accum_nonfinite) h->t += 1;
   return MT_OK;
 }
 
@@ -946,6 +988,11 @@ int mt_train_step(mt_handle* h, const int32_t* tokens, const int32_t* labels, in
 int mt_train_step_device(mt_handle* h, const int32_t* d_tokens, const int32_t* d_labels, int32_t batch, int32_t seq,
                          float* loss_out) {
   return run_step(h, d_tokens, d_labels, batch, seq, true, loss_out);
+}
+
+int mt_train_step_accum(mt_handle* h, const int32_t* tokens, const int32_t* labels, int32_t batch, int32_t seq,
+                        int32_t micro_index, int32_t n_micro, float* loss_out) {
+  return run_step(h, tokens, labels, batch, seq, false, loss_out, micro_index, n_micro);
 }
 
 int mt_sync(mt_handle* h) {

@@ -114,10 +114,11 @@ void emit_bf16(const float* src, uint16_t* dst, int64_t n, int threads) {
   for (int64_t i = 0; i < n; ++i) dst[i] = rne_bits(src[i]);
 }
 
-// One streaming pass per element: gradient in (bf16 slab or fp32), gradient
-// out, m, v, w updated, bf16 copy of w out. The variants are compile-time
-// so the loop body has no control flow.
-template <bool kSlab, bool kGradOut, bool kStore>
+// One streaming pass per element: gradient in (bf16 slab or fp32, optionally
+// added to the running sum in grad_out and scaled), gradient out, m, v, w
+// updated, bf16 copy of w out. The variants are compile-time so the loop
+// body has no control flow.
+template <bool kSlab, bool kGradOut, bool kStore, bool kAcc>
 static void adam_loop(const AdamArgs& a, int threads) {
   const double bc1 = 1.0 - std::pow((double)a.beta1, (double)a.t);
   const double bc2 = 1.0 - std::pow((double)a.beta2, (double)a.t);
@@ -125,6 +126,7 @@ static void adam_loop(const AdamArgs& a, int threads) {
   const float c1 = 1.f - b1, c2 = 1.f - b2;
   const float inv_bc1 = (float)(1.0 / bc1);
   const float inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
+  const float gs = a.grad_scale;
   float* __restrict__ w = a.w;
   float* __restrict__ m = a.m;
   float* __restrict__ v = a.v;
@@ -135,7 +137,8 @@ static void adam_loop(const AdamArgs& a, int threads) {
   const int64_t n = a.n;
 #pragma omp parallel for schedule(static) num_threads(threads)
   for (int64_t i = 0; i < n; ++i) {
-    const float g = kSlab ? bf16_to_f32(slab[i]) : gin[i];
+    float g = kSlab ? bf16_to_f32(slab[i]) : gin[i];
+    if (kAcc) g = (gout[i] + g) * gs;
     if (kGradOut) gout[i] = g;
     const float mi = b1 * m[i] + c1 * g;
     const float vi = b2 * v[i] + c2 * g * g;
@@ -148,31 +151,41 @@ static void adam_loop(const AdamArgs& a, int threads) {
   }
 }
 
+template <bool kSlab, bool kGradOut, bool kStore>
+static void adam_acc(const AdamArgs& a, int threads) {
+  if (a.accumulate) adam_loop<kSlab, kGradOut, kStore, true>(a, threads);
+  else adam_loop<kSlab, kGradOut, kStore, false>(a, threads);
+}
+
 void adam_pass(const AdamArgs& a, int threads) {
   if (!a.apply) {
-    // gradient only (non-finite loss): no optimizer update
+    // gradient only: set or add to the running sum (no optimizer update)
     if (!a.grad_out) return;
     float* __restrict__ gout = a.grad_out;
     const uint16_t* __restrict__ slab = a.slab;
     const float* __restrict__ gin = a.grad_in;
     const int64_t n = a.n;
+    if (a.accumulate) {
 #pragma omp parallel for schedule(static) num_threads(threads)
-    for (int64_t i = 0; i < n; ++i) gout[i] = slab ? bf16_to_f32(slab[i]) : gin[i];
+      for (int64_t i = 0; i < n; ++i) gout[i] += slab ? bf16_to_f32(slab[i]) : gin[i];
+    } else {
+#pragma omp parallel for schedule(static) num_threads(threads)
+      for (int64_t i = 0; i < n; ++i) gout[i] = slab ? bf16_to_f32(slab[i]) : gin[i];
+    }
     return;
   }
   const bool sl = a.slab != nullptr, go = a.grad_out != nullptr, st = a.store != nullptr;
-  if (sl && go && st) adam_loop<true, true, true>(a, threads);
-  else if (sl && go) adam_loop<true, true, false>(a, threads);
-  else if (sl && st) adam_loop<true, false, true>(a, threads);
-  else if (sl) adam_loop<true, false, false>(a, threads);
-  else if (go && st) adam_loop<false, true, true>(a, threads);
-  else if (go) adam_loop<false, true, false>(a, threads);
-  else if (st) adam_loop<false, false, true>(a, threads);
-  else adam_loop<false, false, false>(a, threads);
+  if (a.accumulate && !go) return;  // a running sum needs grad_out
+  if (sl && go && st) adam_acc<true, true, true>(a, threads);
+  else if (sl && go) adam_acc<true, true, false>(a, threads);
+  else if (sl && st) adam_acc<true, false, true>(a, threads);
+  else if (sl) adam_acc<true, false, false>(a, threads);
+  else if (go && st) adam_acc<false, true, true>(a, threads);
+  else if (go) adam_acc<false, true, false>(a, threads);
+  else if (st) adam_acc<false, false, true>(a, threads);
+  else adam_acc<false, false, false>(a, threads);
 }
 
-// All cores but two: the main thread keeps enqueueing device work and the
-// CUDA driver runs its own threads while the worker's team runs Adam.
 int default_threads() {
   const int n = omp_get_num_procs();
   return n > 4 ? n - 2 : (n > 0 ? n : 1);

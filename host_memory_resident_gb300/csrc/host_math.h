@@ -45,6 +45,8 @@ struct AdamArgs {
   int64_t n, t;
   float lr, beta1, beta2, eps;
   bool apply;               // false: only write grad_out
+  bool accumulate = false;  // gradient = grad_out (running sum) + this gradient
+  float grad_scale = 1.f;   // Adam (and grad_out when applying) use gradient * grad_scale
 };
 
 void adam_pass(const AdamArgs& a, int threads);

@@ -127,6 +127,15 @@ int mt_layout(const mt_config* cfg, mt_tensor_desc* out, int cap, int* n_out, in
 int mt_unit_range(const mt_config* cfg, int unit, int64_t* offset, int64_t* length);
 
 /*
+ * Memory plan of `cfg` without a GPU and without allocating: device bytes of
+ * the handle's arena (weight buffers, slabs, checkpoints, activations,
+ * scratch; the same planner mt_init uses), pinned host bytes (bf16 store,
+ * staging slabs, token staging) and the caller's FP32 state (master, m, v,
+ * grad = 16 bytes per element). Any pointer may be NULL.
+ */
+int mt_plan(const mt_config* cfg, int64_t* device_bytes, int64_t* pinned_bytes, int64_t* host_state_bytes);
+
+/*
  * Creates a handle. master, adam_m, adam_v, grad are caller-owned FP32 host
  * arrays of n_total elements in the flat layout; they must stay valid until
  * mt_destroy. The caller initialises master and zeroes m and v. The library
@@ -155,6 +164,19 @@ int mt_train_step(mt_handle* h, const int32_t* tokens, const int32_t* labels, in
  * MT_EDEVICE before any weight is touched by Adam. */
 int mt_train_step_device(mt_handle* h, const int32_t* d_tokens, const int32_t* d_labels, int32_t batch,
                          int32_t seq, float* loss_out);
+
+/*
+ * Gradient accumulation over micro-batches (a way the travelaiplan blog,
+ * "怎麼開始" step 3, suggests to grow the global batch): micro_index runs
+ * 0 .. n_micro-1. Micro-step 0 sets the FP32 gradient to its micro-batch
+ * gradient, later ones add theirs; the last one divides the sum by n_micro
+ * (so `grad` holds the mean, the gradient of the mean loss over all
+ * micro-batches of equal size) and applies one Adam step (t += 1). A
+ * non-finite loss in any micro-step skips that Adam step. mt_train_step is
+ * the n_micro = 1 case.
+ */
+int mt_train_step_accum(mt_handle* h, const int32_t* tokens, const int32_t* labels, int32_t batch, int32_t seq,
+                        int32_t micro_index, int32_t n_micro, float* loss_out);
 
 /* Copies the FP32 gradient of the last step (n elements, n <= n_total). */
 int mt_read_grads(mt_handle* h, float* dst, int64_t n);

@@ -1,0 +1,48 @@
+"""bench.py's multi-rank plumbing on CPU: two gloo ranks (replicas only, no
+data-path collective) agree on the max step time and the summed tokens."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as tmp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    import bench
+    w, r, local, pg = bench.dist_setup()
+    assert (w, r, local) == (world, rank, rank)
+    bench.barrier(pg)
+    t = bench.max_over_ranks(pg, 1.0 + rank)
+    tok = bench.sum_over_ranks(pg, 100.0 * (rank + 1))
+    out.put((rank, t, tok))
+    pg.destroy_process_group()
+
+
+def test_two_gloo_ranks_reduce_time_and_tokens():
+    ctx = tmp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in range(2))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res == [(0, 2.0, 300.0), (1, 2.0, 300.0)]
+
+
+def test_reference_arm_other_ranks_exit_without_work(monkeypatch):
+    import bench
+
+    class A:
+        gpus, steps, warmup = 2, 1, 0
+    assert bench.run_reference(A, None, 2, 1, None) == 0

@@ -1,0 +1,67 @@
+"""Resource calculator (no GPU): the pages' sizing rules and the planner."""
+import pytest
+
+import host_memory_resident_gb300 as mt
+import synth
+from host_memory_resident_gb300 import resources
+
+
+def test_host_state_matches_the_pages_sizing_rules():
+    e7 = resources.estimate(synth.workload("7b"))
+    n = e7["params"]
+    # FP32 master + m + v: 12 bytes per parameter, "about 84 GB" at 7B
+    # (zhichai.net article, introduction; lqnn.cn article section 一: ~12 GB per 1B)
+    master_m_v = e7["host_state_bytes"] * 12 // 16
+    assert master_m_v == 12 * n
+    assert 80e9 < master_m_v < 84e9
+    # full precision with the gradient: 16 bytes per parameter, so 70B needs
+    # about 1.1 TB (travelaiplan blog, 核心功能 point 1)
+    assert 16 * 70e9 == pytest.approx(1.12e12)
+    assert e7["host_state_bytes"] == 16 * n
+    # the bf16 store is 2 bytes per parameter (lqnn.cn section 一: 120B -> ~240 GB)
+    assert e7["pinned_bytes"] >= 2 * n
+
+
+def test_plan_grows_with_tokens_and_not_with_depth_beyond_checkpoints():
+    base = synth.workload("1.1b")
+    a = resources.estimate(base, batch=4)["device_bytes"]
+    b = resources.estimate(base, batch=8)["device_bytes"]
+    assert b > a
+    # deeper model with the same checkpoint interval: only checkpoints grow
+    d1 = resources.estimate(base.with_(n_layers=8), batch=4)["device_bytes"]
+    d2 = resources.estimate(base.with_(n_layers=16), batch=4)["device_bytes"]
+    ckpt = 4 * 2048 * 2048 * 2  # one [M, d] bf16 checkpoint
+    assert d2 - d1 == pytest.approx(2 * ckpt, rel=0.01)
+
+
+def test_suggest_batch_is_the_largest_that_fits():
+    shape = synth.workload("1.1b")
+    budget = resources.estimate(shape, batch=8)["device_bytes"]
+    b = resources.suggest_batch(shape, device_budget=budget)
+    assert b == 8
+    assert resources.suggest_batch(shape, device_budget=1e6) is None
+
+
+def test_streamed_units_follow_the_two_buffer_cache():
+    # 4 layers, 2-layer segments: each segment's layers stay resident from
+    # recompute into backward, so only the recompute re-streams them
+    assert resources.streamed_units(4, 2) == [0, 1, 2, 3, 4, 5, 3, 4, 1, 2]
+    # 1-layer segments: the last layer is still held when backward begins
+    assert resources.streamed_units(3, 1) == [0, 1, 2, 3, 4, 2, 1]
+    # 4-layer segments: backward re-streams all but the last two of a segment
+    assert resources.streamed_units(4, 4) == [0, 1, 2, 3, 4, 5, 1, 2, 3, 4, 2, 1]
+
+
+def test_traffic_matches_the_unit_model():
+    shape = synth.workload("tiny").with_(n_layers=4, ckpt_interval=2)
+    e = resources.estimate(shape)
+    cfg = mt.make_config(shape)
+    lay, n = mt.layout(cfg)
+    units = [0] * 6
+    for t in lay:
+        units[t["unit"]] += t["rows"] * t["cols"]
+    assert e["h2d_bytes_per_step"] == 2 * (2 * sum(units) - units[0] - units[-1])
+    assert e["d2h_bytes_per_step"] == 2 * n
+    e7 = resources.estimate(synth.workload("7b"))
+    # 4-layer segments: layer weights cross the link 2.5 times, the rest once
+    assert 4.5 * e7["params"] < e7["h2d_bytes_per_step"] < 5.0 * 2 * e7["params"]

@@ -357,3 +357,51 @@ def test_overlap_worker_failure_is_reported(tiny):
         else:
             assert code == mt.MT_EWORKER
         assert "injected" in tr.last_error()
+
+
+# ------------------------------------------------------ gradient accumulation
+@pytest.mark.parametrize("overlap", [False, True])
+def test_gradient_accumulation_over_micro_batches(tiny, overlap):
+    """Three micro-batches: no update until the last, which applies Adam to
+    the mean gradient; that gradient matches the oracle's mean of the three
+    micro-batch gradients, and the update matches the oracle's Adam fed the
+    same gradient."""
+    shape = tiny.with_(n_layers=3, ckpt_interval=2)
+    lay, master, _, _ = _setup(shape)
+    micro = [synth.make_tokens(shape.vocab, shape.batch, shape.seq, seed=5 + i) for i in range(3)]
+    w = master.copy()
+    with mt.Trainer(mt.make_config(shape, overlap_adam=overlap), w) as tr:
+        losses = []
+        for i, (tk, lb) in enumerate(micro):
+            losses.append(tr.step_accum(tk, lb, i, 3))
+            tr.sync()
+            if i < 2:
+                assert tr.get_step() == 0 and np.array_equal(w, master)
+        assert tr.get_step() == 1
+        g = tr.read_grads()
+    refs = [oracle.step_grads(shape, bf16_weights(master), tk, lb) for tk, lb in micro]
+    for loss, (rl, _) in zip(losses, refs):
+        assert abs(loss - rl) / rl <= 5e-3
+    ref = sum(r for _, r in refs) / 3.0
+    for t in lay.tensors():
+        a = g[t.offset:t.offset + t.size].astype(np.float64)
+        b = ref[t.offset:t.offset + t.size]
+        assert np.linalg.norm(a - b) / np.linalg.norm(b) <= 2e-2, t.name
+    wo, _, _ = oracle.adam_update(master, np.zeros_like(master), np.zeros_like(master), g, 1,
+                                  shape.lr, shape.beta1, shape.beta2, shape.adam_eps)
+    assert np.max(np.abs(w - wo)) <= 1e-6 * (shape.lr / 1e-3)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("streamed", [True, False])
+def test_planner_matches_the_live_handle(tiny, streamed):
+    """mt_plan, which allocates nothing, reports the device and pinned bytes
+    that mt_init then allocates for the same configuration."""
+    shape = tiny.with_(n_layers=5, ckpt_interval=2)
+    lay, master, _, _ = _setup(shape)
+    cfg = mt.make_config(shape, streamed=streamed)
+    p = mt.plan(cfg)
+    with mt.Trainer(cfg, master.copy()) as tr:
+        st = tr.stats()
+    assert p["device_bytes"] == st["device_bytes"]
+    assert p["pinned_bytes"] == st["pinned_bytes"]
