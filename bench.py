@@ -155,9 +155,10 @@ def host_link_probe(torch, dev, nbytes=1 << 30, reps=5):
     return {"h2d_gbs": gb / t_h, "d2h_gbs": gb / t_d, "bidir_h2d_gbs": gb / t_b, "bidir_d2h_gbs": gb / t_b}
 
 
-def host_adam_probe(mt, n=44_044_288, reps=4, threads=0):
-    """Rate of the library's per-unit host pass (bf16 slab in, FP32 grad out,
-    Adam, bf16 emit) on one 1.1B-layer-sized slice, in GB/s at 32 B/param."""
+def host_adam_probe(mt, n=44_044_288, reps=4, threads=0, keep_grads=False):
+    """Rate of the library's per-unit host pass (bf16 slab in, FP32 grad out
+    if kept, Adam, bf16 emit) on one 1.1B-layer-sized slice, in GB/s at the
+    pass's algorithmic bytes (32 B/param with the grad array, 28 without)."""
     rng = np.random.default_rng(0)
     w = rng.standard_normal(n).astype(np.float32)
     m = np.zeros(n, np.float32)
@@ -168,9 +169,16 @@ def host_adam_probe(mt, n=44_044_288, reps=4, threads=0):
     best = 1e30
     for t in range(1, reps + 1):
         t0 = time.perf_counter()
-        mt.host_adam_slab(w, m, v, slab, t, 1e-3, 0.9, 0.999, 1e-8, grad_out=g, store=store, threads=threads)
+        mt.host_adam_slab(w, m, v, slab, t, 1e-3, 0.9, 0.999, 1e-8, grad_out=g if keep_grads else None,
+                          store=store, threads=threads)
         best = min(best, time.perf_counter() - t0)
-    return 32.0 * n / best / 1e9
+    return host_bytes_per_param(keep_grads) * n / best / 1e9
+
+
+def host_bytes_per_param(keep_grads):
+    """Host DRAM bytes of the per-unit pass: bf16 gradient in (2), master, m,
+    v read and written (24), bf16 store out (2), FP32 gradient out (4) if kept."""
+    return 32.0 if keep_grads else 28.0
 
 
 def gemm_traffic_record():
@@ -377,9 +385,10 @@ def run_ours(args, shape, world, rank, local, pg):
     dev_batches = [(torch.from_numpy(t).to(dev), torch.from_numpy(l).to(dev)) for t, l in batches[:W + K]]
     link = host_link_probe(torch, dev)
     torch.cuda.empty_cache()
-    adam_gbs = host_adam_probe(mt, threads=args.host_threads)
+    adam_gbs = host_adam_probe(mt, threads=args.host_threads, keep_grads=args.keep_grads)
+    hb = host_bytes_per_param(args.keep_grads)
 
-    tr = mt.Trainer(cfg, master)
+    tr = mt.Trainer(cfg, master, keep_grads=args.keep_grads)
     comp = torch.cuda.ExternalStream(tr.stream(0), device=dev)
     for i in range(W):
         tr.step_device(dev_batches[i][0].data_ptr(), dev_batches[i][1].data_ptr(), B, s)
@@ -451,6 +460,7 @@ def run_ours(args, shape, world, rank, local, pg):
         "config": {"workload": workload_desc(shape), "global_batch_tokens": M * world, "seq_len": s,
                    "parallelism": f"replicas x{world} (no collective)" if world > 1 else "single GPU",
                    "overlap_adam": bool(args.overlap),
+                   "fp32_grad_array": bool(args.keep_grads),
                    "l2": "inputs larger than L2: each step streams the whole bf16 store "
                          f"({w_bytes / 1e9:.2f} GB) and the activations"},
         "model_tflops": F / t_step / 1e12,
@@ -465,14 +475,15 @@ def run_ours(args, shape, world, rank, local, pg):
                      "traffic_note": "ncu DRAM bytes of one captured GEMM launch (profiles/gemm_traffic.json) as a "
                                      "ratio to its algorithmic bytes, times the step's mean algorithmic bytes per "
                                      "GEMM launch" if traffic else "no capture of the current GEMM source"},
-        "host_bound": {"adam_probe_gbs": adam_gbs, "t_host_s": 32.0 * n_total / (adam_gbs * 1e9),
-                       "frac": 32.0 * n_total / (adam_gbs * 1e9) / t_step,
-                       "note": "host accumulate + Adam + emit at 32 B/param over the rate the same pass reaches "
-                               "alone on one layer-sized slice; the north-star roofline leaves this bound out"},
+        "host_bound": {"adam_probe_gbs": adam_gbs, "t_host_s": hb * n_total / (adam_gbs * 1e9),
+                       "frac": hb * n_total / (adam_gbs * 1e9) / t_step, "bytes_per_param": hb,
+                       "note": "host Adam + bf16 emit (+ FP32 grad out when kept) over the rate the same pass "
+                               "reaches alone on one layer-sized slice; the north-star roofline leaves this "
+                               "bound out"},
         "kernels": prof_out,
         "host": {"adam_s_per_step": (st1["host_adam_s"] - st0["host_adam_s"]) / K,
                  "adam_compute_s_per_step": (st1["host_compute_s"] - st0["host_compute_s"]) / K,
-                 "adam_compute_gbs": 32.0 * n_total * K / max(st1["host_compute_s"] - st0["host_compute_s"], 1e-9)
+                 "adam_compute_gbs": hb * n_total * K / max(st1["host_compute_s"] - st0["host_compute_s"], 1e-9)
                  / 1e9,
                  "copy_wait_s_per_step": (st1["host_copy_wait_s"] - st0["host_copy_wait_s"]) / K,
                  "slab_wait_s_per_step": (st1["host_wait_s"] - st0["host_wait_s"]) / K,
@@ -509,9 +520,12 @@ def main():
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--host-threads", type=int, default=0)
+    ap.add_argument("--fused-grads", action="store_true",
+                    help="no FP32 gradient array: each slab goes straight into Adam (same arithmetic)")
     ap.add_argument("--overlap", action="store_true",
                     help="overlap_adam = 1: host Adam of a step runs under the next step's device work")
     args = ap.parse_args()
+    args.keep_grads = not args.fused_grads
     if args.kernel == "gemm":
         return run_gemm_kernel(args)
     if args.kernel == "attn":

@@ -206,9 +206,12 @@ def _ptr(a: np.ndarray):
 
 
 class Trainer:
-    """Owns an mt_handle over caller numpy FP32 arrays (master, m, v, grad)."""
+    """Owns an mt_handle over caller numpy FP32 arrays (master, m, v, grad).
 
-    def __init__(self, cfg: Config, master: np.ndarray, m=None, v=None, grad=None):
+    keep_grads=False passes no gradient array: gradients go straight from the
+    staging slabs into Adam (read_grads and accumulation are then refused)."""
+
+    def __init__(self, cfg: Config, master: np.ndarray, m=None, v=None, grad=None, keep_grads: bool = True):
         _, n_total = layout(cfg)
         for a in (master, m, v, grad):
             if a is not None and (a.dtype != np.float32 or a.shape != (n_total,) or not a.flags.c_contiguous):
@@ -218,9 +221,12 @@ class Trainer:
         self.master = master
         self.m = m if m is not None else np.zeros(n_total, np.float32)
         self.v = v if v is not None else np.zeros(n_total, np.float32)
-        self.grad = grad if grad is not None else np.zeros(n_total, np.float32)
+        if not keep_grads and grad is not None:
+            raise ValueError("keep_grads=False takes no gradient array")
+        self.grad = None if not keep_grads else (grad if grad is not None else np.zeros(n_total, np.float32))
         h = C.c_void_p()
-        check(lib().mt_init(C.byref(cfg), _ptr(self.master), _ptr(self.m), _ptr(self.v), _ptr(self.grad),
+        check(lib().mt_init(C.byref(cfg), _ptr(self.master), _ptr(self.m), _ptr(self.v),
+                            _ptr(self.grad) if self.grad is not None else None,
                             n_total, C.byref(h)))
         self.h = h
 

@@ -1,22 +1,27 @@
 // Causal grouped-query attention forward on the 5th-generation tensor cores.
 //
-// One CTA per (128-query tile, head, batch), warp-specialised:
-//   warp 0   TMA producer: Q once, then K and V tiles of 128 keys into a
-//            two-stage ring (3-D tensor map over the qkv rows of one
-//            sequence, so rows past its end arrive as zeros);
-//   warp 1   allocates TMEM and issues tcgen05.mma:
-//              S_j = Q K_j^T      (M 128, N 128, K = hd)  into one of two
-//                                  128-column TMEM buffers,
-//              O  += P_j V_j      (M 128, N = hd, K 128) with P from shared
+// One CTA per (pair of adjacent 128-query tiles, head, batch); the two tiles
+// share every K and V tile the CTA loads. Warp-specialised:
+//   warp 0   TMA producer: both Q tiles once, then K and V tiles of 128 keys
+//            into separate rings (3-D tensor map over the qkv rows of one
+//            sequence, so rows past its end arrive as zeros); K runs one
+//            tile ahead of V;
+//   warp 1   allocates TMEM and issues tcgen05.mma for both tiles t:
+//              S_t = Q_t K_j^T    (M 128, N 128, K = hd) into t's 128-column
+//                                  TMEM buffer, issued as soon as t's softmax
+//                                  has copied S_t of the previous key tile out,
+//              O_t += P_t V_j     (M 128, N = hd, K 128) with P_t from shared
 //                                  memory and V read MN-major in place;
-//   warps 2-9 softmax: two threads per query row (one TMEM lane), each
-//            reading half of the row's 128 scores with tcgen05.ld; the halves
-//            combine their max and sum through shared memory. The causal mask
-//            and the online softmax run in fp32 (log2 domain); P is written as
-//            bf16 into 128-byte-swizzled shared memory (each half fills one
-//            64-key box). O is rescaled in TMEM only when a row's running
-//            maximum grows by more than 2^8, so P stays below 256 and the
-//            final O / l is unchanged.
+//   warps 2-5, 6-9: one softmax group per query tile, one thread per query
+//            row (its TMEM lane) holding the row's 128 scores in registers.
+//            The causal mask and the online softmax run in fp32 (log2
+//            domain); P is written as bf16 into 128-byte-swizzled shared
+//            memory. O is rescaled in TMEM only when a row's running maximum
+//            grows by more than 2^8, so P stays below 256 and the final O / l
+//            is unchanged.
+// While one group exponentiates, the tensor core computes the other group's
+// products and both groups' next scores, so neither the exponential units nor
+// the tensor core waits on a single chain of dependencies.
 // This is the attention of the stateless layer template (zhichai.net
 // article, "以内存为中心的训练新范式" point 4); streaming the keys in tiles keeps
 // its memory O(s), the basis of the long-context runs the travelaiplan blog
@@ -33,9 +38,9 @@
 namespace mt {
 namespace {
 
-constexpr int kQ = 128;                 // queries per CTA (MMA M)
+constexpr int kQ = 128;                 // queries per tile (MMA M)
 constexpr int kKV = 128;                // keys per tile
-constexpr int kThr = 320;               // warp 0 TMA, warp 1 MMA, warps 2-9 softmax
+constexpr int kThr = 320;               // warp 0 TMA, warp 1 MMA, warps 2-9 softmax (two groups)
 constexpr uint32_t kBox = 128 * 128;    // one 64-column x 128-row bf16 box (16 KiB)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescale = 8.0f;        // rescale O only when the max grows by > 2^8
@@ -43,17 +48,17 @@ constexpr float kRescale = 8.0f;        // rescale O only when the max grows by 
 template <int HD>
 struct TcCfg {
   static constexpr int kBoxes = HD / 64;
-  static constexpr uint32_t kTile = kBoxes * kBox;
-  static constexpr uint32_t kQOff = 0;
-  static constexpr uint32_t kKOff = kTile;
-  static constexpr uint32_t kVOff = kKOff + 2 * kTile;
-  static constexpr uint32_t kPOff = kVOff + 2 * kTile;
-  static constexpr uint32_t kPBuf = 2 * kBox;          // one P tile (128 keys)
-  static constexpr uint32_t kBarOff = kPOff + 2 * kPBuf;  // two P buffers
-  static constexpr uint32_t kRedOff = kBarOff + 128;  // [2 halves][128 rows] floats for max / sum
-  // at least 120 KiB so that one CTA (and its 512 TMEM columns) owns the SM
-  static constexpr size_t kSmemRaw = 1024 + kRedOff + 2 * 128 * 4;
-  static constexpr size_t kSmem = kSmemRaw < 122880 ? 122880 : kSmemRaw;
+  static constexpr uint32_t kTile = kBoxes * kBox;     // 128 rows x HD
+  static constexpr int kKS = 2;                        // K ring slots
+  static constexpr int kVS = HD == 64 ? 2 : 1;         // V ring slots (shared memory bound at hd 128)
+  static constexpr uint32_t kQOff = 0;                 // two Q tiles
+  static constexpr uint32_t kKOff = 2 * kTile;
+  static constexpr uint32_t kVOff = kKOff + kKS * kTile;
+  static constexpr uint32_t kPOff = kVOff + kVS * kTile;
+  static constexpr uint32_t kPBuf = 2 * kBox;          // one P tile (128 rows x 128 keys)
+  static constexpr uint32_t kBarOff = kPOff + 2 * kPBuf;
+  static constexpr size_t kSmem = 1024 + kBarOff + 256;
+  static_assert(kSmem <= 232448, "shared memory per block");
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -68,36 +73,45 @@ __global__ void __launch_bounds__(kThr, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
-  uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;   // [2]
-  uint64_t* kv_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;    // [2]
-  uint64_t* s_empty = bars + 7;   // [2]
-  uint64_t* p_full = bars + 9;    // [2]
-  uint64_t* p_empty = bars + 11;  // [2]: PV with that P buffer finished (O current)
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 13);
+  uint64_t* q_full = bars;         // [1]
+  uint64_t* k_full = bars + 1;     // [kKS]
+  uint64_t* k_empty = bars + 3;    // [kKS]
+  uint64_t* v_full = bars + 5;     // [kVS]
+  uint64_t* v_empty = bars + 7;    // [kVS]
+  uint64_t* s_full = bars + 9;     // [2] per tile: S_t written
+  uint64_t* s_empty = bars + 11;   // [2] per tile: S_t copied out by its softmax group
+  uint64_t* p_full = bars + 13;    // [2] per tile: P_t written (and O_t rescaled)
+  uint64_t* p_empty = bars + 15;   // [2] per tile: P_t V finished (O_t current, P_t free)
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 17);
 
   const int nqt = (s + kQ - 1) / kQ;
-  const int qt = nqt - 1 - blockIdx.x;  // heaviest tiles first
+  const int npair = (nqt + 1) / 2;
+  const int pr = npair - 1 - blockIdx.x;  // heaviest pairs first
   const int h = blockIdx.y, b = blockIdx.z;
   const int g = h / (H / Hkv);
-  const int q0 = qt * kQ;
-  const int n_kv = qt + 1;  // causal: key tiles 0..qt
+  const int qt0 = 2 * pr;
+  const int ntile = (qt0 + 1 < nqt) ? 2 : 1;
+  const int nkv[2] = {qt0 + 1, ntile == 2 ? qt0 + 2 : 0};  // causal: key tiles 0..qt
+  const int n_kv = ntile == 2 ? nkv[1] : nkv[0];
   const int qcol = h * HD, kcol = (H + g) * HD, vcol = (H + Hkv + g) * HD;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tm);
     mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 256);
+    for (int i = 0; i < C::kKS; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&p_full[i], 256);
-      mbar_init(&p_empty[i], 1);
+    for (int i = 0; i < C::kVS; ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&s_empty[t], 128);
+      mbar_init(&p_full[t], 128);
+      mbar_init(&p_empty[t], 1);
     }
     fence_barrier_init();
   }
@@ -107,21 +121,49 @@ __global__ void __launch_bounds__(kThr, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   const uint32_t tS[2] = {tmem, tmem + 128};
-  const uint32_t tO = tmem + 256;
+  const uint32_t tO[2] = {tmem + 256, tmem + 256 + HD};
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ loads
-      mbar_arrive_expect_tx(q_full, C::kTile);
-      for (int bx = 0; bx < C::kBoxes; ++bx)
-        tma_load_3d(sm + C::kQOff + bx * kBox, &tm, qcol + bx * 64, q0, b, q_full);
-      for (int j = 0; j < n_kv; ++j) {
-        const int st = j & 1;
-        if (!mbar_wait(&kv_empty[st], ((j >> 1) & 1) ^ 1, err)) break;
-        mbar_arrive_expect_tx(&kv_full[st], 2 * C::kTile);
-        for (int bx = 0; bx < C::kBoxes; ++bx) {
-          tma_load_3d(sm + C::kKOff + st * C::kTile + bx * kBox, &tm, kcol + bx * 64, j * kKV, b, &kv_full[st]);
-          tma_load_3d(sm + C::kVOff + st * C::kTile + bx * kBox, &tm, vcol + bx * 64, j * kKV, b, &kv_full[st]);
+      int nk = 0, nv = 0;  // tiles issued into each ring
+      bool ok = true;
+      auto load_k = [&](int j) -> bool {
+        const int st = j % C::kKS, use = j / C::kKS;
+        if (!mbar_wait(&k_empty[st], (use & 1) ^ 1, err)) return false;
+        mbar_arrive_expect_tx(&k_full[st], C::kTile);
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+          tma_load_3d(sm + C::kKOff + st * C::kTile + bx * kBox, &tm, kcol + bx * 64, j * kKV, b, &k_full[st]);
+        ++nk;
+        return true;
+      };
+      auto load_v = [&](int j) -> bool {
+        const int st = j % C::kVS, use = j / C::kVS;
+        if (!mbar_wait(&v_empty[st], (use & 1) ^ 1, err)) return false;
+        mbar_arrive_expect_tx(&v_full[st], C::kTile);
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+          tma_load_3d(sm + C::kVOff + st * C::kTile + bx * kBox, &tm, vcol + bx * 64, j * kKV, b, &v_full[st]);
+        ++nv;
+        return true;
+      };
+      mbar_arrive_expect_tx(q_full, ntile * C::kTile);
+      for (int t = 0; t < ntile; ++t)
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+          tma_load_3d(sm + C::kQOff + t * C::kTile + bx * kBox, &tm, qcol + bx * 64, (qt0 + t) * kQ, b, q_full);
+      for (int j = 0; ok && j <= n_kv; ++j) {
+        if (j < n_kv) ok = load_k(j);
+        if (ok && j > 0) ok = load_v(j - 1);
+      }
+      if (!ok) {
+        // wait (bounded) for this CTA's copies still in flight before it exits
+        mbar_wait(q_full, 0, err);
+        for (int i = 0; i < C::kKS && i < nk; ++i) {
+          const int last = nk - 1 - ((nk - 1 - i) % C::kKS);  // last tile issued into slot last % kKS
+          mbar_wait(&k_full[last % C::kKS], (last / C::kKS) & 1, err);
+        }
+        for (int i = 0; i < C::kVS && i < nv; ++i) {
+          const int last = nv - 1 - ((nv - 1 - i) % C::kVS);
+          mbar_wait(&v_full[last % C::kVS], (last / C::kVS) & 1, err);
         }
       }
     }
@@ -130,117 +172,117 @@ __global__ void __launch_bounds__(kThr, 1)
       // ------------------------------------------------------------- MMAs
       constexpr uint32_t idesc_s = idesc_bf16_f32(kQ, kKV, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kQ, HD, false, true);
-      const uint32_t sQ = smem_u32(sm + C::kQOff);
-      const uint32_t sP = smem_u32(sm + C::kPOff);
       bool ok = mbar_wait(q_full, 0, err);
+      // S_t(j) for both tiles that still need key tile j, then release K_j
       auto issue_s = [&](int j) -> bool {
-        const int st = j & 1;
-        if (!mbar_wait(&kv_full[st], (j >> 1) & 1, err)) return false;
-        if (!mbar_wait(&s_empty[st], ((j >> 1) & 1) ^ 1, err)) return false;
-        tc_fence_after();
+        const int st = j % C::kKS;
+        if (!mbar_wait(&k_full[st], (j / C::kKS) & 1, err)) return false;
         const uint32_t sK = smem_u32(sm + C::kKOff + st * C::kTile);
+        for (int t = 0; t < 2; ++t) {
+          if (j >= nkv[t]) continue;
+          // the group has copied S_t(j-1) out of TMEM
+          if (j > 0 && !mbar_wait(&s_empty[t], (j - 1) & 1, err)) return false;
+          tc_fence_after();
+          const uint32_t sQ = smem_u32(sm + C::kQOff + t * C::kTile);
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-          tc_mma_bf16(tS[st], smem_desc_kmajor_sw128(sQ + off), smem_desc_kmajor_sw128(sK + off), idesc_s,
-                      kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+            tc_mma_bf16(tS[t], smem_desc_kmajor_sw128(sQ + off), smem_desc_kmajor_sw128(sK + off), idesc_s,
+                        kk > 0 ? 1u : 0u);
+          }
+          tc_commit(&s_full[t]);
         }
-        tc_commit(&s_full[st]);
+        tc_commit(&k_empty[st]);
         return true;
       };
       if (ok) ok = issue_s(0);
       for (int j = 0; ok && j < n_kv; ++j) {
-        if (j + 1 < n_kv && !issue_s(j + 1)) break;
-        if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1, err)) break;
-        tc_fence_after();
-        const uint32_t sV = smem_u32(sm + C::kVOff + (j & 1) * C::kTile);
-        const uint32_t sPj = sP + (j & 1) * C::kPBuf;
+        if (j + 1 < n_kv && !(ok = issue_s(j + 1))) break;
+        const int vs = j % C::kVS;
+        if (!(ok = mbar_wait(&v_full[vs], (j / C::kVS) & 1, err))) break;
+        const uint32_t sV = smem_u32(sm + C::kVOff + vs * C::kTile);
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j >= nkv[t]) continue;
+          if (!(ok = mbar_wait(&p_full[t], j & 1, err))) break;
+          tc_fence_after();
+          const uint32_t sP = smem_u32(sm + C::kPOff + t * C::kPBuf);
 #pragma unroll
-        for (int kk = 0; kk < kKV / 16; ++kk) {
-          const uint32_t aoff = (kk >> 2) * kBox + (kk & 3) * 32;
-          tc_mma_bf16(tO, smem_desc_kmajor_sw128(sPj + aoff), smem_desc_mnmajor_sw128(sV + kk * 2048, kBox), idesc_pv,
-                      (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kKV / 16; ++kk) {
+            const uint32_t aoff = (kk >> 2) * kBox + (kk & 3) * 32;
+            tc_mma_bf16(tO[t], smem_desc_kmajor_sw128(sP + aoff), smem_desc_mnmajor_sw128(sV + kk * 2048, kBox),
+                        idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(&p_empty[t]);
         }
-        tc_commit(&p_empty[j & 1]);
-        tc_commit(&kv_empty[j & 1]);
+        if (ok) tc_commit(&v_empty[vs]);
       }
     }
   } else {
     // ------------------------------------------------------------ softmax
+    const int t = (warp - 2) >> 2;          // query tile of this group
     const int q = warp & 3;                 // TMEM lane quarter
-    const int half = (warp - 2) >> 2;       // which 64 keys / which half of O
     const int row = q * 32 + lane;
-    const int qpos = q0 + row;
+    const int qpos = (qt0 + t) * kQ + row;
+    const int nk = nkv[t];
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const float sc = rsqrtf((float)HD) * kLog2e;
-    float* red = reinterpret_cast<float*>(sm + C::kRedOff);  // [2][128]
     float m_ref = -INFINITY, l = 0.f;
-    uint8_t* sP = sm + C::kPOff + half * kBox;
-    constexpr int kOCols = HD / 2;          // O columns this thread rescales / stores
-    auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(1 + q) : "memory"); };
+    uint8_t* sP = sm + C::kPOff + t * C::kPBuf;
+    const uint32_t rsw = (uint32_t)(row & 7);
     bool ok = true;
-    for (int j = 0; j < n_kv && ok; ++j) {
-      const int st = j & 1;
-      if (!mbar_wait(&s_full[st], (j >> 1) & 1, err)) { ok = false; break; }
+    for (int j = 0; j < nk && ok; ++j) {
+      if (!mbar_wait(&s_full[t], j & 1, err)) { ok = false; break; }
       tc_fence_after();
-      uint32_t r[2][32];
+      uint32_t r[4][32];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) tmem_ld_32x32b_x32(tS[st] + lane_off + half * 64 + c * 32, r[c]);
+      for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tS[t] + lane_off + c * 32, r[c]);
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(&s_empty[st]);
-      // raw scores; only the diagonal tile (the last one) needs the causal mask
-      float v[64];
-      float mraw = -INFINITY;
-      if (j == n_kv - 1) {
-        const int kbase = j * kKV + half * 64;
+      mbar_arrive(&s_empty[t]);
+      // only the diagonal tile (the last one) needs the causal mask
+      if (j == nk - 1) {
+        const int kbase = j * kKV;
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float x = (kbase + c * 32 + i > qpos) ? -INFINITY : __uint_as_float(r[c][i]);
-            v[c * 32 + i] = x;
-            mraw = fmaxf(mraw, x);
-          }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            v[c * 32 + i] = __uint_as_float(r[c][i]);
-            mraw = fmaxf(mraw, v[c * 32 + i]);
-          }
+          for (int i = 0; i < 32; ++i)
+            if (kbase + c * 32 + i > qpos) r[c][i] = __float_as_uint(-INFINITY);
       }
-      float mx = mraw * sc;  // row max in the scaled log2 domain (sc > 0)
-      red[half * 128 + row] = mx;
-      pair_sync();
-      mx = fmaxf(mx, red[(half ^ 1) * 128 + row]);
+      float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          m0 = fmaxf(m0, __uint_as_float(r[c][i]));
+          m1 = fmaxf(m1, __uint_as_float(r[c][i + 1]));
+        }
+      const float mx = fmaxf(m0, m1) * sc;  // row max in the scaled log2 domain (sc > 0)
       if (j == 0) m_ref = mx;
       const bool need = j > 0 && mx > m_ref + kRescale;
       const float m_use = need ? mx : m_ref;
-      // P = exp2(v - m_use) as packed bf16, computed before any wait
-      uint32_t pk[32];
+      // P = exp2(s * sc - m_use), packed to bf16 in place
       float lt0 = 0.f, lt1 = 0.f;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float p0 = ex2_approx(fmaf(v[2 * i], sc, -m_use));
-        const float p1 = ex2_approx(fmaf(v[2 * i + 1], sc, -m_use));
-        lt0 += p0;
-        lt1 += p1;
-        pk[i] = pack_bf16x2(p0, p1);
-      }
-      const float lt = lt0 + lt1;
-      // this P buffer was last read by PV_{j-2}
-      if (j >= 2 && !mbar_wait(&p_empty[st], ((j >> 1) - 1) & 1, err)) { ok = false; break; }
-      if (__any_sync(0xffffffffu, need)) {
-        // O must be current (PV_{j-1} finished) before it is rescaled
-        if (!mbar_wait(&p_empty[(j - 1) & 1], ((j - 1) >> 1) & 1, err)) { ok = false; break; }
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(r[c][2 * i]), sc, -m_use));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(r[c][2 * i + 1]), sc, -m_use));
+          lt0 += p0;
+          lt1 += p1;
+          r[c][i] = pack_bf16x2(p0, p1);
+        }
+      // P_t(j-1) V has finished: O_t is current and the P buffer is free
+      if (j > 0) {
+        if (!mbar_wait(&p_empty[t], (j - 1) & 1, err)) { ok = false; break; }
         tc_fence_after();
+      }
+      if (__any_sync(0xffffffffu, need)) {
         const float factor = need ? exp2f(m_ref - mx) : 1.f;
 #pragma unroll 1
-        for (int c = 0; c < kOCols / 32; ++c) {
+        for (int c = 0; c < HD / 32; ++c) {
           uint32_t ov[32];
-          const uint32_t ta = tO + lane_off + half * kOCols + c * 32;
+          const uint32_t ta = tO[t] + lane_off + c * 32;
           tmem_ld_32x32b_x32(ta, ov);
           tmem_ld_wait();
 #pragma unroll
@@ -252,36 +294,30 @@ __global__ void __launch_bounds__(kThr, 1)
           l *= factor;
           m_ref = mx;
         }
-      } else if (j >= 2) {
-        tc_fence_after();
       }
-      l += lt;
-      // write this half's 64-key box of P buffer st (128-byte swizzle)
-      uint8_t* sPb = sP + st * C::kPBuf;
-      const uint32_t rsw = (uint32_t)(row & 7);
+      l += lt0 + lt1;
+      // the row's 128 keys: two 64-key boxes of 128-byte rows, 128-byte swizzle
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 u = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        *reinterpret_cast<uint4*>(sPb + row * 128 + (((uint32_t)c ^ rsw) * 16)) = u;
-      }
+      for (int bx = 0; bx < 2; ++bx)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int w0 = bx * 32 + 4 * c;  // packed word index in the row
+          const uint4 u = make_uint4(r[w0 >> 4][w0 & 15], r[(w0 + 1) >> 4][(w0 + 1) & 15],
+                                     r[(w0 + 2) >> 4][(w0 + 2) & 15], r[(w0 + 3) >> 4][(w0 + 3) & 15]);
+          *reinterpret_cast<uint4*>(sP + bx * kBox + row * 128 + (((uint32_t)c ^ rsw) * 16)) = u;
+        }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&p_full[st]);
-      pair_sync();  // both halves read red[] before it is rewritten
+      mbar_arrive(&p_full[t]);
     }
-    if (ok) {
-      red[half * 128 + row] = l;
-      pair_sync();
-      l += red[(half ^ 1) * 128 + row];
-    }
-    if (ok && mbar_wait(&p_empty[(n_kv - 1) & 1], ((n_kv - 1) >> 1) & 1, err)) {
+    if (ok && nk > 0 && mbar_wait(&p_empty[t], (nk - 1) & 1, err)) {
       tc_fence_after();
       const float inv = 1.f / l;
-      bf16* orow = o + ((long long)b * s + qpos) * ldo + (long long)h * HD + half * kOCols;
+      bf16* orow = o + ((long long)b * s + qpos) * ldo + (long long)h * HD;
 #pragma unroll 1
-      for (int c = 0; c < kOCols / 32; ++c) {
+      for (int c = 0; c < HD / 32; ++c) {
         uint32_t ov[32];
-        tmem_ld_32x32b_x32(tO + lane_off + half * kOCols + c * 32, ov);
+        tmem_ld_32x32b_x32(tO[t] + lane_off + c * 32, ov);
         tmem_ld_wait();
         if (qpos < s) {
 #pragma unroll
@@ -295,7 +331,7 @@ __global__ void __launch_bounds__(kThr, 1)
           }
         }
       }
-      if (qpos < s && half == 0) lse[((long long)b * H + h) * s + qpos] = (m_ref + log2f(l)) / kLog2e;
+      if (qpos < s) lse[((long long)b * H + h) * s + qpos] = (m_ref + log2f(l)) / kLog2e;
     }
   }
 
@@ -340,7 +376,7 @@ int attn_fwd_tc(const void* qkv, long long ld, void* o, long long ldo, float* ls
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return MT_EINVAL;
-  dim3 grid((s + kQ - 1) / kQ, H, B);
+  dim3 grid(((s + kQ - 1) / kQ + 1) / 2, H, B);
   int* err = device_error_word();
   if (hd == 64)
     attn_fwd_tc_kernel<64><<<grid, kThr, TcCfg<64>::kSmem, stream>>>(tm, (bf16*)o, ldo, lse, s, H, Hkv, err);

@@ -256,7 +256,7 @@ void worker_main(mt_handle* h) {
       a.w = h->master + off;
       a.m = h->adam_m + off;
       a.v = h->adam_v + off;
-      a.grad_out = h->grad + off;
+      a.grad_out = h->grad ? h->grad + off : nullptr;
       a.grad_in = nullptr;
       a.slab = h->staging[job.slab];
       a.store = h->store + off;
@@ -774,7 +774,7 @@ int mt_init(const mt_config* cfg, float* master, float* adam_m, float* adam_v, f
   *out = nullptr;
   const char* why = nullptr;
   if (!cfg || !config_valid(*cfg, &why)) return fail(nullptr, MT_EINVAL, why ? why : "null config");
-  if (!master || !adam_m || !adam_v || !grad) return fail(nullptr, MT_EINVAL, "null host state array");
+  if (!master || !adam_m || !adam_v) return fail(nullptr, MT_EINVAL, "null host state array");
   mt_handle* h = new (std::nothrow) mt_handle();
   if (!h) return fail(nullptr, MT_ENOMEM, "out of host memory");
   h->cfg = *cfg;
@@ -882,6 +882,8 @@ static int run_step(mt_handle* h, const int32_t* tokens, const int32_t* labels, 
   const auto t0 = Clock::now();
   if (n_micro < 1 || micro_index < 0 || micro_index >= n_micro)
     return fail(h, MT_EINVAL, "micro_index must lie in [0, n_micro)");
+  if (n_micro > 1 && !h->grad)
+    return fail(h, MT_ESTATE, "accumulation over micro-batches needs the FP32 gradient array at mt_init");
   Step st{h, B, s, M, h->t + 1};
   st.acc = micro_index > 0;
   st.adam = micro_index == n_micro - 1;
@@ -1017,6 +1019,7 @@ int mt_sync(mt_handle* h) {
 
 int mt_read_grads(mt_handle* h, float* dst, int64_t n) {
   if (!h || !dst || n < 0 || n > h->n_total) return fail(h, MT_EINVAL, "bad arguments to mt_read_grads");
+  if (!h->grad) return fail(h, MT_ESTATE, "no FP32 gradient array: gradients went straight into Adam");
   if (const int r = mt_sync(h)) return r;
   if (dst != h->grad) std::memcpy(dst, h->grad, sizeof(float) * n);
   return MT_OK;

@@ -114,10 +114,17 @@ void emit_bf16(const float* src, uint16_t* dst, int64_t n, int threads) {
   for (int64_t i = 0; i < n; ++i) dst[i] = rne_bits(src[i]);
 }
 
-// One streaming pass per element: gradient in (bf16 slab or fp32, optionally
-// added to the running sum in grad_out and scaled), gradient out, m, v, w
-// updated, bf16 copy of w out. The variants are compile-time so the loop
-// body has no control flow.
+// Per element: gradient in (bf16 slab or fp32, optionally added to the
+// running sum in grad_out and scaled), gradient out, m, v, w updated, bf16
+// copy of w out. The variants are compile-time so the loop bodies have no
+// control flow. Each thread walks its contiguous range in chunks; when the
+// gradient is stored, a chunk is done in two sweeps: the gradient sweep
+// writes grad_out, then the optimizer sweep reads it back while it is still
+// in the core's cache. Host memory sees the same bytes as one fused sweep,
+// but no sweep interleaves six streams, which on the Grace host makes the
+// pair about a quarter faster than the fused loop (measured, 16 cores).
+constexpr int64_t kAdamChunk = 65536;
+
 template <bool kSlab, bool kGradOut, bool kStore, bool kAcc>
 static void adam_loop(const AdamArgs& a, int threads) {
   const double bc1 = 1.0 - std::pow((double)a.beta1, (double)a.t);
@@ -135,19 +142,31 @@ static void adam_loop(const AdamArgs& a, int threads) {
   const uint16_t* __restrict__ slab = a.slab;
   uint16_t* __restrict__ store = a.store;
   const int64_t n = a.n;
-#pragma omp parallel for schedule(static) num_threads(threads)
-  for (int64_t i = 0; i < n; ++i) {
-    float g = kSlab ? bf16_to_f32(slab[i]) : gin[i];
-    if (kAcc) g = (gout[i] + g) * gs;
-    if (kGradOut) gout[i] = g;
-    const float mi = b1 * m[i] + c1 * g;
-    const float vi = b2 * v[i] + c2 * g * g;
-    m[i] = mi;
-    v[i] = vi;
-    // m_hat / (sqrt(v_hat) + eps) with m_hat = m / bc1, v_hat = v / bc2
-    const float wi = w[i] - lr * (mi * inv_bc1) / (std::sqrt(vi) * inv_sqrt_bc2 + eps);
-    w[i] = wi;
-    if (kStore) store[i] = rne_bits(wi);
+#pragma omp parallel num_threads(threads)
+  {
+    const int nt = omp_get_num_threads(), tid = omp_get_thread_num();
+    const int64_t r0 = n * tid / nt, r1 = n * (tid + 1) / nt;
+    for (int64_t c0 = r0; c0 < r1; c0 += kAdamChunk) {
+      const int64_t c1e = c0 + kAdamChunk < r1 ? c0 + kAdamChunk : r1;
+      if (kGradOut) {
+        for (int64_t i = c0; i < c1e; ++i) {
+          float g = kSlab ? bf16_to_f32(slab[i]) : gin[i];
+          if (kAcc) g = (gout[i] + g) * gs;
+          gout[i] = g;
+        }
+      }
+      for (int64_t i = c0; i < c1e; ++i) {
+        const float g = kGradOut ? gout[i] : (kSlab ? bf16_to_f32(slab[i]) : gin[i]);
+        const float mi = b1 * m[i] + c1 * g;
+        const float vi = b2 * v[i] + c2 * g * g;
+        m[i] = mi;
+        v[i] = vi;
+        // m_hat / (sqrt(v_hat) + eps) with m_hat = m / bc1, v_hat = v / bc2
+        const float wi = w[i] - lr * (mi * inv_bc1) / (std::sqrt(vi) * inv_sqrt_bc2 + eps);
+        w[i] = wi;
+        if (kStore) store[i] = rne_bits(wi);
+      }
+    }
   }
 }
 

@@ -50,9 +50,13 @@ def streamed_units(n_layers: int, ckpt_interval: int) -> list[int]:
 
 
 def estimate(shape, batch: int | None = None, seq: int | None = None, ckpt_interval: int | None = None,
-             n_slabs: int | None = None, gemm_tflops: float = 1500.0, host_gbs: float = 150.0,
-             link_gbs: float = 170.0) -> dict:
-    """Memory (exact) and per-step traffic, FLOPs and lower-bound times."""
+             n_slabs: int | None = None, keep_grads: bool = True, gemm_tflops: float = 1500.0,
+             host_gbs: float = 150.0, link_gbs: float = 170.0) -> dict:
+    """Memory (exact) and per-step traffic, FLOPs and lower-bound times.
+
+    keep_grads=False is a handle made without the FP32 gradient array: 12
+    instead of 16 bytes of host state per parameter, 28 instead of 32 bytes
+    of host DRAM traffic per parameter and step."""
     B = batch or shape.batch
     s = seq or shape.seq
     cfg = mt.make_config(shape, batch=B, seq=s, ckpt_interval=ckpt_interval, n_slabs=n_slabs)
@@ -66,13 +70,14 @@ def estimate(shape, batch: int | None = None, seq: int | None = None, ckpt_inter
     flops = model_flops(shape, B, s)
     hw_flops = flops + flops * (1.0 / 3.0)          # recompute adds one forward (about 1/3 of 6N)
     t_gpu = hw_flops / (gemm_tflops * 1e12)
-    t_host = 32.0 * n_total / (host_gbs * 1e9)
+    state = plan["host_state_bytes"] if keep_grads else plan["host_state_bytes"] * 12 // 16
+    t_host = (32.0 if keep_grads else 28.0) * n_total / (host_gbs * 1e9)
     t_link = max(h2d, d2h) / (link_gbs * 1e9)
     return {
         "params": n_total, "tokens_per_step": B * s,
         "device_bytes": plan["device_bytes"], "pinned_bytes": plan["pinned_bytes"],
-        "host_state_bytes": plan["host_state_bytes"],
-        "host_total_bytes": plan["host_state_bytes"] + plan["pinned_bytes"],
+        "host_state_bytes": state,
+        "host_total_bytes": state + plan["pinned_bytes"],
         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
         "model_flops_per_step": flops,
         "t_gpu_s": t_gpu, "t_host_s": t_host, "t_link_s": t_link,

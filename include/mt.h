@@ -130,15 +130,21 @@ int mt_unit_range(const mt_config* cfg, int unit, int64_t* offset, int64_t* leng
  * Memory plan of `cfg` without a GPU and without allocating: device bytes of
  * the handle's arena (weight buffers, slabs, checkpoints, activations,
  * scratch; the same planner mt_init uses), pinned host bytes (bf16 store,
- * staging slabs, token staging) and the caller's FP32 state (master, m, v,
- * grad = 16 bytes per element). Any pointer may be NULL.
+ * staging slabs, token staging) and the caller's FP32 state with the
+ * gradient array (master, m, v, grad = 16 bytes per element; 12 without
+ * the gradient array). Any pointer may be NULL.
  */
 int mt_plan(const mt_config* cfg, int64_t* device_bytes, int64_t* pinned_bytes, int64_t* host_state_bytes);
 
 /*
  * Creates a handle. master, adam_m, adam_v, grad are caller-owned FP32 host
  * arrays of n_total elements in the flat layout; they must stay valid until
- * mt_destroy. The caller initialises master and zeroes m and v. The library
+ * mt_destroy. The caller initialises master and zeroes m and v. grad may be
+ * NULL: each unit's bf16 gradient then goes straight from its staging slab
+ * into Adam (the same arithmetic; the host holds FP32 master, m and v, the
+ * 12 bytes per parameter of the lqnn.cn article's section 一, and no FP32
+ * gradient stream crosses host memory); mt_read_grads then returns
+ * MT_ESTATE and mt_train_step_accum accepts only n_micro = 1. The library
  * allocates the pinned bf16 flat store (filled with round-to-nearest-even
  * bf16 of master), the pinned staging slabs, all device memory and the
  * three streams, and starts the host worker thread. Returns MT_ENOMEM,
@@ -173,12 +179,14 @@ int mt_train_step_device(mt_handle* h, const int32_t* d_tokens, const int32_t* d
  * (so `grad` holds the mean, the gradient of the mean loss over all
  * micro-batches of equal size) and applies one Adam step (t += 1). A
  * non-finite loss in any micro-step skips that Adam step. mt_train_step is
- * the n_micro = 1 case.
+ * the n_micro = 1 case. n_micro > 1 needs the gradient array (MT_ESTATE
+ * without it).
  */
 int mt_train_step_accum(mt_handle* h, const int32_t* tokens, const int32_t* labels, int32_t batch, int32_t seq,
                         int32_t micro_index, int32_t n_micro, float* loss_out);
 
-/* Copies the FP32 gradient of the last step (n elements, n <= n_total). */
+/* Copies the FP32 gradient of the last step (n elements, n <= n_total).
+ * MT_ESTATE when the handle was created without a gradient array. */
 int mt_read_grads(mt_handle* h, float* dst, int64_t n);
 
 /* Waits until the host worker has finished every queued unit (Adam of the

@@ -9,14 +9,19 @@ from host_memory_resident_gb300 import resources
 def test_host_state_matches_the_pages_sizing_rules():
     e7 = resources.estimate(synth.workload("7b"))
     n = e7["params"]
-    # FP32 master + m + v: 12 bytes per parameter, "about 84 GB" at 7B
-    # (zhichai.net article, introduction; lqnn.cn article section 一: ~12 GB per 1B)
-    master_m_v = e7["host_state_bytes"] * 12 // 16
+    # FP32 master + m + v: 12 bytes per parameter, about 12 GB per billion
+    # parameters (lqnn.cn article, section 一), so about 81 GB at 7B
+    master_m_v = resources.estimate(synth.workload("7b"), keep_grads=False)["host_state_bytes"]
     assert master_m_v == 12 * n
     assert 80e9 < master_m_v < 84e9
-    # full precision with the gradient: 16 bytes per parameter, so 70B needs
-    # about 1.1 TB (travelaiplan blog, 核心功能 point 1)
-    assert 16 * 70e9 == pytest.approx(1.12e12)
+    # full precision with the gradient: parameters x 4 bytes x about 4, so a
+    # 70B model needs about 1.1 TB (travelaiplan blog, 核心功能 point 1); a
+    # Llama-2-70B-shaped decoder here
+    s70 = synth.workload("7b").with_(n_layers=80, d_model=8192, n_heads=64, n_kv_heads=8, ffn_dim=28672)
+    e70 = resources.estimate(s70, batch=1, seq=4096)
+    assert 68e9 < e70["params"] < 70e9
+    assert e70["host_state_bytes"] == 16 * e70["params"]
+    assert 1.05e12 < e70["host_state_bytes"] < 1.15e12
     assert e7["host_state_bytes"] == 16 * n
     # the bf16 store is 2 bytes per parameter (lqnn.cn section 一: 120B -> ~240 GB)
     assert e7["pinned_bytes"] >= 2 * n

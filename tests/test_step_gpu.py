@@ -405,3 +405,31 @@ def test_planner_matches_the_live_handle(tiny, streamed):
         st = tr.stats()
     assert p["device_bytes"] == st["device_bytes"]
     assert p["pinned_bytes"] == st["pinned_bytes"]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("overlap", [False, True])
+def test_without_gradient_array_results_are_identical(tiny, overlap):
+    """A handle made without the FP32 gradient array feeds each slab straight
+    into Adam: after two steps master, m and v are bitwise
+    those of a handle that keeps the array; reading gradients and
+    accumulating over micro-batches are refused."""
+    shape = tiny.with_(n_layers=3, ckpt_interval=2)
+    lay, master, _, _ = _setup(shape)
+    batches = [synth.make_tokens(shape.vocab, shape.batch, shape.seq, seed=9, step=i) for i in range(2)]
+    out = []
+    for keep in (True, False):
+        w = master.copy()
+        with mt.Trainer(mt.make_config(shape, overlap_adam=overlap), w, keep_grads=keep) as tr:
+            losses = [tr.step(tk, lb) for tk, lb in batches]
+            tr.sync()
+            if not keep:
+                with pytest.raises(mt.MtError):
+                    tr.read_grads()
+                tk, lb = batches[0]
+                with pytest.raises(mt.MtError):
+                    tr.step_accum(tk, lb, 0, 2)
+            out.append((losses, w.copy(), tr.m.copy(), tr.v.copy()))
+    assert out[0][0] == out[1][0]
+    for a, b in zip(out[0][1:], out[1][1:]):
+        assert np.array_equal(a, b)
