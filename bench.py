@@ -452,7 +452,11 @@ def run_ours(args, shape, world, rank, local, pg):
     prof_out = {k: {"launches": v["launches"], "ms_per_step": v["ms"] / K,
                     "tflops": (v["flops"] / (v["ms"] / 1e3) / 1e12) if v["flops"] and v["ms"] else None,
                     "gbs": (v["bytes"] / (v["ms"] / 1e3) / 1e9) if v["bytes"] and v["ms"] else None}
-                for k, v in prof.items() if v["launches"]}
+                for k, v in prof.items() if v["launches"] and k not in ("h2d", "d2h")}
+    copies = {k: {"copies_per_step": prof[k]["launches"] / K, "ms_per_step": prof[k]["ms"] / K,
+                  "gb_per_step": prof[k]["bytes"] / K / 1e9,
+                  "gbs_while_copying": prof[k]["bytes"] / (prof[k]["ms"] / 1e3) / 1e9 if prof[k]["ms"] else None}
+              for k in ("h2d", "d2h") if k in prof}
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -481,6 +485,7 @@ def run_ours(args, shape, world, rank, local, pg):
                                "reaches alone on one layer-sized slice; the north-star roofline leaves this "
                                "bound out"},
         "kernels": prof_out,
+        "copies": copies,
         "host": {"adam_s_per_step": (st1["host_adam_s"] - st0["host_adam_s"]) / K,
                  "adam_compute_s_per_step": (st1["host_compute_s"] - st0["host_compute_s"]) / K,
                  "adam_compute_gbs": hb * n_total * K / max(st1["host_compute_s"] - st0["host_compute_s"], 1e-9)

@@ -53,12 +53,13 @@ class Stats(C.Structure):
                 ("kernel_launches", C.c_int64), ("host_compute_s", C.c_double), ("host_copy_wait_s", C.c_double)]
 
 
-PROF_CLASSES = ["gemm", "attn_fwd", "attn_bwd", "norm", "rope", "swiglu", "transpose", "ce", "embed", "other"]
+PROF_CLASSES = ["gemm", "attn_fwd", "attn_bwd", "norm", "rope", "swiglu", "transpose", "ce", "embed", "other",
+                "h2d", "d2h"]
 
 
 class KernelProfile(C.Structure):
-    _fields_ = [("launches", C.c_int64 * 10), ("ms", C.c_double * 10), ("flops", C.c_double * 10),
-                ("bytes", C.c_double * 10)]
+    _fields_ = [("launches", C.c_int64 * len(PROF_CLASSES)), ("ms", C.c_double * len(PROF_CLASSES)),
+                ("flops", C.c_double * len(PROF_CLASSES)), ("bytes", C.c_double * len(PROF_CLASSES))]
 
 
 EXPORTS = [

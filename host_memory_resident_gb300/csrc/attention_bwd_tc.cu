@@ -99,9 +99,10 @@ __global__ void __launch_bounds__(kThr, 1)
   uint64_t* ld_full = bars + 1;      // [2] Q + dO stage
   uint64_t* ld_empty = bars + 3;     // [2]
   uint64_t* s_full = bars + 5;       // S^T and dP^T in TMEM
-  uint64_t* p_full = bars + 6;       // P^T, dS^T written (TMEM read)
+  uint64_t* p_full = bars + 6;       // P^T, dS^T written
   uint64_t* p_empty = bars + 7;      // dV, dK MMAs done with them
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 8);
+  uint64_t* s_empty = bars + 8;      // S^T and dP^T copied out of TMEM
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 9);
   float* vec = reinterpret_cast<float*>(sm + C::kVecOff);
 
   const int nt = (s + kT - 1) / kT;
@@ -124,6 +125,7 @@ __global__ void __launch_bounds__(kThr, 1)
     mbar_init(s_full, 1);
     mbar_init(p_full, 256);
     mbar_init(p_empty, 1);
+    mbar_init(s_empty, 256);
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(tmem_holder, 512);
@@ -160,11 +162,12 @@ __global__ void __launch_bounds__(kThr, 1)
       const uint32_t sK = smem_u32(sm + C::kKOff), sV = smem_u32(sm + C::kVOff);
       const uint32_t sP = smem_u32(sm + C::kPOff), sDS = smem_u32(sm + C::kDSOff);
       bool ok = mbar_wait(kv_full, 0, err);
-      for (int it = 0; ok && it < total; ++it) {
-        const int st = it % C::kStages, use = it / C::kStages;
-        if (!mbar_wait(&ld_full[st], use & 1, err)) break;
-        // S^T / dP^T TMEM is free once the previous iteration's softmax read it
-        if (it > 0 && !mbar_wait(p_full, (it - 1) & 1, err)) break;
+      // S^T / dP^T of query tile `it` (its Q and dO stage loaded, the TMEM
+      // they overwrite copied out by the element-wise warps)
+      auto issue_s = [&](int it) -> bool {
+        const int st = it % C::kStages;
+        if (!mbar_wait(&ld_full[st], (it / C::kStages) & 1, err)) return false;
+        if (it > 0 && !mbar_wait(s_empty, (it - 1) & 1, err)) return false;
         tc_fence_after();
         const uint32_t sQ = smem_u32(sm + C::kQOff + st * 2 * C::kTile), sO = sQ + C::kTile;
 #pragma unroll
@@ -174,8 +177,14 @@ __global__ void __launch_bounds__(kThr, 1)
           tc_mma_bf16(tdP, smem_desc_kmajor_sw128(sV + off), smem_desc_kmajor_sw128(sO + off), id_s, kk > 0);
         }
         tc_commit(s_full);
-        if (!mbar_wait(p_full, it & 1, err)) break;
+        return true;
+      };
+      // dV += P^T dO, dK += dS^T Q for query tile `it`, then free its stage
+      auto issue_g = [&](int it) -> bool {
+        const int st = it % C::kStages;
+        if (!mbar_wait(p_full, it & 1, err)) return false;
         tc_fence_after();
+        const uint32_t sQ = smem_u32(sm + C::kQOff + st * 2 * C::kTile), sO = sQ + C::kTile;
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk) {
           const uint32_t aoff = (kk >> 2) * kBox + (kk & 3) * 32;
@@ -186,6 +195,19 @@ __global__ void __launch_bounds__(kThr, 1)
         }
         tc_commit(p_empty);
         tc_commit(&ld_empty[st]);
+        return true;
+      };
+      if (ok && total > 0) ok = issue_s(0);
+      for (int it = 0; ok && it < total; ++it) {
+        if (C::kStages >= 2) {
+          // the next tile's scores overlap this tile's element-wise work
+          if (it + 1 < total && !(ok = issue_s(it + 1))) break;
+          ok = issue_g(it);
+        } else {
+          // one Q/dO stage: the next tile's loads need this tile's products done
+          if (!(ok = issue_g(it))) break;
+          if (it + 1 < total) ok = issue_s(it + 1);
+        }
       }
     }
   } else {
@@ -217,6 +239,8 @@ __global__ void __launch_bounds__(kThr, 1)
         tmem_ld_32x32b_x32(tdP + lane_off + half * 64 + c * 32, rp[c]);
       }
       tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(s_empty);
       const bool diag = (q0 == k0);
       uint32_t pk[32], dk[32];
 #pragma unroll
@@ -290,7 +314,8 @@ __global__ void __launch_bounds__(kThr, 1)
   uint64_t* s_full = bars + 5;
   uint64_t* p_full = bars + 6;
   uint64_t* p_empty = bars + 7;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 8);
+  uint64_t* s_empty = bars + 8;   // S and dP copied out of TMEM
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 9);
 
   const int nt = (s + kT - 1) / kT;
   const int qt = nt - 1 - blockIdx.x;  // heaviest first
@@ -312,6 +337,7 @@ __global__ void __launch_bounds__(kThr, 1)
     mbar_init(s_full, 1);
     mbar_init(p_full, 256);
     mbar_init(p_empty, 1);
+    mbar_init(s_empty, 256);
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(tmem_holder, 512);
@@ -346,10 +372,12 @@ __global__ void __launch_bounds__(kThr, 1)
       const uint32_t sQ = smem_u32(sm + C::kQOff), sO = smem_u32(sm + C::kOOff);
       const uint32_t sDS = smem_u32(sm + C::kDSOff);
       bool ok = mbar_wait(q_full, 0, err);
-      for (int j = 0; ok && j < n_kv; ++j) {
+      // S / dP of key tile j (its K and V loaded, the TMEM they overwrite
+      // copied out by the element-wise warps)
+      auto issue_s = [&](int j) -> bool {
         const int st = j & 1;
-        if (!mbar_wait(&kv_full[st], (j >> 1) & 1, err)) break;
-        if (j > 0 && !mbar_wait(p_full, (j - 1) & 1, err)) break;
+        if (!mbar_wait(&kv_full[st], (j >> 1) & 1, err)) return false;
+        if (j > 0 && !mbar_wait(s_empty, (j - 1) & 1, err)) return false;
         tc_fence_after();
         const uint32_t sK = smem_u32(sm + C::kKVOff + st * 2 * C::kTile), sV = sK + C::kTile;
 #pragma unroll
@@ -359,8 +387,15 @@ __global__ void __launch_bounds__(kThr, 1)
           tc_mma_bf16(tdP, smem_desc_kmajor_sw128(sO + off), smem_desc_kmajor_sw128(sV + off), id_s, kk > 0);
         }
         tc_commit(s_full);
-        if (!mbar_wait(p_full, j & 1, err)) break;
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        // the next tile's scores overlap this tile's element-wise work
+        if (j + 1 < n_kv && !(ok = issue_s(j + 1))) break;
+        if (!(ok = mbar_wait(p_full, j & 1, err))) break;
         tc_fence_after();
+        const uint32_t sK = smem_u32(sm + C::kKVOff + (j & 1) * 2 * C::kTile);
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk) {
           const uint32_t aoff = (kk >> 2) * kBox + (kk & 3) * 32;
@@ -368,7 +403,7 @@ __global__ void __launch_bounds__(kThr, 1)
                       (j > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(p_empty);
-        tc_commit(&kv_empty[st]);
+        tc_commit(&kv_empty[j & 1]);
       }
     }
   } else {
@@ -391,6 +426,8 @@ __global__ void __launch_bounds__(kThr, 1)
         tmem_ld_32x32b_x32(tdP + lane_off + half * 64 + c * 32, rp[c]);
       }
       tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(s_empty);
       const bool diag = (j == n_kv - 1);
       const int kb = j * kT + half * 64;
       uint32_t dk[32];

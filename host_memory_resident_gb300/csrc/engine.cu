@@ -329,7 +329,9 @@ struct Step {
       slot = h->slot_last_use[0] <= h->slot_last_use[1] ? 0 : 1;
       const size_t bytes = sizeof(uint16_t) * h->lay.unit_len[u];
       CK(cudaStreamWaitEvent(h->s_h2d, h->ev_free[slot], 0));
+      prof_copy_begin(h->s_h2d);
       CK(cudaMemcpyAsync(h->wbuf[slot], h->store + h->lay.unit_off[u], bytes, cudaMemcpyHostToDevice, h->s_h2d));
+      prof_copy_end(h->s_h2d, MT_PROF_H2D, (double)bytes);
       CK(cudaEventRecord(h->ev_ready[slot], h->s_h2d));
       h->slot_unit[slot] = u;
       h->st.h2d_bytes += (int64_t)bytes;
@@ -369,7 +371,9 @@ struct Step {
     }
     const size_t bytes = sizeof(uint16_t) * h->lay.unit_len[u];
     CK(cudaStreamWaitEvent(h->s_d2h, h->ev_slab_ready[k], 0));
+    prof_copy_begin(h->s_d2h);
     CK(cudaMemcpyAsync(h->staging[k], h->slab[k], bytes, cudaMemcpyDeviceToHost, h->s_d2h));
+    prof_copy_end(h->s_d2h, MT_PROF_D2H, (double)bytes);
     CK(cudaEventRecord(h->ev_d2h_done[k], h->s_d2h));
     h->st.d2h_bytes += (int64_t)bytes;
     {
@@ -398,6 +402,23 @@ struct Step {
     if (!h->prof_on) return;
     CK(cudaEventRecord(h->prof_events[2 * prof_next + 1], cs()));
     h->prof_recs.push_back({cat, flops, bytes});
+    ++prof_next;
+  }
+  // A copy on `st`, bracketed by events on that stream when profiling is on.
+  void prof_copy_begin(cudaStream_t st) {
+    if (!h->prof_on) return;
+    while (h->prof_events.size() < 2 * (prof_next + 1)) {
+      cudaEvent_t e;
+      CK(cudaEventCreate(&e));
+      h->prof_events.push_back(e);
+    }
+    CK(cudaEventRecord(h->prof_events[2 * prof_next], st));
+  }
+  void prof_copy_end(cudaStream_t st, int cat, double bytes) {
+    h->prof.launches[cat] += 1;
+    if (!h->prof_on) return;
+    CK(cudaEventRecord(h->prof_events[2 * prof_next + 1], st));
+    h->prof_recs.push_back({cat, 0.0, bytes});
     ++prof_next;
   }
 #define KP(cat, nl, fl, by, call) \

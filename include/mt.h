@@ -101,11 +101,15 @@ typedef struct mt_stats {
 #define MT_PROF_CE 7
 #define MT_PROF_EMBED 8
 #define MT_PROF_OTHER 9
-#define MT_PROF_N 10
+#define MT_PROF_H2D 10   /* weight-unit copies, host store -> device buffer */
+#define MT_PROF_D2H 11   /* gradient-slab copies, device slab -> pinned staging */
+#define MT_PROF_N 12
 
 /* Per-class totals: launches, device time (CUDA events around each launch
  * on the compute stream, only while profiling is enabled), algorithmic
- * FLOPs and algorithmic HBM bytes of the timed launches. */
+ * FLOPs and algorithmic HBM bytes of the timed launches. The two copy
+ * classes count copies instead of launches, time them with events on their
+ * own streams, and give the bytes copied. */
 typedef struct mt_kernel_profile {
   int64_t launches[MT_PROF_N];
   double ms[MT_PROF_N];

@@ -49,6 +49,21 @@ def test_exports_every_declared_symbol(L):
     assert set(mt.EXPORTS) <= names
 
 
+def test_binding_structs_match_the_header():
+    """The ctypes mirrors of mt_kernel_profile and mt_config have the header's
+    sizes (a mismatch would let the library write past the Python buffer)."""
+    text = open(os.path.join(ROOT, "include", "mt.h")).read()
+    classes = {int(v): n.lower() for n, v in re.findall(r"#define MT_PROF_(\w+) (\d+)", text) if n != "N"}
+    n_prof = int(re.search(r"#define MT_PROF_N (\d+)", text).group(1))
+    assert len(mt.PROF_CLASSES) == n_prof == len(classes)
+    assert [classes[i] for i in range(n_prof)] == mt.PROF_CLASSES
+    assert C.sizeof(mt.KernelProfile) == n_prof * 8 * 4
+    body = re.search(r"typedef struct mt_config \{(.*?)\} mt_config;", text, re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    n_fields = sum(len(decl.split(",")) for decl in re.findall(r"(?:int32_t|float)\s+([^;]+);", body))
+    assert C.sizeof(mt.Config) == 4 * n_fields
+
+
 @pytest.mark.parametrize("name", ["tiny", "1.1b", "7b", "14b", "7b-256k", "padded", "gqa"])
 def test_layout_matches_oracle(L, name):
     if name == "padded":
