@@ -330,6 +330,73 @@ def run_gemm_kernel(args):
     return 0 if err < 2e-2 else 1
 
 
+def run_misc_kernels(args):
+    """The memory-bound kernels of one 1.1B layer step at the workload's sizes
+    (M = 16384 tokens, d = 2048, f = 5632, 32 + 4 heads of 64, V = 32000, the
+    logits chunk of the head), each timed with CUDA events and reported as
+    GB/s of algorithmic bytes against the measured HBM copy bandwidth. Inputs
+    of each kernel exceed L2 (129 MB) except the RoPE tables and norm weights."""
+    import torch
+    import host_memory_resident_gb300 as mt
+    torch.manual_seed(0)
+    dev = "cuda"
+    M, d, f, H, Hkv, hd, V, s = 16384, 2048, 5632, 32, 4, 64, 32000, 2048
+    B = M // s
+    qn = (H + 2 * Hkv) * hd
+    mc = (1 << 28) // V
+    bf = torch.bfloat16
+    x = torch.randn(M, d, device=dev).to(bf)
+    w = (1 + 0.1 * torch.randn(d, device=dev)).to(bf)
+    y = torch.empty(M, d, device=dev, dtype=bf)
+    rstd = torch.empty(M, device=dev)
+    dy = torch.randn(M, d, device=dev)
+    dres = torch.randn(M, d, device=dev)
+    dx32 = torch.empty(M, d, device=dev)
+    dxb = torch.empty(M, d, device=dev, dtype=bf)
+    part = torch.empty(mt.k_rmsnorm_bwd_parts(M), d, device=dev)
+    dw = torch.empty(d, device=dev, dtype=bf)
+    qkv = torch.randn(M, qn, device=dev).to(bf)
+    pos = torch.arange(s, device=dev, dtype=torch.float64)[:, None]
+    inv = 10000.0 ** (-torch.arange(0, hd, 2, device=dev, dtype=torch.float64) / hd)
+    cos_t, sin_t = torch.cos(pos * inv).float().contiguous(), torch.sin(pos * inv).float().contiguous()
+    gu = torch.randn(M, 2 * f, device=dev).to(bf)
+    a = torch.empty(M, f, device=dev, dtype=bf)
+    da = torch.randn(M, f, device=dev).to(bf)
+    dgu = torch.empty(M, 2 * f, device=dev, dtype=bf)
+    logits = torch.randn(mc, V, device=dev)
+    labels = torch.randint(0, V, (mc,), device=dev, dtype=torch.int32)
+    dz = torch.empty(mc, V, device=dev, dtype=bf)
+    loss_rows = torch.empty(mc, device=dev)
+    cases = [
+        ("rmsnorm_fwd", lambda: mt.k_rmsnorm_fwd(x, w, y, rstd, 1e-5), 4.0 * M * d + 4.0 * M + 2.0 * d),
+        ("rmsnorm_bwd (+ column sums)", lambda: mt.k_rmsnorm_bwd(dy, x, w, rstd, dres, dx32, dxb, part, dw),
+         (4.0 + 2.0 + 4.0 + 4.0 + 2.0) * M * d + 4.0 * M),
+        ("rope (q and k heads, in place)", lambda: mt.k_rope(qkv, B, s, H + Hkv, hd, cos_t, sin_t),
+         4.0 * M * (H + Hkv) * hd),
+        ("swiglu_fwd", lambda: mt.k_swiglu_fwd(gu, a), 6.0 * M * f),
+        ("swiglu_bwd", lambda: mt.k_swiglu_bwd(da, gu, dgu), 10.0 * M * f),
+        ("cross_entropy (one logits chunk)", lambda: mt.k_cross_entropy(logits, labels, dz, loss_rows, 1.0 / M),
+         6.0 * mc * V),
+    ]
+    pk, pk_kind = peaks()
+    peak = pk.get("hbm_gbs")
+    for name, fn, nbytes in cases:
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.iters):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.iters
+        gbs = nbytes / (ms / 1e3) / 1e9
+        print(json.dumps({"kernel": name, "ms": ms, "algorithmic_bytes": nbytes, "gbs": gbs, "hbm_peak_gbs": peak,
+                          "peak_source": pk_kind, "frac": gbs / peak if peak else None}), flush=True)
+    return 0
+
+
 def run_attn_kernel(args):
     """One attention forward shape through mt_k_attn_fwd (profiler captures)."""
     import torch
@@ -374,7 +441,8 @@ def run_ours(args, shape, world, rank, local, pg):
     import host_memory_resident_gb300 as mt
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    cfg = mt.make_config(shape, device=local, host_threads=args.host_threads, overlap_adam=args.overlap)
+    cfg = mt.make_config(shape, device=local, host_threads=args.host_threads, overlap_adam=args.overlap,
+                         unfused_epilogues=args.unfused)
     descs, n_total = mt.layout(cfg)
     segs = [(t["offset"], t["rows"] * t["cols"], "normal" if t["kind"] == 0 else "ones") for t in descs]
     master = synth.init_master(n_total, segs, seed=0)
@@ -465,6 +533,7 @@ def run_ours(args, shape, world, rank, local, pg):
                    "parallelism": f"replicas x{world} (no collective)" if world > 1 else "single GPU",
                    "overlap_adam": bool(args.overlap),
                    "fp32_grad_array": bool(args.keep_grads),
+                   "fused_epilogues": not args.unfused,
                    "l2": "inputs larger than L2: each step streams the whole bf16 store "
                          f"({w_bytes / 1e9:.2f} GB) and the activations"},
         "model_tflops": F / t_step / 1e12,
@@ -518,13 +587,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="1.1b", choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--kernel", default=None, choices=[None, "gemm", "attn"])
+    ap.add_argument("--kernel", default=None, choices=[None, "gemm", "attn", "misc"])
     ap.add_argument("--legacy", action="store_true", help="with --kernel attn: the mma.sync kernels")
     ap.add_argument("--backward", action="store_true", help="with --kernel attn: time the backward")
     ap.add_argument("--shape", default="8192,8192,2048")
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--host-threads", type=int, default=0)
+    ap.add_argument("--unfused", action="store_true",
+                    help="RoPE and SwiGLU as separate kernels instead of GEMM epilogues (same results)")
     ap.add_argument("--fused-grads", action="store_true",
                     help="no FP32 gradient array: each slab goes straight into Adam (same arithmetic)")
     ap.add_argument("--overlap", action="store_true",
@@ -535,6 +606,8 @@ def main():
         return run_gemm_kernel(args)
     if args.kernel == "attn":
         return run_attn_kernel(args)
+    if args.kernel == "misc":
+        return run_misc_kernels(args)
     shape = synth.workload(args.config)
     world, rank, local, pg = dist_setup()
     if args.impl == "reference":

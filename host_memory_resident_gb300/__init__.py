@@ -38,7 +38,12 @@ class Config(C.Structure):
         ("rms_eps", C.c_float), ("rope_theta", C.c_float), ("lr", C.c_float),
         ("beta1", C.c_float), ("beta2", C.c_float), ("adam_eps", C.c_float),
         ("device", C.c_int32), ("host_threads", C.c_int32), ("overlap_adam", C.c_int32),
+        ("unfused_epilogues", C.c_int32),
     ]
+
+
+class TimelineRec(C.Structure):
+    _fields_ = [("cls", C.c_int32), ("stream", C.c_int32), ("start_ms", C.c_double), ("end_ms", C.c_double)]
 
 
 class TensorDesc(C.Structure):
@@ -65,9 +70,9 @@ class KernelProfile(C.Structure):
 EXPORTS = [
     "mt_layout", "mt_unit_range", "mt_plan", "mt_init", "mt_train_step", "mt_train_step_device", "mt_train_step_accum",
     "mt_read_grads", "mt_sync", "mt_get_step", "mt_set_step", "mt_sync_store", "mt_get_stats",
-    "mt_get_stream", "mt_profile_enable", "mt_profile_read", "mt_destroy", "mt_last_error", "mt_debug_inject", "mt_debug_inject_global",
+    "mt_get_stream", "mt_profile_enable", "mt_profile_read", "mt_profile_timeline", "mt_destroy", "mt_last_error", "mt_debug_inject", "mt_debug_inject_global",
     "mt_host_adam", "mt_host_adam_slab", "mt_host_to_bf16",
-    "mt_k_gemm", "mt_k_gemm_ex", "mt_k_transpose", "mt_k_rmsnorm_fwd", "mt_k_rmsnorm_bwd", "mt_k_rmsnorm_bwd_parts",
+    "mt_k_gemm", "mt_k_gemm_ex", "mt_k_gemm_rope", "mt_k_gemm_swiglu_fwd", "mt_k_gemm_swiglu_bwd", "mt_k_transpose", "mt_k_rmsnorm_fwd", "mt_k_rmsnorm_bwd", "mt_k_rmsnorm_bwd_parts",
     "mt_k_rope", "mt_k_swiglu_fwd", "mt_k_swiglu_bwd", "mt_k_attn_fwd", "mt_k_attn_fwd_mma", "mt_k_attn_bwd", "mt_k_attn_bwd_mma",
     "mt_k_cross_entropy", "mt_k_sum", "mt_k_embedding_fwd", "mt_k_embedding_bwd",
     "mt_k_embedding_bwd_work", "mt_k_check_ids", "mt_k_device_error",
@@ -105,6 +110,7 @@ def lib():
         "mt_get_stream": ([P, I, C.POINTER(P)], I),
         "mt_profile_enable": ([P, I], I),
         "mt_profile_read": ([P, C.POINTER(KernelProfile), I], I),
+        "mt_profile_timeline": ([P, C.POINTER(TimelineRec), I, C.POINTER(I)], I),
         "mt_destroy": ([P], I),
         "mt_last_error": ([P], C.c_char_p),
         "mt_debug_inject": ([P, I, I64], I),
@@ -114,6 +120,9 @@ def lib():
         "mt_host_to_bf16": ([P, P, I64], I),
         "mt_k_gemm": ([P, I64, P, I64, P, I64, I, P, I64, I, I, I, P], I),
         "mt_k_gemm_ex": ([P, I64, I, P, I64, I, P, I64, I, P, I64, I, I, I, P], I),
+        "mt_k_gemm_rope": ([P, I64, P, I64, P, I64, I, I, I, P, P, I, I, I, P], I),
+        "mt_k_gemm_swiglu_fwd": ([P, I64, P, I64, P, I64, P, I64, I, I, I, P], I),
+        "mt_k_gemm_swiglu_bwd": ([P, I64, P, I64, P, I64, P, I64, I, I, I, P], I),
         "mt_k_transpose": ([P, I64, P, I64, I, I, P], I),
         "mt_k_rmsnorm_fwd": ([P, P, P, P, I, I, F, P], I),
         "mt_k_rmsnorm_bwd": ([P, P, P, P, P, P, P, P, P, I, I, P], I),
@@ -149,7 +158,7 @@ def check(code, handle=None):
 
 
 def make_config(shape, batch=None, seq=None, streamed=True, device=0, host_threads=0, ckpt_interval=None,
-                n_slabs=None, overlap_adam=False) -> Config:
+                n_slabs=None, overlap_adam=False, unfused_epilogues=False) -> Config:
     """mt_config from a synth.ModelShape-like object."""
     c = Config()
     c.n_layers = shape.n_layers
@@ -173,6 +182,7 @@ def make_config(shape, batch=None, seq=None, streamed=True, device=0, host_threa
     c.device = device
     c.host_threads = host_threads
     c.overlap_adam = 1 if overlap_adam else 0
+    c.unfused_epilogues = 1 if unfused_epilogues else 0
     return c
 
 
@@ -287,6 +297,17 @@ class Trainer:
         return {name: dict(launches=p.launches[i], ms=p.ms[i], flops=p.flops[i], bytes=p.bytes[i])
                 for i, name in enumerate(PROF_CLASSES)}
 
+    def timeline(self) -> list:
+        """Launches and copies of the last profiled step: dicts with the class
+        name, stream (compute / h2d / d2h) and start / end in ms."""
+        n = C.c_int()
+        check(lib().mt_profile_timeline(self.h, None, 0, C.byref(n)), self.h)
+        buf = (TimelineRec * max(n.value, 1))()
+        check(lib().mt_profile_timeline(self.h, buf, n.value, C.byref(n)), self.h)
+        names = ("compute", "h2d", "d2h")
+        return [dict(cls=PROF_CLASSES[r.cls], stream=names[r.stream], start_ms=r.start_ms, end_ms=r.end_ms)
+                for r in buf[:n.value]]
+
     def get_step(self) -> int:
         t = C.c_int64()
         check(lib().mt_get_step(self.h, C.byref(t)))
@@ -394,6 +415,27 @@ def k_rmsnorm_bwd(dy, x, w, rstd, dres, dx32, dxb, partial, dw, stream=None):
     M, d = x.shape
     check(lib().mt_k_rmsnorm_bwd(_dp(dy), _dp(x), _dp(w), _dp(rstd), _dp(dres), _dp(dx32), _dp(dxb), _dp(partial),
                                  _dp(dw), M, d, _st(stream)))
+
+
+def k_gemm_rope(A, B, Cout, cos_t, sin_t, rot_cols, hd, seq, stream=None):
+    """Cout = A B^T with RoPE on columns [0, rot_cols) (position = row mod seq)."""
+    M, N = Cout.shape
+    check(lib().mt_k_gemm_rope(_dp(A), A.stride(0), _dp(B), B.stride(0), _dp(Cout), Cout.stride(0), M, N, A.shape[1],
+                               _dp(cos_t), _dp(sin_t), rot_cols, hd, seq, _st(stream)))
+
+
+def k_gemm_swiglu_fwd(A, W, gu, a, stream=None):
+    """gu = A W^T (W = [gate rows; up rows]) and a = silu(gate) * up."""
+    M, f = a.shape
+    check(lib().mt_k_gemm_swiglu_fwd(_dp(A), A.stride(0), _dp(W), W.stride(0), _dp(gu), gu.stride(0), _dp(a),
+                                     a.stride(0), M, f, A.shape[1], _st(stream)))
+
+
+def k_gemm_swiglu_bwd(dy, W, gu, dgu, stream=None):
+    """dgu = SwiGLU backward of da = dy W (W [K, f] read in place) at gate | up = gu."""
+    M, f = dy.shape[0], W.shape[1]
+    check(lib().mt_k_gemm_swiglu_bwd(_dp(dy), dy.stride(0), _dp(W), W.stride(0), _dp(gu), gu.stride(0), _dp(dgu),
+                                     dgu.stride(0), M, f, dy.shape[1], _st(stream)))
 
 
 def k_rope(x, B, s, n_rot_heads, hd, cos_t, sin_t, inverse=False, stream=None):

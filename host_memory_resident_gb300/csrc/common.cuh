@@ -240,6 +240,39 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// ----------------------------------------- element-wise layer arithmetic
+// Shared by the stand-alone kernels and the fused GEMM epilogues, with the
+// rounding of every product fixed (no contraction into fused multiply-adds
+// the compiler may or may not form), so both paths give the same bits.
+
+// RoPE on one rotate-half pair (x1 = dim i, x2 = dim i + hd/2) at angle
+// (c, s) = (cos, sign * sin): (x1 c - x2 s, x2 c + x1 s).
+__device__ __forceinline__ void rope_pair(float x1, float x2, float c, float s, float& o1, float& o2) {
+  o1 = __fadd_rn(__fmul_rn(x1, c), -__fmul_rn(x2, s));
+  o2 = __fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, s));
+}
+
+// 1 / (1 + e^-g) with the fast exponential and division intrinsics (a few
+// ulp; g -> -inf gives 0, g -> +inf gives 1).
+__device__ __forceinline__ float sigmoid_f32(float g) { return __fdividef(1.f, 1.f + __expf(-g)); }
+
+// SwiGLU forward: silu(g) * u = g * sigmoid(g) * u.
+__device__ __forceinline__ float swiglu_fwd_elem(float g, float u) {
+  return __fmul_rn(__fmul_rn(g, sigmoid_f32(g)), u);
+}
+
+// SwiGLU backward for a = g sigmoid(g) u: dg = da u sg (1 + g (1 - sg)),
+// du = da g sg with sg = sigmoid(g).
+__device__ __forceinline__ void swiglu_bwd_elem(float da, float g, float u, float& dg, float& du) {
+  const float sg = sigmoid_f32(g);
+  const float t = __fadd_rn(1.f, __fmul_rn(g, __fadd_rn(1.f, -sg)));
+  dg = __fmul_rn(__fmul_rn(__fmul_rn(da, u), sg), t);
+  du = __fmul_rn(__fmul_rn(da, g), sg);
+}
+
+// bf16 round trip (round to nearest even, back to fp32).
+__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
 // ------------------------------------------------------ legacy mma.sync
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                             uint32_t& r3) {

@@ -12,7 +12,8 @@
 //    buffer_free_events; zhichai.net article point 2, ping-pong buffers);
 //  * checkpoint recompute: the input of every C-th layer is kept, backward
 //    walks segments from last to first and recomputes each from its
-//    checkpoint (section 三.4; zhichai.net article point 3);
+//    checkpoint (section 三.4; zhichai.net article point 3), except the last
+//    segment, whose activations the forward leaves in place;
 //  * a K-slab device gradient pool: a unit's weight gradients land in a free
 //    slab, a device-to-host stream copies it to pinned staging, and a host
 //    worker thread adds it into the FP32 gradient and runs Adam on that unit
@@ -182,9 +183,11 @@ struct mt_handle {
   mt_stats st{};
   int prof_on = 0;
   std::vector<cudaEvent_t> prof_events;
-  struct ProfRec { int cat; double flops, bytes; };
+  struct ProfRec { int cat, stream; double flops, bytes; };
   std::vector<ProfRec> prof_recs;
   mt_kernel_profile prof{};
+  cudaEvent_t prof_ref = nullptr;        // start of the last profiled step (compute stream)
+  std::vector<mt_timeline_rec> timeline;  // its launches and copies
 };
 
 namespace mt {
@@ -401,7 +404,7 @@ struct Step {
     h->prof.launches[cat] += launches;
     if (!h->prof_on) return;
     CK(cudaEventRecord(h->prof_events[2 * prof_next + 1], cs()));
-    h->prof_recs.push_back({cat, flops, bytes});
+    h->prof_recs.push_back({cat, 0, flops, bytes});
     ++prof_next;
   }
   // A copy on `st`, bracketed by events on that stream when profiling is on.
@@ -418,7 +421,7 @@ struct Step {
     h->prof.launches[cat] += 1;
     if (!h->prof_on) return;
     CK(cudaEventRecord(h->prof_events[2 * prof_next + 1], st));
-    h->prof_recs.push_back({cat, 0.0, bytes});
+    h->prof_recs.push_back({cat, st == h->s_h2d ? 1 : 2, 0.0, bytes});
     ++prof_next;
   }
 #define KP(cat, nl, fl, by, call) \
@@ -450,6 +453,11 @@ struct Step {
   double norm_fwd_bytes() const { return 4.0 * M * h->d + 4.0 * M; }
   double norm_bwd_bytes(bool res) const { return (4.0 + 2.0 + 4.0 + 2.0 + (res ? 4.0 : 0.0)) * M * h->d; }
   double rope_bytes() const { return 4.0 * M * (h->H + h->Hkv) * h->hd; }
+  // RoPE and SwiGLU go into the GEMM epilogues unless the configuration asks
+  // for the separate kernels or a shape does not fit the fused forms.
+  bool fuse_rope() const { return !h->cfg.unfused_epilogues && h->hd % 64 == 0 && 128 % h->hd == 0; }
+  bool fuse_swiglu_fwd() const { return !h->cfg.unfused_epilogues && h->f % 128 == 0; }
+  bool fuse_swiglu_bwd() const { return !h->cfg.unfused_epilogues && h->f % 32 == 0; }
 
   // Forward of layer l with weights W; writes the saved activations into S and
   // the layer output into x_out.
@@ -457,14 +465,29 @@ struct Step {
     const LayerOffsets& o = h->lay.layer;
     const int d = h->d, f = h->f;
     KP(MT_PROF_NORM, 1, 0.0, norm_fwd_bytes(), mt_k_rmsnorm_fwd(S.x, W + o.attn_norm, S.u, S.r1, M, d, h->cfg.rms_eps, cs()));
-    gemm(S.u, d, W + o.wqkv, d, S.qkv, h->qkvN, false, nullptr, 0, M, h->qkvN, d);
-    KP(MT_PROF_ROPE, 1, 0.0, rope_bytes(), mt_k_rope(S.qkv, h->qkvN, B, s, h->H + h->Hkv, h->hd, h->cos_t, h->sin_t, 0, cs()));
+    if (fuse_rope()) {
+      const int qn = h->qkvN;
+      const double bytes = 2.0 * ((double)M * d + (double)qn * d + (double)M * qn) + 8.0 * s * (h->hd / 2);
+      KP(MT_PROF_GEMM, 1, 2.0 * M * (double)qn * d, bytes,
+         gemm_rope(S.u, d, W + o.wqkv, d, S.qkv, qn, M, qn, d, h->cos_t, h->sin_t, (h->H + h->Hkv) * h->hd, h->hd,
+                   s, cs()));
+    } else {
+      gemm(S.u, d, W + o.wqkv, d, S.qkv, h->qkvN, false, nullptr, 0, M, h->qkvN, d);
+      KP(MT_PROF_ROPE, 1, 0.0, rope_bytes(),
+         mt_k_rope(S.qkv, h->qkvN, B, s, h->H + h->Hkv, h->hd, h->cos_t, h->sin_t, 0, cs()));
+    }
     KP(MT_PROF_ATTN_FWD, 1, attn_flops(false), 0.0,
        mt_k_attn_fwd(S.qkv, h->qkvN, S.o, h->hq, S.lse, B, s, h->H, h->Hkv, h->hd, cs()));
     gemm(S.o, h->hq, W + o.wo, h->hq, S.h, d, false, S.x, d, M, d, h->hq);
     KP(MT_PROF_NORM, 1, 0.0, norm_fwd_bytes(), mt_k_rmsnorm_fwd(S.h, W + o.mlp_norm, S.z, S.r2, M, d, h->cfg.rms_eps, cs()));
-    gemm(S.z, d, W + o.wgu, d, S.gu, 2 * f, false, nullptr, 0, M, 2 * f, d);
-    KP(MT_PROF_SWIGLU, 1, 0.0, 6.0 * M * f, mt_k_swiglu_fwd(S.gu, S.a, M, f, cs()));
+    if (fuse_swiglu_fwd()) {
+      const double bytes = 2.0 * ((double)M * d + 2.0 * f * d + 2.0 * M * f + (double)M * f);
+      KP(MT_PROF_GEMM, 1, 2.0 * M * (2.0 * f) * d, bytes,
+         gemm_swiglu_fwd(S.z, d, W + o.wgu, d, S.gu, 2 * f, S.a, f, M, f, d, cs()));
+    } else {
+      gemm(S.z, d, W + o.wgu, d, S.gu, 2 * f, false, nullptr, 0, M, 2 * f, d);
+      KP(MT_PROF_SWIGLU, 1, 0.0, 6.0 * M * f, mt_k_swiglu_fwd(S.gu, S.a, M, f, cs()));
+    }
     gemm(S.a, f, W + o.wdown, f, x_out, d, false, S.h, d, M, d, f);
   }
 
@@ -479,8 +502,15 @@ struct Step {
     // weight [out, in] in place as a [K, N] operand. Nothing is transposed.
     // down projection: dWdown = dy^T a ; da = dy Wdown
     gemm_mn(h->dxb, d, true, S.a, f, true, g + o.wdown, f, false, d, f, M);
-    gemm_mn(h->dxb, d, false, W + o.wdown, f, true, h->da, f, false, M, f, d);
-    KP(MT_PROF_SWIGLU, 1, 0.0, 10.0 * M * f, mt_k_swiglu_bwd(h->da, S.gu, h->dgu, M, f, cs()));
+    if (fuse_swiglu_bwd()) {
+      // da = dy Wdown stays in the SM; the epilogue writes d(gate) | d(up)
+      const double bytes = 2.0 * ((double)M * d + (double)d * f + 2.0 * M * f + 2.0 * M * f);
+      KP(MT_PROF_GEMM, 1, 2.0 * M * (double)f * d, bytes,
+         gemm_swiglu_bwd(h->dxb, d, W + o.wdown, f, S.gu, 2 * f, h->dgu, 2 * f, M, f, d, cs()));
+    } else {
+      gemm_mn(h->dxb, d, false, W + o.wdown, f, true, h->da, f, false, M, f, d);
+      KP(MT_PROF_SWIGLU, 1, 0.0, 10.0 * M * f, mt_k_swiglu_bwd(h->da, S.gu, h->dgu, M, f, cs()));
+    }
     // gate/up projection
     gemm_mn(h->dgu, 2 * f, true, S.z, d, true, g + o.wgu, d, false, 2 * f, d, M);
     gemm_mn(h->dgu, 2 * f, false, W + o.wgu, d, true, h->dn32, d, true, M, d, 2 * f);
@@ -537,6 +567,10 @@ struct Step {
       hh.loss_state[parity()] = 0;
       ++hh.step_seq;
     }
+    if (hh.prof_on) {
+      if (!hh.prof_ref) CK(cudaEventCreate(&hh.prof_ref));
+      CK(cudaEventRecord(hh.prof_ref, hh.s_comp));
+    }
     // The host Adam rewrote the bf16 store since the last step, so nothing
     // left in the two device buffers may be reused: forget their contents.
     hh.slot_unit[0] = hh.slot_unit[1] = -1;
@@ -556,15 +590,26 @@ struct Step {
          mt_k_embedding_fwd(E + (hh.lay.embed - hh.lay.unit_off[0]), hh.d_tok, hh.ckpt[0], M, hh.d, hh.V, cs()));
       release();
     }
+    // The last segment's layers keep their activations in the saved sets,
+    // exactly where its recompute would put them, so the backward starts on
+    // that segment without recomputing it.
+    const int last_a = (hh.nseg - 1) * C;
     bf16* x = hh.ckpt[0];
     for (int l = 0; l < L; ++l) {
       bf16* W = acquire(1 + l);
-      Saved S = hh.saved[0];
-      S.x = x;
       bf16* out;
-      if ((l + 1) % C == 0 && l + 1 < L) out = hh.ckpt[(l + 1) / C];
-      else out = (x == hh.xa) ? hh.xb : hh.xa;
-      layer_fwd(W, S, out);
+      if (l >= last_a) {
+        Saved& S = hh.saved[l - last_a];
+        if (l == last_a) S.x = hh.ckpt[hh.nseg - 1];
+        out = (l + 1 < L) ? hh.saved[l + 1 - last_a].x : hh.xa;
+        layer_fwd(W, S, out);
+      } else {
+        Saved S = hh.saved[0];
+        S.x = x;
+        if ((l + 1) % C == 0) out = hh.ckpt[(l + 1) / C];
+        else out = (x == hh.xa) ? hh.xb : hh.xa;
+        layer_fwd(W, S, out);
+      }
       release();
       x = out;
     }
@@ -575,10 +620,10 @@ struct Step {
       release();
       slab_end(k, L + 1);
     }
-    // ---- backward over segments, last to first, recomputing each
+    // ---- backward over segments, last to first, recomputing all but the last
     for (int seg = hh.nseg - 1; seg >= 0; --seg) {
       const int a = seg * C, b = std::min(L, a + C);
-      for (int l = a; l < b; ++l) {
+      for (int l = a; l < b && seg < hh.nseg - 1; ++l) {
         bf16* W = acquire(1 + l);
         Saved& S = hh.saved[l - a];
         if (l == a) S.x = hh.ckpt[seg];
@@ -622,6 +667,7 @@ void destroy_resources(mt_handle* h) {
   for (auto e : h->ev_slab_ready) if (e) cudaEventDestroy(e);
   for (auto e : h->ev_d2h_done) if (e) cudaEventDestroy(e);
   for (auto e : h->prof_events) if (e) cudaEventDestroy(e);
+  if (h->prof_ref) cudaEventDestroy(h->prof_ref);
   for (int i = 0; i < 2; ++i)
     if (h->ev_loss[i]) cudaEventDestroy(h->ev_loss[i]);
   if (h->ev_resident) cudaEventDestroy(h->ev_resident);
@@ -958,13 +1004,19 @@ static int run_step(mt_handle* h, const int32_t* tokens, const int32_t* labels, 
     CK(cudaStreamSynchronize(h->s_d2h));
     CK(cudaStreamSynchronize(h->s_h2d));
     if (h->prof_on) {
+      h->timeline.clear();
       for (size_t i = 0; i < h->prof_recs.size(); ++i) {
-        float ms = 0.f;
+        float ms = 0.f, t0 = 0.f, t1 = 0.f;
         CK(cudaEventElapsedTime(&ms, h->prof_events[2 * i], h->prof_events[2 * i + 1]));
         const auto& r = h->prof_recs[i];
         h->prof.ms[r.cat] += ms;
         h->prof.flops[r.cat] += r.flops;
         h->prof.bytes[r.cat] += r.bytes;
+        if (h->prof_ref) {
+          CK(cudaEventElapsedTime(&t0, h->prof_ref, h->prof_events[2 * i]));
+          CK(cudaEventElapsedTime(&t1, h->prof_ref, h->prof_events[2 * i + 1]));
+          h->timeline.push_back(mt_timeline_rec{r.cat, r.stream, (double)t0, (double)t1});
+        }
       }
     }
     h->prof_recs.clear();
@@ -1089,6 +1141,14 @@ int mt_profile_read(mt_handle* h, mt_kernel_profile* out, int reset) {
   if (!h || !out) return MT_EINVAL;
   *out = h->prof;
   if (reset) h->prof = mt_kernel_profile{};
+  return MT_OK;
+}
+
+int mt_profile_timeline(mt_handle* h, mt_timeline_rec* out, int cap, int* n_out) {
+  if (!h || !n_out || cap < 0 || (cap > 0 && !out)) return MT_EINVAL;
+  const int n = (int)h->timeline.size();
+  for (int i = 0; i < n && i < cap; ++i) out[i] = h->timeline[i];
+  *n_out = n;
   return MT_OK;
 }
 

@@ -16,10 +16,21 @@
 //   * warp 1 allocates 512 TMEM columns (two 128 x 256 fp32 accumulators) and
 //     one lane issues tcgen05.mma (M=128, N=256, K=16), committing each stage
 //     back to the producer and each finished accumulator to the epilogue;
-//   * warps 2-5 drain an accumulator with tcgen05.ld while the MMA warp fills
-//     the other one, add the optional bf16 residual, round and store.
+//   * warps 2-9 drain an accumulator with tcgen05.ld while the MMA warp fills
+//     the other one (two warps per TMEM lane quarter, each taking half of the
+//     tile's columns), add the optional bf16 residual, round and store.
 // Tiles are visited in groups of kGroupM row blocks so the A panel of a group
 // stays in L2 while the group sweeps all column blocks.
+//
+// Fused epilogues (each rounds to bf16 where the separate kernels would have
+// read a bf16 tensor, so results equal the unfused sequence bit for bit):
+//   * RoPE: the QKV projection rotates the q and k heads of its tile
+//     (rotate-half pairs, position = row mod seq) before storing;
+//   * SwiGLU forward: the gate/up projection's B tile pairs 128 gate rows
+//     with the matching 128 up rows, so the epilogue stores gate | up and
+//     a = silu(gate) * up;
+//   * SwiGLU backward: the down projection's input gradient da never leaves
+//     the SM; the epilogue reads gate | up and stores d(gate) | d(up).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -38,12 +49,15 @@ constexpr int kBN = 256;
 constexpr int kBK = 64;
 constexpr int kStages = 4;
 constexpr int kGroupM = 32;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;       // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
+constexpr int kEpiWarps = 8;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kABytes = kBM * kBK * 2;  // 16 KiB
 constexpr uint32_t kBBytes = kBN * kBK * 2;  // 32 KiB
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr size_t kSmemBytes = 1024 /*align slack*/ + (size_t)kStages * kStageBytes + 256 /*barriers*/;
+
+enum : int { kEpiPlain = 0, kEpiRope = 1, kEpiSwigluFwd = 2, kEpiSwigluBwd = 3 };
 
 struct GemmArgs {
   int M, N, K;
@@ -54,7 +68,46 @@ struct GemmArgs {
   int c_f32;
   int num_mb, num_nb;
   int* err;
+  // fused epilogues
+  bf16* C2;               // SwiGLU forward: a [M, f]
+  long long ldc2;
+  const bf16* X;          // SwiGLU backward: gate | up [M, 2f]
+  long long ldx;
+  int f;                  // SwiGLU: ffn width (gate columns [0, f), up [f, 2f))
+  const float* cos_t;     // RoPE tables [seq, hd/2]
+  const float* sin_t;
+  int rot_cols, hd, seq;  // RoPE: rotate columns [0, rot_cols) in heads of hd
 };
+
+__device__ __forceinline__ void store_bf16x32(bf16* p, const float (&v)[32]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint4 u;
+    u.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
+    u.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
+    u.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
+    u.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
+    reinterpret_cast<uint4*>(p)[j] = u;
+  }
+}
+
+__device__ __forceinline__ void load_bf16x32(const bf16* p, float (&v)[32]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint4 u = reinterpret_cast<const uint4*>(p)[j];
+    const float2 f0 = unpack_bf16x2(u.x), f1 = unpack_bf16x2(u.y), f2 = unpack_bf16x2(u.z), f3 = unpack_bf16x2(u.w);
+    v[8 * j + 0] = f0.x; v[8 * j + 1] = f0.y; v[8 * j + 2] = f1.x; v[8 * j + 3] = f1.y;
+    v[8 * j + 4] = f2.x; v[8 * j + 5] = f2.y; v[8 * j + 6] = f3.x; v[8 * j + 7] = f3.y;
+  }
+}
+
+__device__ __forceinline__ void load_f32x32(const float* p, float (&v)[32]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float4 u = reinterpret_cast<const float4*>(p)[j];
+    v[4 * j + 0] = u.x; v[4 * j + 1] = u.y; v[4 * j + 2] = u.z; v[4 * j + 3] = u.w;
+  }
+}
 
 __device__ __forceinline__ void tile_coords(int t, int num_mb, int num_nb, int& mb, int& nb) {
   const int per_group = kGroupM * num_nb;
@@ -70,7 +123,7 @@ __device__ __forceinline__ void tile_coords(int t, int num_mb, int num_nb, int& 
 // [K][M], B as [K][N], MN contiguous) and staged as 64 x 64 boxes.
 constexpr uint32_t kBoxBytes = 64 * 64 * 2;  // one 64 MN x 64 K box
 
-template <bool A_MN, bool B_MN>
+template <bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_abt_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     GemmArgs args) {
@@ -97,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull_bar[a], 1);
-      mbar_init(&tempty_bar[a], 4 * 32);
+      mbar_init(&tempty_bar[a], kEpiWarps * 32);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -128,7 +181,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             tma_load_2d(sa, &tmap_a, kb * kBK, mb * kBM, &full_bar[stage]);
           }
-          if (B_MN) {
+          if (EPI == kEpiSwigluFwd) {
+            // 128 gate rows, then the 128 up rows of the same ffn columns
+            tma_load_2d(sb, &tmap_b, kb * kBK, nb * (kBN / 2), &full_bar[stage]);
+            tma_load_2d(sb + (kBN / 2) * kBK * 2, &tmap_b, kb * kBK, args.f + nb * (kBN / 2), &full_bar[stage]);
+          } else if (B_MN) {
 #pragma unroll
             for (int j = 0; j < kBN / 64; ++j)
               tma_load_2d(sb + j * kBoxBytes, &tmap_b, nb * kBN + j * 64, kb * kBK, &full_bar[stage]);
@@ -175,8 +232,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ---------------- epilogue: warps 2..5 cover TMEM lane quarters (warp % 4)
+    // ---------------- epilogue: warps 2..9; warp % 4 is the TMEM lane quarter,
+    // (warp - 2) / 4 the half of the tile's columns (or heads) it stores
     const int q = warp & 3;
+    const int hs = (warp - 2) >> 2;
     int it = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
       const int acc = it & 1;
@@ -187,62 +246,144 @@ __global__ void __launch_bounds__(kThreads, 1)
       tile_coords(t, args.num_mb, args.num_nb, mb, nb);
       const int row = mb * kBM + q * 32 + lane;
       const bool row_ok = row < args.M;
+      const uint32_t tacc = tmem_base + (uint32_t)(acc * kBN) + ((uint32_t)(q * 32) << 16);
+      if (EPI == kEpiRope) {
+        // heads of hd columns; dims i and i + hd/2 of a head form a pair, so
+        // chunk j of the first half pairs with chunk j of the second half
+        const int hd = args.hd, half = hd >> 1;
+        const int pos = row_ok ? row % args.seq : 0;
+        const int nh = kBN / hd;  // heads per tile, split between the two halves
 #pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
-        __syncwarp();
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem_base + (uint32_t)(acc * kBN + c * 32) + ((uint32_t)(q * 32) << 16), r);
-        tmem_ld_wait();
-        const int col0 = nb * kBN + c * 32;
-        if (!row_ok || col0 >= args.N) continue;
-        float v[32];
+        for (int hb = hs * (nh / 2); hb < (hs + 1) * (nh / 2); ++hb) {
+          const int col_h = nb * kBN + hb * hd;
+#pragma unroll 1
+          for (int j = 0; j < hd / 64; ++j) {
+            __syncwarp();
+            uint32_t ra[32], rb[32];
+            tmem_ld_32x32b_x32(tacc + (uint32_t)(hb * hd + j * 32), ra);
+            tmem_ld_32x32b_x32(tacc + (uint32_t)(hb * hd + j * 32 + half), rb);
+            tmem_ld_wait();
+            if (!row_ok || col_h >= args.N) continue;
+            float va[32], vb[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-        const bool full = col0 + 32 <= args.N;
-        if (args.R != nullptr) {
-          const bf16* rp = args.R + (long long)row * args.ldr + col0;
-          if (full) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint4 u = reinterpret_cast<const uint4*>(rp)[j];
-              float2 f0 = unpack_bf16x2(u.x), f1 = unpack_bf16x2(u.y), f2 = unpack_bf16x2(u.z),
-                     f3 = unpack_bf16x2(u.w);
-              v[j * 8 + 0] += f0.x; v[j * 8 + 1] += f0.y; v[j * 8 + 2] += f1.x; v[j * 8 + 3] += f1.y;
-              v[j * 8 + 4] += f2.x; v[j * 8 + 5] += f2.y; v[j * 8 + 6] += f3.x; v[j * 8 + 7] += f3.y;
+            for (int i = 0; i < 32; ++i) {
+              va[i] = bf16_round(__uint_as_float(ra[i]));
+              vb[i] = bf16_round(__uint_as_float(rb[i]));
             }
-          } else {
+            if (col_h < args.rot_cols) {
+              float cs[32], sn[32];
+              load_f32x32(args.cos_t + (long long)pos * half + j * 32, cs);
+              load_f32x32(args.sin_t + (long long)pos * half + j * 32, sn);
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (col0 + i < args.N) v[i] += __bfloat162float(rp[i]);
+              for (int i = 0; i < 32; ++i) rope_pair(va[i], vb[i], cs[i], sn[i], va[i], vb[i]);
+            }
+            bf16* cp = reinterpret_cast<bf16*>(args.C) + (long long)row * args.ldc + col_h + j * 32;
+            store_bf16x32(cp, va);
+            store_bf16x32(cp + half, vb);
           }
         }
-        if (args.c_f32) {
-          float* cp = reinterpret_cast<float*>(args.C) + (long long)row * args.ldc + col0;
-          if (full) {
+      } else if (EPI == kEpiSwigluFwd) {
+        // accumulator columns [0, 128) are gate, [128, 256) up, of ffn
+        // columns nb * 128 + [0, 128)
+#pragma unroll 1
+        for (int c = hs * (kBN / 128); c < (hs + 1) * (kBN / 128); ++c) {
+          __syncwarp();
+          uint32_t rg[32], ru[32];
+          tmem_ld_32x32b_x32(tacc + (uint32_t)(c * 32), rg);
+          tmem_ld_32x32b_x32(tacc + (uint32_t)(kBN / 2 + c * 32), ru);
+          tmem_ld_wait();
+          if (!row_ok) continue;
+          const int fc = nb * (kBN / 2) + c * 32;
+          float g[32], u[32], a[32];
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              reinterpret_cast<float4*>(cp)[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (col0 + i < args.N) cp[i] = v[i];
+          for (int i = 0; i < 32; ++i) {
+            g[i] = bf16_round(__uint_as_float(rg[i]));
+            u[i] = bf16_round(__uint_as_float(ru[i]));
+            a[i] = swiglu_fwd_elem(g[i], u[i]);
           }
-        } else {
-          bf16* cp = reinterpret_cast<bf16*>(args.C) + (long long)row * args.ldc + col0;
-          if (full) {
+          bf16* cp = reinterpret_cast<bf16*>(args.C) + (long long)row * args.ldc;
+          store_bf16x32(cp + fc, g);
+          store_bf16x32(cp + args.f + fc, u);
+          store_bf16x32(args.C2 + (long long)row * args.ldc2 + fc, a);
+        }
+      } else if (EPI == kEpiSwigluBwd) {
+        // the tile is da for ffn columns nb * 256 + [0, 256)
+#pragma unroll 1
+        for (int c = hs * (kBN / 64); c < (hs + 1) * (kBN / 64); ++c) {
+          __syncwarp();
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tacc + (uint32_t)(c * 32), r);
+          tmem_ld_wait();
+          const int col0 = nb * kBN + c * 32;
+          if (!row_ok || col0 >= args.N) continue;
+          float g[32], u[32], dg[32], du[32];
+          const bf16* xp = args.X + (long long)row * args.ldx + col0;
+          load_bf16x32(xp, g);
+          load_bf16x32(xp + args.f, u);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint4 u;
-              u.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
-              u.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
-              u.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
-              u.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
-              reinterpret_cast<uint4*>(cp)[j] = u;
+          for (int i = 0; i < 32; ++i) swiglu_bwd_elem(bf16_round(__uint_as_float(r[i])), g[i], u[i], dg[i], du[i]);
+          bf16* cp = reinterpret_cast<bf16*>(args.C) + (long long)row * args.ldc + col0;
+          store_bf16x32(cp, dg);
+          store_bf16x32(cp + args.f, du);
+        }
+      } else {
+#pragma unroll 1
+        for (int c = hs * (kBN / 64); c < (hs + 1) * (kBN / 64); ++c) {
+          __syncwarp();
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tacc + (uint32_t)(c * 32), r);
+          tmem_ld_wait();
+          const int col0 = nb * kBN + c * 32;
+          if (!row_ok || col0 >= args.N) continue;
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+          const bool full = col0 + 32 <= args.N;
+          if (args.R != nullptr) {
+            const bf16* rp = args.R + (long long)row * args.ldr + col0;
+            if (full) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint4 u = reinterpret_cast<const uint4*>(rp)[j];
+                float2 f0 = unpack_bf16x2(u.x), f1 = unpack_bf16x2(u.y), f2 = unpack_bf16x2(u.z),
+                       f3 = unpack_bf16x2(u.w);
+                v[j * 8 + 0] += f0.x; v[j * 8 + 1] += f0.y; v[j * 8 + 2] += f1.x; v[j * 8 + 3] += f1.y;
+                v[j * 8 + 4] += f2.x; v[j * 8 + 5] += f2.y; v[j * 8 + 6] += f3.x; v[j * 8 + 7] += f3.y;
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (col0 + i < args.N) v[i] += __bfloat162float(rp[i]);
+            }
+          }
+          if (args.c_f32) {
+            float* cp = reinterpret_cast<float*>(args.C) + (long long)row * args.ldc + col0;
+            if (full) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                reinterpret_cast<float4*>(cp)[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (col0 + i < args.N) cp[i] = v[i];
             }
           } else {
+            bf16* cp = reinterpret_cast<bf16*>(args.C) + (long long)row * args.ldc + col0;
+            if (full) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (col0 + i < args.N) cp[i] = __float2bfloat16_rn(v[i]);
+              for (int j = 0; j < 4; ++j) {
+                uint4 u;
+                u.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
+                u.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
+                u.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
+                u.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
+                reinterpret_cast<uint4*>(cp)[j] = u;
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (col0 + i < args.N) cp[i] = __float2bfloat16_rn(v[i]);
+            }
           }
         }
       }
@@ -275,10 +416,16 @@ int get_encode() {
     int dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaFuncSetAttribute(gemm_abt_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    cudaFuncSetAttribute(gemm_abt_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    cudaFuncSetAttribute(gemm_abt_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    cudaFuncSetAttribute(gemm_abt_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    const int sm = (int)kSmemBytes;
+    cudaFuncSetAttribute(gemm_abt_kernel<false, false, kEpiPlain>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+    cudaFuncSetAttribute(gemm_abt_kernel<false, true, kEpiPlain>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+    cudaFuncSetAttribute(gemm_abt_kernel<true, false, kEpiPlain>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+    cudaFuncSetAttribute(gemm_abt_kernel<true, true, kEpiPlain>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+    cudaFuncSetAttribute(gemm_abt_kernel<false, false, kEpiRope>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+    cudaFuncSetAttribute(gemm_abt_kernel<false, false, kEpiSwigluFwd>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         sm);
+    cudaFuncSetAttribute(gemm_abt_kernel<false, true, kEpiSwigluBwd>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         sm);
   });
   return g_encode ? 0 : -1;
 }
@@ -299,45 +446,115 @@ int make_tmap(CUtensorMap* m, const void* ptr, long long rows, long long cols, l
 
 }  // namespace
 
-int gemm_ex(const void* A, long long lda, int a_mn, const void* B, long long ldb, int b_mn, void* C, long long ldc,
-            int c_f32, const void* R, long long ldr, int M, int N, int K, cudaStream_t stream) {
+namespace {
+
+// Validates the operands, builds the tensor maps and launches one GEMM with
+// the epilogue `epi` (whose extra fields `args` already holds).
+int launch(int epi, const void* A, long long lda, int a_mn, const void* B, long long ldb, int b_mn, GemmArgs& args,
+           cudaStream_t stream) {
+  const int M = args.M, N = args.N, K = args.K;
   if (M < 0 || N < 0 || K < 0) return MT_EINVAL;
   if (M == 0 || N == 0) return MT_OK;
   if (K == 0) return MT_EINVAL;
   if (get_encode() != 0) return MT_ECUDA;
   // TMA: 16-byte aligned bases and row pitches; vector epilogue: 16-byte rows.
   auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
-  if (!al16(A) || !al16(B) || !al16(C) || (R && !al16(R))) return MT_EINVAL;
+  if (!al16(A) || !al16(B) || !al16(args.C) || (args.R && !al16(args.R))) return MT_EINVAL;
   if ((lda * 2) % 16 || (ldb * 2) % 16) return MT_EINVAL;
   if (a_mn ? lda < M : lda < K) return MT_EINVAL;
   if (b_mn ? ldb < N : ldb < K) return MT_EINVAL;
-  if (ldc < N || (c_f32 ? (ldc % 4) : (ldc % 8))) return MT_EINVAL;
-  if (R && (ldr % 8 || ldr < N)) return MT_EINVAL;
+  if (args.ldc < N || (args.c_f32 ? (args.ldc % 4) : (args.ldc % 8))) return MT_EINVAL;
+  if (args.R && (args.ldr % 8 || args.ldr < N)) return MT_EINVAL;
   CUtensorMap ta, tb;
   // K-major: rows = M (or N), cols = K, box kBM (kBN) x 64; MN-major: rows = K,
-  // cols = M (or N), box 64 x 64.
+  // cols = M (or N), box 64 x 64. The SwiGLU forward loads its B tile as two
+  // 128-row boxes (gate rows, then up rows).
   const int ea = a_mn ? make_tmap(&ta, A, K, M, lda, kBK, 64) : make_tmap(&ta, A, M, K, lda, kBM, kBK);
-  const int eb = b_mn ? make_tmap(&tb, B, K, N, ldb, kBK, 64) : make_tmap(&tb, B, N, K, ldb, kBN, kBK);
+  const int eb = b_mn ? make_tmap(&tb, B, K, N, ldb, kBK, 64)
+                      : make_tmap(&tb, B, N, K, ldb, epi == kEpiSwigluFwd ? kBN / 2 : kBN, kBK);
   if (ea || eb) return MT_EINVAL;
-  GemmArgs args;
-  args.M = M;
-  args.N = N;
-  args.K = K;
-  args.C = C;
-  args.ldc = ldc;
-  args.R = reinterpret_cast<const bf16*>(R);
-  args.ldr = ldr;
-  args.c_f32 = c_f32;
   args.num_mb = (M + kBM - 1) / kBM;
   args.num_nb = (N + kBN - 1) / kBN;
   args.err = device_error_word();
   const int tiles = args.num_mb * args.num_nb;
   const int grid = tiles < g_num_sms ? tiles : g_num_sms;
-  if (!a_mn && !b_mn) gemm_abt_kernel<false, false><<<grid, kThreads, kSmemBytes, stream>>>(ta, tb, args);
-  else if (!a_mn) gemm_abt_kernel<false, true><<<grid, kThreads, kSmemBytes, stream>>>(ta, tb, args);
-  else if (!b_mn) gemm_abt_kernel<true, false><<<grid, kThreads, kSmemBytes, stream>>>(ta, tb, args);
-  else gemm_abt_kernel<true, true><<<grid, kThreads, kSmemBytes, stream>>>(ta, tb, args);
+  if (epi == kEpiRope) {
+    if (a_mn || b_mn) return MT_EINVAL;
+    gemm_abt_kernel<false, false, kEpiRope><<<grid, kThreads, kSmemBytes, stream>>>(ta, tb, args);
+  } else if (epi == kEpiSwigluFwd) {
+    if (a_mn || b_mn) return MT_EINVAL;
+    gemm_abt_kernel<false, false, kEpiSwigluFwd><<<grid, kThreads, kSmemBytes, stream>>>(ta, tb, args);
+  } else if (epi == kEpiSwigluBwd) {
+    if (a_mn || !b_mn) return MT_EINVAL;
+    gemm_abt_kernel<false, true, kEpiSwigluBwd><<<grid, kThreads, kSmemBytes, stream>>>(ta, tb, args);
+  } else if (!a_mn && !b_mn) {
+    gemm_abt_kernel<false, false, kEpiPlain><<<grid, kThreads, kSmemBytes, stream>>>(ta, tb, args);
+  } else if (!a_mn) {
+    gemm_abt_kernel<false, true, kEpiPlain><<<grid, kThreads, kSmemBytes, stream>>>(ta, tb, args);
+  } else if (!b_mn) {
+    gemm_abt_kernel<true, false, kEpiPlain><<<grid, kThreads, kSmemBytes, stream>>>(ta, tb, args);
+  } else {
+    gemm_abt_kernel<true, true, kEpiPlain><<<grid, kThreads, kSmemBytes, stream>>>(ta, tb, args);
+  }
   return cudaGetLastError() == cudaSuccess ? MT_OK : MT_ECUDA;
+}
+
+GemmArgs base_args(int M, int N, int K, void* C, long long ldc, int c_f32) {
+  GemmArgs a{};
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.C = C;
+  a.ldc = ldc;
+  a.c_f32 = c_f32;
+  return a;
+}
+
+bool al16p(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+int gemm_ex(const void* A, long long lda, int a_mn, const void* B, long long ldb, int b_mn, void* C, long long ldc,
+            int c_f32, const void* R, long long ldr, int M, int N, int K, cudaStream_t stream) {
+  GemmArgs args = base_args(M, N, K, C, ldc, c_f32);
+  args.R = reinterpret_cast<const bf16*>(R);
+  args.ldr = ldr;
+  return launch(kEpiPlain, A, lda, a_mn, B, ldb, b_mn, args, stream);
+}
+
+int gemm_rope(const void* A, long long lda, const void* B, long long ldb, void* C, long long ldc, int M, int N, int K,
+              const float* cos_t, const float* sin_t, int rot_cols, int hd, int seq, cudaStream_t stream) {
+  if (hd <= 0 || hd % 64 || (kBN / 2) % hd || N % hd || rot_cols < 0 || rot_cols % hd || rot_cols > N || seq <= 0 ||
+      !cos_t || !sin_t || ldc % 8)
+    return MT_EINVAL;
+  GemmArgs args = base_args(M, N, K, C, ldc, 0);
+  args.cos_t = cos_t;
+  args.sin_t = sin_t;
+  args.rot_cols = rot_cols;
+  args.hd = hd;
+  args.seq = seq;
+  return launch(kEpiRope, A, lda, 0, B, ldb, 0, args, stream);
+}
+
+int gemm_swiglu_fwd(const void* A, long long lda, const void* W, long long ldw, void* gu, long long ldgu, void* a,
+                    long long lda_out, int M, int f, int K, cudaStream_t stream) {
+  if (f <= 0 || f % (kBN / 2) || ldgu < 2LL * f || ldgu % 8 || lda_out < f || lda_out % 8 || !al16p(a))
+    return MT_EINVAL;
+  GemmArgs args = base_args(M, 2 * f, K, gu, ldgu, 0);
+  args.C2 = reinterpret_cast<bf16*>(a);
+  args.ldc2 = lda_out;
+  args.f = f;
+  return launch(kEpiSwigluFwd, A, lda, 0, W, ldw, 0, args, stream);
+}
+
+int gemm_swiglu_bwd(const void* dy, long long lddy, const void* W, long long ldw, const void* gu, long long ldgu,
+                    void* dgu, long long lddgu, int M, int f, int K, cudaStream_t stream) {
+  if (f <= 0 || f % 32 || ldgu < 2LL * f || ldgu % 8 || lddgu < 2LL * f || lddgu % 8 || !al16p(gu)) return MT_EINVAL;
+  GemmArgs args = base_args(M, f, K, dgu, lddgu, 0);
+  args.X = reinterpret_cast<const bf16*>(gu);
+  args.ldx = ldgu;
+  args.f = f;
+  return launch(kEpiSwigluBwd, dy, lddy, 0, W, ldw, 1, args, stream);
 }
 
 int gemm_abt(const void* A, long long lda, const void* B, long long ldb, void* C, long long ldc, int c_f32,

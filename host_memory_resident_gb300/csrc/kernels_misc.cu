@@ -35,9 +35,9 @@ int* device_error_word() {
 
 namespace {
 
-constexpr int kNormBwdMaxVec = 4;       // 16-byte vectors per thread: d <= 8192
-constexpr int kNormBwdThreads = 256;
-constexpr int kNormBwdMaxParts = 608;   // 4 blocks per SM on 152 SMs
+constexpr int kNormBwdVec = 4;          // 8-element vectors per thread and row: 32 elements
+constexpr int kNormBwdMaxWarps = 8;     // warps per row: d <= 8 * 32 * 32 = 8192
+constexpr int kNormBwdMaxParts = 608;   // row groups (dw partial sums): 4 per SM on 152 SMs
 
 inline int launch_ok() { return cudaGetLastError() == cudaSuccess ? MT_OK : MT_ECUDA; }
 
@@ -93,67 +93,96 @@ __global__ void rmsnorm_fwd_kernel(const bf16* __restrict__ x, const bf16* __res
 }
 
 // ------------------------------------------------------------ RMSNorm bwd
-// Block b handles a contiguous row range; per row: dot = sum(dy*w*x),
-// dx = rstd*w*dy - x*rstd^3*dot/d (+ dres); dw partial += dy*x*rstd.
-__global__ void __launch_bounds__(kNormBwdThreads)
+// Row groups of W warps (W = ceil(d / 1024)); each thread holds up to 32
+// elements of a row. Group g takes a contiguous range of rows; per row:
+// dot = sum(dy*w*x) (warp shuffles, then one named barrier across the
+// group's warps), dx = rstd*w*dy - x*rstd^3*dot/d (+ dres), and the thread's
+// dw partial += dy*x*rstd. The group's partial goes to partial[g] and the
+// column sums run in a fixed order, so dw is deterministic.
+template <int W>
+__global__ void __launch_bounds__(256, 2)
     rmsnorm_bwd_kernel(const float* __restrict__ dy, const bf16* __restrict__ x, const bf16* __restrict__ w,
                        const float* __restrict__ rstd, const float* dres, float* dx_f32, bf16* __restrict__ dx_bf16,
-                       float* __restrict__ partial, int M, int d, int rows_per_block) {
-  __shared__ float red[kNormBwdThreads / 32];
-  const int tid = threadIdx.x;
+                       float* __restrict__ partial, int M, int d, int n_groups, int rows_per_group) {
+  constexpr int G = 8 / W > 0 ? 8 / W : 1;  // groups per block
+  __shared__ float red[G][2][W];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gl = warp / W, wg = warp % W;   // group within the block, warp within the group
+  const int gid = blockIdx.x * G + gl;
+  if (gid >= n_groups) return;  // whole groups leave together (named barriers count only their warps)
   const int nvec = d >> 3;
-  const int r0 = blockIdx.x * rows_per_block;
-  const int r1 = min(M, r0 + rows_per_block);
-  float wv[kNormBwdMaxVec][8];
-  float acc[kNormBwdMaxVec][8];
+  const int r0 = gid * rows_per_group, r1 = min(M, r0 + rows_per_group);
+  uint4 wp[kNormBwdVec];                    // w as packed bf16 pairs
+  float acc[kNormBwdVec][8];
 #pragma unroll
-  for (int k = 0; k < kNormBwdMaxVec; ++k) {
-    const int v = tid + k * kNormBwdThreads;
+  for (int k = 0; k < kNormBwdVec; ++k) {
+    const int v = lane + 32 * (wg + W * k);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) { acc[k][i] = 0.f; wv[k][i] = 0.f; }
-    if (v < nvec) load_bf16x8(w + v * 8, wv[k]);
+    for (int i = 0; i < 8; ++i) acc[k][i] = 0.f;
+    wp[k] = v < nvec ? *reinterpret_cast<const uint4*>(w + v * 8) : make_uint4(0, 0, 0, 0);
   }
-  for (int row = r0; row < r1; ++row) {
+  for (int row = r0, it = 0; row < r1; ++row, ++it) {
     const float r = rstd[row];
     const float* dyr = dy + (long long)row * d;
     const bf16* xr = x + (long long)row * d;
-    float dyv[kNormBwdMaxVec][8], xv[kNormBwdMaxVec][8];
+    float dyv[kNormBwdVec][8];
+    uint4 xp[kNormBwdVec];
     float dot = 0.f;
 #pragma unroll
-    for (int k = 0; k < kNormBwdMaxVec; ++k) {
-      const int v = tid + k * kNormBwdThreads;
+    for (int k = 0; k < kNormBwdVec; ++k) {
+      const int v = lane + 32 * (wg + W * k);
       if (v < nvec) {
-        float4 a = reinterpret_cast<const float4*>(dyr + v * 8)[0];
-        float4 b = reinterpret_cast<const float4*>(dyr + v * 8)[1];
+        const float4 a = reinterpret_cast<const float4*>(dyr + v * 8)[0];
+        const float4 b = reinterpret_cast<const float4*>(dyr + v * 8)[1];
         dyv[k][0] = a.x; dyv[k][1] = a.y; dyv[k][2] = a.z; dyv[k][3] = a.w;
         dyv[k][4] = b.x; dyv[k][5] = b.y; dyv[k][6] = b.z; dyv[k][7] = b.w;
-        load_bf16x8(xr + v * 8, xv[k]);
+        xp[k] = *reinterpret_cast<const uint4*>(xr + v * 8);
+      } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) dot += dyv[k][i] * wv[k][i] * xv[k][i];
+        for (int i = 0; i < 8; ++i) dyv[k][i] = 0.f;
+        xp[k] = make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kNormBwdVec; ++k) {
+      const uint32_t xw[4] = {xp[k].x, xp[k].y, xp[k].z, xp[k].w};
+      const uint32_t ww[4] = {wp[k].x, wp[k].y, wp[k].z, wp[k].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 xf = unpack_bf16x2(xw[i]), wf = unpack_bf16x2(ww[i]);
+        dot += dyv[k][2 * i] * wf.x * xf.x;
+        dot += dyv[k][2 * i + 1] * wf.y * xf.y;
       }
     }
     dot = warp_sum(dot);
-    if ((tid & 31) == 0) red[tid >> 5] = dot;
-    __syncthreads();
-    float tot = 0.f;
+    float tot = dot;
+    if (W > 1) {
+      if (lane == 0) red[gl][it & 1][wg] = dot;
+      asm volatile("bar.sync %0, %1;" ::"r"(1 + gl), "r"(32 * W) : "memory");
+      tot = 0.f;
 #pragma unroll
-    for (int i = 0; i < kNormBwdThreads / 32; ++i) tot += red[i];
-    __syncthreads();
+      for (int i = 0; i < W; ++i) tot += red[gl][it & 1][i];
+    }
     const float c = r * r * r * tot / (float)d;
 #pragma unroll
-    for (int k = 0; k < kNormBwdMaxVec; ++k) {
-      const int v = tid + k * kNormBwdThreads;
+    for (int k = 0; k < kNormBwdVec; ++k) {
+      const int v = lane + 32 * (wg + W * k);
       if (v < nvec) {
+        const uint32_t xw[4] = {xp[k].x, xp[k].y, xp[k].z, xp[k].w};
+        const uint32_t ww[4] = {wp[k].x, wp[k].y, wp[k].z, wp[k].w};
         float o[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          o[i] = r * wv[k][i] * dyv[k][i] - xv[k][i] * c;
-          acc[k][i] += dyv[k][i] * xv[k][i] * r;
+        for (int i = 0; i < 4; ++i) {
+          const float2 xf = unpack_bf16x2(xw[i]), wf = unpack_bf16x2(ww[i]);
+          o[2 * i] = r * wf.x * dyv[k][2 * i] - xf.x * c;
+          o[2 * i + 1] = r * wf.y * dyv[k][2 * i + 1] - xf.y * c;
+          acc[k][2 * i] += dyv[k][2 * i] * xf.x * r;
+          acc[k][2 * i + 1] += dyv[k][2 * i + 1] * xf.y * r;
         }
         const long long off = (long long)row * d + v * 8;
         if (dres != nullptr) {
-          float4 a = reinterpret_cast<const float4*>(dres + off)[0];
-          float4 b = reinterpret_cast<const float4*>(dres + off)[1];
+          const float4 a = reinterpret_cast<const float4*>(dres + off)[0];
+          const float4 b = reinterpret_cast<const float4*>(dres + off)[1];
           o[0] += a.x; o[1] += a.y; o[2] += a.z; o[3] += a.w;
           o[4] += b.x; o[5] += b.y; o[6] += b.z; o[7] += b.w;
         }
@@ -166,23 +195,35 @@ __global__ void __launch_bounds__(kNormBwdThreads)
     }
   }
 #pragma unroll
-  for (int k = 0; k < kNormBwdMaxVec; ++k) {
-    const int v = tid + k * kNormBwdThreads;
+  for (int k = 0; k < kNormBwdVec; ++k) {
+    const int v = lane + 32 * (wg + W * k);
     if (v < nvec) {
-      float* p = partial + (long long)blockIdx.x * d + v * 8;
+      float* p = partial + (long long)gid * d + v * 8;
       reinterpret_cast<float4*>(p)[0] = make_float4(acc[k][0], acc[k][1], acc[k][2], acc[k][3]);
       reinterpret_cast<float4*>(p)[1] = make_float4(acc[k][4], acc[k][5], acc[k][6], acc[k][7]);
     }
   }
 }
 
-// dw[c] = sum over parts p (in order) of partial[p, c], rounded to bf16.
-__global__ void colsum_to_bf16_kernel(const float* __restrict__ partial, int n_part, int d, bf16* __restrict__ out) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= d) return;
+// dw[c] = sum over parts p of partial[p, c], rounded to bf16. Block: 32
+// columns x 8 part classes; class j sums parts j, j+8, ... in order, then
+// the 8 class sums are added in order (a fixed order for every launch).
+__global__ void __launch_bounds__(256)
+    colsum_to_bf16_kernel(const float* __restrict__ partial, int n_part, int d, bf16* __restrict__ out) {
+  __shared__ float cls[8][32];
+  const int cl = threadIdx.x & 31, j = threadIdx.x >> 5;
+  const int c = blockIdx.x * 32 + cl;
   float s = 0.f;
-  for (int p = 0; p < n_part; ++p) s += partial[(long long)p * d + c];
-  out[c] = __float2bfloat16_rn(s);
+  if (c < d)
+    for (int p = j; p < n_part; p += 8) s += partial[(long long)p * d + c];
+  cls[j][cl] = s;
+  __syncthreads();
+  if (j == 0 && c < d) {
+    float t = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) t += cls[i][cl];
+    out[c] = __float2bfloat16_rn(t);
+  }
 }
 
 // ------------------------------------------------------------------ RoPE
@@ -207,13 +248,14 @@ __global__ void rope_kernel(bf16* __restrict__ xbuf, long long ld, int M, int s,
   const float2 b = __bfloat1622float2(*pb);
   const float c0 = cos_t[(long long)t * half + i], c1 = cos_t[(long long)t * half + i + 1];
   const float s0 = sign * sin_t[(long long)t * half + i], s1 = sign * sin_t[(long long)t * half + i + 1];
-  *pa = __floats2bfloat162_rn(a.x * c0 - b.x * s0, a.y * c1 - b.y * s1);
-  *pb = __floats2bfloat162_rn(b.x * c0 + a.x * s0, b.y * c1 + a.y * s1);
+  float o1x, o2x, o1y, o2y;
+  rope_pair(a.x, b.x, c0, s0, o1x, o2x);
+  rope_pair(a.y, b.y, c1, s1, o1y, o2y);
+  *pa = __floats2bfloat162_rn(o1x, o1y);
+  *pb = __floats2bfloat162_rn(o2x, o2y);
 }
 
 // ---------------------------------------------------------------- SwiGLU
-__device__ __forceinline__ float sigmoidf_(float g) { return 1.f / (1.f + expf(-g)); }
-
 __global__ void swiglu_fwd_kernel(const bf16* __restrict__ gu, bf16* __restrict__ a, int M, int f) {
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const int nv = f >> 3;
@@ -225,7 +267,7 @@ __global__ void swiglu_fwd_kernel(const bf16* __restrict__ gu, bf16* __restrict_
   load_bf16x8(gr, g);
   load_bf16x8(gr + f, u);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) o[i] = g[i] * sigmoidf_(g[i]) * u[i];
+  for (int i = 0; i < 8; ++i) o[i] = swiglu_fwd_elem(g[i], u[i]);
   store_bf16x8(a + (long long)row * f + v * 8, o);
 }
 
@@ -242,11 +284,7 @@ __global__ void swiglu_bwd_kernel(const bf16* __restrict__ da, const bf16* __res
   load_bf16x8(gr + f, u);
   load_bf16x8(da + (long long)row * f + v * 8, d);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float sg = sigmoidf_(g[i]);
-    dg[i] = d[i] * u[i] * sg * (1.f + g[i] * (1.f - sg));
-    du[i] = d[i] * g[i] * sg;
-  }
+  for (int i = 0; i < 8; ++i) swiglu_bwd_elem(d[i], g[i], u[i], dg[i], du[i]);
   bf16* o = dgu + (long long)row * 2 * f + v * 8;
   store_bf16x8(o, dg);
   store_bf16x8(o + f, du);
@@ -531,6 +569,21 @@ int mt_k_gemm_ex(const void* A, int64_t lda, int a_mn_major, const void* B, int6
   return gemm_ex(A, lda, a_mn_major, B, ldb, b_mn_major, C, ldc, c_f32, R, ldr, M, N, K, (cudaStream_t)stream);
 }
 
+int mt_k_gemm_rope(const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, int M, int N, int K,
+                   const float* cos_t, const float* sin_t, int rot_cols, int hd, int seq, void* stream) {
+  return gemm_rope(A, lda, B, ldb, C, ldc, M, N, K, cos_t, sin_t, rot_cols, hd, seq, (cudaStream_t)stream);
+}
+
+int mt_k_gemm_swiglu_fwd(const void* A, int64_t lda, const void* W, int64_t ldw, void* gu, int64_t ldgu, void* a,
+                         int64_t lda_out, int M, int f, int K, void* stream) {
+  return gemm_swiglu_fwd(A, lda, W, ldw, gu, ldgu, a, lda_out, M, f, K, (cudaStream_t)stream);
+}
+
+int mt_k_gemm_swiglu_bwd(const void* dy, int64_t lddy, const void* W, int64_t ldw, const void* gu, int64_t ldgu,
+                         void* dgu, int64_t lddgu, int M, int f, int K, void* stream) {
+  return gemm_swiglu_bwd(dy, lddy, W, ldw, gu, ldgu, dgu, lddgu, M, f, K, (cudaStream_t)stream);
+}
+
 int mt_k_transpose(const void* in, int64_t ld_in, void* out, int64_t ld_out, int rows, int cols, void* stream) {
   if (rows < 0 || cols < 0 || ld_in < cols || ld_out < rows) return MT_EINVAL;
   if (rows == 0 || cols == 0) return MT_OK;
@@ -552,20 +605,36 @@ int mt_k_rmsnorm_bwd_parts(int M) { return M < kNormBwdMaxParts ? (M > 0 ? M : 1
 
 int mt_k_rmsnorm_bwd(const float* dy, const void* x, const void* w, const float* rstd, const float* dres,
                      float* dx_f32, void* dx_bf16, float* partial, void* dw_out, int M, int d, void* stream) {
-  if (M < 0 || d <= 0 || d % 8 || d > 8 * kNormBwdThreads * kNormBwdMaxVec) return MT_EINVAL;
+  if (M < 0 || d <= 0 || d % 8 || d > 8 * kNormBwdVec * 32 * kNormBwdMaxWarps) return MT_EINVAL;
   if (!al16(dy) || !al16(x) || !al16(w) || (dres && !al16(dres)) || (dx_f32 && !al16(dx_f32)) ||
       (dx_bf16 && !al16(dx_bf16)) || !al16(partial))
     return MT_EINVAL;
   cudaStream_t st = (cudaStream_t)stream;
   const int parts = mt_k_rmsnorm_bwd_parts(M);
   if (M > 0) {
-    const int rpb = (M + parts - 1) / parts;
-    rmsnorm_bwd_kernel<<<parts, kNormBwdThreads, 0, st>>>(dy, (const bf16*)x, (const bf16*)w, rstd, dres, dx_f32,
-                                                          (bf16*)dx_bf16, partial, M, d, rpb);
+    const int W = (d + 8 * kNormBwdVec * 32 - 1) / (8 * kNormBwdVec * 32);  // warps per row
+    const int rpg = (M + parts - 1) / parts;
+    const int ngroups = (M + rpg - 1) / rpg;  // every group has at least one row
+    auto go = [&](auto kernel, int w_) {
+      const int g = 8 / w_ > 0 ? 8 / w_ : 1;
+      kernel<<<(ngroups + g - 1) / g, 32 * w_ * g, 0, st>>>(dy, (const bf16*)x, (const bf16*)w, rstd, dres, dx_f32,
+                                                           (bf16*)dx_bf16, partial, M, d, ngroups, rpg);
+    };
+    switch (W) {
+      case 1: go(rmsnorm_bwd_kernel<1>, 1); break;
+      case 2: go(rmsnorm_bwd_kernel<2>, 2); break;
+      case 3: go(rmsnorm_bwd_kernel<3>, 3); break;
+      case 4: go(rmsnorm_bwd_kernel<4>, 4); break;
+      case 5: go(rmsnorm_bwd_kernel<5>, 5); break;
+      case 6: go(rmsnorm_bwd_kernel<6>, 6); break;
+      case 7: go(rmsnorm_bwd_kernel<7>, 7); break;
+      default: go(rmsnorm_bwd_kernel<8>, 8); break;
+    }
+    colsum_to_bf16_kernel<<<(d + 31) / 32, 256, 0, st>>>(partial, ngroups, d, (bf16*)dw_out);
   } else {
     cudaMemsetAsync(partial, 0, sizeof(float) * d, st);
+    colsum_to_bf16_kernel<<<(d + 31) / 32, 256, 0, st>>>(partial, 1, d, (bf16*)dw_out);
   }
-  colsum_to_bf16_kernel<<<(d + 255) / 256, 256, 0, st>>>(partial, parts, d, (bf16*)dw_out);
   return launch_ok();
 }
 

@@ -22,6 +22,15 @@ void set_last_error_message(const std::string& msg);
 int gemm_ex(const void* A, long long lda, int a_mn, const void* B, long long ldb, int b_mn, void* C, long long ldc,
             int c_f32, const void* R, long long ldr, int M, int N, int K, cudaStream_t stream);
 
+// GEMMs with fused epilogues; see mt_k_gemm_rope, mt_k_gemm_swiglu_fwd,
+// mt_k_gemm_swiglu_bwd.
+int gemm_rope(const void* A, long long lda, const void* B, long long ldb, void* C, long long ldc, int M, int N, int K,
+              const float* cos_t, const float* sin_t, int rot_cols, int hd, int seq, cudaStream_t stream);
+int gemm_swiglu_fwd(const void* A, long long lda, const void* W, long long ldw, void* gu, long long ldgu, void* a,
+                    long long lda_out, int M, int f, int K, cudaStream_t stream);
+int gemm_swiglu_bwd(const void* dy, long long lddy, const void* W, long long ldw, const void* gu, long long ldgu,
+                    void* dgu, long long lddgu, int M, int f, int K, cudaStream_t stream);
+
 // Causal GQA attention forward on tcgen05 (hd 64 or 128); see mt_k_attn_fwd.
 int attn_fwd_tc(const void* qkv, long long ld, void* o, long long ldo, float* lse, int B, int s, int H, int Hkv,
                 int hd, cudaStream_t stream);

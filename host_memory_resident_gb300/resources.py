@@ -28,15 +28,17 @@ def streamed_units(n_layers: int, ckpt_interval: int) -> list[int]:
     """Units copied host-to-device in one streamed step, in order.
 
     The step visits units as: embedding, layers 1..L, head (forward); then per
-    checkpoint segment, last to first, its layers in order (recompute) and in
-    reverse (backward). Two device buffers hold the two most recently used
-    units; a visit to a unit not held loads it into the least recently used.
+    checkpoint segment, last to first, its layers in order (recompute, except
+    for the last segment, whose activations the forward keeps) and in reverse
+    (backward). Two device buffers hold the two most recently used units; a
+    visit to a unit not held loads it into the least recently used.
     """
     L, C = n_layers, ckpt_interval
     visits = list(range(L + 2))
-    for a in reversed(range(0, L, C)):
+    starts = list(range(0, L, C))
+    for a in reversed(starts):
         seg = list(range(1 + a, 1 + min(L, a + C)))
-        visits += seg + seg[::-1]
+        visits += (seg if a != starts[-1] else []) + seg[::-1]
     held, loads = [], []
     for u in visits:
         if u in held:

@@ -64,6 +64,9 @@ typedef struct mt_config {
                             the host worker finishes Adam on the last units; the next step uploads each
                             unit only after its Adam has finished. Results are identical to 0. Call
                             mt_sync before reading master / m / v yourself. */
+  int32_t unfused_epilogues; /* 1: RoPE and SwiGLU (forward and backward) run as separate kernels
+                                after their GEMMs instead of in the GEMM epilogues; the results are
+                                bitwise identical either way (0, the default, is faster) */
 } mt_config;
 
 /* One tensor of the flat layout. kind 0 = matrix, 1 = norm weight. */
@@ -211,6 +214,21 @@ int mt_get_stream(mt_handle* h, int which, void** stream);
 int mt_profile_enable(mt_handle* h, int on);
 /* Copies the accumulated per-class profile; reset = 1 clears it. */
 int mt_profile_read(mt_handle* h, mt_kernel_profile* out, int reset);
+
+/* One launch or copy of the last profiled step: its class (MT_PROF_*), the
+ * stream it ran on (0 compute, 1 host-to-device, 2 device-to-host) and its
+ * start and end in ms after that step's first compute-stream event (a copy
+ * may start before it: negative). */
+typedef struct mt_timeline_rec {
+  int32_t cls;
+  int32_t stream;
+  double start_ms, end_ms;
+} mt_timeline_rec;
+
+/* Copies up to `cap` records of the last step run with profiling enabled
+ * (in issue order) into `out` and sets *n_out to their total number (call
+ * with cap = 0 to size the buffer). No records before a profiled step. */
+int mt_profile_timeline(mt_handle* h, mt_timeline_rec* out, int cap, int* n_out);
 int mt_destroy(mt_handle* h);
 /* Last error message of `h`, or of the calling thread when h is NULL. */
 const char* mt_last_error(mt_handle* h);

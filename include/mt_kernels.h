@@ -52,6 +52,39 @@ int mt_k_gemm(const void* A, int64_t lda, const void* B, int64_t ldb, void* C, i
 int mt_k_gemm_ex(const void* A, int64_t lda, int a_mn_major, const void* B, int64_t ldb, int b_mn_major, void* C,
                  int64_t ldc, int c_f32, const void* R, int64_t ldr, int M, int N, int K, void* stream);
 
+/*
+ * QKV projection with RoPE in the epilogue: C = A B^T as mt_k_gemm (bf16 C),
+ * then each row's columns [0, rot_cols) - heads of hd columns - are rotated
+ * like mt_k_rope (inverse = 0) at position (row mod seq), from the
+ * bf16-rounded products. The result equals mt_k_gemm followed by mt_k_rope
+ * bit for bit (the zhichai.net article's stateless template, point 4: the
+ * attention input of one layer). hd 64 or 128, N and rot_cols multiples of
+ * hd; cos/sin fp32 [seq_max, hd/2].
+ */
+int mt_k_gemm_rope(const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, int M, int N, int K,
+                   const float* cos_t, const float* sin_t, int rot_cols, int hd, int seq, void* stream);
+
+/*
+ * Gate/up projection with SwiGLU in the epilogue: W bf16 [2f, K] holds the
+ * gate rows then the up rows (K-major, like mt_k_gemm's B). Writes
+ * gu = A W^T (bf16 [M, 2f], row pitch ldgu) and a = silu(gate) * up from the
+ * bf16-rounded gate and up (bf16 [M, f], row pitch lda_out): the same bits as
+ * mt_k_gemm then mt_k_swiglu_fwd. f a multiple of 128.
+ */
+int mt_k_gemm_swiglu_fwd(const void* A, int64_t lda, const void* W, int64_t ldw, void* gu, int64_t ldgu, void* a,
+                         int64_t lda_out, int M, int f, int K, void* stream);
+
+/*
+ * Down projection input gradient with the SwiGLU backward in the epilogue:
+ * da = dy W (dy bf16 [M, K], W the down weight bf16 [K, f] read in place, as
+ * mt_k_gemm_ex with b_mn_major = 1) is rounded to bf16 and turned into
+ * dgu = (d gate | d up) [M, 2f] with gate | up read from gu [M, 2f]; da is
+ * never written. The same bits as mt_k_gemm_ex then mt_k_swiglu_bwd. f a
+ * multiple of 32.
+ */
+int mt_k_gemm_swiglu_bwd(const void* dy, int64_t lddy, const void* W, int64_t ldw, const void* gu, int64_t ldgu,
+                         void* dgu, int64_t lddgu, int M, int f, int K, void* stream);
+
 /* out[c, r] = in[r, c] for a bf16 [rows, cols] matrix (ld_in >= cols, ld_out >= rows). */
 int mt_k_transpose(const void* in, int64_t ld_in, void* out, int64_t ld_out, int rows, int cols, void* stream);
 

@@ -191,6 +191,71 @@ def test_swiglu(M, f):
     assert_close(host(dgu), np.concatenate([dg, du], 1), l2=5e-3, elem=1e-2, what="swiglu bwd")
 
 
+# ------------------------------------------------------- fused GEMM epilogues
+# Each fused GEMM must give the bits of the GEMM followed by the separate
+# element-wise kernel (both round to bf16 at the same points and share the
+# element-wise arithmetic); the separate kernels are checked against the
+# oracle above, the fused ones once more here.
+@pytest.mark.parametrize("Bt,seq,H,Hkv,hd,K", [(3, 100, 8, 2, 64, 192), (1, 257, 4, 2, 128, 128),
+                                               (2, 260, 32, 4, 64, 2048)])
+def test_gemm_rope_equals_gemm_then_rope(Bt, seq, H, Hkv, hd, K):
+    rng = np.random.default_rng(seq + hd + K)
+    M, N = Bt * seq, (H + 2 * Hkv) * hd
+    A, Ah = bf(rng.standard_normal((M, K)))
+    W, Wh = bf(rng.standard_normal((N, K)) / np.sqrt(K))
+    cos, sin = ops.rope_tables(seq, hd, 10000.0)
+    ct, _ = f32(cos)
+    st, _ = f32(sin)
+    ref = torch.empty((M, N), device=DEV, dtype=torch.bfloat16)
+    mt.k_gemm(A, W, ref)
+    mt.k_rope(ref, Bt, seq, H + Hkv, hd, ct, st)
+    got = torch.full((M, N), float("nan"), device=DEV, dtype=torch.bfloat16)
+    mt.k_gemm_rope(A, W, got, ct, st, (H + Hkv) * hd, hd, seq)
+    torch.cuda.synchronize()
+    assert torch.equal(got, ref)
+    rot = (H + Hkv) * hd
+    y = ops.linear_fwd(Ah, Wh)
+    y[:, :rot] = ops.rope_fwd(y[:, :rot].reshape(Bt, seq, H + Hkv, hd), cos, sin).reshape(M, rot)
+    assert_close(host(got), y, l2=5e-3, elem=2e-2, what="gemm+rope")
+
+
+@pytest.mark.parametrize("M,f,K", [(64, 256, 64), (300, 5632, 2048), (130, 11008, 512)])
+def test_gemm_swiglu_fwd_equals_gemm_then_swiglu(M, f, K):
+    rng = np.random.default_rng(M + f + K)
+    A, Ah = bf(rng.standard_normal((M, K)))
+    W, Wh = bf(rng.standard_normal((2 * f, K)) * (2.0 / np.sqrt(K)))
+    gu_ref = torch.empty((M, 2 * f), device=DEV, dtype=torch.bfloat16)
+    a_ref = torch.empty((M, f), device=DEV, dtype=torch.bfloat16)
+    mt.k_gemm(A, W, gu_ref)
+    mt.k_swiglu_fwd(gu_ref, a_ref)
+    gu = torch.full((M, 2 * f), float("nan"), device=DEV, dtype=torch.bfloat16)
+    a = torch.full((M, f), float("nan"), device=DEV, dtype=torch.bfloat16)
+    mt.k_gemm_swiglu_fwd(A, W, gu, a)
+    torch.cuda.synchronize()
+    assert torch.equal(gu, gu_ref)
+    assert torch.equal(a, a_ref)
+    y = ops.linear_fwd(Ah, Wh)
+    assert_close(host(a), ops.swiglu_fwd(y[:, :f], y[:, f:]), l2=1e-2, elem=2e-2, what="gemm+swiglu")
+
+
+@pytest.mark.parametrize("M,f,K", [(64, 256, 64), (300, 5632, 2048), (130, 11008, 512)])
+def test_gemm_swiglu_bwd_equals_gemm_then_swiglu_bwd(M, f, K):
+    rng = np.random.default_rng(M + f + K + 1)
+    dy, dyh = bf(rng.standard_normal((M, K)))
+    Wd, Wdh = bf(rng.standard_normal((K, f)) / np.sqrt(K))  # the down weight [d, f]
+    gu, guh = bf(rng.standard_normal((M, 2 * f)) * 2)
+    da = torch.empty((M, f), device=DEV, dtype=torch.bfloat16)
+    mt.k_gemm_ex(dy, False, Wd, True, da)
+    dgu_ref = torch.empty((M, 2 * f), device=DEV, dtype=torch.bfloat16)
+    mt.k_swiglu_bwd(da, gu, dgu_ref)
+    dgu = torch.full((M, 2 * f), float("nan"), device=DEV, dtype=torch.bfloat16)
+    mt.k_gemm_swiglu_bwd(dy, Wd, gu, dgu)
+    torch.cuda.synchronize()
+    assert torch.equal(dgu, dgu_ref)
+    dg, du = ops.swiglu_bwd(dyh @ Wdh, guh[:, :f], guh[:, f:])
+    assert_close(host(dgu), np.concatenate([dg, du], 1), l2=1e-2, elem=2e-2, what="gemm+swiglu bwd")
+
+
 # ---------------------------------------------------------------- attention
 ATTN_CASES = [
     (2, 32, 4, 4, 16),     # tiny

@@ -48,13 +48,17 @@ def test_suggest_batch_is_the_largest_that_fits():
 
 
 def test_streamed_units_follow_the_two_buffer_cache():
-    # 4 layers, 2-layer segments: each segment's layers stay resident from
-    # recompute into backward, so only the recompute re-streams them
-    assert resources.streamed_units(4, 2) == [0, 1, 2, 3, 4, 5, 3, 4, 1, 2]
+    # 4 layers, 2-layer segments: the last segment is not recomputed (its
+    # last layer is still held, the other one is loaded again); the first
+    # segment's layers stay resident from recompute into backward
+    assert resources.streamed_units(4, 2) == [0, 1, 2, 3, 4, 5, 3, 1, 2]
     # 1-layer segments: the last layer is still held when backward begins
     assert resources.streamed_units(3, 1) == [0, 1, 2, 3, 4, 2, 1]
-    # 4-layer segments: backward re-streams all but the last two of a segment
-    assert resources.streamed_units(4, 4) == [0, 1, 2, 3, 4, 5, 1, 2, 3, 4, 2, 1]
+    # one 4-layer segment: no recompute; backward re-loads all but the last layer
+    assert resources.streamed_units(4, 4) == [0, 1, 2, 3, 4, 5, 3, 2, 1]
+    # two 4-layer segments: the first segment's backward re-streams all but
+    # the last two of its layers
+    assert resources.streamed_units(8, 4) == list(range(10)) + [7, 6, 5, 1, 2, 3, 4, 2, 1]
 
 
 def test_traffic_matches_the_unit_model():
@@ -65,8 +69,8 @@ def test_traffic_matches_the_unit_model():
     units = [0] * 6
     for t in lay:
         units[t["unit"]] += t["rows"] * t["cols"]
-    assert e["h2d_bytes_per_step"] == 2 * (2 * sum(units) - units[0] - units[-1])
+    assert e["h2d_bytes_per_step"] == 2 * (sum(units) + units[3] + units[1] + units[2])
     assert e["d2h_bytes_per_step"] == 2 * n
     e7 = resources.estimate(synth.workload("7b"))
-    # 4-layer segments: layer weights cross the link 2.5 times, the rest once
-    assert 4.5 * e7["params"] < e7["h2d_bytes_per_step"] < 5.0 * 2 * e7["params"]
+    # 4-layer segments: layer weights cross the link about 2.4 times, the rest once
+    assert 4.5 * e7["params"] < e7["h2d_bytes_per_step"] < 5.0 * e7["params"]

@@ -159,10 +159,13 @@ def test_streaming_traffic_counts(tiny):
     lay, master, tokens, labels = _setup(shape)
     *_, st = _run(shape, master, tokens, labels)
     units = [u.length for u in lay.units]
-    # forward streams every unit once; backward re-streams each layer once for
-    # its segment's recompute, and the layer stays resident for its backward
-    # (a 2-layer segment fits the two buffers); bf16 = 2 bytes per element
-    assert st["h2d_bytes"] == 2 * (2 * sum(units) - units[0] - units[-1])
+    # forward streams every unit once (units 0..5); the last segment (units 3,
+    # 4) keeps its activations: unit 4 is still held, unit 3 is loaded again;
+    # the first segment (units 1, 2) is re-streamed for its recompute and stays
+    # resident for its backward; bf16 = 2 bytes per element
+    loads = [0, 1, 2, 3, 4, 5, 3, 1, 2]
+    assert st["h2d_bytes"] == 2 * sum(units[u] for u in loads)
+    assert st["h2d_units"] == len(loads)
     assert st["d2h_bytes"] == 2 * sum(units)
 
 
@@ -433,3 +436,28 @@ def test_without_gradient_array_results_are_identical(tiny, overlap):
     assert out[0][0] == out[1][0]
     for a, b in zip(out[0][1:], out[1][1:]):
         assert np.array_equal(a, b)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", ["tiny", "1.1b"])
+def test_fused_epilogues_change_no_bit(tiny, name):
+    """RoPE and SwiGLU in the GEMM epilogues give the loss, gradients and
+    updated master of the separate kernels, bit for bit (the 1.1B shape at
+    full width, 2 layers, one 256-token sequence)."""
+    if name == "tiny":
+        shape, B, s = tiny.with_(n_layers=3, ckpt_interval=2), None, None
+    else:
+        shape, B, s = synth.workload("1.1b").with_(n_layers=2, ckpt_interval=1), 1, 256
+    lay, master, _, _ = _setup(shape)
+    tokens, labels = synth.make_tokens(shape.vocab, B or shape.batch, s or shape.seq, seed=3)
+    out = []
+    for unfused in (False, True):
+        w = master.copy()
+        cfg = mt.make_config(shape, batch=B, seq=s, unfused_epilogues=unfused)
+        with mt.Trainer(cfg, w) as tr:
+            loss = tr.step(tokens, labels)
+            g = tr.read_grads()
+        out.append((loss, g, w))
+    assert out[0][0] == out[1][0]
+    assert np.array_equal(out[0][1], out[1][1])
+    assert np.array_equal(out[0][2], out[1][2])
