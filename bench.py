@@ -181,6 +181,57 @@ def host_bytes_per_param(keep_grads):
     return 32.0 if keep_grads else 28.0
 
 
+def _union(iv):
+    """Merge [start, end) intervals; returns the sorted disjoint list."""
+    out = []
+    for a, b in sorted(iv):
+        if out and a <= out[-1][1]:
+            out[-1][1] = max(out[-1][1], b)
+        else:
+            out.append([a, b])
+    return out
+
+
+def _overlap(iv, cover):
+    """Total length of the intervals `iv` that lies inside the union `cover`."""
+    tot = 0.0
+    for a, b in iv:
+        for c, d in cover:
+            lo, hi = max(a, c), min(b, d)
+            if hi > lo:
+                tot += hi - lo
+    return tot
+
+
+def timeline_summary(tl):
+    """Copy/compute overlap and host/GPU concurrency of one profiled step."""
+    def ivs(stream):
+        return [(r["start_ms"], r["end_ms"]) for r in tl if r["stream"] == stream]
+    comp = _union(ivs("compute"))
+    host = _union(ivs("host_adam"))
+    end = max(r["end_ms"] for r in tl) if tl else 0.0
+    out = {"span_ms": end, "gpu_busy_ms": sum(b - a for a, b in comp),
+           "host_adam_busy_ms": sum(b - a for a, b in host),
+           "host_and_gpu_busy_ms": _overlap(host, comp)}
+    for k in ("h2d", "d2h"):
+        iv = ivs(k)
+        t = sum(b - a for a, b in iv)
+        out[k] = {"copies": len(iv), "ms": t, "hidden_under_compute_ms": _overlap(iv, comp),
+                  "hidden_frac": _overlap(iv, comp) / t if t else None}
+    heads = [r for r in tl if r["stream"] == "compute" and r["cls"] == "ce"]
+    if heads:
+        out["forward_end_ms"] = min(r["start_ms"] for r in heads)
+    return out
+
+
+def write_trace(tl, path):
+    """Chrome / Perfetto trace (one track per stream and one for the host worker)."""
+    ev = [{"name": r["cls"], "ph": "X", "ts": r["start_ms"] * 1e3, "dur": max(r["end_ms"] - r["start_ms"], 0.0) * 1e3,
+           "pid": 0, "tid": r["stream"]} for r in tl]
+    with open(path, "w") as f:
+        json.dump({"traceEvents": ev, "displayTimeUnit": "ms"}, f)
+
+
 def gemm_traffic_record():
     """DRAM bytes per GEMM launch from the committed ncu summary, if it was
     taken on the current GEMM source (else None)."""
@@ -502,6 +553,17 @@ def run_ours(args, shape, world, rank, local, pg):
     barrier(pg)
     e2e_max = max_over_ranks(pg, e2.elapsed_time(e3) / 1e3)
     stats = tr.stats()
+    # ---- one more step, profiled: launch / copy / host-worker timeline
+    tr.profile(True)
+    tr.step_device(dev_batches[0][0].data_ptr(), dev_batches[0][1].data_ptr(), B, s)
+    tr.sync()
+    tl = tr.timeline()
+    tr.read_profile(reset=True)
+    tr.profile(False)
+    tl_sum = timeline_summary(tl)
+    if args.timeline and rank == 0:
+        write_trace(tl, args.timeline)
+        tl_sum["trace"] = args.timeline
     tr.close()
 
     tokens_all = sum_over_ranks(pg, float(M * K))
@@ -555,6 +617,7 @@ def run_ours(args, shape, world, rank, local, pg):
                                "bound out"},
         "kernels": prof_out,
         "copies": copies,
+        "timeline": tl_sum,
         "host": {"adam_s_per_step": (st1["host_adam_s"] - st0["host_adam_s"]) / K,
                  "adam_compute_s_per_step": (st1["host_compute_s"] - st0["host_compute_s"]) / K,
                  "adam_compute_gbs": hb * n_total * K / max(st1["host_compute_s"] - st0["host_compute_s"], 1e-9)
@@ -594,14 +657,16 @@ def main():
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--host-threads", type=int, default=0)
+    ap.add_argument("--timeline", default=None, help="write the profiled step's Chrome/Perfetto trace here")
     ap.add_argument("--unfused", action="store_true",
                     help="RoPE and SwiGLU as separate kernels instead of GEMM epilogues (same results)")
     ap.add_argument("--fused-grads", action="store_true",
                     help="no FP32 gradient array: each slab goes straight into Adam (same arithmetic)")
-    ap.add_argument("--overlap", action="store_true",
-                    help="overlap_adam = 1: host Adam of a step runs under the next step's device work")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="overlap_adam = 0: each step returns only after its host Adam has finished")
     args = ap.parse_args()
     args.keep_grads = not args.fused_grads
+    args.overlap = not args.no_overlap
     if args.kernel == "gemm":
         return run_gemm_kernel(args)
     if args.kernel == "attn":

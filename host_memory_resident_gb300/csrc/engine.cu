@@ -109,6 +109,7 @@ struct Job {
   bool acc;       // add to the running gradient sum (micro-steps after the first)
   bool adam;      // last micro-step: apply Adam to (sum) * scale
   float scale;
+  std::chrono::steady_clock::time_point step0;  // host time the step began (timeline)
 };
 
 }  // namespace
@@ -188,6 +189,10 @@ struct mt_handle {
   mt_kernel_profile prof{};
   cudaEvent_t prof_ref = nullptr;        // start of the last profiled step (compute stream)
   std::vector<mt_timeline_rec> timeline;  // its launches and copies
+  int64_t timeline_seq = -1;             // that step's sequence number
+  std::vector<mt_timeline_rec> host_tl;   // worker records of step host_tl_seq (under mu)
+  int64_t host_tl_seq = -1;
+  std::chrono::steady_clock::time_point step0{};  // host time the current step began
 };
 
 namespace mt {
@@ -206,13 +211,22 @@ void worker_main(mt_handle* h) {
       std::unique_lock<std::mutex> lk(h->mu);
       h->cv.wait(lk, [&] { return h->stop || !h->jobs.empty(); });
       if (h->stop && h->jobs.empty()) return;
-      // Units of a fully enqueued step go first, in the order the next
-      // forward needs them (lowest unit first); units of the step whose
-      // backward is still being enqueued go in arrival order, which frees
-      // staging slabs soonest.
+      // Order: older steps first; within a fully enqueued step, lowest unit
+      // first (the order the next forward needs them); within the step whose
+      // backward is still being enqueued, arrival order. Jobs whose slab copy
+      // has landed go before jobs still waiting for theirs, so the worker
+      // never idles on one copy (the embedding's, the last of a step) while
+      // other slabs are ready. At most K jobs are queued: the scan and its
+      // non-blocking event queries are cheap.
+      // When no copy has landed, the earliest issued one (the queue is in
+      // issue order) is the one to wait for.
       auto it = h->jobs.end();
-      for (auto j = h->jobs.begin(); j != h->jobs.end(); ++j)
-        if (j->seq <= h->enqueued_seq && (it == h->jobs.end() || j->unit < it->unit)) it = j;
+      for (auto j = h->jobs.begin(); j != h->jobs.end(); ++j) {
+        if (cudaEventQuery(h->ev_d2h_done[j->slab]) != cudaSuccess) continue;
+        if (it == h->jobs.end() || j->seq < it->seq ||
+            (j->seq == it->seq && j->seq <= h->enqueued_seq && j->unit < it->unit))
+          it = j;
+      }
       if (it == h->jobs.end()) it = h->jobs.begin();
       job = *it;
       h->jobs.erase(it);
@@ -276,6 +290,17 @@ void worker_main(mt_handle* h) {
       wait_s = std::chrono::duration<double>(tc - tw).count();
       adam_pass(a, h->threads);
       compute_s = seconds_since(tc);
+      if (h->prof_on) {
+        auto ms = [&](Clock::time_point x) { return std::chrono::duration<double, std::milli>(x - job.step0).count(); };
+        const double t_end = ms(Clock::now());
+        std::lock_guard<std::mutex> lk(h->mu);
+        if (job.seq != h->host_tl_seq) {
+          h->host_tl.clear();
+          h->host_tl_seq = job.seq;
+        }
+        h->host_tl.push_back(mt_timeline_rec{job.unit, 4, ms(tw), ms(tc)});
+        h->host_tl.push_back(mt_timeline_rec{job.unit, 3, ms(tc), t_end});
+      }
     }
     {
       std::lock_guard<std::mutex> lk(h->mu);
@@ -381,7 +406,7 @@ struct Step {
     h->st.d2h_bytes += (int64_t)bytes;
     {
       std::lock_guard<std::mutex> lk(h->mu);
-      h->jobs.push_back(Job{u, k, t_next, parity(), h->step_seq, acc, adam, gscale});
+      h->jobs.push_back(Job{u, k, t_next, parity(), h->step_seq, acc, adam, gscale, h->step0});
       ++h->unit_pending[u];
     }
     h->cv.notify_all();
@@ -567,6 +592,7 @@ struct Step {
       hh.loss_state[parity()] = 0;
       ++hh.step_seq;
     }
+    hh.step0 = Clock::now();
     if (hh.prof_on) {
       if (!hh.prof_ref) CK(cudaEventCreate(&hh.prof_ref));
       CK(cudaEventRecord(hh.prof_ref, hh.s_comp));
@@ -1005,6 +1031,7 @@ static int run_step(mt_handle* h, const int32_t* tokens, const int32_t* labels, 
     CK(cudaStreamSynchronize(h->s_h2d));
     if (h->prof_on) {
       h->timeline.clear();
+      h->timeline_seq = h->step_seq;
       for (size_t i = 0; i < h->prof_recs.size(); ++i) {
         float ms = 0.f, t0 = 0.f, t1 = 0.f;
         CK(cudaEventElapsedTime(&ms, h->prof_events[2 * i], h->prof_events[2 * i + 1]));
@@ -1146,8 +1173,13 @@ int mt_profile_read(mt_handle* h, mt_kernel_profile* out, int reset) {
 
 int mt_profile_timeline(mt_handle* h, mt_timeline_rec* out, int cap, int* n_out) {
   if (!h || !n_out || cap < 0 || (cap > 0 && !out)) return MT_EINVAL;
-  const int n = (int)h->timeline.size();
-  for (int i = 0; i < n && i < cap; ++i) out[i] = h->timeline[i];
+  std::vector<mt_timeline_rec> all = h->timeline;
+  {
+    std::lock_guard<std::mutex> lk(h->mu);
+    if (h->host_tl_seq == h->timeline_seq) all.insert(all.end(), h->host_tl.begin(), h->host_tl.end());
+  }
+  const int n = (int)all.size();
+  for (int i = 0; i < n && i < cap; ++i) out[i] = all[i];
   *n_out = n;
   return MT_OK;
 }

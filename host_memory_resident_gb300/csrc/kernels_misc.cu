@@ -255,6 +255,46 @@ __global__ void rope_kernel(bf16* __restrict__ xbuf, long long ld, int M, int s,
   *pb = __floats2bfloat162_rn(o2x, o2y);
 }
 
+// Same rotation, 8 consecutive pairs per thread with 16-byte loads and
+// stores (row pitch a multiple of 8 elements, hd a multiple of 16).
+__global__ void rope_vec_kernel(bf16* __restrict__ xbuf, long long ld, int M, int s, int nheads, int hd,
+                                const float* __restrict__ cos_t, const float* __restrict__ sin_t, float sign) {
+  const int half = hd >> 1;
+  const int per = half >> 3;  // threads per (row, head)
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long total = (long long)M * nheads * per;
+  if (idx >= total) return;
+  const int p = (int)(idx % per);
+  const long long rh = idx / per;
+  const int head = (int)(rh % nheads);
+  const int row = (int)(rh / nheads);
+  const int t = row % s;
+  const int i = 8 * p;
+  bf16* base = xbuf + (long long)row * ld + (long long)head * hd;
+  uint4* pa = reinterpret_cast<uint4*>(base + i);
+  uint4* pb = reinterpret_cast<uint4*>(base + i + half);
+  const uint4 ua = *pa, ub = *pb;
+  const float4* ct = reinterpret_cast<const float4*>(cos_t + (long long)t * half + i);
+  const float4* st = reinterpret_cast<const float4*>(sin_t + (long long)t * half + i);
+  const float4 c0 = ct[0], c1 = ct[1], s0 = st[0], s1 = st[1];
+  const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  const float sn[8] = {sign * s0.x, sign * s0.y, sign * s0.z, sign * s0.w,
+                       sign * s1.x, sign * s1.y, sign * s1.z, sign * s1.w};
+  const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
+  uint32_t oa[4], ob[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 a = unpack_bf16x2(wa[k]), b = unpack_bf16x2(wb[k]);
+    float o1x, o2x, o1y, o2y;
+    rope_pair(a.x, b.x, c[2 * k], sn[2 * k], o1x, o2x);
+    rope_pair(a.y, b.y, c[2 * k + 1], sn[2 * k + 1], o1y, o2y);
+    oa[k] = pack_bf16x2(o1x, o1y);
+    ob[k] = pack_bf16x2(o2x, o2y);
+  }
+  *pa = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+  *pb = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+}
+
 // ---------------------------------------------------------------- SwiGLU
 __global__ void swiglu_fwd_kernel(const bf16* __restrict__ gu, bf16* __restrict__ a, int M, int f) {
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -642,9 +682,16 @@ int mt_k_rope(void* x, int64_t ld, int B, int s, int n_rot_heads, int hd, const 
               int inverse, void* stream) {
   if (B < 0 || s <= 0 || n_rot_heads < 0 || hd < 4 || hd % 4 || ld < (int64_t)n_rot_heads * hd || ld % 2)
     return MT_EINVAL;
+  const int threads = 256;
+  if (hd % 16 == 0 && ld % 8 == 0 && al16(x) && al16(cos_t) && al16(sin_t)) {
+    const long long total = (long long)B * s * n_rot_heads * (hd / 16);
+    if (total == 0) return MT_OK;
+    rope_vec_kernel<<<(unsigned)((total + threads - 1) / threads), threads, 0, (cudaStream_t)stream>>>(
+        (bf16*)x, ld, B * s, s, n_rot_heads, hd, cos_t, sin_t, inverse ? -1.f : 1.f);
+    return launch_ok();
+  }
   const long long total = (long long)B * s * n_rot_heads * (hd / 4);
   if (total == 0) return MT_OK;
-  const int threads = 256;
   rope_kernel<<<(unsigned)((total + threads - 1) / threads), threads, 0, (cudaStream_t)stream>>>(
       (bf16*)x, ld, B * s, s, n_rot_heads, hd, cos_t, sin_t, inverse ? -1.f : 1.f);
   return launch_ok();

@@ -215,10 +215,13 @@ int mt_profile_enable(mt_handle* h, int on);
 /* Copies the accumulated per-class profile; reset = 1 clears it. */
 int mt_profile_read(mt_handle* h, mt_kernel_profile* out, int reset);
 
-/* One launch or copy of the last profiled step: its class (MT_PROF_*), the
- * stream it ran on (0 compute, 1 host-to-device, 2 device-to-host) and its
- * start and end in ms after that step's first compute-stream event (a copy
- * may start before it: negative). */
+/* One interval of the last profiled step, in ms after the step began (a
+ * copy may start before: negative). stream 0, 1, 2: a launch on the compute
+ * stream or a copy on the host-to-device or device-to-host stream, timed
+ * with CUDA events from the step's first compute-stream event; cls is its
+ * MT_PROF_* class. stream 3: the host worker's accumulate + Adam pass over
+ * unit cls; stream 4: the worker waiting for that unit's slab copy (host
+ * clock from the start of the mt_train_step call). */
 typedef struct mt_timeline_rec {
   int32_t cls;
   int32_t stream;

@@ -175,6 +175,26 @@ def test_rope_fwd_inverse(B, s, H, Hkv, hd):
     assert_close(host(z)[:, :rot], back, l2=5e-3, elem=1e-2, what="rope inverse")
 
 
+def test_rope_unaligned_pitch_matches_aligned():
+    """A row pitch that is not a multiple of 8 elements takes the scalar
+    kernel; it must give the bits of the 16-byte-vector kernel."""
+    rng = np.random.default_rng(7)
+    B, s, H, Hkv, hd = 2, 70, 4, 2, 64
+    qn = (H + 2 * Hkv) * hd
+    x, _ = bf(rng.standard_normal((B * s, qn)))
+    cos, sin = ops.rope_tables(s, hd, 10000.0)
+    ct, _ = f32(cos)
+    st, _ = f32(sin)
+    wide = torch.zeros((B * s, qn + 2), device=DEV, dtype=torch.bfloat16)
+    wide[:, :qn] = x
+    y = x.clone()
+    mt.k_rope(y, B, s, H + Hkv, hd, ct, st)
+    z = wide[:, :qn]
+    mt.k_rope(z, B, s, H + Hkv, hd, ct, st)
+    torch.cuda.synchronize()
+    assert torch.equal(z, y)
+
+
 # ------------------------------------------------------------------- SwiGLU
 @pytest.mark.parametrize("M,f", [(64, 256), (199, 5632)])
 def test_swiglu(M, f):

@@ -461,3 +461,34 @@ def test_fused_epilogues_change_no_bit(tiny, name):
     assert out[0][0] == out[1][0]
     assert np.array_equal(out[0][1], out[1][1])
     assert np.array_equal(out[0][2], out[1][2])
+
+
+@pytest.mark.gpu
+def test_profile_timeline_covers_the_step(tiny):
+    """A profiled step's timeline has every launch and copy of the step and
+    one host-worker interval per unit, each with end >= start."""
+    shape = tiny.with_(n_layers=4, ckpt_interval=2)
+    lay, master, tokens, labels = _setup(shape)
+    with mt.Trainer(mt.make_config(shape), master.copy()) as tr:
+        tr.step(tokens, labels)  # unprofiled: no timeline yet
+        assert tr.timeline() == []
+        st0 = tr.stats()
+        tr.profile(True)
+        tr.step(tokens, labels)
+        tr.sync()
+        tl = tr.timeline()
+        st1 = tr.stats()
+    n_units = shape.n_layers + 2
+    by = {}
+    for r in tl:
+        by.setdefault(r["stream"], []).append(r)
+        assert r["end_ms"] >= r["start_ms"]
+    assert len(by["h2d"]) == st1["h2d_units"] - st0["h2d_units"]
+    assert len(by["d2h"]) == n_units
+    assert sorted(int(r["cls"].split()[1]) for r in by["host_adam"]) == list(range(n_units))
+    assert len(by["host_wait"]) == n_units
+    # every compute record is a launch (or a fixed group of launches) of the step
+    assert 0 < len(by["compute"]) <= st1["kernel_launches"] - st0["kernel_launches"]
+    # the host pass of a unit ends after that unit's slab copy
+    d2h_end = max(r["end_ms"] for r in by["d2h"])
+    assert max(r["end_ms"] for r in by["host_adam"]) >= d2h_end - 1.0
