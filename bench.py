@@ -554,16 +554,18 @@ def run_ours(args, shape, world, rank, local, pg):
     e2e_max = max_over_ranks(pg, e2.elapsed_time(e3) / 1e3)
     stats = tr.stats()
     # ---- one more step, profiled: launch / copy / host-worker timeline
-    tr.profile(True)
-    tr.step_device(dev_batches[0][0].data_ptr(), dev_batches[0][1].data_ptr(), B, s)
-    tr.sync()
-    tl = tr.timeline()
-    tr.read_profile(reset=True)
-    tr.profile(False)
-    tl_sum = timeline_summary(tl)
-    if args.timeline and rank == 0:
-        write_trace(tl, args.timeline)
-        tl_sum["trace"] = args.timeline
+    tl_sum = None
+    if not args.no_timeline:
+        tr.profile(True)
+        tr.step_device(dev_batches[0][0].data_ptr(), dev_batches[0][1].data_ptr(), B, s)
+        tr.sync()
+        tl = tr.timeline()
+        tr.read_profile(reset=True)
+        tr.profile(False)
+        tl_sum = timeline_summary(tl)
+        if args.timeline and rank == 0:
+            write_trace(tl, args.timeline)
+            tl_sum["trace"] = args.timeline
     tr.close()
 
     tokens_all = sum_over_ranks(pg, float(M * K))
@@ -658,6 +660,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--host-threads", type=int, default=0)
     ap.add_argument("--timeline", default=None, help="write the profiled step's Chrome/Perfetto trace here")
+    ap.add_argument("--no-timeline", action="store_true", help="skip the extra profiled step (long configs)")
     ap.add_argument("--unfused", action="store_true",
                     help="RoPE and SwiGLU as separate kernels instead of GEMM epilogues (same results)")
     ap.add_argument("--fused-grads", action="store_true",

@@ -1,19 +1,20 @@
 // Causal grouped-query attention backward on the 5th-generation tensor cores.
 // Deterministic: every gradient element is accumulated by one CTA in a fixed
-// order (no atomics). Two kernels, both warp-specialised like the forward
-// (warp 0 TMA, warp 1 TMEM allocation + tcgen05.mma, warps 2-9 element-wise
-// work with two threads per TMEM lane):
+// order (no atomics). Two kernels, warp-specialised like the forward (warp 0
+// TMA, warp 1 TMEM allocation + tcgen05.mma, warps 2-9 element-wise work):
 //
 //  dK/dV: one CTA per (128-key tile, KV head, batch). For every query head
-//         of the group and every query tile at or after the diagonal:
+//         of the group and every 64-query sub-tile at or after the diagonal:
 //           S^T  = K Q^T,  dP^T = V dO^T                       (TMEM)
 //           P^T  = exp(S^T * scale - lse[q]),  dS^T = P^T (dP^T - delta[q])
 //                                                              (bf16, smem)
 //           dV  += P^T dO,  dK += dS^T Q   with dO and Q read MN-major
-//         then dK *= scale.
-//  dQ:    one CTA per (128-query tile, head, batch). For every key tile up to
-//         the diagonal:  S = Q K^T, dP = dO V^T (TMEM); dS (bf16, smem);
-//           dQ += dS K with K read MN-major; then dQ *= scale.
+//         then dK *= scale. Two element-wise groups take alternate
+//         sub-tiles, each with its own TMEM and shared-memory buffers.
+//  dQ:    one CTA per (128-query tile, head, batch), two threads per query
+//         row. For every 128-key tile up to the diagonal: S = Q K^T,
+//         dP = dO V^T (TMEM); dS (bf16, smem); dQ += dS K with K read
+//         MN-major; then dQ *= scale.
 // delta = rowsum(dO * O) comes from the pre-pass in attention.cu. This is the
 // backward of the stateless layer template's attention (travelaiplan blog,
 // 核心功能 point 3: a hand-written backward per layer instead of autograd).
@@ -22,6 +23,7 @@
 
 #include <cmath>
 #include <mutex>
+#include <string>
 
 #include "common.cuh"
 #include "mt_internal.h"
@@ -70,62 +72,80 @@ __device__ __forceinline__ void tmem_row_to_bf16(uint32_t taddr, int ncols, floa
   }
 }
 
-// ------------------------------------------------------------------ dK / dV
+// ------------------------------------------- dK / dV, 64-query sub-tiles
+// One CTA per (128-key tile, KV head, batch); it walks the group's query
+// heads and, per head, the 64-query sub-tiles at or after the diagonal.
+// Sub-tile `it` belongs to element-wise group it % 2 (warps 2-5 or 6-9, one
+// thread per key row), whose S^T and dP^T live in that group's 64-column TMEM
+// buffers and whose P^T and dS^T go to that group's shared-memory tiles. The
+// MMA warp issues dV/dK of sub-tile `it` as soon as its group has stored P^T
+// and dS^T, then S^T/dP^T of sub-tile it + 2 into the buffers just freed, so
+// one group's exponentials overlap the other group's products. Q and dO
+// sub-tiles stream through a 3-stage TMA ring. Each group stages its
+// sub-tile's 64 (lse, delta) pairs in shared memory; threads read two query
+// columns per 16-byte broadcast load.
 template <int HD>
-struct KvTc {
+struct KvTc2 {
   static constexpr int kBoxes = HD / 64;
-  static constexpr uint32_t kTile = kBoxes * kBox;
-  static constexpr int kStages = HD == 128 ? 1 : 2;     // Q + dO stages
+  static constexpr uint32_t kBox64 = 64 * 128;           // 64 columns x 64 rows of bf16
+  static constexpr uint32_t kKV = kBoxes * kBox;         // K or V tile, 128 keys
+  static constexpr uint32_t kQ = kBoxes * kBox64;        // Q or dO sub-tile, 64 queries
+  static constexpr int kStages = 3;
   static constexpr uint32_t kKOff = 0;
-  static constexpr uint32_t kVOff = kTile;
-  static constexpr uint32_t kQOff = 2 * kTile;           // [stage] Q then dO
-  static constexpr uint32_t kPOff = kQOff + kStages * 2 * kTile;  // P^T tile
-  static constexpr uint32_t kDSOff = kPOff + 2 * kBox;            // dS^T tile
-  static constexpr uint32_t kBarOff = kDSOff + 2 * kBox;
-  static constexpr uint32_t kVecOff = kBarOff + 256;     // [2][2][128] floats: lse*log2e, delta
-  static constexpr size_t kSmem = 1024 + kVecOff + 2 * 2 * 128 * 4;
+  static constexpr uint32_t kVOff = kKV;
+  static constexpr uint32_t kStOff = 2 * kKV;            // [stage] Q then dO
+  static constexpr uint32_t kPOff = kStOff + kStages * 2 * kQ;  // [group] P^T then dS^T, 128 keys x 64 queries
+  static constexpr uint32_t kBarOff = kPOff + 2 * 2 * kBox;
+  static constexpr uint32_t kVecOff = kBarOff + 256;     // [group][64] (lse * log2e, delta)
+  static constexpr size_t kSmem = 1024 + kVecOff + 2 * 64 * 8;
+  static_assert(kSmem <= 232448, "shared memory per block");
 };
 
 template <int HD>
 __global__ void __launch_bounds__(kThr, 1)
-    attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tqkv, const __grid_constant__ CUtensorMap tdo,
-                            const float* __restrict__ lse, const float* __restrict__ delta, bf16* __restrict__ dqkv,
-                            long long lddq, int s, int H, int Hkv, int* err) {
-  using C = KvTc<HD>;
+    attn_bwd_dkdv_tc2_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_constant__ CUtensorMap tq64,
+                             const __grid_constant__ CUtensorMap tdo64, const float* __restrict__ lse,
+                             const float* __restrict__ delta, bf16* __restrict__ dqkv, long long lddq, int s, int H,
+                             int Hkv, int* err) {
+  using C = KvTc2<HD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024b(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
-  uint64_t* kv_full = bars;          // K and V tiles
-  uint64_t* ld_full = bars + 1;      // [2] Q + dO stage
-  uint64_t* ld_empty = bars + 3;     // [2]
-  uint64_t* s_full = bars + 5;       // S^T and dP^T in TMEM
-  uint64_t* p_full = bars + 6;       // P^T, dS^T written
-  uint64_t* p_empty = bars + 7;      // dV, dK MMAs done with them
-  uint64_t* s_empty = bars + 8;      // S^T and dP^T copied out of TMEM
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 9);
-  float* vec = reinterpret_cast<float*>(sm + C::kVecOff);
+  uint64_t* kv_full = bars;           // K and V tiles
+  uint64_t* ld_full = bars + 1;       // [3] Q + dO stage
+  uint64_t* ld_empty = bars + 4;      // [3]
+  uint64_t* s_full = bars + 7;        // [2] per group: S^T, dP^T in TMEM
+  uint64_t* s_empty = bars + 9;       // [2] per group: copied out of TMEM
+  uint64_t* p_full = bars + 11;       // [2] per group: P^T, dS^T stored
+  uint64_t* p_empty = bars + 13;      // [2] per group: dV, dK products done with them
+  uint64_t* done = bars + 15;         // all dV, dK products done (completes once)
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 16);
 
-  const int nt = (s + kT - 1) / kT;
+  const int n64 = (s + 63) / 64;
   const int kt = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int grp = H / Hkv;
   const int k0 = kt * kT;
-  const int per_head = nt - kt;       // query tiles kt .. nt-1
+  const int per_head = n64 - 2 * kt;  // 64-query sub-tiles from the diagonal on
   const int total = grp * per_head;
   const int kcol = (H + g) * HD, vcol = (H + Hkv + g) * HD;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    tma_prefetch_desc(&tqkv);
-    tma_prefetch_desc(&tdo);
+    tma_prefetch_desc(&tkv);
+    tma_prefetch_desc(&tq64);
+    tma_prefetch_desc(&tdo64);
     mbar_init(kv_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&ld_full[i], 1);
       mbar_init(&ld_empty[i], 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(p_full, 256);
-    mbar_init(p_empty, 1);
-    mbar_init(s_empty, 256);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], 128);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&p_empty[i], 1);
+    }
+    mbar_init(done, 1);
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(tmem_holder, 512);
@@ -133,148 +153,172 @@ __global__ void __launch_bounds__(kThr, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + HD;
+  const uint32_t tS[2] = {tmem, tmem + 64}, tdP[2] = {tmem + 128, tmem + 192};
+  const uint32_t tdV = tmem + 256, tdK = tmem + 256 + HD;
 
   if (warp == 0) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(kv_full, 2 * C::kTile);
+      int nld = 0;
+      bool ok = true;
+      mbar_arrive_expect_tx(kv_full, 2 * C::kKV);
       for (int bx = 0; bx < C::kBoxes; ++bx) {
-        tma_load_3d(sm + C::kKOff + bx * kBox, &tqkv, kcol + bx * 64, k0, b, kv_full);
-        tma_load_3d(sm + C::kVOff + bx * kBox, &tqkv, vcol + bx * 64, k0, b, kv_full);
+        tma_load_3d(sm + C::kKOff + bx * kBox, &tkv, kcol + bx * 64, k0, b, kv_full);
+        tma_load_3d(sm + C::kVOff + bx * kBox, &tkv, vcol + bx * 64, k0, b, kv_full);
       }
       for (int it = 0; it < total; ++it) {
         const int st = it % C::kStages, use = it / C::kStages;
-        if (!mbar_wait(&ld_empty[st], (use & 1) ^ 1, err)) break;
+        if (!mbar_wait(&ld_empty[st], (use & 1) ^ 1, err)) { ok = false; break; }
         const int h = g * grp + it / per_head;
-        const int q0 = (kt + it % per_head) * kT;
-        uint8_t* qs = sm + C::kQOff + st * 2 * C::kTile;
-        mbar_arrive_expect_tx(&ld_full[st], 2 * C::kTile);
+        const int q0 = (2 * kt + it % per_head) * 64;
+        uint8_t* qs = sm + C::kStOff + st * 2 * C::kQ;
+        mbar_arrive_expect_tx(&ld_full[st], 2 * C::kQ);
         for (int bx = 0; bx < C::kBoxes; ++bx) {
-          tma_load_3d(qs + bx * kBox, &tqkv, h * HD + bx * 64, q0, b, &ld_full[st]);
-          tma_load_3d(qs + C::kTile + bx * kBox, &tdo, h * HD + bx * 64, q0, b, &ld_full[st]);
+          tma_load_3d(qs + bx * C::kBox64, &tq64, h * HD + bx * 64, q0, b, &ld_full[st]);
+          tma_load_3d(qs + C::kQ + bx * C::kBox64, &tdo64, h * HD + bx * 64, q0, b, &ld_full[st]);
+        }
+        ++nld;
+      }
+      if (!ok) {
+        // wait (bounded) for this CTA's copies still in flight before it exits
+        mbar_wait(kv_full, 0, err);
+        for (int i = 0; i < C::kStages && i < nld; ++i) {
+          const int last = nld - 1 - i;
+          mbar_wait(&ld_full[last % C::kStages], (last / C::kStages) & 1, err);
         }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16_f32(kT, kT, false, false);   // S^T, dP^T
-      constexpr uint32_t id_g = idesc_bf16_f32(kT, HD, false, true);    // dV, dK (B MN-major)
+      constexpr uint32_t id_s = idesc_bf16_f32(kT, 64, false, false);  // S^T, dP^T: M 128 keys, N 64 queries
+      constexpr uint32_t id_g = idesc_bf16_f32(kT, HD, false, true);   // dV, dK: B (dO, Q) MN-major
       const uint32_t sK = smem_u32(sm + C::kKOff), sV = smem_u32(sm + C::kVOff);
-      const uint32_t sP = smem_u32(sm + C::kPOff), sDS = smem_u32(sm + C::kDSOff);
       bool ok = mbar_wait(kv_full, 0, err);
-      // S^T / dP^T of query tile `it` (its Q and dO stage loaded, the TMEM
-      // they overwrite copied out by the element-wise warps)
-      auto issue_s = [&](int it) -> bool {
-        const int st = it % C::kStages;
-        if (!mbar_wait(&ld_full[st], (it / C::kStages) & 1, err)) return false;
-        if (it > 0 && !mbar_wait(s_empty, (it - 1) & 1, err)) return false;
+      auto issue_s = [&](int i) -> bool {
+        const int G = i & 1, li = i >> 1, st = i % C::kStages;
+        if (!mbar_wait(&ld_full[st], (i / C::kStages) & 1, err)) return false;
+        if (li > 0 && !mbar_wait(&s_empty[G], (li - 1) & 1, err)) return false;
         tc_fence_after();
-        const uint32_t sQ = smem_u32(sm + C::kQOff + st * 2 * C::kTile), sO = sQ + C::kTile;
+        const uint32_t sQ = smem_u32(sm + C::kStOff + st * 2 * C::kQ), sO = sQ + C::kQ;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-          tc_mma_bf16(tS, smem_desc_kmajor_sw128(sK + off), smem_desc_kmajor_sw128(sQ + off), id_s, kk > 0);
-          tc_mma_bf16(tdP, smem_desc_kmajor_sw128(sV + off), smem_desc_kmajor_sw128(sO + off), id_s, kk > 0);
+          const uint32_t ka = (kk >> 2) * kBox + (kk & 3) * 32, kb = (kk >> 2) * C::kBox64 + (kk & 3) * 32;
+          tc_mma_bf16(tS[G], smem_desc_kmajor_sw128(sK + ka), smem_desc_kmajor_sw128(sQ + kb), id_s, kk > 0);
+          tc_mma_bf16(tdP[G], smem_desc_kmajor_sw128(sV + ka), smem_desc_kmajor_sw128(sO + kb), id_s, kk > 0);
         }
-        tc_commit(s_full);
-        return true;
-      };
-      // dV += P^T dO, dK += dS^T Q for query tile `it`, then free its stage
-      auto issue_g = [&](int it) -> bool {
-        const int st = it % C::kStages;
-        if (!mbar_wait(p_full, it & 1, err)) return false;
-        tc_fence_after();
-        const uint32_t sQ = smem_u32(sm + C::kQOff + st * 2 * C::kTile), sO = sQ + C::kTile;
-#pragma unroll
-        for (int kk = 0; kk < kT / 16; ++kk) {
-          const uint32_t aoff = (kk >> 2) * kBox + (kk & 3) * 32;
-          const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-          tc_mma_bf16(tdV, smem_desc_kmajor_sw128(sP + aoff), smem_desc_mnmajor_sw128(sO + kk * 2048, kBox), id_g, acc);
-          tc_mma_bf16(tdK, smem_desc_kmajor_sw128(sDS + aoff), smem_desc_mnmajor_sw128(sQ + kk * 2048, kBox), id_g,
-                      acc);
-        }
-        tc_commit(p_empty);
-        tc_commit(&ld_empty[st]);
+        tc_commit(&s_full[G]);
         return true;
       };
       if (ok && total > 0) ok = issue_s(0);
+      if (ok && total > 1) ok = issue_s(1);
       for (int it = 0; ok && it < total; ++it) {
-        if (C::kStages >= 2) {
-          // the next tile's scores overlap this tile's element-wise work
-          if (it + 1 < total && !(ok = issue_s(it + 1))) break;
-          ok = issue_g(it);
-        } else {
-          // one Q/dO stage: the next tile's loads need this tile's products done
-          if (!(ok = issue_g(it))) break;
-          if (it + 1 < total) ok = issue_s(it + 1);
+        const int G = it & 1, li = it >> 1, st = it % C::kStages;
+        if (!(ok = mbar_wait(&p_full[G], li & 1, err))) break;
+        tc_fence_after();
+        const uint32_t sQ = smem_u32(sm + C::kStOff + st * 2 * C::kQ), sO = sQ + C::kQ;
+        const uint32_t sP = smem_u32(sm + C::kPOff + G * 2 * kBox), sDS = sP + kBox;
+#pragma unroll
+        for (int kk = 0; kk < 64 / 16; ++kk) {
+          const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+          tc_mma_bf16(tdV, smem_desc_kmajor_sw128(sP + kk * 32), smem_desc_mnmajor_sw128(sO + kk * 2048, C::kBox64),
+                      id_g, acc);
+          tc_mma_bf16(tdK, smem_desc_kmajor_sw128(sDS + kk * 32),
+                      smem_desc_mnmajor_sw128(sQ + kk * 2048, C::kBox64), id_g, acc);
         }
+        tc_commit(&p_empty[G]);
+        tc_commit(&ld_empty[st]);
+        if (it + 2 < total) ok = issue_s(it + 2);
       }
+      // The accumulators are final once every product above has completed.
+      // The readers wait on this single-use barrier: waiting on a group's
+      // p_empty for its last completion could match an earlier phase of the
+      // same parity that the other group never observed.
+      if (ok) tc_commit(done);
     }
   } else {
-    const int q = warp & 3, half = (warp - 2) >> 2;
+    const int G = (warp - 2) >> 2, q = warp & 3;
     const int row = q * 32 + lane;  // key row within the tile
     const int key = k0 + row;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const float sc = rsqrtf((float)HD) * kLog2e;
-    const int tid = threadIdx.x - 64;  // 0..255
+    uint8_t* sP = sm + C::kPOff + G * 2 * kBox;
+    uint8_t* sDS = sP + kBox;
+    float2* vec = reinterpret_cast<float2*>(sm + C::kVecOff) + G * 64;
+    const int tg = threadIdx.x - 64 - 128 * G;  // 0..127 within the group
+    const uint32_t rsw = (uint32_t)(row & 7);
+    auto group_sync = [&]() { asm volatile("bar.sync %0, 128;" ::"r"(1 + G) : "memory"); };
+    // a wait's outcome, the same for the whole warp (tcgen05.ld is warp-wide)
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) { return __all_sync(0xffffffffu, mbar_wait(bar, parity, err)); };
     bool ok = true;
-    for (int it = 0; it < total && ok; ++it) {
+    // every thread of the group runs every iteration's two group barriers,
+    // also after a failed wait (it then skips the work), so none is left
+    // waiting at a barrier
+    for (int it = G; it < total; it += 2) {
+      const int li = it >> 1;
       const int h = g * grp + it / per_head;
-      const int q0 = (kt + it % per_head) * kT;
-      float* lv = vec + (it & 1) * 256;  // [lse*log2e | delta] for this query tile
-      {
-        const int qi = tid & 127;
-        const int qq = q0 + qi;
-        const long long idx = ((long long)b * H + h) * s + qq;
-        if (tid < 128) lv[qi] = qq < s ? lse[idx] * kLog2e : INFINITY;
-        else lv[128 + qi] = qq < s ? delta[idx] : 0.f;
+      const int jj = it % per_head;
+      const int q0 = (2 * kt + jj) * 64;
+      // (lse * log2e, delta) of the sub-tile's 64 queries; the group's reads
+      // of the previous sub-tile's pairs end before they are overwritten
+      group_sync();
+      if (tg < 64) {
+        const long long vi = ((long long)b * H + h) * s + q0 + tg;
+        vec[tg] = q0 + tg < s ? make_float2(lse[vi] * kLog2e, delta[vi]) : make_float2(INFINITY, 0.f);
       }
-      asm volatile("bar.sync 5, 256;" ::: "memory");
-      if (!mbar_wait(s_full, it & 1, err)) { ok = false; break; }
+      group_sync();
+      if (!ok) continue;
+      if (!wait_all(&s_full[G], li & 1)) { ok = false; continue; }
       tc_fence_after();
       uint32_t rs[2][32], rp[2][32];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        tmem_ld_32x32b_x32(tS + lane_off + half * 64 + c * 32, rs[c]);
-        tmem_ld_32x32b_x32(tdP + lane_off + half * 64 + c * 32, rp[c]);
+        tmem_ld_32x32b_x32(tS[G] + lane_off + c * 32, rs[c]);
+        tmem_ld_32x32b_x32(tdP[G] + lane_off + c * 32, rp[c]);
       }
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(s_empty);
-      const bool diag = (q0 == k0);
-      uint32_t pk[32], dk[32];
+      mbar_arrive(&s_empty[G]);
+      const bool diag = q0 < k0 + kT;  // the sub-tile reaches the diagonal: mask key > query
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
+        const float4 ld = reinterpret_cast<const float4*>(vec)[i];  // columns 2i, 2i+1
+        const float l2s[2] = {ld.x, ld.z}, dls[2] = {ld.y, ld.w};
         float pv[2], dv[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int ci = 2 * i + e;  // column within this half
-          const int qi = half * 64 + ci;
-          const float sv = __uint_as_float(rs[ci >> 5][ci & 31]);
-          float p = ex2_approx(fmaf(sv, sc, -lv[qi]));
-          if (diag && q0 + qi < key) p = 0.f;
+          const int c = 2 * i + e;  // query column within the sub-tile
+          float p = ex2_approx(fmaf(__uint_as_float(rs[c >> 5][c & 31]), sc, -l2s[e]));
+          if (diag && q0 + c < key) p = 0.f;
           pv[e] = p;
-          dv[e] = p * (__uint_as_float(rp[ci >> 5][ci & 31]) - lv[128 + qi]);
+          dv[e] = p * (__uint_as_float(rp[c >> 5][c & 31]) - dls[e]);
         }
-        pk[i] = pack_bf16x2(pv[0], pv[1]);
-        dk[i] = pack_bf16x2(dv[0], dv[1]);
+        rs[i >> 4][i & 15] = pack_bf16x2(pv[0], pv[1]);
+        rp[i >> 4][i & 15] = pack_bf16x2(dv[0], dv[1]);
       }
-      // P^T / dS^T smem is free once the previous dV / dK MMAs finished
-      if (it > 0 && !mbar_wait(p_empty, (it - 1) & 1, err)) { ok = false; break; }
-      store_half_row(sm + C::kPOff, half, row, pk);
-      store_half_row(sm + C::kDSOff, half, row, dk);
+      // this group's P^T / dS^T tiles were last read by dV/dK of sub-tile it - 2
+      if (li > 0 && !wait_all(&p_empty[G], (li - 1) & 1)) { ok = false; continue; }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int w0 = 4 * c;
+        const uint32_t off = row * 128 + (((uint32_t)c ^ rsw) * 16);
+        *reinterpret_cast<uint4*>(sP + off) = make_uint4(rs[w0 >> 4][w0 & 15], rs[(w0 + 1) >> 4][(w0 + 1) & 15],
+                                                          rs[(w0 + 2) >> 4][(w0 + 2) & 15],
+                                                          rs[(w0 + 3) >> 4][(w0 + 3) & 15]);
+        *reinterpret_cast<uint4*>(sDS + off) = make_uint4(rp[w0 >> 4][w0 & 15], rp[(w0 + 1) >> 4][(w0 + 1) & 15],
+                                                           rp[(w0 + 2) >> 4][(w0 + 2) & 15],
+                                                           rp[(w0 + 3) >> 4][(w0 + 3) & 15]);
+      }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[G]);
     }
-    if (ok && total > 0 && mbar_wait(p_empty, (total - 1) & 1, err)) {
+    if (ok && total > 0 && wait_all(done, 0)) {
       tc_fence_after();
       const bool store = key < s;
       const long long r0 = (long long)b * s + key;
-      bf16* dkrow = dqkv + r0 * lddq + (long long)kcol + half * (HD / 2);
-      bf16* dvrow = dqkv + r0 * lddq + (long long)vcol + half * (HD / 2);
-      tmem_row_to_bf16(tdK + lane_off + half * (HD / 2), HD / 2, rsqrtf((float)HD), dkrow, store);
-      tmem_row_to_bf16(tdV + lane_off + half * (HD / 2), HD / 2, 1.f, dvrow, store);
+      if (G == 0)
+        tmem_row_to_bf16(tdV + lane_off, HD, 1.f, dqkv + r0 * lddq + (long long)vcol, store);
+      else
+        tmem_row_to_bf16(tdK + lane_off, HD, rsqrtf((float)HD), dqkv + r0 * lddq + (long long)kcol, store);
     }
   }
   tc_fence_before();
@@ -473,17 +517,18 @@ void init_once() {
   if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
       q == cudaDriverEntryPointSuccess)
     g_enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)KvTc<64>::kSmem);
-  cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       (int)KvTc<128>::kSmem);
+  cudaFuncSetAttribute(attn_bwd_dkdv_tc2_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)KvTc2<64>::kSmem);
+  cudaFuncSetAttribute(attn_bwd_dkdv_tc2_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)KvTc2<128>::kSmem);
   cudaFuncSetAttribute(attn_bwd_dq_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)QTc<64>::kSmem);
   cudaFuncSetAttribute(attn_bwd_dq_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)QTc<128>::kSmem);
 }
 
-bool make_map3(CUtensorMap* m, const void* p, long long ld, int s, int B) {
+bool make_map3(CUtensorMap* m, const void* p, long long ld, int s, int B, int rows = kT) {
   cuuint64_t dims[3] = {(cuuint64_t)ld, (cuuint64_t)s, (cuuint64_t)B};
   cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)s * ld * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)kT, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return g_enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -503,23 +548,30 @@ int attn_bwd_tc(const void* qkv, long long ld, const void* dout, long long lddo,
   if ((reinterpret_cast<uintptr_t>(qkv) & 15) || (reinterpret_cast<uintptr_t>(dout) & 15) ||
       (reinterpret_cast<uintptr_t>(dqkv) & 15) || ld % 8 || lddo % 8 || lddq % 8)
     return MT_EINVAL;
-  CUtensorMap tq, td;
-  if (!make_map3(&tq, qkv, ld, s, B) || !make_map3(&td, dout, lddo, s, B)) return MT_EINVAL;
+  CUtensorMap tq, td, tq64, td64;
+  if (!make_map3(&tq, qkv, ld, s, B) || !make_map3(&td, dout, lddo, s, B) || !make_map3(&tq64, qkv, ld, s, B, 64) ||
+      !make_map3(&td64, dout, lddo, s, B, 64))
+    return MT_EINVAL;
   const int nt = (s + kT - 1) / kT;
   int* err = device_error_word();
   dim3 g1(nt, Hkv, B), g2(nt, H, B);
   if (hd == 64) {
-    attn_bwd_dkdv_tc_kernel<64><<<g1, kThr, KvTc<64>::kSmem, stream>>>(tq, td, lse, delta, (bf16*)dqkv, lddq, s, H,
-                                                                       Hkv, err);
+    attn_bwd_dkdv_tc2_kernel<64><<<g1, kThr, KvTc2<64>::kSmem, stream>>>(tq, tq64, td64, lse, delta, (bf16*)dqkv,
+                                                                         lddq, s, H, Hkv, err);
     attn_bwd_dq_tc_kernel<64><<<g2, kThr, QTc<64>::kSmem, stream>>>(tq, td, lse, delta, (bf16*)dqkv, lddq, s, H, Hkv,
                                                                    err);
   } else {
-    attn_bwd_dkdv_tc_kernel<128><<<g1, kThr, KvTc<128>::kSmem, stream>>>(tq, td, lse, delta, (bf16*)dqkv, lddq, s,
-                                                                         H, Hkv, err);
+    attn_bwd_dkdv_tc2_kernel<128><<<g1, kThr, KvTc2<128>::kSmem, stream>>>(tq, tq64, td64, lse, delta, (bf16*)dqkv,
+                                                                           lddq, s, H, Hkv, err);
     attn_bwd_dq_tc_kernel<128><<<g2, kThr, QTc<128>::kSmem, stream>>>(tq, td, lse, delta, (bf16*)dqkv, lddq, s, H,
                                                                      Hkv, err);
   }
-  return cudaGetLastError() == cudaSuccess ? MT_OK : MT_ECUDA;
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_last_error_message(std::string("attention backward launch: ") + cudaGetErrorString(e));
+    return MT_ECUDA;
+  }
+  return MT_OK;
 }
 
 }  // namespace mt
