@@ -101,6 +101,24 @@ __device__ __forceinline__ void load_bf16x32(const bf16* p, float (&v)[32]) {
   }
 }
 
+// The 32 gate and 32 up values (bf16, packed) of one row at ffn column col0
+// for the SwiGLU-backward epilogue; zeros outside the matrix.
+__device__ __forceinline__ void load_gate_up(const GemmArgs& a, int row, bool row_ok, int col0, uint4 (&g)[4],
+                                             uint4 (&u)[4]) {
+  if (row_ok && col0 < a.N) {
+    const uint4* gp = reinterpret_cast<const uint4*>(a.X + (long long)row * a.ldx + col0);
+    const uint4* up = reinterpret_cast<const uint4*>(a.X + (long long)row * a.ldx + a.f + col0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      g[j] = gp[j];
+      u[j] = up[j];
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) g[j] = u[j] = make_uint4(0, 0, 0, 0);
+  }
+}
+
 __device__ __forceinline__ void load_f32x32(const float* p, float (&v)[32]) {
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
@@ -240,12 +258,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
       const int acc = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
-      if (!mbar_wait(&tfull_bar[acc], use & 1, args.err)) { *abort_flag = 1; break; }
-      tc_fence_after();
       int mb, nb;
       tile_coords(t, args.num_mb, args.num_nb, mb, nb);
       const int row = mb * kBM + q * 32 + lane;
       const bool row_ok = row < args.M;
+      // SwiGLU backward: the gate | up values of this warp's first chunk do
+      // not depend on the accumulator; their loads overlap the wait for it
+      uint4 xg[4], xu[4];
+      const int xc0 = hs * (kBN / 64);
+      if (EPI == kEpiSwigluBwd) load_gate_up(args, row, row_ok, nb * kBN + xc0 * 32, xg, xu);
+      if (!mbar_wait(&tfull_bar[acc], use & 1, args.err)) { *abort_flag = 1; break; }
+      tc_fence_after();
       const uint32_t tacc = tmem_base + (uint32_t)(acc * kBN) + ((uint32_t)(q * 32) << 16);
       if (EPI == kEpiRope) {
         // heads of hd columns; dims i and i + hd/2 of a head form a pair, so
@@ -307,24 +330,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           store_bf16x32(args.C2 + (long long)row * args.ldc2 + fc, a);
         }
       } else if (EPI == kEpiSwigluBwd) {
-        // the tile is da for ffn columns nb * 256 + [0, 256)
+        // the tile is da for ffn columns nb * 256 + [0, 256); the next
+        // chunk's gate | up loads are issued before this chunk's arithmetic
 #pragma unroll 1
-        for (int c = hs * (kBN / 64); c < (hs + 1) * (kBN / 64); ++c) {
+        for (int c = xc0; c < xc0 + kBN / 64; ++c) {
           __syncwarp();
+          uint4 ng[4], nu[4];
+          if (c + 1 < xc0 + kBN / 64) load_gate_up(args, row, row_ok, nb * kBN + (c + 1) * 32, ng, nu);
           uint32_t r[32];
           tmem_ld_32x32b_x32(tacc + (uint32_t)(c * 32), r);
           tmem_ld_wait();
           const int col0 = nb * kBN + c * 32;
-          if (!row_ok || col0 >= args.N) continue;
-          float g[32], u[32], dg[32], du[32];
-          const bf16* xp = args.X + (long long)row * args.ldx + col0;
-          load_bf16x32(xp, g);
-          load_bf16x32(xp + args.f, u);
+          if (row_ok && col0 < args.N) {
+            float dg[32], du[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) swiglu_bwd_elem(bf16_round(__uint_as_float(r[i])), g[i], u[i], dg[i], du[i]);
-          bf16* cp = reinterpret_cast<bf16*>(args.C) + (long long)row * args.ldc + col0;
-          store_bf16x32(cp, dg);
-          store_bf16x32(cp + args.f, du);
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t gw[4] = {xg[j].x, xg[j].y, xg[j].z, xg[j].w};
+              const uint32_t uw[4] = {xu[j].x, xu[j].y, xu[j].z, xu[j].w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const float2 g2 = unpack_bf16x2(gw[k]), u2 = unpack_bf16x2(uw[k]);
+                const int i = 8 * j + 2 * k;
+                swiglu_bwd_elem(bf16_round(__uint_as_float(r[i])), g2.x, u2.x, dg[i], du[i]);
+                swiglu_bwd_elem(bf16_round(__uint_as_float(r[i + 1])), g2.y, u2.y, dg[i + 1], du[i + 1]);
+              }
+            }
+            bf16* cp = reinterpret_cast<bf16*>(args.C) + (long long)row * args.ldc + col0;
+            store_bf16x32(cp, dg);
+            store_bf16x32(cp + args.f, du);
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            xg[j] = ng[j];
+            xu[j] = nu[j];
+          }
         }
       } else {
 #pragma unroll 1
