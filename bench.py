@@ -253,16 +253,33 @@ def oracle_sample(shape):
     model (t_layer = their difference), plus Adam on a 2^24-element slice."""
     import oracle
     s = shape.seq
-    toks, labs = synth.make_tokens(shape.vocab, 1, s, seed=1)
-    times = {}
-    for L in (1, 2):
-        sh = shape.with_(n_layers=L, ckpt_interval=1)
-        lay = oracle.build_layout(sh)
-        master = synth.init_master(lay.n_total, lay.segments(), seed=0)
-        t0 = time.perf_counter()
-        oracle.step_grads(sh, master, toks, labs, dtype=np.float32)
-        times[L] = time.perf_counter() - t0
-        del master
+
+    def sample(seq):
+        toks, labs = synth.make_tokens(shape.vocab, 1, seq, seed=1)
+        times = {}
+        for L in (1, 2):
+            sh = shape.with_(n_layers=L, ckpt_interval=1)
+            lay = oracle.build_layout(sh)
+            master = synth.init_master(lay.n_total, lay.segments(), seed=0)
+            t0 = time.perf_counter()
+            oracle.step_grads(sh, master, toks, labs, dtype=np.float32)
+            times[L] = time.perf_counter() - t0
+            del master
+        return times
+
+    extrapolated = ""
+    if s > 16384:
+        # long sequences: time 8192 and 16384 tokens and extrapolate each term
+        # as a s + b s^2 (the attention part grows with s^2)
+        ta, tb = sample(8192), sample(16384)
+        times = {}
+        for L in (1, 2):
+            b2 = (tb[L] - 2.0 * ta[L]) / (16384.0 * 16384.0 - 2.0 * 8192.0 * 8192.0)
+            a1 = (ta[L] - b2 * 8192.0 * 8192.0) / 8192.0
+            times[L] = max(a1, 0.0) * s + max(b2, 0.0) * s * s
+        extrapolated = "extrapolated from 8192 and 16384 tokens as a s + b s^2; "
+    else:
+        times = sample(s)
     n = 1 << 24
     rng = np.random.default_rng(0)
     w = rng.standard_normal(n).astype(np.float32)
@@ -278,7 +295,7 @@ def oracle_sample(shape):
     t_step = shape.batch * (shape.n_layers * t_layer + t_rest) + t_adam
     return {
         "value": shape.batch * s / t_step, "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
-        "sample": (f"composed: 1 sequence of {s} tokens through 1- and 2-layer full-width models "
+        "sample": (f"composed: {extrapolated}1 sequence of {s} tokens through 1- and 2-layer full-width models "
                    f"(t_layer {t_layer:.2f} s, rest {t_rest:.2f} s, float32 numpy) + Adam on 2^24 elements "
                    f"scaled to {lay_full.n_total} params; step = {shape.batch} x ({shape.n_layers} t_layer + rest)"
                    f" + Adam = {t_step:.1f} s"),

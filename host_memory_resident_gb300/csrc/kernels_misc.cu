@@ -37,7 +37,7 @@ namespace {
 
 constexpr int kNormBwdVec = 4;          // 8-element vectors per thread and row: 32 elements
 constexpr int kNormBwdMaxWarps = 8;     // warps per row: d <= 8 * 32 * 32 = 8192
-constexpr int kNormBwdMaxParts = 608;   // row groups (dw partial sums): 4 per SM on 152 SMs
+constexpr int kNormBwdMaxParts = 1216;  // row groups (dw partial sums): 8 per SM on 152 SMs (2 blocks of 4)
 
 inline int launch_ok() { return cudaGetLastError() == cudaSuccess ? MT_OK : MT_ECUDA; }
 
@@ -206,22 +206,23 @@ __global__ void __launch_bounds__(256, 2)
 }
 
 // dw[c] = sum over parts p of partial[p, c], rounded to bf16. Block: 32
-// columns x 8 part classes; class j sums parts j, j+8, ... in order, then
-// the 8 class sums are added in order (a fixed order for every launch).
-__global__ void __launch_bounds__(256)
+// columns x 16 part classes; class j sums parts j, j+16, ... in order, then
+// the 16 class sums are added in order (a fixed order for every launch).
+constexpr int kColsumClasses = 16;
+__global__ void __launch_bounds__(32 * kColsumClasses)
     colsum_to_bf16_kernel(const float* __restrict__ partial, int n_part, int d, bf16* __restrict__ out) {
-  __shared__ float cls[8][32];
+  __shared__ float cls[kColsumClasses][32];
   const int cl = threadIdx.x & 31, j = threadIdx.x >> 5;
   const int c = blockIdx.x * 32 + cl;
   float s = 0.f;
   if (c < d)
-    for (int p = j; p < n_part; p += 8) s += partial[(long long)p * d + c];
+    for (int p = j; p < n_part; p += kColsumClasses) s += partial[(long long)p * d + c];
   cls[j][cl] = s;
   __syncthreads();
   if (j == 0 && c < d) {
     float t = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) t += cls[i][cl];
+    for (int i = 0; i < kColsumClasses; ++i) t += cls[i][cl];
     out[c] = __float2bfloat16_rn(t);
   }
 }
@@ -670,10 +671,10 @@ int mt_k_rmsnorm_bwd(const float* dy, const void* x, const void* w, const float*
       case 7: go(rmsnorm_bwd_kernel<7>, 7); break;
       default: go(rmsnorm_bwd_kernel<8>, 8); break;
     }
-    colsum_to_bf16_kernel<<<(d + 31) / 32, 256, 0, st>>>(partial, ngroups, d, (bf16*)dw_out);
+    colsum_to_bf16_kernel<<<(d + 31) / 32, 32 * kColsumClasses, 0, st>>>(partial, ngroups, d, (bf16*)dw_out);
   } else {
     cudaMemsetAsync(partial, 0, sizeof(float) * d, st);
-    colsum_to_bf16_kernel<<<(d + 31) / 32, 256, 0, st>>>(partial, 1, d, (bf16*)dw_out);
+    colsum_to_bf16_kernel<<<(d + 31) / 32, 32 * kColsumClasses, 0, st>>>(partial, 1, d, (bf16*)dw_out);
   }
   return launch_ok();
 }
