@@ -15,8 +15,10 @@
 //   warps 2-5, 6-9: one softmax group per query tile, one thread per query
 //            row (its TMEM lane) holding the row's 128 scores in registers.
 //            The causal mask and the online softmax run in fp32 (log2
-//            domain); P is written as bf16 into 128-byte-swizzled shared
-//            memory. O is rescaled in TMEM only when a row's running maximum
+//            domain); P is written as bf16 into TMEM columns of its own at
+//            hd 64 (read by the P V product as its A operand), or into
+//            128-byte-swizzled shared memory at hd 128, where S and O fill
+//            TMEM. O is rescaled in TMEM only when a row's running maximum
 //            grows by more than 2^8, so P stays below 256 and the final O / l
 //            is unchanged.
 // While one group exponentiates, the tensor core computes the other group's
@@ -122,6 +124,10 @@ __global__ void __launch_bounds__(kThr, 1)
   const uint32_t tmem = *tmem_holder;
   const uint32_t tS[2] = {tmem, tmem + 128};
   const uint32_t tO[2] = {tmem + 256, tmem + 256 + HD};
+  // hd 64 leaves TMEM columns 384-511 free: P of each tile goes there and the
+  // P V product reads it as its A operand (no shared-memory round trip)
+  constexpr bool kPT = HD == 64;
+  const uint32_t tP[2] = {tmem + 384, tmem + 448};
 
   if (warp == 0) {
     if (lane == 0) {
@@ -209,8 +215,12 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
           for (int kk = 0; kk < kKV / 16; ++kk) {
             const uint32_t aoff = (kk >> 2) * kBox + (kk & 3) * 32;
-            tc_mma_bf16(tO[t], smem_desc_kmajor_sw128(sP + aoff), smem_desc_mnmajor_sw128(sV + kk * 2048, kBox),
-                        idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+            if (kPT)
+              tc_mma_bf16_ta(tO[t], tP[t] + kk * 8, smem_desc_mnmajor_sw128(sV + kk * 2048, kBox), idesc_pv,
+                             (j > 0 || kk > 0) ? 1u : 0u);
+            else
+              tc_mma_bf16(tO[t], smem_desc_kmajor_sw128(sP + aoff), smem_desc_mnmajor_sw128(sV + kk * 2048, kBox),
+                          idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(&p_empty[t]);
         }
@@ -296,17 +306,29 @@ __global__ void __launch_bounds__(kThr, 1)
         }
       }
       l += lt0 + lt1;
-      // the row's 128 keys: two 64-key boxes of 128-byte rows, 128-byte swizzle
+      if (kPT) {
+        // the row's 64 packed words into its TMEM lane, keys in order
 #pragma unroll
-      for (int bx = 0; bx < 2; ++bx)
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t pw[32];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const int w0 = bx * 32 + 4 * c;  // packed word index in the row
-          const uint4 u = make_uint4(r[w0 >> 4][w0 & 15], r[(w0 + 1) >> 4][(w0 + 1) & 15],
-                                     r[(w0 + 2) >> 4][(w0 + 2) & 15], r[(w0 + 3) >> 4][(w0 + 3) & 15]);
-          *reinterpret_cast<uint4*>(sP + bx * kBox + row * 128 + (((uint32_t)c ^ rsw) * 16)) = u;
+          for (int w = 0; w < 32; ++w) pw[w] = r[(32 * h2 + w) >> 4][(32 * h2 + w) & 15];
+          tmem_st_32x32b_x32(tP[t] + lane_off + h2 * 32, pw);
         }
-      fence_proxy_async_smem();
+        tmem_st_wait();
+      } else {
+        // the row's 128 keys: two 64-key boxes of 128-byte rows, 128-byte swizzle
+#pragma unroll
+        for (int bx = 0; bx < 2; ++bx)
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int w0 = bx * 32 + 4 * c;  // packed word index in the row
+            const uint4 u = make_uint4(r[w0 >> 4][w0 & 15], r[(w0 + 1) >> 4][(w0 + 1) & 15],
+                                       r[(w0 + 2) >> 4][(w0 + 2) & 15], r[(w0 + 3) >> 4][(w0 + 3) & 15]);
+            *reinterpret_cast<uint4*>(sP + bx * kBox + row * 128 + (((uint32_t)c ^ rsw) * 16)) = u;
+          }
+        fence_proxy_async_smem();
+      }
       tc_fence_before();
       mbar_arrive(&p_full[t]);
     }
