@@ -373,27 +373,52 @@ def run_reference(args, shape, world, rank, pg):
 
 
 def run_gemm_kernel(args):
-    """One GEMM shape through mt_k_gemm (a small case for profiler captures)."""
+    """One GEMM shape through mt_k_gemm (a small case for profiler captures).
+    --epilogue swiglu|swiglu_bwd|rope times the fused forms at the same
+    M, N, K (N = 2f for SwiGLU forward, f for its backward, the QKV width for
+    RoPE with 64-wide heads, 2048-token sequences)."""
     import torch
     import host_memory_resident_gb300 as mt
     M, N, K = (int(x) for x in args.shape.split(","))
     torch.manual_seed(0)
-    A = torch.randn(M, K, device="cuda").to(torch.bfloat16)
-    B = (torch.randn(N, K, device="cuda") / math.sqrt(K)).to(torch.bfloat16)
-    Cm = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+    dev = "cuda"
+    A = torch.randn(M, K, device=dev).to(torch.bfloat16)
+    epi = args.epilogue
+    if epi == "swiglu_bwd":
+        B = (torch.randn(K, N, device=dev) / math.sqrt(K)).to(torch.bfloat16)  # down weight [d, f]
+        gu = torch.randn(M, 2 * N, device=dev).to(torch.bfloat16)
+        Cm = torch.empty(M, 2 * N, device=dev, dtype=torch.bfloat16)
+        fn = lambda: mt.k_gemm_swiglu_bwd(A, B, gu, Cm)  # noqa: E731
+    else:
+        B = (torch.randn(N, K, device=dev) / math.sqrt(K)).to(torch.bfloat16)
+        Cm = torch.empty(M, N, device=dev, dtype=torch.bfloat16)
+        if epi == "swiglu":
+            a = torch.empty(M, N // 2, device=dev, dtype=torch.bfloat16)
+            fn = lambda: mt.k_gemm_swiglu_fwd(A, B, Cm, a)  # noqa: E731
+        elif epi == "rope":
+            hd, seq = 64, 2048
+            pos = torch.arange(seq, device=dev, dtype=torch.float64)[:, None]
+            inv = 10000.0 ** (-torch.arange(0, hd, 2, device=dev, dtype=torch.float64) / hd)
+            ct, st = torch.cos(pos * inv).float().contiguous(), torch.sin(pos * inv).float().contiguous()
+            rot = (N // hd - (N // hd) // 10) * hd  # q and k heads of a 32 + 4 + 4 head layout
+            fn = lambda: mt.k_gemm_rope(A, B, Cm, ct, st, rot, hd, seq)  # noqa: E731
+        else:
+            fn = lambda: mt.k_gemm(A, B, Cm)  # noqa: E731
     for _ in range(2):
-        mt.k_gemm(A, B, Cm)
+        fn()
     torch.cuda.synchronize()
     s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s0.record()
     for _ in range(args.iters):
-        mt.k_gemm(A, B, Cm)
+        fn()
     s1.record()
     torch.cuda.synchronize()
     ms = s0.elapsed_time(s1) / args.iters
-    ref = A[:256].float() @ B.float().t()
-    err = (Cm[:256].float() - ref).abs().max().item() / ref.abs().max().item()
-    print(json.dumps({"kernel": "gemm_abt", "M": M, "N": N, "K": K, "ms": ms,
+    err = 0.0
+    if epi is None:
+        ref = A[:256].float() @ B.float().t()
+        err = (Cm[:256].float() - ref).abs().max().item() / ref.abs().max().item()
+    print(json.dumps({"kernel": "gemm_abt" + (f"+{epi}" if epi else ""), "M": M, "N": N, "K": K, "ms": ms,
                       "tflops": 2.0 * M * N * K / ms / 1e9, "max_rel_err_rows0_255": err}), flush=True)
     return 0 if err < 2e-2 else 1
 
@@ -673,6 +698,8 @@ def main():
     ap.add_argument("--legacy", action="store_true", help="with --kernel attn: the mma.sync kernels")
     ap.add_argument("--backward", action="store_true", help="with --kernel attn: time the backward")
     ap.add_argument("--shape", default="8192,8192,2048")
+    ap.add_argument("--epilogue", default=None, choices=[None, "swiglu", "swiglu_bwd", "rope"],
+                    help="with --kernel gemm: a fused-epilogue form")
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--host-threads", type=int, default=0)

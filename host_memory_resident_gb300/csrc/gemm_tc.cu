@@ -77,17 +77,29 @@ struct GemmArgs {
   const float* cos_t;     // RoPE tables [seq, hd/2]
   const float* sin_t;
   int rot_cols, hd, seq;  // RoPE: rotate columns [0, rot_cols) in heads of hd
+  int st32;               // C (and C2) rows 32-byte aligned: whole-sector 32-byte stores
 };
 
-__device__ __forceinline__ void store_bf16x32(bf16* p, const float (&v)[32]) {
+// One 32-byte store (a whole L2 sector); p 32-byte aligned.
+__device__ __forceinline__ void st_global_32b(void* p, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3, uint32_t w4,
+                                              uint32_t w5, uint32_t w6, uint32_t w7) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w0), "r"(w1), "r"(w2), "r"(w3),
+               "r"(w4), "r"(w5), "r"(w6), "r"(w7)
+               : "memory");
+}
+
+// 32 values as bf16 at p (16-byte aligned; 32-byte aligned when st32).
+__device__ __forceinline__ void store_bf16x32(bf16* p, const float (&v)[32], int st32 = 0) {
+  uint32_t w[16];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint4 u;
-    u.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
-    u.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
-    u.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
-    u.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
-    reinterpret_cast<uint4*>(p)[j] = u;
+  for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+  if (st32) {
+    st_global_32b(p, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+    st_global_32b(p + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      reinterpret_cast<uint4*>(p)[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
   }
 }
 
@@ -301,8 +313,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int i = 0; i < 32; ++i) rope_pair(va[i], vb[i], cs[i], sn[i], va[i], vb[i]);
             }
             bf16* cp = reinterpret_cast<bf16*>(args.C) + (long long)row * args.ldc + col_h + j * 32;
-            store_bf16x32(cp, va);
-            store_bf16x32(cp + half, vb);
+            store_bf16x32(cp, va, args.st32);
+            store_bf16x32(cp + half, vb, args.st32);
           }
         }
       } else if (EPI == kEpiSwigluFwd) {
@@ -325,9 +337,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             a[i] = swiglu_fwd_elem(g[i], u[i]);
           }
           bf16* cp = reinterpret_cast<bf16*>(args.C) + (long long)row * args.ldc;
-          store_bf16x32(cp + fc, g);
-          store_bf16x32(cp + args.f + fc, u);
-          store_bf16x32(args.C2 + (long long)row * args.ldc2 + fc, a);
+          store_bf16x32(cp + fc, g, args.st32);
+          store_bf16x32(cp + args.f + fc, u, args.st32);
+          store_bf16x32(args.C2 + (long long)row * args.ldc2 + fc, a, args.st32);
         }
       } else if (EPI == kEpiSwigluBwd) {
         // the tile is da for ffn columns nb * 256 + [0, 256); the next
@@ -356,8 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
             bf16* cp = reinterpret_cast<bf16*>(args.C) + (long long)row * args.ldc + col0;
-            store_bf16x32(cp, dg);
-            store_bf16x32(cp + args.f, du);
+            store_bf16x32(cp, dg, args.st32);
+            store_bf16x32(cp + args.f, du, args.st32);
           }
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -397,7 +409,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (args.c_f32) {
             float* cp = reinterpret_cast<float*>(args.C) + (long long)row * args.ldc + col0;
-            if (full) {
+            if (full && args.st32) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                st_global_32b(cp + 8 * j, __float_as_uint(v[8 * j]), __float_as_uint(v[8 * j + 1]),
+                              __float_as_uint(v[8 * j + 2]), __float_as_uint(v[8 * j + 3]),
+                              __float_as_uint(v[8 * j + 4]), __float_as_uint(v[8 * j + 5]),
+                              __float_as_uint(v[8 * j + 6]), __float_as_uint(v[8 * j + 7]));
+            } else if (full) {
 #pragma unroll
               for (int j = 0; j < 8; ++j)
                 reinterpret_cast<float4*>(cp)[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
@@ -409,15 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             bf16* cp = reinterpret_cast<bf16*>(args.C) + (long long)row * args.ldc + col0;
             if (full) {
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                uint4 u;
-                u.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
-                u.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
-                u.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
-                u.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
-                reinterpret_cast<uint4*>(cp)[j] = u;
-              }
+              store_bf16x32(cp, v, args.st32);
             } else {
 #pragma unroll
               for (int i = 0; i < 32; ++i)
@@ -515,6 +526,9 @@ int launch(int epi, const void* A, long long lda, int a_mn, const void* B, long 
   args.num_mb = (M + kBM - 1) / kBM;
   args.num_nb = (N + kBN - 1) / kBN;
   args.err = device_error_word();
+  auto al32 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31) == 0; };
+  args.st32 = al32(args.C) && (args.c_f32 ? args.ldc % 8 == 0 : args.ldc % 16 == 0) &&
+              (args.C2 == nullptr || (al32(args.C2) && args.ldc2 % 16 == 0)) ? 1 : 0;
   const int tiles = args.num_mb * args.num_nb;
   const int grid = tiles < g_num_sms ? tiles : g_num_sms;
   if (epi == kEpiRope) {
