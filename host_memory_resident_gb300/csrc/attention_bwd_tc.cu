@@ -141,8 +141,8 @@ __global__ void __launch_bounds__(kThr, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 128);
-      mbar_init(&p_full[i], 128);
+      mbar_init(&s_empty[i], 4);  // one arrival per element-wise warp
+      mbar_init(&p_full[i], 4);
       mbar_init(&p_empty[i], 1);
     }
     mbar_init(done, 1);
@@ -247,7 +247,7 @@ __global__ void __launch_bounds__(kThr, 1)
     const uint32_t rsw = (uint32_t)(row & 7);
     auto group_sync = [&]() { asm volatile("bar.sync %0, 128;" ::"r"(1 + G) : "memory"); };
     // a wait's outcome, the same for the whole warp (tcgen05.ld is warp-wide)
-    auto wait_all = [&](uint64_t* bar, uint32_t parity) { return __all_sync(0xffffffffu, mbar_wait(bar, parity, err)); };
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) { return mbar_wait_warp(bar, parity, err); };
     bool ok = true;
     // every thread of the group runs every iteration's two group barriers,
     // also after a failed wait (it then skips the work), so none is left
@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(kThr, 1)
       }
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(&s_empty[G]);
+      mbar_arrive_warp(&s_empty[G]);
       const bool diag = q0 < k0 + kT;  // the sub-tile reaches the diagonal: mask key > query
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(kThr, 1)
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&p_full[G]);
+      mbar_arrive_warp(&p_full[G]);
     }
     if (ok && total > 0 && wait_all(done, 0)) {
       tc_fence_after();
@@ -379,9 +379,9 @@ __global__ void __launch_bounds__(kThr, 1)
       mbar_init(&kv_empty[i], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_full, 256);
+    mbar_init(p_full, 8);  // one arrival per element-wise warp
     mbar_init(p_empty, 1);
-    mbar_init(s_empty, 256);
+    mbar_init(s_empty, 8);
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(tmem_holder, 512);
@@ -461,7 +461,7 @@ __global__ void __launch_bounds__(kThr, 1)
     const float dl = qpos < s ? delta[vidx] : 0.f;
     bool ok = true;
     for (int j = 0; j < n_kv && ok; ++j) {
-      if (!mbar_wait(s_full, j & 1, err)) { ok = false; break; }
+      if (!mbar_wait_warp(s_full, j & 1, err)) { ok = false; break; }
       tc_fence_after();
       uint32_t rs[2][32], rp[2][32];
 #pragma unroll
@@ -471,7 +471,7 @@ __global__ void __launch_bounds__(kThr, 1)
       }
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(s_empty);
+      mbar_arrive_warp(s_empty);
       const bool diag = (j == n_kv - 1);
       const int kb = j * kT + half * 64;
       uint32_t dk[32];
@@ -487,13 +487,13 @@ __global__ void __launch_bounds__(kThr, 1)
         }
         dk[i] = pack_bf16x2(dv[0], dv[1]);
       }
-      if (j > 0 && !mbar_wait(p_empty, (j - 1) & 1, err)) { ok = false; break; }
+      if (j > 0 && !mbar_wait_warp(p_empty, (j - 1) & 1, err)) { ok = false; break; }
       store_half_row(sm + C::kDSOff, half, row, dk);
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive_warp(p_full);
     }
-    if (ok && mbar_wait(p_empty, (n_kv - 1) & 1, err)) {
+    if (ok && mbar_wait_warp(p_empty, (n_kv - 1) & 1, err)) {
       tc_fence_after();
       bf16* dqrow = dqkv + ((long long)b * s + qpos) * lddq + (long long)h * HD + half * (HD / 2);
       tmem_row_to_bf16(tdQ + lane_off + half * (HD / 2), HD / 2, rsqrtf((float)HD), dqrow, qpos < s);

@@ -111,8 +111,8 @@ __global__ void __launch_bounds__(kThr, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
-      mbar_init(&s_empty[t], 128);
-      mbar_init(&p_full[t], 128);
+      mbar_init(&s_empty[t], 4);  // one arrival per softmax warp
+      mbar_init(&p_full[t], 4);
       mbar_init(&p_empty[t], 1);
     }
     fence_barrier_init();
@@ -241,14 +241,14 @@ __global__ void __launch_bounds__(kThr, 1)
     const uint32_t rsw = (uint32_t)(row & 7);
     bool ok = true;
     for (int j = 0; j < nk && ok; ++j) {
-      if (!mbar_wait(&s_full[t], j & 1, err)) { ok = false; break; }
+      if (!mbar_wait_warp(&s_full[t], j & 1, err)) { ok = false; break; }
       tc_fence_after();
       uint32_t r[4][32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tS[t] + lane_off + c * 32, r[c]);
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(&s_empty[t]);
+      mbar_arrive_warp(&s_empty[t]);
       // only the diagonal tile (the last one) needs the causal mask
       if (j == nk - 1) {
         const int kbase = j * kKV;
@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(kThr, 1)
         }
       // P_t(j-1) V has finished: O_t is current and the P buffer is free
       if (j > 0) {
-        if (!mbar_wait(&p_empty[t], (j - 1) & 1, err)) { ok = false; break; }
+        if (!mbar_wait_warp(&p_empty[t], (j - 1) & 1, err)) { ok = false; break; }
         tc_fence_after();
       }
       if (__any_sync(0xffffffffu, need)) {
@@ -330,9 +330,9 @@ __global__ void __launch_bounds__(kThr, 1)
         fence_proxy_async_smem();
       }
       tc_fence_before();
-      mbar_arrive(&p_full[t]);
+      mbar_arrive_warp(&p_full[t]);
     }
-    if (ok && nk > 0 && mbar_wait(&p_empty[t], (nk - 1) & 1, err)) {
+    if (ok && nk > 0 && mbar_wait_warp(&p_empty[t], (nk - 1) & 1, err)) {
       tc_fence_after();
       const float inv = 1.f / l;
       bf16* orow = o + ((long long)b * s + qpos) * ldo + (long long)h * HD;
