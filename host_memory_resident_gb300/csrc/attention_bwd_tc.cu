@@ -475,17 +475,20 @@ __global__ void __launch_bounds__(kThr, 1)
       const bool diag = (j == n_kv - 1);
       const int kb = j * kT + half * 64;
       uint32_t dk[32];
+      const float2 sc2 = make_float2(sc, sc), nl2 = make_float2(-l2, -l2), ndl = make_float2(-dl, -dl);
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        float dv[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int ci = 2 * i + e;
-          float p = ex2_approx(fmaf(__uint_as_float(rs[ci >> 5][ci & 31]), sc, -l2));
-          if (diag && kb + ci > qpos) p = 0.f;
-          dv[e] = p * (__uint_as_float(rp[ci >> 5][ci & 31]) - dl);
+        const int ci = 2 * i;
+        const float2 x = ffma2(make_float2(__uint_as_float(rs[ci >> 5][ci & 31]), __uint_as_float(rs[ci >> 5][(ci + 1) & 31])),
+                               sc2, nl2);
+        float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        if (diag) {
+          if (kb + ci > qpos) pp.x = 0.f;
+          if (kb + ci + 1 > qpos) pp.y = 0.f;
         }
-        dk[i] = pack_bf16x2(dv[0], dv[1]);
+        const float2 dp = make_float2(__uint_as_float(rp[ci >> 5][ci & 31]), __uint_as_float(rp[ci >> 5][(ci + 1) & 31]));
+        const float2 dv = fmul2(pp, fadd2(dp, ndl));
+        dk[i] = pack_bf16x2(dv.x, dv.y);
       }
       if (j > 0 && !mbar_wait_warp(p_empty, (j - 1) & 1, err)) { ok = false; break; }
       store_half_row(sm + C::kDSOff, half, row, dk);

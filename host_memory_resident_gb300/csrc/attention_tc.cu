@@ -262,26 +262,27 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          m0 = fmaxf(m0, __uint_as_float(r[c][i]));
-          m1 = fmaxf(m1, __uint_as_float(r[c][i + 1]));
+        for (int i = 0; i < 32; i += 4) {
+          m0 = fmax3(m0, __uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1]));
+          m1 = fmax3(m1, __uint_as_float(r[c][i + 2]), __uint_as_float(r[c][i + 3]));
         }
       const float mx = fmaxf(m0, m1) * sc;  // row max in the scaled log2 domain (sc > 0)
       if (j == 0) m_ref = mx;
       const bool need = j > 0 && mx > m_ref + kRescale;
       const float m_use = need ? mx : m_ref;
       // P = exp2(s * sc - m_use), packed to bf16 in place
-      float lt0 = 0.f, lt1 = 0.f;
+      float2 lt = make_float2(0.f, 0.f);
+      const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m_use, -m_use);
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(r[c][2 * i]), sc, -m_use));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(r[c][2 * i + 1]), sc, -m_use));
-          lt0 += p0;
-          lt1 += p1;
-          r[c][i] = pack_bf16x2(p0, p1);
+          const float2 x = ffma2(make_float2(__uint_as_float(r[c][2 * i]), __uint_as_float(r[c][2 * i + 1])), sc2, nm2);
+          const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          lt = fadd2(lt, pp);
+          r[c][i] = pack_bf16x2(pp.x, pp.y);
         }
+      const float lt0 = lt.x, lt1 = lt.y;
       // P_t(j-1) V has finished: O_t is current and the P buffer is free
       if (j > 0) {
         if (!mbar_wait_warp(&p_empty[t], (j - 1) & 1, err)) { ok = false; break; }
