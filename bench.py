@@ -535,7 +535,7 @@ def run_ours(args, shape, world, rank, local, pg):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     cfg = mt.make_config(shape, device=local, host_threads=args.host_threads, overlap_adam=args.overlap,
-                         unfused_epilogues=args.unfused)
+                         unfused_epilogues=args.unfused, keep_attention=args.keep_attention)
     descs, n_total = mt.layout(cfg)
     segs = [(t["offset"], t["rows"] * t["cols"], "normal" if t["kind"] == 0 else "ones") for t in descs]
     master = synth.init_master(n_total, segs, seed=0)
@@ -640,6 +640,7 @@ def run_ours(args, shape, world, rank, local, pg):
                    "overlap_adam": bool(args.overlap),
                    "fp32_grad_array": bool(args.keep_grads),
                    "fused_epilogues": not args.unfused,
+                   "keep_attention": bool(args.keep_attention),
                    "l2": "inputs larger than L2: each step streams the whole bf16 store "
                          f"({w_bytes / 1e9:.2f} GB) and the activations"},
         "model_tflops": F / t_step / 1e12,
@@ -705,6 +706,8 @@ def main():
     ap.add_argument("--host-threads", type=int, default=0)
     ap.add_argument("--timeline", default=None, help="write the profiled step's Chrome/Perfetto trace here")
     ap.add_argument("--no-timeline", action="store_true", help="skip the extra profiled step (long configs)")
+    ap.add_argument("--keep-attention", action="store_true",
+                    help="keep attention outputs from the forward so the recompute skips attention (same results)")
     ap.add_argument("--unfused", action="store_true",
                     help="RoPE and SwiGLU as separate kernels instead of GEMM epilogues (same results)")
     ap.add_argument("--fused-grads", action="store_true",

@@ -146,6 +146,10 @@ struct mt_handle {
   mt::bf16 *xa = nullptr, *xb = nullptr;
   std::vector<mt::bf16*> ckpt;
   std::vector<mt::Saved> saved;
+  // keep_attention: every layer's attention output and log-sum-exp from the
+  // forward, so the backward's recompute skips the attention core
+  std::vector<mt::bf16*> att_o;
+  std::vector<float*> att_lse;
   mt::bf16 *xh = nullptr, *dz = nullptr;
   float *rf = nullptr, *logits = nullptr, *loss_rows = nullptr, *loss_dev = nullptr;
   float *dx32 = nullptr, *dh32 = nullptr, *dn32 = nullptr, *delta = nullptr, *npart = nullptr;
@@ -486,7 +490,10 @@ struct Step {
 
   // Forward of layer l with weights W; writes the saved activations into S and
   // the layer output into x_out.
-  void layer_fwd(const bf16* W, const Saved& S, bf16* x_out) {
+  // With keep_attention, S.o / S.lse point at layer l's kept tensors; the
+  // forward writes them and a recompute reads them instead of re-running the
+  // attention (the same values, so the step's results are unchanged).
+  void layer_fwd(const bf16* W, const Saved& S, bf16* x_out, bool recompute = false) {
     const LayerOffsets& o = h->lay.layer;
     const int d = h->d, f = h->f;
     KP(MT_PROF_NORM, 1, 0.0, norm_fwd_bytes(), mt_k_rmsnorm_fwd(S.x, W + o.attn_norm, S.u, S.r1, M, d, h->cfg.rms_eps, cs()));
@@ -501,8 +508,9 @@ struct Step {
       KP(MT_PROF_ROPE, 1, 0.0, rope_bytes(),
          mt_k_rope(S.qkv, h->qkvN, B, s, h->H + h->Hkv, h->hd, h->cos_t, h->sin_t, 0, cs()));
     }
-    KP(MT_PROF_ATTN_FWD, 1, attn_flops(false), 0.0,
-       mt_k_attn_fwd(S.qkv, h->qkvN, S.o, h->hq, S.lse, B, s, h->H, h->Hkv, h->hd, cs()));
+    if (!(recompute && h->cfg.keep_attention))
+      KP(MT_PROF_ATTN_FWD, 1, attn_flops(false), 0.0,
+         mt_k_attn_fwd(S.qkv, h->qkvN, S.o, h->hq, S.lse, B, s, h->H, h->Hkv, h->hd, cs()));
     gemm(S.o, h->hq, W + o.wo, h->hq, S.h, d, false, S.x, d, M, d, h->hq);
     KP(MT_PROF_NORM, 1, 0.0, norm_fwd_bytes(), mt_k_rmsnorm_fwd(S.h, W + o.mlp_norm, S.z, S.r2, M, d, h->cfg.rms_eps, cs()));
     if (fuse_swiglu_fwd()) {
@@ -627,11 +635,19 @@ struct Step {
       if (l >= last_a) {
         Saved& S = hh.saved[l - last_a];
         if (l == last_a) S.x = hh.ckpt[hh.nseg - 1];
+        if (hh.cfg.keep_attention) {
+          S.o = hh.att_o[l];
+          S.lse = hh.att_lse[l];
+        }
         out = (l + 1 < L) ? hh.saved[l + 1 - last_a].x : hh.xa;
         layer_fwd(W, S, out);
       } else {
         Saved S = hh.saved[0];
         S.x = x;
+        if (hh.cfg.keep_attention) {
+          S.o = hh.att_o[l];
+          S.lse = hh.att_lse[l];
+        }
         if ((l + 1) % C == 0) out = hh.ckpt[(l + 1) / C];
         else out = (x == hh.xa) ? hh.xb : hh.xa;
         layer_fwd(W, S, out);
@@ -653,8 +669,12 @@ struct Step {
         bf16* W = acquire(1 + l);
         Saved& S = hh.saved[l - a];
         if (l == a) S.x = hh.ckpt[seg];
+        if (hh.cfg.keep_attention) {
+          S.o = hh.att_o[l];
+          S.lse = hh.att_lse[l];
+        }
         bf16* out = (l + 1 < b) ? hh.saved[l + 1 - a].x : hh.xa;
-        layer_fwd(W, S, out);
+        layer_fwd(W, S, out, true);
         release();
       }
       for (int l = b - 1; l >= a; --l) {
@@ -745,6 +765,12 @@ void plan_device(mt_handle* h, Arena& A) {
     S.r2 = take<float>(A, M);
     S.gu = take<bf16>(A, M * 2 * f);
     S.a = take<bf16>(A, M * f);
+  }
+  h->att_o.assign(h->cfg.keep_attention ? h->L : 0, nullptr);
+  h->att_lse.assign(h->cfg.keep_attention ? h->L : 0, nullptr);
+  for (int l = 0; l < (int)h->att_o.size(); ++l) {
+    h->att_o[l] = take<bf16>(A, M * hq);
+    h->att_lse[l] = take<float>(A, M * H);
   }
   h->xh = take<bf16>(A, M * d);
   h->rf = take<float>(A, M);

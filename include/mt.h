@@ -67,6 +67,10 @@ typedef struct mt_config {
   int32_t unfused_epilogues; /* 1: RoPE and SwiGLU (forward and backward) run as separate kernels
                                 after their GEMMs instead of in the GEMM epilogues; the results are
                                 bitwise identical either way (0, the default, is faster) */
+  int32_t keep_attention;    /* 1: keep every layer's attention output and log-sum-exp from the
+                                forward (L * (M * H * hd * 2 + M * H * 4) more device bytes) so the
+                                backward's recompute skips the attention core; results are bitwise
+                                identical. 0 (default): recompute whole layers from the checkpoints */
 } mt_config;
 
 /* One tensor of the flat layout. kind 0 = matrix, 1 = norm weight. */

@@ -492,3 +492,29 @@ def test_profile_timeline_covers_the_step(tiny):
     # the host pass of a unit ends after that unit's slab copy
     d2h_end = max(r["end_ms"] for r in by["d2h"])
     assert max(r["end_ms"] for r in by["host_adam"]) >= d2h_end - 1.0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name,C", [("tiny", 2), ("tiny", 1), ("1.1b", 1)])
+def test_keep_attention_changes_no_bit(tiny, name, C):
+    """Keeping each layer's attention output and log-sum-exp for the backward
+    (instead of recomputing the attention) gives the loss, gradients and
+    updated master bit for bit; the planner still equals the live handle."""
+    if name == "tiny":
+        shape, B, s = tiny.with_(n_layers=4, ckpt_interval=C), None, None
+    else:
+        shape, B, s = synth.workload("1.1b").with_(n_layers=2, ckpt_interval=C), 1, 256
+    lay, master, _, _ = _setup(shape)
+    tokens, labels = synth.make_tokens(shape.vocab, B or shape.batch, s or shape.seq, seed=4)
+    out = []
+    for keep in (False, True):
+        w = master.copy()
+        cfg = mt.make_config(shape, batch=B, seq=s, keep_attention=keep)
+        with mt.Trainer(cfg, w) as tr:
+            losses = [tr.step(tokens, labels) for _ in range(2)]
+            g = tr.read_grads()
+            assert mt.plan(cfg)["device_bytes"] == tr.stats()["device_bytes"]
+        out.append((losses, g, w))
+    assert out[0][0] == out[1][0]
+    assert np.array_equal(out[0][1], out[1][1])
+    assert np.array_equal(out[0][2], out[1][2])
