@@ -376,7 +376,9 @@ def run_gemm_kernel(args):
     """One GEMM shape through mt_k_gemm (a small case for profiler captures).
     --epilogue swiglu|swiglu_bwd|rope times the fused forms at the same
     M, N, K (N = 2f for SwiGLU forward, f for its backward, the QKV width for
-    RoPE with 64-wide heads, 2048-token sequences)."""
+    RoPE with 64-wide heads, 2048-token sequences); wgrad times the weight
+    gradient G [M, N] over K tokens (split along K when it has few tiles),
+    wgrad_nosplit the same product unsplit."""
     import torch
     import host_memory_resident_gb300 as mt
     M, N, K = (int(x) for x in args.shape.split(","))
@@ -384,7 +386,14 @@ def run_gemm_kernel(args):
     dev = "cuda"
     A = torch.randn(M, K, device=dev).to(torch.bfloat16)
     epi = args.epilogue
-    if epi == "swiglu_bwd":
+    if epi in ("wgrad", "wgrad_nosplit"):
+        # weight gradient G [M, N] = dY^T X over K tokens, both token-major
+        A = torch.randn(K, M, device=dev).to(torch.bfloat16)
+        B = (torch.randn(K, N, device=dev) / math.sqrt(K)).to(torch.bfloat16)
+        Cm = torch.empty(M, N, device=dev, dtype=torch.bfloat16)
+        ws = torch.empty(mt.k_gemm_wgrad_ws(M, N), device=dev) if epi == "wgrad" else None
+        fn = lambda: mt.k_gemm_wgrad(A, B, Cm, ws)  # noqa: E731
+    elif epi == "swiglu_bwd":
         B = (torch.randn(K, N, device=dev) / math.sqrt(K)).to(torch.bfloat16)  # down weight [d, f]
         gu = torch.randn(M, 2 * N, device=dev).to(torch.bfloat16)
         Cm = torch.empty(M, 2 * N, device=dev, dtype=torch.bfloat16)
@@ -418,7 +427,11 @@ def run_gemm_kernel(args):
     if epi is None:
         ref = A[:256].float() @ B.float().t()
         err = (Cm[:256].float() - ref).abs().max().item() / ref.abs().max().item()
+    if epi in ("wgrad", "wgrad_nosplit"):
+        ref = A[:, :256].float().t() @ B.float()
+        err = (Cm[:256].float() - ref).abs().max().item() / ref.abs().max().item()
     print(json.dumps({"kernel": "gemm_abt" + (f"+{epi}" if epi else ""), "M": M, "N": N, "K": K, "ms": ms,
+                      "splits": mt.k_gemm_splitk(M, N, K) if epi == "wgrad" else 1,
                       "tflops": 2.0 * M * N * K / ms / 1e9, "max_rel_err_rows0_255": err}), flush=True)
     return 0 if err < 2e-2 else 1
 
@@ -699,7 +712,7 @@ def main():
     ap.add_argument("--legacy", action="store_true", help="with --kernel attn: the mma.sync kernels")
     ap.add_argument("--backward", action="store_true", help="with --kernel attn: time the backward")
     ap.add_argument("--shape", default="8192,8192,2048")
-    ap.add_argument("--epilogue", default=None, choices=[None, "swiglu", "swiglu_bwd", "rope"],
+    ap.add_argument("--epilogue", default=None, choices=[None, "swiglu", "swiglu_bwd", "rope", "wgrad", "wgrad_nosplit"],
                     help="with --kernel gemm: a fused-epilogue form")
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -72,7 +72,7 @@ EXPORTS = [
     "mt_read_grads", "mt_sync", "mt_get_step", "mt_set_step", "mt_sync_store", "mt_get_stats",
     "mt_get_stream", "mt_profile_enable", "mt_profile_read", "mt_profile_timeline", "mt_destroy", "mt_last_error", "mt_debug_inject", "mt_debug_inject_global",
     "mt_host_adam", "mt_host_adam_slab", "mt_host_to_bf16",
-    "mt_k_gemm", "mt_k_gemm_ex", "mt_k_gemm_rope", "mt_k_gemm_swiglu_fwd", "mt_k_gemm_swiglu_bwd", "mt_k_transpose", "mt_k_rmsnorm_fwd", "mt_k_rmsnorm_bwd", "mt_k_rmsnorm_bwd_parts",
+    "mt_k_gemm", "mt_k_gemm_ex", "mt_k_gemm_rope", "mt_k_gemm_swiglu_fwd", "mt_k_gemm_swiglu_bwd", "mt_k_gemm_wgrad", "mt_k_gemm_splitk", "mt_k_gemm_wgrad_ws", "mt_k_transpose", "mt_k_rmsnorm_fwd", "mt_k_rmsnorm_bwd", "mt_k_rmsnorm_bwd_parts",
     "mt_k_rope", "mt_k_swiglu_fwd", "mt_k_swiglu_bwd", "mt_k_attn_fwd", "mt_k_attn_fwd_mma", "mt_k_attn_bwd", "mt_k_attn_bwd_mma",
     "mt_k_cross_entropy", "mt_k_sum", "mt_k_embedding_fwd", "mt_k_embedding_bwd",
     "mt_k_embedding_bwd_work", "mt_k_check_ids", "mt_k_device_error",
@@ -123,6 +123,9 @@ def lib():
         "mt_k_gemm_rope": ([P, I64, P, I64, P, I64, I, I, I, P, P, I, I, I, P], I),
         "mt_k_gemm_swiglu_fwd": ([P, I64, P, I64, P, I64, P, I64, I, I, I, P], I),
         "mt_k_gemm_swiglu_bwd": ([P, I64, P, I64, P, I64, P, I64, I, I, I, P], I),
+        "mt_k_gemm_wgrad": ([P, I64, P, I64, P, I64, I, I, I, P, I64, P], I),
+        "mt_k_gemm_splitk": ([I, I, I], I),
+        "mt_k_gemm_wgrad_ws": ([I, I], I64),
         "mt_k_transpose": ([P, I64, P, I64, I, I, P], I),
         "mt_k_rmsnorm_fwd": ([P, P, P, P, I, I, F, P], I),
         "mt_k_rmsnorm_bwd": ([P, P, P, P, P, P, P, P, P, I, I, P], I),
@@ -437,6 +440,23 @@ def k_gemm_swiglu_bwd(dy, W, gu, dgu, stream=None):
     M, f = dy.shape[0], W.shape[1]
     check(lib().mt_k_gemm_swiglu_bwd(_dp(dy), dy.stride(0), _dp(W), W.stride(0), _dp(gu), gu.stride(0), _dp(dgu),
                                      dgu.stride(0), M, f, dy.shape[1], _st(stream)))
+
+
+def k_gemm_wgrad(dY, X, G, ws=None, stream=None):
+    """G = dY^T X (dY [K, M], X [K, N], G bf16 [M, N]), split along K into the
+    fp32 workspace ws when the output has few tiles."""
+    K, M = dY.shape
+    N = X.shape[1]
+    check(lib().mt_k_gemm_wgrad(_dp(dY), dY.stride(0), _dp(X), X.stride(0), _dp(G), G.stride(0), M, N, K, _dp(ws),
+                                ws.numel() if ws is not None else 0, _st(stream)))
+
+
+def k_gemm_splitk(M, N, K):
+    return lib().mt_k_gemm_splitk(M, N, K)
+
+
+def k_gemm_wgrad_ws(M, N):
+    return lib().mt_k_gemm_wgrad_ws(M, N)
 
 
 def k_rope(x, B, s, n_rot_heads, hd, cos_t, sin_t, inverse=False, stream=None):

@@ -154,6 +154,9 @@ struct mt_handle {
   float *rf = nullptr, *logits = nullptr, *loss_rows = nullptr, *loss_dev = nullptr;
   float *dx32 = nullptr, *dh32 = nullptr, *dn32 = nullptr, *delta = nullptr, *npart = nullptr;
   mt::bf16 *dxb = nullptr, *dhb = nullptr, *da = nullptr, *dgu = nullptr, *dob = nullptr, *dqkv = nullptr;
+  // fp32 partial products of the weight gradients that are split along K
+  float* wg_ws = nullptr;
+  size_t wg_ws_elems = 0;
 
   // streams and events
   cudaStream_t s_comp = nullptr, s_h2d = nullptr, s_d2h = nullptr;
@@ -474,6 +477,14 @@ struct Step {
     KP(MT_PROF_GEMM, 1, 2.0 * m * n * k, bytes,
        gemm_ex(A, lda, a_mn ? 1 : 0, Bm, ldb, b_mn ? 1 : 0, C, ldc, f32 ? 1 : 0, nullptr, 0, m, n, k, cs()));
   }
+  // Weight gradient g[m, n] = dY^T X over the step's M tokens (both read
+  // token-major), split along the tokens when the output has few tiles.
+  void gemm_wg(const bf16* dY, long long ldy, const bf16* X, long long ldx, bf16* g, long long ldg, int m, int n) {
+    const int sp = splitk_factor(m, n, M);
+    const double bytes = 2.0 * ((double)m * M + (double)n * M) + 2.0 * m * n;
+    KP(MT_PROF_GEMM, sp > 1 ? 2 : 1, 2.0 * m * n * (double)M, bytes,
+       gemm_wgrad(dY, ldy, 1, X, ldx, 1, g, ldg, m, n, M, h->wg_ws, h->wg_ws_elems, cs()));
+  }
   double attn_flops(bool bwd) const {
     // causal: half of the s x s score matrix; forward 2 products, backward 5
     const double per = 2.0 * B * (double)h->H * s * (double)s * h->hd / 2.0;
@@ -534,7 +545,7 @@ struct Step {
     // (MN-major operands, K = tokens); input gradients dX = dY W read the
     // weight [out, in] in place as a [K, N] operand. Nothing is transposed.
     // down projection: dWdown = dy^T a ; da = dy Wdown
-    gemm_mn(h->dxb, d, true, S.a, f, true, g + o.wdown, f, false, d, f, M);
+    gemm_wg(h->dxb, d, S.a, f, g + o.wdown, f, d, f);
     if (fuse_swiglu_bwd()) {
       // da = dy Wdown stays in the SM; the epilogue writes d(gate) | d(up)
       const double bytes = 2.0 * ((double)M * d + (double)d * f + 2.0 * M * f + 2.0 * M * f);
@@ -545,20 +556,20 @@ struct Step {
       KP(MT_PROF_SWIGLU, 1, 0.0, 10.0 * M * f, mt_k_swiglu_bwd(h->da, S.gu, h->dgu, M, f, cs()));
     }
     // gate/up projection
-    gemm_mn(h->dgu, 2 * f, true, S.z, d, true, g + o.wgu, d, false, 2 * f, d, M);
+    gemm_wg(h->dgu, 2 * f, S.z, d, g + o.wgu, d, 2 * f, d);
     gemm_mn(h->dgu, 2 * f, false, W + o.wgu, d, true, h->dn32, d, true, M, d, 2 * f);
     KP(MT_PROF_NORM, 2, 0.0, norm_bwd_bytes(true),
        mt_k_rmsnorm_bwd(h->dn32, S.h, W + o.mlp_norm, S.r2, h->dx32, h->dh32, h->dhb, h->npart, g + o.mlp_norm, M,
                         d, cs()));
     // output projection
-    gemm_mn(h->dhb, d, true, S.o, hq, true, g + o.wo, hq, false, d, hq, M);
+    gemm_wg(h->dhb, d, S.o, hq, g + o.wo, hq, d, hq);
     gemm_mn(h->dhb, d, false, W + o.wo, hq, true, h->dob, hq, false, M, hq, d);
     // attention and RoPE
     KP(MT_PROF_ATTN_BWD, 3, attn_flops(true), 0.0,
        mt_k_attn_bwd(S.qkv, qn, S.o, hq, h->dob, hq, S.lse, h->delta, h->dqkv, qn, B, s, h->H, h->Hkv, h->hd, cs()));
     KP(MT_PROF_ROPE, 1, 0.0, rope_bytes(), mt_k_rope(h->dqkv, qn, B, s, h->H + h->Hkv, h->hd, h->cos_t, h->sin_t, 1, cs()));
     // qkv projection
-    gemm_mn(h->dqkv, qn, true, S.u, d, true, g + o.wqkv, d, false, qn, d, M);
+    gemm_wg(h->dqkv, qn, S.u, d, g + o.wqkv, d, qn, d);
     gemm_mn(h->dqkv, qn, false, W + o.wqkv, d, true, h->dn32, d, true, M, d, qn);
     KP(MT_PROF_NORM, 2, 0.0, norm_bwd_bytes(true),
        mt_k_rmsnorm_bwd(h->dn32, S.x, W + o.attn_norm, S.r1, h->dh32, h->dx32, h->dxb, h->npart, g + o.attn_norm, M,
@@ -583,7 +594,7 @@ struct Step {
     CK(cudaMemcpyAsync(h->loss_pinned + parity(), h->loss_dev, sizeof(float), cudaMemcpyDeviceToHost, cs()));
     CK(cudaEventRecord(h->ev_loss[parity()], cs()));
     // dHead = dz^T xh ; dxh = dz Head (both read in place)
-    gemm_mn(h->dz, V, true, h->xh, d, true, g + h->lay.head, d, false, V, d, M);
+    gemm_wg(h->dz, V, h->xh, d, g + h->lay.head, d, V, d);
     gemm_mn(h->dz, V, false, head, d, true, h->dn32, d, true, M, d, V);
     KP(MT_PROF_NORM, 2, 0.0, norm_bwd_bytes(false),
        mt_k_rmsnorm_bwd(h->dn32, xL, wf, h->rf, nullptr, h->dx32, h->dxb, h->npart, g + h->lay.final_norm, M, d,
@@ -788,6 +799,13 @@ void plan_device(mt_handle* h, Arena& A) {
   h->dob = take<bf16>(A, M * hq);
   h->dqkv = take<bf16>(A, M * qn);
   h->delta = take<float>(A, M * H);
+  {
+    const int shp[5][2] = {{(int)d, (int)f}, {(int)(2 * f), (int)d}, {(int)d, (int)hq}, {(int)qn, (int)d}, {(int)V, (int)d}};
+    size_t ws = 0;
+    for (auto& x : shp) ws = std::max(ws, splitk_ws_elems(x[0], x[1]));
+    h->wg_ws_elems = ws;
+    h->wg_ws = ws ? take<float>(A, ws) : nullptr;
+  }
   h->npart = take<float>(A, (size_t)mt_k_rmsnorm_bwd_parts((int)M) * d);
 
 }

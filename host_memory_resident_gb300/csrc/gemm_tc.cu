@@ -78,6 +78,11 @@ struct GemmArgs {
   const float* sin_t;
   int rot_cols, hd, seq;  // RoPE: rotate columns [0, rot_cols) in heads of hd
   int st32;               // C (and C2) rows 32-byte aligned: whole-sector 32-byte stores
+  // split K: work unit t is output tile t % tiles over K blocks
+  // [s * kbps, (s + 1) * kbps) with s = t / tiles; slice s of the (fp32)
+  // output starts split_stride elements after slice s - 1
+  int splits, kbps;
+  long long split_stride;
 };
 
 // One 32-byte store (a whole L2 sector); p 32-byte aligned.
@@ -139,6 +144,18 @@ __device__ __forceinline__ void load_f32x32(const float* p, float (&v)[32]) {
   }
 }
 
+__device__ __forceinline__ void tile_coords(int t, int num_mb, int num_nb, int& mb, int& nb);
+
+// Work unit t: its output tile (mb, nb), split sp and K-block range [kb0, kb1).
+__device__ __forceinline__ void unit_coords(int t, const GemmArgs& a, int num_kb, int& mb, int& nb, int& sp, int& kb0,
+                                            int& kb1) {
+  const int tiles = a.num_mb * a.num_nb;
+  sp = t / tiles;
+  tile_coords(t - sp * tiles, a.num_mb, a.num_nb, mb, nb);
+  kb0 = sp * a.kbps;
+  kb1 = min(num_kb, kb0 + a.kbps);
+}
+
 __device__ __forceinline__ void tile_coords(int t, int num_mb, int num_nb, int& mb, int& nb) {
   const int per_group = kGroupM * num_nb;
   const int group = t / per_group;
@@ -152,6 +169,27 @@ __device__ __forceinline__ void tile_coords(int t, int num_mb, int num_nb, int& 
 // A_MN / B_MN: the operand is stored MN-major in global memory (A as
 // [K][M], B as [K][N], MN contiguous) and staged as 64 x 64 boxes.
 constexpr uint32_t kBoxBytes = 64 * 64 * 2;  // one 64 MN x 64 K box
+
+// out[m, n] = bf16(sum over s = 0 .. S-1, in order, of ws[s][m][n]); one
+// thread per 8 columns. The split-K weight gradients end here.
+__global__ void splitk_reduce_kernel(const float* __restrict__ ws, int S, long long slice, int M, int N,
+                                     bf16* __restrict__ out, long long ldo) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int nv = N >> 3;
+  if (idx >= (long long)M * nv) return;
+  const int row = (int)(idx / nv), v = (int)(idx % nv);
+  const float* p = ws + (long long)row * N + v * 8;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int sp = 0; sp < S; ++sp) {
+    const float4 a = reinterpret_cast<const float4*>(p + sp * slice)[0];
+    const float4 b = reinterpret_cast<const float4*>(p + sp * slice)[1];
+    acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+    acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+  }
+  *reinterpret_cast<uint4*>(out + (long long)row * ldo + v * 8) =
+      make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                 pack_bf16x2(acc[6], acc[7]));
+}
 
 template <bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -168,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int num_tiles = args.num_mb * args.num_nb;
+  const int num_tiles = args.num_mb * args.num_nb * args.splits;  // work units
   const int num_kb = (args.K + kBK - 1) / kBK;
 
   if (threadIdx.x == 0) {
@@ -197,9 +235,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x) {
-        int mb, nb;
-        tile_coords(t, args.num_mb, args.num_nb, mb, nb);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        int mb, nb, sp, kb0, kb1;
+        unit_coords(t, args, num_kb, mb, nb, sp, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1, args.err)) { *abort_flag = 1; break; }
           uint8_t* sa = smem + stage * kStageBytes;
           uint8_t* sb = sa + kABytes;
@@ -239,8 +277,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&tempty_bar[acc], (use & 1) ^ 1, args.err)) { *abort_flag = 1; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
+        int mb, nb, sp, kb0, kb1;
+        unit_coords(t, args, num_kb, mb, nb, sp, kb0, kb1);
         bool ok = true;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full_bar[stage], phase, args.err)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * kStageBytes);
@@ -252,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      : smem_desc_kmajor_sw128(sa + kk * 32);
             const uint64_t bd = B_MN ? smem_desc_mnmajor_sw128(sb + kk * 2048, kBoxBytes)
                                      : smem_desc_kmajor_sw128(sb + kk * 32);
-            tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            tc_mma_bf16(d_tmem, ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(&empty_bar[stage]);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -270,8 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
       const int acc = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
-      int mb, nb;
-      tile_coords(t, args.num_mb, args.num_nb, mb, nb);
+      int mb, nb, sp, kb0, kb1;
+      unit_coords(t, args, (args.K + kBK - 1) / kBK, mb, nb, sp, kb0, kb1);
       const int row = mb * kBM + q * 32 + lane;
       const bool row_ok = row < args.M;
       // SwiGLU backward: the gate | up values of this warp's first chunk do
@@ -408,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (args.c_f32) {
-            float* cp = reinterpret_cast<float*>(args.C) + (long long)row * args.ldc + col0;
+            float* cp = reinterpret_cast<float*>(args.C) + sp * args.split_stride + (long long)row * args.ldc + col0;
             if (full && args.st32) {
 #pragma unroll
               for (int j = 0; j < 4; ++j)
@@ -515,6 +555,11 @@ int launch(int epi, const void* A, long long lda, int a_mn, const void* B, long 
   if (b_mn ? ldb < N : ldb < K) return MT_EINVAL;
   if (args.ldc < N || (args.c_f32 ? (args.ldc % 4) : (args.ldc % 8))) return MT_EINVAL;
   if (args.R && (args.ldr % 8 || args.ldr < N)) return MT_EINVAL;
+  // split K: every split gets at least one K block
+  const int num_kb = (K + kBK - 1) / kBK;
+  if (args.splits < 1) args.splits = 1;
+  args.kbps = (num_kb + args.splits - 1) / args.splits;
+  args.splits = (num_kb + args.kbps - 1) / args.kbps;
   CUtensorMap ta, tb;
   // K-major: rows = M (or N), cols = K, box kBM (kBN) x 64; MN-major: rows = K,
   // cols = M (or N), box 64 x 64. The SwiGLU forward loads its B tile as two
@@ -529,7 +574,7 @@ int launch(int epi, const void* A, long long lda, int a_mn, const void* B, long 
   auto al32 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31) == 0; };
   args.st32 = al32(args.C) && (args.c_f32 ? args.ldc % 8 == 0 : args.ldc % 16 == 0) &&
               (args.C2 == nullptr || (al32(args.C2) && args.ldc2 % 16 == 0)) ? 1 : 0;
-  const int tiles = args.num_mb * args.num_nb;
+  const int tiles = args.num_mb * args.num_nb * args.splits;
   const int grid = tiles < g_num_sms ? tiles : g_num_sms;
   if (epi == kEpiRope) {
     if (a_mn || b_mn) return MT_EINVAL;
@@ -560,6 +605,7 @@ GemmArgs base_args(int M, int N, int K, void* C, long long ldc, int c_f32) {
   a.C = C;
   a.ldc = ldc;
   a.c_f32 = c_f32;
+  a.splits = 1;
   return a;
 }
 
@@ -573,6 +619,54 @@ int gemm_ex(const void* A, long long lda, int a_mn, const void* B, long long ldb
   args.R = reinterpret_cast<const bf16*>(R);
   args.ldr = ldr;
   return launch(kEpiPlain, A, lda, a_mn, B, ldb, b_mn, args, stream);
+}
+
+int splitk_factor(int M, int N, int K) {
+  // Output tiles that leave a large share of the 152 SMs idle in the last
+  // wave are split along K when that shortens the launch: time in K-block
+  // units, waves x K blocks per split, plus the reduction's bytes at HBM
+  // speed (one K block of one tile: about 0.37 us; HBM: about 6.5 TB/s).
+  constexpr int kSMs = 152;
+  constexpr double kKBlockUs = 0.371, kHbmBytesPerUs = 6.5e6;
+  const long long tiles = (long long)((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+  const int num_kb = (K + kBK - 1) / kBK;
+  if (N % 8 || tiles >= 4 * kSMs || num_kb < 16) return 1;
+  int best = 1;
+  double best_us = 0.0;
+  for (int sp = 1; sp <= 4; ++sp) {
+    const int kbps = (num_kb + sp - 1) / sp;
+    const int spe = (num_kb + kbps - 1) / kbps;
+    const double waves = (double)((tiles * spe + kSMs - 1) / kSMs);
+    double us = waves * kbps * kKBlockUs;
+    if (spe > 1) us += (double)(spe * 4 + 2) * M * N / kHbmBytesPerUs;
+    if (sp == 1 || us < best_us) {
+      best = spe;
+      best_us = us;
+    }
+  }
+  return best;
+}
+
+size_t splitk_ws_elems(int M, int N) {
+  const long long tiles = (long long)((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+  return (N % 8 || tiles >= 4 * 152) ? 0 : (size_t)4 * M * N;
+}
+
+int gemm_wgrad(const void* A, long long lda, int a_mn, const void* B, long long ldb, int b_mn, void* C, long long ldc,
+               int M, int N, int K, float* ws, size_t ws_elems, cudaStream_t stream) {
+  const int sp = splitk_factor(M, N, K);
+  if (sp <= 1 || ws == nullptr || (size_t)sp * M * N > ws_elems || ldc % 8 ||
+      (reinterpret_cast<uintptr_t>(C) & 15))
+    return gemm_ex(A, lda, a_mn, B, ldb, b_mn, C, ldc, 0, nullptr, 0, M, N, K, stream);
+  GemmArgs args = base_args(M, N, K, ws, N, 1);
+  args.splits = sp;
+  args.split_stride = (long long)M * N;
+  const int r = launch(kEpiPlain, A, lda, a_mn, B, ldb, b_mn, args, stream);
+  if (r != MT_OK) return r;
+  const long long threads = (long long)M * (N / 8);
+  splitk_reduce_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(ws, args.splits, args.split_stride, M, N,
+                                                                              reinterpret_cast<bf16*>(C), ldc);
+  return cudaGetLastError() == cudaSuccess ? MT_OK : MT_ECUDA;
 }
 
 int gemm_rope(const void* A, long long lda, const void* B, long long ldb, void* C, long long ldc, int M, int N, int K,

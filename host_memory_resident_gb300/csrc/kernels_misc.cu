@@ -625,6 +625,16 @@ int mt_k_gemm_swiglu_bwd(const void* dy, int64_t lddy, const void* W, int64_t ld
   return gemm_swiglu_bwd(dy, lddy, W, ldw, gu, ldgu, dgu, lddgu, M, f, K, (cudaStream_t)stream);
 }
 
+int mt_k_gemm_wgrad(const void* dY, int64_t lddy, const void* X, int64_t ldx, void* G, int64_t ldg, int M, int N,
+                    int K, float* ws, int64_t ws_elems, void* stream) {
+  if (ws_elems < 0) return MT_EINVAL;
+  return gemm_wgrad(dY, lddy, 1, X, ldx, 1, G, ldg, M, N, K, ws, (size_t)ws_elems, (cudaStream_t)stream);
+}
+
+int mt_k_gemm_splitk(int M, int N, int K) { return (M <= 0 || N <= 0 || K <= 0) ? 1 : splitk_factor(M, N, K); }
+
+int64_t mt_k_gemm_wgrad_ws(int M, int N) { return (M <= 0 || N <= 0) ? 0 : (int64_t)splitk_ws_elems(M, N); }
+
 int mt_k_transpose(const void* in, int64_t ld_in, void* out, int64_t ld_out, int rows, int cols, void* stream) {
   if (rows < 0 || cols < 0 || ld_in < cols || ld_out < rows) return MT_EINVAL;
   if (rows == 0 || cols == 0) return MT_OK;

@@ -22,6 +22,17 @@ void set_last_error_message(const std::string& msg);
 int gemm_ex(const void* A, long long lda, int a_mn, const void* B, long long ldb, int b_mn, void* C, long long ldc,
             int c_f32, const void* R, long long ldr, int M, int N, int K, cudaStream_t stream);
 
+// Split-K factor the library uses for C[M, N] over K (1: no split; depends
+// on the shape only, so planning needs no GPU).
+int splitk_factor(int M, int N, int K);
+// Workspace elements gemm_wgrad needs to split C[M, N] for any K (0: never).
+size_t splitk_ws_elems(int M, int N);
+// C (bf16) = op(A) op(B)^T over K, split along K into fp32 slices of ws
+// (splitk_factor(M, N, K) * M * N elements) and summed in a fixed order when
+// that is faster; a plain product otherwise. Deterministic.
+int gemm_wgrad(const void* A, long long lda, int a_mn, const void* B, long long ldb, int b_mn, void* C, long long ldc,
+               int M, int N, int K, float* ws, size_t ws_elems, cudaStream_t stream);
+
 // GEMMs with fused epilogues; see mt_k_gemm_rope, mt_k_gemm_swiglu_fwd,
 // mt_k_gemm_swiglu_bwd.
 int gemm_rope(const void* A, long long lda, const void* B, long long ldb, void* C, long long ldc, int M, int N, int K,

@@ -85,6 +85,27 @@ int mt_k_gemm_swiglu_fwd(const void* A, int64_t lda, const void* W, int64_t ldw,
 int mt_k_gemm_swiglu_bwd(const void* dy, int64_t lddy, const void* W, int64_t ldw, const void* gu, int64_t ldgu,
                          void* dgu, int64_t lddgu, int M, int f, int K, void* stream);
 
+/*
+ * Weight gradient of a linear layer, G = dY^T X over K tokens: dY bf16
+ * [K, M] (pitch lddy), X bf16 [K, N] (pitch ldx), G bf16 [M, N] (pitch ldg,
+ * a multiple of 8; G 16-byte aligned). When M x N has too few 128 x 256
+ * output tiles to fill the 152 SMs (mt_k_gemm_splitk(M, N, K) > 1), the K
+ * tokens are split into that many contiguous ranges, each range's fp32
+ * product goes to its own slice of the device workspace ws (ws_elems fp32
+ * elements, at least mt_k_gemm_wgrad_ws(M, N); caller-owned) and the slices
+ * are summed in slice order and rounded once to bf16: deterministic, and
+ * equal to the unsplit product up to fp32 summation order. With ws NULL or
+ * too small it is the plain product (mt_k_gemm_ex, a_mn = b_mn = 1). The
+ * layer-wise backward of the streamed template (the zhichai.net article,
+ * point 5) computes every dW this way before the slab copy.
+ */
+int mt_k_gemm_wgrad(const void* dY, int64_t lddy, const void* X, int64_t ldx, void* G, int64_t ldg, int M, int N,
+                    int K, float* ws, int64_t ws_elems, void* stream);
+/* Split factor mt_k_gemm_wgrad uses for G [M, N] over K tokens (1: none). */
+int mt_k_gemm_splitk(int M, int N, int K);
+/* fp32 workspace elements mt_k_gemm_wgrad may use for G [M, N] at any K. */
+int64_t mt_k_gemm_wgrad_ws(int M, int N);
+
 /* out[c, r] = in[r, c] for a bf16 [rows, cols] matrix (ld_in >= cols, ld_out >= rows). */
 int mt_k_transpose(const void* in, int64_t ld_in, void* out, int64_t ld_out, int rows, int cols, void* stream);
 

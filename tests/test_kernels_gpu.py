@@ -114,6 +114,37 @@ def test_gemm_deterministic():
     assert torch.equal(c1, c2)
 
 
+@pytest.mark.parametrize("M,N,K", [(384, 512, 8192), (296, 520, 5000), (2560, 2048, 16384)])
+def test_gemm_wgrad_split_k(M, N, K):
+    """Split-K weight gradient: near the fp64 product, deterministic, and the
+    unsplit product (bit for bit) when the workspace is missing or short."""
+    sp = mt.k_gemm_splitk(M, N, K)
+    assert sp > 1
+    rng = np.random.default_rng(M + N + K)
+    dY, dYh = bf(rng.standard_normal((K, M)) / np.sqrt(K))
+    X, Xh = bf(rng.standard_normal((K, N)))
+    ws = torch.empty(mt.k_gemm_wgrad_ws(M, N), device=DEV, dtype=torch.float32)
+    assert ws.numel() >= sp * M * N
+    g1 = torch.full((M, N), float("nan"), device=DEV, dtype=torch.bfloat16)
+    g2 = torch.full((M, N), float("nan"), device=DEV, dtype=torch.bfloat16)
+    mt.k_gemm_wgrad(dY, X, g1, ws)
+    ws.fill_(float("nan"))
+    mt.k_gemm_wgrad(dY, X, g2, ws)
+    plain = torch.empty((M, N), device=DEV, dtype=torch.bfloat16)
+    mt.k_gemm_ex(dY, True, X, True, plain)
+    g3 = torch.empty((M, N), device=DEV, dtype=torch.bfloat16)
+    mt.k_gemm_wgrad(dY, X, g3, ws[: sp * M * N - 1])
+    torch.cuda.synchronize()
+    assert torch.equal(g1, g2)
+    assert torch.equal(g3, plain)
+    if M * N * K <= 8192 * 512 * 384:
+        ref = dYh.T @ Xh
+    else:   # rows sampled from the full product
+        rows = np.arange(0, M, 37)
+        ref, g1 = dYh[:, rows].T @ Xh, g1[torch.as_tensor(rows, device=DEV)]
+    assert_close(host(g1), ref, l2=5e-3, elem=1e-2, what=f"wgrad {M}x{N}x{K} split {sp}")
+
+
 # ---------------------------------------------------------------- transpose
 @pytest.mark.parametrize("rows,cols", [(1, 1), (64, 64), (100, 37), (2048, 5632)])
 def test_transpose_exact(rows, cols):

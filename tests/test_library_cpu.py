@@ -181,3 +181,12 @@ def test_null_handle_calls_fail_cleanly(L):
     assert L.mt_train_step(None, None, None, 1, 1, C.byref(loss)) == mt.MT_EINVAL
     assert L.mt_read_grads(None, None, 0) == mt.MT_EINVAL
     assert L.mt_destroy(None) == mt.MT_EINVAL
+
+
+def test_gemm_splitk_factor_choices(L):
+    # 160 tiles of the 1.1B QKV gradient over 16384 tokens: split; 2000 tiles
+    # of the head gradient, or a short K: not split
+    assert mt.k_gemm_splitk(2560, 2048, 16384) > 1
+    assert mt.k_gemm_splitk(32000, 2048, 16384) == 1
+    assert mt.k_gemm_splitk(2560, 2048, 512) == 1
+    assert mt.k_gemm_wgrad_ws(32000, 2048) == 0
