@@ -183,7 +183,6 @@ struct mt_handle {
   std::vector<int> unit_pending;  // queued or running jobs per unit
   int64_t step_seq = 0;        // sequence number of the step being enqueued
   bool accum_nonfinite = false;  // a micro-step of the current accumulation had a non-finite loss
-  int64_t enqueued_seq = 0;    // last step whose units are all queued
   int64_t inject_sleep_ms = 0, inject_fail_at = 0, deadline_ms = 600000;
   int64_t worker_units_total = 0;
 
@@ -218,11 +217,12 @@ void worker_main(mt_handle* h) {
       std::unique_lock<std::mutex> lk(h->mu);
       h->cv.wait(lk, [&] { return h->stop || !h->jobs.empty(); });
       if (h->stop && h->jobs.empty()) return;
-      // Order: older steps first; within a fully enqueued step, lowest unit
-      // first (the order the next forward needs them); within the step whose
-      // backward is still being enqueued, arrival order. Jobs whose slab copy
-      // has landed go before jobs still waiting for theirs, so the worker
-      // never idles on one copy (the embedding's, the last of a step) while
+      // Order: older steps first, then the lowest unit among jobs whose slab
+      // copy has landed. The next step's forward needs units lowest first,
+      // so the units it needs last (the top layers, whose gradients land
+      // first) are left for the end of the pass and the forward starts
+      // while the worker is still busy; a unit that lands while others wait
+      // is taken ahead of them. The worker never idles on one copy while
       // other slabs are ready. At most K jobs are queued: the scan and its
       // non-blocking event queries are cheap.
       // When no copy has landed, the earliest issued one (the queue is in
@@ -230,9 +230,7 @@ void worker_main(mt_handle* h) {
       auto it = h->jobs.end();
       for (auto j = h->jobs.begin(); j != h->jobs.end(); ++j) {
         if (cudaEventQuery(h->ev_d2h_done[j->slab]) != cudaSuccess) continue;
-        if (it == h->jobs.end() || j->seq < it->seq ||
-            (j->seq == it->seq && j->seq <= h->enqueued_seq && j->unit < it->unit))
-          it = j;
+        if (it == h->jobs.end() || j->seq < it->seq || (j->seq == it->seq && j->unit < it->unit)) it = j;
       }
       if (it == h->jobs.end()) it = h->jobs.begin();
       job = *it;
@@ -383,27 +381,43 @@ struct Step {
     cur_slot = -1;
   }
 
-  // Take the next slab for a unit's weight gradients.
+  // Take a slab for a unit's weight gradients: any whose host staging the
+  // worker has consumed (the worker takes units out of arrival order, so
+  // slabs come free out of order too). Blocks, with the deadline, while all
+  // K are held: the back-pressure that keeps the backward at most K units
+  // ahead of the host.
   int slab_begin() {
-    const int k = h->next_slab;
-    h->next_slab = (h->next_slab + 1) % h->cfg.n_slabs;
+    const int n = h->cfg.n_slabs;
+    int k = -1;
+    const auto t0 = Clock::now();
+    {
+      std::unique_lock<std::mutex> lk(h->mu);
+      auto pick = [&] {
+        for (int i = 0; i < n; ++i) {
+          const int j = (h->next_slab + i) % n;
+          if (!h->staging_busy[j]) {
+            k = j;
+            return true;
+          }
+        }
+        return false;
+      };
+      const bool ok = h->cv.wait_for(lk, std::chrono::milliseconds(h->deadline_ms),
+                                     [&] { return h->worker_error || pick(); });
+      h->st.host_wait_s += seconds_since(t0);
+      if (h->worker_error) throw StepError{h->worker_error, h->worker_msg};
+      if (!ok) throw StepError{MT_ETIMEOUT, "timed out waiting for a free gradient slab"};
+      h->staging_busy[k] = 1;
+      h->next_slab = (k + 1) % n;
+    }
+    // the slab's previous copy has landed (the worker consumed it); the wait
+    // orders the device-side reuse after it
     CK(cudaStreamWaitEvent(h->s_comp, h->ev_d2h_done[k], 0));
     return k;
   }
   // Ship slab k of unit u to the host and queue it for the worker.
   void slab_end(int k, int u) {
     CK(cudaEventRecord(h->ev_slab_ready[k], h->s_comp));
-    // back-pressure: staging k must have been consumed by the worker
-    const auto t0 = Clock::now();
-    {
-      std::unique_lock<std::mutex> lk(h->mu);
-      const bool ok = h->cv.wait_for(lk, std::chrono::milliseconds(h->deadline_ms),
-                                     [&] { return !h->staging_busy[k] || h->worker_error; });
-      h->st.host_wait_s += seconds_since(t0);
-      if (h->worker_error) throw StepError{h->worker_error, h->worker_msg};
-      if (!ok) throw StepError{MT_ETIMEOUT, "timed out waiting for a free gradient slab"};
-      h->staging_busy[k] = 1;
-    }
     const size_t bytes = sizeof(uint16_t) * h->lay.unit_len[u];
     CK(cudaStreamWaitEvent(h->s_d2h, h->ev_slab_ready[k], 0));
     prof_copy_begin(h->s_d2h);
@@ -1057,11 +1071,6 @@ static int run_step(mt_handle* h, const int32_t* tokens, const int32_t* labels, 
       h->worker_msg.clear();
     }
     st.run();
-    {
-      std::lock_guard<std::mutex> lk(h->mu);
-      h->enqueued_seq = h->step_seq;  // every unit of the step is queued
-    }
-    h->cv.notify_all();
     if (!h->cfg.overlap_adam) {
       // wait for the worker to finish every unit of this step
       std::unique_lock<std::mutex> lk(h->mu);
@@ -1101,7 +1110,6 @@ static int run_step(mt_handle* h, const int32_t* tokens, const int32_t* labels, 
     cudaStreamSynchronize(h->s_d2h);
     std::unique_lock<std::mutex> lk(h->mu);
     h->jobs.clear();
-    h->enqueued_seq = h->step_seq;
     const bool idle = h->cv.wait_for(lk, std::chrono::milliseconds(std::min<int64_t>(h->deadline_ms, 60000)),
                                      [&] { return h->in_flight == 0; });
     if (e.code == MT_ETIMEOUT || e.code == MT_EDEVICE || e.code == MT_ECUDA || !idle) h->broken = 1;

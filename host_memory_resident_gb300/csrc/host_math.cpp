@@ -10,6 +10,7 @@
 // master gradient by a CPU worker (lqnn.cn article section 三.3).
 #include <omp.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstring>
 
@@ -117,10 +118,11 @@ void emit_bf16(const float* src, uint16_t* dst, int64_t n, int threads) {
 // Per element: gradient in (bf16 slab or fp32, optionally added to the
 // running sum in grad_out and scaled), gradient out, m, v, w updated, bf16
 // copy of w out. The variants are compile-time so the loop bodies have no
-// control flow. Each thread walks its contiguous range in chunks; when the
-// gradient is stored, a chunk is done in two sweeps: the gradient sweep
-// writes grad_out, then the optimizer sweep reads it back while it is still
-// in the core's cache. Host memory sees the same bytes as one fused sweep,
+// control flow. Threads take chunks from a shared counter, so a thread that
+// loses its core for a while (the host also runs the step's launches and the
+// copy engine's driver work) holds up nothing. When the gradient is stored,
+// a chunk is done in two sweeps: the gradient sweep writes grad_out, then
+// the optimizer sweep reads it back while it is still in the core's cache. Host memory sees the same bytes as one fused sweep,
 // but no sweep interleaves six streams, which on the Grace host makes the
 // pair about a quarter faster than the fused loop (measured, 16 cores).
 constexpr int64_t kAdamChunk = 65536;
@@ -142,12 +144,13 @@ static void adam_loop(const AdamArgs& a, int threads) {
   const uint16_t* __restrict__ slab = a.slab;
   uint16_t* __restrict__ store = a.store;
   const int64_t n = a.n;
+  std::atomic<int64_t> next{0};
 #pragma omp parallel num_threads(threads)
   {
-    const int nt = omp_get_num_threads(), tid = omp_get_thread_num();
-    const int64_t r0 = n * tid / nt, r1 = n * (tid + 1) / nt;
-    for (int64_t c0 = r0; c0 < r1; c0 += kAdamChunk) {
-      const int64_t c1e = c0 + kAdamChunk < r1 ? c0 + kAdamChunk : r1;
+    for (;;) {
+      const int64_t c0 = next.fetch_add(kAdamChunk, std::memory_order_relaxed);
+      if (c0 >= n) break;
+      const int64_t c1e = c0 + kAdamChunk < n ? c0 + kAdamChunk : n;
       if (kGradOut) {
         for (int64_t i = c0; i < c1e; ++i) {
           float g = kSlab ? bf16_to_f32(slab[i]) : gin[i];
