@@ -13,6 +13,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstring>
+#include <vector>
 
 #include "host_math.h"
 
@@ -120,12 +121,27 @@ void emit_bf16(const float* src, uint16_t* dst, int64_t n, int threads) {
 // copy of w out. The variants are compile-time so the loop bodies have no
 // control flow. Threads take chunks from a shared counter, so a thread that
 // loses its core for a while (the host also runs the step's launches and the
-// copy engine's driver work) holds up nothing. When the gradient is stored,
-// a chunk is done in two sweeps: the gradient sweep writes grad_out, then
-// the optimizer sweep reads it back while it is still in the core's cache. Host memory sees the same bytes as one fused sweep,
-// but no sweep interleaves six streams, which on the Grace host makes the
-// pair about a quarter faster than the fused loop (measured, 16 cores).
+// copy engine's driver work) holds up nothing.
+//
+// A chunk is done in up to three sweeps that each touch few host-memory
+// streams: the gradient sweep (slab in, grad_out out), the moment sweep (m,
+// v in and out; the gradient and the per-element step go through the core's
+// cache) and the weight sweep (w in and out, the bf16 copy out). Host memory
+// sees the same bytes as one fused sweep, but on the Grace host fewer
+// interleaved streams per sweep run faster: measured on 16 cores, 2^28
+// elements, 14 threads, the three sweeps reach 238 GB/s against 224 GB/s for
+// gradient + fused optimizer sweeps and about 150 GB/s for one fused sweep;
+// without the gradient array, 272 GB/s against 230 GB/s fused. The
+// arithmetic is that of the fused form, operation for operation.
 constexpr int64_t kAdamChunk = 65536;
+
+// Per-thread scratch of kAdamChunk floats for the per-element step (the
+// worker's OpenMP threads persist, so each allocates it once).
+static float* chunk_scratch() {
+  thread_local std::vector<float> buf;
+  if (buf.size() < (size_t)kAdamChunk) buf.resize(kAdamChunk);
+  return buf.data();
+}
 
 template <bool kSlab, bool kGradOut, bool kStore, bool kAcc>
 static void adam_loop(const AdamArgs& a, int threads) {
@@ -147,25 +163,31 @@ static void adam_loop(const AdamArgs& a, int threads) {
   std::atomic<int64_t> next{0};
 #pragma omp parallel num_threads(threads)
   {
+    float* __restrict__ step = chunk_scratch();
     for (;;) {
       const int64_t c0 = next.fetch_add(kAdamChunk, std::memory_order_relaxed);
       if (c0 >= n) break;
-      const int64_t c1e = c0 + kAdamChunk < n ? c0 + kAdamChunk : n;
+      const int64_t len = c0 + kAdamChunk < n ? kAdamChunk : n - c0;
       if (kGradOut) {
-        for (int64_t i = c0; i < c1e; ++i) {
+        for (int64_t i = c0; i < c0 + len; ++i) {
           float g = kSlab ? bf16_to_f32(slab[i]) : gin[i];
           if (kAcc) g = (gout[i] + g) * gs;
           gout[i] = g;
         }
       }
-      for (int64_t i = c0; i < c1e; ++i) {
+      for (int64_t k = 0; k < len; ++k) {
+        const int64_t i = c0 + k;
         const float g = kGradOut ? gout[i] : (kSlab ? bf16_to_f32(slab[i]) : gin[i]);
         const float mi = b1 * m[i] + c1 * g;
         const float vi = b2 * v[i] + c2 * g * g;
         m[i] = mi;
         v[i] = vi;
-        // m_hat / (sqrt(v_hat) + eps) with m_hat = m / bc1, v_hat = v / bc2
-        const float wi = w[i] - lr * (mi * inv_bc1) / (std::sqrt(vi) * inv_sqrt_bc2 + eps);
+        // lr * m_hat / (sqrt(v_hat) + eps) with m_hat = m / bc1, v_hat = v / bc2
+        step[k] = lr * (mi * inv_bc1) / (std::sqrt(vi) * inv_sqrt_bc2 + eps);
+      }
+      for (int64_t k = 0; k < len; ++k) {
+        const int64_t i = c0 + k;
+        const float wi = w[i] - step[k];
         w[i] = wi;
         if (kStore) store[i] = rne_bits(wi);
       }
