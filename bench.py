@@ -542,6 +542,18 @@ def run_attn_kernel(args):
     return 0
 
 
+def host_mem_available():
+    """MemAvailable of /proc/meminfo in bytes (None where it is not readable)."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        return None
+    return None
+
+
 def run_ours(args, shape, world, rank, local, pg):
     import torch
     import host_memory_resident_gb300 as mt
@@ -550,6 +562,17 @@ def run_ours(args, shape, world, rank, local, pg):
     cfg = mt.make_config(shape, device=local, host_threads=args.host_threads, overlap_adam=args.overlap,
                          unfused_epilogues=args.unfused, keep_attention=args.keep_attention)
     descs, n_total = mt.layout(cfg)
+    # refuse, before allocating, a workload whose host state and pinned
+    # buffers do not fit the host's available memory (14B needs ~266 GB)
+    plan = mt.plan(cfg)
+    need = plan["host_state_bytes"] * (16 if args.keep_grads else 12) // 16 + plan["pinned_bytes"]
+    avail = host_mem_available()
+    if avail is not None and need > 0.9 * avail:
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "config": {"workload": shape.name}, "value": None,
+                              "error": f"host memory: the workload needs {need / 1e9:.1f} GB of host state and "
+                                       f"pinned buffers, {avail / 1e9:.1f} GB available"}), flush=True)
+        return 3
     segs = [(t["offset"], t["rows"] * t["cols"], "normal" if t["kind"] == 0 else "ones") for t in descs]
     master = synth.init_master(n_total, segs, seed=0)
     B, s = shape.batch, shape.seq
