@@ -7,13 +7,13 @@
 //         of the group and every 64-query sub-tile at or after the diagonal:
 //           S^T  = K Q^T,  dP^T = V dO^T                       (TMEM)
 //           P^T  = exp(S^T * scale - lse[q]),  dS^T = P^T (dP^T - delta[q])
-//                                                              (bf16, smem)
+//                                                              (bf16, TMEM)
 //           dV  += P^T dO,  dK += dS^T Q   with dO and Q read MN-major
 //         then dK *= scale. Two element-wise groups take alternate
 //         sub-tiles, each with its own TMEM and shared-memory buffers.
 //  dQ:    one CTA per (128-query tile, head, batch), two threads per query
 //         row. For every 128-key tile up to the diagonal: S = Q K^T,
-//         dP = dO V^T (TMEM); dS (bf16, smem); dQ += dS K with K read
+//         dP = dO V^T (TMEM); dS (bf16, TMEM); dQ += dS K with K read
 //         MN-major; then dQ *= scale.
 // delta = rowsum(dO * O) comes from the pre-pass in attention.cu. This is the
 // backward of the stateless layer template's attention (travelaiplan blog,
@@ -38,17 +38,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ uint8_t* align1024b(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
-
-// Store one 64-column half-row of a 128 x 128 bf16 K-major operand tile
-// (128-byte swizzle); `pk` holds 32 packed bf16 pairs.
-__device__ __forceinline__ void store_half_row(uint8_t* tile, int half, int row, const uint32_t (&pk)[32]) {
-  uint8_t* base = tile + half * kBox + row * 128;
-  const uint32_t rsw = (uint32_t)(row & 7);
-#pragma unroll
-  for (int c = 0; c < 8; ++c)
-    *reinterpret_cast<uint4*>(base + (((uint32_t)c ^ rsw) * 16)) =
-        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
 }
 
 // Write `ncols` fp32 TMEM columns of this thread's lane as bf16 (times scale).
@@ -77,28 +66,32 @@ __device__ __forceinline__ void tmem_row_to_bf16(uint32_t taddr, int ncols, floa
 // heads and, per head, the 64-query sub-tiles at or after the diagonal.
 // Sub-tile `it` belongs to element-wise group it % 2 (warps 2-5 or 6-9, one
 // thread per key row), whose S^T and dP^T live in that group's 64-column TMEM
-// buffers and whose P^T and dS^T go to that group's shared-memory tiles. The
-// MMA warp issues dV/dK of sub-tile `it` as soon as its group has stored P^T
-// and dS^T, then S^T/dP^T of sub-tile it + 2 into the buffers just freed, so
-// one group's exponentials overlap the other group's products. Q and dO
-// sub-tiles stream through a 3-stage TMA ring. Each group stages its
-// sub-tile's 64 (lse, delta) pairs in shared memory; threads read two query
-// columns per 16-byte broadcast load.
+// buffers. The group writes P^T and dS^T back, packed bf16, into the first
+// 32 columns of those same buffers, where the dV and dK products read them
+// as their TMEM A operand. The MMA warp issues dV/dK of sub-tile `it` as soon
+// as its group has stored P^T and dS^T, then S^T/dP^T of sub-tile it + 2
+// into the same buffers (the products run in issue order, so dV/dK read
+// them first), so one group's exponentials overlap the other group's
+// products. With no P^T / dS^T tiles in shared memory, Q and dO sub-tiles
+// stream through a deep TMA ring (5 stages at hd 128, 8 at hd 64) whose
+// loads are issued several sub-tiles ahead of their products. Each group
+// stages its sub-tile's 64 (lse, delta) pairs in shared memory; threads read
+// two query columns per 16-byte broadcast load.
 template <int HD>
 struct KvTc2 {
   static constexpr int kBoxes = HD / 64;
   static constexpr uint32_t kBox64 = 64 * 128;           // 64 columns x 64 rows of bf16
   static constexpr uint32_t kKV = kBoxes * kBox;         // K or V tile, 128 keys
   static constexpr uint32_t kQ = kBoxes * kBox64;        // Q or dO sub-tile, 64 queries
-  static constexpr int kStages = 3;
+  static constexpr int kStages = HD == 64 ? 8 : 5;
   static constexpr uint32_t kKOff = 0;
   static constexpr uint32_t kVOff = kKV;
   static constexpr uint32_t kStOff = 2 * kKV;            // [stage] Q then dO
-  static constexpr uint32_t kPOff = kStOff + kStages * 2 * kQ;  // [group] P^T then dS^T, 128 keys x 64 queries
-  static constexpr uint32_t kBarOff = kPOff + 2 * 2 * kBox;
+  static constexpr uint32_t kBarOff = kStOff + kStages * 2 * kQ;
   static constexpr uint32_t kVecOff = kBarOff + 256;     // [group][64] (lse * log2e, delta)
   static constexpr size_t kSmem = 1024 + kVecOff + 2 * 64 * 8;
   static_assert(kSmem <= 232448, "shared memory per block");
+  static_assert(2 * kStages + 16 <= 256 / 8, "barrier area");
 };
 
 template <int HD>
@@ -111,15 +104,14 @@ __global__ void __launch_bounds__(kThr, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024b(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
-  uint64_t* kv_full = bars;           // K and V tiles
-  uint64_t* ld_full = bars + 1;       // [3] Q + dO stage
-  uint64_t* ld_empty = bars + 4;      // [3]
-  uint64_t* s_full = bars + 7;        // [2] per group: S^T, dP^T in TMEM
-  uint64_t* s_empty = bars + 9;       // [2] per group: copied out of TMEM
-  uint64_t* p_full = bars + 11;       // [2] per group: P^T, dS^T stored
-  uint64_t* p_empty = bars + 13;      // [2] per group: dV, dK products done with them
-  uint64_t* done = bars + 15;         // all dV, dK products done (completes once)
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 16);
+  uint64_t* kv_full = bars;                      // K and V tiles
+  uint64_t* ld_full = bars + 1;                  // [kStages] Q + dO stage
+  uint64_t* ld_empty = ld_full + C::kStages;     // [kStages]
+  uint64_t* s_full = ld_empty + C::kStages;      // [2] per group: S^T, dP^T in TMEM
+  uint64_t* s_empty = s_full + 2;                // [2] per group: copied out of TMEM
+  uint64_t* p_full = s_empty + 2;                // [2] per group: P^T, dS^T stored in TMEM
+  uint64_t* done = p_full + 2;                   // all dV, dK products done (completes once)
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
 
   const int n64 = (s + 63) / 64;
   const int kt = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -143,7 +135,6 @@ __global__ void __launch_bounds__(kThr, 1)
       mbar_init(&s_full[i], 1);
       mbar_init(&s_empty[i], 4);  // one arrival per element-wise warp
       mbar_init(&p_full[i], 4);
-      mbar_init(&p_empty[i], 1);
     }
     mbar_init(done, 1);
     fence_barrier_init();
@@ -215,22 +206,19 @@ __global__ void __launch_bounds__(kThr, 1)
         if (!(ok = mbar_wait(&p_full[G], li & 1, err))) break;
         tc_fence_after();
         const uint32_t sQ = smem_u32(sm + C::kStOff + st * 2 * C::kQ), sO = sQ + C::kQ;
-        const uint32_t sP = smem_u32(sm + C::kPOff + G * 2 * kBox), sDS = sP + kBox;
+        // A operands from TMEM: 16 queries of P^T (dS^T) are 8 packed columns
 #pragma unroll
         for (int kk = 0; kk < 64 / 16; ++kk) {
           const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-          tc_mma_bf16(tdV, smem_desc_kmajor_sw128(sP + kk * 32), smem_desc_mnmajor_sw128(sO + kk * 2048, C::kBox64),
-                      id_g, acc);
-          tc_mma_bf16(tdK, smem_desc_kmajor_sw128(sDS + kk * 32),
-                      smem_desc_mnmajor_sw128(sQ + kk * 2048, C::kBox64), id_g, acc);
+          tc_mma_bf16_ta(tdV, tS[G] + kk * 8, smem_desc_mnmajor_sw128(sO + kk * 2048, C::kBox64), id_g, acc);
+          tc_mma_bf16_ta(tdK, tdP[G] + kk * 8, smem_desc_mnmajor_sw128(sQ + kk * 2048, C::kBox64), id_g, acc);
         }
-        tc_commit(&p_empty[G]);
         tc_commit(&ld_empty[st]);
         if (it + 2 < total) ok = issue_s(it + 2);
       }
       // The accumulators are final once every product above has completed.
-      // The readers wait on this single-use barrier: waiting on a group's
-      // p_empty for its last completion could match an earlier phase of the
+      // The readers wait on this single-use barrier: waiting on a per-group
+      // barrier for its last completion could match an earlier phase of the
       // same parity that the other group never observed.
       if (ok) tc_commit(done);
     }
@@ -240,11 +228,8 @@ __global__ void __launch_bounds__(kThr, 1)
     const int key = k0 + row;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const float sc = rsqrtf((float)HD) * kLog2e;
-    uint8_t* sP = sm + C::kPOff + G * 2 * kBox;
-    uint8_t* sDS = sP + kBox;
     float2* vec = reinterpret_cast<float2*>(sm + C::kVecOff) + G * 64;
     const int tg = threadIdx.x - 64 - 128 * G;  // 0..127 within the group
-    const uint32_t rsw = (uint32_t)(row & 7);
     auto group_sync = [&]() { asm volatile("bar.sync %0, 128;" ::"r"(1 + G) : "memory"); };
     // a wait's outcome, the same for the whole warp (tcgen05.ld is warp-wide)
     auto wait_all = [&](uint64_t* bar, uint32_t parity) { return mbar_wait_warp(bar, parity, err); };
@@ -294,20 +279,19 @@ __global__ void __launch_bounds__(kThr, 1)
         rs[i >> 4][i & 15] = pack_bf16x2(pv[0], pv[1]);
         rp[i >> 4][i & 15] = pack_bf16x2(dv[0], dv[1]);
       }
-      // this group's P^T / dS^T tiles were last read by dV/dK of sub-tile it - 2
-      if (li > 0 && !wait_all(&p_empty[G], (li - 1) & 1)) { ok = false; continue; }
+      // P^T and dS^T into the first 32 columns of the row's S^T and dP^T
+      // lanes. The products that last read them (dV/dK of sub-tile it - 2)
+      // completed before S^T of this sub-tile did, which s_full reported.
+      {
+        uint32_t pw[32];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int w0 = 4 * c;
-        const uint32_t off = row * 128 + (((uint32_t)c ^ rsw) * 16);
-        *reinterpret_cast<uint4*>(sP + off) = make_uint4(rs[w0 >> 4][w0 & 15], rs[(w0 + 1) >> 4][(w0 + 1) & 15],
-                                                          rs[(w0 + 2) >> 4][(w0 + 2) & 15],
-                                                          rs[(w0 + 3) >> 4][(w0 + 3) & 15]);
-        *reinterpret_cast<uint4*>(sDS + off) = make_uint4(rp[w0 >> 4][w0 & 15], rp[(w0 + 1) >> 4][(w0 + 1) & 15],
-                                                           rp[(w0 + 2) >> 4][(w0 + 2) & 15],
-                                                           rp[(w0 + 3) >> 4][(w0 + 3) & 15]);
+        for (int w = 0; w < 32; ++w) pw[w] = rs[w >> 4][w & 15];
+        tmem_st_32x32b_x32(tS[G] + lane_off, pw);
+#pragma unroll
+        for (int w = 0; w < 32; ++w) pw[w] = rp[w >> 4][w & 15];
+        tmem_st_32x32b_x32(tdP[G] + lane_off, pw);
       }
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       mbar_arrive_warp(&p_full[G]);
     }
@@ -331,16 +315,27 @@ __global__ void __launch_bounds__(kThr, 1)
 }
 
 // ---------------------------------------------------------------------- dQ
+// One CTA per (128-query tile, head, batch), two threads per query row (one
+// per 64-key half). Per 128-key tile j: S = Q K^T and dP = dO V^T into TMEM;
+// the element-wise warps write dS (packed bf16) into one of two 64-column
+// TMEM buffers, where dQ += dS K reads it as its A operand. K and V stream
+// through separate TMA rings: V is free as soon as dP has run, K once dQ
+// has, so the loads of tile j + 1 are issued while tile j - 1 is still being
+// multiplied instead of after it.
 template <int HD>
 struct QTc {
   static constexpr int kBoxes = HD / 64;
   static constexpr uint32_t kTile = kBoxes * kBox;
+  static constexpr int kKS = HD == 64 ? 4 : 3;             // K ring stages
+  static constexpr int kVS = HD == 64 ? 4 : 2;             // V ring stages
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kOOff = kTile;                 // dO
-  static constexpr uint32_t kKVOff = 2 * kTile;            // [2] K then V
-  static constexpr uint32_t kDSOff = kKVOff + 2 * 2 * kTile;
-  static constexpr uint32_t kBarOff = kDSOff + 2 * kBox;
+  static constexpr uint32_t kKOff = 2 * kTile;             // [kKS]
+  static constexpr uint32_t kVOff = kKOff + kKS * kTile;   // [kVS]
+  static constexpr uint32_t kBarOff = kVOff + kVS * kTile;
   static constexpr size_t kSmem = 1024 + kBarOff + 256;
+  static_assert(kSmem <= 232448, "shared memory per block");
+  static_assert(2 * (kKS + kVS) + 6 <= 256 / 8, "barrier area");
 };
 
 template <int HD>
@@ -353,13 +348,15 @@ __global__ void __launch_bounds__(kThr, 1)
   uint8_t* sm = align1024b(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;   // [2]
-  uint64_t* kv_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;
-  uint64_t* p_full = bars + 6;
-  uint64_t* p_empty = bars + 7;
-  uint64_t* s_empty = bars + 8;   // S and dP copied out of TMEM
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 9);
+  uint64_t* k_full = bars + 1;           // [kKS]
+  uint64_t* k_empty = k_full + C::kKS;   // [kKS]
+  uint64_t* v_full = k_empty + C::kKS;   // [kVS]
+  uint64_t* v_empty = v_full + C::kVS;   // [kVS]
+  uint64_t* s_full = v_empty + C::kVS;   // S and dP in TMEM
+  uint64_t* s_empty = s_full + 1;        // S and dP copied out of TMEM
+  uint64_t* p_full = s_full + 2;         // dS stored in TMEM
+  uint64_t* done = s_full + 3;           // every dQ product done (completes once)
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(s_full + 4);
 
   const int nt = (s + kT - 1) / kT;
   const int qt = nt - 1 - blockIdx.x;  // heaviest first
@@ -374,14 +371,18 @@ __global__ void __launch_bounds__(kThr, 1)
     tma_prefetch_desc(&tqkv);
     tma_prefetch_desc(&tdo);
     mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+    for (int i = 0; i < C::kKS; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < C::kVS; ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_full, 8);  // one arrival per element-wise warp
-    mbar_init(p_empty, 1);
-    mbar_init(s_empty, 8);
+    mbar_init(s_empty, 8);  // one arrival per element-wise warp
+    mbar_init(p_full, 8);
+    mbar_init(done, 1);
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(tmem_holder, 512);
@@ -390,6 +391,7 @@ __global__ void __launch_bounds__(kThr, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256;
+  const uint32_t tDS[2] = {tmem + 384, tmem + 448};  // dS of even / odd key tiles, 64 packed columns
 
   if (warp == 0) {
     if (lane == 0) {
@@ -398,14 +400,31 @@ __global__ void __launch_bounds__(kThr, 1)
         tma_load_3d(sm + C::kQOff + bx * kBox, &tqkv, h * HD + bx * 64, q0, b, q_full);
         tma_load_3d(sm + C::kOOff + bx * kBox, &tdo, h * HD + bx * 64, q0, b, q_full);
       }
+      int nk = 0, nv = 0;  // K and V tiles whose loads were issued
       for (int j = 0; j < n_kv; ++j) {
-        const int st = j & 1;
-        if (!mbar_wait(&kv_empty[st], ((j >> 1) & 1) ^ 1, err)) break;
-        uint8_t* ks = sm + C::kKVOff + st * 2 * C::kTile;
-        mbar_arrive_expect_tx(&kv_full[st], 2 * C::kTile);
-        for (int bx = 0; bx < C::kBoxes; ++bx) {
-          tma_load_3d(ks + bx * kBox, &tqkv, kcol + bx * 64, j * kT, b, &kv_full[st]);
-          tma_load_3d(ks + C::kTile + bx * kBox, &tqkv, vcol + bx * 64, j * kT, b, &kv_full[st]);
+        const int ks = j % C::kKS, vs = j % C::kVS;
+        if (!mbar_wait(&k_empty[ks], ((j / C::kKS) & 1) ^ 1, err)) break;
+        mbar_arrive_expect_tx(&k_full[ks], C::kTile);
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+          tma_load_3d(sm + C::kKOff + ks * C::kTile + bx * kBox, &tqkv, kcol + bx * 64, j * kT, b, &k_full[ks]);
+        ++nk;
+        if (!mbar_wait(&v_empty[vs], ((j / C::kVS) & 1) ^ 1, err)) break;
+        mbar_arrive_expect_tx(&v_full[vs], C::kTile);
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+          tma_load_3d(sm + C::kVOff + vs * C::kTile + bx * kBox, &tqkv, vcol + bx * 64, j * kT, b, &v_full[vs]);
+        ++nv;
+      }
+      if (nk < n_kv || nv < n_kv) {
+        // a wait gave up: wait (bounded) for this CTA's copies still in
+        // flight before it exits
+        mbar_wait(q_full, 0, err);
+        for (int i = 0; i < C::kKS && i < nk; ++i) {
+          const int last = nk - 1 - i;
+          mbar_wait(&k_full[last % C::kKS], (last / C::kKS) & 1, err);
+        }
+        for (int i = 0; i < C::kVS && i < nv; ++i) {
+          const int last = nv - 1 - i;
+          mbar_wait(&v_full[last % C::kVS], (last / C::kVS) & 1, err);
         }
       }
     }
@@ -414,16 +433,16 @@ __global__ void __launch_bounds__(kThr, 1)
       constexpr uint32_t id_s = idesc_bf16_f32(kT, kT, false, false);
       constexpr uint32_t id_q = idesc_bf16_f32(kT, HD, false, true);
       const uint32_t sQ = smem_u32(sm + C::kQOff), sO = smem_u32(sm + C::kOOff);
-      const uint32_t sDS = smem_u32(sm + C::kDSOff);
       bool ok = mbar_wait(q_full, 0, err);
       // S / dP of key tile j (its K and V loaded, the TMEM they overwrite
-      // copied out by the element-wise warps)
+      // copied out by the element-wise warps); V is released when dP is done
       auto issue_s = [&](int j) -> bool {
-        const int st = j & 1;
-        if (!mbar_wait(&kv_full[st], (j >> 1) & 1, err)) return false;
+        const int ks = j % C::kKS, vs = j % C::kVS;
+        if (!mbar_wait(&k_full[ks], (j / C::kKS) & 1, err)) return false;
+        if (!mbar_wait(&v_full[vs], (j / C::kVS) & 1, err)) return false;
         if (j > 0 && !mbar_wait(s_empty, (j - 1) & 1, err)) return false;
         tc_fence_after();
-        const uint32_t sK = smem_u32(sm + C::kKVOff + st * 2 * C::kTile), sV = sK + C::kTile;
+        const uint32_t sK = smem_u32(sm + C::kKOff + ks * C::kTile), sV = smem_u32(sm + C::kVOff + vs * C::kTile);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
@@ -431,6 +450,7 @@ __global__ void __launch_bounds__(kThr, 1)
           tc_mma_bf16(tdP, smem_desc_kmajor_sw128(sO + off), smem_desc_kmajor_sw128(sV + off), id_s, kk > 0);
         }
         tc_commit(s_full);
+        tc_commit(&v_empty[vs]);
         return true;
       };
       if (ok) ok = issue_s(0);
@@ -439,16 +459,15 @@ __global__ void __launch_bounds__(kThr, 1)
         if (j + 1 < n_kv && !(ok = issue_s(j + 1))) break;
         if (!(ok = mbar_wait(p_full, j & 1, err))) break;
         tc_fence_after();
-        const uint32_t sK = smem_u32(sm + C::kKVOff + (j & 1) * 2 * C::kTile);
+        const uint32_t sK = smem_u32(sm + C::kKOff + (j % C::kKS) * C::kTile);
+        // A operand from TMEM: 16 keys of dS are 8 packed columns
 #pragma unroll
-        for (int kk = 0; kk < kT / 16; ++kk) {
-          const uint32_t aoff = (kk >> 2) * kBox + (kk & 3) * 32;
-          tc_mma_bf16(tdQ, smem_desc_kmajor_sw128(sDS + aoff), smem_desc_mnmajor_sw128(sK + kk * 2048, kBox), id_q,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc_commit(p_empty);
-        tc_commit(&kv_empty[j & 1]);
+        for (int kk = 0; kk < kT / 16; ++kk)
+          tc_mma_bf16_ta(tdQ, tDS[j & 1] + kk * 8, smem_desc_mnmajor_sw128(sK + kk * 2048, kBox), id_q,
+                         (j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&k_empty[j % C::kKS]);
       }
+      if (ok) tc_commit(done);
     }
   } else {
     const int q = warp & 3, half = (warp - 2) >> 2;
@@ -490,13 +509,15 @@ __global__ void __launch_bounds__(kThr, 1)
         const float2 dv = fmul2(pp, fadd2(dp, ndl));
         dk[i] = pack_bf16x2(dv.x, dv.y);
       }
-      if (j > 0 && !mbar_wait_warp(p_empty, (j - 1) & 1, err)) { ok = false; break; }
-      store_half_row(sm + C::kDSOff, half, row, dk);
-      fence_proxy_async_smem();
+      // dS of this half's 64 keys into its 32 columns of buffer j % 2. The
+      // product that last read that buffer (dQ of tile j - 2) completed
+      // before S of tile j did, which s_full reported.
+      tmem_st_32x32b_x32(tDS[j & 1] + lane_off + half * 32, dk);
+      tmem_st_wait();
       tc_fence_before();
       mbar_arrive_warp(p_full);
     }
-    if (ok && mbar_wait_warp(p_empty, (n_kv - 1) & 1, err)) {
+    if (ok && mbar_wait_warp(done, 0, err)) {
       tc_fence_after();
       bf16* dqrow = dqkv + ((long long)b * s + qpos) * lddq + (long long)h * HD + half * (HD / 2);
       tmem_row_to_bf16(tdQ + lane_off + half * (HD / 2), HD / 2, rsqrtf((float)HD), dqrow, qpos < s);
