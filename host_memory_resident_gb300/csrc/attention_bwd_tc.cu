@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kThr, 1)
     attn_bwd_dkdv_tc2_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_constant__ CUtensorMap tq64,
                              const __grid_constant__ CUtensorMap tdo64, const float* __restrict__ lse,
                              const float* __restrict__ delta, bf16* __restrict__ dqkv, long long lddq, int s, int H,
-                             int Hkv, int* err) {
+                             int Hkv, int hc, int* err) {
   using C = KvTc2<HD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024b(smem_raw);
@@ -114,7 +114,10 @@ __global__ void __launch_bounds__(kThr, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
 
   const int n64 = (s + 63) / 64;
-  const int kt = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int nkt = (s + kT - 1) / kT;
+  int hb, kt;  // (batch, KV head) pair and key tile; kt = 0 is the longest
+  chunked_tile_order(blockIdx.x, (int)gridDim.x / nkt, nkt, hc, hb, kt);
+  const int g = hb % Hkv, b = hb / Hkv;
   const int grp = H / Hkv;
   const int k0 = kt * kT;
   const int per_head = n64 - 2 * kt;  // 64-query sub-tiles from the diagonal on
@@ -234,22 +237,29 @@ __global__ void __launch_bounds__(kThr, 1)
     // a wait's outcome, the same for the whole warp (tcgen05.ld is warp-wide)
     auto wait_all = [&](uint64_t* bar, uint32_t parity) { return mbar_wait_warp(bar, parity, err); };
     bool ok = true;
+    // (lse * log2e, delta) of query tg of sub-tile `i`; read one group
+    // iteration ahead so the loads' latency overlaps a sub-tile's work
+    auto load_vec = [&](int i) -> float2 {
+      const int hh = g * grp + i / per_head;
+      const int qq = (2 * kt + i % per_head) * 64 + tg;
+      const long long vi = ((long long)b * H + hh) * s + qq;
+      return qq < s ? make_float2(lse[vi] * kLog2e, delta[vi]) : make_float2(INFINITY, 0.f);
+    };
+    float2 vnext = make_float2(0.f, 0.f);
+    if (tg < 64 && G < total) vnext = load_vec(G);
     // every thread of the group runs every iteration's two group barriers,
     // also after a failed wait (it then skips the work), so none is left
     // waiting at a barrier
     for (int it = G; it < total; it += 2) {
       const int li = it >> 1;
-      const int h = g * grp + it / per_head;
       const int jj = it % per_head;
       const int q0 = (2 * kt + jj) * 64;
-      // (lse * log2e, delta) of the sub-tile's 64 queries; the group's reads
-      // of the previous sub-tile's pairs end before they are overwritten
+      // the sub-tile's 64 pairs into shared memory; the group's reads of the
+      // previous sub-tile's pairs end before they are overwritten
       group_sync();
-      if (tg < 64) {
-        const long long vi = ((long long)b * H + h) * s + q0 + tg;
-        vec[tg] = q0 + tg < s ? make_float2(lse[vi] * kLog2e, delta[vi]) : make_float2(INFINITY, 0.f);
-      }
+      if (tg < 64) vec[tg] = vnext;
       group_sync();
+      if (tg < 64 && it + 2 < total) vnext = load_vec(it + 2);
       if (!ok) continue;
       if (!wait_all(&s_full[G], li & 1)) { ok = false; continue; }
       tc_fence_after();
@@ -342,7 +352,7 @@ template <int HD>
 __global__ void __launch_bounds__(kThr, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tqkv, const __grid_constant__ CUtensorMap tdo,
                           const float* __restrict__ lse, const float* __restrict__ delta, bf16* __restrict__ dqkv,
-                          long long lddq, int s, int H, int Hkv, int* err) {
+                          long long lddq, int s, int H, int Hkv, int hc, int* err) {
   using C = QTc<HD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024b(smem_raw);
@@ -359,8 +369,10 @@ __global__ void __launch_bounds__(kThr, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(s_full + 4);
 
   const int nt = (s + kT - 1) / kT;
-  const int qt = nt - 1 - blockIdx.x;  // heaviest first
-  const int h = blockIdx.y, b = blockIdx.z;
+  int hb, rank;  // (batch, head) pair; rank 0 is the longest query tile
+  chunked_tile_order(blockIdx.x, (int)gridDim.x / nt, nt, hc, hb, rank);
+  const int qt = nt - 1 - rank;
+  const int h = hb % H, b = hb / H;
   const int g = h / (H / Hkv);
   const int q0 = qt * kT;
   const int n_kv = qt + 1;
@@ -577,18 +589,25 @@ int attn_bwd_tc(const void* qkv, long long ld, const void* dout, long long lddo,
       !make_map3(&td64, dout, lddo, s, B, 64))
     return MT_EINVAL;
   const int nt = (s + kT - 1) / kT;
+  // one CTA per (tile, head, batch) on a 1-D grid, in the chunked order
+  if ((long long)nt * H * B > 0x7fffffffLL) return MT_EINVAL;
+  const int grp = H / Hkv;
+  // dK/dV of a KV head streams its group's Q and dO; dQ of a query head
+  // streams its KV head's K and V, shared by the group's query heads
+  const int hc1 = attn_head_chunk((long long)grp * s * hd * 4, B * Hkv);
+  const int hc2 = attn_head_chunk((long long)s * hd * 4 / grp, B * H);
   int* err = device_error_word();
-  dim3 g1(nt, Hkv, B), g2(nt, H, B);
+  const unsigned g1 = (unsigned)(nt * Hkv * B), g2 = (unsigned)(nt * H * B);
   if (hd == 64) {
     attn_bwd_dkdv_tc2_kernel<64><<<g1, kThr, KvTc2<64>::kSmem, stream>>>(tq, tq64, td64, lse, delta, (bf16*)dqkv,
-                                                                         lddq, s, H, Hkv, err);
+                                                                         lddq, s, H, Hkv, hc1, err);
     attn_bwd_dq_tc_kernel<64><<<g2, kThr, QTc<64>::kSmem, stream>>>(tq, td, lse, delta, (bf16*)dqkv, lddq, s, H, Hkv,
-                                                                   err);
+                                                                   hc2, err);
   } else {
     attn_bwd_dkdv_tc2_kernel<128><<<g1, kThr, KvTc2<128>::kSmem, stream>>>(tq, tq64, td64, lse, delta, (bf16*)dqkv,
-                                                                           lddq, s, H, Hkv, err);
+                                                                           lddq, s, H, Hkv, hc1, err);
     attn_bwd_dq_tc_kernel<128><<<g2, kThr, QTc<128>::kSmem, stream>>>(tq, td, lse, delta, (bf16*)dqkv, lddq, s, H,
-                                                                     Hkv, err);
+                                                                     Hkv, hc2, err);
   }
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {

@@ -70,7 +70,7 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 template <int HD>
 __global__ void __launch_bounds__(kThr, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm, bf16* __restrict__ o, long long ldo,
-                       float* __restrict__ lse, int s, int H, int Hkv, int* err) {
+                       float* __restrict__ lse, int s, int H, int Hkv, int hc, int* err) {
   using C = TcCfg<HD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
@@ -88,8 +88,10 @@ __global__ void __launch_bounds__(kThr, 1)
 
   const int nqt = (s + kQ - 1) / kQ;
   const int npair = (nqt + 1) / 2;
-  const int pr = npair - 1 - blockIdx.x;  // heaviest pairs first
-  const int h = blockIdx.y, b = blockIdx.z;
+  int hb, rank;  // (batch, head) pair; rank 0 is the longest pair of query tiles
+  chunked_tile_order(blockIdx.x, (int)gridDim.x / npair, npair, hc, hb, rank);
+  const int pr = npair - 1 - rank;
+  const int h = hb % H, b = hb / H;
   const int g = h / (H / Hkv);
   const int qt0 = 2 * pr;
   const int ntile = (qt0 + 1 < nqt) ? 2 : 1;
@@ -399,12 +401,18 @@ int attn_fwd_tc(const void* qkv, long long ld, void* o, long long ldo, float* ls
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return MT_EINVAL;
-  dim3 grid(((s + kQ - 1) / kQ + 1) / 2, H, B);
+  const int npair = ((s + kQ - 1) / kQ + 1) / 2;
+  // one CTA per (pair of query tiles, head, batch) on a 1-D grid, in the
+  // chunked order; a query head streams its KV head's K and V, shared by
+  // the group's query heads
+  if ((long long)npair * H * B > 0x7fffffffLL) return MT_EINVAL;
+  const int hc = attn_head_chunk((long long)s * hd * 4 / (H / Hkv), B * H);
+  const unsigned grid = (unsigned)(npair * H * B);
   int* err = device_error_word();
   if (hd == 64)
-    attn_fwd_tc_kernel<64><<<grid, kThr, TcCfg<64>::kSmem, stream>>>(tm, (bf16*)o, ldo, lse, s, H, Hkv, err);
+    attn_fwd_tc_kernel<64><<<grid, kThr, TcCfg<64>::kSmem, stream>>>(tm, (bf16*)o, ldo, lse, s, H, Hkv, hc, err);
   else
-    attn_fwd_tc_kernel<128><<<grid, kThr, TcCfg<128>::kSmem, stream>>>(tm, (bf16*)o, ldo, lse, s, H, Hkv, err);
+    attn_fwd_tc_kernel<128><<<grid, kThr, TcCfg<128>::kSmem, stream>>>(tm, (bf16*)o, ldo, lse, s, H, Hkv, hc, err);
   return cudaGetLastError() == cudaSuccess ? MT_OK : MT_ECUDA;
 }
 

@@ -36,6 +36,21 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Launch order of attention tiles over a 1-D grid: the linear block index L
+// walks chunks of `hc` of the `nh` heads; within a chunk it takes tile rank
+// (0 = the longest tile) across the chunk's heads. The CTAs in flight then
+// share a few heads' streamed operands in L2 while the longest tiles of
+// each chunk start first.
+__device__ __forceinline__ void chunked_tile_order(int L, int nh, int ntiles, int hc, int& head, int& rank) {
+  const int per_chunk = hc * ntiles;
+  const int c = L / per_chunk;
+  const int r = L - c * per_chunk;
+  const int h0 = c * hc;
+  const int hn = min(hc, nh - h0);
+  rank = r / hn;
+  head = h0 + r % hn;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

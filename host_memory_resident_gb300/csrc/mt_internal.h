@@ -22,6 +22,17 @@ void set_last_error_message(const std::string& msg);
 int gemm_ex(const void* A, long long lda, int a_mn, const void* B, long long ldb, int b_mn, void* C, long long ldc,
             int c_f32, const void* R, long long ldr, int M, int N, int K, cudaStream_t stream);
 
+// Heads per chunk of the attention kernels' launch order: as many as keep
+// the streamed operands of the CTAs in flight (bytes_per_head each) within
+// about 48 MiB of the 129 MB L2; at least 1, at most nh.
+inline int attn_head_chunk(long long bytes_per_head, int nh) {
+  const long long budget = 48LL << 20;
+  long long hc = bytes_per_head > 0 ? budget / bytes_per_head : nh;
+  if (hc < 1) hc = 1;
+  if (hc > nh) hc = nh;
+  return (int)hc;
+}
+
 // Split-K factor the library uses for C[M, N] over K (1: no split; depends
 // on the shape only, so planning needs no GPU).
 int splitk_factor(int M, int N, int K);
