@@ -185,19 +185,21 @@ __global__ void __launch_bounds__(kThr, 1)
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(kT, 64, false, false);  // S^T, dP^T: M 128 keys, N 64 queries
       constexpr uint32_t id_g = idesc_bf16_f32(kT, HD, false, true);   // dV, dK: B (dO, Q) MN-major
-      const uint32_t sK = smem_u32(sm + C::kKOff), sV = smem_u32(sm + C::kVOff);
+      const uint64_t dK = smem_desc_kmajor_sw128(smem_u32(sm + C::kKOff));
+      const uint64_t dV = smem_desc_kmajor_sw128(smem_u32(sm + C::kVOff));
       bool ok = mbar_wait(kv_full, 0, err);
       auto issue_s = [&](int i) -> bool {
         const int G = i & 1, li = i >> 1, st = i % C::kStages;
         if (!mbar_wait(&ld_full[st], (i / C::kStages) & 1, err)) return false;
         if (li > 0 && !mbar_wait(&s_empty[G], (li - 1) & 1, err)) return false;
         tc_fence_after();
-        const uint32_t sQ = smem_u32(sm + C::kStOff + st * 2 * C::kQ), sO = sQ + C::kQ;
+        const uint64_t dQ = smem_desc_kmajor_sw128(smem_u32(sm + C::kStOff + st * 2 * C::kQ));
+        const uint64_t dO = desc_advance(dQ, C::kQ);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t ka = (kk >> 2) * kBox + (kk & 3) * 32, kb = (kk >> 2) * C::kBox64 + (kk & 3) * 32;
-          tc_mma_bf16(tS[G], smem_desc_kmajor_sw128(sK + ka), smem_desc_kmajor_sw128(sQ + kb), id_s, kk > 0);
-          tc_mma_bf16(tdP[G], smem_desc_kmajor_sw128(sV + ka), smem_desc_kmajor_sw128(sO + kb), id_s, kk > 0);
+          tc_mma_bf16(tS[G], desc_advance(dK, ka), desc_advance(dQ, kb), id_s, kk > 0);
+          tc_mma_bf16(tdP[G], desc_advance(dV, ka), desc_advance(dO, kb), id_s, kk > 0);
         }
         tc_commit(&s_full[G]);
         return true;
@@ -208,13 +210,14 @@ __global__ void __launch_bounds__(kThr, 1)
         const int G = it & 1, li = it >> 1, st = it % C::kStages;
         if (!(ok = mbar_wait(&p_full[G], li & 1, err))) break;
         tc_fence_after();
-        const uint32_t sQ = smem_u32(sm + C::kStOff + st * 2 * C::kQ), sO = sQ + C::kQ;
+        const uint32_t sQ = smem_u32(sm + C::kStOff + st * 2 * C::kQ);
+        const uint64_t mQ = smem_desc_mnmajor_sw128(sQ, C::kBox64), mO = desc_advance(mQ, C::kQ);
         // A operands from TMEM: 16 queries of P^T (dS^T) are 8 packed columns
 #pragma unroll
         for (int kk = 0; kk < 64 / 16; ++kk) {
           const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-          tc_mma_bf16_ta(tdV, tS[G] + kk * 8, smem_desc_mnmajor_sw128(sO + kk * 2048, C::kBox64), id_g, acc);
-          tc_mma_bf16_ta(tdK, tdP[G] + kk * 8, smem_desc_mnmajor_sw128(sQ + kk * 2048, C::kBox64), id_g, acc);
+          tc_mma_bf16_ta(tdV, tS[G] + kk * 8, desc_advance(mO, kk * 2048), id_g, acc);
+          tc_mma_bf16_ta(tdK, tdP[G] + kk * 8, desc_advance(mQ, kk * 2048), id_g, acc);
         }
         tc_commit(&ld_empty[st]);
         if (it + 2 < total) ok = issue_s(it + 2);
@@ -444,7 +447,8 @@ __global__ void __launch_bounds__(kThr, 1)
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(kT, kT, false, false);
       constexpr uint32_t id_q = idesc_bf16_f32(kT, HD, false, true);
-      const uint32_t sQ = smem_u32(sm + C::kQOff), sO = smem_u32(sm + C::kOOff);
+      const uint64_t dQ = smem_desc_kmajor_sw128(smem_u32(sm + C::kQOff));
+      const uint64_t dO = smem_desc_kmajor_sw128(smem_u32(sm + C::kOOff));
       bool ok = mbar_wait(q_full, 0, err);
       // S / dP of key tile j (its K and V loaded, the TMEM they overwrite
       // copied out by the element-wise warps); V is released when dP is done
@@ -454,12 +458,13 @@ __global__ void __launch_bounds__(kThr, 1)
         if (!mbar_wait(&v_full[vs], (j / C::kVS) & 1, err)) return false;
         if (j > 0 && !mbar_wait(s_empty, (j - 1) & 1, err)) return false;
         tc_fence_after();
-        const uint32_t sK = smem_u32(sm + C::kKOff + ks * C::kTile), sV = smem_u32(sm + C::kVOff + vs * C::kTile);
+        const uint64_t dK = smem_desc_kmajor_sw128(smem_u32(sm + C::kKOff + ks * C::kTile));
+        const uint64_t dV = smem_desc_kmajor_sw128(smem_u32(sm + C::kVOff + vs * C::kTile));
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-          tc_mma_bf16(tS, smem_desc_kmajor_sw128(sQ + off), smem_desc_kmajor_sw128(sK + off), id_s, kk > 0);
-          tc_mma_bf16(tdP, smem_desc_kmajor_sw128(sO + off), smem_desc_kmajor_sw128(sV + off), id_s, kk > 0);
+          tc_mma_bf16(tS, desc_advance(dQ, off), desc_advance(dK, off), id_s, kk > 0);
+          tc_mma_bf16(tdP, desc_advance(dO, off), desc_advance(dV, off), id_s, kk > 0);
         }
         tc_commit(s_full);
         tc_commit(&v_empty[vs]);
@@ -471,12 +476,11 @@ __global__ void __launch_bounds__(kThr, 1)
         if (j + 1 < n_kv && !(ok = issue_s(j + 1))) break;
         if (!(ok = mbar_wait(p_full, j & 1, err))) break;
         tc_fence_after();
-        const uint32_t sK = smem_u32(sm + C::kKOff + (j % C::kKS) * C::kTile);
+        const uint64_t mK = smem_desc_mnmajor_sw128(smem_u32(sm + C::kKOff + (j % C::kKS) * C::kTile), kBox);
         // A operand from TMEM: 16 keys of dS are 8 packed columns
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk)
-          tc_mma_bf16_ta(tdQ, tDS[j & 1] + kk * 8, smem_desc_mnmajor_sw128(sK + kk * 2048, kBox), id_q,
-                         (j > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_bf16_ta(tdQ, tDS[j & 1] + kk * 8, desc_advance(mK, kk * 2048), id_q, (j > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&k_empty[j % C::kKS]);
       }
       if (ok) tc_commit(done);

@@ -182,21 +182,22 @@ __global__ void __launch_bounds__(kThr, 1)
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kQ, HD, false, true);
       bool ok = mbar_wait(q_full, 0, err);
       // S_t(j) for both tiles that still need key tile j, then release K_j
+      const uint64_t dQ0 = smem_desc_kmajor_sw128(smem_u32(sm + C::kQOff));
+      const uint64_t dP0 = smem_desc_kmajor_sw128(smem_u32(sm + C::kPOff));
       auto issue_s = [&](int j) -> bool {
         const int st = j % C::kKS;
         if (!mbar_wait(&k_full[st], (j / C::kKS) & 1, err)) return false;
-        const uint32_t sK = smem_u32(sm + C::kKOff + st * C::kTile);
+        const uint64_t dK = smem_desc_kmajor_sw128(smem_u32(sm + C::kKOff + st * C::kTile));
         for (int t = 0; t < 2; ++t) {
           if (j >= nkv[t]) continue;
           // the group has copied S_t(j-1) out of TMEM
           if (j > 0 && !mbar_wait(&s_empty[t], (j - 1) & 1, err)) return false;
           tc_fence_after();
-          const uint32_t sQ = smem_u32(sm + C::kQOff + t * C::kTile);
+          const uint64_t dQ = desc_advance(dQ0, t * C::kTile);
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-            tc_mma_bf16(tS[t], smem_desc_kmajor_sw128(sQ + off), smem_desc_kmajor_sw128(sK + off), idesc_s,
-                        kk > 0 ? 1u : 0u);
+            tc_mma_bf16(tS[t], desc_advance(dQ, off), desc_advance(dK, off), idesc_s, kk > 0 ? 1u : 0u);
           }
           tc_commit(&s_full[t]);
         }
@@ -208,21 +209,20 @@ __global__ void __launch_bounds__(kThr, 1)
         if (j + 1 < n_kv && !(ok = issue_s(j + 1))) break;
         const int vs = j % C::kVS;
         if (!(ok = mbar_wait(&v_full[vs], (j / C::kVS) & 1, err))) break;
-        const uint32_t sV = smem_u32(sm + C::kVOff + vs * C::kTile);
+        const uint64_t mV = smem_desc_mnmajor_sw128(smem_u32(sm + C::kVOff + vs * C::kTile), kBox);
         for (int t = 0; t < 2 && ok; ++t) {
           if (j >= nkv[t]) continue;
           if (!(ok = mbar_wait(&p_full[t], j & 1, err))) break;
           tc_fence_after();
-          const uint32_t sP = smem_u32(sm + C::kPOff + t * C::kPBuf);
+          const uint64_t dP = desc_advance(dP0, t * C::kPBuf);
 #pragma unroll
           for (int kk = 0; kk < kKV / 16; ++kk) {
             const uint32_t aoff = (kk >> 2) * kBox + (kk & 3) * 32;
             if (kPT)
-              tc_mma_bf16_ta(tO[t], tP[t] + kk * 8, smem_desc_mnmajor_sw128(sV + kk * 2048, kBox), idesc_pv,
-                             (j > 0 || kk > 0) ? 1u : 0u);
+              tc_mma_bf16_ta(tO[t], tP[t] + kk * 8, desc_advance(mV, kk * 2048), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
             else
-              tc_mma_bf16(tO[t], smem_desc_kmajor_sw128(sP + aoff), smem_desc_mnmajor_sw128(sV + kk * 2048, kBox),
-                          idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+              tc_mma_bf16(tO[t], desc_advance(dP, aoff), desc_advance(mV, kk * 2048), idesc_pv,
+                          (j > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(&p_empty[t]);
         }

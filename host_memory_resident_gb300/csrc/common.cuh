@@ -262,6 +262,13 @@ __device__ __forceinline__ uint64_t smem_desc_mnmajor_sw128(uint32_t saddr, uint
   return d;
 }
 
+// The descriptor of the same operand `byte_off` bytes further on: only the
+// 14-bit start-address field (address / 16) changes, and shared-memory
+// addresses stay below 256 KiB, so the add never carries out of it. Built
+// once per tile and advanced per K step, it keeps the single MMA-issuing
+// thread's instruction count per product low.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t d, uint32_t byte_off) { return d + (uint64_t)(byte_off >> 4); }
+
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 D; a_mn / b_mn set
 // the operand's transpose bit (MN-major in shared memory).
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t m, uint32_t n, bool a_mn = false, bool b_mn = false) {
