@@ -147,7 +147,10 @@ __global__ void __launch_bounds__(kThr, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const uint32_t tS[2] = {tmem, tmem + 64}, tdP[2] = {tmem + 128, tmem + 192};
+  // per-group S^T and dP^T buffers, as arithmetic (an array indexed by the
+  // group would live in local memory)
+  auto tS = [&](int grp_) { return tmem + 64u * (uint32_t)grp_; };
+  auto tdP = [&](int grp_) { return tmem + 128u + 64u * (uint32_t)grp_; };
   const uint32_t tdV = tmem + 256, tdK = tmem + 256 + HD;
 
   if (warp == 0) {
@@ -198,8 +201,8 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t ka = (kk >> 2) * kBox + (kk & 3) * 32, kb = (kk >> 2) * C::kBox64 + (kk & 3) * 32;
-          tc_mma_bf16(tS[G], desc_advance(dK, ka), desc_advance(dQ, kb), id_s, kk > 0);
-          tc_mma_bf16(tdP[G], desc_advance(dV, ka), desc_advance(dO, kb), id_s, kk > 0);
+          tc_mma_bf16(tS(G), desc_advance(dK, ka), desc_advance(dQ, kb), id_s, kk > 0);
+          tc_mma_bf16(tdP(G), desc_advance(dV, ka), desc_advance(dO, kb), id_s, kk > 0);
         }
         tc_commit(&s_full[G]);
         return true;
@@ -216,8 +219,8 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
         for (int kk = 0; kk < 64 / 16; ++kk) {
           const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-          tc_mma_bf16_ta(tdV, tS[G] + kk * 8, desc_advance(mO, kk * 2048), id_g, acc);
-          tc_mma_bf16_ta(tdK, tdP[G] + kk * 8, desc_advance(mQ, kk * 2048), id_g, acc);
+          tc_mma_bf16_ta(tdV, tS(G) + kk * 8, desc_advance(mO, kk * 2048), id_g, acc);
+          tc_mma_bf16_ta(tdK, tdP(G) + kk * 8, desc_advance(mQ, kk * 2048), id_g, acc);
         }
         tc_commit(&ld_empty[st]);
         if (it + 2 < total) ok = issue_s(it + 2);
@@ -269,8 +272,8 @@ __global__ void __launch_bounds__(kThr, 1)
       uint32_t rs[2][32], rp[2][32];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        tmem_ld_32x32b_x32(tS[G] + lane_off + c * 32, rs[c]);
-        tmem_ld_32x32b_x32(tdP[G] + lane_off + c * 32, rp[c]);
+        tmem_ld_32x32b_x32(tS(G) + lane_off + c * 32, rs[c]);
+        tmem_ld_32x32b_x32(tdP(G) + lane_off + c * 32, rp[c]);
       }
       tmem_ld_wait();
       tc_fence_before();
@@ -299,10 +302,10 @@ __global__ void __launch_bounds__(kThr, 1)
         uint32_t pw[32];
 #pragma unroll
         for (int w = 0; w < 32; ++w) pw[w] = rs[w >> 4][w & 15];
-        tmem_st_32x32b_x32(tS[G] + lane_off, pw);
+        tmem_st_32x32b_x32(tS(G) + lane_off, pw);
 #pragma unroll
         for (int w = 0; w < 32; ++w) pw[w] = rp[w >> 4][w & 15];
-        tmem_st_32x32b_x32(tdP[G] + lane_off, pw);
+        tmem_st_32x32b_x32(tdP(G) + lane_off, pw);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -406,7 +409,8 @@ __global__ void __launch_bounds__(kThr, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256;
-  const uint32_t tDS[2] = {tmem + 384, tmem + 448};  // dS of even / odd key tiles, 64 packed columns
+  // dS of even / odd key tiles, 64 packed columns each
+  auto tDS = [&](int j_) { return tmem + 384u + 64u * (uint32_t)(j_ & 1); };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -480,7 +484,7 @@ __global__ void __launch_bounds__(kThr, 1)
         // A operand from TMEM: 16 keys of dS are 8 packed columns
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk)
-          tc_mma_bf16_ta(tdQ, tDS[j & 1] + kk * 8, desc_advance(mK, kk * 2048), id_q, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_bf16_ta(tdQ, tDS(j) + kk * 8, desc_advance(mK, kk * 2048), id_q, (j > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&k_empty[j % C::kKS]);
       }
       if (ok) tc_commit(done);
@@ -528,7 +532,7 @@ __global__ void __launch_bounds__(kThr, 1)
       // dS of this half's 64 keys into its 32 columns of buffer j % 2. The
       // product that last read that buffer (dQ of tile j - 2) completed
       // before S of tile j did, which s_full reported.
-      tmem_st_32x32b_x32(tDS[j & 1] + lane_off + half * 32, dk);
+      tmem_st_32x32b_x32(tDS(j) + lane_off + half * 32, dk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive_warp(p_full);

@@ -124,12 +124,14 @@ __global__ void __launch_bounds__(kThr, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const uint32_t tS[2] = {tmem, tmem + 128};
-  const uint32_t tO[2] = {tmem + 256, tmem + 256 + HD};
+  // per-tile TMEM buffers, as arithmetic (an array indexed by the tile
+  // would live in local memory)
+  auto tS = [&](int t_) { return tmem + 128u * (uint32_t)t_; };
+  auto tO = [&](int t_) { return tmem + 256u + (uint32_t)HD * (uint32_t)t_; };
   // hd 64 leaves TMEM columns 384-511 free: P of each tile goes there and the
   // P V product reads it as its A operand (no shared-memory round trip)
   constexpr bool kPT = HD == 64;
-  const uint32_t tP[2] = {tmem + 384, tmem + 448};
+  auto tP = [&](int t_) { return tmem + 384u + 64u * (uint32_t)t_; };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -197,7 +199,7 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-            tc_mma_bf16(tS[t], desc_advance(dQ, off), desc_advance(dK, off), idesc_s, kk > 0 ? 1u : 0u);
+            tc_mma_bf16(tS(t), desc_advance(dQ, off), desc_advance(dK, off), idesc_s, kk > 0 ? 1u : 0u);
           }
           tc_commit(&s_full[t]);
         }
@@ -219,9 +221,9 @@ __global__ void __launch_bounds__(kThr, 1)
           for (int kk = 0; kk < kKV / 16; ++kk) {
             const uint32_t aoff = (kk >> 2) * kBox + (kk & 3) * 32;
             if (kPT)
-              tc_mma_bf16_ta(tO[t], tP[t] + kk * 8, desc_advance(mV, kk * 2048), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+              tc_mma_bf16_ta(tO(t), tP(t) + kk * 8, desc_advance(mV, kk * 2048), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
             else
-              tc_mma_bf16(tO[t], desc_advance(dP, aoff), desc_advance(mV, kk * 2048), idesc_pv,
+              tc_mma_bf16(tO(t), desc_advance(dP, aoff), desc_advance(mV, kk * 2048), idesc_pv,
                           (j > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(&p_empty[t]);
@@ -247,7 +249,7 @@ __global__ void __launch_bounds__(kThr, 1)
       tc_fence_after();
       uint32_t r[4][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tS[t] + lane_off + c * 32, r[c]);
+      for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tS(t) + lane_off + c * 32, r[c]);
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive_warp(&s_empty[t]);
@@ -295,7 +297,7 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll 1
         for (int c = 0; c < HD / 32; ++c) {
           uint32_t ov[32];
-          const uint32_t ta = tO[t] + lane_off + c * 32;
+          const uint32_t ta = tO(t) + lane_off + c * 32;
           tmem_ld_32x32b_x32(ta, ov);
           tmem_ld_wait();
 #pragma unroll
@@ -316,7 +318,7 @@ __global__ void __launch_bounds__(kThr, 1)
           uint32_t pw[32];
 #pragma unroll
           for (int w = 0; w < 32; ++w) pw[w] = r[(32 * h2 + w) >> 4][(32 * h2 + w) & 15];
-          tmem_st_32x32b_x32(tP[t] + lane_off + h2 * 32, pw);
+          tmem_st_32x32b_x32(tP(t) + lane_off + h2 * 32, pw);
         }
         tmem_st_wait();
       } else {
@@ -342,7 +344,7 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll 1
       for (int c = 0; c < HD / 32; ++c) {
         uint32_t ov[32];
-        tmem_ld_32x32b_x32(tO[t] + lane_off + c * 32, ov);
+        tmem_ld_32x32b_x32(tO(t) + lane_off + c * 32, ov);
         tmem_ld_wait();
         if (qpos < s) {
 #pragma unroll
