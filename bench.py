@@ -384,6 +384,7 @@ def run_gemm_kernel(args):
     M, N, K = (int(x) for x in args.shape.split(","))
     torch.manual_seed(0)
     dev = "cuda"
+    mt.k_gemm_tile_policy(args.tile)
     A = torch.randn(M, K, device=dev).to(torch.bfloat16)
     epi = args.epilogue
     if epi in ("wgrad", "wgrad_nosplit"):
@@ -430,7 +431,7 @@ def run_gemm_kernel(args):
     if epi in ("wgrad", "wgrad_nosplit"):
         ref = A[:, :256].float().t() @ B.float()
         err = (Cm[:256].float() - ref).abs().max().item() / ref.abs().max().item()
-    print(json.dumps({"kernel": "gemm_abt" + (f"+{epi}" if epi else ""), "M": M, "N": N, "K": K, "ms": ms,
+    print(json.dumps({"kernel": "gemm_abt" + (f"+{epi}" if epi else ""), "M": M, "N": N, "K": K, "tile": args.tile, "ms": ms,
                       "splits": mt.k_gemm_splitk(M, N, K) if epi == "wgrad" else 1,
                       "tflops": 2.0 * M * N * K / ms / 1e9, "max_rel_err_rows0_255": err}), flush=True)
     return 0 if err < 2e-2 else 1
@@ -738,6 +739,8 @@ def main():
     ap.add_argument("--epilogue", default=None, choices=[None, "swiglu", "swiglu_bwd", "rope", "wgrad", "wgrad_nosplit"],
                     help="with --kernel gemm: a fused-epilogue form")
     ap.add_argument("--iters", type=int, default=20)
+    ap.add_argument("--tile", type=int, default=0, choices=[0, 1, 2],
+                    help="with --kernel gemm: tile shape of plain products (0 library's choice, 1 128x256, 2 256x256)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--host-threads", type=int, default=0)
     ap.add_argument("--timeline", default=None, help="write the profiled step's Chrome/Perfetto trace here")

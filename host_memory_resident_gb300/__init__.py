@@ -72,7 +72,7 @@ EXPORTS = [
     "mt_read_grads", "mt_sync", "mt_get_step", "mt_set_step", "mt_sync_store", "mt_get_stats",
     "mt_get_stream", "mt_profile_enable", "mt_profile_read", "mt_profile_timeline", "mt_destroy", "mt_last_error", "mt_debug_inject", "mt_debug_inject_global",
     "mt_host_adam", "mt_host_adam_slab", "mt_host_to_bf16",
-    "mt_k_gemm", "mt_k_gemm_ex", "mt_k_gemm_rope", "mt_k_gemm_swiglu_fwd", "mt_k_gemm_swiglu_bwd", "mt_k_gemm_wgrad", "mt_k_gemm_splitk", "mt_k_gemm_wgrad_ws", "mt_k_transpose", "mt_k_rmsnorm_fwd", "mt_k_rmsnorm_bwd", "mt_k_rmsnorm_bwd_parts",
+    "mt_k_gemm", "mt_k_gemm_ex", "mt_k_gemm_rope", "mt_k_gemm_swiglu_fwd", "mt_k_gemm_swiglu_bwd", "mt_k_gemm_wgrad", "mt_k_gemm_splitk", "mt_k_gemm_tile_policy", "mt_k_gemm_wgrad_ws", "mt_k_transpose", "mt_k_rmsnorm_fwd", "mt_k_rmsnorm_bwd", "mt_k_rmsnorm_bwd_parts",
     "mt_k_rope", "mt_k_swiglu_fwd", "mt_k_swiglu_bwd", "mt_k_attn_fwd", "mt_k_attn_fwd_mma", "mt_k_attn_bwd", "mt_k_attn_bwd_mma",
     "mt_k_cross_entropy", "mt_k_sum", "mt_k_embedding_fwd", "mt_k_embedding_bwd",
     "mt_k_embedding_bwd_work", "mt_k_check_ids", "mt_k_device_error",
@@ -125,6 +125,7 @@ def lib():
         "mt_k_gemm_swiglu_bwd": ([P, I64, P, I64, P, I64, P, I64, I, I, I, P], I),
         "mt_k_gemm_wgrad": ([P, I64, P, I64, P, I64, I, I, I, P, I64, P], I),
         "mt_k_gemm_splitk": ([I, I, I], I),
+        "mt_k_gemm_tile_policy": ([I], I),
         "mt_k_gemm_wgrad_ws": ([I, I], I64),
         "mt_k_transpose": ([P, I64, P, I64, I, I, P], I),
         "mt_k_rmsnorm_fwd": ([P, P, P, P, I, I, F, P], I),
@@ -449,6 +450,11 @@ def k_gemm_wgrad(dY, X, G, ws=None, stream=None):
     N = X.shape[1]
     check(lib().mt_k_gemm_wgrad(_dp(dY), dY.stride(0), _dp(X), X.stride(0), _dp(G), G.stride(0), M, N, K, _dp(ws),
                                 ws.numel() if ws is not None else 0, _st(stream)))
+
+
+def k_gemm_tile_policy(policy):
+    """0: library's tile choice; 1: 128 x 256 tiles; 2: 256 x 256 (plain products)."""
+    check(lib().mt_k_gemm_tile_policy(policy))
 
 
 def k_gemm_splitk(M, N, K):

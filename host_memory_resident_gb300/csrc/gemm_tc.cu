@@ -191,10 +191,31 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int S, long l
                  pack_bf16x2(acc[6], acc[7]));
 }
 
-template <bool A_MN, bool B_MN, int EPI>
+// W2: 256 x 256 tiles, each K step two products (A rows 0-127 and 128-255)
+// sharing the B operand, into two 256-column accumulators that fill TMEM (so
+// one tile's epilogue is not overlapped with the next tile's products) and a
+// 3-stage ring of 64 KiB stages. Per 64-deep K block an SM then takes in 64
+// KiB for 8 products instead of 48 KiB for 4.
+template <bool W2>
+struct TileCfg {
+  static constexpr int kBMt = W2 ? 256 : kBM;
+  static constexpr int kSt = W2 ? 3 : kStages;
+  static constexpr uint32_t kAB = (uint32_t)kBMt * kBK * 2;
+  static constexpr uint32_t kStB = kAB + kBBytes;
+  static constexpr size_t kSmem = 1024 + (size_t)kSt * kStB + 256;
+  static_assert(kSmem <= 232448, "shared memory per block");
+};
+
+template <bool A_MN, bool B_MN, int EPI, bool W2 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_abt_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     GemmArgs args) {
+  static_assert(!W2 || EPI == kEpiPlain, "256-row tiles only with the plain epilogue");
+  using T = TileCfg<W2>;
+  constexpr int kBM = T::kBMt;            // rows of a tile (shadows the 128-row default)
+  constexpr int kStages = T::kSt;
+  constexpr uint32_t kABytes = T::kAB;
+  constexpr uint32_t kStageBytes = T::kStB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
@@ -267,13 +288,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, A_MN, B_MN);
+      constexpr uint32_t idesc = idesc_bf16_f32(128, kBN, A_MN, B_MN);  // one M = 128 product
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
       for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x, ++it) {
-        const int acc = it & 1;
-        const uint32_t use = (uint32_t)(it >> 1);
+        // two accumulators used in turn, or (W2) one pair of them per tile
+        const int acc = W2 ? 0 : (it & 1);
+        const uint32_t use = W2 ? (uint32_t)it : (uint32_t)(it >> 1);
         if (!mbar_wait(&tempty_bar[acc], (use & 1) ^ 1, args.err)) { *abort_flag = 1; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
@@ -293,6 +315,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bd = B_MN ? smem_desc_mnmajor_sw128(sb + kk * 2048, kBoxBytes)
                                      : smem_desc_kmajor_sw128(sb + kk * 32);
             tc_mma_bf16(d_tmem, ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+            if (W2)  // A rows 128-255 start 16 KiB into the stage in both layouts
+              tc_mma_bf16(d_tmem + (uint32_t)kBN, desc_advance(ad, kABytes / 2), bd, idesc,
+                          (kb > kb0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(&empty_bar[stage]);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -308,11 +333,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hs = (warp - 2) >> 2;
     int it = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
-      const int acc = it & 1;
-      const uint32_t use = (uint32_t)(it >> 1);
+      const int acc = W2 ? 0 : (it & 1);
+      const uint32_t use = W2 ? (uint32_t)it : (uint32_t)(it >> 1);
       int mb, nb, sp, kb0, kb1;
       unit_coords(t, args, (args.K + kBK - 1) / kBK, mb, nb, sp, kb0, kb1);
-      const int row = mb * kBM + q * 32 + lane;
+      // W2: warp half hs reads the accumulator of tile rows hs * 128 + [0, 128)
+      // (all 256 columns); otherwise half hs of the columns of all 128 rows
+      const int row = mb * kBM + (W2 ? hs * 128 : 0) + q * 32 + lane;
       const bool row_ok = row < args.M;
       // SwiGLU backward: the gate | up values of this warp's first chunk do
       // not depend on the accumulator; their loads overlap the wait for it
@@ -321,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (EPI == kEpiSwigluBwd) load_gate_up(args, row, row_ok, nb * kBN + xc0 * 32, xg, xu);
       if (!mbar_wait(&tfull_bar[acc], use & 1, args.err)) { *abort_flag = 1; break; }
       tc_fence_after();
-      const uint32_t tacc = tmem_base + (uint32_t)(acc * kBN) + ((uint32_t)(q * 32) << 16);
+      const uint32_t tacc = tmem_base + (uint32_t)((W2 ? hs : acc) * kBN) + ((uint32_t)(q * 32) << 16);
       if (EPI == kEpiRope) {
         // heads of hd columns; dims i and i + hd/2 of a head form a pair, so
         // chunk j of the first half pairs with chunk j of the second half
@@ -419,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
 #pragma unroll 1
-        for (int c = hs * (kBN / 64); c < (hs + 1) * (kBN / 64); ++c) {
+        for (int c = W2 ? 0 : hs * (kBN / 64); c < (W2 ? kBN / 32 : (hs + 1) * (kBN / 64)); ++c) {
           __syncwarp();
           uint32_t r[32];
           tmem_ld_32x32b_x32(tacc + (uint32_t)(c * 32), r);
@@ -511,6 +538,15 @@ int get_encode() {
     cudaFuncSetAttribute(gemm_abt_kernel<false, true, kEpiPlain>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
     cudaFuncSetAttribute(gemm_abt_kernel<true, false, kEpiPlain>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
     cudaFuncSetAttribute(gemm_abt_kernel<true, true, kEpiPlain>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+    const int sw = (int)TileCfg<true>::kSmem;
+    cudaFuncSetAttribute(gemm_abt_kernel<false, false, kEpiPlain, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         sw);
+    cudaFuncSetAttribute(gemm_abt_kernel<false, true, kEpiPlain, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         sw);
+    cudaFuncSetAttribute(gemm_abt_kernel<true, false, kEpiPlain, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         sw);
+    cudaFuncSetAttribute(gemm_abt_kernel<true, true, kEpiPlain, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         sw);
     cudaFuncSetAttribute(gemm_abt_kernel<false, false, kEpiRope>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
     cudaFuncSetAttribute(gemm_abt_kernel<false, false, kEpiSwigluFwd>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          sm);
@@ -538,6 +574,25 @@ int make_tmap(CUtensorMap* m, const void* ptr, long long rows, long long cols, l
 
 namespace {
 
+int g_tile_policy = 0;  // 0: the choice below; 1: 128-row tiles; 2: 256-row tiles where allowed
+
+// Whether a plain product takes 256 x 256 tiles: time in units of one
+// 128 x 256 x 64 tile step, waves of 152 tiles times K blocks; a 256-row
+// tile step costs 2 x 0.97 of them. Measured on GB300 (CUDA events, both
+// shapes forced): the wide tiles gain 2-4% where the wave counts match
+// (8192 x 8192 x 4096, 16384 x 11264 x 2048, 16384 x 32000 x 2048) and lose
+// 3-16% where halving the tile count leaves a thin last wave (16384 x 2048
+// by 2048 or 5632, 16384 x 2560 x 2048).
+bool wide_tiles(int M, int N, int K) {
+  if (g_tile_policy != 0) return g_tile_policy == 2;
+  constexpr int kSMs = 152;
+  const long long t128 = (long long)((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+  const long long t256 = (long long)((M + 255) / 256) * ((N + kBN - 1) / kBN);
+  const double c128 = (double)((t128 + kSMs - 1) / kSMs);
+  const double c256 = (double)((t256 + kSMs - 1) / kSMs) * 2.0 * 0.97;
+  return c256 < c128 * 0.995;
+}
+
 // Validates the operands, builds the tensor maps and launches one GEMM with
 // the epilogue `epi` (whose extra fields `args` already holds).
 int launch(int epi, const void* A, long long lda, int a_mn, const void* B, long long ldb, int b_mn, GemmArgs& args,
@@ -560,15 +615,18 @@ int launch(int epi, const void* A, long long lda, int a_mn, const void* B, long 
   if (args.splits < 1) args.splits = 1;
   args.kbps = (num_kb + args.splits - 1) / args.splits;
   args.splits = (num_kb + args.kbps - 1) / args.kbps;
+  // 256 x 256 tiles for plain unsplit products with enough of them
+  const bool w2 = epi == kEpiPlain && args.splits == 1 && wide_tiles(M, N, K);
+  const int bm = w2 ? 256 : kBM;
   CUtensorMap ta, tb;
-  // K-major: rows = M (or N), cols = K, box kBM (kBN) x 64; MN-major: rows = K,
+  // K-major: rows = M (or N), cols = K, box bm (kBN) x 64; MN-major: rows = K,
   // cols = M (or N), box 64 x 64. The SwiGLU forward loads its B tile as two
   // 128-row boxes (gate rows, then up rows).
-  const int ea = a_mn ? make_tmap(&ta, A, K, M, lda, kBK, 64) : make_tmap(&ta, A, M, K, lda, kBM, kBK);
+  const int ea = a_mn ? make_tmap(&ta, A, K, M, lda, kBK, 64) : make_tmap(&ta, A, M, K, lda, bm, kBK);
   const int eb = b_mn ? make_tmap(&tb, B, K, N, ldb, kBK, 64)
                       : make_tmap(&tb, B, N, K, ldb, epi == kEpiSwigluFwd ? kBN / 2 : kBN, kBK);
   if (ea || eb) return MT_EINVAL;
-  args.num_mb = (M + kBM - 1) / kBM;
+  args.num_mb = (M + bm - 1) / bm;
   args.num_nb = (N + kBN - 1) / kBN;
   args.err = device_error_word();
   auto al32 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31) == 0; };
@@ -585,6 +643,16 @@ int launch(int epi, const void* A, long long lda, int a_mn, const void* B, long 
   } else if (epi == kEpiSwigluBwd) {
     if (a_mn || !b_mn) return MT_EINVAL;
     gemm_abt_kernel<false, true, kEpiSwigluBwd><<<grid, kThreads, kSmemBytes, stream>>>(ta, tb, args);
+  } else if (w2) {
+    constexpr size_t sw = TileCfg<true>::kSmem;
+    if (!a_mn && !b_mn)
+      gemm_abt_kernel<false, false, kEpiPlain, true><<<grid, kThreads, sw, stream>>>(ta, tb, args);
+    else if (!a_mn)
+      gemm_abt_kernel<false, true, kEpiPlain, true><<<grid, kThreads, sw, stream>>>(ta, tb, args);
+    else if (!b_mn)
+      gemm_abt_kernel<true, false, kEpiPlain, true><<<grid, kThreads, sw, stream>>>(ta, tb, args);
+    else
+      gemm_abt_kernel<true, true, kEpiPlain, true><<<grid, kThreads, sw, stream>>>(ta, tb, args);
   } else if (!a_mn && !b_mn) {
     gemm_abt_kernel<false, false, kEpiPlain><<<grid, kThreads, kSmemBytes, stream>>>(ta, tb, args);
   } else if (!a_mn) {
@@ -612,6 +680,12 @@ GemmArgs base_args(int M, int N, int K, void* C, long long ldc, int c_f32) {
 bool al16p(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 }  // namespace
+
+int gemm_tile_policy(int policy) {
+  if (policy < 0 || policy > 2) return MT_EINVAL;
+  g_tile_policy = policy;
+  return MT_OK;
+}
 
 int gemm_ex(const void* A, long long lda, int a_mn, const void* B, long long ldb, int b_mn, void* C, long long ldc,
             int c_f32, const void* R, long long ldr, int M, int N, int K, cudaStream_t stream) {

@@ -631,6 +631,8 @@ int mt_k_gemm_wgrad(const void* dY, int64_t lddy, const void* X, int64_t ldx, vo
   return gemm_wgrad(dY, lddy, 1, X, ldx, 1, G, ldg, M, N, K, ws, (size_t)ws_elems, (cudaStream_t)stream);
 }
 
+int mt_k_gemm_tile_policy(int policy) { return gemm_tile_policy(policy); }
+
 int mt_k_gemm_splitk(int M, int N, int K) { return (M <= 0 || N <= 0 || K <= 0) ? 1 : splitk_factor(M, N, K); }
 
 int64_t mt_k_gemm_wgrad_ws(int M, int N) { return (M <= 0 || N <= 0) ? 0 : (int64_t)splitk_ws_elems(M, N); }

@@ -33,6 +33,10 @@ inline int attn_head_chunk(long long bytes_per_head, int nh) {
   return (int)hc;
 }
 
+// Tile shape of plain products: 0 the built-in choice, 1 always 128 x 256,
+// 2 always 256 x 256 where allowed (plain epilogue, no split). Process-wide.
+int gemm_tile_policy(int policy);
+
 // Split-K factor the library uses for C[M, N] over K (1: no split; depends
 // on the shape only, so planning needs no GPU).
 int splitk_factor(int M, int N, int K);

@@ -101,6 +101,16 @@ int mt_k_gemm_swiglu_bwd(const void* dy, int64_t lddy, const void* W, int64_t ld
  */
 int mt_k_gemm_wgrad(const void* dY, int64_t lddy, const void* X, int64_t ldx, void* G, int64_t ldg, int M, int N,
                     int K, float* ws, int64_t ws_elems, void* stream);
+/*
+ * Tile shape of plain products (no fused epilogue, no K split), process-wide:
+ * 0 = the library's choice (default; 256 x 256 tiles for products with many
+ * tiles, where an SM's operand bytes per product are the limit, else
+ * 128 x 256), 1 = always 128 x 256, 2 = always 256 x 256. Results are the
+ * same up to fp32 summation order within a tile (none: both shapes sum K in
+ * the same order, so they are bitwise equal). Not thread-safe against
+ * concurrent launches. Returns MT_EINVAL for other values.
+ */
+int mt_k_gemm_tile_policy(int policy);
 /* Split factor mt_k_gemm_wgrad uses for G [M, N] over K tokens (1: none). */
 int mt_k_gemm_splitk(int M, int N, int K);
 /* fp32 workspace elements mt_k_gemm_wgrad may use for G [M, N] at any K. */

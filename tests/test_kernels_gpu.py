@@ -114,6 +114,43 @@ def test_gemm_deterministic():
     assert torch.equal(c1, c2)
 
 
+@pytest.mark.parametrize("a_mn,b_mn", [(False, False), (False, True), (True, False), (True, True)])
+def test_gemm_wide_tiles_bitwise(a_mn, b_mn):
+    """256 x 256 tiles give the same bits as 128 x 256 tiles (both sum K in
+    the same order), for either operand layout, with a residual and with
+    fp32 output, on ragged M, N and K; and match the fp64 product."""
+    rng = np.random.default_rng(7 + 2 * a_mn + b_mn)
+    M, N, K = 600, 520, 1000
+    A, Ah = bf(rng.standard_normal((K, M) if a_mn else (M, K)))
+    B, Bh = bf(rng.standard_normal((K, N) if b_mn else (N, K)) / np.sqrt(K))
+    R, Rh = bf(rng.standard_normal((M, N)))
+    outs = {}
+    try:
+        for pol in (1, 2):
+            mt.k_gemm_tile_policy(pol)
+            c16 = torch.full((M, N), float("nan"), device=DEV, dtype=torch.bfloat16)
+            c32 = torch.full((M, N), float("nan"), device=DEV, dtype=torch.float32)
+            mt.k_gemm_ex(A, a_mn, B, b_mn, c16, R)
+            mt.k_gemm_ex(A, a_mn, B, b_mn, c32)
+            torch.cuda.synchronize()
+            outs[pol] = (c16, c32)
+    finally:
+        mt.k_gemm_tile_policy(0)
+    assert torch.equal(outs[1][0], outs[2][0])
+    assert torch.equal(outs[1][1], outs[2][1])
+    a64 = Ah.T if a_mn else Ah
+    b64 = Bh.T if b_mn else Bh
+    ref = a64 @ b64.T
+    assert_close(host(outs[2][1]), ref, l2=1e-4, elem=1e-3, what="wide tiles fp32")
+    assert_close(host(outs[2][0]), ref + Rh, l2=5e-3, elem=1e-2, what="wide tiles bf16 + residual")
+
+
+def test_gemm_tile_policy_rejects_bad_values():
+    with pytest.raises(mt.MtError):
+        mt.k_gemm_tile_policy(3)
+    mt.k_gemm_tile_policy(0)
+
+
 @pytest.mark.parametrize("M,N,K", [(384, 512, 8192), (296, 520, 5000), (2560, 2048, 16384)])
 def test_gemm_wgrad_split_k(M, N, K):
     """Split-K weight gradient: near the fp64 product, deterministic, and the
