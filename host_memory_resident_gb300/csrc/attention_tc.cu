@@ -8,19 +8,23 @@
 //            tile ahead of V;
 //   warp 1   allocates TMEM and issues tcgen05.mma for both tiles t:
 //              S_t = Q_t K_j^T    (M 128, N 128, K = hd) into t's 128-column
-//                                  TMEM buffer, issued as soon as t's softmax
-//                                  has copied S_t of the previous key tile out,
-//              O_t += P_t V_j     (M 128, N = hd, K 128) with P_t from shared
-//                                  memory and V read MN-major in place;
+//                                  TMEM buffer,
+//              O_t += P_t V_j     (M 128, N = hd, K 128) with P_t read from
+//                                  TMEM as the A operand and V read MN-major
+//                                  in place;
 //   warps 2-5, 6-9: one softmax group per query tile, one thread per query
 //            row (its TMEM lane) holding the row's 128 scores in registers.
 //            The causal mask and the online softmax run in fp32 (log2
-//            domain); P is written as bf16 into TMEM columns of its own at
-//            hd 64 (read by the P V product as its A operand), or into
-//            128-byte-swizzled shared memory at hd 128, where S and O fill
-//            TMEM. O is rescaled in TMEM only when a row's running maximum
-//            grows by more than 2^8, so P stays below 256 and the final O / l
-//            is unchanged.
+//            domain); P is written back as bf16 into TMEM: at hd 64 into
+//            columns of its own, so S_t of the next key tile is issued as
+//            soon as the group has copied S_t out; at hd 128, where S and O
+//            fill TMEM, into the first 64 columns of S_t's own buffer, so
+//            S_t of the next key tile is issued right after P_t V (the
+//            products run in issue order). No P tile passes through shared
+//            memory, whose port the operand reads and the TMA writes share.
+//            O is rescaled in TMEM only when a row's running maximum grows
+//            by more than 2^8, so P stays below 256 and the final O / l is
+//            unchanged.
 // While one group exponentiates, the tensor core computes the other group's
 // products and both groups' next scores, so neither the exponential units nor
 // the tensor core waits on a single chain of dependencies.
@@ -51,14 +55,12 @@ template <int HD>
 struct TcCfg {
   static constexpr int kBoxes = HD / 64;
   static constexpr uint32_t kTile = kBoxes * kBox;     // 128 rows x HD
-  static constexpr int kKS = 2;                        // K ring slots
-  static constexpr int kVS = HD == 64 ? 2 : 1;         // V ring slots (shared memory bound at hd 128)
+  static constexpr int kKS = 3;                        // K ring slots
+  static constexpr int kVS = HD == 64 ? 3 : 2;         // V ring slots
   static constexpr uint32_t kQOff = 0;                 // two Q tiles
   static constexpr uint32_t kKOff = 2 * kTile;
   static constexpr uint32_t kVOff = kKOff + kKS * kTile;
-  static constexpr uint32_t kPOff = kVOff + kVS * kTile;
-  static constexpr uint32_t kPBuf = 2 * kBox;          // one P tile (128 rows x 128 keys)
-  static constexpr uint32_t kBarOff = kPOff + 2 * kPBuf;
+  static constexpr uint32_t kBarOff = kVOff + kVS * kTile;
   static constexpr size_t kSmem = 1024 + kBarOff + 256;
   static_assert(kSmem <= 232448, "shared memory per block");
 };
@@ -75,16 +77,16 @@ __global__ void __launch_bounds__(kThr, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
-  uint64_t* q_full = bars;         // [1]
-  uint64_t* k_full = bars + 1;     // [kKS]
-  uint64_t* k_empty = bars + 3;    // [kKS]
-  uint64_t* v_full = bars + 5;     // [kVS]
-  uint64_t* v_empty = bars + 7;    // [kVS]
-  uint64_t* s_full = bars + 9;     // [2] per tile: S_t written
-  uint64_t* s_empty = bars + 11;   // [2] per tile: S_t copied out by its softmax group
-  uint64_t* p_full = bars + 13;    // [2] per tile: P_t written (and O_t rescaled)
-  uint64_t* p_empty = bars + 15;   // [2] per tile: P_t V finished (O_t current, P_t free)
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 17);
+  uint64_t* q_full = bars;                   // [1]
+  uint64_t* k_full = bars + 1;               // [kKS]
+  uint64_t* k_empty = k_full + C::kKS;       // [kKS]
+  uint64_t* v_full = k_empty + C::kKS;       // [kVS]
+  uint64_t* v_empty = v_full + C::kVS;       // [kVS]
+  uint64_t* s_full = v_empty + C::kVS;       // [2] per tile: S_t written
+  uint64_t* s_empty = s_full + 2;            // [2] per tile: S_t copied out by its softmax group
+  uint64_t* p_full = s_empty + 2;            // [2] per tile: P_t written (and O_t rescaled)
+  uint64_t* p_empty = p_full + 2;            // [2] per tile: P_t V finished (O_t current, P_t free)
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(p_empty + 2);
 
   const int nqt = (s + kQ - 1) / kQ;
   const int npair = (nqt + 1) / 2;
@@ -128,10 +130,10 @@ __global__ void __launch_bounds__(kThr, 1)
   // would live in local memory)
   auto tS = [&](int t_) { return tmem + 128u * (uint32_t)t_; };
   auto tO = [&](int t_) { return tmem + 256u + (uint32_t)HD * (uint32_t)t_; };
-  // hd 64 leaves TMEM columns 384-511 free: P of each tile goes there and the
-  // P V product reads it as its A operand (no shared-memory round trip)
-  constexpr bool kPT = HD == 64;
-  auto tP = [&](int t_) { return tmem + 384u + 64u * (uint32_t)t_; };
+  // P_t in TMEM: hd 64 leaves columns 384-511 free for it; at hd 128 it
+  // takes the first 64 columns of S_t's buffer (kAlias)
+  constexpr bool kAlias = HD == 128;
+  auto tP = [&](int t_) { return kAlias ? tS(t_) : tmem + 384u + 64u * (uint32_t)t_; };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -183,52 +185,86 @@ __global__ void __launch_bounds__(kThr, 1)
       constexpr uint32_t idesc_s = idesc_bf16_f32(kQ, kKV, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kQ, HD, false, true);
       bool ok = mbar_wait(q_full, 0, err);
-      // S_t(j) for both tiles that still need key tile j, then release K_j
       const uint64_t dQ0 = smem_desc_kmajor_sw128(smem_u32(sm + C::kQOff));
-      const uint64_t dP0 = smem_desc_kmajor_sw128(smem_u32(sm + C::kPOff));
-      auto issue_s = [&](int j) -> bool {
-        const int st = j % C::kKS;
-        if (!mbar_wait(&k_full[st], (j / C::kKS) & 1, err)) return false;
-        const uint64_t dK = smem_desc_kmajor_sw128(smem_u32(sm + C::kKOff + st * C::kTile));
-        for (int t = 0; t < 2; ++t) {
-          if (j >= nkv[t]) continue;
-          // the group has copied S_t(j-1) out of TMEM
-          if (j > 0 && !mbar_wait(&s_empty[t], (j - 1) & 1, err)) return false;
-          tc_fence_after();
-          const uint64_t dQ = desc_advance(dQ0, t * C::kTile);
+      // S_t(j) = Q_t K_j^T; K_j has landed (the caller waited for it)
+      auto mma_s = [&](int j, int t) {
+        const uint64_t dK = smem_desc_kmajor_sw128(smem_u32(sm + C::kKOff + (j % C::kKS) * C::kTile));
+        const uint64_t dQ = desc_advance(dQ0, t * C::kTile);
 #pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-            tc_mma_bf16(tS(t), desc_advance(dQ, off), desc_advance(dK, off), idesc_s, kk > 0 ? 1u : 0u);
-          }
-          tc_commit(&s_full[t]);
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+          tc_mma_bf16(tS(t), desc_advance(dQ, off), desc_advance(dK, off), idesc_s, kk > 0 ? 1u : 0u);
         }
-        tc_commit(&k_empty[st]);
-        return true;
+        tc_commit(&s_full[t]);
       };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; ok && j < n_kv; ++j) {
-        if (j + 1 < n_kv && !(ok = issue_s(j + 1))) break;
-        const int vs = j % C::kVS;
-        if (!(ok = mbar_wait(&v_full[vs], (j / C::kVS) & 1, err))) break;
-        const uint64_t mV = smem_desc_mnmajor_sw128(smem_u32(sm + C::kVOff + vs * C::kTile), kBox);
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (j >= nkv[t]) continue;
-          if (!(ok = mbar_wait(&p_full[t], j & 1, err))) break;
-          tc_fence_after();
-          const uint64_t dP = desc_advance(dP0, t * C::kPBuf);
+      // O_t += P_t(j) V_j, P_t from TMEM (16 keys = 8 packed columns per step)
+      auto mma_pv = [&](int j, int t, uint64_t mV) {
 #pragma unroll
-          for (int kk = 0; kk < kKV / 16; ++kk) {
-            const uint32_t aoff = (kk >> 2) * kBox + (kk & 3) * 32;
-            if (kPT)
-              tc_mma_bf16_ta(tO(t), tP(t) + kk * 8, desc_advance(mV, kk * 2048), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-            else
-              tc_mma_bf16(tO(t), desc_advance(dP, aoff), desc_advance(mV, kk * 2048), idesc_pv,
-                          (j > 0 || kk > 0) ? 1u : 0u);
-          }
-          tc_commit(&p_empty[t]);
+        for (int kk = 0; kk < kKV / 16; ++kk)
+          tc_mma_bf16_ta(tO(t), tP(t) + kk * 8, desc_advance(mV, kk * 2048), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&p_empty[t]);
+      };
+      auto wait_k = [&](int j) { return mbar_wait(&k_full[j % C::kKS], (j / C::kKS) & 1, err); };
+      if (kAlias) {
+        // P_t(j) occupies S_t's columns until P_t(j) V has read it, so
+        // S_t(j + 1) is issued right after that product
+        if (ok && (ok = wait_k(0))) {
+          tc_fence_after();
+          for (int t = 0; t < 2; ++t)
+            if (nkv[t] > 0) mma_s(0, t);
+          tc_commit(&k_empty[0]);
         }
-        if (ok) tc_commit(&v_empty[vs]);
+        for (int j = 0; ok && j < n_kv; ++j) {
+          const int vs = j % C::kVS;
+          if (!(ok = mbar_wait(&v_full[vs], (j / C::kVS) & 1, err))) break;
+          const uint64_t mV = smem_desc_mnmajor_sw128(smem_u32(sm + C::kVOff + vs * C::kTile), kBox);
+          bool k_next = false;  // K_{j+1} waited for
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (j >= nkv[t]) continue;
+            if (!(ok = mbar_wait(&p_full[t], j & 1, err))) break;
+            tc_fence_after();
+            mma_pv(j, t, mV);
+            if (j + 1 < nkv[t]) {
+              if (!k_next) {
+                if (!(ok = wait_k(j + 1))) break;
+                k_next = true;
+                tc_fence_after();
+              }
+              mma_s(j + 1, t);
+            }
+          }
+          if (!ok) break;
+          tc_commit(&v_empty[vs]);
+          if (k_next) tc_commit(&k_empty[(j + 1) % C::kKS]);
+        }
+      } else {
+        // S_t(j) for both tiles that still need key tile j, then release K_j;
+        // S_t(j) overwrites S_t(j-1) once the group has copied it out
+        auto issue_s = [&](int j) -> bool {
+          if (!wait_k(j)) return false;
+          for (int t = 0; t < 2; ++t) {
+            if (j >= nkv[t]) continue;
+            if (j > 0 && !mbar_wait(&s_empty[t], (j - 1) & 1, err)) return false;
+            tc_fence_after();
+            mma_s(j, t);
+          }
+          tc_commit(&k_empty[j % C::kKS]);
+          return true;
+        };
+        if (ok) ok = issue_s(0);
+        for (int j = 0; ok && j < n_kv; ++j) {
+          if (j + 1 < n_kv && !(ok = issue_s(j + 1))) break;
+          const int vs = j % C::kVS;
+          if (!(ok = mbar_wait(&v_full[vs], (j / C::kVS) & 1, err))) break;
+          const uint64_t mV = smem_desc_mnmajor_sw128(smem_u32(sm + C::kVOff + vs * C::kTile), kBox);
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (j >= nkv[t]) continue;
+            if (!(ok = mbar_wait(&p_full[t], j & 1, err))) break;
+            tc_fence_after();
+            mma_pv(j, t, mV);
+          }
+          if (ok) tc_commit(&v_empty[vs]);
+        }
       }
     }
   } else {
@@ -241,8 +277,6 @@ __global__ void __launch_bounds__(kThr, 1)
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const float sc = rsqrtf((float)HD) * kLog2e;
     float m_ref = -INFINITY, l = 0.f;
-    uint8_t* sP = sm + C::kPOff + t * C::kPBuf;
-    const uint32_t rsw = (uint32_t)(row & 7);
     bool ok = true;
     for (int j = 0; j < nk && ok; ++j) {
       if (!mbar_wait_warp(&s_full[t], j & 1, err)) { ok = false; break; }
@@ -311,29 +345,15 @@ __global__ void __launch_bounds__(kThr, 1)
         }
       }
       l += lt0 + lt1;
-      if (kPT) {
-        // the row's 64 packed words into its TMEM lane, keys in order
+      // the row's 64 packed words into its TMEM lane, keys in order
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          uint32_t pw[32];
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t pw[32];
 #pragma unroll
-          for (int w = 0; w < 32; ++w) pw[w] = r[(32 * h2 + w) >> 4][(32 * h2 + w) & 15];
-          tmem_st_32x32b_x32(tP(t) + lane_off + h2 * 32, pw);
-        }
-        tmem_st_wait();
-      } else {
-        // the row's 128 keys: two 64-key boxes of 128-byte rows, 128-byte swizzle
-#pragma unroll
-        for (int bx = 0; bx < 2; ++bx)
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const int w0 = bx * 32 + 4 * c;  // packed word index in the row
-            const uint4 u = make_uint4(r[w0 >> 4][w0 & 15], r[(w0 + 1) >> 4][(w0 + 1) & 15],
-                                       r[(w0 + 2) >> 4][(w0 + 2) & 15], r[(w0 + 3) >> 4][(w0 + 3) & 15]);
-            *reinterpret_cast<uint4*>(sP + bx * kBox + row * 128 + (((uint32_t)c ^ rsw) * 16)) = u;
-          }
-        fence_proxy_async_smem();
+        for (int w = 0; w < 32; ++w) pw[w] = r[(32 * h2 + w) >> 4][(32 * h2 + w) & 15];
+        tmem_st_32x32b_x32(tP(t) + lane_off + h2 * 32, pw);
       }
+      tmem_st_wait();
       tc_fence_before();
       mbar_arrive_warp(&p_full[t]);
     }
