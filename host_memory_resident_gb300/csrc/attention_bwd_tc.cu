@@ -24,6 +24,7 @@
 #include <cmath>
 #include <mutex>
 #include <string>
+#include <type_traits>
 
 #include "common.cuh"
 #include "mt_internal.h"
@@ -278,23 +279,32 @@ __global__ void __launch_bounds__(kThr, 1)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive_warp(&s_empty[G]);
-      const bool diag = q0 < k0 + kT;  // the sub-tile reaches the diagonal: mask key > query
+      // P^T = exp2(S^T * scale - lse), dS^T = P^T (dP^T - delta), packed in
+      // place; only a sub-tile that reaches the diagonal masks key > query
+      // (two copies of the loop, so the others carry no compare and select)
+      auto elementwise = [&](auto masked_tag) {
+        constexpr bool kMasked = decltype(masked_tag)::value;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float4 ld = reinterpret_cast<const float4*>(vec)[i];  // columns 2i, 2i+1
-        const float l2s[2] = {ld.x, ld.z}, dls[2] = {ld.y, ld.w};
-        float pv[2], dv[2];
+        for (int i = 0; i < 32; ++i) {
+          const float4 ld = reinterpret_cast<const float4*>(vec)[i];  // columns 2i, 2i+1
+          const float l2s[2] = {ld.x, ld.z}, dls[2] = {ld.y, ld.w};
+          float pv[2], dv[2];
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int c = 2 * i + e;  // query column within the sub-tile
-          float p = ex2_approx(fmaf(__uint_as_float(rs[c >> 5][c & 31]), sc, -l2s[e]));
-          if (diag && q0 + c < key) p = 0.f;
-          pv[e] = p;
-          dv[e] = p * (__uint_as_float(rp[c >> 5][c & 31]) - dls[e]);
+          for (int e = 0; e < 2; ++e) {
+            const int c = 2 * i + e;  // query column within the sub-tile
+            float p = ex2_approx(fmaf(__uint_as_float(rs[c >> 5][c & 31]), sc, -l2s[e]));
+            if (kMasked && q0 + c < key) p = 0.f;
+            pv[e] = p;
+            dv[e] = p * (__uint_as_float(rp[c >> 5][c & 31]) - dls[e]);
+          }
+          rs[i >> 4][i & 15] = pack_bf16x2(pv[0], pv[1]);
+          rp[i >> 4][i & 15] = pack_bf16x2(dv[0], dv[1]);
         }
-        rs[i >> 4][i & 15] = pack_bf16x2(pv[0], pv[1]);
-        rp[i >> 4][i & 15] = pack_bf16x2(dv[0], dv[1]);
-      }
+      };
+      if (q0 < k0 + kT)
+        elementwise(std::true_type{});
+      else
+        elementwise(std::false_type{});
       // P^T and dS^T into the first 32 columns of the row's S^T and dP^T
       // lanes. The products that last read them (dV/dK of sub-tile it - 2)
       // completed before S^T of this sub-tile did, which s_full reported.
