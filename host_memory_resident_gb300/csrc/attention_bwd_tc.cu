@@ -521,24 +521,33 @@ __global__ void __launch_bounds__(kThr, 1)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive_warp(s_empty);
-      const bool diag = (j == n_kv - 1);
       const int kb = j * kT + half * 64;
       uint32_t dk[32];
       const float2 sc2 = make_float2(sc, sc), nl2 = make_float2(-l2, -l2), ndl = make_float2(-dl, -dl);
+      // only the diagonal key tile (the last) masks key > query; the others
+      // run a copy of the loop without the compares
+      auto elementwise = [&](auto masked_tag) {
+        constexpr bool kMasked = decltype(masked_tag)::value;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int ci = 2 * i;
-        const float2 x = ffma2(make_float2(__uint_as_float(rs[ci >> 5][ci & 31]), __uint_as_float(rs[ci >> 5][(ci + 1) & 31])),
-                               sc2, nl2);
-        float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-        if (diag) {
-          if (kb + ci > qpos) pp.x = 0.f;
-          if (kb + ci + 1 > qpos) pp.y = 0.f;
+        for (int i = 0; i < 32; ++i) {
+          const int ci = 2 * i;
+          const float2 x = ffma2(
+              make_float2(__uint_as_float(rs[ci >> 5][ci & 31]), __uint_as_float(rs[ci >> 5][(ci + 1) & 31])), sc2, nl2);
+          float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          if (kMasked) {
+            if (kb + ci > qpos) pp.x = 0.f;
+            if (kb + ci + 1 > qpos) pp.y = 0.f;
+          }
+          const float2 dp =
+              make_float2(__uint_as_float(rp[ci >> 5][ci & 31]), __uint_as_float(rp[ci >> 5][(ci + 1) & 31]));
+          const float2 dv = fmul2(pp, fadd2(dp, ndl));
+          dk[i] = pack_bf16x2(dv.x, dv.y);
         }
-        const float2 dp = make_float2(__uint_as_float(rp[ci >> 5][ci & 31]), __uint_as_float(rp[ci >> 5][(ci + 1) & 31]));
-        const float2 dv = fmul2(pp, fadd2(dp, ndl));
-        dk[i] = pack_bf16x2(dv.x, dv.y);
-      }
+      };
+      if (j == n_kv - 1)
+        elementwise(std::true_type{});
+      else
+        elementwise(std::false_type{});
       // dS of this half's 64 keys into its 32 columns of buffer j % 2. The
       // product that last read that buffer (dQ of tile j - 2) completed
       // before S of tile j did, which s_full reported.
