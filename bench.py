@@ -555,25 +555,33 @@ def host_mem_available():
     return None
 
 
+def host_memory_refusal(mt, cfg, shape, keep_grads, avail):
+    """The error line for a workload whose host state and pinned buffers
+    exceed 90% of the available host memory `avail` (bytes), else None."""
+    plan = mt.plan(cfg)
+    need = plan["host_state_bytes"] * (16 if keep_grads else 12) // 16 + plan["pinned_bytes"]
+    if avail is None or need <= 0.9 * avail:
+        return None
+    return {"metric": METRIC, "config": {"workload": shape.name}, "value": None,
+            "error": f"host memory: the workload needs {need / 1e9:.1f} GB of host state and "
+                     f"pinned buffers, {avail / 1e9:.1f} GB available"}
+
+
 def run_ours(args, shape, world, rank, local, pg):
     import torch
     import host_memory_resident_gb300 as mt
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
     cfg = mt.make_config(shape, device=local, host_threads=args.host_threads, overlap_adam=args.overlap,
                          unfused_epilogues=args.unfused, keep_attention=args.keep_attention)
     descs, n_total = mt.layout(cfg)
-    # refuse, before allocating, a workload whose host state and pinned
-    # buffers do not fit the host's available memory (14B needs ~266 GB)
-    plan = mt.plan(cfg)
-    need = plan["host_state_bytes"] * (16 if args.keep_grads else 12) // 16 + plan["pinned_bytes"]
-    avail = host_mem_available()
-    if avail is not None and need > 0.9 * avail:
+    # refuse, before touching the GPU or allocating, a workload whose host
+    # state and pinned buffers do not fit the host's memory (14B: ~285 GB)
+    refusal = host_memory_refusal(mt, cfg, shape, args.keep_grads, host_mem_available())
+    if refusal is not None:
         if rank == 0:
-            print(json.dumps({"metric": METRIC, "config": {"workload": shape.name}, "value": None,
-                              "error": f"host memory: the workload needs {need / 1e9:.1f} GB of host state and "
-                                       f"pinned buffers, {avail / 1e9:.1f} GB available"}), flush=True)
+            print(json.dumps(refusal), flush=True)
         return 3
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
     segs = [(t["offset"], t["rows"] * t["cols"], "normal" if t["kind"] == 0 else "ones") for t in descs]
     master = synth.init_master(n_total, segs, seed=0)
     B, s = shape.batch, shape.seq

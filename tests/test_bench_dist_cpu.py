@@ -46,3 +46,18 @@ def test_reference_arm_other_ranks_exit_without_work(monkeypatch):
     class A:
         gpus, steps, warmup = 2, 1, 0
     assert bench.run_reference(A, None, 2, 1, None) == 0
+
+
+def test_bench_refuses_workloads_beyond_host_memory():
+    """The bench's guard: the 14B workload's host state and pinned buffers
+    (about 285 GB) do not fit 199 GB of host memory; the 1.1B workload's do."""
+    import bench
+    import host_memory_resident_gb300 as mt
+    import synth
+    big, small = synth.workload("14b"), synth.workload("1.1b")
+    avail = 199 * 2**30
+    r = bench.host_memory_refusal(mt, mt.make_config(big), big, True, avail)
+    assert r is not None and r["value"] is None and "host memory" in r["error"]
+    assert bench.host_memory_refusal(mt, mt.make_config(small), small, True, avail) is None
+    # unknown available memory: no refusal
+    assert bench.host_memory_refusal(mt, mt.make_config(big), big, True, None) is None
