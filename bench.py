@@ -6,11 +6,14 @@ bf16 weights host->device through two buffers, forward with checkpoints,
 fused head + cross entropy, segment recompute + backward, K-slab gradient
 offload, host accumulate + Adam on the FP32 master (all through libmt.so).
 
-Prints one JSON line (rank 0):
-  value  tokens/s over all ranks, token/label arrays already in device memory
+The default workload is the 7B decoder (2 x 4096 tokens, C = 4, K = 12);
+``--config`` picks another. Prints one JSON line (rank 0):
+  value  tokens/s over all ranks, token/label arrays already in device memory,
+         timed with per-launch profiling off
   e2e    the same through mt_train_step with host token/label arrays
   roofline  the dominant kernel (the tcgen05 GEMM): algorithmic FLOPs of its
-         launches in the timed region / their CUDA-event device time
+         launches / their CUDA-event device time, over a separate profiled
+         pass of the same steps
   step_roofline  model FLOPs at the bf16 peak vs weight + gradient bytes over
          the measured host link, whichever is slower
   cpu_baseline  the oracle on this host's cores on a bounded sample
@@ -246,11 +249,13 @@ def gemm_traffic_record():
 
 
 # ----------------------------------------------------------- CPU baseline
-def oracle_sample(shape):
+def oracle_sample(shape, max_tokens=16384):
     """Time the oracle on a bounded sample of the workload and compose the
     full step: B * (L * t_layer + t_rest) + t_adam(N). The sample is one
-    sequence at full width and full length through a 1-layer and a 2-layer
-    model (t_layer = their difference), plus Adam on a 2^24-element slice."""
+    sequence at full width through a 1-layer and a 2-layer model (t_layer =
+    their difference), plus Adam on a 2^24-element slice. Sequences longer
+    than ``max_tokens`` are timed at max_tokens / 2 and max_tokens and each
+    term is extrapolated as a s + b s^2 (the attention part grows with s^2)."""
     import oracle
     s = shape.seq
 
@@ -268,16 +273,15 @@ def oracle_sample(shape):
         return times
 
     extrapolated = ""
-    if s > 16384:
-        # long sequences: time 8192 and 16384 tokens and extrapolate each term
-        # as a s + b s^2 (the attention part grows with s^2)
-        ta, tb = sample(8192), sample(16384)
+    if s > max_tokens:
+        s1, s2 = max_tokens // 2, max_tokens
+        ta, tb = sample(s1), sample(s2)
         times = {}
         for L in (1, 2):
-            b2 = (tb[L] - 2.0 * ta[L]) / (16384.0 * 16384.0 - 2.0 * 8192.0 * 8192.0)
-            a1 = (ta[L] - b2 * 8192.0 * 8192.0) / 8192.0
+            b2 = (tb[L] - 2.0 * ta[L]) / (s2 * float(s2) - 2.0 * s1 * float(s1))
+            a1 = (ta[L] - b2 * s1 * float(s1)) / s1
             times[L] = max(a1, 0.0) * s + max(b2, 0.0) * s * s
-        extrapolated = "extrapolated from 8192 and 16384 tokens as a s + b s^2; "
+        extrapolated = f"extrapolated from {s1} and {s2} tokens as a s + b s^2; "
     else:
         times = sample(s)
     n = 1 << 24
@@ -347,14 +351,33 @@ def sum_over_ranks(pg, x):
 
 
 # ------------------------------------------------------------------- arms
+def config_dict(args, shape, world, n_total):
+    """The workload description both arms print (identical keys and values)."""
+    return {"workload": workload_desc(shape), "global_batch_tokens": shape.batch * shape.seq * world,
+            "seq_len": shape.seq,
+            "parallelism": f"replicas x{world} (no collective)" if world > 1 else "single GPU",
+            "overlap_adam": bool(args.overlap),
+            "fp32_grad_array": bool(args.keep_grads),
+            "fused_epilogues": not args.unfused,
+            "keep_attention": bool(args.keep_attention),
+            "l2": "inputs larger than L2: each step streams the whole bf16 store "
+                  f"({2.0 * n_total / 1e9:.2f} GB) and the activations"}
+
+
+REFERENCE_MAX_TOKENS = 512   # per-step sample of the reference arm (see run_reference)
+
+
 def run_reference(args, shape, world, rank, pg):
     """The oracle as it stands, on this host's cores (rank 0 only)."""
     if rank != 0:
         return 0
+    import oracle
     vals = []
     base = None
     for i in range(args.warmup + args.steps):
-        b = oracle_sample(shape)
+        # each step is a bounded sample (sequences over 512 tokens timed at
+        # 256 and 512 and extrapolated) so the whole run takes a few minutes
+        b = oracle_sample(shape, max_tokens=REFERENCE_MAX_TOKENS)
         if i >= args.warmup:
             vals.append(b["value"])
             base = b
@@ -364,7 +387,7 @@ def run_reference(args, shape, world, rank, pg):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": shape.batch * shape.seq / value * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded uniform token ids, normal(0, 0.02) weights)",
-        "config": {"workload": workload_desc(shape), "parallelism": "none (host cores)"},
+        "config": config_dict(args, shape, world, oracle.build_layout(shape).n_total),
         "cpu_baseline": {k: base[k] for k in ("value", "unit", "cores", "kind", "sample")},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -599,9 +622,9 @@ def run_ours(args, shape, world, rank, local, pg):
     for i in range(W):
         tr.step_device(dev_batches[i][0].data_ptr(), dev_batches[i][1].data_ptr(), B, s)
 
-    # ---- timed region: K steps, token/label arrays resident in device memory
-    tr.profile(True)
-    tr.read_profile(reset=True)
+    # ---- timed region: K steps, token/label arrays resident in device memory,
+    # per-launch profiling off (the per-class profile is a separate pass below)
+    tr.profile(False)
     st0 = tr.stats()
     clocks = ClockSampler(local)
     clocks.start()
@@ -622,8 +645,6 @@ def run_ours(args, shape, world, rank, local, pg):
     barrier(pg)
     clk = clocks.stop()
     st1 = tr.stats()
-    prof = tr.read_profile(reset=True)
-    tr.profile(False)
     t_max = max_over_ranks(pg, e0.elapsed_time(e1) / 1e3)
 
     # ---- end to end: host token/label arrays through mt_train_step
@@ -640,6 +661,17 @@ def run_ours(args, shape, world, rank, local, pg):
     barrier(pg)
     e2e_max = max_over_ranks(pg, e2.elapsed_time(e3) / 1e3)
     stats = tr.stats()
+    # ---- per-class profile: the same steps again with CUDA events around
+    # every launch and copy (on the stream each runs on)
+    KP = min(K, args.profile_steps)
+    tr.profile(True)
+    tr.read_profile(reset=True)
+    for i in range(KP):
+        tk, lb = dev_batches[W + i]
+        tr.step_device(tk.data_ptr(), lb.data_ptr(), B, s)
+    tr.sync()
+    prof = tr.read_profile(reset=True)
+    tr.profile(False)
     # ---- one more step, profiled: launch / copy / host-worker timeline
     tl_sum = None
     if not args.no_timeline:
@@ -668,32 +700,27 @@ def run_ours(args, shape, world, rank, local, pg):
     t_comp = F / (pk["bf16_tflops"] * 1e12)
     t_link = max(2 * w_bytes / (link["bidir_h2d_gbs"] * 1e9), w_bytes / (link["bidir_d2h_gbs"] * 1e9))
     t_roof = max(t_comp, t_link)
-    prof_out = {k: {"launches": v["launches"], "ms_per_step": v["ms"] / K,
+    prof_out = {k: {"launches_per_step": v["launches"] / KP, "ms_per_step": v["ms"] / KP,
                     "tflops": (v["flops"] / (v["ms"] / 1e3) / 1e12) if v["flops"] and v["ms"] else None,
                     "gbs": (v["bytes"] / (v["ms"] / 1e3) / 1e9) if v["bytes"] and v["ms"] else None}
                 for k, v in prof.items() if v["launches"] and k not in ("h2d", "d2h")}
-    copies = {k: {"copies_per_step": prof[k]["launches"] / K, "ms_per_step": prof[k]["ms"] / K,
-                  "gb_per_step": prof[k]["bytes"] / K / 1e9,
+    copies = {k: {"copies_per_step": prof[k]["launches"] / KP, "ms_per_step": prof[k]["ms"] / KP,
+                  "gb_per_step": prof[k]["bytes"] / KP / 1e9,
                   "gbs_while_copying": prof[k]["bytes"] / (prof[k]["ms"] / 1e3) / 1e9 if prof[k]["ms"] else None}
               for k in ("h2d", "d2h") if k in prof}
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded uniform token ids, normal(0, 0.02) weights, norms 1.0)",
-        "config": {"workload": workload_desc(shape), "global_batch_tokens": M * world, "seq_len": s,
-                   "parallelism": f"replicas x{world} (no collective)" if world > 1 else "single GPU",
-                   "overlap_adam": bool(args.overlap),
-                   "fp32_grad_array": bool(args.keep_grads),
-                   "fused_epilogues": not args.unfused,
-                   "keep_attention": bool(args.keep_attention),
-                   "l2": "inputs larger than L2: each step streams the whole bf16 store "
-                         f"({w_bytes / 1e9:.2f} GB) and the activations"},
+        "config": config_dict(args, shape, world, n_total),
         "model_tflops": F / t_step / 1e12,
         "step_roofline": {"model_flops": F, "t_compute_s": t_comp, "t_link_s": t_link, "t_roof_s": t_roof,
                           "frac": t_roof / t_step, "peak_tflops": pk["bf16_tflops"], "host_link": link,
                           "weight_bytes": w_bytes, "peak_source": pk_kind},
         "roofline": {"bound": "tensor", "kernel": "gemm_abt (tcgen05)", "achieved": gemm_tf, "peak": peak_tf,
                      "unit": "TFLOP/s", "frac": (gemm_tf / peak_tf) if gemm_tf else None,
+                     "measured_over": f"{KP} profiled steps run after the timed ones (CUDA events around each "
+                                      "launch on the compute stream)",
                      "peak_source": f"bf16_tflops_sustained, of {pk_kind}",
                      "traffic": (traffic["traffic_over_algorithmic"] * g["bytes"] / max(g["launches"], 1))
                      if traffic else None,
@@ -739,7 +766,9 @@ def main():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="1.1b", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--config", default="7b", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--profile-steps", type=int, default=5,
+                    help="steps of the separate per-class profiled pass (at most --steps)")
     ap.add_argument("--kernel", default=None, choices=[None, "gemm", "attn", "misc"])
     ap.add_argument("--legacy", action="store_true", help="with --kernel attn: the mma.sync kernels")
     ap.add_argument("--backward", action="store_true", help="with --kernel attn: time the backward")

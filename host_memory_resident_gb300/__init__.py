@@ -58,7 +58,7 @@ class Stats(C.Structure):
                 ("kernel_launches", C.c_int64), ("host_compute_s", C.c_double), ("host_copy_wait_s", C.c_double)]
 
 
-PROF_CLASSES = ["gemm", "attn_fwd", "attn_bwd", "norm", "rope", "swiglu", "transpose", "ce", "embed", "other",
+PROF_CLASSES = ["gemm", "attn_fwd", "attn_bwd", "norm", "rope", "swiglu", "reserved", "ce", "embed", "other",
                 "h2d", "d2h"]
 
 
@@ -72,7 +72,7 @@ EXPORTS = [
     "mt_read_grads", "mt_sync", "mt_get_step", "mt_set_step", "mt_sync_store", "mt_get_stats",
     "mt_get_stream", "mt_profile_enable", "mt_profile_read", "mt_profile_timeline", "mt_destroy", "mt_last_error", "mt_debug_inject", "mt_debug_inject_global",
     "mt_host_adam", "mt_host_adam_slab", "mt_host_to_bf16",
-    "mt_k_gemm", "mt_k_gemm_ex", "mt_k_gemm_rope", "mt_k_gemm_swiglu_fwd", "mt_k_gemm_swiglu_bwd", "mt_k_gemm_wgrad", "mt_k_gemm_splitk", "mt_k_gemm_tile_policy", "mt_k_gemm_wgrad_ws", "mt_k_transpose", "mt_k_rmsnorm_fwd", "mt_k_rmsnorm_bwd", "mt_k_rmsnorm_bwd_parts",
+    "mt_k_gemm", "mt_k_gemm_ex", "mt_k_gemm_rope", "mt_k_gemm_swiglu_fwd", "mt_k_gemm_swiglu_bwd", "mt_k_gemm_wgrad", "mt_k_gemm_splitk", "mt_k_gemm_tile_policy", "mt_k_gemm_wgrad_ws", "mt_k_rmsnorm_fwd", "mt_k_rmsnorm_bwd", "mt_k_rmsnorm_bwd_parts",
     "mt_k_rope", "mt_k_swiglu_fwd", "mt_k_swiglu_bwd", "mt_k_attn_fwd", "mt_k_attn_fwd_mma", "mt_k_attn_bwd", "mt_k_attn_bwd_mma",
     "mt_k_cross_entropy", "mt_k_sum", "mt_k_embedding_fwd", "mt_k_embedding_bwd",
     "mt_k_embedding_bwd_work", "mt_k_check_ids", "mt_k_device_error",
@@ -127,7 +127,6 @@ def lib():
         "mt_k_gemm_splitk": ([I, I, I], I),
         "mt_k_gemm_tile_policy": ([I], I),
         "mt_k_gemm_wgrad_ws": ([I, I], I64),
-        "mt_k_transpose": ([P, I64, P, I64, I, I, P], I),
         "mt_k_rmsnorm_fwd": ([P, P, P, P, I, I, F, P], I),
         "mt_k_rmsnorm_bwd": ([P, P, P, P, P, P, P, P, P, I, I, P], I),
         "mt_k_rmsnorm_bwd_parts": ([I], I),
@@ -400,11 +399,6 @@ def k_gemm_ex(A, a_mn, B, b_mn, Cout, R=None, stream=None):
     f32 = 1 if Cout.dtype == torch.float32 else 0
     check(lib().mt_k_gemm_ex(_dp(A), A.stride(0), 1 if a_mn else 0, _dp(B), B.stride(0), 1 if b_mn else 0, _dp(Cout),
                              Cout.stride(0), f32, _dp(R), R.stride(0) if R is not None else 0, M, N, K, _st(stream)))
-
-
-def k_transpose(x, out, stream=None):
-    rows, cols = x.shape
-    check(lib().mt_k_transpose(_dp(x), x.stride(0), _dp(out), out.stride(0), rows, cols, _st(stream)))
 
 
 def k_rmsnorm_fwd(x, w, y, rstd, eps, stream=None):

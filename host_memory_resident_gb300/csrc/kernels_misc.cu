@@ -1,5 +1,5 @@
 // Memory-bound kernels of the stateless layer template: RMSNorm, RoPE,
-// SwiGLU, transpose, embedding gather / deterministic scatter-add, cross
+// SwiGLU, embedding gather / deterministic scatter-add, cross
 // entropy, fixed-order sums. Each is a plain streaming pass with 16-byte
 // vector accesses where the layout allows; their cost is HBM bandwidth.
 // The operators are those of a Llama-style decoder layer run through the
@@ -331,32 +331,6 @@ __global__ void swiglu_bwd_kernel(const bf16* __restrict__ da, const bf16* __res
   store_bf16x8(o + f, du);
 }
 
-// ------------------------------------------------------------- transpose
-constexpr int kTT = 64;
-__global__ void transpose_kernel(const bf16* __restrict__ in, long long ld_in, bf16* __restrict__ out,
-                                 long long ld_out, int rows, int cols) {
-  __shared__ bf16 tile[kTT][kTT + 2];
-  const int c0 = blockIdx.x * kTT, r0 = blockIdx.y * kTT;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
-  for (int i = ty; i < kTT; i += 8) {
-    const int r = r0 + i;
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int c = c0 + tx + 32 * j;
-      tile[i][tx + 32 * j] = (r < rows && c < cols) ? in[(long long)r * ld_in + c] : __float2bfloat16_rn(0.f);
-    }
-  }
-  __syncthreads();
-  for (int i = ty; i < kTT; i += 8) {
-    const int c = c0 + i;
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int r = r0 + tx + 32 * j;
-      if (c < cols && r < rows) out[(long long)c * ld_out + r] = tile[tx + 32 * j][i];
-    }
-  }
-}
-
 // ------------------------------------------------------------- embedding
 __global__ void embedding_fwd_kernel(const bf16* __restrict__ E, const int32_t* __restrict__ tok, bf16* __restrict__ x,
                                      int M, int d, int V, int* err) {
@@ -636,14 +610,6 @@ int mt_k_gemm_tile_policy(int policy) { return gemm_tile_policy(policy); }
 int mt_k_gemm_splitk(int M, int N, int K) { return (M <= 0 || N <= 0 || K <= 0) ? 1 : splitk_factor(M, N, K); }
 
 int64_t mt_k_gemm_wgrad_ws(int M, int N) { return (M <= 0 || N <= 0) ? 0 : (int64_t)splitk_ws_elems(M, N); }
-
-int mt_k_transpose(const void* in, int64_t ld_in, void* out, int64_t ld_out, int rows, int cols, void* stream) {
-  if (rows < 0 || cols < 0 || ld_in < cols || ld_out < rows) return MT_EINVAL;
-  if (rows == 0 || cols == 0) return MT_OK;
-  dim3 grid((cols + kTT - 1) / kTT, (rows + kTT - 1) / kTT);
-  transpose_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>((const bf16*)in, ld_in, (bf16*)out, ld_out, rows, cols);
-  return launch_ok();
-}
 
 int mt_k_rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int M, int d, float eps, void* stream) {
   if (M < 0 || d <= 0 || d % 8 || !al16(x) || !al16(w) || !al16(y)) return MT_EINVAL;

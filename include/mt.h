@@ -104,7 +104,7 @@ typedef struct mt_stats {
 #define MT_PROF_NORM 3
 #define MT_PROF_ROPE 4
 #define MT_PROF_SWIGLU 5
-#define MT_PROF_TRANSPOSE 6
+#define MT_PROF_RESERVED 6  /* no kernel of the step falls in this class */
 #define MT_PROF_CE 7
 #define MT_PROF_EMBED 8
 #define MT_PROF_OTHER 9

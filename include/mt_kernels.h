@@ -116,9 +116,6 @@ int mt_k_gemm_splitk(int M, int N, int K);
 /* fp32 workspace elements mt_k_gemm_wgrad may use for G [M, N] at any K. */
 int64_t mt_k_gemm_wgrad_ws(int M, int N);
 
-/* out[c, r] = in[r, c] for a bf16 [rows, cols] matrix (ld_in >= cols, ld_out >= rows). */
-int mt_k_transpose(const void* in, int64_t ld_in, void* out, int64_t ld_out, int rows, int cols, void* stream);
-
 /*
  * RMSNorm forward: y[m,:] = x[m,:] * rstd[m] * w, rstd = 1/sqrt(mean(x^2)+eps).
  * x, y bf16 [M, d] (ld = d), w bf16 [d], rstd fp32 [M]. d multiple of 8.

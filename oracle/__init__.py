@@ -25,7 +25,8 @@ out, with two structural knobs kept so their invariance can be tested:
 ``ckpt_interval`` (segment recompute) and ``streamed`` (weights copied into a
 two-slot scratch before use). Readings of points the articles leave open
 (flat order, RoPE convention, loss normalisation, init, Adam constants) are
-listed in ``oracle/readings.py``.
+stated in the docstring of the function that takes them (``layout``,
+``ops``, ``adam``).
 
 Pins (tests marked ``not gpu``): central finite differences of the whole
 step, comparison with torch autograd built from torch library ops, closed

@@ -1,18 +1,38 @@
-"""The oracle's step with bf16 rounding at the device's storage points.
+"""The oracle's step with bf16 rounding at chosen storage points.
 
-TEST INFRASTRUCTURE ONLY, used to derive tolerances, never as a reference
+TEST INFRASTRUCTURE ONLY, used to study tolerances, never as a reference
 for parity. The method computes on bf16 copies of the weights and gradients
 with an FP32 optimizer state (zhichai.net article, introduction: mixed
-precision with bf16 weights and gradients, FP32 optimizer state); any such
-implementation stores bf16 values at fixed points of the layer (weights,
-normalised activations, q/k/v, attention output, gate/up pre-activations,
-SwiGLU output, the residual stream, gradient operands, softmax and dS
-operands of attention, gradient slabs). This module evaluates the plain
-definition of the step (the same operators as ``oracle.ops``) and rounds the
-value to bf16 at exactly those points, in float64 otherwise. The distance
-between its gradients and the exact oracle's is the error floor that bf16
-storage alone imposes on the step; it says nothing about any kernel's
-arithmetic order and shares no code with the CUDA library.
+precision with bf16 weights and gradients, FP32 optimizer state). A bf16
+implementation of the step stores bf16 values at some fixed points of the
+layer; this module evaluates the plain definition of the step (the same
+operators as ``oracle.ops``, in float64) and rounds the value to bf16 at the
+points named in ``points`` only. Each point can be switched on or off on its
+own, so the error that each storage point alone adds to every gradient
+tensor can be measured against the exact oracle. With no point switched on
+the step is the exact one (equal to ``oracle.step_grads`` up to float64
+rounding order). It says nothing about any kernel's arithmetic order and
+shares no code with the CUDA library.
+
+Storage points (``POINTS``):
+
+* ``norm_out``   outputs of the three RMSNorms (u, z, final x-hat): operands
+                 of the following projections;
+* ``qkv``        the QKV projection's output and the rotated q, k: operands
+                 of the attention products;
+* ``attn_p``     the softmax weights as an operand of P V (forward: the
+                 unnormalised exponentials) and of P^T dO (backward);
+* ``attn_ds``    dS as an operand of dS K and dS^T Q;
+* ``attn_out``   the attention output O: operand of the output projection
+                 and of the backward's rowsum(dO * O);
+* ``residual``   the residual stream h = x + O Wo^T, y = h + a Wdown^T (and
+                 so the layer inputs and checkpoints);
+* ``gate_up``    the gate/up projection's output;
+* ``swiglu_out`` a = silu(gate) * up: operand of the down projection;
+* ``grad_operands`` the output-side gradients fed to the input- and
+                 weight-gradient products (dz of the head, dy, da, d(gate|up),
+                 dh, dO, dqkv);
+* ``grad_slab``  every weight gradient as written (the bf16 gradient slab).
 """
 from __future__ import annotations
 
@@ -20,6 +40,9 @@ import numpy as np
 
 from . import ops
 from .layout import build_layout
+
+POINTS = ("norm_out", "qkv", "attn_p", "attn_ds", "attn_out", "residual", "gate_up",
+          "swiglu_out", "grad_operands", "grad_slab")
 
 
 def to_bf16(x):
@@ -32,7 +55,14 @@ def to_bf16(x):
     return out.astype(np.float64)
 
 
-def _attn_fwd(q, k, v, R):
+def _identity(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+def _attn_fwd(q, k, v, Rp):
+    """Causal softmax attention; the unnormalised weights pass through Rp
+    before the P V product and the row sum divides afterwards (a bf16
+    implementation cannot store P/den without a second pass)."""
     B, s, H, hd = q.shape
     grp = H // k.shape[2]
     o = np.zeros_like(q)
@@ -45,12 +75,13 @@ def _attn_fwd(q, k, v, R):
             mx = sc.max(1, keepdims=True)
             e = np.exp(sc - mx)
             den = e.sum(1, keepdims=True)
-            o[b, :, h] = (R(e) @ v[b, :, g]) / den      # unnormalised P is a bf16 operand
+            o[b, :, h] = (Rp(e) @ v[b, :, g]) / den
             lse[b, h] = (mx + np.log(den))[:, 0]
     return o, lse
 
 
-def _attn_bwd(q, k, v, o, lse, do, R):
+def _attn_bwd(q, k, v, o, lse, do, Rp, Rds):
+    """Gradients of _attn_fwd from the saved log-sum-exp; delta = rowsum(dO * O)."""
     B, s, H, hd = q.shape
     grp = H // k.shape[2]
     dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
@@ -60,20 +91,32 @@ def _attn_bwd(q, k, v, o, lse, do, R):
             g = h // grp
             sc = (q[b, :, h] @ k[b, :, g].T) / np.sqrt(hd)
             p = np.where(mask, 0.0, np.exp(sc - lse[b, h][:, None]))
-            D = np.sum(do[b, :, h] * o[b, :, h], axis=1, keepdims=True)   # rowsum(dO * O)
+            D = np.sum(do[b, :, h] * o[b, :, h], axis=1, keepdims=True)
             ds = p * (do[b, :, h] @ v[b, :, g].T - D)
-            pb, dsb = R(p), R(ds)
+            pb, dsb = Rp(p), Rds(ds)
             dv[b, :, g] += pb.T @ do[b, :, h]
             dq[b, :, h] = (dsb @ k[b, :, g]) / np.sqrt(hd)
             dk[b, :, g] += (dsb.T @ q[b, :, h]) / np.sqrt(hd)
     return dq, dk, dv
 
 
-def step_grads_bf16_storage(shape, master, tokens, labels):
-    """Loss and flat gradient of one step with bf16 storage points (float64)."""
-    R = to_bf16
+def step_grads_bf16_storage(shape, master, tokens, labels, points=POINTS):
+    """Loss and flat gradient (float64) of one step at the bf16 values of
+    ``master``, rounding to bf16 at the storage points in ``points``."""
+    points = frozenset(points)
+    unknown = points - frozenset(POINTS)
+    if unknown:
+        raise ValueError(f"unknown storage points {sorted(unknown)}")
+
+    def rnd(name):
+        return to_bf16 if name in points else _identity
+
+    Rn, Rq, Rp, Rds = rnd("norm_out"), rnd("qkv"), rnd("attn_p"), rnd("attn_ds")
+    Ro, Rh, Rgu, Ra = rnd("attn_out"), rnd("residual"), rnd("gate_up"), rnd("swiglu_out")
+    Rg, Rs = rnd("grad_operands"), rnd("grad_slab")
+
     lay = build_layout(shape)
-    W = R(master)
+    W = to_bf16(master)
     B, s = tokens.shape
     H, Hkv, hd, f = shape.n_heads, shape.n_kv_heads, shape.head_dim, shape.ffn_dim
     cos, sin = ops.rope_tables(s, hd, shape.rope_theta)
@@ -85,59 +128,59 @@ def step_grads_bf16_storage(shape, master, tokens, labels):
 
     def put(u, name, g):
         t = next(t for t in lay.units[u].tensors if t.name == name)
-        grad[t.offset:t.offset + t.size] = R(g).reshape(-1)      # bf16 gradient slab
+        grad[t.offset:t.offset + t.size] = Rs(g).reshape(-1)
 
-    x = R(P(0)["embed"][tokens.reshape(-1)])
+    x = P(0)["embed"][tokens.reshape(-1)]          # bf16 weights: exact either way
     caches = []
     for layer in range(shape.n_layers):
         p = P(1 + layer)
         M = x.shape[0]
         u, r1 = ops.rmsnorm_fwd(x, p["attn_norm"], shape.rms_eps)
-        u = R(u)
-        qkv = R(u @ p["wqkv"].T)
+        u = Rn(u)
+        qkv = Rq(u @ p["wqkv"].T)
         q = qkv[:, :H * hd].reshape(B, s, H, hd)
         k = qkv[:, H * hd:(H + Hkv) * hd].reshape(B, s, Hkv, hd)
         v = qkv[:, (H + Hkv) * hd:].reshape(B, s, Hkv, hd)
-        qr, kr = R(ops.rope_fwd(q, cos, sin)), R(ops.rope_fwd(k, cos, sin))
-        o, lse = _attn_fwd(qr, kr, v, R)
-        o2 = R(o.reshape(M, -1))
-        h = R(x + o2 @ p["wo"].T)
+        qr, kr = Rq(ops.rope_fwd(q, cos, sin)), Rq(ops.rope_fwd(k, cos, sin))
+        o, lse = _attn_fwd(qr, kr, v, Rp)
+        o2 = Ro(o.reshape(M, -1))
+        h = Rh(x + o2 @ p["wo"].T)
         z, r2 = ops.rmsnorm_fwd(h, p["mlp_norm"], shape.rms_eps)
-        z = R(z)
-        gu = R(z @ p["wgu"].T)
+        z = Rn(z)
+        gu = Rgu(z @ p["wgu"].T)
         g_, up = gu[:, :f], gu[:, f:]
-        a = R(ops.swiglu_fwd(g_, up))
-        y = R(h + a @ p["wdown"].T)
+        a = Ra(ops.swiglu_fwd(g_, up))
+        y = Rh(h + a @ p["wdown"].T)
         caches.append(dict(x=x, u=u, r1=r1, qr=qr, kr=kr, v=v, o2=o2, lse=lse, h=h, z=z, r2=r2, g=g_, up=up,
                            a=a))
         x = y
     ph = P(shape.n_layers + 1)
     xh, rf = ops.rmsnorm_fwd(x, ph["final_norm"], shape.rms_eps)
-    xh = R(xh)
+    xh = Rn(xh)
     loss, dz = ops.cross_entropy_fwd_bwd(xh @ ph["head"].T, labels.reshape(-1))
-    dz = R(dz)
+    dz = Rg(dz)
     put(shape.n_layers + 1, "head", dz.T @ xh)
     dx, dfin = ops.rmsnorm_bwd(dz @ ph["head"], x, ph["final_norm"], rf)
     put(shape.n_layers + 1, "final_norm", dfin)
     for layer in reversed(range(shape.n_layers)):
         c, p = caches[layer], P(1 + layer)
         M = dx.shape[0]
-        dyb = R(dx)
+        dyb = Rg(dx)
         put(1 + layer, "wdown", dyb.T @ c["a"])
-        da = R(dyb @ p["wdown"])
+        da = Rg(dyb @ p["wdown"])
         dg, dup = ops.swiglu_bwd(da, c["g"], c["up"])
-        dgu = R(np.concatenate([dg, dup], 1))
+        dgu = Rg(np.concatenate([dg, dup], 1))
         put(1 + layer, "wgu", dgu.T @ c["z"])
         dhn, dmlp = ops.rmsnorm_bwd(dgu @ p["wgu"], c["h"], p["mlp_norm"], c["r2"])
         put(1 + layer, "mlp_norm", dmlp)
         dh = dx + dhn
-        dhb = R(dh)
+        dhb = Rg(dh)
         put(1 + layer, "wo", dhb.T @ c["o2"])
-        do = R(dhb @ p["wo"])
+        do = Rg(dhb @ p["wo"])
         dq, dk, dv = _attn_bwd(c["qr"], c["kr"], c["v"], c["o2"].reshape(B, s, H, hd), c["lse"],
-                               do.reshape(B, s, H, hd), R)
+                               do.reshape(B, s, H, hd), Rp, Rds)
         dq, dk = ops.rope_bwd(dq, cos, sin), ops.rope_bwd(dk, cos, sin)
-        dqkv = R(np.concatenate([dq.reshape(M, -1), dk.reshape(M, -1), dv.reshape(M, -1)], 1))
+        dqkv = Rg(np.concatenate([dq.reshape(M, -1), dk.reshape(M, -1), dv.reshape(M, -1)], 1))
         put(1 + layer, "wqkv", dqkv.T @ c["u"])
         dxn, dan = ops.rmsnorm_bwd(dqkv @ p["wqkv"], c["x"], p["attn_norm"], c["r1"])
         put(1 + layer, "attn_norm", dan)

@@ -61,3 +61,33 @@ def test_bench_refuses_workloads_beyond_host_memory():
     assert bench.host_memory_refusal(mt, mt.make_config(small), small, True, avail) is None
     # unknown available memory: no refusal
     assert bench.host_memory_refusal(mt, mt.make_config(big), big, True, None) is None
+
+
+def test_default_workload_fits_the_host():
+    """The bench's default workload (7B: about 126 GB of host state and
+    pinned buffers) fits 199 GB of host memory."""
+    import bench
+    import host_memory_resident_gb300 as mt
+    import synth
+    sh = synth.workload("7b")
+    assert bench.host_memory_refusal(mt, mt.make_config(sh), sh, True, 199 * 2**30) is None
+
+
+def test_reference_arm_line_carries_the_repo_arms_config(capsys):
+    """Both arms describe the workload with the same config dict, so their
+    lines compare like for like; run here on the tiny workload."""
+    import json
+
+    import bench
+    import oracle
+    import synth
+
+    class A:
+        gpus, steps, warmup = 1, 1, 0
+        overlap, keep_grads, unfused, keep_attention = True, True, False, False
+    sh = synth.workload("tiny")
+    assert bench.run_reference(A, sh, 1, 0, None) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    assert line["config"] == bench.config_dict(A, sh, 1, oracle.build_layout(sh).n_total)
+    assert line["e2e"]["value"] == line["value"] and line["cpu_baseline"]["kind"] == "oracle"
