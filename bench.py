@@ -753,7 +753,9 @@ def run_ours(args, shape, world, rank, local, pg):
         "wall_s_timed": wall,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cb = oracle_sample(shape)
+        # about 10-30 s of host work: sequences longer than 2048 tokens (1024
+        # from d = 4096 up) are timed at half and full budget and extrapolated
+        cb = oracle_sample(shape, max_tokens=2048 if shape.d_model < 4096 else 1024)
         line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
     if rank == 0:
         print(json.dumps(line), flush=True)
