@@ -127,8 +127,8 @@ def lib():
         "mt_k_gemm_splitk": ([I, I, I], I),
         "mt_k_gemm_tile_policy": ([I], I),
         "mt_k_gemm_wgrad_ws": ([I, I], I64),
-        "mt_k_rmsnorm_fwd": ([P, P, P, P, I, I, F, P], I),
-        "mt_k_rmsnorm_bwd": ([P, P, P, P, P, P, P, P, P, I, I, P], I),
+        "mt_k_rmsnorm_fwd": ([P, I, P, P, P, I, I, F, P], I),
+        "mt_k_rmsnorm_bwd": ([P, P, I, P, P, P, P, P, P, P, I, I, P], I),
         "mt_k_rmsnorm_bwd_parts": ([I], I),
         "mt_k_rope": ([P, I64, I, I, I, I, P, P, I, P], I),
         "mt_k_swiglu_fwd": ([P, P, I, I, P], I),
@@ -139,7 +139,7 @@ def lib():
         "mt_k_attn_bwd_mma": ([P, I64, P, I64, P, I64, P, P, P, I64, I, I, I, I, I, P], I),
         "mt_k_cross_entropy": ([P, I64, P, P, I64, P, I, I, F, P], I),
         "mt_k_sum": ([P, I, P, P], I),
-        "mt_k_embedding_fwd": ([P, P, P, I, I, I, P], I),
+        "mt_k_embedding_fwd": ([P, P, P, I, I, I, I, P], I),
         "mt_k_embedding_bwd": ([P, P, P, I, I, I, P, P], I),
         "mt_k_embedding_bwd_work": ([I, I], I64),
         "mt_k_check_ids": ([P, I, I, P, P], I),
@@ -381,7 +381,8 @@ def _st(stream):
 
 
 def k_gemm(A, B, Cout, R=None, stream=None):
-    """Cout = A @ B.T (+ R). A [M,K], B [N,K] bf16; Cout bf16 or fp32 [M,N]."""
+    """Cout = A @ B.T (+ R). A [M,K], B [N,K] bf16; Cout bf16 or fp32 [M,N];
+    R (optional) of Cout's dtype."""
     import torch
     M, K = A.shape
     N = B.shape[0]
@@ -401,9 +402,15 @@ def k_gemm_ex(A, a_mn, B, b_mn, Cout, R=None, stream=None):
                              Cout.stride(0), f32, _dp(R), R.stride(0) if R is not None else 0, M, N, K, _st(stream)))
 
 
+def _is_f32(t):
+    import torch
+    return 1 if t.dtype == torch.float32 else 0
+
+
 def k_rmsnorm_fwd(x, w, y, rstd, eps, stream=None):
+    """x bf16 or fp32 [M, d]; y bf16."""
     M, d = x.shape
-    check(lib().mt_k_rmsnorm_fwd(_dp(x), _dp(w), _dp(y), _dp(rstd), M, d, eps, _st(stream)))
+    check(lib().mt_k_rmsnorm_fwd(_dp(x), _is_f32(x), _dp(w), _dp(y), _dp(rstd), M, d, eps, _st(stream)))
 
 
 def k_rmsnorm_bwd_parts(M):
@@ -412,8 +419,8 @@ def k_rmsnorm_bwd_parts(M):
 
 def k_rmsnorm_bwd(dy, x, w, rstd, dres, dx32, dxb, partial, dw, stream=None):
     M, d = x.shape
-    check(lib().mt_k_rmsnorm_bwd(_dp(dy), _dp(x), _dp(w), _dp(rstd), _dp(dres), _dp(dx32), _dp(dxb), _dp(partial),
-                                 _dp(dw), M, d, _st(stream)))
+    check(lib().mt_k_rmsnorm_bwd(_dp(dy), _dp(x), _is_f32(x), _dp(w), _dp(rstd), _dp(dres), _dp(dx32), _dp(dxb),
+                                 _dp(partial), _dp(dw), M, d, _st(stream)))
 
 
 def k_gemm_rope(A, B, Cout, cos_t, sin_t, rot_cols, hd, seq, stream=None):
@@ -505,8 +512,9 @@ def k_sum(x, out, stream=None):
 
 
 def k_embedding_fwd(E, tok, x, stream=None):
+    """x bf16 or fp32 [M, d]."""
     V, d = E.shape
-    check(lib().mt_k_embedding_fwd(_dp(E), _dp(tok), _dp(x), tok.numel(), d, V, _st(stream)))
+    check(lib().mt_k_embedding_fwd(_dp(E), _dp(tok), _dp(x), _is_f32(x), tok.numel(), d, V, _st(stream)))
 
 
 def k_embedding_bwd_work(M, V):

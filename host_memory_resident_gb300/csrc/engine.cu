@@ -85,15 +85,19 @@ T* take(Arena& a, size_t n) {
   return reinterpret_cast<T*>(a.take(sizeof(T) * (n ? n : 1)));
 }
 
-// Activations saved for one layer's backward.
+// Activations saved for one layer's backward. The residual stream (layer
+// input x, h, the checkpoints) is fp32: the method's bf16 storage is that of
+// the weights, gradients and the operands of the products, and the stream
+// itself is no operand (rounding it to bf16 twice per layer compounds with
+// depth).
 struct Saved {
-  bf16* x;     // layer input [M, d]
+  float* x;    // layer input [M, d] (fp32 residual stream)
   bf16* u;     // attention-norm output [M, d]
   float* r1;   // its rstd [M]
   bf16* qkv;   // q, k (after RoPE), v [M, qkvN]
   bf16* o;     // attention output [M, hq]
   float* lse;  // [B, H, s]
-  bf16* h;     // after attention residual [M, d]
+  float* h;    // after attention residual [M, d] (fp32)
   bf16* z;     // mlp-norm output [M, d]
   float* r2;   // [M]
   bf16* gu;    // gate | up [M, 2f]
@@ -143,8 +147,8 @@ struct mt_handle {
   std::vector<mt::bf16*> slab;
   int32_t *d_tok = nullptr, *d_lab = nullptr, *d_flag = nullptr, *d_ework = nullptr;
   float *cos_t = nullptr, *sin_t = nullptr;
-  mt::bf16 *xa = nullptr, *xb = nullptr;
-  std::vector<mt::bf16*> ckpt;
+  float *xa = nullptr, *xb = nullptr;   // fp32 residual stream between checkpoints
+  std::vector<float*> ckpt;             // fp32 layer inputs, one per segment
   std::vector<mt::Saved> saved;
   // keep_attention: every layer's attention output and log-sum-exp from the
   // forward, so the backward's recompute skips the attention core
@@ -479,8 +483,8 @@ struct Step {
 
   // C[M,N] = A[M,K] * B[N,K]^T (+R)
   void gemm(const bf16* A, long long lda, const bf16* Bm, long long ldb, void* C, long long ldc, bool f32,
-            const bf16* R, long long ldr, int m, int n, int k) {
-    const double bytes = 2.0 * ((double)m * k + (double)n * k) + (f32 ? 4.0 : 2.0) * m * n + (R ? 2.0 * m * n : 0.0);
+            const void* R, long long ldr, int m, int n, int k) {
+    const double bytes = 2.0 * ((double)m * k + (double)n * k) + (f32 ? 4.0 : 2.0) * m * n * (R ? 2.0 : 1.0);
     KP(MT_PROF_GEMM, 1, 2.0 * m * n * k, bytes,
        gemm_abt(A, lda, Bm, ldb, C, ldc, f32 ? 1 : 0, R, ldr, m, n, k, cs()));
   }
@@ -504,8 +508,10 @@ struct Step {
     const double per = 2.0 * B * (double)h->H * s * (double)s * h->hd / 2.0;
     return (bwd ? 5.0 : 2.0) * per;
   }
-  double norm_fwd_bytes() const { return 4.0 * M * h->d + 4.0 * M; }
-  double norm_bwd_bytes(bool res) const { return (4.0 + 2.0 + 4.0 + 2.0 + (res ? 4.0 : 0.0)) * M * h->d; }
+  // fp32 x in, bf16 y out (+ rstd); backward: fp32 dy and x in, fp32 and
+  // bf16 dx out (+ the fp32 residual-branch gradient in)
+  double norm_fwd_bytes() const { return 6.0 * M * h->d + 4.0 * M; }
+  double norm_bwd_bytes(bool res) const { return (4.0 + 4.0 + 4.0 + 2.0 + (res ? 4.0 : 0.0)) * M * h->d; }
   double rope_bytes() const { return 4.0 * M * (h->H + h->Hkv) * h->hd; }
   // RoPE and SwiGLU go into the GEMM epilogues unless the configuration asks
   // for the separate kernels or a shape does not fit the fused forms.
@@ -518,10 +524,11 @@ struct Step {
   // With keep_attention, S.o / S.lse point at layer l's kept tensors; the
   // forward writes them and a recompute reads them instead of re-running the
   // attention (the same values, so the step's results are unchanged).
-  void layer_fwd(const bf16* W, const Saved& S, bf16* x_out, bool recompute = false) {
+  void layer_fwd(const bf16* W, const Saved& S, float* x_out, bool recompute = false) {
     const LayerOffsets& o = h->lay.layer;
     const int d = h->d, f = h->f;
-    KP(MT_PROF_NORM, 1, 0.0, norm_fwd_bytes(), mt_k_rmsnorm_fwd(S.x, W + o.attn_norm, S.u, S.r1, M, d, h->cfg.rms_eps, cs()));
+    KP(MT_PROF_NORM, 1, 0.0, norm_fwd_bytes(),
+       mt_k_rmsnorm_fwd(S.x, 1, W + o.attn_norm, S.u, S.r1, M, d, h->cfg.rms_eps, cs()));
     if (fuse_rope()) {
       const int qn = h->qkvN;
       const double bytes = 2.0 * ((double)M * d + (double)qn * d + (double)M * qn) + 8.0 * s * (h->hd / 2);
@@ -536,8 +543,10 @@ struct Step {
     if (!(recompute && h->cfg.keep_attention))
       KP(MT_PROF_ATTN_FWD, 1, attn_flops(false), 0.0,
          mt_k_attn_fwd(S.qkv, h->qkvN, S.o, h->hq, S.lse, B, s, h->H, h->Hkv, h->hd, cs()));
-    gemm(S.o, h->hq, W + o.wo, h->hq, S.h, d, false, S.x, d, M, d, h->hq);
-    KP(MT_PROF_NORM, 1, 0.0, norm_fwd_bytes(), mt_k_rmsnorm_fwd(S.h, W + o.mlp_norm, S.z, S.r2, M, d, h->cfg.rms_eps, cs()));
+    // h = x + o Wo^T and x_out = h + a Wdown^T stay fp32
+    gemm(S.o, h->hq, W + o.wo, h->hq, S.h, d, true, S.x, d, M, d, h->hq);
+    KP(MT_PROF_NORM, 1, 0.0, norm_fwd_bytes(),
+       mt_k_rmsnorm_fwd(S.h, 1, W + o.mlp_norm, S.z, S.r2, M, d, h->cfg.rms_eps, cs()));
     if (fuse_swiglu_fwd()) {
       const double bytes = 2.0 * ((double)M * d + 2.0 * f * d + 2.0 * M * f + (double)M * f);
       KP(MT_PROF_GEMM, 1, 2.0 * M * (2.0 * f) * d, bytes,
@@ -546,7 +555,7 @@ struct Step {
       gemm(S.z, d, W + o.wgu, d, S.gu, 2 * f, false, nullptr, 0, M, 2 * f, d);
       KP(MT_PROF_SWIGLU, 1, 0.0, 6.0 * M * f, mt_k_swiglu_fwd(S.gu, S.a, M, f, cs()));
     }
-    gemm(S.a, f, W + o.wdown, f, x_out, d, false, S.h, d, M, d, f);
+    gemm(S.a, f, W + o.wdown, f, x_out, d, true, S.h, d, M, d, f);
   }
 
   // Backward of one layer: reads dx32/dxb (gradient w.r.t. the layer output),
@@ -573,7 +582,7 @@ struct Step {
     gemm_wg(h->dgu, 2 * f, S.z, d, g + o.wgu, d, 2 * f, d);
     gemm_mn(h->dgu, 2 * f, false, W + o.wgu, d, true, h->dn32, d, true, M, d, 2 * f);
     KP(MT_PROF_NORM, 2, 0.0, norm_bwd_bytes(true),
-       mt_k_rmsnorm_bwd(h->dn32, S.h, W + o.mlp_norm, S.r2, h->dx32, h->dh32, h->dhb, h->npart, g + o.mlp_norm, M,
+       mt_k_rmsnorm_bwd(h->dn32, S.h, 1, W + o.mlp_norm, S.r2, h->dx32, h->dh32, h->dhb, h->npart, g + o.mlp_norm, M,
                         d, cs()));
     // output projection
     gemm_wg(h->dhb, d, S.o, hq, g + o.wo, hq, d, hq);
@@ -586,16 +595,16 @@ struct Step {
     gemm_wg(h->dqkv, qn, S.u, d, g + o.wqkv, d, qn, d);
     gemm_mn(h->dqkv, qn, false, W + o.wqkv, d, true, h->dn32, d, true, M, d, qn);
     KP(MT_PROF_NORM, 2, 0.0, norm_bwd_bytes(true),
-       mt_k_rmsnorm_bwd(h->dn32, S.x, W + o.attn_norm, S.r1, h->dh32, h->dx32, h->dxb, h->npart, g + o.attn_norm, M,
+       mt_k_rmsnorm_bwd(h->dn32, S.x, 1, W + o.attn_norm, S.r1, h->dh32, h->dx32, h->dxb, h->npart, g + o.attn_norm, M,
                         d, cs()));
   }
 
   // Final norm, logits, cross entropy and their backward (head unit).
-  void head(const bf16* W, const bf16* xL, bf16* g) {
+  void head(const bf16* W, const float* xL, bf16* g) {
     const int d = h->d, V = h->V;
     const bf16* wf = W + h->lay.final_norm;
     const bf16* head = W + h->lay.head;
-    KP(MT_PROF_NORM, 1, 0.0, norm_fwd_bytes(), mt_k_rmsnorm_fwd(xL, wf, h->xh, h->rf, M, d, h->cfg.rms_eps, cs()));
+    KP(MT_PROF_NORM, 1, 0.0, norm_fwd_bytes(), mt_k_rmsnorm_fwd(xL, 1, wf, h->xh, h->rf, M, d, h->cfg.rms_eps, cs()));
     const float scale = 1.f / (float)M;
     for (int r0 = 0; r0 < M; r0 += h->Mchunk) {
       const int mc = std::min(h->Mchunk, M - r0);
@@ -611,7 +620,7 @@ struct Step {
     gemm_wg(h->dz, V, h->xh, d, g + h->lay.head, d, V, d);
     gemm_mn(h->dz, V, false, head, d, true, h->dn32, d, true, M, d, V);
     KP(MT_PROF_NORM, 2, 0.0, norm_bwd_bytes(false),
-       mt_k_rmsnorm_bwd(h->dn32, xL, wf, h->rf, nullptr, h->dx32, h->dxb, h->npart, g + h->lay.final_norm, M, d,
+       mt_k_rmsnorm_bwd(h->dn32, xL, 1, wf, h->rf, nullptr, h->dx32, h->dxb, h->npart, g + h->lay.final_norm, M, d,
                         cs()));
   }
 
@@ -646,17 +655,17 @@ struct Step {
     {
       bf16* E = acquire(0);
       KP(MT_PROF_EMBED, 1, 0.0, 4.0 * M * hh.d,
-         mt_k_embedding_fwd(E + (hh.lay.embed - hh.lay.unit_off[0]), hh.d_tok, hh.ckpt[0], M, hh.d, hh.V, cs()));
+         mt_k_embedding_fwd(E + (hh.lay.embed - hh.lay.unit_off[0]), hh.d_tok, hh.ckpt[0], 1, M, hh.d, hh.V, cs()));
       release();
     }
     // The last segment's layers keep their activations in the saved sets,
     // exactly where its recompute would put them, so the backward starts on
     // that segment without recomputing it.
     const int last_a = (hh.nseg - 1) * C;
-    bf16* x = hh.ckpt[0];
+    float* x = hh.ckpt[0];
     for (int l = 0; l < L; ++l) {
       bf16* W = acquire(1 + l);
-      bf16* out;
+      float* out;
       if (l >= last_a) {
         Saved& S = hh.saved[l - last_a];
         if (l == last_a) S.x = hh.ckpt[hh.nseg - 1];
@@ -698,7 +707,7 @@ struct Step {
           S.o = hh.att_o[l];
           S.lse = hh.att_lse[l];
         }
-        bf16* out = (l + 1 < b) ? hh.saved[l + 1 - a].x : hh.xa;
+        float* out = (l + 1 < b) ? hh.saved[l + 1 - a].x : hh.xa;
         layer_fwd(W, S, out, true);
         release();
       }
@@ -771,21 +780,21 @@ void plan_device(mt_handle* h, Arena& A) {
   h->d_ework = take<int32_t>(A, (size_t)mt_k_embedding_bwd_work((int)M, (int)V));
   h->cos_t = take<float>(A, (size_t)h->cfg.max_seq * (h->hd / 2));
   h->sin_t = take<float>(A, (size_t)h->cfg.max_seq * (h->hd / 2));
-  h->xa = take<bf16>(A, M * d);
-  h->xb = take<bf16>(A, M * d);
+  h->xa = take<float>(A, M * d);
+  h->xb = take<float>(A, M * d);
   h->ckpt.assign(h->nseg, nullptr);
-  for (auto& p : h->ckpt) p = take<bf16>(A, M * d);
+  for (auto& p : h->ckpt) p = take<float>(A, M * d);
   const int slots = std::min(h->cfg.ckpt_interval, h->L);
   h->saved.assign(slots, Saved{});
   for (int i = 0; i < slots; ++i) {
     Saved& S = h->saved[i];
-    S.x = take<bf16>(A, M * d);
+    S.x = take<float>(A, M * d);
     S.u = take<bf16>(A, M * d);
     S.r1 = take<float>(A, M);
     S.qkv = take<bf16>(A, M * qn);
     S.o = take<bf16>(A, M * hq);
     S.lse = take<float>(A, M * H);
-    S.h = take<bf16>(A, M * d);
+    S.h = take<float>(A, M * d);
     S.z = take<bf16>(A, M * d);
     S.r2 = take<float>(A, M);
     S.gu = take<bf16>(A, M * 2 * f);

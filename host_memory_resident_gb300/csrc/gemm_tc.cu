@@ -2,6 +2,10 @@
 //
 //   C[M, N] = A[M, K] * B[N, K]^T  (+ R[M, N])      fp32 accumulate
 //
+// C and the optional residual R are both bf16 or both fp32 (the decoder's
+// residual stream is kept in fp32: x + O Wo^T and h + a Wdown^T add the
+// fp32 accumulator to the fp32 stream and store fp32).
+//
 // A and B are row-major with K contiguous ("K-major"), which is the layout of
 // a linear layer's forward product y = x W^T with W stored [out, in]. The
 // backward products are expressed in the same form by the caller (dgrad with
@@ -18,19 +22,23 @@
 //     back to the producer and each finished accumulator to the epilogue;
 //   * warps 2-9 drain an accumulator with tcgen05.ld while the MMA warp fills
 //     the other one (two warps per TMEM lane quarter, each taking half of the
-//     tile's columns), add the optional bf16 residual, round and store.
+//     tile's columns), add the optional residual and store (bf16 or fp32).
 // Tiles are visited in groups of kGroupM row blocks so the A panel of a group
 // stays in L2 while the group sweeps all column blocks.
 //
-// Fused epilogues (each rounds to bf16 where the separate kernels would have
-// read a bf16 tensor, so results equal the unfused sequence bit for bit):
+// Fused epilogues. Each works on the fp32 accumulator and rounds to bf16 only
+// what it stores, so the only bf16 roundings are those of the stored
+// operands of later products:
 //   * RoPE: the QKV projection rotates the q and k heads of its tile
-//     (rotate-half pairs, position = row mod seq) before storing;
+//     (rotate-half pairs, position = row mod seq) from the fp32 products
+//     and stores the rotated values;
 //   * SwiGLU forward: the gate/up projection's B tile pairs 128 gate rows
-//     with the matching 128 up rows, so the epilogue stores gate | up and
-//     a = silu(gate) * up;
+//     with the matching 128 up rows, so the epilogue computes
+//     a = silu(gate) * up from the fp32 gate and up and stores a and (for
+//     the backward) gate | up;
 //   * SwiGLU backward: the down projection's input gradient da never leaves
-//     the SM; the epilogue reads gate | up and stores d(gate) | d(up).
+//     the SM; the epilogue turns the fp32 da and the stored gate | up into
+//     d(gate) | d(up).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -63,7 +71,7 @@ struct GemmArgs {
   int M, N, K;
   void* C;
   long long ldc;
-  const bf16* R;
+  const void* R;          // residual of C's type (bf16, or fp32 when c_f32)
   long long ldr;
   int c_f32;
   int num_mb, num_nb;
@@ -369,8 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             float va[32], vb[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              va[i] = bf16_round(__uint_as_float(ra[i]));
-              vb[i] = bf16_round(__uint_as_float(rb[i]));
+              va[i] = __uint_as_float(ra[i]);
+              vb[i] = __uint_as_float(rb[i]);
             }
             if (col_h < args.rot_cols) {
               float cs[32], sn[32];
@@ -399,8 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           float g[32], u[32], a[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            g[i] = bf16_round(__uint_as_float(rg[i]));
-            u[i] = bf16_round(__uint_as_float(ru[i]));
+            g[i] = __uint_as_float(rg[i]);
+            u[i] = __uint_as_float(ru[i]);
             a[i] = swiglu_fwd_elem(g[i], u[i]);
           }
           bf16* cp = reinterpret_cast<bf16*>(args.C) + (long long)row * args.ldc;
@@ -430,8 +438,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int k = 0; k < 4; ++k) {
                 const float2 g2 = unpack_bf16x2(gw[k]), u2 = unpack_bf16x2(uw[k]);
                 const int i = 8 * j + 2 * k;
-                swiglu_bwd_elem(bf16_round(__uint_as_float(r[i])), g2.x, u2.x, dg[i], du[i]);
-                swiglu_bwd_elem(bf16_round(__uint_as_float(r[i + 1])), g2.y, u2.y, dg[i + 1], du[i + 1]);
+                swiglu_bwd_elem(__uint_as_float(r[i]), g2.x, u2.x, dg[i], du[i]);
+                swiglu_bwd_elem(__uint_as_float(r[i + 1]), g2.y, u2.y, dg[i + 1], du[i + 1]);
               }
             }
             bf16* cp = reinterpret_cast<bf16*>(args.C) + (long long)row * args.ldc + col0;
@@ -457,8 +465,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
           const bool full = col0 + 32 <= args.N;
-          if (args.R != nullptr) {
-            const bf16* rp = args.R + (long long)row * args.ldr + col0;
+          if (args.R != nullptr && args.c_f32) {
+            const float* rp = reinterpret_cast<const float*>(args.R) + (long long)row * args.ldr + col0;
+            if (full) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float4 u = reinterpret_cast<const float4*>(rp)[j];
+                v[4 * j + 0] += u.x; v[4 * j + 1] += u.y; v[4 * j + 2] += u.z; v[4 * j + 3] += u.w;
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (col0 + i < args.N) v[i] += rp[i];
+            }
+          } else if (args.R != nullptr) {
+            const bf16* rp = reinterpret_cast<const bf16*>(args.R) + (long long)row * args.ldr + col0;
             if (full) {
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
@@ -610,6 +631,7 @@ int launch(int epi, const void* A, long long lda, int a_mn, const void* B, long 
   if (b_mn ? ldb < N : ldb < K) return MT_EINVAL;
   if (args.ldc < N || (args.c_f32 ? (args.ldc % 4) : (args.ldc % 8))) return MT_EINVAL;
   if (args.R && (args.ldr % 8 || args.ldr < N)) return MT_EINVAL;
+  if (args.R && args.splits > 1) return MT_EINVAL;
   // split K: every split gets at least one K block
   const int num_kb = (K + kBK - 1) / kBK;
   if (args.splits < 1) args.splits = 1;
@@ -690,7 +712,7 @@ int gemm_tile_policy(int policy) {
 int gemm_ex(const void* A, long long lda, int a_mn, const void* B, long long ldb, int b_mn, void* C, long long ldc,
             int c_f32, const void* R, long long ldr, int M, int N, int K, cudaStream_t stream) {
   GemmArgs args = base_args(M, N, K, C, ldc, c_f32);
-  args.R = reinterpret_cast<const bf16*>(R);
+  args.R = R;
   args.ldr = ldr;
   return launch(kEpiPlain, A, lda, a_mn, B, ldb, b_mn, args, stream);
 }

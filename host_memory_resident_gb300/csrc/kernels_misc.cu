@@ -47,6 +47,42 @@ __device__ __forceinline__ void load_bf16x8(const bf16* p, float (&f)[8]) {
   f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y; f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
 }
 
+__device__ __forceinline__ void load_f32x8(const float* p, float (&f)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+// Eight consecutive values of a bf16 or fp32 row as fp32.
+__device__ __forceinline__ void load_x8(const bf16* p, float (&f)[8]) { load_bf16x8(p, f); }
+__device__ __forceinline__ void load_x8(const float* p, float (&f)[8]) { load_f32x8(p, f); }
+
+// Eight x values held in registers: packed bf16 pairs, or fp32.
+template <typename TX>
+struct XReg;
+template <>
+struct XReg<bf16> {
+  uint4 p;
+  __device__ __forceinline__ void load(const bf16* q) { p = *reinterpret_cast<const uint4*>(q); }
+  __device__ __forceinline__ void zero() { p = make_uint4(0, 0, 0, 0); }
+  __device__ __forceinline__ float2 pair(int i) const {
+    const uint32_t w = i == 0 ? p.x : i == 1 ? p.y : i == 2 ? p.z : p.w;
+    return unpack_bf16x2(w);
+  }
+};
+template <>
+struct XReg<float> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const float* q) {
+    a = reinterpret_cast<const float4*>(q)[0];
+    b = reinterpret_cast<const float4*>(q)[1];
+  }
+  __device__ __forceinline__ void zero() { a = b = make_float4(0.f, 0.f, 0.f, 0.f); }
+  __device__ __forceinline__ float2 pair(int i) const {
+    return i == 0 ? make_float2(a.x, a.y) : i == 1 ? make_float2(a.z, a.w) : i == 2 ? make_float2(b.x, b.y)
+                                                                                    : make_float2(b.z, b.w);
+  }
+};
+
 __device__ __forceinline__ void store_bf16x8(bf16* p, const float (&f)[8]) {
   uint4 u;
   u.x = pack_bf16x2(f[0], f[1]);
@@ -63,18 +99,20 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // ------------------------------------------------------------ RMSNorm fwd
-// One warp per row: sum of squares, then y = x * rstd * w.
-__global__ void rmsnorm_fwd_kernel(const bf16* __restrict__ x, const bf16* __restrict__ w, bf16* __restrict__ y,
+// One warp per row: sum of squares, then y = x * rstd * w. x is the
+// residual stream (fp32) or any bf16 row.
+template <typename TX>
+__global__ void rmsnorm_fwd_kernel(const TX* __restrict__ x, const bf16* __restrict__ w, bf16* __restrict__ y,
                                    float* __restrict__ rstd, int M, int d, float eps) {
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= M) return;
-  const bf16* xr = x + (long long)row * d;
+  const TX* xr = x + (long long)row * d;
   const int nvec = d >> 3;
   float ss = 0.f;
   for (int v = lane; v < nvec; v += 32) {
     float f[8];
-    load_bf16x8(xr + v * 8, f);
+    load_x8(xr + v * 8, f);
 #pragma unroll
     for (int i = 0; i < 8; ++i) ss += f[i] * f[i];
   }
@@ -84,7 +122,7 @@ __global__ void rmsnorm_fwd_kernel(const bf16* __restrict__ x, const bf16* __res
   bf16* yr = y + (long long)row * d;
   for (int v = lane; v < nvec; v += 32) {
     float f[8], g[8];
-    load_bf16x8(xr + v * 8, f);
+    load_x8(xr + v * 8, f);
     load_bf16x8(w + v * 8, g);
 #pragma unroll
     for (int i = 0; i < 8; ++i) f[i] = f[i] * r * g[i];
@@ -99,9 +137,9 @@ __global__ void rmsnorm_fwd_kernel(const bf16* __restrict__ x, const bf16* __res
 // group's warps), dx = rstd*w*dy - x*rstd^3*dot/d (+ dres), and the thread's
 // dw partial += dy*x*rstd. The group's partial goes to partial[g] and the
 // column sums run in a fixed order, so dw is deterministic.
-template <int W>
+template <int W, typename TX>
 __global__ void __launch_bounds__(256, 2)
-    rmsnorm_bwd_kernel(const float* __restrict__ dy, const bf16* __restrict__ x, const bf16* __restrict__ w,
+    rmsnorm_bwd_kernel(const float* __restrict__ dy, const TX* __restrict__ x, const bf16* __restrict__ w,
                        const float* __restrict__ rstd, const float* dres, float* dx_f32, bf16* __restrict__ dx_bf16,
                        float* __restrict__ partial, int M, int d, int n_groups, int rows_per_group) {
   constexpr int G = 8 / W > 0 ? 8 / W : 1;  // groups per block
@@ -124,9 +162,9 @@ __global__ void __launch_bounds__(256, 2)
   for (int row = r0, it = 0; row < r1; ++row, ++it) {
     const float r = rstd[row];
     const float* dyr = dy + (long long)row * d;
-    const bf16* xr = x + (long long)row * d;
+    const TX* xr = x + (long long)row * d;
     float dyv[kNormBwdVec][8];
-    uint4 xp[kNormBwdVec];
+    XReg<TX> xp[kNormBwdVec];
     float dot = 0.f;
 #pragma unroll
     for (int k = 0; k < kNormBwdVec; ++k) {
@@ -136,20 +174,19 @@ __global__ void __launch_bounds__(256, 2)
         const float4 b = reinterpret_cast<const float4*>(dyr + v * 8)[1];
         dyv[k][0] = a.x; dyv[k][1] = a.y; dyv[k][2] = a.z; dyv[k][3] = a.w;
         dyv[k][4] = b.x; dyv[k][5] = b.y; dyv[k][6] = b.z; dyv[k][7] = b.w;
-        xp[k] = *reinterpret_cast<const uint4*>(xr + v * 8);
+        xp[k].load(xr + v * 8);
       } else {
 #pragma unroll
         for (int i = 0; i < 8; ++i) dyv[k][i] = 0.f;
-        xp[k] = make_uint4(0, 0, 0, 0);
+        xp[k].zero();
       }
     }
 #pragma unroll
     for (int k = 0; k < kNormBwdVec; ++k) {
-      const uint32_t xw[4] = {xp[k].x, xp[k].y, xp[k].z, xp[k].w};
       const uint32_t ww[4] = {wp[k].x, wp[k].y, wp[k].z, wp[k].w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float2 xf = unpack_bf16x2(xw[i]), wf = unpack_bf16x2(ww[i]);
+        const float2 xf = xp[k].pair(i), wf = unpack_bf16x2(ww[i]);
         dot += dyv[k][2 * i] * wf.x * xf.x;
         dot += dyv[k][2 * i + 1] * wf.y * xf.y;
       }
@@ -168,12 +205,11 @@ __global__ void __launch_bounds__(256, 2)
     for (int k = 0; k < kNormBwdVec; ++k) {
       const int v = lane + 32 * (wg + W * k);
       if (v < nvec) {
-        const uint32_t xw[4] = {xp[k].x, xp[k].y, xp[k].z, xp[k].w};
         const uint32_t ww[4] = {wp[k].x, wp[k].y, wp[k].z, wp[k].w};
         float o[8];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float2 xf = unpack_bf16x2(xw[i]), wf = unpack_bf16x2(ww[i]);
+          const float2 xf = xp[k].pair(i), wf = unpack_bf16x2(ww[i]);
           o[2 * i] = r * wf.x * dyv[k][2 * i] - xf.x * c;
           o[2 * i + 1] = r * wf.y * dyv[k][2 * i + 1] - xf.y * c;
           acc[k][2 * i] += dyv[k][2 * i] * xf.x * r;
@@ -343,6 +379,30 @@ __global__ void embedding_fwd_kernel(const bf16* __restrict__ E, const int32_t* 
   const uint4* src = reinterpret_cast<const uint4*>(E + (long long)(ok ? id : 0) * d);
   uint4* dst = reinterpret_cast<uint4*>(x + (long long)row * d);
   for (int v = lane; v < (d >> 3); v += 32) dst[v] = ok ? src[v] : make_uint4(0, 0, 0, 0);
+}
+
+// The same gather into an fp32 row (the start of the fp32 residual stream;
+// every bf16 value is exact in fp32).
+__global__ void embedding_fwd_f32_kernel(const bf16* __restrict__ E, const int32_t* __restrict__ tok,
+                                         float* __restrict__ x, int M, int d, int V, int* err) {
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= M) return;
+  const int id = tok[row];
+  const bool ok = id >= 0 && id < V;
+  if (!ok && lane == 0) set_device_error(err, kDevErrBadToken);
+  const bf16* src = E + (long long)(ok ? id : 0) * d;
+  float* dst = x + (long long)row * d;
+  for (int v = lane; v < (d >> 3); v += 32) {
+    float f[8];
+    load_bf16x8(src + v * 8, f);
+    if (!ok) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) f[i] = 0.f;
+    }
+    reinterpret_cast<float4*>(dst + v * 8)[0] = make_float4(f[0], f[1], f[2], f[3]);
+    reinterpret_cast<float4*>(dst + v * 8)[1] = make_float4(f[4], f[5], f[6], f[7]);
+  }
 }
 
 // Stable counting sort of token positions by id, in one CTA of 1024 threads.
@@ -611,18 +671,24 @@ int mt_k_gemm_splitk(int M, int N, int K) { return (M <= 0 || N <= 0 || K <= 0) 
 
 int64_t mt_k_gemm_wgrad_ws(int M, int N) { return (M <= 0 || N <= 0) ? 0 : (int64_t)splitk_ws_elems(M, N); }
 
-int mt_k_rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int M, int d, float eps, void* stream) {
+int mt_k_rmsnorm_fwd(const void* x, int x_f32, const void* w, void* y, float* rstd, int M, int d, float eps,
+                     void* stream) {
   if (M < 0 || d <= 0 || d % 8 || !al16(x) || !al16(w) || !al16(y)) return MT_EINVAL;
   if (M == 0) return MT_OK;
   const int rows_per_block = 8;
-  rmsnorm_fwd_kernel<<<(M + rows_per_block - 1) / rows_per_block, 32 * rows_per_block, 0, (cudaStream_t)stream>>>(
-      (const bf16*)x, (const bf16*)w, (bf16*)y, rstd, M, d, eps);
+  const dim3 grid((M + rows_per_block - 1) / rows_per_block), block(32 * rows_per_block);
+  if (x_f32)
+    rmsnorm_fwd_kernel<float><<<grid, block, 0, (cudaStream_t)stream>>>((const float*)x, (const bf16*)w, (bf16*)y,
+                                                                        rstd, M, d, eps);
+  else
+    rmsnorm_fwd_kernel<bf16><<<grid, block, 0, (cudaStream_t)stream>>>((const bf16*)x, (const bf16*)w, (bf16*)y,
+                                                                       rstd, M, d, eps);
   return launch_ok();
 }
 
 int mt_k_rmsnorm_bwd_parts(int M) { return M < kNormBwdMaxParts ? (M > 0 ? M : 1) : kNormBwdMaxParts; }
 
-int mt_k_rmsnorm_bwd(const float* dy, const void* x, const void* w, const float* rstd, const float* dres,
+int mt_k_rmsnorm_bwd(const float* dy, const void* x, int x_f32, const void* w, const float* rstd, const float* dres,
                      float* dx_f32, void* dx_bf16, float* partial, void* dw_out, int M, int d, void* stream) {
   if (M < 0 || d <= 0 || d % 8 || d > 8 * kNormBwdVec * 32 * kNormBwdMaxWarps) return MT_EINVAL;
   if (!al16(dy) || !al16(x) || !al16(w) || (dres && !al16(dres)) || (dx_f32 && !al16(dx_f32)) ||
@@ -634,21 +700,27 @@ int mt_k_rmsnorm_bwd(const float* dy, const void* x, const void* w, const float*
     const int W = (d + 8 * kNormBwdVec * 32 - 1) / (8 * kNormBwdVec * 32);  // warps per row
     const int rpg = (M + parts - 1) / parts;
     const int ngroups = (M + rpg - 1) / rpg;  // every group has at least one row
-    auto go = [&](auto kernel, int w_) {
+    auto go = [&](auto kernel, int w_, auto xt) {
+      using TX = decltype(xt);
       const int g = 8 / w_ > 0 ? 8 / w_ : 1;
-      kernel<<<(ngroups + g - 1) / g, 32 * w_ * g, 0, st>>>(dy, (const bf16*)x, (const bf16*)w, rstd, dres, dx_f32,
+      kernel<<<(ngroups + g - 1) / g, 32 * w_ * g, 0, st>>>(dy, (const TX*)x, (const bf16*)w, rstd, dres, dx_f32,
                                                            (bf16*)dx_bf16, partial, M, d, ngroups, rpg);
     };
-    switch (W) {
-      case 1: go(rmsnorm_bwd_kernel<1>, 1); break;
-      case 2: go(rmsnorm_bwd_kernel<2>, 2); break;
-      case 3: go(rmsnorm_bwd_kernel<3>, 3); break;
-      case 4: go(rmsnorm_bwd_kernel<4>, 4); break;
-      case 5: go(rmsnorm_bwd_kernel<5>, 5); break;
-      case 6: go(rmsnorm_bwd_kernel<6>, 6); break;
-      case 7: go(rmsnorm_bwd_kernel<7>, 7); break;
-      default: go(rmsnorm_bwd_kernel<8>, 8); break;
-    }
+    auto dispatch = [&](auto xt) {
+      using TX = decltype(xt);
+      switch (W) {
+        case 1: go(rmsnorm_bwd_kernel<1, TX>, 1, xt); break;
+        case 2: go(rmsnorm_bwd_kernel<2, TX>, 2, xt); break;
+        case 3: go(rmsnorm_bwd_kernel<3, TX>, 3, xt); break;
+        case 4: go(rmsnorm_bwd_kernel<4, TX>, 4, xt); break;
+        case 5: go(rmsnorm_bwd_kernel<5, TX>, 5, xt); break;
+        case 6: go(rmsnorm_bwd_kernel<6, TX>, 6, xt); break;
+        case 7: go(rmsnorm_bwd_kernel<7, TX>, 7, xt); break;
+        default: go(rmsnorm_bwd_kernel<8, TX>, 8, xt); break;
+      }
+    };
+    if (x_f32) dispatch(0.f);
+    else dispatch(bf16{});
     colsum_to_bf16_kernel<<<(d + 31) / 32, 32 * kColsumClasses, 0, st>>>(partial, ngroups, d, (bf16*)dw_out);
   } else {
     cudaMemsetAsync(partial, 0, sizeof(float) * d, st);
@@ -710,11 +782,15 @@ int mt_k_sum(const float* x, int n, float* out, void* stream) {
   return launch_ok();
 }
 
-int mt_k_embedding_fwd(const void* E, const int32_t* tok, void* x, int M, int d, int V, void* stream) {
+int mt_k_embedding_fwd(const void* E, const int32_t* tok, void* x, int x_f32, int M, int d, int V, void* stream) {
   if (M < 0 || d <= 0 || d % 8 || V <= 0 || !al16(E) || !al16(x)) return MT_EINVAL;
   if (M == 0) return MT_OK;
-  embedding_fwd_kernel<<<(M + 7) / 8, 256, 0, (cudaStream_t)stream>>>((const bf16*)E, tok, (bf16*)x, M, d, V,
-                                                                      device_error_word());
+  if (x_f32)
+    embedding_fwd_f32_kernel<<<(M + 7) / 8, 256, 0, (cudaStream_t)stream>>>((const bf16*)E, tok, (float*)x, M, d, V,
+                                                                            device_error_word());
+  else
+    embedding_fwd_kernel<<<(M + 7) / 8, 256, 0, (cudaStream_t)stream>>>((const bf16*)E, tok, (bf16*)x, M, d, V,
+                                                                        device_error_word());
   return launch_ok();
 }
 

@@ -34,8 +34,11 @@ extern "C" {
  * Dense product on tcgen05 tensor cores: C[M,N] = A[M,K] * B[N,K]^T (+ R).
  * A, B bf16 K-contiguous, 16-byte aligned, lda/ldb multiples of 8. C is bf16
  * (c_f32 = 0, ldc multiple of 8) or fp32 (c_f32 = 1, ldc multiple of 4). R is
- * an optional bf16 [M,N] residual (ldr multiple of 8) added before rounding.
- * The linear layers y = x W^T of a decoder layer (W stored [out, in]).
+ * an optional [M,N] residual of C's element type (bf16 or fp32; 16-byte
+ * aligned, ldr multiple of 8) added to the fp32 accumulator before the store.
+ * The linear layers y = x W^T of a decoder layer (W stored [out, in]); with
+ * fp32 C and R the output and down projections add into the fp32 residual
+ * stream.
  */
 int mt_k_gemm(const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, int c_f32,
               const void* R, int64_t ldr, int M, int N, int K, void* stream);
@@ -54,12 +57,12 @@ int mt_k_gemm_ex(const void* A, int64_t lda, int a_mn_major, const void* B, int6
 
 /*
  * QKV projection with RoPE in the epilogue: C = A B^T as mt_k_gemm (bf16 C),
- * then each row's columns [0, rot_cols) - heads of hd columns - are rotated
- * like mt_k_rope (inverse = 0) at position (row mod seq), from the
- * bf16-rounded products. The result equals mt_k_gemm followed by mt_k_rope
- * bit for bit (the zhichai.net article's stateless template, point 4: the
- * attention input of one layer). hd 64 or 128, N and rot_cols multiples of
- * hd; cos/sin fp32 [seq_max, hd/2].
+ * where each row's columns [0, rot_cols) - heads of hd columns - are rotated
+ * like mt_k_rope (inverse = 0) at position (row mod seq) from the fp32
+ * products and rounded to bf16 once (mt_k_gemm followed by mt_k_rope rounds
+ * twice: before and after the rotation). The attention input of one layer
+ * (the zhichai.net article's stateless template, point 4). hd 64 or 128, N
+ * and rot_cols multiples of hd; cos/sin fp32 [seq_max, hd/2].
  */
 int mt_k_gemm_rope(const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, int M, int N, int K,
                    const float* cos_t, const float* sin_t, int rot_cols, int hd, int seq, void* stream);
@@ -67,20 +70,21 @@ int mt_k_gemm_rope(const void* A, int64_t lda, const void* B, int64_t ldb, void*
 /*
  * Gate/up projection with SwiGLU in the epilogue: W bf16 [2f, K] holds the
  * gate rows then the up rows (K-major, like mt_k_gemm's B). Writes
- * gu = A W^T (bf16 [M, 2f], row pitch ldgu) and a = silu(gate) * up from the
- * bf16-rounded gate and up (bf16 [M, f], row pitch lda_out): the same bits as
- * mt_k_gemm then mt_k_swiglu_fwd. f a multiple of 128.
+ * gu = A W^T (bf16 [M, 2f], row pitch ldgu; kept for the backward) and
+ * a = silu(gate) * up computed from the fp32 gate and up (bf16 [M, f], row
+ * pitch lda_out). mt_k_gemm then mt_k_swiglu_fwd computes a from the
+ * bf16-rounded gate and up instead. f a multiple of 128.
  */
 int mt_k_gemm_swiglu_fwd(const void* A, int64_t lda, const void* W, int64_t ldw, void* gu, int64_t ldgu, void* a,
                          int64_t lda_out, int M, int f, int K, void* stream);
 
 /*
  * Down projection input gradient with the SwiGLU backward in the epilogue:
- * da = dy W (dy bf16 [M, K], W the down weight bf16 [K, f] read in place, as
- * mt_k_gemm_ex with b_mn_major = 1) is rounded to bf16 and turned into
- * dgu = (d gate | d up) [M, 2f] with gate | up read from gu [M, 2f]; da is
- * never written. The same bits as mt_k_gemm_ex then mt_k_swiglu_bwd. f a
- * multiple of 32.
+ * the fp32 da = dy W (dy bf16 [M, K], W the down weight bf16 [K, f] read in
+ * place, as mt_k_gemm_ex with b_mn_major = 1) is turned into
+ * dgu = (d gate | d up) [M, 2f] (bf16) with gate | up read from gu [M, 2f];
+ * da is never written or rounded (mt_k_gemm_ex then mt_k_swiglu_bwd rounds
+ * it to bf16 first). f a multiple of 32.
  */
 int mt_k_gemm_swiglu_bwd(const void* dy, int64_t lddy, const void* W, int64_t ldw, const void* gu, int64_t ldgu,
                          void* dgu, int64_t lddgu, int M, int f, int K, void* stream);
@@ -118,19 +122,22 @@ int64_t mt_k_gemm_wgrad_ws(int M, int N);
 
 /*
  * RMSNorm forward: y[m,:] = x[m,:] * rstd[m] * w, rstd = 1/sqrt(mean(x^2)+eps).
- * x, y bf16 [M, d] (ld = d), w bf16 [d], rstd fp32 [M]. d multiple of 8.
+ * x [M, d] is bf16 (x_f32 = 0) or fp32 (x_f32 = 1: the residual stream);
+ * y bf16 [M, d] (ld = d), w bf16 [d], rstd fp32 [M]. d multiple of 8.
  */
-int mt_k_rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int M, int d, float eps, void* stream);
+int mt_k_rmsnorm_fwd(const void* x, int x_f32, const void* w, void* y, float* rstd, int M, int d, float eps,
+                     void* stream);
 
 /*
- * RMSNorm backward. dy: gradient w.r.t. y, fp32 [M, d]; x bf16 [M, d];
+ * RMSNorm backward. dy: gradient w.r.t. y, fp32 [M, d]; x [M, d] bf16
+ * (x_f32 = 0) or fp32 (x_f32 = 1);
  * dres: optional fp32 [M, d] added to dx (the residual branch). Writes
  * dx_f32 (fp32 [M,d], may be NULL) and dx_bf16 (bf16 [M,d], may be NULL),
  * per-block partial sums of dw into `partial` (fp32 [n_part, d], scratch)
  * and the final dw (summed over rows in a fixed order) as bf16 into dw_out.
  * dx_f32 may alias dres. mt_k_rmsnorm_bwd_parts() gives n_part for M.
  */
-int mt_k_rmsnorm_bwd(const float* dy, const void* x, const void* w, const float* rstd, const float* dres,
+int mt_k_rmsnorm_bwd(const float* dy, const void* x, int x_f32, const void* w, const float* rstd, const float* dres,
                      float* dx_f32, void* dx_bf16, float* partial, void* dw_out, int M, int d, void* stream);
 int mt_k_rmsnorm_bwd_parts(int M);
 
@@ -194,9 +201,10 @@ int mt_k_cross_entropy(const float* logits, int64_t ldl, const int32_t* labels, 
 /* out[0] = sum of x[0..n) in a fixed order (fp64 accumulation), fp32 result. */
 int mt_k_sum(const float* x, int n, float* out, void* stream);
 
-/* x[m, :] = E[tok[m], :]; E bf16 [V, d], x bf16 [M, d]. Ids outside [0, V)
- * give a zero row and set the device error word. */
-int mt_k_embedding_fwd(const void* E, const int32_t* tok, void* x, int M, int d, int V, void* stream);
+/* x[m, :] = E[tok[m], :]; E bf16 [V, d], x [M, d] bf16 (x_f32 = 0) or fp32
+ * (x_f32 = 1, exact). Ids outside [0, V) give a zero row and set the device
+ * error word. */
+int mt_k_embedding_fwd(const void* E, const int32_t* tok, void* x, int x_f32, int M, int d, int V, void* stream);
 
 /*
  * dE[v, :] = sum over m with tok[m] = v of dx[m, :], bf16 [V, d] output,

@@ -35,7 +35,7 @@ def test_plan_grows_with_tokens_and_not_with_depth_beyond_checkpoints():
     # deeper model with the same checkpoint interval: only checkpoints grow
     d1 = resources.estimate(base.with_(n_layers=8), batch=4)["device_bytes"]
     d2 = resources.estimate(base.with_(n_layers=16), batch=4)["device_bytes"]
-    ckpt = 4 * 2048 * 2048 * 2  # one [M, d] bf16 checkpoint
+    ckpt = 4 * 2048 * 2048 * 4  # one [M, d] fp32 checkpoint (the residual stream is fp32)
     assert d2 - d1 == pytest.approx(2 * ckpt, rel=0.01)
 
 

@@ -9,13 +9,14 @@ inputs in test_library_cpu.py.
 
 Bars:
   * loss: relative error <= 5e-3;
-  * every gradient tensor: relative L2 error <= 2e-2, raised to 1.25x the
-    tensor's bf16-storage floor where that floor comes within 25% of 2e-2.
-    The floor is the error of oracle.bf16_emulation (the exact step with
-    bf16 rounding at the storage points any bf16 implementation has) against
-    the exact oracle; it reaches 2.5% (7B shape) and 3.0% (14B shape) on the
-    last layer's attention-side tensors and about 2.0% on most 14B tensors,
-    and the device reproduces it to within rounding noise;
+  * every gradient tensor: relative L2 error <= 2e-2, except where bf16
+    operands alone come within 20% of that: there the bar is 1.25x the
+    tensor's operand floor. The floor is the error of oracle.bf16_emulation
+    with rounding at the operands of the products and the gradient slab
+    only (the bf16 operands and gradients the method prescribes) against
+    the exact oracle (tests/golden/bf16_floor.json); the device keeps the
+    residual stream in fp32 and rounds nothing else that changes the result
+    by more than a few hundredths of that floor;
   * post-Adam master: the library's Adam is fed the library's own FP32
     gradients and compared with the oracle's Adam on the same gradients,
     |err| <= 1e-6 * (lr / 1e-3) (an independent-gradient comparison cannot
@@ -81,10 +82,10 @@ def bf16_weights(master):
 
 
 def _bar(case, t, default=2e-2):
-    """2e-2, raised to 1.25 x the bf16-storage floor where that floor is
-    within 25% of it or above."""
-    floor = FLOORS.get(case, {}).get(f"{t.name}@{t.offset}", 0.0)
-    return max(default, 1.25 * floor)
+    """2e-2, or 1.25 x the bf16-operand floor of the tensor where that floor
+    is 1.6e-2 or more (within 20% of the bar)."""
+    floor = FLOORS.get(case, {}).get(f"{t.name}@{t.offset}", 0.0) if case else 0.0
+    return max(default, 1.25 * floor) if floor >= 1.6e-2 else default
 
 
 def _check_parity(case, shape, lay, master, tokens, labels, oracle_dtype=np.float64, **kw):
@@ -98,6 +99,10 @@ def _check_parity(case, shape, lay, master, tokens, labels, oracle_dtype=np.floa
         a = g[t.offset:t.offset + t.size].astype(np.float64)
         b = ref[t.offset:t.offset + t.size]
         errs[(t.name, t.offset)] = np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30)
+    print(f"parity {case}: loss {loss:.6f} oracle {ref_loss:.6f}; gradient rel L2 (floor, bar):")
+    for t in lay.tensors():
+        fl = FLOORS.get(case, {}).get(f"{t.name}@{t.offset}", float("nan")) if case else float("nan")
+        print(f"  {t.name}@{t.offset}: {errs[(t.name, t.offset)]:.5f} ({fl:.5f}, {_bar(case, t):.5f})")
     for t in lay.tensors():
         e = errs[(t.name, t.offset)]
         worst = max(worst, e)
@@ -132,11 +137,26 @@ def test_tiny_larger_weights_parity(tiny):
     _check_parity("tiny-x10", tiny, lay, master, tokens, labels)
 
 
-@pytest.mark.parametrize("name,B,s", [("1.1b", 1, 512), ("7b", 1, 256), ("14b", 1, 128)])
+@pytest.mark.parametrize("name,B,s", [("1.1b", 1, 512), ("7b", 1, 256), ("14b", 1, 128), ("7b-s4096", 1, 4096),
+                                      ("14b-s4096", 1, 4096)])
 def test_full_width_reduced_depth_parity(name, B, s):
-    shape = synth.workload(name).with_(n_layers=2, ckpt_interval=1)
+    """The large workloads' layers at full width and 2 layers; at 4096
+    tokens the step's own QKV + RoPE epilogue, the GQA attention (groups of
+    5 at 14B) over 32 query tiles and the cross entropy run at the
+    workloads' sequence length."""
+    shape = synth.workload(name.split("-")[0]).with_(n_layers=2, ckpt_interval=1)
     lay, master, tokens, labels = _setup(shape, B=B, s=s)
     _check_parity(name, shape, lay, master, tokens, labels, oracle_dtype=np.float32)
+
+
+def test_full_depth_1p1b_parity():
+    """The 1.1B workload at full depth (22 layers, checkpoint interval 4, so
+    6 segments with a kept last segment of 2 layers, 12 gradient slabs over
+    24 units) on one 2048-token sequence against the oracle: loss, every
+    gradient tensor, post-Adam master."""
+    shape = synth.workload("1.1b")
+    lay, master, tokens, labels = _setup(shape, B=1, s=2048)
+    _check_parity("1.1b-full", shape, lay, master, tokens, labels, oracle_dtype=np.float32)
 
 
 def test_invariance_ckpt_interval_and_streaming(tiny):
@@ -188,7 +208,7 @@ def test_multi_step_matches_oracle_adam_chain(tiny):
             assert np.linalg.norm(g - ref) / np.linalg.norm(ref) <= 2e-2
             wo, mo, vo = oracle.adam_update(wo, mo, vo, g, step + 1, tiny.lr, tiny.beta1, tiny.beta2,
                                             tiny.adam_eps)
-            assert np.max(np.abs(w - wo)) <= 3e-6
+            assert np.max(np.abs(w - wo)) <= 1e-6 * (tiny.lr / 1e-3)
             losses.append(loss)
         assert tr.get_step() == 3
 
@@ -440,27 +460,19 @@ def test_without_gradient_array_results_are_identical(tiny, overlap):
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("name", ["tiny", "1.1b"])
-def test_fused_epilogues_change_no_bit(tiny, name):
-    """RoPE and SwiGLU in the GEMM epilogues give the loss, gradients and
-    updated master of the separate kernels, bit for bit (the 1.1B shape at
-    full width, 2 layers, one 256-token sequence)."""
+def test_unfused_epilogues_meet_the_same_bars(tiny, name):
+    """RoPE and SwiGLU as separate kernels (which round the GEMM output to
+    bf16 first) instead of GEMM epilogues (which work on the fp32 product):
+    both forms match the oracle at the step's bars (the 1.1B shape at full
+    width, 2 layers, one 256-token sequence)."""
     if name == "tiny":
-        shape, B, s = tiny.with_(n_layers=3, ckpt_interval=2), None, None
+        shape, B, s, case = tiny.with_(n_layers=3, ckpt_interval=2), None, None, None
     else:
-        shape, B, s = synth.workload("1.1b").with_(n_layers=2, ckpt_interval=1), 1, 256
+        shape, B, s, case = synth.workload("1.1b").with_(n_layers=2, ckpt_interval=1), 1, 256, None
     lay, master, _, _ = _setup(shape)
     tokens, labels = synth.make_tokens(shape.vocab, B or shape.batch, s or shape.seq, seed=3)
-    out = []
     for unfused in (False, True):
-        w = master.copy()
-        cfg = mt.make_config(shape, batch=B, seq=s, unfused_epilogues=unfused)
-        with mt.Trainer(cfg, w) as tr:
-            loss = tr.step(tokens, labels)
-            g = tr.read_grads()
-        out.append((loss, g, w))
-    assert out[0][0] == out[1][0]
-    assert np.array_equal(out[0][1], out[1][1])
-    assert np.array_equal(out[0][2], out[1][2])
+        _check_parity(case, shape, lay, master, tokens, labels, unfused_epilogues=unfused)
 
 
 @pytest.mark.gpu
