@@ -353,7 +353,11 @@ def sum_over_ranks(pg, x):
 # ------------------------------------------------------------------- arms
 def config_dict(args, shape, world, n_total):
     """The workload description both arms print (identical keys and values)."""
-    return {"workload": workload_desc(shape), "global_batch_tokens": shape.batch * shape.seq * world,
+    nm = getattr(args, "micro_batches", 1)
+    extra = {"micro_batches": nm, "note": f"gradient accumulation over {nm} micro-batches of {shape.batch} x "
+                                          f"{shape.seq} tokens, one host Adam per step"} if nm > 1 else {}
+    return {"workload": workload_desc(shape), **extra,
+            "global_batch_tokens": shape.batch * shape.seq * world * nm,
             "seq_len": shape.seq,
             "parallelism": f"replicas x{world} (no collective)" if world > 1 else "single GPU",
             "overlap_adam": bool(args.overlap),
@@ -608,19 +612,40 @@ def run_ours(args, shape, world, rank, local, pg):
     segs = [(t["offset"], t["rows"] * t["cols"], "normal" if t["kind"] == 0 else "ones") for t in descs]
     master = synth.init_master(n_total, segs, seed=0)
     B, s = shape.batch, shape.seq
-    M = B * s
+    NM = args.micro_batches
+    M = B * s * NM             # tokens per step (all micro-batches)
     W, K = args.warmup, args.steps
-    batches = [synth.make_tokens(shape.vocab, B, s, seed=1 + 1000 * rank, step=i) for i in range(W + 2 * K)]
-    dev_batches = [(torch.from_numpy(t).to(dev), torch.from_numpy(l).to(dev)) for t, l in batches[:W + K]]
+    batches = [[synth.make_tokens(shape.vocab, B, s, seed=1 + 1000 * rank, step=i * NM + j) for j in range(NM)]
+               for i in range(W + 2 * K)]
+    dev_batches = [[(torch.from_numpy(t).to(dev), torch.from_numpy(l).to(dev)) for t, l in mb]
+                   for mb in batches[:W + K]]
     link = host_link_probe(torch, dev)
     torch.cuda.empty_cache()
     adam_gbs = host_adam_probe(mt, threads=args.host_threads, keep_grads=args.keep_grads)
-    hb = host_bytes_per_param(args.keep_grads)
+    # host bytes per parameter per step: one accumulate pass per micro-batch
+    # but the last (bf16 slab in, fp32 running sum read and written), then Adam
+    hb = host_bytes_per_param(args.keep_grads) + (NM - 1) * 10.0
 
     tr = mt.Trainer(cfg, master, keep_grads=args.keep_grads)
     comp = torch.cuda.ExternalStream(tr.stream(0), device=dev)
+
+    def step_dev(i):
+        """One step from device-resident ids: one mt_train_step_device, or
+        NM micro-steps of gradient accumulation (host ids; Adam after the
+        last)."""
+        if NM == 1:
+            tk, lb = dev_batches[i][0]
+            return tr.step_device(tk.data_ptr(), lb.data_ptr(), B, s)
+        return [tr.step_accum(tk, lb, j, NM) for j, (tk, lb) in enumerate(batches[i])][-1]
+
+    def step_host(i):
+        if NM == 1:
+            tk, lb = batches[i][0]
+            return tr.step(tk, lb)
+        return [tr.step_accum(tk, lb, j, NM) for j, (tk, lb) in enumerate(batches[i])][-1]
+
     for i in range(W):
-        tr.step_device(dev_batches[i][0].data_ptr(), dev_batches[i][1].data_ptr(), B, s)
+        step_dev(i)
 
     # ---- timed region: K steps, token/label arrays resident in device memory,
     # per-launch profiling off (the per-class profile is a separate pass below)
@@ -636,8 +661,7 @@ def run_ours(args, shape, world, rank, local, pg):
     t0 = time.perf_counter()
     losses = []
     for i in range(K):
-        tk, lb = dev_batches[W + i]
-        losses.append(tr.step_device(tk.data_ptr(), lb.data_ptr(), B, s))
+        losses.append(step_dev(W + i))
     tr.sync()  # the last step's host Adam belongs to the timed work
     e1.record(comp)
     torch.cuda.synchronize(dev)
@@ -653,8 +677,7 @@ def run_ours(args, shape, world, rank, local, pg):
     e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2.record(comp)
     for i in range(K):
-        tk, lb = batches[W + K + i]
-        losses.append(tr.step(tk, lb))
+        losses.append(step_host(W + K + i))
     tr.sync()
     e3.record(comp)
     torch.cuda.synchronize(dev)
@@ -667,8 +690,7 @@ def run_ours(args, shape, world, rank, local, pg):
     tr.profile(True)
     tr.read_profile(reset=True)
     for i in range(KP):
-        tk, lb = dev_batches[W + i]
-        tr.step_device(tk.data_ptr(), lb.data_ptr(), B, s)
+        step_dev(W + i)
     tr.sync()
     prof = tr.read_profile(reset=True)
     tr.profile(False)
@@ -676,7 +698,7 @@ def run_ours(args, shape, world, rank, local, pg):
     tl_sum = None
     if not args.no_timeline:
         tr.profile(True)
-        tr.step_device(dev_batches[0][0].data_ptr(), dev_batches[0][1].data_ptr(), B, s)
+        step_dev(0)
         tr.sync()
         tl = tr.timeline()
         tr.read_profile(reset=True)
@@ -690,7 +712,7 @@ def run_ours(args, shape, world, rank, local, pg):
     tokens_all = sum_over_ranks(pg, float(M * K))
     value = tokens_all / t_max
     pk, pk_kind = peaks()
-    F = model_flops(shape, B, s)
+    F = model_flops(shape, B, s) * NM
     t_step = t_max / K
     g = prof["gemm"]
     gemm_tf = g["flops"] / (g["ms"] / 1e3) / 1e12 if g["ms"] > 0 else None
@@ -698,7 +720,7 @@ def run_ours(args, shape, world, rank, local, pg):
     traffic = gemm_traffic_record()
     w_bytes = 2.0 * n_total
     t_comp = F / (pk["bf16_tflops"] * 1e12)
-    t_link = max(2 * w_bytes / (link["bidir_h2d_gbs"] * 1e9), w_bytes / (link["bidir_d2h_gbs"] * 1e9))
+    t_link = NM * max(2 * w_bytes / (link["bidir_h2d_gbs"] * 1e9), w_bytes / (link["bidir_d2h_gbs"] * 1e9))
     t_roof = max(t_comp, t_link)
     prof_out = {k: {"launches_per_step": v["launches"] / KP, "ms_per_step": v["ms"] / KP,
                     "tflops": (v["flops"] / (v["ms"] / 1e3) / 1e12) if v["flops"] and v["ms"] else None,
@@ -748,7 +770,7 @@ def run_ours(args, shape, world, rank, local, pg):
         "clocks": clk,
         "gpu_launches": int(st1["kernel_launches"] - st0["kernel_launches"]),
         "e2e": {"value": tokens_all / e2e_max, "unit": "tokens/s", "h2d_bytes_per_step": 2 * 4 * M,
-                "d2h_bytes_per_step": 4},
+                "d2h_bytes_per_step": 4 * NM},
         "loss": {"first": losses[0], "last": losses[-1]},
         "wall_s_timed": wall,
     }
@@ -790,6 +812,9 @@ def main():
                     help="RoPE and SwiGLU as separate kernels instead of GEMM epilogues (same results)")
     ap.add_argument("--fused-grads", action="store_true",
                     help="no FP32 gradient array: each slab goes straight into Adam (same arithmetic)")
+    ap.add_argument("--micro-batches", type=int, default=1,
+                    help="one step = this many micro-batches of gradient accumulation (host ids), Adam after the "
+                         "last (global batch grows by this factor)")
     ap.add_argument("--no-overlap", action="store_true",
                     help="overlap_adam = 0: each step returns only after its host Adam has finished")
     args = ap.parse_args()

@@ -38,7 +38,7 @@ class Config(C.Structure):
         ("rms_eps", C.c_float), ("rope_theta", C.c_float), ("lr", C.c_float),
         ("beta1", C.c_float), ("beta2", C.c_float), ("adam_eps", C.c_float),
         ("device", C.c_int32), ("host_threads", C.c_int32), ("overlap_adam", C.c_int32),
-        ("unfused_epilogues", C.c_int32), ("keep_attention", C.c_int32),
+        ("unfused_epilogues", C.c_int32), ("keep_attention", C.c_int32), ("head_chunk_rows", C.c_int32),
     ]
 
 
@@ -161,7 +161,8 @@ def check(code, handle=None):
 
 
 def make_config(shape, batch=None, seq=None, streamed=True, device=0, host_threads=0, ckpt_interval=None,
-                n_slabs=None, overlap_adam=False, unfused_epilogues=False, keep_attention=False) -> Config:
+                n_slabs=None, overlap_adam=False, unfused_epilogues=False, keep_attention=False,
+                head_chunk_rows=0) -> Config:
     """mt_config from a synth.ModelShape-like object."""
     c = Config()
     c.n_layers = shape.n_layers
@@ -187,6 +188,7 @@ def make_config(shape, batch=None, seq=None, streamed=True, device=0, host_threa
     c.overlap_adam = 1 if overlap_adam else 0
     c.unfused_epilogues = 1 if unfused_epilogues else 0
     c.keep_attention = 1 if keep_attention else 0
+    c.head_chunk_rows = int(head_chunk_rows)
     return c
 
 

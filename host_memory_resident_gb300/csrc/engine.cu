@@ -157,7 +157,11 @@ struct mt_handle {
   mt::bf16 *xh = nullptr, *dz = nullptr;
   float *rf = nullptr, *logits = nullptr, *loss_rows = nullptr, *loss_dev = nullptr;
   float *dx32 = nullptr, *dh32 = nullptr, *dn32 = nullptr, *delta = nullptr, *npart = nullptr;
-  mt::bf16 *dxb = nullptr, *dhb = nullptr, *da = nullptr, *dgu = nullptr, *dob = nullptr, *dqkv = nullptr;
+  mt::bf16 *dxb = nullptr, *dhb = nullptr, *da = nullptr, *dob = nullptr, *dqkv = nullptr;
+  // head: dz per chunk of Mchunk rows (dz_chunked) with the head's weight
+  // gradient summed in fp32 (dhead32, V x d), else dz for every token
+  bool dz_chunked = false;
+  float* dhead32 = nullptr;
   // fp32 partial products of the weight gradients that are split along K
   float* wg_ws = nullptr;
   size_t wg_ws_elems = 0;
@@ -207,6 +211,11 @@ struct mt_handle {
 
 namespace mt {
 namespace {
+// The down projection's input gradient takes the SwiGLU backward in its
+// epilogue (so the da buffer is not needed) unless the configuration asks
+// for the separate kernels or the ffn width does not fit the fused form.
+bool swiglu_bwd_fused(const mt_handle* h) { return !h->cfg.unfused_epilogues && h->f % 32 == 0; }
+
 
 void set_err(mt_handle* h, const std::string& m) {
   if (h) h->err = m;
@@ -517,7 +526,7 @@ struct Step {
   // for the separate kernels or a shape does not fit the fused forms.
   bool fuse_rope() const { return !h->cfg.unfused_epilogues && h->hd % 64 == 0 && 128 % h->hd == 0; }
   bool fuse_swiglu_fwd() const { return !h->cfg.unfused_epilogues && h->f % 128 == 0; }
-  bool fuse_swiglu_bwd() const { return !h->cfg.unfused_epilogues && h->f % 32 == 0; }
+  bool fuse_swiglu_bwd() const { return swiglu_bwd_fused(h); }
 
   // Forward of layer l with weights W; writes the saved activations into S and
   // the layer output into x_out.
@@ -567,20 +576,23 @@ struct Step {
     // Weight gradients dW = dY^T X read both token-major activations in place
     // (MN-major operands, K = tokens); input gradients dX = dY W read the
     // weight [out, in] in place as a [K, N] operand. Nothing is transposed.
-    // down projection: dWdown = dy^T a ; da = dy Wdown
+    // down projection: dWdown = dy^T a ; da = dy Wdown. d(gate | up)
+    // overwrites the saved gate | up in place (each element is read before it
+    // is written, by the same thread; nothing reads gate | up afterwards)
+    bf16* dgu = S.gu;
     gemm_wg(h->dxb, d, S.a, f, g + o.wdown, f, d, f);
     if (fuse_swiglu_bwd()) {
       // da = dy Wdown stays in the SM; the epilogue writes d(gate) | d(up)
       const double bytes = 2.0 * ((double)M * d + (double)d * f + 2.0 * M * f + 2.0 * M * f);
       KP(MT_PROF_GEMM, 1, 2.0 * M * (double)f * d, bytes,
-         gemm_swiglu_bwd(h->dxb, d, W + o.wdown, f, S.gu, 2 * f, h->dgu, 2 * f, M, f, d, cs()));
+         gemm_swiglu_bwd(h->dxb, d, W + o.wdown, f, S.gu, 2 * f, dgu, 2 * f, M, f, d, cs()));
     } else {
       gemm_mn(h->dxb, d, false, W + o.wdown, f, true, h->da, f, false, M, f, d);
-      KP(MT_PROF_SWIGLU, 1, 0.0, 10.0 * M * f, mt_k_swiglu_bwd(h->da, S.gu, h->dgu, M, f, cs()));
+      KP(MT_PROF_SWIGLU, 1, 0.0, 10.0 * M * f, mt_k_swiglu_bwd(h->da, S.gu, dgu, M, f, cs()));
     }
     // gate/up projection
-    gemm_wg(h->dgu, 2 * f, S.z, d, g + o.wgu, d, 2 * f, d);
-    gemm_mn(h->dgu, 2 * f, false, W + o.wgu, d, true, h->dn32, d, true, M, d, 2 * f);
+    gemm_wg(dgu, 2 * f, S.z, d, g + o.wgu, d, 2 * f, d);
+    gemm_mn(dgu, 2 * f, false, W + o.wgu, d, true, h->dn32, d, true, M, d, 2 * f);
     KP(MT_PROF_NORM, 2, 0.0, norm_bwd_bytes(true),
        mt_k_rmsnorm_bwd(h->dn32, S.h, 1, W + o.mlp_norm, S.r2, h->dx32, h->dh32, h->dhb, h->npart, g + o.mlp_norm, M,
                         d, cs()));
@@ -599,26 +611,46 @@ struct Step {
                         d, cs()));
   }
 
-  // Final norm, logits, cross entropy and their backward (head unit).
+  // Final norm, logits, cross entropy and their backward (head unit). The
+  // logits are made Mchunk rows at a time (fp32). dz is kept for every token
+  // and the head's two gradient products run once over all of them, or, when
+  // the handle keeps dz per chunk (dz_chunked), each chunk's products run
+  // right after its cross entropy: dxh rows of the chunk, and the head's
+  // weight gradient summed over the chunks in an fp32 accumulator that is
+  // rounded to bf16 once at the end.
   void head(const bf16* W, const float* xL, bf16* g) {
     const int d = h->d, V = h->V;
     const bf16* wf = W + h->lay.final_norm;
     const bf16* head = W + h->lay.head;
     KP(MT_PROF_NORM, 1, 0.0, norm_fwd_bytes(), mt_k_rmsnorm_fwd(xL, 1, wf, h->xh, h->rf, M, d, h->cfg.rms_eps, cs()));
     const float scale = 1.f / (float)M;
+    const bool per_chunk = h->dz_chunked && M > h->Mchunk;
     for (int r0 = 0; r0 < M; r0 += h->Mchunk) {
       const int mc = std::min(h->Mchunk, M - r0);
+      bf16* dzc = per_chunk ? h->dz : h->dz + (size_t)r0 * V;
       gemm(h->xh + (size_t)r0 * d, d, head, d, h->logits, V, true, nullptr, 0, mc, V, d);
       KP(MT_PROF_CE, 1, 0.0, 6.0 * mc * (double)V,
-         mt_k_cross_entropy(h->logits, V, h->d_lab + r0, h->dz + (size_t)r0 * V, V, h->loss_rows + r0, mc, V, scale,
-                            cs()));
+         mt_k_cross_entropy(h->logits, V, h->d_lab + r0, dzc, V, h->loss_rows + r0, mc, V, scale, cs()));
+      if (per_chunk) {
+        // dxh of the chunk's rows = dz_c Head; dHead (+)= dz_c^T xh_c
+        gemm_mn(dzc, V, false, head, d, true, h->dn32 + (size_t)r0 * d, d, true, mc, d, V);
+        const double bytes = 2.0 * ((double)mc * V + (double)mc * d) + 4.0 * V * (double)d * (r0 > 0 ? 2.0 : 1.0);
+        KP(MT_PROF_GEMM, 1, 2.0 * V * (double)d * mc, bytes,
+           gemm_ex(dzc, V, 1, h->xh + (size_t)r0 * d, d, 1, h->dhead32, d, 1, r0 > 0 ? h->dhead32 : nullptr, d, V,
+                   d, mc, cs()));
+      }
     }
     KP(MT_PROF_OTHER, 1, 0.0, 4.0 * M, mt_k_sum(h->loss_rows, M, h->loss_dev, cs()));
     CK(cudaMemcpyAsync(h->loss_pinned + parity(), h->loss_dev, sizeof(float), cudaMemcpyDeviceToHost, cs()));
     CK(cudaEventRecord(h->ev_loss[parity()], cs()));
-    // dHead = dz^T xh ; dxh = dz Head (both read in place)
-    gemm_wg(h->dz, V, h->xh, d, g + h->lay.head, d, V, d);
-    gemm_mn(h->dz, V, false, head, d, true, h->dn32, d, true, M, d, V);
+    if (per_chunk) {
+      KP(MT_PROF_OTHER, 1, 0.0, 6.0 * V * (double)d,
+         convert_f32_bf16(h->dhead32, g + h->lay.head, (long long)V * d, cs()));
+    } else {
+      // dHead = dz^T xh ; dxh = dz Head (both read in place)
+      gemm_wg(h->dz, V, h->xh, d, g + h->lay.head, d, V, d);
+      gemm_mn(h->dz, V, false, head, d, true, h->dn32, d, true, M, d, V);
+    }
     KP(MT_PROF_NORM, 2, 0.0, norm_bwd_bytes(false),
        mt_k_rmsnorm_bwd(h->dn32, xL, 1, wf, h->rf, nullptr, h->dx32, h->dxb, h->npart, g + h->lay.final_norm, M, d,
                         cs()));
@@ -780,20 +812,24 @@ void plan_device(mt_handle* h, Arena& A) {
   h->d_ework = take<int32_t>(A, (size_t)mt_k_embedding_bwd_work((int)M, (int)V));
   h->cos_t = take<float>(A, (size_t)h->cfg.max_seq * (h->hd / 2));
   h->sin_t = take<float>(A, (size_t)h->cfg.max_seq * (h->hd / 2));
+  // xa holds the last layer's output; xb (with xa) the outputs inside a
+  // segment of more than one layer
   h->xa = take<float>(A, M * d);
-  h->xb = take<float>(A, M * d);
+  h->xb = h->cfg.ckpt_interval > 1 ? take<float>(A, M * d) : nullptr;
   h->ckpt.assign(h->nseg, nullptr);
   for (auto& p : h->ckpt) p = take<float>(A, M * d);
   const int slots = std::min(h->cfg.ckpt_interval, h->L);
   h->saved.assign(slots, Saved{});
   for (int i = 0; i < slots; ++i) {
     Saved& S = h->saved[i];
-    S.x = take<float>(A, M * d);
+    // the first layer of a segment reads its checkpoint in place
+    S.x = i > 0 ? take<float>(A, M * d) : nullptr;
     S.u = take<bf16>(A, M * d);
     S.r1 = take<float>(A, M);
     S.qkv = take<bf16>(A, M * qn);
-    S.o = take<bf16>(A, M * hq);
-    S.lse = take<float>(A, M * H);
+    // with keep_attention the layers' own kept tensors stand in for these
+    S.o = h->cfg.keep_attention ? nullptr : take<bf16>(A, M * hq);
+    S.lse = h->cfg.keep_attention ? nullptr : take<float>(A, M * H);
     S.h = take<float>(A, M * d);
     S.z = take<bf16>(A, M * d);
     S.r2 = take<float>(A, M);
@@ -809,7 +845,8 @@ void plan_device(mt_handle* h, Arena& A) {
   h->xh = take<bf16>(A, M * d);
   h->rf = take<float>(A, M);
   h->logits = take<float>(A, (size_t)h->Mchunk * V);
-  h->dz = take<bf16>(A, M * V);
+  h->dz = take<bf16>(A, (h->dz_chunked ? (size_t)h->Mchunk : M) * V);
+  h->dhead32 = h->dz_chunked ? take<float>(A, (size_t)V * d) : nullptr;
   h->loss_rows = take<float>(A, M);
   h->loss_dev = take<float>(A, 4);
   h->dx32 = take<float>(A, M * d);
@@ -817,8 +854,7 @@ void plan_device(mt_handle* h, Arena& A) {
   h->dn32 = take<float>(A, M * d);
   h->dxb = take<bf16>(A, M * d);
   h->dhb = take<bf16>(A, M * d);
-  h->da = take<bf16>(A, M * f);
-  h->dgu = take<bf16>(A, M * 2 * f);
+  h->da = swiglu_bwd_fused(h) ? nullptr : take<bf16>(A, M * f);  // only the unfused SwiGLU backward
   h->dob = take<bf16>(A, M * hq);
   h->dqkv = take<bf16>(A, M * qn);
   h->delta = take<float>(A, M * H);
@@ -845,10 +881,19 @@ void set_dims(mt_handle* h, const mt_config& c) {
   h->hq = h->H * h->hd;
   h->nseg = (h->L + c.ckpt_interval - 1) / c.ckpt_interval;
   h->Mmax = c.max_batch * c.max_seq;
-  int64_t mc = (1LL << 28) / h->V;
-  mc = mc / 128 * 128;
-  if (mc < 128) mc = 128;
-  h->Mchunk = (int)std::min<int64_t>(mc, h->Mmax);
+  if (c.head_chunk_rows > 0) {
+    h->Mchunk = (int)std::min<int64_t>(c.head_chunk_rows, h->Mmax);
+    h->dz_chunked = h->Mchunk < h->Mmax;
+  } else {
+    int64_t mc = (1LL << 28) / h->V;
+    mc = mc / 128 * 128;
+    if (mc < 128) mc = 128;
+    h->Mchunk = (int)std::min<int64_t>(mc, h->Mmax);
+    // per-chunk dz only where it takes less memory than dz for every token
+    const double full = 2.0 * h->Mmax * (double)h->V;
+    const double chunked = 2.0 * h->Mchunk * (double)h->V + 4.0 * h->V * (double)h->d;
+    h->dz_chunked = h->Mchunk < h->Mmax && chunked < full;
+  }
 }
 
 int fail(mt_handle* h, int code, const std::string& msg) {

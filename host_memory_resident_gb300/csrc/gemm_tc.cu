@@ -116,16 +116,6 @@ __device__ __forceinline__ void store_bf16x32(bf16* p, const float (&v)[32], int
   }
 }
 
-__device__ __forceinline__ void load_bf16x32(const bf16* p, float (&v)[32]) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint4 u = reinterpret_cast<const uint4*>(p)[j];
-    const float2 f0 = unpack_bf16x2(u.x), f1 = unpack_bf16x2(u.y), f2 = unpack_bf16x2(u.z), f3 = unpack_bf16x2(u.w);
-    v[8 * j + 0] = f0.x; v[8 * j + 1] = f0.y; v[8 * j + 2] = f1.x; v[8 * j + 3] = f1.y;
-    v[8 * j + 4] = f2.x; v[8 * j + 5] = f2.y; v[8 * j + 6] = f3.x; v[8 * j + 7] = f3.y;
-  }
-}
-
 // The 32 gate and 32 up values (bf16, packed) of one row at ffn column col0
 // for the SwiGLU-backward epilogue; zeros outside the matrix.
 __device__ __forceinline__ void load_gate_up(const GemmArgs& a, int row, bool row_ok, int col0, uint4 (&g)[4],

@@ -36,6 +36,7 @@ bool config_valid(const mt_config& c, const char** why) {
   if ((int64_t)c.max_batch * c.max_seq > (1LL << 30)) return bad("max_batch * max_seq too large");
   if (c.ckpt_interval < 1) return bad("ckpt_interval must be >= 1");
   if (c.n_slabs < 2) return bad("n_slabs must be >= 2");
+  if (c.head_chunk_rows < 0) return bad("head_chunk_rows must be >= 0");
   if (!(c.rms_eps > 0.f) || !(c.rope_theta > 0.f)) return bad("rms_eps and rope_theta must be > 0");
   if (!(c.lr >= 0.f) || !(c.beta1 >= 0.f && c.beta1 < 1.f) || !(c.beta2 >= 0.f && c.beta2 < 1.f) ||
       !(c.adam_eps >= 0.f))

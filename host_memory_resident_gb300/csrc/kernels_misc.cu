@@ -6,6 +6,7 @@
 // per-layer template of the zhichai.net article ("以内存为中心的训练新范式",
 // point 4) with the backward written by hand (travelaiplan blog, 核心功能
 // point 3).
+#include <algorithm>
 #include <cfloat>
 #include <cmath>
 #include <mutex>
@@ -554,14 +555,17 @@ __device__ __forceinline__ void online_merge(float& m, float& s, float m2, float
   }
 }
 
+// Persistent: a grid of a few blocks per SM walks the rows, so the rows in
+// flight (blocks x V x 4 bytes) stay well inside L2 and the second pass over
+// a row (the gradient) reads it from L2 instead of HBM.
 __global__ void __launch_bounds__(kCeThreads)
     cross_entropy_kernel(const float* __restrict__ logits, long long ldl, const int32_t* __restrict__ labels,
-                         bf16* __restrict__ dz, long long lddz, float* __restrict__ loss_rows, int V, float scale,
-                         int* err) {
+                         bf16* __restrict__ dz, long long lddz, float* __restrict__ loss_rows, int M, int V,
+                         float scale, int* err) {
   __shared__ float sm_m[kCeThreads / 32], sm_s[kCeThreads / 32];
-  const int row = blockIdx.x;
-  const float* z = logits + (long long)row * ldl;
   const int tid = threadIdx.x;
+  for (int row = blockIdx.x; row < M; row += gridDim.x) {
+  const float* z = logits + (long long)row * ldl;
   float m = -INFINITY, s = 0.f;
   const int nv = V >> 2;
   for (int v = tid; v < nv; v += kCeThreads) {
@@ -576,6 +580,7 @@ __global__ void __launch_bounds__(kCeThreads)
     const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
     online_merge(m, s, m2, s2);
   }
+  __syncthreads();  // the previous row's reads of sm_m / sm_s are done
   if ((tid & 31) == 0) { sm_m[tid >> 5] = m; sm_s[tid >> 5] = s; }
   __syncthreads();
   m = sm_m[0];
@@ -601,6 +606,19 @@ __global__ void __launch_bounds__(kCeThreads)
     u.x = pack_bf16x2(p0 * scale, p1 * scale);
     u.y = pack_bf16x2(p2 * scale, p3 * scale);
     *reinterpret_cast<uint2*>(dr + j) = u;
+  }
+  }
+}
+
+// dst = bf16(src), 8 elements per thread where the tail allows.
+__global__ void f32_to_bf16_kernel(const float* __restrict__ src, bf16* __restrict__ dst, long long n) {
+  const long long i = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  if (i + 8 <= n) {
+    float f[8];
+    load_f32x8(src + i, f);
+    store_bf16x8(dst + i, f);
+  } else {
+    for (long long j = i; j < n; ++j) dst[j] = __float2bfloat16_rn(src[j]);
   }
 }
 
@@ -628,6 +646,14 @@ __global__ void check_ids_kernel(const int32_t* __restrict__ ids, int n, int V, 
 inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 }  // namespace
+
+int convert_f32_bf16(const float* src, void* dst, long long n, cudaStream_t stream) {
+  if (n < 0 || !al16(src) || !al16(dst)) return MT_EINVAL;
+  if (n == 0) return MT_OK;
+  const long long threads = (n + 7) / 8;
+  f32_to_bf16_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(src, (bf16*)dst, n);
+  return launch_ok();
+}
 }  // namespace mt
 
 using namespace mt;
@@ -771,8 +797,18 @@ int mt_k_cross_entropy(const float* logits, int64_t ldl, const int32_t* labels, 
   if (M < 0 || V <= 0 || V % 4 || ldl < V || ldl % 4 || lddz < V || lddz % 4 || !al16(logits)) return MT_EINVAL;
   if ((reinterpret_cast<uintptr_t>(dz) & 7) != 0) return MT_EINVAL;
   if (M == 0) return MT_OK;
-  cross_entropy_kernel<<<M, kCeThreads, 0, (cudaStream_t)stream>>>(logits, ldl, labels, (bf16*)dz, lddz, loss_rows,
-                                                                   V, scale, device_error_word());
+  // rows in flight: 4 blocks per SM, fewer for long rows (at most ~48 MB)
+  static int sms[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return MT_ECUDA;
+  if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+  const long long per_row = 4LL * V;
+  long long blocks = (48LL << 20) / per_row;
+  blocks = std::max<long long>(sms[dev], std::min<long long>(blocks, 4LL * sms[dev]));
+  blocks = std::min<long long>(blocks, M);
+  cross_entropy_kernel<<<(unsigned)blocks, kCeThreads, 0, (cudaStream_t)stream>>>(
+      logits, ldl, labels, (bf16*)dz, lddz, loss_rows, M, V, scale, device_error_word());
   return launch_ok();
 }
 

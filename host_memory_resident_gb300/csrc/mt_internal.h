@@ -66,6 +66,9 @@ int attn_bwd_tc(const void* qkv, long long ld, const void* dout, long long lddo,
                 const float* delta, void* dqkv, long long lddq, int B, int s, int H, int Hkv, int hd,
                 cudaStream_t stream);
 
+// dst[i] = bf16(src[i]) for i < n (round to nearest even).
+int convert_f32_bf16(const float* src, void* dst, long long n, cudaStream_t stream);
+
 // C = A * B^T (+ R); see mt_k_gemm.
 int gemm_abt(const void* A, long long lda, const void* B, long long ldb, void* C, long long ldc, int c_f32,
              const void* R, long long ldr, int M, int N, int K, cudaStream_t stream);

@@ -65,12 +65,18 @@ typedef struct mt_config {
                             unit only after its Adam has finished. Results are identical to 0. Call
                             mt_sync before reading master / m / v yourself. */
   int32_t unfused_epilogues; /* 1: RoPE and SwiGLU (forward and backward) run as separate kernels
-                                after their GEMMs instead of in the GEMM epilogues; the results are
-                                bitwise identical either way (0, the default, is faster) */
+                                after their GEMMs, which round the GEMM output to bf16 first; 0 (the
+                                default, faster): the GEMM epilogues apply them to the fp32 product and
+                                round once. Both match the same bars against the exact step */
   int32_t keep_attention;    /* 1: keep every layer's attention output and log-sum-exp from the
                                 forward (L * (M * H * hd * 2 + M * H * 4) more device bytes) so the
                                 backward's recompute skips the attention core; results are bitwise
                                 identical. 0 (default): recompute whole layers from the checkpoints */
+  int32_t head_chunk_rows;   /* rows of one logits chunk of the head. 0 (default): about 2^28 / V
+                                rows, and the head's gradient dz is kept per chunk (the head's weight
+                                gradient summed over chunks in fp32) only where that takes less
+                                memory than dz for every token; > 0: chunks of this many rows, dz
+                                per chunk whenever there is more than one chunk */
 } mt_config;
 
 /* One tensor of the flat layout. kind 0 = matrix, 1 = norm weight. */

@@ -56,13 +56,19 @@ POINTS = OPERAND_POINTS + OTHER_POINTS
 
 
 def to_bf16(x):
-    """Round-to-nearest-even to bf16, returned as float64 (plain numpy)."""
+    """Round-to-nearest-even to bf16, returned as float64 (plain numpy; done
+    in slices of 2^24 elements so the integer temporaries stay small)."""
     a = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
-    u = a.view(np.uint32).astype(np.uint64)
-    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
-    out = (r & 0xFFFFFFFF).astype(np.uint32).view(np.float32)
-    out = np.where(np.isnan(a), np.float32(np.nan), out)
-    return out.astype(np.float64)
+    out = np.empty(a.shape, dtype=np.float64)
+    flat_a, flat_o = a.reshape(-1), out.reshape(-1)
+    step = 1 << 24
+    for i in range(0, flat_a.size, step):
+        c = flat_a[i:i + step]
+        u = c.view(np.uint32).astype(np.uint64)
+        r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
+        b = (r & 0xFFFFFFFF).astype(np.uint32).view(np.float32)
+        flat_o[i:i + step] = np.where(np.isnan(c), np.float32(np.nan), b)
+    return out
 
 
 def _identity(x):

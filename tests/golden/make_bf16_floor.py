@@ -56,7 +56,9 @@ def master_for(shape, scale):
 def floor_for(shape, B, s, scale):
     lay, master = master_for(shape, scale)
     tokens, labels = synth.make_tokens(shape.vocab, B or shape.batch, s or shape.seq, seed=1)
-    wb = to_bf16(master).astype(np.float32)      # the bf16 weight values both sides use
+    wb = np.empty(master.shape, dtype=np.float32)  # the bf16 weight values both sides use
+    for i in range(0, master.size, 1 << 26):
+        wb[i:i + (1 << 26)] = to_bf16(master[i:i + (1 << 26)])
     del master
     gc.collect()
     _, ref = oracle.step_grads(shape, wb, tokens, labels, dtype=np.float64, streamed=True, out_dtype=np.float32)

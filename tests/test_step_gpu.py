@@ -159,6 +159,23 @@ def test_full_depth_1p1b_parity():
     _check_parity("1.1b-full", shape, lay, master, tokens, labels, oracle_dtype=np.float32)
 
 
+@pytest.mark.parametrize("name", ["tiny", "1.1b"])
+def test_head_in_chunks_matches_the_oracle(tiny, name):
+    """The head one chunk of rows at a time (a ragged last chunk): each
+    chunk's logits, cross entropy and gradient products, the head's weight
+    gradient summed over the chunks in fp32 and rounded once. Loss, every
+    gradient and the post-Adam master against the oracle at the step's bars
+    (tiny: chunks of 24, 24, 16 rows; 1.1B width, 2 layers, 512 tokens:
+    200, 200, 112)."""
+    if name == "tiny":
+        shape, B, s, rows, case = tiny, None, None, 24, "tiny"
+    else:
+        shape, B, s, rows, case = synth.workload("1.1b").with_(n_layers=2, ckpt_interval=1), 1, 512, 200, "1.1b"
+    lay, master, tokens, labels = _setup(shape, B=B, s=s)
+    _check_parity(case, shape, lay, master, tokens, labels, head_chunk_rows=rows,
+                  oracle_dtype=np.float64 if name == "tiny" else np.float32)
+
+
 def test_invariance_ckpt_interval_and_streaming(tiny):
     shape = tiny.with_(n_layers=4)
     lay, master, tokens, labels = _setup(shape)
@@ -416,13 +433,13 @@ def test_gradient_accumulation_over_micro_batches(tiny, overlap):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("streamed", [True, False])
-def test_planner_matches_the_live_handle(tiny, streamed):
+@pytest.mark.parametrize("streamed,rows", [(True, 0), (False, 0), (True, 24)])
+def test_planner_matches_the_live_handle(tiny, streamed, rows):
     """mt_plan, which allocates nothing, reports the device and pinned bytes
     that mt_init then allocates for the same configuration."""
     shape = tiny.with_(n_layers=5, ckpt_interval=2)
     lay, master, _, _ = _setup(shape)
-    cfg = mt.make_config(shape, streamed=streamed)
+    cfg = mt.make_config(shape, streamed=streamed, head_chunk_rows=rows)
     p = mt.plan(cfg)
     with mt.Trainer(cfg, master.copy()) as tr:
         st = tr.stats()
