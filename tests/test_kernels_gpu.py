@@ -372,6 +372,9 @@ ATTN_CASES = [
     (1, 257, 2, 2, 128),   # ragged, hd 128
     (1, 1, 2, 1, 64),      # single token: output = v
     (1, 1024, 2, 2, 128),
+    (1, 1, 2, 1, 128),     # single token at hd 128
+    (2, 300, 8, 2, 128),   # GQA, several 128-query sub-tiles per key tile, ragged
+    (1, 640, 5, 1, 128),   # 5 query heads per KV head (the 14B grouping), 5 tiles
 ]
 
 
@@ -421,8 +424,10 @@ def test_attention_bwd(B, s, H, Hkv, hd):
 
 
 # ------------------------------------------------------------ cross entropy
-@pytest.mark.parametrize("M,V", [(64, 512), (37, 32000), (5, 152064)])
+@pytest.mark.parametrize("M,V", [(64, 512), (37, 32000), (5, 152064), (2000, 512), (400, 152064)])
 def test_cross_entropy(M, V):
+    """Rows are spread over a fixed grid of a few blocks per SM, so the
+    larger cases give each block several rows."""
     rng = np.random.default_rng(M + V)
     z, zh = f32(rng.standard_normal((M, V)) * 3)
     lab_np = rng.integers(0, V, size=M).astype(np.int32)
