@@ -310,7 +310,7 @@ class Trainer:
         check(lib().mt_profile_timeline(self.h, None, 0, C.byref(n)), self.h)
         buf = (TimelineRec * max(n.value, 1))()
         check(lib().mt_profile_timeline(self.h, buf, n.value, C.byref(n)), self.h)
-        names = ("compute", "h2d", "d2h", "host_adam", "host_wait")
+        names = ("compute", "h2d", "d2h", "host_adam", "host_wait", "host_adam_prev", "host_wait_prev")
         return [dict(cls=PROF_CLASSES[r.cls] if r.stream < 3 else f"unit {r.cls}", stream=names[r.stream],
                      start_ms=r.start_ms, end_ms=r.end_ms) for r in buf[:n.value]]
 

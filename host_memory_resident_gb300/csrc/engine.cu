@@ -206,6 +206,11 @@ struct mt_handle {
   int64_t timeline_seq = -1;             // that step's sequence number
   std::vector<mt_timeline_rec> host_tl;   // worker records of step host_tl_seq (under mu)
   int64_t host_tl_seq = -1;
+  std::chrono::steady_clock::time_point host_tl_step0{};
+  // the step before: its records, relative to its own start
+  std::vector<mt_timeline_rec> host_tl_prev;
+  int64_t host_tl_prev_seq = -1;
+  std::chrono::steady_clock::time_point host_tl_prev_step0{};
   std::chrono::steady_clock::time_point step0{};  // host time the current step began
 };
 
@@ -313,8 +318,12 @@ void worker_main(mt_handle* h) {
         const double t_end = ms(Clock::now());
         std::lock_guard<std::mutex> lk(h->mu);
         if (job.seq != h->host_tl_seq) {
+          h->host_tl_prev.swap(h->host_tl);
+          h->host_tl_prev_seq = h->host_tl_seq;
+          h->host_tl_prev_step0 = h->host_tl_step0;
           h->host_tl.clear();
           h->host_tl_seq = job.seq;
+          h->host_tl_step0 = job.step0;
         }
         h->host_tl.push_back(mt_timeline_rec{job.unit, 4, ms(tw), ms(tc)});
         h->host_tl.push_back(mt_timeline_rec{job.unit, 3, ms(tc), t_end});
@@ -1282,7 +1291,17 @@ int mt_profile_timeline(mt_handle* h, mt_timeline_rec* out, int cap, int* n_out)
   std::vector<mt_timeline_rec> all = h->timeline;
   {
     std::lock_guard<std::mutex> lk(h->mu);
-    if (h->host_tl_seq == h->timeline_seq) all.insert(all.end(), h->host_tl.begin(), h->host_tl.end());
+    if (h->host_tl_seq == h->timeline_seq) {
+      all.insert(all.end(), h->host_tl.begin(), h->host_tl.end());
+      // the previous step's worker intervals that run into this step (its
+      // host tail under overlap_adam), on this step's clock, as streams 5, 6
+      if (h->host_tl_prev_seq == h->timeline_seq - 1) {
+        const double dt =
+            std::chrono::duration<double, std::milli>(h->host_tl_prev_step0 - h->host_tl_step0).count();
+        for (const auto& r : h->host_tl_prev)
+          if (r.end_ms + dt > 0.0) all.push_back(mt_timeline_rec{r.cls, r.stream + 2, r.start_ms + dt, r.end_ms + dt});
+      }
+    }
   }
   const int n = (int)all.size();
   for (int i = 0; i < n && i < cap; ++i) out[i] = all[i];

@@ -231,9 +231,13 @@ void adam_pass(const AdamArgs& a, int threads) {
   else adam_acc<false, false, false>(a, threads);
 }
 
+// Every core: the pass takes 64K-element chunks from a shared counter, so a
+// thread that shares its core with the launching thread or the driver holds
+// up nothing. Measured in the 7B step on the 16-core Grace host: 16 threads
+// 8,159-8,298 tokens/s against 7,892-7,985 with 14.
 int default_threads() {
   const int n = omp_get_num_procs();
-  return n > 4 ? n - 2 : (n > 0 ? n : 1);
+  return n > 0 ? n : 1;
 }
 
 }  // namespace mt

@@ -11,6 +11,7 @@
 #include <cmath>
 #include <mutex>
 #include <string>
+#include <type_traits>
 
 #include "common.cuh"
 #include "mt_internal.h"
@@ -36,7 +37,7 @@ int* device_error_word() {
 
 namespace {
 
-constexpr int kNormBwdVec = 4;          // 8-element vectors per thread and row: 32 elements
+constexpr int kNormBwdVec = 4;          // 8-element vectors per thread and row, at most: 32 elements
 constexpr int kNormBwdMaxWarps = 8;     // warps per row: d <= 8 * 32 * 32 = 8192
 constexpr int kNormBwdMaxParts = 1216;  // row groups (dw partial sums): 8 per SM on 152 SMs (2 blocks of 4)
 
@@ -131,6 +132,52 @@ __global__ void rmsnorm_fwd_kernel(const TX* __restrict__ x, const bf16* __restr
   }
 }
 
+// One row per block of kNormFwdThreads threads, each holding up to VPT
+// vectors of 8 elements of the row in registers: x is read from HBM once
+// (sum of squares, fixed-order block sum, then y = x * rstd * w from the
+// registers). Rows up to 8 * VPT * kNormFwdThreads elements.
+constexpr int kNormFwdThreads = 128;
+template <typename TX, int VPT>
+__global__ void __launch_bounds__(kNormFwdThreads)
+    rmsnorm_fwd_row_kernel(const TX* __restrict__ x, const bf16* __restrict__ w, bf16* __restrict__ y,
+                           float* __restrict__ rstd, int d, float eps) {
+  __shared__ float red[kNormFwdThreads / 32];
+  const int row = blockIdx.x, tid = threadIdx.x;
+  const int nvec = d >> 3;
+  const TX* xr = x + (long long)row * d;
+  float v[VPT][8];
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int vi = tid + k * kNormFwdThreads;
+    if (vi < nvec) {
+      load_x8(xr + vi * 8, v[k]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss += v[k][i] * v[k][i];
+    }
+  }
+  ss = warp_sum(ss);
+  if ((tid & 31) == 0) red[tid >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int i = 0; i < kNormFwdThreads / 32; ++i) tot += red[i];
+  const float r = rsqrtf(tot / (float)d + eps);
+  if (tid == 0) rstd[row] = r;
+  bf16* yr = y + (long long)row * d;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int vi = tid + k * kNormFwdThreads;
+    if (vi < nvec) {
+      float g[8];
+      load_bf16x8(w + vi * 8, g);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[k][i] = v[k][i] * r * g[i];
+      store_bf16x8(yr + vi * 8, v[k]);
+    }
+  }
+}
+
 // ------------------------------------------------------------ RMSNorm bwd
 // Row groups of W warps (W = ceil(d / 1024)); each thread holds up to 32
 // elements of a row. Group g takes a contiguous range of rows; per row:
@@ -138,8 +185,8 @@ __global__ void rmsnorm_fwd_kernel(const TX* __restrict__ x, const bf16* __restr
 // group's warps), dx = rstd*w*dy - x*rstd^3*dot/d (+ dres), and the thread's
 // dw partial += dy*x*rstd. The group's partial goes to partial[g] and the
 // column sums run in a fixed order, so dw is deterministic.
-template <int W, typename TX>
-__global__ void __launch_bounds__(256, 2)
+template <int W, typename TX, int VEC>
+__global__ void __launch_bounds__(256, VEC == 2 ? 3 : 2)
     rmsnorm_bwd_kernel(const float* __restrict__ dy, const TX* __restrict__ x, const bf16* __restrict__ w,
                        const float* __restrict__ rstd, const float* dres, float* dx_f32, bf16* __restrict__ dx_bf16,
                        float* __restrict__ partial, int M, int d, int n_groups, int rows_per_group) {
@@ -151,10 +198,10 @@ __global__ void __launch_bounds__(256, 2)
   if (gid >= n_groups) return;  // whole groups leave together (named barriers count only their warps)
   const int nvec = d >> 3;
   const int r0 = gid * rows_per_group, r1 = min(M, r0 + rows_per_group);
-  uint4 wp[kNormBwdVec];                    // w as packed bf16 pairs
-  float acc[kNormBwdVec][8];
+  uint4 wp[VEC];                    // w as packed bf16 pairs
+  float acc[VEC][8];
 #pragma unroll
-  for (int k = 0; k < kNormBwdVec; ++k) {
+  for (int k = 0; k < VEC; ++k) {
     const int v = lane + 32 * (wg + W * k);
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[k][i] = 0.f;
@@ -164,11 +211,11 @@ __global__ void __launch_bounds__(256, 2)
     const float r = rstd[row];
     const float* dyr = dy + (long long)row * d;
     const TX* xr = x + (long long)row * d;
-    float dyv[kNormBwdVec][8];
-    XReg<TX> xp[kNormBwdVec];
+    float dyv[VEC][8];
+    XReg<TX> xp[VEC];
     float dot = 0.f;
 #pragma unroll
-    for (int k = 0; k < kNormBwdVec; ++k) {
+    for (int k = 0; k < VEC; ++k) {
       const int v = lane + 32 * (wg + W * k);
       if (v < nvec) {
         const float4 a = reinterpret_cast<const float4*>(dyr + v * 8)[0];
@@ -183,7 +230,7 @@ __global__ void __launch_bounds__(256, 2)
       }
     }
 #pragma unroll
-    for (int k = 0; k < kNormBwdVec; ++k) {
+    for (int k = 0; k < VEC; ++k) {
       const uint32_t ww[4] = {wp[k].x, wp[k].y, wp[k].z, wp[k].w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -203,7 +250,7 @@ __global__ void __launch_bounds__(256, 2)
     }
     const float c = r * r * r * tot / (float)d;
 #pragma unroll
-    for (int k = 0; k < kNormBwdVec; ++k) {
+    for (int k = 0; k < VEC; ++k) {
       const int v = lane + 32 * (wg + W * k);
       if (v < nvec) {
         const uint32_t ww[4] = {wp[k].x, wp[k].y, wp[k].z, wp[k].w};
@@ -232,7 +279,7 @@ __global__ void __launch_bounds__(256, 2)
     }
   }
 #pragma unroll
-  for (int k = 0; k < kNormBwdVec; ++k) {
+  for (int k = 0; k < VEC; ++k) {
     const int v = lane + 32 * (wg + W * k);
     if (v < nvec) {
       float* p = partial + (long long)gid * d + v * 8;
@@ -544,69 +591,98 @@ __global__ void embedding_bwd_reduce_kernel(const float* __restrict__ dx, const 
 }
 
 // ---------------------------------------------------------- cross entropy
-constexpr int kCeThreads = 256;
+constexpr int kCeThreads = 512;
+constexpr int kCeUnroll = 4;  // independent 16-byte loads in flight per thread
 
-__device__ __forceinline__ void online_merge(float& m, float& s, float m2, float s2) {
+
+// Merge of two (max, sum of 2^(y - max)) pairs in log2 units.
+__device__ __forceinline__ void online_merge2(float& m, float& s, float m2, float s2) {
   if (m2 > m) {
-    s = s * expf(m - m2) + s2;
+    s = s * ex2_approx(m - m2) + s2;
     m = m2;
   } else if (m2 != -INFINITY) {
-    s += s2 * expf(m2 - m);
+    s += s2 * ex2_approx(m2 - m);
   }
 }
 
-// Persistent: a grid of a few blocks per SM walks the rows, so the rows in
-// flight (blocks x V x 4 bytes) stay well inside L2 and the second pass over
-// a row (the gradient) reads it from L2 instead of HBM.
-__global__ void __launch_bounds__(kCeThreads)
+// Persistent: a grid of one or two 512-thread blocks per SM walks the rows,
+// so the rows in flight (blocks x V x 4 bytes) stay well inside L2 and the
+// second pass over a row (the gradient) reads it from L2 instead of HBM;
+// each thread keeps kCeUnroll 16-byte loads in flight. The exponentials run
+// in base 2 (e^x = 2^(x log2 e)) on the special-function unit: one fused
+// multiply-add and one ex2 per logit and pass.
+__global__ void __launch_bounds__(kCeThreads, 2)
     cross_entropy_kernel(const float* __restrict__ logits, long long ldl, const int32_t* __restrict__ labels,
                          bf16* __restrict__ dz, long long lddz, float* __restrict__ loss_rows, int M, int V,
                          float scale, int* err) {
+  constexpr float kL2e = 1.4426950408889634f, kLn2 = 0.6931471805599453f;
   __shared__ float sm_m[kCeThreads / 32], sm_s[kCeThreads / 32];
   const int tid = threadIdx.x;
-  for (int row = blockIdx.x; row < M; row += gridDim.x) {
-  const float* z = logits + (long long)row * ldl;
-  float m = -INFINITY, s = 0.f;
   const int nv = V >> 2;
-  for (int v = tid; v < nv; v += kCeThreads) {
-    const float4 q = reinterpret_cast<const float4*>(z)[v];
-    const float mx = fmaxf(fmaxf(q.x, q.y), fmaxf(q.z, q.w));
-    const float ls = expf(q.x - mx) + expf(q.y - mx) + expf(q.z - mx) + expf(q.w - mx);
-    online_merge(m, s, mx, ls);
-  }
+  for (int row = blockIdx.x; row < M; row += gridDim.x) {
+    const float* z = logits + (long long)row * ldl;
+    float m = -INFINITY, s = 0.f;  // log2 units: m = max of z log2 e, s = sum of 2^(z log2 e - m)
+    for (int v0 = tid; v0 < nv; v0 += kCeUnroll * kCeThreads) {
+      float4 q[kCeUnroll];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    online_merge(m, s, m2, s2);
-  }
-  __syncthreads();  // the previous row's reads of sm_m / sm_s are done
-  if ((tid & 31) == 0) { sm_m[tid >> 5] = m; sm_s[tid >> 5] = s; }
-  __syncthreads();
-  m = sm_m[0];
-  s = sm_s[0];
-  for (int i = 1; i < kCeThreads / 32; ++i) online_merge(m, s, sm_m[i], sm_s[i]);
-  const float lse = m + logf(s);
-  const int label = labels[row];
-  const bool lab_ok = label >= 0 && label < V;
-  if (tid == 0) {
-    if (!lab_ok) set_device_error(err, kDevErrBadToken);
-    loss_rows[row] = lse - (lab_ok ? z[label] : 0.f);
-  }
-  bf16* dr = dz + (long long)row * lddz;
-  for (int v = tid; v < nv; v += kCeThreads) {
-    const float4 q = reinterpret_cast<const float4*>(z)[v];
-    const int j = v * 4;
-    float p0 = expf(q.x - lse), p1 = expf(q.y - lse), p2 = expf(q.z - lse), p3 = expf(q.w - lse);
-    if (j == label) p0 -= 1.f;
-    if (j + 1 == label) p1 -= 1.f;
-    if (j + 2 == label) p2 -= 1.f;
-    if (j + 3 == label) p3 -= 1.f;
-    uint2 u;
-    u.x = pack_bf16x2(p0 * scale, p1 * scale);
-    u.y = pack_bf16x2(p2 * scale, p3 * scale);
-    *reinterpret_cast<uint2*>(dr + j) = u;
-  }
+      for (int u = 0; u < kCeUnroll; ++u) {
+        const int v = v0 + u * kCeThreads;
+        if (v < nv) q[u] = reinterpret_cast<const float4*>(z)[v];
+      }
+#pragma unroll
+      for (int u = 0; u < kCeUnroll; ++u) {
+        if (v0 + u * kCeThreads < nv) {
+          const float mx = fmaxf(fmaxf(q[u].x, q[u].y), fmaxf(q[u].z, q[u].w)) * kL2e;
+          const float ls = ex2_approx(fmaf(q[u].x, kL2e, -mx)) + ex2_approx(fmaf(q[u].y, kL2e, -mx)) +
+                           ex2_approx(fmaf(q[u].z, kL2e, -mx)) + ex2_approx(fmaf(q[u].w, kL2e, -mx));
+          online_merge2(m, s, mx, ls);
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+      online_merge2(m, s, m2, s2);
+    }
+    __syncthreads();  // the previous row's reads of sm_m / sm_s are done
+    if ((tid & 31) == 0) { sm_m[tid >> 5] = m; sm_s[tid >> 5] = s; }
+    __syncthreads();
+    m = sm_m[0];
+    s = sm_s[0];
+    for (int i = 1; i < kCeThreads / 32; ++i) online_merge2(m, s, sm_m[i], sm_s[i]);
+    const float lse2 = m + log2f(s);  // log2 of the softmax denominator
+    const int label = labels[row];
+    const bool lab_ok = label >= 0 && label < V;
+    if (tid == 0) {
+      if (!lab_ok) set_device_error(err, kDevErrBadToken);
+      loss_rows[row] = lse2 * kLn2 - (lab_ok ? z[label] : 0.f);
+    }
+    bf16* dr = dz + (long long)row * lddz;
+    for (int v0 = tid; v0 < nv; v0 += kCeUnroll * kCeThreads) {
+      float4 q[kCeUnroll];
+#pragma unroll
+      for (int u = 0; u < kCeUnroll; ++u) {
+        const int v = v0 + u * kCeThreads;
+        if (v < nv) q[u] = reinterpret_cast<const float4*>(z)[v];
+      }
+#pragma unroll
+      for (int u = 0; u < kCeUnroll; ++u) {
+        const int v = v0 + u * kCeThreads;
+        if (v >= nv) continue;
+        const int j = v * 4;
+        float p0 = ex2_approx(fmaf(q[u].x, kL2e, -lse2)), p1 = ex2_approx(fmaf(q[u].y, kL2e, -lse2));
+        float p2 = ex2_approx(fmaf(q[u].z, kL2e, -lse2)), p3 = ex2_approx(fmaf(q[u].w, kL2e, -lse2));
+        if (j == label) p0 -= 1.f;
+        if (j + 1 == label) p1 -= 1.f;
+        if (j + 2 == label) p2 -= 1.f;
+        if (j + 3 == label) p3 -= 1.f;
+        uint2 w;
+        w.x = pack_bf16x2(p0 * scale, p1 * scale);
+        w.y = pack_bf16x2(p2 * scale, p3 * scale);
+        *reinterpret_cast<uint2*>(dr + j) = w;
+      }
+    }
   }
 }
 
@@ -701,6 +777,32 @@ int mt_k_rmsnorm_fwd(const void* x, int x_f32, const void* w, void* y, float* rs
                      void* stream) {
   if (M < 0 || d <= 0 || d % 8 || !al16(x) || !al16(w) || !al16(y)) return MT_EINVAL;
   if (M == 0) return MT_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int vpt = (d / 8 + kNormFwdThreads - 1) / kNormFwdThreads;
+  if (vpt <= 8) {
+    auto go = [&](auto xt, auto vt) {
+      using TX = decltype(xt);
+      constexpr int V = decltype(vt)::value;
+      rmsnorm_fwd_row_kernel<TX, V><<<M, kNormFwdThreads, 0, st>>>((const TX*)x, (const bf16*)w, (bf16*)y, rstd, d,
+                                                                    eps);
+    };
+    auto by_vpt = [&](auto xt) {
+      switch (vpt) {
+        case 1: go(xt, std::integral_constant<int, 1>{}); break;
+        case 2: go(xt, std::integral_constant<int, 2>{}); break;
+        case 3: go(xt, std::integral_constant<int, 3>{}); break;
+        case 4: go(xt, std::integral_constant<int, 4>{}); break;
+        case 5: go(xt, std::integral_constant<int, 5>{}); break;
+        case 6: go(xt, std::integral_constant<int, 6>{}); break;
+        case 7: go(xt, std::integral_constant<int, 7>{}); break;
+        default: go(xt, std::integral_constant<int, 8>{}); break;
+      }
+    };
+    if (x_f32) by_vpt(0.f);
+    else by_vpt(bf16{});
+    return launch_ok();
+  }
+  // longer rows: one warp per row, two passes over x
   const int rows_per_block = 8;
   const dim3 grid((M + rows_per_block - 1) / rows_per_block), block(32 * rows_per_block);
   if (x_f32)
@@ -723,7 +825,10 @@ int mt_k_rmsnorm_bwd(const float* dy, const void* x, int x_f32, const void* w, c
   cudaStream_t st = (cudaStream_t)stream;
   const int parts = mt_k_rmsnorm_bwd_parts(M);
   if (M > 0) {
-    const int W = (d + 8 * kNormBwdVec * 32 - 1) / (8 * kNormBwdVec * 32);  // warps per row
+    // 16 elements a thread (more warps per row, more loads in flight) where
+    // 8 warps cover the row, else 32
+    const int vec = d <= 8 * 2 * 32 * kNormBwdMaxWarps ? 2 : kNormBwdVec;
+    const int W = (d + 8 * vec * 32 - 1) / (8 * vec * 32);  // warps per row
     const int rpg = (M + parts - 1) / parts;
     const int ngroups = (M + rpg - 1) / rpg;  // every group has at least one row
     auto go = [&](auto kernel, int w_, auto xt) {
@@ -732,18 +837,23 @@ int mt_k_rmsnorm_bwd(const float* dy, const void* x, int x_f32, const void* w, c
       kernel<<<(ngroups + g - 1) / g, 32 * w_ * g, 0, st>>>(dy, (const TX*)x, (const bf16*)w, rstd, dres, dx_f32,
                                                            (bf16*)dx_bf16, partial, M, d, ngroups, rpg);
     };
-    auto dispatch = [&](auto xt) {
+    auto by_w = [&](auto xt, auto vt) {
       using TX = decltype(xt);
+      constexpr int V = decltype(vt)::value;
       switch (W) {
-        case 1: go(rmsnorm_bwd_kernel<1, TX>, 1, xt); break;
-        case 2: go(rmsnorm_bwd_kernel<2, TX>, 2, xt); break;
-        case 3: go(rmsnorm_bwd_kernel<3, TX>, 3, xt); break;
-        case 4: go(rmsnorm_bwd_kernel<4, TX>, 4, xt); break;
-        case 5: go(rmsnorm_bwd_kernel<5, TX>, 5, xt); break;
-        case 6: go(rmsnorm_bwd_kernel<6, TX>, 6, xt); break;
-        case 7: go(rmsnorm_bwd_kernel<7, TX>, 7, xt); break;
-        default: go(rmsnorm_bwd_kernel<8, TX>, 8, xt); break;
+        case 1: go(rmsnorm_bwd_kernel<1, TX, V>, 1, xt); break;
+        case 2: go(rmsnorm_bwd_kernel<2, TX, V>, 2, xt); break;
+        case 3: go(rmsnorm_bwd_kernel<3, TX, V>, 3, xt); break;
+        case 4: go(rmsnorm_bwd_kernel<4, TX, V>, 4, xt); break;
+        case 5: go(rmsnorm_bwd_kernel<5, TX, V>, 5, xt); break;
+        case 6: go(rmsnorm_bwd_kernel<6, TX, V>, 6, xt); break;
+        case 7: go(rmsnorm_bwd_kernel<7, TX, V>, 7, xt); break;
+        default: go(rmsnorm_bwd_kernel<8, TX, V>, 8, xt); break;
       }
+    };
+    auto dispatch = [&](auto xt) {
+      if (vec == 2) by_w(xt, std::integral_constant<int, 2>{});
+      else by_w(xt, std::integral_constant<int, kNormBwdVec>{});
     };
     if (x_f32) dispatch(0.f);
     else dispatch(bf16{});
@@ -797,7 +907,8 @@ int mt_k_cross_entropy(const float* logits, int64_t ldl, const int32_t* labels, 
   if (M < 0 || V <= 0 || V % 4 || ldl < V || ldl % 4 || lddz < V || lddz % 4 || !al16(logits)) return MT_EINVAL;
   if ((reinterpret_cast<uintptr_t>(dz) & 7) != 0) return MT_EINVAL;
   if (M == 0) return MT_OK;
-  // rows in flight: 4 blocks per SM, fewer for long rows (at most ~48 MB)
+  // rows in flight: two blocks per SM, one for long rows (about 48 MB of
+  // logits in flight at most where the rows allow)
   static int sms[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -805,7 +916,7 @@ int mt_k_cross_entropy(const float* logits, int64_t ldl, const int32_t* labels, 
   if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
   const long long per_row = 4LL * V;
   long long blocks = (48LL << 20) / per_row;
-  blocks = std::max<long long>(sms[dev], std::min<long long>(blocks, 4LL * sms[dev]));
+  blocks = std::max<long long>(sms[dev], std::min<long long>(blocks, 2LL * sms[dev]));
   blocks = std::min<long long>(blocks, M);
   cross_entropy_kernel<<<(unsigned)blocks, kCeThreads, 0, (cudaStream_t)stream>>>(
       logits, ldl, labels, (bf16*)dz, lddz, loss_rows, M, V, scale, device_error_word());

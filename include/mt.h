@@ -59,7 +59,7 @@ typedef struct mt_config {
   float rope_theta;      /* RoPE base, e.g. 10000 */
   float lr, beta1, beta2, adam_eps; /* Adam, no weight decay */
   int32_t device;        /* CUDA device ordinal */
-  int32_t host_threads;  /* threads for host accumulate + Adam; 0 = all cores but two */
+  int32_t host_threads;  /* threads for host accumulate + Adam; 0 = every core */
   int32_t overlap_adam;  /* 1: mt_train_step returns once the device work and the loss are done while
                             the host worker finishes Adam on the last units; the next step uploads each
                             unit only after its Adam has finished. Results are identical to 0. Call
@@ -231,7 +231,9 @@ int mt_profile_read(mt_handle* h, mt_kernel_profile* out, int reset);
  * with CUDA events from the step's first compute-stream event; cls is its
  * MT_PROF_* class. stream 3: the host worker's accumulate + Adam pass over
  * unit cls; stream 4: the worker waiting for that unit's slab copy (host
- * clock from the start of the mt_train_step call). */
+ * clock from the start of the mt_train_step call); streams 5, 6: the same
+ * for units of the step before that ran into this one (its host tail when
+ * overlap_adam = 1), on this step's clock. */
 typedef struct mt_timeline_rec {
   int32_t cls;
   int32_t stream;

@@ -230,7 +230,10 @@ int64_t mt_k_embedding_bwd_work(int M, int V);
  * (V); larger sizes return MT_EINVAL with a message in mt_last_error(NULL).
  * It calls no allocation routine. The first call on a device looks up the
  * array's device address (cudaGetSymbolAddress, with that device current);
- * make that first call before any stream capture. All calls share the one
+ * make that first call before any stream capture. The address is kept for
+ * the life of the process: after cudaDeviceReset (or anything else that
+ * replaces the device's primary context) it is stale and the entry point
+ * must not be called again in that process. All calls share the one
  * array: calls that can overlap on the GPU (other streams, other threads)
  * race and must be serialised by the caller. Nothing a previous call left in
  * the array affects the result. Ids outside [0, V) are left out of the sums

@@ -91,3 +91,19 @@ def test_reference_arm_line_carries_the_repo_arms_config(capsys):
     assert line["impl"] == "reference"
     assert line["config"] == bench.config_dict(A, sh, 1, oracle.build_layout(sh).n_total)
     assert line["e2e"]["value"] == line["value"] and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_timeline_gap_classification():
+    """Idle gaps of the compute stream are split into time the host
+    optimizer was busy, time only a copy was, and the rest."""
+    import bench
+    tl = [{"stream": "compute", "cls": "gemm", "start_ms": 0, "end_ms": 10},
+          {"stream": "compute", "cls": "gemm", "start_ms": 20, "end_ms": 30},
+          {"stream": "compute", "cls": "ce", "start_ms": 40, "end_ms": 50},
+          {"stream": "h2d", "cls": "unit 1", "start_ms": 12, "end_ms": 18},
+          {"stream": "host_adam", "cls": "unit 1", "start_ms": 31, "end_ms": 35},
+          {"stream": "d2h", "cls": "unit 2", "start_ms": 33, "end_ms": 38}]
+    s = bench.timeline_summary(tl)
+    assert s["gpu_idle"] == {"ms": 20, "while_host_optimizer_busy_ms": 4.0, "copy_only_ms": 9.0, "neither_ms": 7.0}
+    assert s["h2d"]["hidden_frac"] == 0.0 and s["d2h"]["hidden_frac"] == 0.0
+    assert bench._subtract([(0, 10)], [(2, 3), (5, 12)]) == [(0, 2), (3, 5)]

@@ -10,13 +10,15 @@ inputs in test_library_cpu.py.
 Bars:
   * loss: relative error <= 5e-3;
   * every gradient tensor: relative L2 error <= 2e-2, except where bf16
-    operands alone come within 20% of that: there the bar is 1.25x the
+    operands alone reach 80% of that (1.6e-2): there the bar is 1.25x the
     tensor's operand floor. The floor is the error of oracle.bf16_emulation
     with rounding at the operands of the products and the gradient slab
     only (the bf16 operands and gradients the method prescribes) against
     the exact oracle (tests/golden/bf16_floor.json); the device keeps the
-    residual stream in fp32 and rounds nothing else that changes the result
-    by more than a few hundredths of that floor;
+    residual stream in fp32 and adds two roundings of its own (the saved
+    gate | up, dq / dk before the inverse rotation), which put its error
+    up to 0.03-0.09 points above the floor at 2 layers and up to 0.22 points
+    above it at the 1.1B workload's 22 layers;
   * post-Adam master: the library's Adam is fed the library's own FP32
     gradients and compared with the oracle's Adam on the same gradients,
     |err| <= 1e-6 * (lr / 1e-3) (an independent-gradient comparison cannot
@@ -83,7 +85,7 @@ def bf16_weights(master):
 
 def _bar(case, t, default=2e-2):
     """2e-2, or 1.25 x the bf16-operand floor of the tensor where that floor
-    is 1.6e-2 or more (within 20% of the bar)."""
+    is 1.6e-2 or more (bf16 operands alone at 80% of the bar or over it)."""
     floor = FLOORS.get(case, {}).get(f"{t.name}@{t.offset}", 0.0) if case else 0.0
     return max(default, 1.25 * floor) if floor >= 1.6e-2 else default
 

@@ -62,6 +62,26 @@ def test_noalloc_matches_regular_entry_point_twice(M, V, d):
         assert np.linalg.norm(got - exact) / np.linalg.norm(exact) <= 5e-3
 
 
+def test_noalloc_at_its_largest_accepted_sizes():
+    """M and V at the limits fill the fixed array exactly (start[V + 1],
+    cursor[V], perm[M]); the result must still be the regular entry point's,
+    bit for bit, twice in a row."""
+    fn = _noalloc()
+    M, V, d = 524288, 262144, 8
+    rng = np.random.default_rng(5)
+    for call in range(2):
+        tok = torch.from_numpy(rng.integers(0, V if call == 0 else 1000, size=M).astype(np.int32)).cuda()
+        dx = torch.from_numpy(rng.standard_normal((M, d)).astype(np.float32)).cuda()
+        ref = torch.empty((V, d), device="cuda", dtype=torch.bfloat16)
+        work = torch.empty(mt.k_embedding_bwd_work(M, V), device="cuda", dtype=torch.int32)
+        mt.k_embedding_bwd(dx, tok, ref, work)
+        out = torch.full((V, d), 7.0, device="cuda", dtype=torch.bfloat16)
+        code = fn(C.c_void_p(dx.data_ptr()), C.c_void_p(tok.data_ptr()), C.c_void_p(out.data_ptr()), M, d, V, None)
+        assert code == mt.MT_OK, mt.lib().mt_last_error(None)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref), f"call {call}"
+
+
 def test_noalloc_rejects_sizes_above_its_limits():
     fn = _noalloc()
     dx = torch.zeros((8, 64), device="cuda")
