@@ -841,6 +841,9 @@ def main():
                     help="RoPE and SwiGLU as separate kernels instead of GEMM epilogues (same results)")
     ap.add_argument("--fused-grads", action="store_true",
                     help="no FP32 gradient array: each slab goes straight into Adam (same arithmetic)")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="run the workload at this depth instead of its own (a reduced-depth variant, named as "
+                         "such in the line; for widths whose full-depth host state does not fit the host)")
     ap.add_argument("--micro-batches", type=int, default=1,
                     help="one step = this many micro-batches of gradient accumulation (host ids), Adam after the "
                          "last (global batch grows by this factor)")
@@ -856,6 +859,8 @@ def main():
     if args.kernel == "misc":
         return run_misc_kernels(args)
     shape = synth.workload(args.config)
+    if args.layers:
+        shape = shape.with_(name=f"{shape.name} ({args.layers} of {shape.n_layers} layers)", n_layers=args.layers)
     world, rank, local, pg = dist_setup()
     if args.impl == "reference":
         return run_reference(args, shape, world, rank, pg)

@@ -73,7 +73,7 @@ EXPORTS = [
     "mt_get_stream", "mt_profile_enable", "mt_profile_read", "mt_profile_timeline", "mt_destroy", "mt_last_error", "mt_debug_inject", "mt_debug_inject_global",
     "mt_host_adam", "mt_host_adam_slab", "mt_host_to_bf16",
     "mt_k_gemm", "mt_k_gemm_ex", "mt_k_gemm_rope", "mt_k_gemm_swiglu_fwd", "mt_k_gemm_swiglu_bwd", "mt_k_gemm_wgrad", "mt_k_gemm_splitk", "mt_k_gemm_tile_policy", "mt_k_gemm_wgrad_ws", "mt_k_rmsnorm_fwd", "mt_k_rmsnorm_bwd", "mt_k_rmsnorm_bwd_parts",
-    "mt_k_rope", "mt_k_swiglu_fwd", "mt_k_swiglu_bwd", "mt_k_attn_fwd", "mt_k_attn_fwd_mma", "mt_k_attn_bwd", "mt_k_attn_bwd_mma",
+    "mt_k_rope", "mt_k_swiglu_fwd", "mt_k_swiglu_bwd", "mt_k_attn_fwd", "mt_k_attn_fwd_mma", "mt_k_attn_bwd", "mt_k_attn_bwd_rope", "mt_k_attn_bwd_mma",
     "mt_k_cross_entropy", "mt_k_sum", "mt_k_embedding_fwd", "mt_k_embedding_bwd",
     "mt_k_embedding_bwd_work", "mt_k_check_ids", "mt_k_device_error",
 ]
@@ -136,6 +136,7 @@ def lib():
         "mt_k_attn_fwd": ([P, I64, P, I64, P, I, I, I, I, I, P], I),
         "mt_k_attn_fwd_mma": ([P, I64, P, I64, P, I, I, I, I, I, P], I),
         "mt_k_attn_bwd": ([P, I64, P, I64, P, I64, P, P, P, I64, I, I, I, I, I, P], I),
+        "mt_k_attn_bwd_rope": ([P, I64, P, I64, P, I64, P, P, P, I64, I, I, I, I, I, P, P, P], I),
         "mt_k_attn_bwd_mma": ([P, I64, P, I64, P, I64, P, P, P, I64, I, I, I, I, I, P], I),
         "mt_k_cross_entropy": ([P, I64, P, P, I64, P, I, I, F, P], I),
         "mt_k_sum": ([P, I, P, P], I),
@@ -496,6 +497,13 @@ def k_attn_fwd_mma(qkv, o, lse, B, s, H, Hkv, hd, stream=None):
 def k_attn_bwd(qkv, o, dout, lse, delta, dqkv, B, s, H, Hkv, hd, stream=None):
     check(lib().mt_k_attn_bwd(_dp(qkv), qkv.stride(0), _dp(o), o.stride(0), _dp(dout), dout.stride(0), _dp(lse),
                               _dp(delta), _dp(dqkv), dqkv.stride(0), B, s, H, Hkv, hd, _st(stream)))
+
+
+def k_attn_bwd_rope(qkv, o, dout, lse, delta, dqkv, B, s, H, Hkv, hd, cos_t, sin_t, stream=None):
+    """Attention backward with dq, dk rotated back by RoPE's inverse."""
+    check(lib().mt_k_attn_bwd_rope(_dp(qkv), qkv.stride(0), _dp(o), o.stride(0), _dp(dout), dout.stride(0),
+                                   _dp(lse), _dp(delta), _dp(dqkv), dqkv.stride(0), B, s, H, Hkv, hd, _dp(cos_t),
+                                   _dp(sin_t), _st(stream)))
 
 
 def k_attn_bwd_mma(qkv, o, dout, lse, delta, dqkv, B, s, H, Hkv, hd, stream=None):

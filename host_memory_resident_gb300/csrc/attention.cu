@@ -622,9 +622,10 @@ extern "C" int mt_k_attn_fwd_mma(const void* qkv, int64_t ldqkv, void* o, int64_
   }
 }
 
-extern "C" int mt_k_attn_bwd(const void* qkv, int64_t ldqkv, const void* o, int64_t ldo, const void* dout,
-                             int64_t lddo, const float* lse, float* delta, void* dqkv, int64_t lddqkv, int B, int s,
-                             int H, int Hkv, int hd, void* stream) {
+namespace {
+int attn_bwd_any(const void* qkv, int64_t ldqkv, const void* o, int64_t ldo, const void* dout, int64_t lddo,
+                 const float* lse, float* delta, void* dqkv, int64_t lddqkv, int B, int s, int H, int Hkv, int hd,
+                 const float* cos_t, const float* sin_t, void* stream) {
   if ((hd == 64 || hd == 128) && attn_args_ok(qkv, ldqkv, B, s, H, Hkv, hd) &&
       attn_args_ok(dout, lddo, B, s, H, Hkv, hd) && attn_args_ok(dqkv, lddqkv, B, s, H, Hkv, hd) &&
       ldqkv >= (int64_t)(H + 2 * Hkv) * hd && lddqkv >= (int64_t)(H + 2 * Hkv) * hd && ldo % 2 == 0 &&
@@ -639,9 +640,29 @@ extern "C" int mt_k_attn_bwd(const void* qkv, int64_t ldqkv, const void* o, int6
       attn_delta_kernel<128><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>((const bf16*)o, ldo, (const bf16*)dout,
                                                                          lddo, delta, B, s, H);
     if (cudaGetLastError() != cudaSuccess) return MT_ECUDA;
-    return attn_bwd_tc(qkv, ldqkv, dout, lddo, lse, delta, dqkv, lddqkv, B, s, H, Hkv, hd, st);
+    return attn_bwd_tc(qkv, ldqkv, dout, lddo, lse, delta, dqkv, lddqkv, B, s, H, Hkv, hd, cos_t, sin_t, st);
   }
-  return mt_k_attn_bwd_mma(qkv, ldqkv, o, ldo, dout, lddo, lse, delta, dqkv, lddqkv, B, s, H, Hkv, hd, stream);
+  const int r = mt_k_attn_bwd_mma(qkv, ldqkv, o, ldo, dout, lddo, lse, delta, dqkv, lddqkv, B, s, H, Hkv, hd, stream);
+  if (r != MT_OK || cos_t == nullptr) return r;
+  // the legacy path rotates back in a separate pass (bf16 in, bf16 out)
+  return mt_k_rope(dqkv, lddqkv, B, s, H + Hkv, hd, cos_t, sin_t, 1, stream);
+}
+}  // namespace
+
+extern "C" int mt_k_attn_bwd(const void* qkv, int64_t ldqkv, const void* o, int64_t ldo, const void* dout,
+                             int64_t lddo, const float* lse, float* delta, void* dqkv, int64_t lddqkv, int B, int s,
+                             int H, int Hkv, int hd, void* stream) {
+  return attn_bwd_any(qkv, ldqkv, o, ldo, dout, lddo, lse, delta, dqkv, lddqkv, B, s, H, Hkv, hd, nullptr, nullptr,
+                      stream);
+}
+
+extern "C" int mt_k_attn_bwd_rope(const void* qkv, int64_t ldqkv, const void* o, int64_t ldo, const void* dout,
+                                  int64_t lddo, const float* lse, float* delta, void* dqkv, int64_t lddqkv, int B,
+                                  int s, int H, int Hkv, int hd, const float* cos_t, const float* sin_t, void* stream) {
+  if (cos_t == nullptr || sin_t == nullptr || (reinterpret_cast<uintptr_t>(cos_t) & 15) ||
+      (reinterpret_cast<uintptr_t>(sin_t) & 15))
+    return MT_EINVAL;
+  return attn_bwd_any(qkv, ldqkv, o, ldo, dout, lddo, lse, delta, dqkv, lddqkv, B, s, H, Hkv, hd, cos_t, sin_t, stream);
 }
 
 extern "C" int mt_k_attn_bwd_mma(const void* qkv, int64_t ldqkv, const void* o, int64_t ldo, const void* dout,

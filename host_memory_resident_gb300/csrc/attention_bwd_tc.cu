@@ -62,6 +62,43 @@ __device__ __forceinline__ void tmem_row_to_bf16(uint32_t taddr, int ncols, floa
   }
 }
 
+// RoPE's inverse rotation on N columns of this thread's TMEM lane and their
+// partners hd/2 further (times scale), stored as bf16: (x1, x2) ->
+// (x1 c + x2 s, x2 c - x1 s) at the row's position, so dq / dk leave the
+// kernel as gradients of the un-rotated q / k, rounded once. cs / sn point at
+// the position's cos / sin entries of the N pairs.
+template <int N>
+__device__ __forceinline__ void tmem_pair_rope_to_bf16(uint32_t ta, uint32_t tb, float scale, const float* cs,
+                                                       const float* sn, bf16* da, bf16* db, bool store) {
+  uint32_t va[N], vb[N];
+  if constexpr (N == 32) {
+    tmem_ld_32x32b_x32(ta, va);
+    tmem_ld_32x32b_x32(tb, vb);
+  } else {
+    tmem_ld_32x32b_x16(ta, va);
+    tmem_ld_32x32b_x16(tb, vb);
+  }
+  tmem_ld_wait();
+  if (!store) return;
+  uint32_t pa[N / 2], pb[N / 2];
+#pragma unroll
+  for (int k = 0; k < N / 2; ++k) {
+    float o[2][2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int i = 2 * k + e;
+      rope_pair(__uint_as_float(va[i]) * scale, __uint_as_float(vb[i]) * scale, cs[i], -sn[i], o[0][e], o[1][e]);
+    }
+    pa[k] = pack_bf16x2(o[0][0], o[0][1]);
+    pb[k] = pack_bf16x2(o[1][0], o[1][1]);
+  }
+#pragma unroll
+  for (int j = 0; j < N / 8; ++j) {
+    reinterpret_cast<uint4*>(da)[j] = make_uint4(pa[4 * j], pa[4 * j + 1], pa[4 * j + 2], pa[4 * j + 3]);
+    reinterpret_cast<uint4*>(db)[j] = make_uint4(pb[4 * j], pb[4 * j + 1], pb[4 * j + 2], pb[4 * j + 3]);
+  }
+}
+
 // ------------------------------------------- dK / dV, 64-query sub-tiles
 // One CTA per (128-key tile, KV head, batch); it walks the group's query
 // heads and, per head, the 64-query sub-tiles at or after the diagonal.
@@ -100,7 +137,8 @@ __global__ void __launch_bounds__(kThr, 1)
     attn_bwd_dkdv_tc2_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_constant__ CUtensorMap tq64,
                              const __grid_constant__ CUtensorMap tdo64, const float* __restrict__ lse,
                              const float* __restrict__ delta, bf16* __restrict__ dqkv, long long lddq, int s, int H,
-                             int Hkv, int hc, int* err) {
+                             int Hkv, int hc, const float* __restrict__ cos_t, const float* __restrict__ sin_t,
+                             int* err) {
   using C = KvTc2<HD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024b(smem_raw);
@@ -325,10 +363,20 @@ __global__ void __launch_bounds__(kThr, 1)
       tc_fence_after();
       const bool store = key < s;
       const long long r0 = (long long)b * s + key;
-      if (G == 0)
+      bf16* dkrow = dqkv + r0 * lddq + (long long)kcol;
+      if (G == 0) {
         tmem_row_to_bf16(tdV + lane_off, HD, 1.f, dqkv + r0 * lddq + (long long)vcol, store);
-      else
-        tmem_row_to_bf16(tdK + lane_off, HD, rsqrtf((float)HD), dqkv + r0 * lddq + (long long)kcol, store);
+      } else if (cos_t == nullptr) {
+        tmem_row_to_bf16(tdK + lane_off, HD, rsqrtf((float)HD), dkrow, store);
+      } else {
+        // dk rotated back at the key's position (one 32-pair chunk per step)
+        const long long tb = (long long)(store ? key : 0) * (HD / 2);
+#pragma unroll 1
+        for (int j = 0; j < HD / 64; ++j)
+          tmem_pair_rope_to_bf16<32>(tdK + lane_off + j * 32, tdK + lane_off + HD / 2 + j * 32, rsqrtf((float)HD),
+                                     cos_t + tb + j * 32, sin_t + tb + j * 32, dkrow + j * 32,
+                                     dkrow + HD / 2 + j * 32, store);
+      }
     }
   }
   tc_fence_before();
@@ -368,7 +416,8 @@ template <int HD>
 __global__ void __launch_bounds__(kThr, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tqkv, const __grid_constant__ CUtensorMap tdo,
                           const float* __restrict__ lse, const float* __restrict__ delta, bf16* __restrict__ dqkv,
-                          long long lddq, int s, int H, int Hkv, int hc, int* err) {
+                          long long lddq, int s, int H, int Hkv, int hc, const float* __restrict__ cos_t,
+                          const float* __restrict__ sin_t, int* err) {
   using C = QTc<HD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024b(smem_raw);
@@ -558,8 +607,17 @@ __global__ void __launch_bounds__(kThr, 1)
     }
     if (ok && mbar_wait_warp(done, 0, err)) {
       tc_fence_after();
-      bf16* dqrow = dqkv + ((long long)b * s + qpos) * lddq + (long long)h * HD + half * (HD / 2);
-      tmem_row_to_bf16(tdQ + lane_off + half * (HD / 2), HD / 2, rsqrtf((float)HD), dqrow, qpos < s);
+      bf16* dqh = dqkv + ((long long)b * s + qpos) * lddq + (long long)h * HD;
+      if (cos_t == nullptr) {
+        tmem_row_to_bf16(tdQ + lane_off + half * (HD / 2), HD / 2, rsqrtf((float)HD), dqh + half * (HD / 2), qpos < s);
+      } else {
+        // dq rotated back at the query's position: this thread takes pairs
+        // [half * HD/4, (half + 1) * HD/4) and their partners HD/2 further
+        constexpr int N = HD / 4;
+        const long long tb = (long long)(qpos < s ? qpos : 0) * (HD / 2) + half * N;
+        tmem_pair_rope_to_bf16<N>(tdQ + lane_off + half * N, tdQ + lane_off + HD / 2 + half * N, rsqrtf((float)HD),
+                                  cos_t + tb, sin_t + tb, dqh + half * N, dqh + HD / 2 + half * N, qpos < s);
+      }
     }
   }
   tc_fence_before();
@@ -601,10 +659,11 @@ bool make_map3(CUtensorMap* m, const void* p, long long ld, int s, int B, int ro
 }  // namespace
 
 // Backward matrix products of attention on tcgen05 (hd 64 or 128); delta must
-// already hold rowsum(dO * O). Writes dq, dk, dv into dqkv.
+// already hold rowsum(dO * O). Writes dq, dk, dv into dqkv; with cos_t /
+// sin_t (RoPE tables [s_max, hd/2]) dq and dk are rotated back first.
 int attn_bwd_tc(const void* qkv, long long ld, const void* dout, long long lddo, const float* lse,
                 const float* delta, void* dqkv, long long lddq, int B, int s, int H, int Hkv, int hd,
-                cudaStream_t stream) {
+                const float* cos_t, const float* sin_t, cudaStream_t stream) {
   std::call_once(g_once, init_once);
   if (!g_enc) return MT_ECUDA;
   if (hd != 64 && hd != 128) return MT_EINVAL;
@@ -627,14 +686,14 @@ int attn_bwd_tc(const void* qkv, long long ld, const void* dout, long long lddo,
   const unsigned g1 = (unsigned)(nt * Hkv * B), g2 = (unsigned)(nt * H * B);
   if (hd == 64) {
     attn_bwd_dkdv_tc2_kernel<64><<<g1, kThr, KvTc2<64>::kSmem, stream>>>(tq, tq64, td64, lse, delta, (bf16*)dqkv,
-                                                                         lddq, s, H, Hkv, hc1, err);
+                                                                         lddq, s, H, Hkv, hc1, cos_t, sin_t, err);
     attn_bwd_dq_tc_kernel<64><<<g2, kThr, QTc<64>::kSmem, stream>>>(tq, td, lse, delta, (bf16*)dqkv, lddq, s, H, Hkv,
-                                                                   hc2, err);
+                                                                   hc2, cos_t, sin_t, err);
   } else {
     attn_bwd_dkdv_tc2_kernel<128><<<g1, kThr, KvTc2<128>::kSmem, stream>>>(tq, tq64, td64, lse, delta, (bf16*)dqkv,
-                                                                           lddq, s, H, Hkv, hc1, err);
+                                                                           lddq, s, H, Hkv, hc1, cos_t, sin_t, err);
     attn_bwd_dq_tc_kernel<128><<<g2, kThr, QTc<128>::kSmem, stream>>>(tq, td, lse, delta, (bf16*)dqkv, lddq, s, H,
-                                                                     Hkv, hc2, err);
+                                                                     Hkv, hc2, cos_t, sin_t, err);
   }
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {

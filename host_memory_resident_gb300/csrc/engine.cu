@@ -608,10 +608,12 @@ struct Step {
     // output projection
     gemm_wg(h->dhb, d, S.o, hq, g + o.wo, hq, d, hq);
     gemm_mn(h->dhb, d, false, W + o.wo, hq, true, h->dob, hq, false, M, hq, d);
-    // attention and RoPE
-    KP(MT_PROF_ATTN_BWD, 3, attn_flops(true), 0.0,
-       mt_k_attn_bwd(S.qkv, qn, S.o, hq, h->dob, hq, S.lse, h->delta, h->dqkv, qn, B, s, h->H, h->Hkv, h->hd, cs()));
-    KP(MT_PROF_ROPE, 1, 0.0, rope_bytes(), mt_k_rope(h->dqkv, qn, B, s, h->H + h->Hkv, h->hd, h->cos_t, h->sin_t, 1, cs()));
+    // attention, and RoPE's inverse rotation of dq / dk (in the tcgen05
+    // kernels' stores at hd 64 / 128; a separate pass at hd 16)
+    const bool tc_attn = h->hd == 64 || h->hd == 128;
+    KP(MT_PROF_ATTN_BWD, tc_attn ? 3 : 4, attn_flops(true), 0.0,
+       mt_k_attn_bwd_rope(S.qkv, qn, S.o, hq, h->dob, hq, S.lse, h->delta, h->dqkv, qn, B, s, h->H, h->Hkv, h->hd,
+                          h->cos_t, h->sin_t, cs()));
     // qkv projection
     gemm_wg(h->dqkv, qn, S.u, d, g + o.wqkv, d, qn, d);
     gemm_mn(h->dqkv, qn, false, W + o.wqkv, d, true, h->dn32, d, true, M, d, qn);

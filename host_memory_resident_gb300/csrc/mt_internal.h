@@ -62,9 +62,11 @@ int attn_fwd_tc(const void* qkv, long long ld, void* o, long long ldo, float* ls
                 int hd, cudaStream_t stream);
 
 // Attention backward products on tcgen05 (hd 64 or 128); delta precomputed.
+// With cos_t / sin_t non-null, dq and dk are stored rotated back (RoPE's
+// inverse at position row mod s).
 int attn_bwd_tc(const void* qkv, long long ld, const void* dout, long long lddo, const float* lse,
                 const float* delta, void* dqkv, long long lddq, int B, int s, int H, int Hkv, int hd,
-                cudaStream_t stream);
+                const float* cos_t, const float* sin_t, cudaStream_t stream);
 
 // dst[i] = bf16(src[i]) for i < n (round to nearest even).
 int convert_f32_bf16(const float* src, void* dst, long long n, cudaStream_t stream);

@@ -184,6 +184,20 @@ int mt_k_attn_bwd(const void* qkv, int64_t ldqkv, const void* o, int64_t ldo, co
                   const float* lse, float* delta, void* dqkv, int64_t lddqkv, int B, int s, int H, int Hkv, int hd,
                   void* stream);
 
+/*
+ * The same backward with RoPE's inverse rotation applied to dq and dk before
+ * they are stored (position = row mod s; cos_t / sin_t fp32 [s_max, hd/2],
+ * 16-byte aligned, as mt_k_rope), so dqkv holds the gradients w.r.t. the
+ * un-rotated q, k and v. At hd 64 / 128 the rotation runs on the fp32
+ * accumulators in the tcgen05 kernels' stores (dq and dk rounded to bf16
+ * once); at hd 16 it is mt_k_attn_bwd followed by mt_k_rope (inverse = 1).
+ * The backward of the decoder layer's "RoPE then attention" (the stateless
+ * template, zhichai.net article point 4).
+ */
+int mt_k_attn_bwd_rope(const void* qkv, int64_t ldqkv, const void* o, int64_t ldo, const void* dout, int64_t lddo,
+                       const float* lse, float* delta, void* dqkv, int64_t lddqkv, int B, int s, int H, int Hkv,
+                       int hd, const float* cos_t, const float* sin_t, void* stream);
+
 /* The same backward on the legacy mma.sync path (any hd); mt_k_attn_bwd uses
  * it for hd = 16 and runs hd 64 / 128 on tcgen05. Kept for comparison. */
 int mt_k_attn_bwd_mma(const void* qkv, int64_t ldqkv, const void* o, int64_t ldo, const void* dout, int64_t lddo,

@@ -423,6 +423,40 @@ def test_attention_bwd(B, s, H, Hkv, hd):
     assert_close(g[:, (H + Hkv) * hd:], dv.reshape(B * s, -1), l2=2e-2, elem=3e-2, what="dv")
 
 
+@pytest.mark.parametrize("B,s,H,Hkv,hd", [(2, 32, 4, 4, 16), (2, 130, 4, 1, 64), (1, 257, 2, 2, 128),
+                                          (2, 300, 8, 2, 128)])
+def test_attention_bwd_with_rope_inverse(B, s, H, Hkv, hd):
+    """dq and dk rotated back by RoPE's inverse in the backward's stores: the
+    oracle's attention backward followed by its RoPE backward; at hd 64 / 128
+    within one bf16 rounding of the rotation of the unfused kernel's fp32
+    result (so rounded once), and closer to the exact values than the
+    unfused sequence (backward to bf16, then the separate rotation)."""
+    qkv, q, k, v = _attn_inputs(B, s, H, Hkv, hd, s * hd + 5)
+    o = torch.empty((B * s, H * hd), device=DEV, dtype=torch.bfloat16)
+    lse = torch.empty((B, H, s), device=DEV)
+    mt.k_attn_fwd(qkv, o, lse, B, s, H, Hkv, hd)
+    rng = np.random.default_rng(s + 1)
+    do, doh = bf(rng.standard_normal((B * s, H * hd)))
+    cos, sin = ops.rope_tables(s, hd, 10000.0)
+    ct, _ = f32(cos)
+    st, _ = f32(sin)
+    delta = torch.empty((B, H, s), device=DEV)
+    got = torch.zeros_like(qkv)
+    mt.k_attn_bwd_rope(qkv, o, do, lse, delta, got, B, s, H, Hkv, hd, ct, st)
+    twice = torch.zeros_like(qkv)
+    mt.k_attn_bwd(qkv, o, do, lse, delta, twice, B, s, H, Hkv, hd)
+    mt.k_rope(twice, B, s, H + Hkv, hd, ct, st, inverse=True)
+    torch.cuda.synchronize()
+    dq, dk, dv = ops.attention_bwd(q, k, v, doh.reshape(B, s, H, hd))
+    dq, dk = ops.rope_bwd(dq, cos, sin), ops.rope_bwd(dk, cos, sin)
+    g, g2 = host(got), host(twice)
+    exact_qk = np.concatenate([dq.reshape(B * s, -1), dk.reshape(B * s, -1)], 1)
+    assert_close(g[:, :(H + Hkv) * hd], exact_qk, l2=2e-2, elem=3e-2, what="dq, dk rotated back")
+    assert torch.equal(got[:, (H + Hkv) * hd:], twice[:, (H + Hkv) * hd:])   # dv untouched
+    if hd != 16:
+        assert rel_l2(g[:, :(H + Hkv) * hd], exact_qk) < rel_l2(g2[:, :(H + Hkv) * hd], exact_qk)
+
+
 # ------------------------------------------------------------ cross entropy
 @pytest.mark.parametrize("M,V", [(64, 512), (37, 32000), (5, 152064), (2000, 512), (400, 152064)])
 def test_cross_entropy(M, V):

@@ -15,10 +15,11 @@ Bars:
     with rounding at the operands of the products and the gradient slab
     only (the bf16 operands and gradients the method prescribes) against
     the exact oracle (tests/golden/bf16_floor.json); the device keeps the
-    residual stream in fp32 and adds two roundings of its own (the saved
-    gate | up, dq / dk before the inverse rotation), which put its error
-    up to 0.03-0.09 points above the floor at 2 layers and up to 0.22 points
-    above it at the 1.1B workload's 22 layers;
+    residual stream in fp32 and adds one rounding of its own (the saved
+    gate | up the SwiGLU backward reads; at head dim 16 also dq / dk before
+    the separate inverse rotation), which with fp32 summation order puts its
+    error up to 0.03-0.09 points above the floor at 2 layers and up to 0.18
+    points above it at the 1.1B workload's 22 layers;
   * post-Adam master: the library's Adam is fed the library's own FP32
     gradients and compared with the oracle's Adam on the same gradients,
     |err| <= 1e-6 * (lr / 1e-3) (an independent-gradient comparison cannot
