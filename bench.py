@@ -281,58 +281,75 @@ def gemm_traffic_record():
 # ----------------------------------------------------------- CPU baseline
 def oracle_sample(shape, max_tokens=16384):
     """Time the oracle on a bounded sample of the workload and compose the
-    full step: B * (L * t_layer + t_rest) + t_adam(N). The sample is one
-    sequence at full width through a 1-layer and a 2-layer model (t_layer =
-    their difference), plus Adam on a 2^24-element slice. Sequences longer
-    than ``max_tokens`` are timed at max_tokens / 2 and max_tokens and each
-    term is extrapolated as a s + b s^2 (the attention part grows with s^2)."""
+    full step. Timed directly on one sequence of ss = min(seq, max_tokens)
+    tokens at full width: one layer's forward (oracle.layer_forward) and
+    backward (oracle.layer_backward), the attention core inside them
+    (oracle.ops.attention_fwd / attention_bwd) on its own, and the head
+    (final RMSNorm, logits, cross entropy and their backward). The oracle's
+    step runs every layer's forward twice (forward, recompute from the
+    checkpoints) and its backward once: t_layer = 2 t_fwd + t_bwd. For a
+    longer sequence s the attention part is scaled by (s / ss)^2 and the
+    rest of the layer and the head by s / ss. Then
+    step = B (L t_layer + t_head) + Adam on the N parameters (a 2^24 slice
+    scaled)."""
     import oracle
+    from oracle import ops
     s = shape.seq
-
-    def sample(seq):
-        toks, labs = synth.make_tokens(shape.vocab, 1, seq, seed=1)
-        times = {}
-        for L in (1, 2):
-            sh = shape.with_(n_layers=L, ckpt_interval=1)
-            lay = oracle.build_layout(sh)
-            master = synth.init_master(lay.n_total, lay.segments(), seed=0)
-            t0 = time.perf_counter()
-            oracle.step_grads(sh, master, toks, labs, dtype=np.float32)
-            times[L] = time.perf_counter() - t0
-            del master
-        return times
-
-    extrapolated = ""
-    if s > max_tokens:
-        s1, s2 = max_tokens // 2, max_tokens
-        ta, tb = sample(s1), sample(s2)
-        times = {}
-        for L in (1, 2):
-            b2 = (tb[L] - 2.0 * ta[L]) / (s2 * float(s2) - 2.0 * s1 * float(s1))
-            a1 = (ta[L] - b2 * s1 * float(s1)) / s1
-            times[L] = max(a1, 0.0) * s + max(b2, 0.0) * s * s
-        extrapolated = f"extrapolated from {s1} and {s2} tokens as a s + b s^2; "
-    else:
-        times = sample(s)
-    n = 1 << 24
+    ss = min(s, max_tokens)
+    d, hd, H, Hkv = shape.d_model, shape.head_dim, shape.n_heads, shape.n_kv_heads
+    sh1 = shape.with_(n_layers=1, ckpt_interval=1)
+    lay = oracle.build_layout(sh1)
+    master = synth.init_master(lay.n_total, lay.segments(), seed=0)
+    P = {t.name: master[t.offset:t.offset + t.size].reshape(t.shape) for t in lay.units[1].tensors}
+    Ph = {t.name: master[t.offset:t.offset + t.size].reshape(t.shape) for t in lay.units[2].tensors}
     rng = np.random.default_rng(0)
+    x = rng.standard_normal((ss, d)).astype(np.float32)
+    dy = (rng.standard_normal((ss, d)) * 1e-3).astype(np.float32)
+    cos, sin = ops.rope_tables(ss, hd, shape.rope_theta, np.float32)
+    t0 = time.perf_counter()
+    _, cache = oracle.layer_forward(sh1, P, x, cos, sin, 1, ss)
+    t1 = time.perf_counter()
+    oracle.layer_backward(sh1, P, dy, cache, cos, sin, 1, ss)
+    t2 = time.perf_counter()
+    t_layer_ss = 2.0 * (t1 - t0) + (t2 - t1)
+    q = rng.standard_normal((1, ss, H, hd)).astype(np.float32)
+    k = rng.standard_normal((1, ss, Hkv, hd)).astype(np.float32)
+    v = rng.standard_normal((1, ss, Hkv, hd)).astype(np.float32)
+    t0 = time.perf_counter()
+    ops.attention_fwd(q, k, v)
+    t1 = time.perf_counter()
+    ops.attention_bwd(q, k, v, q)
+    t2 = time.perf_counter()
+    t_att_ss = min(2.0 * (t1 - t0) + (t2 - t1), t_layer_ss)
+    labels = rng.integers(0, shape.vocab, size=ss)
+    t0 = time.perf_counter()
+    xh, rf = ops.rmsnorm_fwd(x, Ph["final_norm"], shape.rms_eps)
+    _, dlogits = ops.cross_entropy_fwd_bwd(ops.linear_fwd(xh, Ph["head"]), labels)
+    dxh, _ = ops.linear_bwd(dlogits, xh, Ph["head"])
+    ops.rmsnorm_bwd(dxh, x, Ph["final_norm"], rf)
+    t_head_ss = time.perf_counter() - t0
+    del master, cache
+    r = s / ss
+    t_layer = (t_layer_ss - t_att_ss) * r + t_att_ss * r * r
+    t_head = t_head_ss * r
+    n = 1 << 24
     w = rng.standard_normal(n).astype(np.float32)
     g = rng.standard_normal(n).astype(np.float32) * 1e-3
     t0 = time.perf_counter()
     oracle.adam_update(w, np.zeros(n, np.float32), np.zeros(n, np.float32), g, 1, shape.lr, shape.beta1,
                        shape.beta2, shape.adam_eps, dtype=np.float32)
     t_adam_slice = time.perf_counter() - t0
-    t_layer = max(times[2] - times[1], 1e-9)
-    t_rest = max(times[1] - t_layer, 0.0)
     lay_full = oracle.build_layout(shape)
     t_adam = t_adam_slice * lay_full.n_total / n
-    t_step = shape.batch * (shape.n_layers * t_layer + t_rest) + t_adam
+    t_step = shape.batch * (shape.n_layers * t_layer + t_head) + t_adam
+    scaled = f"timed at {ss} of {s} tokens, attention scaled by (s/ss)^2, the rest by s/ss; " if ss < s else ""
     return {
         "value": shape.batch * s / t_step, "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
-        "sample": (f"composed: {extrapolated}1 sequence of {s} tokens through 1- and 2-layer full-width models "
-                   f"(t_layer {t_layer:.2f} s, rest {t_rest:.2f} s, float32 numpy) + Adam on 2^24 elements "
-                   f"scaled to {lay_full.n_total} params; step = {shape.batch} x ({shape.n_layers} t_layer + rest)"
-                   f" + Adam = {t_step:.1f} s"),
+        "sample": (f"composed from one full-width layer's forward and backward, its attention core and the head on "
+                   f"one sequence (float32 numpy; {scaled}t_layer {t_layer:.2f} s = 2 forwards + 1 backward, of which "
+                   f"attention {t_att_ss * r * r:.2f} s; t_head {t_head:.2f} s) + Adam on 2^24 elements scaled to "
+                   f"{lay_full.n_total} params; step = {shape.batch} x ({shape.n_layers} t_layer + t_head) + Adam = "
+                   f"{t_step:.1f} s"),
     }
 
 
@@ -410,7 +427,7 @@ def run_reference(args, shape, world, rank, pg):
     base = None
     for i in range(args.warmup + args.steps):
         # each step is a bounded sample (sequences over 512 tokens timed at
-        # 256 and 512 and extrapolated) so the whole run takes a few minutes
+        # 256 and 512 and extended) so the whole run takes a few minutes
         b = oracle_sample(shape, max_tokens=REFERENCE_MAX_TOKENS)
         if i >= args.warmup:
             vals.append(b["value"])
