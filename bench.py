@@ -234,11 +234,18 @@ def timeline_summary(tl):
            "host_adam_busy_ms": sum(b - a for a, b in host),
            "host_adam_prev_step_ms": sum(b - a for a, b in _union(ivs("host_adam_prev"))),
            "host_and_gpu_busy_ms": _overlap(host, comp)}
+    # a copy costs the device time only where it runs in an idle gap of the
+    # compute stream while the host optimizer is not busy
+    gaps0 = [(b0, a1) for (a0, b0), (a1, b1) in zip(comp, comp[1:]) if a1 > b0]
+    host_any = _union(ivs("host_adam") + ivs("host_adam_prev"))
+    exposed_gaps = _subtract(gaps0, host_any)
     for k in ("h2d", "d2h"):
         iv = ivs(k)
         t = sum(b - a for a, b in iv)
+        ex = _overlap(_union(iv), exposed_gaps)
         out[k] = {"copies": len(iv), "ms": t, "hidden_under_compute_ms": _overlap(iv, comp),
-                  "hidden_frac": _overlap(iv, comp) / t if t else None}
+                  "hidden_frac": _overlap(iv, comp) / t if t else None,
+                  "exposed_ms": ex, "not_exposed_frac": 1.0 - ex / t if t else None}
     # Compute-stream idle gaps between the step's first and last launch, by
     # what else was busy: the host optimizer (the device work waits for its
     # updated weights or free slabs), only a copy (waiting on the host link),

@@ -106,4 +106,7 @@ def test_timeline_gap_classification():
     s = bench.timeline_summary(tl)
     assert s["gpu_idle"] == {"ms": 20, "while_host_optimizer_busy_ms": 4.0, "copy_only_ms": 9.0, "neither_ms": 7.0}
     assert s["h2d"]["hidden_frac"] == 0.0 and s["d2h"]["hidden_frac"] == 0.0
+    # the d2h copy runs 2 ms of its 5 under the host optimizer: not exposed
+    assert s["h2d"]["exposed_ms"] == 6.0 and s["d2h"]["exposed_ms"] == 3.0
+    assert abs(s["d2h"]["not_exposed_frac"] - 0.4) < 1e-12
     assert bench._subtract([(0, 10)], [(2, 3), (5, 12)]) == [(0, 2), (3, 5)]
