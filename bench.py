@@ -638,16 +638,17 @@ def host_mem_available():
     return None
 
 
-def host_memory_refusal(mt, cfg, shape, keep_grads, avail):
-    """The error line for a workload whose host state and pinned buffers
-    exceed 90% of the available host memory `avail` (bytes), else None."""
+def host_memory_refusal(mt, cfg, shape, keep_grads, avail, ranks=1):
+    """The error line for a workload whose host state and pinned buffers,
+    times the `ranks` replicas on this host, exceed 90% of the available
+    host memory `avail` (bytes), else None."""
     plan = mt.plan(cfg)
-    need = plan["host_state_bytes"] * (16 if keep_grads else 12) // 16 + plan["pinned_bytes"]
+    need = (plan["host_state_bytes"] * (16 if keep_grads else 12) // 16 + plan["pinned_bytes"]) * ranks
     if avail is None or need <= 0.9 * avail:
         return None
     return {"metric": METRIC, "config": {"workload": shape.name}, "value": None,
-            "error": f"host memory: the workload needs {need / 1e9:.1f} GB of host state and "
-                     f"pinned buffers, {avail / 1e9:.1f} GB available"}
+            "error": f"host memory: {ranks} replica(s) of the workload need {need / 1e9:.1f} GB of host state "
+                     f"and pinned buffers, {avail / 1e9:.1f} GB available"}
 
 
 def run_ours(args, shape, world, rank, local, pg):
@@ -658,7 +659,8 @@ def run_ours(args, shape, world, rank, local, pg):
     descs, n_total = mt.layout(cfg)
     # refuse, before touching the GPU or allocating, a workload whose host
     # state and pinned buffers do not fit the host's memory (14B: ~285 GB)
-    refusal = host_memory_refusal(mt, cfg, shape, args.keep_grads, host_mem_available())
+    local_ranks = int(os.environ.get("LOCAL_WORLD_SIZE", world))
+    refusal = host_memory_refusal(mt, cfg, shape, args.keep_grads, host_mem_available(), ranks=local_ranks)
     if refusal is not None:
         if rank == 0:
             print(json.dumps(refusal), flush=True)

@@ -823,12 +823,21 @@ int mt_k_rmsnorm_bwd(const float* dy, const void* x, int x_f32, const void* w, c
       (dx_bf16 && !al16(dx_bf16)) || !al16(partial))
     return MT_EINVAL;
   cudaStream_t st = (cudaStream_t)stream;
-  const int parts = mt_k_rmsnorm_bwd_parts(M);
+  // 16 elements a thread (more warps per row, more loads in flight) where
+  // 8 warps cover the row, else 32
+  const int vec = d <= 8 * 2 * 32 * kNormBwdMaxWarps ? 2 : kNormBwdVec;
+  // row groups: one wave of resident blocks (no tail wave, and fewer dw
+  // partial rows for the column sums), at most mt_k_rmsnorm_bwd_parts(M)
+  static int sms[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return MT_ECUDA;
+  if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+  const int w_row = (d + 8 * vec * 32 - 1) / (8 * vec * 32);
+  const int resident = sms[dev] * (vec == 2 ? 3 : 2) * (8 / w_row > 0 ? 8 / w_row : 1);
+  const int parts = std::min(mt_k_rmsnorm_bwd_parts(M), std::max(resident, 1));
   if (M > 0) {
-    // 16 elements a thread (more warps per row, more loads in flight) where
-    // 8 warps cover the row, else 32
-    const int vec = d <= 8 * 2 * 32 * kNormBwdMaxWarps ? 2 : kNormBwdVec;
-    const int W = (d + 8 * vec * 32 - 1) / (8 * vec * 32);  // warps per row
+    const int W = w_row;  // warps per row
     const int rpg = (M + parts - 1) / parts;
     const int ngroups = (M + rpg - 1) / rpg;  // every group has at least one row
     auto go = [&](auto kernel, int w_, auto xt) {

@@ -65,12 +65,15 @@ def test_bench_refuses_workloads_beyond_host_memory():
 
 def test_default_workload_fits_the_host():
     """The bench's default workload (7B: about 126 GB of host state and
-    pinned buffers) fits 199 GB of host memory."""
+    pinned buffers) fits 199 GB of host memory once, not twice: replicas on
+    one host are refused before anything is allocated."""
     import bench
     import host_memory_resident_gb300 as mt
     import synth
     sh = synth.workload("7b")
     assert bench.host_memory_refusal(mt, mt.make_config(sh), sh, True, 199 * 2**30) is None
+    r = bench.host_memory_refusal(mt, mt.make_config(sh), sh, True, 199 * 2**30, ranks=2)
+    assert r is not None and "2 replica(s)" in r["error"]
 
 
 def test_reference_arm_line_carries_the_repo_arms_config(capsys):
