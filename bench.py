@@ -807,7 +807,7 @@ def run_ours(args, shape, world, rank, local, pg):
         "host_bound": {"adam_probe_gbs": adam_gbs, "t_host_s": hb * n_total / (adam_gbs * 1e9),
                        "frac": hb * n_total / (adam_gbs * 1e9) / t_step, "bytes_per_param": hb,
                        "note": "host Adam + bf16 emit (+ FP32 grad out when kept) over the rate the same pass "
-                               "reaches alone on one layer-sized slice; the north-star roofline leaves this "
+                               "reaches alone on one layer-sized slice; the step roofline (FLOPs vs host link) leaves this "
                                "bound out"},
         "kernels": prof_out,
         "copies": copies,

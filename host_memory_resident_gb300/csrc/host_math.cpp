@@ -232,7 +232,7 @@ void adam_pass(const AdamArgs& a, int threads) {
 }
 
 // Every core: the pass takes 64K-element chunks from a shared counter, so a
-// thread that shares its core with the launching thread or the driver holds
+// thread that shares its core with the launching thread or the CUDA driver holds
 // up nothing. Measured in the 7B step on the 16-core Grace host: 16 threads
 // 8,159-8,298 tokens/s against 7,892-7,985 with 14.
 int default_threads() {
