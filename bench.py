@@ -704,6 +704,7 @@ def run_ours(args, shape, world, rank, local, pg):
 
     for i in range(W):
         step_dev(i)
+    tr.sync()  # the warm-up's host Adam (overlap mode) ends before the timed region starts
 
     # ---- timed region: K steps, token/label arrays resident in device memory,
     # per-launch profiling off (the per-class profile is a separate pass below)

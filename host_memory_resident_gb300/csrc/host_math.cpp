@@ -204,18 +204,29 @@ static void adam_acc(const AdamArgs& a, int threads) {
 
 void adam_pass(const AdamArgs& a, int threads) {
   if (!a.apply) {
-    // gradient only: set or add to the running sum (no optimizer update)
+    // gradient only: set or add to the running sum (no optimizer update),
+    // in chunks from a shared counter like the optimizer pass
     if (!a.grad_out) return;
     float* __restrict__ gout = a.grad_out;
     const uint16_t* __restrict__ slab = a.slab;
     const float* __restrict__ gin = a.grad_in;
     const int64_t n = a.n;
-    if (a.accumulate) {
-#pragma omp parallel for schedule(static) num_threads(threads)
-      for (int64_t i = 0; i < n; ++i) gout[i] += slab ? bf16_to_f32(slab[i]) : gin[i];
-    } else {
-#pragma omp parallel for schedule(static) num_threads(threads)
-      for (int64_t i = 0; i < n; ++i) gout[i] = slab ? bf16_to_f32(slab[i]) : gin[i];
+    const bool acc = a.accumulate;
+    std::atomic<int64_t> next{0};
+#pragma omp parallel num_threads(threads)
+    for (;;) {
+      const int64_t c0 = next.fetch_add(kAdamChunk, std::memory_order_relaxed);
+      if (c0 >= n) break;
+      const int64_t c1 = c0 + kAdamChunk < n ? c0 + kAdamChunk : n;
+      if (slab && acc) {
+        for (int64_t i = c0; i < c1; ++i) gout[i] += bf16_to_f32(slab[i]);
+      } else if (slab) {
+        for (int64_t i = c0; i < c1; ++i) gout[i] = bf16_to_f32(slab[i]);
+      } else if (acc) {
+        for (int64_t i = c0; i < c1; ++i) gout[i] += gin[i];
+      } else {
+        for (int64_t i = c0; i < c1; ++i) gout[i] = gin[i];
+      }
     }
     return;
   }
