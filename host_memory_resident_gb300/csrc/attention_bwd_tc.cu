@@ -4,13 +4,13 @@
 // TMA, warp 1 TMEM allocation + tcgen05.mma, warps 2-9 element-wise work):
 //
 //  dK/dV: one CTA per (128-key tile, KV head, batch). For every query head
-//         of the group and every 64-query sub-tile at or after the diagonal:
-//           S^T  = K Q^T,  dP^T = V dO^T                       (TMEM)
+//         of the group and every 128-query sub-tile at or after the diagonal:
+//           S^T  = K Q^T, then dP^T = V dO^T, in one TMEM buffer
 //           P^T  = exp(S^T * scale - lse[q]),  dS^T = P^T (dP^T - delta[q])
-//                                                              (bf16, TMEM)
+//                                                     (bf16, a second buffer)
 //           dV  += P^T dO,  dK += dS^T Q   with dO and Q read MN-major
-//         then dK *= scale. Two element-wise groups take alternate
-//         sub-tiles, each with its own TMEM and shared-memory buffers.
+//         then dK *= scale. Every product is 128 x 128 or 128 x hd; all
+//         eight element-wise warps work on one sub-tile, two threads per key.
 //  dQ:    one CTA per (128-query tile, head, batch), two threads per query
 //         row. For every 128-key tile up to the diagonal: S = Q K^T,
 //         dP = dO V^T (TMEM); dS (bf16, TMEM); dQ += dS K with K read
@@ -99,85 +99,97 @@ __device__ __forceinline__ void tmem_pair_rope_to_bf16(uint32_t ta, uint32_t tb,
   }
 }
 
-// ------------------------------------------- dK / dV, 64-query sub-tiles
+// ------------------------------------------ dK / dV, 128-query sub-tiles
 // One CTA per (128-key tile, KV head, batch); it walks the group's query
-// heads and, per head, the 64-query sub-tiles at or after the diagonal.
-// Sub-tile `it` belongs to element-wise group it % 2 (warps 2-5 or 6-9, one
-// thread per key row), whose S^T and dP^T live in that group's 64-column TMEM
-// buffers. The group writes P^T and dS^T back, packed bf16, into the first
-// 32 columns of those same buffers, where the dV and dK products read them
-// as their TMEM A operand. The MMA warp issues dV/dK of sub-tile `it` as soon
-// as its group has stored P^T and dS^T, then S^T/dP^T of sub-tile it + 2
-// into the same buffers (the products run in issue order, so dV/dK read
-// them first), so one group's exponentials overlap the other group's
-// products. With no P^T / dS^T tiles in shared memory, Q and dO sub-tiles
-// stream through a deep TMA ring (5 stages at hd 128, 8 at hd 64) whose
-// loads are issued several sub-tiles ahead of their products. Each group
-// stages its sub-tile's 64 (lse, delta) pairs in shared memory; threads read
-// two query columns per 16-byte broadcast load.
+// heads and, per head, the 128-query sub-tiles from the diagonal on. Per
+// sub-tile j the MMA thread issues, in this order,
+//   dP^T j   (into tA, once the element-wise warps have copied S^T j out),
+//   dV += P^T j dO   (once they have stored P^T j in tB),
+//   S^T j + 1   (into tA, once they have copied dP^T j out),
+//   dK += dS^T j Q   (once they have stored dS^T j in tB),
+// so the element-wise warps compute P^T j while dP^T j runs, and dS^T j
+// while dV j and S^T j + 1 run. Every product is M 128 x N 128 (or hd):
+// a product with N = 64 costs about 1.5 times its arithmetic in issue, and
+// the issue slots it needs are the ones the element-wise warps take. TMEM
+// holds tA (S^T then dP^T, fp32), tB (P^T | dS^T packed as bf16 pairs, the
+// A operands of the dV and dK products), dV and dK: 128 + 128 + 2 hd <= 512
+// columns. Q and dO tiles of 128 queries share four shared-memory slots
+// (see slot_q / slot_o). The element-wise warps stage the sub-tile's 128
+// (lse, delta) pairs in shared memory, double-buffered, one barrier per
+// sub-tile; each thread reads two query columns per 16-byte broadcast load.
 template <int HD>
 struct KvTc2 {
   static constexpr int kBoxes = HD / 64;
-  static constexpr uint32_t kBox64 = 64 * 128;           // 64 columns x 64 rows of bf16
-  static constexpr uint32_t kKV = kBoxes * kBox;         // K or V tile, 128 keys
-  static constexpr uint32_t kQ = kBoxes * kBox64;        // Q or dO sub-tile, 64 queries
-  static constexpr int kStages = HD == 64 ? 8 : 5;
+  static constexpr uint32_t kKV = kBoxes * kBox;         // K, V, Q or dO tile of 128 rows
+  static constexpr int kSlots = 4;                       // Q / dO slots, shared by both
   static constexpr uint32_t kKOff = 0;
   static constexpr uint32_t kVOff = kKV;
-  static constexpr uint32_t kStOff = 2 * kKV;            // [stage] Q then dO
-  static constexpr uint32_t kBarOff = kStOff + kStages * 2 * kQ;
-  static constexpr uint32_t kVecOff = kBarOff + 256;     // [group][64] (lse * log2e, delta)
-  static constexpr size_t kSmem = 1024 + kVecOff + 2 * 64 * 8;
+  static constexpr uint32_t kSlotOff = 2 * kKV;          // [slot]
+  static constexpr uint32_t kBarOff = kSlotOff + kSlots * kKV;
+  static constexpr uint32_t kVecOff = kBarOff + 256;     // [2][128] (lse * log2e, delta)
+  static constexpr size_t kSmem = 1024 + kVecOff + 2 * 128 * 8;
   static_assert(kSmem <= 232448, "shared memory per block");
-  static_assert(2 * kStages + 16 <= 256 / 8, "barrier area");
 };
+
+// Slots of Q(j) and dO(j), the operands of 128-query sub-tile j: a slot is
+// released by the product that last reads it (dO by dV, Q by dK, which runs
+// later), and sub-tile j + 2 takes the slots in that order, Q(j + 2) the one
+// dO(j) held and dO(j + 2) the one Q(j) held. Each slot is used once per two
+// sub-tiles, so both slots of sub-tile j are in their use j / 2.
+__device__ __forceinline__ int slot_q(int j) { return (0x3120 >> (4 * (j & 3))) & 15; }
+__device__ __forceinline__ int slot_o(int j) { return (0x2031 >> (4 * (j & 3))) & 15; }
 
 template <int HD>
 __global__ void __launch_bounds__(kThr, 1)
-    attn_bwd_dkdv_tc2_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_constant__ CUtensorMap tq64,
-                             const __grid_constant__ CUtensorMap tdo64, const float* __restrict__ lse,
-                             const float* __restrict__ delta, bf16* __restrict__ dqkv, long long lddq, int s, int H,
-                             int Hkv, int hc, const float* __restrict__ cos_t, const float* __restrict__ sin_t,
-                             int* err) {
+    attn_bwd_dkdv_tc2_kernel(const __grid_constant__ CUtensorMap tqkv, const __grid_constant__ CUtensorMap tdo,
+                             const float* __restrict__ lse, const float* __restrict__ delta,
+                             bf16* __restrict__ dqkv, long long lddq, int s, int H, int Hkv, int hc,
+                             const float* __restrict__ cos_t, const float* __restrict__ sin_t, int* err) {
   using C = KvTc2<HD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024b(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
-  uint64_t* kv_full = bars;                      // K and V tiles
-  uint64_t* ld_full = bars + 1;                  // [kStages] Q + dO stage
-  uint64_t* ld_empty = ld_full + C::kStages;     // [kStages]
-  uint64_t* s_full = ld_empty + C::kStages;      // [2] per group: S^T, dP^T in TMEM
-  uint64_t* s_empty = s_full + 2;                // [2] per group: copied out of TMEM
-  uint64_t* p_full = s_empty + 2;                // [2] per group: P^T, dS^T stored in TMEM
-  uint64_t* done = p_full + 2;                   // all dV, dK products done (completes once)
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* kv_full = bars;                       // K and V tiles
+  uint64_t* slot_full = bars + 1;                 // [kSlots]
+  uint64_t* slot_empty = slot_full + C::kSlots;   // [kSlots]
+  uint64_t* s_full = slot_empty + C::kSlots;      // S^T in tA
+  uint64_t* s_read = s_full + 1;                  // S^T copied out of tA (8 warps)
+  uint64_t* d_full = s_full + 2;                  // dP^T in tA
+  uint64_t* d_read = s_full + 3;                  // dP^T copied out of tA (8 warps)
+  uint64_t* pv_full = s_full + 4;                 // P^T stored in tB (8 warps)
+  uint64_t* gv_done = s_full + 5;                 // dV product of the sub-tile done
+  uint64_t* ds_full = s_full + 6;                 // dS^T stored in tB (8 warps)
+  uint64_t* gk_done = s_full + 7;                 // dK product of the sub-tile done
+  uint64_t* done = s_full + 8;                    // all products done (completes once)
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(s_full + 9);
 
-  const int n64 = (s + 63) / 64;
-  const int nkt = (s + kT - 1) / kT;
+  const int nqt = (s + kT - 1) / kT;
   int hb, kt;  // (batch, KV head) pair and key tile; kt = 0 is the longest
-  chunked_tile_order(blockIdx.x, (int)gridDim.x / nkt, nkt, hc, hb, kt);
+  chunked_tile_order(blockIdx.x, (int)gridDim.x / nqt, nqt, hc, hb, kt);
   const int g = hb % Hkv, b = hb / Hkv;
   const int grp = H / Hkv;
   const int k0 = kt * kT;
-  const int per_head = n64 - 2 * kt;  // 64-query sub-tiles from the diagonal on
+  const int per_head = nqt - kt;  // 128-query sub-tiles from the diagonal on
   const int total = grp * per_head;
   const int kcol = (H + g) * HD, vcol = (H + Hkv + g) * HD;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    tma_prefetch_desc(&tkv);
-    tma_prefetch_desc(&tq64);
-    tma_prefetch_desc(&tdo64);
+    tma_prefetch_desc(&tqkv);
+    tma_prefetch_desc(&tdo);
     mbar_init(kv_full, 1);
-    for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(&ld_full[i], 1);
-      mbar_init(&ld_empty[i], 1);
+    for (int i = 0; i < C::kSlots; ++i) {
+      mbar_init(&slot_full[i], 1);
+      mbar_init(&slot_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 4);  // one arrival per element-wise warp
-      mbar_init(&p_full[i], 4);
-    }
+    mbar_init(s_full, 1);
+    mbar_init(s_read, 8);  // one arrival per element-wise warp
+    mbar_init(d_full, 1);
+    mbar_init(d_read, 8);
+    mbar_init(pv_full, 8);
+    mbar_init(gv_done, 1);
+    mbar_init(ds_full, 8);
+    mbar_init(gk_done, 1);
     mbar_init(done, 1);
     fence_barrier_init();
   }
@@ -186,185 +198,218 @@ __global__ void __launch_bounds__(kThr, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  // per-group S^T and dP^T buffers, as arithmetic (an array indexed by the
-  // group would live in local memory)
-  auto tS = [&](int grp_) { return tmem + 64u * (uint32_t)grp_; };
-  auto tdP = [&](int grp_) { return tmem + 128u + 64u * (uint32_t)grp_; };
-  const uint32_t tdV = tmem + 256, tdK = tmem + 256 + HD;
+  // TMEM columns: tA holds S^T, then dP^T, of the sub-tile (fp32, 128
+  // queries); tB holds P^T (columns 0-63) and dS^T (64-127) packed as bf16
+  // pairs, the A operands of the dV and dK products; then dV and dK.
+  const uint32_t tA = tmem, tB = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + HD;
 
   if (warp == 0) {
     if (lane == 0) {
-      int nld = 0;
+      int nld = 0;  // Q / dO loads issued
       bool ok = true;
       mbar_arrive_expect_tx(kv_full, 2 * C::kKV);
       for (int bx = 0; bx < C::kBoxes; ++bx) {
-        tma_load_3d(sm + C::kKOff + bx * kBox, &tkv, kcol + bx * 64, k0, b, kv_full);
-        tma_load_3d(sm + C::kVOff + bx * kBox, &tkv, vcol + bx * 64, k0, b, kv_full);
+        tma_load_3d(sm + C::kKOff + bx * kBox, &tqkv, kcol + bx * 64, k0, b, kv_full);
+        tma_load_3d(sm + C::kVOff + bx * kBox, &tqkv, vcol + bx * 64, k0, b, kv_full);
       }
-      for (int it = 0; it < total; ++it) {
-        const int st = it % C::kStages, use = it / C::kStages;
-        if (!mbar_wait(&ld_empty[st], (use & 1) ^ 1, err)) { ok = false; break; }
-        const int h = g * grp + it / per_head;
-        const int q0 = (2 * kt + it % per_head) * 64;
-        uint8_t* qs = sm + C::kStOff + st * 2 * C::kQ;
-        mbar_arrive_expect_tx(&ld_full[st], 2 * C::kQ);
-        for (int bx = 0; bx < C::kBoxes; ++bx) {
-          tma_load_3d(qs + bx * C::kBox64, &tq64, h * HD + bx * 64, q0, b, &ld_full[st]);
-          tma_load_3d(qs + C::kQ + bx * C::kBox64, &tdo64, h * HD + bx * 64, q0, b, &ld_full[st]);
+      for (int j = 0; j < total && ok; ++j) {
+        const int h = g * grp + j / per_head;
+        const int q0 = k0 + (j % per_head) * kT;
+        const int u = j >> 1;
+        for (int w = 0; w < 2; ++w) {  // Q, then dO
+          const int sl = w == 0 ? slot_q(j) : slot_o(j);
+          if (u > 0 && !mbar_wait(&slot_empty[sl], (u - 1) & 1, err)) { ok = false; break; }
+          uint8_t* dst = sm + C::kSlotOff + sl * C::kKV;
+          mbar_arrive_expect_tx(&slot_full[sl], C::kKV);
+          for (int bx = 0; bx < C::kBoxes; ++bx) {
+            if (w == 0)
+              tma_load_3d(dst + bx * kBox, &tqkv, h * HD + bx * 64, q0, b, &slot_full[sl]);
+            else
+              tma_load_3d(dst + bx * kBox, &tdo, h * HD + bx * 64, q0, b, &slot_full[sl]);
+          }
+          ++nld;
         }
-        ++nld;
       }
       if (!ok) {
         // wait (bounded) for this CTA's copies still in flight before it exits
         mbar_wait(kv_full, 0, err);
-        for (int i = 0; i < C::kStages && i < nld; ++i) {
-          const int last = nld - 1 - i;
-          mbar_wait(&ld_full[last % C::kStages], (last / C::kStages) & 1, err);
+        for (int i = nld - 1; i >= 0 && i >= nld - C::kSlots; --i) {
+          const int j = i >> 1;
+          const int sl = (i & 1) ? slot_o(j) : slot_q(j);
+          mbar_wait(&slot_full[sl], (j >> 1) & 1, err);
         }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16_f32(kT, 64, false, false);  // S^T, dP^T: M 128 keys, N 64 queries
+      constexpr uint32_t id_s = idesc_bf16_f32(kT, kT, false, false);  // S^T, dP^T: 128 keys x 128 queries
       constexpr uint32_t id_g = idesc_bf16_f32(kT, HD, false, true);   // dV, dK: B (dO, Q) MN-major
       const uint64_t dK = smem_desc_kmajor_sw128(smem_u32(sm + C::kKOff));
       const uint64_t dV = smem_desc_kmajor_sw128(smem_u32(sm + C::kVOff));
-      bool ok = mbar_wait(kv_full, 0, err);
-      auto issue_s = [&](int i) -> bool {
-        const int G = i & 1, li = i >> 1, st = i % C::kStages;
-        if (!mbar_wait(&ld_full[st], (i / C::kStages) & 1, err)) return false;
-        if (li > 0 && !mbar_wait(&s_empty[G], (li - 1) & 1, err)) return false;
-        tc_fence_after();
-        const uint64_t dQ = smem_desc_kmajor_sw128(smem_u32(sm + C::kStOff + st * 2 * C::kQ));
-        const uint64_t dO = desc_advance(dQ, C::kQ);
+      auto slot_addr = [&](int sl) { return smem_u32(sm + C::kSlotOff + sl * C::kKV); };
+      // A (K or V rows) and B (Q or dO rows) both K-major over hd
+      auto scores = [&](uint64_t da, int sl) {
+        const uint64_t db = smem_desc_kmajor_sw128(slot_addr(sl));
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t ka = (kk >> 2) * kBox + (kk & 3) * 32, kb = (kk >> 2) * C::kBox64 + (kk & 3) * 32;
-          tc_mma_bf16(tS(G), desc_advance(dK, ka), desc_advance(dQ, kb), id_s, kk > 0);
-          tc_mma_bf16(tdP(G), desc_advance(dV, ka), desc_advance(dO, kb), id_s, kk > 0);
+          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+          tc_mma_bf16(tA, desc_advance(da, off), desc_advance(db, off), id_s, kk > 0);
         }
-        tc_commit(&s_full[G]);
-        return true;
       };
-      if (ok && total > 0) ok = issue_s(0);
-      if (ok && total > 1) ok = issue_s(1);
-      for (int it = 0; ok && it < total; ++it) {
-        const int G = it & 1, li = it >> 1, st = it % C::kStages;
-        if (!(ok = mbar_wait(&p_full[G], li & 1, err))) break;
-        tc_fence_after();
-        const uint32_t sQ = smem_u32(sm + C::kStOff + st * 2 * C::kQ);
-        const uint64_t mQ = smem_desc_mnmajor_sw128(sQ, C::kBox64), mO = desc_advance(mQ, C::kQ);
-        // A operands from TMEM: 16 queries of P^T (dS^T) are 8 packed columns
+      // dX += (P^T or dS^T, from tB at column ta) x (dO or Q, MN-major), over the 128 queries
+      auto grads = [&](uint32_t dacc, uint32_t ta, int sl, bool first) {
+        const uint64_t mb = smem_desc_mnmajor_sw128(slot_addr(sl), kBox);
 #pragma unroll
-        for (int kk = 0; kk < 64 / 16; ++kk) {
-          const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-          tc_mma_bf16_ta(tdV, tS(G) + kk * 8, desc_advance(mO, kk * 2048), id_g, acc);
-          tc_mma_bf16_ta(tdK, tdP(G) + kk * 8, desc_advance(mQ, kk * 2048), id_g, acc);
-        }
-        tc_commit(&ld_empty[st]);
-        if (it + 2 < total) ok = issue_s(it + 2);
+        for (int kk = 0; kk < kT / 16; ++kk)
+          tc_mma_bf16_ta(dacc, ta + kk * 8, desc_advance(mb, kk * 2048), id_g, (first && kk == 0) ? 0u : 1u);
+      };
+      bool ok = mbar_wait(kv_full, 0, err) && mbar_wait(&slot_full[slot_q(0)], 0, err);
+      if (ok) {
+        tc_fence_after();
+        scores(dK, slot_q(0));
+        tc_commit(s_full);
       }
-      // The accumulators are final once every product above has completed.
-      // The readers wait on this single-use barrier: waiting on a per-group
-      // barrier for its last completion could match an earlier phase of the
-      // same parity that the other group never observed.
+      // per sub-tile j: dP^T j, dV j, S^T j + 1, dK j, so the element-wise
+      // warps' work on one product's result overlaps the next product
+      for (int j = 0; ok && j < total; ++j) {
+        const uint32_t ph = j & 1, u = (j >> 1) & 1;
+        if (!(ok = mbar_wait(s_read, ph, err) && mbar_wait(&slot_full[slot_o(j)], u, err))) break;
+        tc_fence_after();
+        scores(dV, slot_o(j));
+        tc_commit(d_full);
+        if (!(ok = mbar_wait(pv_full, ph, err))) break;
+        tc_fence_after();
+        grads(tdV, tB, slot_o(j), j == 0);
+        tc_commit(gv_done);
+        tc_commit(&slot_empty[slot_o(j)]);
+        if (j + 1 < total) {
+          const uint32_t u1 = ((j + 1) >> 1) & 1;
+          if (!(ok = mbar_wait(d_read, ph, err) && mbar_wait(&slot_full[slot_q(j + 1)], u1, err))) break;
+          tc_fence_after();
+          scores(dK, slot_q(j + 1));
+          tc_commit(s_full);
+        }
+        if (!(ok = mbar_wait(ds_full, ph, err))) break;
+        tc_fence_after();
+        grads(tdK, tB + 64, slot_q(j), j == 0);
+        tc_commit(gk_done);
+        tc_commit(&slot_empty[slot_q(j)]);
+      }
       if (ok) tc_commit(done);
     }
   } else {
-    const int G = (warp - 2) >> 2, q = warp & 3;
-    const int row = q * 32 + lane;  // key row within the tile
+    // two threads per key row: quarter q of the rows, half hf of the queries
+    const int q = warp & 3, hf = (warp - 2) >> 2;
+    const int row = q * 32 + lane;
     const int key = k0 + row;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const float sc = rsqrtf((float)HD) * kLog2e;
-    float2* vec = reinterpret_cast<float2*>(sm + C::kVecOff) + G * 64;
-    const int tg = threadIdx.x - 64 - 128 * G;  // 0..127 within the group
-    auto group_sync = [&]() { asm volatile("bar.sync %0, 128;" ::"r"(1 + G) : "memory"); };
-    // a wait's outcome, the same for the whole warp (tcgen05.ld is warp-wide)
+    float2* vecs = reinterpret_cast<float2*>(sm + C::kVecOff);  // [2][128]
+    const int te = threadIdx.x - 64;  // 0..255
+    auto all_sync = [&]() { asm volatile("bar.sync 1, 256;" ::: "memory"); };
     auto wait_all = [&](uint64_t* bar, uint32_t parity) { return mbar_wait_warp(bar, parity, err); };
     bool ok = true;
-    // (lse * log2e, delta) of query tg of sub-tile `i`; read one group
-    // iteration ahead so the loads' latency overlaps a sub-tile's work
-    auto load_vec = [&](int i) -> float2 {
-      const int hh = g * grp + i / per_head;
-      const int qq = (2 * kt + i % per_head) * 64 + tg;
+    // (lse * log2e, delta) of query te of sub-tile j, read one sub-tile ahead
+    auto load_vec = [&](int j) -> float2 {
+      const int hh = g * grp + j / per_head;
+      const int qq = k0 + (j % per_head) * kT + te;
       const long long vi = ((long long)b * H + hh) * s + qq;
       return qq < s ? make_float2(lse[vi] * kLog2e, delta[vi]) : make_float2(INFINITY, 0.f);
     };
     float2 vnext = make_float2(0.f, 0.f);
-    if (tg < 64 && G < total) vnext = load_vec(G);
-    // every thread of the group runs every iteration's two group barriers,
-    // also after a failed wait (it then skips the work), so none is left
-    // waiting at a barrier
-    for (int it = G; it < total; it += 2) {
-      const int li = it >> 1;
-      const int jj = it % per_head;
-      const int q0 = (2 * kt + jj) * 64;
-      // the sub-tile's 64 pairs into shared memory; the group's reads of the
-      // previous sub-tile's pairs end before they are overwritten
-      group_sync();
-      if (tg < 64) vec[tg] = vnext;
-      group_sync();
-      if (tg < 64 && it + 2 < total) vnext = load_vec(it + 2);
+    if (te < kT && total > 0) vnext = load_vec(0);
+    // every thread runs every sub-tile's barrier, also after a failed wait
+    for (int j = 0; j < total; ++j) {
+      const uint32_t ph = j & 1;
+      const bool diag = (j % per_head) == 0;
+      const int q0 = k0 + (j % per_head) * kT;
+      float2* vec = vecs + (j & 1) * kT;
+      // the buffer written here was last read in sub-tile j - 2, which every
+      // thread finished before the barrier of sub-tile j - 1
+      if (te < kT) vec[te] = vnext;
+      all_sync();
+      if (te < kT && j + 1 < total) vnext = load_vec(j + 1);
       if (!ok) continue;
-      if (!wait_all(&s_full[G], li & 1)) { ok = false; continue; }
+      if (!wait_all(s_full, ph)) { ok = false; continue; }
       tc_fence_after();
       uint32_t rs[2][32], rp[2][32];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        tmem_ld_32x32b_x32(tS(G) + lane_off + c * 32, rs[c]);
-        tmem_ld_32x32b_x32(tdP(G) + lane_off + c * 32, rp[c]);
-      }
+      tmem_ld_32x32b_x32(tA + lane_off + hf * 64, rs[0]);
+      tmem_ld_32x32b_x32(tA + lane_off + hf * 64 + 32, rs[1]);
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive_warp(&s_empty[G]);
-      // P^T = exp2(S^T * scale - lse), dS^T = P^T (dP^T - delta), packed in
-      // place; only a sub-tile that reaches the diagonal masks key > query
-      // (two copies of the loop, so the others carry no compare and select)
-      auto elementwise = [&](auto masked_tag) {
+      mbar_arrive_warp(s_read);
+      // P^T = exp2(S^T * scale - lse); the diagonal sub-tile masks key > query
+      const float4* v4 = reinterpret_cast<const float4*>(vec + hf * 64);
+      auto probs = [&](auto masked_tag) {
         constexpr bool kMasked = decltype(masked_tag)::value;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float4 ld = reinterpret_cast<const float4*>(vec)[i];  // columns 2i, 2i+1
-          const float l2s[2] = {ld.x, ld.z}, dls[2] = {ld.y, ld.w};
-          float pv[2], dv[2];
+          const float4 ld = v4[i];  // columns 2i, 2i+1 of this half
+          const float l2s[2] = {ld.x, ld.z};
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int c = 2 * i + e;  // query column within the sub-tile
+            const int c = 2 * i + e;
             float p = ex2_approx(fmaf(__uint_as_float(rs[c >> 5][c & 31]), sc, -l2s[e]));
-            if (kMasked && q0 + c < key) p = 0.f;
-            pv[e] = p;
-            dv[e] = p * (__uint_as_float(rp[c >> 5][c & 31]) - dls[e]);
+            if (kMasked && q0 + hf * 64 + c < key) p = 0.f;
+            rs[c >> 5][c & 31] = __float_as_uint(p);
           }
-          rs[i >> 4][i & 15] = pack_bf16x2(pv[0], pv[1]);
-          rp[i >> 4][i & 15] = pack_bf16x2(dv[0], dv[1]);
         }
       };
-      if (q0 < k0 + kT)
-        elementwise(std::true_type{});
+      if (diag)
+        probs(std::true_type{});
       else
-        elementwise(std::false_type{});
-      // P^T and dS^T into the first 32 columns of the row's S^T and dP^T
-      // lanes. The products that last read them (dV/dK of sub-tile it - 2)
-      // completed before S^T of this sub-tile did, which s_full reported.
+        probs(std::false_type{});
       {
         uint32_t pw[32];
 #pragma unroll
-        for (int w = 0; w < 32; ++w) pw[w] = rs[w >> 4][w & 15];
-        tmem_st_32x32b_x32(tS(G) + lane_off, pw);
+        for (int i = 0; i < 32; ++i)
+          pw[i] = pack_bf16x2(__uint_as_float(rs[(2 * i) >> 5][(2 * i) & 31]),
+                              __uint_as_float(rs[(2 * i + 1) >> 5][(2 * i + 1) & 31]));
+        // P^T of sub-tile j - 1 has been read by its dV product
+        if (j > 0 && !wait_all(gv_done, ph ^ 1)) { ok = false; continue; }
+        tmem_st_32x32b_x32(tB + lane_off + hf * 32, pw);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive_warp(pv_full);
+      }
+      if (!wait_all(d_full, ph)) { ok = false; continue; }
+      tc_fence_after();
+      tmem_ld_32x32b_x32(tA + lane_off + hf * 64, rp[0]);
+      tmem_ld_32x32b_x32(tA + lane_off + hf * 64 + 32, rp[1]);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive_warp(d_read);
+      // dS^T = P^T (dP^T - delta), packed in place
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float4 ld = v4[i];
+        const float dls[2] = {ld.y, ld.w};
+        float dv[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int c = 2 * i + e;
+          dv[e] = __uint_as_float(rs[c >> 5][c & 31]) * (__uint_as_float(rp[c >> 5][c & 31]) - dls[e]);
+        }
+        rp[i >> 4][i & 15] = pack_bf16x2(dv[0], dv[1]);
+      }
+      {
+        uint32_t pw[32];
 #pragma unroll
         for (int w = 0; w < 32; ++w) pw[w] = rp[w >> 4][w & 15];
-        tmem_st_32x32b_x32(tdP(G) + lane_off, pw);
+        // dS^T of sub-tile j - 1 has been read by its dK product
+        if (j > 0 && !wait_all(gk_done, ph ^ 1)) { ok = false; continue; }
+        tmem_st_32x32b_x32(tB + 64 + lane_off + hf * 32, pw);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive_warp(ds_full);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive_warp(&p_full[G]);
     }
     if (ok && total > 0 && wait_all(done, 0)) {
       tc_fence_after();
       const bool store = key < s;
       const long long r0 = (long long)b * s + key;
       bf16* dkrow = dqkv + r0 * lddq + (long long)kcol;
-      if (G == 0) {
+      if (hf == 0) {
         tmem_row_to_bf16(tdV + lane_off, HD, 1.f, dqkv + r0 * lddq + (long long)vcol, store);
       } else if (cos_t == nullptr) {
         tmem_row_to_bf16(tdK + lane_off, HD, rsqrtf((float)HD), dkrow, store);
@@ -372,10 +417,10 @@ __global__ void __launch_bounds__(kThr, 1)
         // dk rotated back at the key's position (one 32-pair chunk per step)
         const long long tb = (long long)(store ? key : 0) * (HD / 2);
 #pragma unroll 1
-        for (int j = 0; j < HD / 64; ++j)
-          tmem_pair_rope_to_bf16<32>(tdK + lane_off + j * 32, tdK + lane_off + HD / 2 + j * 32, rsqrtf((float)HD),
-                                     cos_t + tb + j * 32, sin_t + tb + j * 32, dkrow + j * 32,
-                                     dkrow + HD / 2 + j * 32, store);
+        for (int jj = 0; jj < HD / 64; ++jj)
+          tmem_pair_rope_to_bf16<32>(tdK + lane_off + jj * 32, tdK + lane_off + HD / 2 + jj * 32, rsqrtf((float)HD),
+                                     cos_t + tb + jj * 32, sin_t + tb + jj * 32, dkrow + jj * 32,
+                                     dkrow + HD / 2 + jj * 32, store);
       }
     }
   }
@@ -646,10 +691,10 @@ void init_once() {
   cudaFuncSetAttribute(attn_bwd_dq_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)QTc<128>::kSmem);
 }
 
-bool make_map3(CUtensorMap* m, const void* p, long long ld, int s, int B, int rows = kT) {
+bool make_map3(CUtensorMap* m, const void* p, long long ld, int s, int B) {
   cuuint64_t dims[3] = {(cuuint64_t)ld, (cuuint64_t)s, (cuuint64_t)B};
   cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)s * ld * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)kT, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return g_enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -670,10 +715,8 @@ int attn_bwd_tc(const void* qkv, long long ld, const void* dout, long long lddo,
   if ((reinterpret_cast<uintptr_t>(qkv) & 15) || (reinterpret_cast<uintptr_t>(dout) & 15) ||
       (reinterpret_cast<uintptr_t>(dqkv) & 15) || ld % 8 || lddo % 8 || lddq % 8)
     return MT_EINVAL;
-  CUtensorMap tq, td, tq64, td64;
-  if (!make_map3(&tq, qkv, ld, s, B) || !make_map3(&td, dout, lddo, s, B) || !make_map3(&tq64, qkv, ld, s, B, 64) ||
-      !make_map3(&td64, dout, lddo, s, B, 64))
-    return MT_EINVAL;
+  CUtensorMap tq, td;
+  if (!make_map3(&tq, qkv, ld, s, B) || !make_map3(&td, dout, lddo, s, B)) return MT_EINVAL;
   const int nt = (s + kT - 1) / kT;
   // one CTA per (tile, head, batch) on a 1-D grid, in the chunked order
   if ((long long)nt * H * B > 0x7fffffffLL) return MT_EINVAL;
@@ -685,12 +728,12 @@ int attn_bwd_tc(const void* qkv, long long ld, const void* dout, long long lddo,
   int* err = device_error_word();
   const unsigned g1 = (unsigned)(nt * Hkv * B), g2 = (unsigned)(nt * H * B);
   if (hd == 64) {
-    attn_bwd_dkdv_tc2_kernel<64><<<g1, kThr, KvTc2<64>::kSmem, stream>>>(tq, tq64, td64, lse, delta, (bf16*)dqkv,
+    attn_bwd_dkdv_tc2_kernel<64><<<g1, kThr, KvTc2<64>::kSmem, stream>>>(tq, td, lse, delta, (bf16*)dqkv,
                                                                          lddq, s, H, Hkv, hc1, cos_t, sin_t, err);
     attn_bwd_dq_tc_kernel<64><<<g2, kThr, QTc<64>::kSmem, stream>>>(tq, td, lse, delta, (bf16*)dqkv, lddq, s, H, Hkv,
                                                                    hc2, cos_t, sin_t, err);
   } else {
-    attn_bwd_dkdv_tc2_kernel<128><<<g1, kThr, KvTc2<128>::kSmem, stream>>>(tq, tq64, td64, lse, delta, (bf16*)dqkv,
+    attn_bwd_dkdv_tc2_kernel<128><<<g1, kThr, KvTc2<128>::kSmem, stream>>>(tq, td, lse, delta, (bf16*)dqkv,
                                                                            lddq, s, H, Hkv, hc1, cos_t, sin_t, err);
     attn_bwd_dq_tc_kernel<128><<<g2, kThr, QTc<128>::kSmem, stream>>>(tq, td, lse, delta, (bf16*)dqkv, lddq, s, H,
                                                                      Hkv, hc2, cos_t, sin_t, err);
