@@ -340,19 +340,22 @@ __global__ void __launch_bounds__(kThr, 1)
       mbar_arrive_warp(s_read);
       // P^T = exp2(S^T * scale - lse); the diagonal sub-tile masks key > query
       const float4* v4 = reinterpret_cast<const float4*>(vec + hf * 64);
+      const float2 sc2 = make_float2(sc, sc);
       auto probs = [&](auto masked_tag) {
         constexpr bool kMasked = decltype(masked_tag)::value;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const float4 ld = v4[i];  // columns 2i, 2i+1 of this half
-          const float l2s[2] = {ld.x, ld.z};
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int c = 2 * i + e;
-            float p = ex2_approx(fmaf(__uint_as_float(rs[c >> 5][c & 31]), sc, -l2s[e]));
-            if (kMasked && q0 + hf * 64 + c < key) p = 0.f;
-            rs[c >> 5][c & 31] = __float_as_uint(p);
+          const int c = 2 * i;
+          const float2 x = ffma2(make_float2(__uint_as_float(rs[c >> 5][c & 31]), __uint_as_float(rs[c >> 5][(c + 1) & 31])),
+                                 sc2, make_float2(-ld.x, -ld.z));
+          float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+          if (kMasked) {
+            if (q0 + hf * 64 + c < key) p0 = 0.f;
+            if (q0 + hf * 64 + c + 1 < key) p1 = 0.f;
           }
+          rs[c >> 5][c & 31] = __float_as_uint(p0);
+          rs[c >> 5][(c + 1) & 31] = __float_as_uint(p1);
         }
       };
       if (diag)
@@ -383,14 +386,11 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const float4 ld = v4[i];
-        const float dls[2] = {ld.y, ld.w};
-        float dv[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int c = 2 * i + e;
-          dv[e] = __uint_as_float(rs[c >> 5][c & 31]) * (__uint_as_float(rp[c >> 5][c & 31]) - dls[e]);
-        }
-        rp[i >> 4][i & 15] = pack_bf16x2(dv[0], dv[1]);
+        const int c = 2 * i;
+        const float2 pp = make_float2(__uint_as_float(rs[c >> 5][c & 31]), __uint_as_float(rs[c >> 5][(c + 1) & 31]));
+        const float2 dp = make_float2(__uint_as_float(rp[c >> 5][c & 31]), __uint_as_float(rp[c >> 5][(c + 1) & 31]));
+        const float2 dv = fmul2(pp, fadd2(dp, make_float2(-ld.y, -ld.w)));
+        rp[i >> 4][i & 15] = pack_bf16x2(dv.x, dv.y);
       }
       {
         uint32_t pw[32];
