@@ -115,8 +115,9 @@ __device__ __forceinline__ void tmem_pair_rope_to_bf16(uint32_t ta, uint32_t tb,
 // A operands of the dV and dK products), dV and dK: 128 + 128 + 2 hd <= 512
 // columns. Q and dO tiles of 128 queries share four shared-memory slots
 // (see slot_q / slot_o). The element-wise warps stage the sub-tile's 128
-// (lse, delta) pairs in shared memory, double-buffered, one barrier per
-// sub-tile; each thread reads two query columns per 16-byte broadcast load.
+// lse and 128 delta values in shared memory, double-buffered, one barrier
+// per sub-tile; each thread reads four query columns per 16-byte broadcast
+// load, in two-wide fp32 instructions.
 template <int HD>
 struct KvTc2 {
   static constexpr int kBoxes = HD / 64;
@@ -126,7 +127,7 @@ struct KvTc2 {
   static constexpr uint32_t kVOff = kKV;
   static constexpr uint32_t kSlotOff = 2 * kKV;          // [slot]
   static constexpr uint32_t kBarOff = kSlotOff + kSlots * kKV;
-  static constexpr uint32_t kVecOff = kBarOff + 256;     // [2][128] (lse * log2e, delta)
+  static constexpr uint32_t kVecOff = kBarOff + 256;     // [2][lse * log2e x 128 | delta x 128]
   static constexpr size_t kSmem = 1024 + kVecOff + 2 * 128 * 8;
   static_assert(kSmem <= 232448, "shared memory per block");
 };
@@ -304,7 +305,7 @@ __global__ void __launch_bounds__(kThr, 1)
     const int key = k0 + row;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const float sc = rsqrtf((float)HD) * kLog2e;
-    float2* vecs = reinterpret_cast<float2*>(sm + C::kVecOff);  // [2][128]
+    float* vecs = reinterpret_cast<float*>(sm + C::kVecOff);  // [2][256]
     const int te = threadIdx.x - 64;  // 0..255
     auto all_sync = [&]() { asm volatile("bar.sync 1, 256;" ::: "memory"); };
     auto wait_all = [&](uint64_t* bar, uint32_t parity) { return mbar_wait_warp(bar, parity, err); };
@@ -323,10 +324,13 @@ __global__ void __launch_bounds__(kThr, 1)
       const uint32_t ph = j & 1;
       const bool diag = (j % per_head) == 0;
       const int q0 = k0 + (j % per_head) * kT;
-      float2* vec = vecs + (j & 1) * kT;
+      float* vec = vecs + (j & 1) * 2 * kT;
       // the buffer written here was last read in sub-tile j - 2, which every
       // thread finished before the barrier of sub-tile j - 1
-      if (te < kT) vec[te] = vnext;
+      if (te < kT) {
+        vec[te] = vnext.x;
+        vec[kT + te] = vnext.y;
+      }
       all_sync();
       if (te < kT && j + 1 < total) vnext = load_vec(j + 1);
       if (!ok) continue;
@@ -338,24 +342,31 @@ __global__ void __launch_bounds__(kThr, 1)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive_warp(s_read);
-      // P^T = exp2(S^T * scale - lse); the diagonal sub-tile masks key > query
-      const float4* v4 = reinterpret_cast<const float4*>(vec + hf * 64);
+      // P^T = exp2(S^T * scale - lse); the diagonal sub-tile masks key > query.
+      // P stays in rs (fp32, for dS^T); pw gets it packed as bf16 pairs.
+      const float4* l4 = reinterpret_cast<const float4*>(vec + hf * 64);
+      const float4* d4 = reinterpret_cast<const float4*>(vec + kT + hf * 64);
       const float2 sc2 = make_float2(sc, sc);
+      uint32_t pw[32];
       auto probs = [&](auto masked_tag) {
         constexpr bool kMasked = decltype(masked_tag)::value;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float4 ld = v4[i];  // columns 2i, 2i+1 of this half
-          const int c = 2 * i;
-          const float2 x = ffma2(make_float2(__uint_as_float(rs[c >> 5][c & 31]), __uint_as_float(rs[c >> 5][(c + 1) & 31])),
-                                 sc2, make_float2(-ld.x, -ld.z));
-          float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
-          if (kMasked) {
-            if (q0 + hf * 64 + c < key) p0 = 0.f;
-            if (q0 + hf * 64 + c + 1 < key) p1 = 0.f;
+        for (int i = 0; i < 16; ++i) {
+          const float4 l = l4[i];  // columns 4i .. 4i + 3 of this half
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int c = 4 * i + 2 * h2;
+            const float2 x = ffma2(make_float2(__uint_as_float(rs[c >> 5][c & 31]), __uint_as_float(rs[c >> 5][(c + 1) & 31])),
+                                   sc2, h2 == 0 ? make_float2(-l.x, -l.y) : make_float2(-l.z, -l.w));
+            float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+            if (kMasked) {
+              if (q0 + hf * 64 + c < key) p0 = 0.f;
+              if (q0 + hf * 64 + c + 1 < key) p1 = 0.f;
+            }
+            rs[c >> 5][c & 31] = __float_as_uint(p0);
+            rs[c >> 5][(c + 1) & 31] = __float_as_uint(p1);
+            pw[c >> 1] = pack_bf16x2(p0, p1);
           }
-          rs[c >> 5][c & 31] = __float_as_uint(p0);
-          rs[c >> 5][(c + 1) & 31] = __float_as_uint(p1);
         }
       };
       if (diag)
@@ -363,11 +374,6 @@ __global__ void __launch_bounds__(kThr, 1)
       else
         probs(std::false_type{});
       {
-        uint32_t pw[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          pw[i] = pack_bf16x2(__uint_as_float(rs[(2 * i) >> 5][(2 * i) & 31]),
-                              __uint_as_float(rs[(2 * i + 1) >> 5][(2 * i + 1) & 31]));
         // P^T of sub-tile j - 1 has been read by its dV product
         if (j > 0 && !wait_all(gv_done, ph ^ 1)) { ok = false; continue; }
         tmem_st_32x32b_x32(tB + lane_off + hf * 32, pw);
@@ -384,16 +390,18 @@ __global__ void __launch_bounds__(kThr, 1)
       mbar_arrive_warp(d_read);
       // dS^T = P^T (dP^T - delta), packed in place
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float4 ld = v4[i];
-        const int c = 2 * i;
-        const float2 pp = make_float2(__uint_as_float(rs[c >> 5][c & 31]), __uint_as_float(rs[c >> 5][(c + 1) & 31]));
-        const float2 dp = make_float2(__uint_as_float(rp[c >> 5][c & 31]), __uint_as_float(rp[c >> 5][(c + 1) & 31]));
-        const float2 dv = fmul2(pp, fadd2(dp, make_float2(-ld.y, -ld.w)));
-        rp[i >> 4][i & 15] = pack_bf16x2(dv.x, dv.y);
+      for (int i = 0; i < 16; ++i) {
+        const float4 d = d4[i];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int c = 4 * i + 2 * h2;
+          const float2 pp = make_float2(__uint_as_float(rs[c >> 5][c & 31]), __uint_as_float(rs[c >> 5][(c + 1) & 31]));
+          const float2 dp = make_float2(__uint_as_float(rp[c >> 5][c & 31]), __uint_as_float(rp[c >> 5][(c + 1) & 31]));
+          const float2 dv = fmul2(pp, fadd2(dp, h2 == 0 ? make_float2(-d.x, -d.y) : make_float2(-d.z, -d.w)));
+          rp[(c >> 1) >> 4][(c >> 1) & 15] = pack_bf16x2(dv.x, dv.y);
+        }
       }
       {
-        uint32_t pw[32];
 #pragma unroll
         for (int w = 0; w < 32; ++w) pw[w] = rp[w >> 4][w & 15];
         // dS^T of sub-tile j - 1 has been read by its dK product
