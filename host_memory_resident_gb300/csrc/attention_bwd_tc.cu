@@ -336,10 +336,8 @@ __global__ void __launch_bounds__(kThr, 1)
       if (!ok) continue;
       if (!wait_all(s_full, ph)) { ok = false; continue; }
       tc_fence_after();
-      uint32_t rs[2][32], rp[2][32];
-      tmem_ld_32x32b_x32(tA + lane_off + hf * 64, rs[0]);
-      tmem_ld_32x32b_x32(tA + lane_off + hf * 64 + 32, rs[1]);
-      tmem_ld_wait();
+      uint32_t rs[64], rp[64];
+      tmem_ld_32x32b_x64_sync(tA + lane_off + hf * 64, rs);
       tc_fence_before();
       mbar_arrive_warp(s_read);
       // P^T = exp2(S^T * scale - lse); the diagonal sub-tile masks key > query.
@@ -356,15 +354,15 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
             const int c = 4 * i + 2 * h2;
-            const float2 x = ffma2(make_float2(__uint_as_float(rs[c >> 5][c & 31]), __uint_as_float(rs[c >> 5][(c + 1) & 31])),
-                                   sc2, h2 == 0 ? make_float2(-l.x, -l.y) : make_float2(-l.z, -l.w));
+            const float2 x = ffma2(make_float2(__uint_as_float(rs[c]), __uint_as_float(rs[c + 1])), sc2,
+                                   h2 == 0 ? make_float2(-l.x, -l.y) : make_float2(-l.z, -l.w));
             float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
             if (kMasked) {
               if (q0 + hf * 64 + c < key) p0 = 0.f;
               if (q0 + hf * 64 + c + 1 < key) p1 = 0.f;
             }
-            rs[c >> 5][c & 31] = __float_as_uint(p0);
-            rs[c >> 5][(c + 1) & 31] = __float_as_uint(p1);
+            rs[c] = __float_as_uint(p0);
+            rs[c + 1] = __float_as_uint(p1);
             pw[c >> 1] = pack_bf16x2(p0, p1);
           }
         }
@@ -376,16 +374,13 @@ __global__ void __launch_bounds__(kThr, 1)
       {
         // P^T of sub-tile j - 1 has been read by its dV product
         if (j > 0 && !wait_all(gv_done, ph ^ 1)) { ok = false; continue; }
-        tmem_st_32x32b_x32(tB + lane_off + hf * 32, pw);
-        tmem_st_wait();
+        tmem_st_32x32b_x32_sync(tB + lane_off + hf * 32, pw);
         tc_fence_before();
         mbar_arrive_warp(pv_full);
       }
       if (!wait_all(d_full, ph)) { ok = false; continue; }
       tc_fence_after();
-      tmem_ld_32x32b_x32(tA + lane_off + hf * 64, rp[0]);
-      tmem_ld_32x32b_x32(tA + lane_off + hf * 64 + 32, rp[1]);
-      tmem_ld_wait();
+      tmem_ld_32x32b_x64_sync(tA + lane_off + hf * 64, rp);
       tc_fence_before();
       mbar_arrive_warp(d_read);
       // dS^T = P^T (dP^T - delta), packed in place
@@ -395,19 +390,16 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
           const int c = 4 * i + 2 * h2;
-          const float2 pp = make_float2(__uint_as_float(rs[c >> 5][c & 31]), __uint_as_float(rs[c >> 5][(c + 1) & 31]));
-          const float2 dp = make_float2(__uint_as_float(rp[c >> 5][c & 31]), __uint_as_float(rp[c >> 5][(c + 1) & 31]));
+          const float2 pp = make_float2(__uint_as_float(rs[c]), __uint_as_float(rs[c + 1]));
+          const float2 dp = make_float2(__uint_as_float(rp[c]), __uint_as_float(rp[c + 1]));
           const float2 dv = fmul2(pp, fadd2(dp, h2 == 0 ? make_float2(-d.x, -d.y) : make_float2(-d.z, -d.w)));
-          rp[(c >> 1) >> 4][(c >> 1) & 15] = pack_bf16x2(dv.x, dv.y);
+          rp[c >> 1] = pack_bf16x2(dv.x, dv.y);  // in place: word c / 2 was read at this step or before
         }
       }
       {
-#pragma unroll
-        for (int w = 0; w < 32; ++w) pw[w] = rp[w >> 4][w & 15];
         // dS^T of sub-tile j - 1 has been read by its dK product
         if (j > 0 && !wait_all(gk_done, ph ^ 1)) { ok = false; continue; }
-        tmem_st_32x32b_x32(tB + 64 + lane_off + hf * 32, pw);
-        tmem_st_wait();
+        tmem_st_32x32b_x32_sync(tB + 64 + lane_off + hf * 32, *reinterpret_cast<const uint32_t(*)[32]>(rp));
         tc_fence_before();
         mbar_arrive_warp(ds_full);
       }
