@@ -603,9 +603,17 @@ def run_attn_kernel(args):
         delta = torch.empty(B, H, s, device="cuda")
         dqkv = torch.empty_like(qkv)
         bwd = mt.k_attn_bwd_mma if args.legacy else mt.k_attn_bwd
+        if args.rope:
+            # RoPE tables [s, hd/2] (base 10000): the backward rotates dq, dk back in its stores
+            inv = 10000.0 ** (-torch.arange(0, hd // 2, device="cuda", dtype=torch.float64) * 2.0 / hd)
+            ang = torch.arange(s, device="cuda", dtype=torch.float64)[:, None] * inv[None, :]
+            cos_t, sin_t = ang.cos().float().contiguous(), ang.sin().float().contiguous()
 
-        def fn(*_):
-            bwd(qkv, o, dout, lse, delta, dqkv, B, s, H, Hkv, hd)
+            def fn(*_):
+                mt.k_attn_bwd_rope(qkv, o, dout, lse, delta, dqkv, B, s, H, Hkv, hd, cos_t, sin_t)
+        else:
+            def fn(*_):
+                bwd(qkv, o, dout, lse, delta, dqkv, B, s, H, Hkv, hd)
     else:
         fn = fwd
     for _ in range(2):
@@ -620,7 +628,8 @@ def run_attn_kernel(args):
     ms = s0.elapsed_time(s1) / args.iters
     # causal: two (forward) or five (backward) products over half the score matrix
     flops = (5.0 if args.backward else 2.0) * B * H * s * s * hd
-    name = ("attn_bwd" if args.backward else "attn_fwd") + ("_mma" if args.legacy else "")
+    name = ("attn_bwd" if args.backward else "attn_fwd") + ("_mma" if args.legacy else "") + \
+        ("_rope" if args.backward and args.rope else "")
     print(json.dumps({"kernel": name, "shape": [B, s, H, Hkv, hd], "ms": ms,
                       "tflops": flops / ms / 1e9}), flush=True)
     return 0
@@ -852,6 +861,8 @@ def main():
     ap.add_argument("--kernel", default=None, choices=[None, "gemm", "attn", "misc"])
     ap.add_argument("--legacy", action="store_true", help="with --kernel attn: the mma.sync kernels")
     ap.add_argument("--backward", action="store_true", help="with --kernel attn: time the backward")
+    ap.add_argument("--rope", action="store_true",
+                    help="with --kernel attn --backward: the form that rotates dq, dk back (the step's)")
     ap.add_argument("--shape", default="8192,8192,2048")
     ap.add_argument("--epilogue", default=None, choices=[None, "swiglu", "swiglu_bwd", "rope", "wgrad", "wgrad_nosplit"],
                     help="with --kernel gemm: a fused-epilogue form")

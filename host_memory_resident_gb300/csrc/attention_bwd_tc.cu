@@ -62,14 +62,31 @@ __device__ __forceinline__ void tmem_row_to_bf16(uint32_t taddr, int ncols, floa
   }
 }
 
+// N consecutive fp32 values from a 16-byte-aligned address, in 16-byte loads
+// (a RoPE table row: one position's cos or sin entries).
+template <int N>
+__device__ __forceinline__ void load_f32_vec(const float* p, float (&v)[N]) {
+  static_assert(N % 4 == 0, "16-byte loads");
+#pragma unroll
+  for (int j = 0; j < N / 4; ++j) {
+    const float4 u = __ldg(reinterpret_cast<const float4*>(p) + j);
+    v[4 * j] = u.x;
+    v[4 * j + 1] = u.y;
+    v[4 * j + 2] = u.z;
+    v[4 * j + 3] = u.w;
+  }
+}
+
 // RoPE's inverse rotation on N columns of this thread's TMEM lane and their
 // partners hd/2 further (times scale), stored as bf16: (x1, x2) ->
 // (x1 c + x2 s, x2 c - x1 s) at the row's position, so dq / dk leave the
-// kernel as gradients of the un-rotated q / k, rounded once. cs / sn point at
-// the position's cos / sin entries of the N pairs.
+// kernel as gradients of the un-rotated q / k, rounded once. cs / sn hold
+// the position's cos / sin entries of the N pairs (loaded by the caller
+// ahead of time: each thread's row is a different position, so the loads
+// cannot coalesce across the warp and their latency is best hidden).
 template <int N>
-__device__ __forceinline__ void tmem_pair_rope_to_bf16(uint32_t ta, uint32_t tb, float scale, const float* cs,
-                                                       const float* sn, bf16* da, bf16* db, bool store) {
+__device__ __forceinline__ void tmem_pair_rope_to_bf16(uint32_t ta, uint32_t tb, float scale, const float (&cs)[N],
+                                                       const float (&sn)[N], bf16* da, bf16* db, bool store) {
   uint32_t va[N], vb[N];
   if constexpr (N == 32) {
     tmem_ld_32x32b_x32(ta, va);
@@ -404,23 +421,34 @@ __global__ void __launch_bounds__(kThr, 1)
         mbar_arrive_warp(ds_full);
       }
     }
+    // the dk rows' first RoPE chunk is read while the last products run
+    const bool store = key < s;
+    const bool rot = hf == 1 && cos_t != nullptr;
+    const long long tb = (long long)(store ? key : 0) * (HD / 2);
+    float rc[32], rsn[32];
+    if (rot && ok && total > 0) {
+      load_f32_vec<32>(cos_t + tb, rc);
+      load_f32_vec<32>(sin_t + tb, rsn);
+    }
     if (ok && total > 0 && wait_all(done, 0)) {
       tc_fence_after();
-      const bool store = key < s;
       const long long r0 = (long long)b * s + key;
       bf16* dkrow = dqkv + r0 * lddq + (long long)kcol;
       if (hf == 0) {
         tmem_row_to_bf16(tdV + lane_off, HD, 1.f, dqkv + r0 * lddq + (long long)vcol, store);
-      } else if (cos_t == nullptr) {
+      } else if (!rot) {
         tmem_row_to_bf16(tdK + lane_off, HD, rsqrtf((float)HD), dkrow, store);
       } else {
-        // dk rotated back at the key's position (one 32-pair chunk per step)
-        const long long tb = (long long)(store ? key : 0) * (HD / 2);
+        // dk rotated back at the key's position, one 32-pair chunk per step
 #pragma unroll 1
-        for (int jj = 0; jj < HD / 64; ++jj)
+        for (int jj = 0; jj < HD / 64; ++jj) {
+          if (jj > 0) {
+            load_f32_vec<32>(cos_t + tb + jj * 32, rc);
+            load_f32_vec<32>(sin_t + tb + jj * 32, rsn);
+          }
           tmem_pair_rope_to_bf16<32>(tdK + lane_off + jj * 32, tdK + lane_off + HD / 2 + jj * 32, rsqrtf((float)HD),
-                                     cos_t + tb + jj * 32, sin_t + tb + jj * 32, dkrow + jj * 32,
-                                     dkrow + HD / 2 + jj * 32, store);
+                                     rc, rsn, dkrow + jj * 32, dkrow + HD / 2 + jj * 32, store);
+        }
       }
     }
   }
@@ -650,18 +678,24 @@ __global__ void __launch_bounds__(kThr, 1)
       tc_fence_before();
       mbar_arrive_warp(p_full);
     }
+    // dq rotated back at the query's position: this thread takes pairs
+    // [half * HD/4, (half + 1) * HD/4) and their partners HD/2 further; their
+    // cos / sin entries are read while the last products run
+    constexpr int N = HD / 4;
+    const long long tb = (long long)(qpos < s ? qpos : 0) * (HD / 2) + half * N;
+    float rc[N], rsn[N];
+    if (cos_t != nullptr && ok) {
+      load_f32_vec<N>(cos_t + tb, rc);
+      load_f32_vec<N>(sin_t + tb, rsn);
+    }
     if (ok && mbar_wait_warp(done, 0, err)) {
       tc_fence_after();
       bf16* dqh = dqkv + ((long long)b * s + qpos) * lddq + (long long)h * HD;
       if (cos_t == nullptr) {
         tmem_row_to_bf16(tdQ + lane_off + half * (HD / 2), HD / 2, rsqrtf((float)HD), dqh + half * (HD / 2), qpos < s);
       } else {
-        // dq rotated back at the query's position: this thread takes pairs
-        // [half * HD/4, (half + 1) * HD/4) and their partners HD/2 further
-        constexpr int N = HD / 4;
-        const long long tb = (long long)(qpos < s ? qpos : 0) * (HD / 2) + half * N;
         tmem_pair_rope_to_bf16<N>(tdQ + lane_off + half * N, tdQ + lane_off + HD / 2 + half * N, rsqrtf((float)HD),
-                                  cos_t + tb, sin_t + tb, dqh + half * N, dqh + HD / 2 + half * N, qpos < s);
+                                  rc, rsn, dqh + half * N, dqh + HD / 2 + half * N, qpos < s);
       }
     }
   }
@@ -712,6 +746,10 @@ int attn_bwd_tc(const void* qkv, long long ld, const void* dout, long long lddo,
   std::call_once(g_once, init_once);
   if (!g_enc) return MT_ECUDA;
   if (hd != 64 && hd != 128) return MT_EINVAL;
+  // the rotation reads each position's table row in 16-byte loads
+  if ((cos_t == nullptr) != (sin_t == nullptr) || (reinterpret_cast<uintptr_t>(cos_t) & 15) ||
+      (reinterpret_cast<uintptr_t>(sin_t) & 15))
+    return MT_EINVAL;
   if ((reinterpret_cast<uintptr_t>(qkv) & 15) || (reinterpret_cast<uintptr_t>(dout) & 15) ||
       (reinterpret_cast<uintptr_t>(dqkv) & 15) || ld % 8 || lddo % 8 || lddq % 8)
     return MT_EINVAL;
