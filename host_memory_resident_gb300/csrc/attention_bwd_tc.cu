@@ -468,7 +468,8 @@ __global__ void __launch_bounds__(kThr, 1)
 // TMEM buffers, where dQ += dS K reads it as its A operand. K and V stream
 // through separate TMA rings: V is free as soon as dP has run, K once dQ
 // has, so the loads of tile j + 1 are issued while tile j - 1 is still being
-// multiplied instead of after it.
+// multiplied instead of after it. Both land on one barrier per tile: every
+// wait of the MMA thread lets the products it has queued drain.
 template <int HD>
 struct QTc {
   static constexpr int kBoxes = HD / 64;
@@ -482,7 +483,8 @@ struct QTc {
   static constexpr uint32_t kBarOff = kVOff + kVS * kTile;
   static constexpr size_t kSmem = 1024 + kBarOff + 256;
   static_assert(kSmem <= 232448, "shared memory per block");
-  static_assert(2 * (kKS + kVS) + 6 <= 256 / 8, "barrier area");
+  static_assert(kKS + 2 * kVS + 6 <= 256 / 8, "barrier area");
+  static_assert(kVS <= kKS, "tiles in flight are bounded by the V ring");
 };
 
 template <int HD>
@@ -496,10 +498,9 @@ __global__ void __launch_bounds__(kThr, 1)
   uint8_t* sm = align1024b(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
   uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;           // [kKS]
-  uint64_t* k_empty = k_full + C::kKS;   // [kKS]
-  uint64_t* v_full = k_empty + C::kKS;   // [kVS]
-  uint64_t* v_empty = v_full + C::kVS;   // [kVS]
+  uint64_t* kv_full = bars + 1;           // [kVS] K and V of tile j, on barrier j % kVS
+  uint64_t* k_empty = kv_full + C::kVS;   // [kKS]
+  uint64_t* v_empty = k_empty + C::kKS;   // [kVS]
   uint64_t* s_full = v_empty + C::kVS;   // S and dP in TMEM
   uint64_t* s_empty = s_full + 1;        // S and dP copied out of TMEM
   uint64_t* p_full = s_full + 2;         // dS stored in TMEM
@@ -521,12 +522,9 @@ __global__ void __launch_bounds__(kThr, 1)
     tma_prefetch_desc(&tqkv);
     tma_prefetch_desc(&tdo);
     mbar_init(q_full, 1);
-    for (int i = 0; i < C::kKS; ++i) {
-      mbar_init(&k_full[i], 1);
-      mbar_init(&k_empty[i], 1);
-    }
+    for (int i = 0; i < C::kKS; ++i) mbar_init(&k_empty[i], 1);
     for (int i = 0; i < C::kVS; ++i) {
-      mbar_init(&v_full[i], 1);
+      mbar_init(&kv_full[i], 1);
       mbar_init(&v_empty[i], 1);
     }
     mbar_init(s_full, 1);
@@ -551,31 +549,28 @@ __global__ void __launch_bounds__(kThr, 1)
         tma_load_3d(sm + C::kQOff + bx * kBox, &tqkv, h * HD + bx * 64, q0, b, q_full);
         tma_load_3d(sm + C::kOOff + bx * kBox, &tdo, h * HD + bx * 64, q0, b, q_full);
       }
-      int nk = 0, nv = 0;  // K and V tiles whose loads were issued
+      // K and V of tile j land on one barrier (kv_full[j % kVS]), so the MMA
+      // thread makes one wait for both; the V ring is the shallower, so at
+      // most kVS tiles are in flight
+      int nkv = 0;  // tiles whose loads were issued
       for (int j = 0; j < n_kv; ++j) {
         const int ks = j % C::kKS, vs = j % C::kVS;
         if (!mbar_wait(&k_empty[ks], ((j / C::kKS) & 1) ^ 1, err)) break;
-        mbar_arrive_expect_tx(&k_full[ks], C::kTile);
-        for (int bx = 0; bx < C::kBoxes; ++bx)
-          tma_load_3d(sm + C::kKOff + ks * C::kTile + bx * kBox, &tqkv, kcol + bx * 64, j * kT, b, &k_full[ks]);
-        ++nk;
         if (!mbar_wait(&v_empty[vs], ((j / C::kVS) & 1) ^ 1, err)) break;
-        mbar_arrive_expect_tx(&v_full[vs], C::kTile);
-        for (int bx = 0; bx < C::kBoxes; ++bx)
-          tma_load_3d(sm + C::kVOff + vs * C::kTile + bx * kBox, &tqkv, vcol + bx * 64, j * kT, b, &v_full[vs]);
-        ++nv;
+        mbar_arrive_expect_tx(&kv_full[vs], 2 * C::kTile);
+        for (int bx = 0; bx < C::kBoxes; ++bx) {
+          tma_load_3d(sm + C::kKOff + ks * C::kTile + bx * kBox, &tqkv, kcol + bx * 64, j * kT, b, &kv_full[vs]);
+          tma_load_3d(sm + C::kVOff + vs * C::kTile + bx * kBox, &tqkv, vcol + bx * 64, j * kT, b, &kv_full[vs]);
+        }
+        ++nkv;
       }
-      if (nk < n_kv || nv < n_kv) {
+      if (nkv < n_kv) {
         // a wait gave up: wait (bounded) for this CTA's copies still in
         // flight before it exits
         mbar_wait(q_full, 0, err);
-        for (int i = 0; i < C::kKS && i < nk; ++i) {
-          const int last = nk - 1 - i;
-          mbar_wait(&k_full[last % C::kKS], (last / C::kKS) & 1, err);
-        }
-        for (int i = 0; i < C::kVS && i < nv; ++i) {
-          const int last = nv - 1 - i;
-          mbar_wait(&v_full[last % C::kVS], (last / C::kVS) & 1, err);
+        for (int i = 0; i < C::kVS && i < nkv; ++i) {
+          const int last = nkv - 1 - i;
+          mbar_wait(&kv_full[last % C::kVS], (last / C::kVS) & 1, err);
         }
       }
     }
@@ -590,8 +585,7 @@ __global__ void __launch_bounds__(kThr, 1)
       // copied out by the element-wise warps); V is released when dP is done
       auto issue_s = [&](int j) -> bool {
         const int ks = j % C::kKS, vs = j % C::kVS;
-        if (!mbar_wait(&k_full[ks], (j / C::kKS) & 1, err)) return false;
-        if (!mbar_wait(&v_full[vs], (j / C::kVS) & 1, err)) return false;
+        if (!mbar_wait(&kv_full[vs], (j / C::kVS) & 1, err)) return false;
         if (j > 0 && !mbar_wait(s_empty, (j - 1) & 1, err)) return false;
         tc_fence_after();
         const uint64_t dK = smem_desc_kmajor_sw128(smem_u32(sm + C::kKOff + ks * C::kTile));
