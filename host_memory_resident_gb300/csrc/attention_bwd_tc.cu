@@ -131,7 +131,10 @@ __device__ __forceinline__ void tmem_pair_rope_to_bf16(uint32_t ta, uint32_t tb,
 // holds tA (S^T then dP^T, fp32), tB (P^T | dS^T packed as bf16 pairs, the
 // A operands of the dV and dK products), dV and dK: 128 + 128 + 2 hd <= 512
 // columns. Q and dO tiles of 128 queries share four shared-memory slots
-// (see slot_q / slot_o). The element-wise warps stage the sub-tile's 128
+// (see slot_q / slot_o); one element-wise warp checks that they have landed
+// and releases them, so the MMA thread makes four waits and two commits per
+// sub-tile (each of its waits and commits lets the products it has queued
+// drain). The element-wise warps stage the sub-tile's 128
 // lse and 128 delta values in shared memory, double-buffered, one barrier
 // per sub-tile; each thread reads four query columns per 16-byte broadcast
 // load, in two-wide fp32 instructions.
@@ -169,17 +172,15 @@ __global__ void __launch_bounds__(kThr, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kBarOff);
   uint64_t* kv_full = bars;                       // K and V tiles
   uint64_t* slot_full = bars + 1;                 // [kSlots]
-  uint64_t* slot_empty = slot_full + C::kSlots;   // [kSlots]
-  uint64_t* s_full = slot_empty + C::kSlots;      // S^T in tA
-  uint64_t* s_read = s_full + 1;                  // S^T copied out of tA (8 warps)
-  uint64_t* d_full = s_full + 2;                  // dP^T in tA
-  uint64_t* d_read = s_full + 3;                  // dP^T copied out of tA (8 warps)
+  uint64_t* slot_empty = slot_full + C::kSlots;   // [kSlots] released by the loads warp
+  uint64_t* s_full = slot_empty + C::kSlots;      // S^T j in tA (so dV j - 1, issued before it, is done)
+  uint64_t* s_read = s_full + 1;                  // S^T copied out of tA, dO j landed (8 warps)
+  uint64_t* d_full = s_full + 2;                  // dP^T j in tA (so dK j - 1, issued before it, is done)
+  uint64_t* d_read = s_full + 3;                  // dP^T copied out of tA, Q j + 1 landed (8 warps)
   uint64_t* pv_full = s_full + 4;                 // P^T stored in tB (8 warps)
-  uint64_t* gv_done = s_full + 5;                 // dV product of the sub-tile done
-  uint64_t* ds_full = s_full + 6;                 // dS^T stored in tB (8 warps)
-  uint64_t* gk_done = s_full + 7;                 // dK product of the sub-tile done
-  uint64_t* done = s_full + 8;                    // all products done (completes once)
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(s_full + 9);
+  uint64_t* ds_full = s_full + 5;                 // dS^T stored in tB (8 warps)
+  uint64_t* done = s_full + 6;                    // all products done (completes once)
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(s_full + 7);
 
   const int nqt = (s + kT - 1) / kT;
   int hb, kt;  // (batch, KV head) pair and key tile; kt = 0 is the longest
@@ -205,9 +206,7 @@ __global__ void __launch_bounds__(kThr, 1)
     mbar_init(d_full, 1);
     mbar_init(d_read, 8);
     mbar_init(pv_full, 8);
-    mbar_init(gv_done, 1);
     mbar_init(ds_full, 8);
-    mbar_init(gk_done, 1);
     mbar_init(done, 1);
     fence_barrier_init();
   }
@@ -288,21 +287,24 @@ __global__ void __launch_bounds__(kThr, 1)
         tc_commit(s_full);
       }
       // per sub-tile j: dP^T j, dV j, S^T j + 1, dK j, so the element-wise
-      // warps' work on one product's result overlaps the next product
+      // warps' work on one product's result overlaps the next product. Each
+      // wait or commit of this thread stalls the tensor pipe until what it
+      // has queued drains, so it makes four waits and two commits per
+      // sub-tile: the loads warp checks that Q / dO have landed before the
+      // group's arrivals, and releases their slots, and since products run
+      // in issue order s_full j and d_full j also report dV j - 1 and
+      // dK j - 1 done
       for (int j = 0; ok && j < total; ++j) {
-        const uint32_t ph = j & 1, u = (j >> 1) & 1;
-        if (!(ok = mbar_wait(s_read, ph, err) && mbar_wait(&slot_full[slot_o(j)], u, err))) break;
+        const uint32_t ph = j & 1;
+        if (!(ok = mbar_wait(s_read, ph, err))) break;
         tc_fence_after();
         scores(dV, slot_o(j));
         tc_commit(d_full);
         if (!(ok = mbar_wait(pv_full, ph, err))) break;
         tc_fence_after();
         grads(tdV, tB, slot_o(j), j == 0);
-        tc_commit(gv_done);
-        tc_commit(&slot_empty[slot_o(j)]);
         if (j + 1 < total) {
-          const uint32_t u1 = ((j + 1) >> 1) & 1;
-          if (!(ok = mbar_wait(d_read, ph, err) && mbar_wait(&slot_full[slot_q(j + 1)], u1, err))) break;
+          if (!(ok = mbar_wait(d_read, ph, err))) break;
           tc_fence_after();
           scores(dK, slot_q(j + 1));
           tc_commit(s_full);
@@ -310,8 +312,6 @@ __global__ void __launch_bounds__(kThr, 1)
         if (!(ok = mbar_wait(ds_full, ph, err))) break;
         tc_fence_after();
         grads(tdK, tB + 64, slot_q(j), j == 0);
-        tc_commit(gk_done);
-        tc_commit(&slot_empty[slot_q(j)]);
       }
       if (ok) tc_commit(done);
     }
@@ -326,6 +326,14 @@ __global__ void __launch_bounds__(kThr, 1)
     const int te = threadIdx.x - 64;  // 0..255
     auto all_sync = [&]() { asm volatile("bar.sync 1, 256;" ::: "memory"); };
     auto wait_all = [&](uint64_t* bar, uint32_t parity) { return mbar_wait_warp(bar, parity, err); };
+    // one warp also checks that the Q / dO tiles the next products read have
+    // landed, before the group's arrival that lets the MMA thread issue them,
+    // and releases each slot once its last reader is known to be done
+    const bool loads_warp = warp == 2;
+    auto wait_slot = [&](int sl, int jj) { return !loads_warp || wait_all(&slot_full[sl], (jj >> 1) & 1); };
+    auto release = [&](int sl) {
+      if (loads_warp) mbar_arrive_warp(&slot_empty[sl]);
+    };
     bool ok = true;
     // (lse * log2e, delta) of query te of sub-tile j, read one sub-tile ahead
     auto load_vec = [&](int j) -> float2 {
@@ -351,7 +359,9 @@ __global__ void __launch_bounds__(kThr, 1)
       all_sync();
       if (te < kT && j + 1 < total) vnext = load_vec(j + 1);
       if (!ok) continue;
-      if (!wait_all(s_full, ph)) { ok = false; continue; }
+      if (!wait_slot(slot_o(j), j) || !wait_all(s_full, ph)) { ok = false; continue; }
+      // S^T j done, so dV j - 1, the last reader of dO j - 1's slot, is too
+      if (j > 0) release(slot_o(j - 1));
       tc_fence_after();
       uint32_t rs[64], rp[64];
       tmem_ld_32x32b_x64_sync(tA + lane_off + hf * 64, rs);
@@ -390,12 +400,14 @@ __global__ void __launch_bounds__(kThr, 1)
         probs(std::false_type{});
       {
         // P^T of sub-tile j - 1 has been read by its dV product
-        if (j > 0 && !wait_all(gv_done, ph ^ 1)) { ok = false; continue; }
+        // P^T j - 1 was read by dV j - 1, done before S^T j
         tmem_st_32x32b_x32_sync(tB + lane_off + hf * 32, pw);
         tc_fence_before();
         mbar_arrive_warp(pv_full);
       }
-      if (!wait_all(d_full, ph)) { ok = false; continue; }
+      if ((j + 1 < total && !wait_slot(slot_q(j + 1), j + 1)) || !wait_all(d_full, ph)) { ok = false; continue; }
+      // dP^T j done, so dK j - 1, the last reader of Q j - 1's slot, is too
+      if (j > 0) release(slot_q(j - 1));
       tc_fence_after();
       tmem_ld_32x32b_x64_sync(tA + lane_off + hf * 64, rp);
       tc_fence_before();
@@ -415,7 +427,7 @@ __global__ void __launch_bounds__(kThr, 1)
       }
       {
         // dS^T of sub-tile j - 1 has been read by its dK product
-        if (j > 0 && !wait_all(gk_done, ph ^ 1)) { ok = false; continue; }
+        // dS^T j - 1 was read by dK j - 1, done before dP^T j
         tmem_st_32x32b_x32_sync(tB + 64 + lane_off + hf * 32, *reinterpret_cast<const uint32_t(*)[32]>(rp));
         tc_fence_before();
         mbar_arrive_warp(ds_full);
