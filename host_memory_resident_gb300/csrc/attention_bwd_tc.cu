@@ -480,8 +480,10 @@ __global__ void __launch_bounds__(kThr, 1)
 // TMEM buffers, where dQ += dS K reads it as its A operand. K and V stream
 // through separate TMA rings: V is free as soon as dP has run, K once dQ
 // has, so the loads of tile j + 1 are issued while tile j - 1 is still being
-// multiplied instead of after it. Both land on one barrier per tile: every
-// wait of the MMA thread lets the products it has queued drain.
+// multiplied instead of after it. Both land on one barrier per tile, which
+// one element-wise warp checks (and it frees each V stage once S / dP of its
+// tile are done): every wait or commit of the MMA thread lets the products
+// it has queued drain, and it makes two of each per key tile.
 template <int HD>
 struct QTc {
   static constexpr int kBoxes = HD / 64;
@@ -597,7 +599,10 @@ __global__ void __launch_bounds__(kThr, 1)
       // copied out by the element-wise warps); V is released when dP is done
       auto issue_s = [&](int j) -> bool {
         const int ks = j % C::kKS, vs = j % C::kVS;
-        if (!mbar_wait(&kv_full[vs], (j / C::kVS) & 1, err)) return false;
+        // tile 0's K / V are checked here; later tiles' by the element-wise
+        // loads warp before its s_empty arrival (each wait of this thread
+        // lets the products it has queued drain)
+        if (j == 0 && !mbar_wait(&kv_full[0], 0, err)) return false;
         if (j > 0 && !mbar_wait(s_empty, (j - 1) & 1, err)) return false;
         tc_fence_after();
         const uint64_t dK = smem_desc_kmajor_sw128(smem_u32(sm + C::kKOff + ks * C::kTile));
@@ -609,7 +614,6 @@ __global__ void __launch_bounds__(kThr, 1)
           tc_mma_bf16(tdP, desc_advance(dO, off), desc_advance(dV, off), id_s, kk > 0);
         }
         tc_commit(s_full);
-        tc_commit(&v_empty[vs]);
         return true;
       };
       if (ok) ok = issue_s(0);
@@ -637,16 +641,22 @@ __global__ void __launch_bounds__(kThr, 1)
     const float l2 = qpos < s ? lse[vidx] * kLog2e : INFINITY;
     const float dl = qpos < s ? delta[vidx] : 0.f;
     bool ok = true;
+    // one warp checks that the next tile's K / V have landed (before the
+    // arrival that lets the MMA thread issue its products) and frees each V
+    // stage once S / dP of its tile are done
+    const bool loads_warp = warp == 2;
     for (int j = 0; j < n_kv && ok; ++j) {
-      if (!mbar_wait_warp(s_full, j & 1, err)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t rs[2][32], rp[2][32];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        tmem_ld_32x32b_x32(tS + lane_off + half * 64 + c * 32, rs[c]);
-        tmem_ld_32x32b_x32(tdP + lane_off + half * 64 + c * 32, rp[c]);
+      if (loads_warp && j + 1 < n_kv &&
+          !mbar_wait_warp(&kv_full[(j + 1) % C::kVS], ((j + 1) / C::kVS) & 1, err)) {
+        ok = false;
+        break;
       }
-      tmem_ld_wait();
+      if (!mbar_wait_warp(s_full, j & 1, err)) { ok = false; break; }
+      if (loads_warp) mbar_arrive_warp(&v_empty[j % C::kVS]);
+      tc_fence_after();
+      uint32_t rs[64], rp[64];
+      tmem_ld_32x32b_x64_sync(tS + lane_off + half * 64, rs);
+      tmem_ld_32x32b_x64_sync(tdP + lane_off + half * 64, rp);
       tc_fence_before();
       mbar_arrive_warp(s_empty);
       const int kb = j * kT + half * 64;
@@ -659,15 +669,13 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int ci = 2 * i;
-          const float2 x = ffma2(
-              make_float2(__uint_as_float(rs[ci >> 5][ci & 31]), __uint_as_float(rs[ci >> 5][(ci + 1) & 31])), sc2, nl2);
+          const float2 x = ffma2(make_float2(__uint_as_float(rs[ci]), __uint_as_float(rs[ci + 1])), sc2, nl2);
           float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
           if (kMasked) {
             if (kb + ci > qpos) pp.x = 0.f;
             if (kb + ci + 1 > qpos) pp.y = 0.f;
           }
-          const float2 dp =
-              make_float2(__uint_as_float(rp[ci >> 5][ci & 31]), __uint_as_float(rp[ci >> 5][(ci + 1) & 31]));
+          const float2 dp = make_float2(__uint_as_float(rp[ci]), __uint_as_float(rp[ci + 1]));
           const float2 dv = fmul2(pp, fadd2(dp, ndl));
           dk[i] = pack_bf16x2(dv.x, dv.y);
         }
