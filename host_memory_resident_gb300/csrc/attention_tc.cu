@@ -27,7 +27,10 @@
 //            unchanged.
 // While one group exponentiates, the tensor core computes the other group's
 // products and both groups' next scores, so neither the exponential units nor
-// the tensor core waits on a single chain of dependencies.
+// the tensor core waits on a single chain of dependencies. Every wait or
+// commit of the MMA thread lets the products it has queued drain; at hd 128
+// it makes one of each per tile and key tile (a softmax warp checks the K / V
+// loads and frees their stages).
 // This is the attention of the stateless layer template (zhichai.net
 // article, "以内存为中心的训练新范式" point 4); streaming the keys in tiles keeps
 // its memory O(s), the basis of the long-context runs the travelaiplan blog
@@ -105,13 +108,16 @@ __global__ void __launch_bounds__(kThr, 1)
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tm);
     mbar_init(q_full, 1);
+    // at hd 128 each softmax group frees the K / V stages its tile has
+    // finished with (one arrival per query tile); at hd 64 the MMA thread does
+    const uint32_t rel = HD == 128 ? (uint32_t)ntile : 1u;
     for (int i = 0; i < C::kKS; ++i) {
       mbar_init(&k_full[i], 1);
-      mbar_init(&k_empty[i], 1);
+      mbar_init(&k_empty[i], rel);
     }
     for (int i = 0; i < C::kVS; ++i) {
       mbar_init(&v_full[i], 1);
-      mbar_init(&v_empty[i], 1);
+      mbar_init(&v_empty[i], rel);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
@@ -207,35 +213,33 @@ __global__ void __launch_bounds__(kThr, 1)
       auto wait_k = [&](int j) { return mbar_wait(&k_full[j % C::kKS], (j / C::kKS) & 1, err); };
       if (kAlias) {
         // P_t(j) occupies S_t's columns until P_t(j) V has read it, so
-        // S_t(j + 1) is issued right after that product
+        // S_t(j + 1) is issued right after that product. Every wait or
+        // commit of this thread lets the products it has queued drain, so
+        // it makes one wait (p_full) and one commit (s_full) per tile and
+        // key tile: the softmax group checks that V j and K j + 1 have
+        // landed before its p_full arrival and frees the K / V stages, and
+        // S_t(j + 1) done also reports P_t(j) V done; only a tile's last
+        // P V commits to p_empty
         if (ok && (ok = wait_k(0))) {
           tc_fence_after();
           for (int t = 0; t < 2; ++t)
             if (nkv[t] > 0) mma_s(0, t);
-          tc_commit(&k_empty[0]);
         }
         for (int j = 0; ok && j < n_kv; ++j) {
           const int vs = j % C::kVS;
-          if (!(ok = mbar_wait(&v_full[vs], (j / C::kVS) & 1, err))) break;
           const uint64_t mV = smem_desc_mnmajor_sw128(smem_u32(sm + C::kVOff + vs * C::kTile), kBox);
-          bool k_next = false;  // K_{j+1} waited for
           for (int t = 0; t < 2 && ok; ++t) {
             if (j >= nkv[t]) continue;
             if (!(ok = mbar_wait(&p_full[t], j & 1, err))) break;
             tc_fence_after();
-            mma_pv(j, t, mV);
-            if (j + 1 < nkv[t]) {
-              if (!k_next) {
-                if (!(ok = wait_k(j + 1))) break;
-                k_next = true;
-                tc_fence_after();
-              }
+#pragma unroll
+            for (int kk = 0; kk < kKV / 16; ++kk)
+              tc_mma_bf16_ta(tO(t), tP(t) + kk * 8, desc_advance(mV, kk * 2048), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+            if (j + 1 < nkv[t])
               mma_s(j + 1, t);
-            }
+            else
+              tc_commit(&p_empty[t]);
           }
-          if (!ok) break;
-          tc_commit(&v_empty[vs]);
-          if (k_next) tc_commit(&k_empty[(j + 1) % C::kKS]);
         }
       } else {
         // S_t(j) for both tiles that still need key tile j, then release K_j;
@@ -278,8 +282,24 @@ __global__ void __launch_bounds__(kThr, 1)
     const float sc = rsqrtf((float)HD) * kLog2e;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
+    // at hd 128, one warp of the group checks that V j and K j + 1 have
+    // landed (while the group waits for S_t(j) anyway) and frees the K / V
+    // stages this tile has finished with
+    const bool loads_warp = kAlias && q == 2;
     for (int j = 0; j < nk && ok; ++j) {
+      if (loads_warp) {
+        if (!mbar_wait_warp(&v_full[j % C::kVS], (j / C::kVS) & 1, err)) { ok = false; break; }
+        if (j + 1 < nk && !mbar_wait_warp(&k_full[(j + 1) % C::kKS], ((j + 1) / C::kKS) & 1, err)) {
+          ok = false;
+          break;
+        }
+      }
       if (!mbar_wait_warp(&s_full[t], j & 1, err)) { ok = false; break; }
+      if (loads_warp) {
+        // S_t(j) done: K j read; P_t(j-1) V, issued before S_t(j), done: V j-1 read
+        mbar_arrive_warp(&k_empty[j % C::kKS]);
+        if (j > 0) mbar_arrive_warp(&v_empty[(j - 1) % C::kVS]);
+      }
       tc_fence_after();
       uint32_t r[4][32];
 #pragma unroll
@@ -321,8 +341,9 @@ __global__ void __launch_bounds__(kThr, 1)
           r[c][i] = pack_bf16x2(pp.x, pp.y);
         }
       const float lt0 = lt.x, lt1 = lt.y;
-      // P_t(j-1) V has finished: O_t is current and the P buffer is free
-      if (j > 0) {
+      // P_t(j-1) V has finished: O_t is current and the P buffer is free (at
+      // hd 128 S_t(j), issued after it, has completed)
+      if (j > 0 && !kAlias) {
         if (!mbar_wait_warp(&p_empty[t], (j - 1) & 1, err)) { ok = false; break; }
         tc_fence_after();
       }
@@ -357,7 +378,7 @@ __global__ void __launch_bounds__(kThr, 1)
       tc_fence_before();
       mbar_arrive_warp(&p_full[t]);
     }
-    if (ok && nk > 0 && mbar_wait_warp(&p_empty[t], (nk - 1) & 1, err)) {
+    if (ok && nk > 0 && mbar_wait_warp(&p_empty[t], kAlias ? 0u : (uint32_t)((nk - 1) & 1), err)) {
       tc_fence_after();
       const float inv = 1.f / l;
       bf16* orow = o + ((long long)b * s + qpos) * ldo + (long long)h * HD;
