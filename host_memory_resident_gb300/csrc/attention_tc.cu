@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(kThr, 1)
   uint64_t* s_full = v_empty + C::kVS;       // [2] per tile: S_t written
   uint64_t* s_empty = s_full + 2;            // [2] per tile: S_t copied out by its softmax group
   uint64_t* p_full = s_empty + 2;            // [2] per tile: P_t written (and O_t rescaled)
-  uint64_t* p_empty = p_full + 2;            // [2] per tile: P_t V finished (O_t current, P_t free)
+  uint64_t* p_empty = p_full + 2;            // [2] per tile: P_t V finished (hd 64: every key tile; hd 128: the last)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(p_empty + 2);
 
   const int nqt = (s + kQ - 1) / kQ;
