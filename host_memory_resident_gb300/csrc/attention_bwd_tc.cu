@@ -399,7 +399,6 @@ __global__ void __launch_bounds__(kThr, 1)
       else
         probs(std::false_type{});
       {
-        // P^T of sub-tile j - 1 has been read by its dV product
         // P^T j - 1 was read by dV j - 1, done before S^T j
         tmem_st_32x32b_x32_sync(tB + lane_off + hf * 32, pw);
         tc_fence_before();
@@ -426,7 +425,6 @@ __global__ void __launch_bounds__(kThr, 1)
         }
       }
       {
-        // dS^T of sub-tile j - 1 has been read by its dK product
         // dS^T j - 1 was read by dK j - 1, done before dP^T j
         tmem_st_32x32b_x32_sync(tB + 64 + lane_off + hf * 32, *reinterpret_cast<const uint32_t(*)[32]>(rp));
         tc_fence_before();
